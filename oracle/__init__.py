@@ -1,0 +1,15 @@
+"""CPU oracle for Kimi Delta Attention -- test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  The CUDA library never imports, links or calls
+it, and the two share no code.
+"""
+from .kda_ref import (  # noqa: F401
+    build_oracle,
+    recurrent,
+    recurrent_seq_head,
+    unrolled_bruteforce,
+    chunkwise_naive,
+    delta_invariant_keys,
+    rel_err,
+)

@@ -1,0 +1,240 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each pin is a function of the oracle build (``mutant``) so that the last test
+can show that a planted mistake in the oracle fails at least one pin.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import chunkwise_naive, rel_err, unrolled_bruteforce
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_case(T, dk, dv, seed, g_scale=5.0, s0_std=0.5):
+    rng = np.random.default_rng(seed)
+    k = rng.standard_normal((T, dk))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    q = rng.standard_normal((T, dk))
+    q /= np.linalg.norm(q, axis=1, keepdims=True)
+    v = rng.standard_normal((T, dv))
+    g = -g_scale / (1.0 + np.exp(-rng.standard_normal((T, dk))))
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal(T)))
+    S0 = s0_std * rng.standard_normal((dk, dv))
+    f32 = lambda a: np.ascontiguousarray(a, dtype=np.float32)
+    return f32(q), f32(k), f32(v), f32(g), f32(beta), f32(S0)
+
+
+def _run1(q, k, v, g, beta, S0, mutant=0):
+    """Oracle on one (sequence, head)."""
+    T = q.shape[0]
+    o, f = oracle.recurrent(q[:, None], k[:, None], v[:, None], g[:, None], beta[:, None],
+                            np.array([0, T], dtype=np.int32), None if S0 is None else S0[None, None],
+                            threads=1, mutant=mutant)
+    return o[:, 0], f[0, 0]
+
+
+# ---------------------------------------------------------------- pins
+def pin_delta_invariant(mutant=0, dk=16, dv=16):
+    """g = 0, beta = 1, orthonormal keys: the state returns each written value exactly
+    (Q05: the write subtracts the old prediction).  Returns the max error."""
+    n = dk
+    K = oracle.delta_invariant_keys(dk, n, seed=3).astype(np.float32)
+    rng = np.random.default_rng(4)
+    V = rng.standard_normal((n, dv)).astype(np.float32)
+    S0 = (0.3 * rng.standard_normal((dk, dv))).astype(np.float32)
+    g = np.zeros((n, dk), np.float32)
+    beta = np.ones(n, np.float32)
+    _, S = _run1(K, K, V, g, beta, S0, mutant)
+    # keys are the fp32-rounded QR rows; the invariant holds for exactly orthonormal
+    # keys, so compare against the prediction for the keys actually stored
+    Kd = K.astype(np.float64)
+    Vd = V.astype(np.float64)
+    G = Kd @ Kd.T
+    assert np.max(np.abs(G - np.eye(n))) < 1e-6
+    return float(np.max(np.abs(S.T @ Kd.T - Vd.T)))
+
+
+def pin_repeated_key_overwrites(mutant=0):
+    """Lab A toy (hand-worked): a repeated key returns its latest value, not a sum."""
+    with open(os.path.join(GOLDEN, "lab_a_delta_toy.json")) as fh:
+        fx = json.load(fh)
+    f32 = lambda a: np.asarray(a, dtype=np.float32)
+    o, S = _run1(f32(fx["q"]), f32(fx["k"]), f32(fx["v"]), f32(fx["g"]), f32(fx["beta"]), None, mutant)
+    return max(float(np.max(np.abs(o - np.asarray(fx["expected_out"])))),
+               float(np.max(np.abs(S - np.asarray(fx["expected_final_state"])))))
+
+
+def pin_bruteforce(mutant=0, dk=6, dv=6, T=8, seed=11):
+    """Explicit product of transition matrices, T <= 8."""
+    q, k, v, g, beta, S0 = _rand_case(T, dk, dv, seed)
+    o, S = _run1(q, k, v, g, beta, S0, mutant)
+    ou, Su = unrolled_bruteforce(q, k, v, g, beta, S0)
+    return max(rel_err(o, ou), rel_err(S, Su))
+
+
+def pin_chunkwise(mutant=0, dk=8, dv=8, T=70, C=16, seed=5):
+    """Naive chunkwise rewrite (explicit inverse) equals the recurrence."""
+    q, k, v, g, beta, S0 = _rand_case(T, dk, dv, seed)
+    o, S = _run1(q, k, v, g, beta, S0, mutant)
+    oc, Sc = chunkwise_naive(q, k, v, g, beta, S0, chunk=C)
+    return max(rel_err(o, oc), rel_err(S, Sc))
+
+
+def pin_closed_form_no_write(mutant=0, dk=8, dv=5, T=9, seed=6):
+    """beta = 0: S_t = Diag(exp sum g) S_0 and o_t = S_t^T q_t."""
+    q, k, v, g, beta, S0 = _rand_case(T, dk, dv, seed, g_scale=1.0)
+    beta[:] = 0
+    o, S = _run1(q, k, v, g, beta, S0, mutant)
+    G = np.cumsum(g.astype(np.float64), axis=0)
+    ref_o = np.stack([(np.exp(G[t])[:, None] * S0).T @ q[t] for t in range(T)])
+    ref_S = np.exp(G[-1])[:, None] * S0
+    return max(rel_err(o, ref_o), rel_err(S, ref_S))
+
+
+def pin_closed_form_first_token(mutant=0, dk=8, dv=5, seed=7):
+    """S_0 = 0: o_1 = beta_1 (k_1 . q_1) v_1 whatever g_1 is."""
+    q, k, v, g, beta, _ = _rand_case(1, dk, dv, seed)
+    o, _ = _run1(q, k, v, g, beta, None, mutant)
+    ref = float(beta[0]) * float(np.dot(k[0].astype(np.float64), q[0])) * v[0].astype(np.float64)
+    return rel_err(o[0], ref)
+
+
+# ---------------------------------------------------------------- tests on the real oracle
+def test_delta_rule_invariant():
+    assert pin_delta_invariant() < 1e-6
+    assert pin_delta_invariant(dk=32, dv=8) < 1e-6
+
+
+def test_repeated_key_overwrites_lab_a():
+    assert pin_repeated_key_overwrites() < 1e-12
+    # and the additive alternative the lab contrasts is really different
+    with open(os.path.join(GOLDEN, "lab_a_delta_toy.json")) as fh:
+        fx = json.load(fh)
+    assert fx["additive_final_state"] != fx["expected_final_state"]
+
+
+@pytest.mark.parametrize("dk,dv,T", [(6, 6, 8), (5, 3, 7), (3, 7, 8), (4, 4, 1)])
+def test_bruteforce_unrolling(dk, dv, T):
+    assert pin_bruteforce(dk=dk, dv=dv, T=T) < 1e-12
+
+
+@pytest.mark.parametrize("C", [1, 3, 16, 64])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 150])
+def test_chunkwise_rewrite(C, T):
+    assert pin_chunkwise(T=T, C=C, dk=8, dv=6) < 1e-10
+
+
+def test_chunkwise_rewrite_full_head_dim():
+    assert pin_chunkwise(dk=128, dv=128, T=200, C=64, seed=9) < 1e-10
+
+
+def test_closed_forms():
+    assert pin_closed_form_no_write() < 1e-12
+    assert pin_closed_form_first_token() < 1e-12
+    # g = 0, beta = 0: o_t = S_0^T q_t
+    q, k, v, g, beta, S0 = _rand_case(5, 8, 4, 8)
+    g[:] = 0
+    beta[:] = 0
+    o, _ = _run1(q, k, v, g, beta, S0)
+    assert rel_err(o, q.astype(np.float64) @ S0.astype(np.float64)) < 1e-12
+
+
+def test_norm_bound():
+    """||k|| = 1, beta in [0,1], g <= 0 make (I - beta k k^T) Diag(e^g) a contraction:
+    ||S_t||_2 <= ||S_{t-1}||_2 + beta_t ||v_t||."""
+    q, k, v, g, beta, S0 = _rand_case(40, 16, 16, 10)
+    S = S0
+    for t in range(40):
+        _, Sn = _run1(q[t:t + 1], k[t:t + 1], v[t:t + 1], g[t:t + 1], beta[t:t + 1], S.astype(np.float32))
+        lhs = np.linalg.norm(Sn, 2)
+        rhs = np.linalg.norm(S.astype(np.float32).astype(np.float64), 2) + beta[t] * np.linalg.norm(v[t])
+        assert lhs <= rhs * (1 + 1e-9)
+        S = Sn
+
+
+def test_varlen_equals_independent_runs_and_heads_independent():
+    rng = np.random.default_rng(12)
+    lens = [5, 1, 17, 9]
+    T, H, dk, dv = sum(lens), 3, 8, 6
+    cases = [_rand_case(T, dk, dv, 100 + h) for h in range(H)]
+    st = lambda i: np.ascontiguousarray(np.stack([c[i] for c in cases], axis=1))
+    q, k, v, g, beta = st(0), st(1), st(2), st(3), st(4)
+    S0 = (0.1 * rng.standard_normal((len(lens), H, dk, dv))).astype(np.float32)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    o, S = oracle.recurrent(q, k, v, g, beta, cu, S0, threads=4)
+    for n in range(len(lens)):
+        for h in range(H):
+            b, e = cu[n], cu[n + 1]
+            on, Sn = _run1(q[b:e, h], k[b:e, h], v[b:e, h], g[b:e, h], beta[b:e, h], S0[n, h])
+            assert np.array_equal(on, o[b:e, h])
+            assert np.array_equal(Sn, S[n, h])
+
+
+def test_chained_calls_equal_one_shot():
+    """Carrying final_state into init_state reproduces the one-shot run (up to the fp32 hand-off)."""
+    q, k, v, g, beta, S0 = _rand_case(50, 8, 8, 13)
+    o, S = _run1(q, k, v, g, beta, S0)
+    o1, S1 = _run1(q[:20], k[:20], v[:20], g[:20], beta[:20], S0)
+    o2, S2 = _run1(q[20:], k[20:], v[20:], g[20:], beta[20:], S1.astype(np.float32))
+    assert rel_err(np.concatenate([o1, o2]), o) < 1e-6
+    assert rel_err(S2, S) < 1e-6
+
+
+def test_bf16_inputs_widen_exactly():
+    import torch
+    q, k, v, g, beta, S0 = _rand_case(12, 8, 8, 14)
+    tb = lambda a: torch.from_numpy(a).to(torch.bfloat16)
+    qb, kb, vb = tb(q), tb(k), tb(v)
+    o_b, S_b = _run1(qb, kb, vb, g, beta, S0)
+    o_f, S_f = _run1(qb.float().numpy(), kb.float().numpy(), vb.float().numpy(), g, beta, S0)
+    assert np.array_equal(o_b, o_f) and np.array_equal(S_b, S_f)
+
+
+def test_bounded_decay_lab_b_closed_form():
+    """Lab B: with log-decay bounded below by g_min = -5, the largest reciprocal of the
+    cumulative decay inside an L-token tile is exp(5 (L - 1)).  L = 16 stays finite in
+    fp32 and bf16 (about 3.7e32); L = 64 (exp(315)) overflows both."""
+    f32_max = float(np.finfo(np.float32).max)
+    bf16_max = 3.3895313892515355e38
+    worst = lambda L: 5.0 * (L - 1)
+    assert np.exp(worst(16)) < bf16_max and np.exp(worst(16)) < f32_max
+    assert abs(np.exp(worst(16)) - 3.733241996799e32) / 3.733241996799e32 < 1e-9
+    assert worst(64) > np.log(f32_max)
+    # the sub-tile-relative factors used by the GPU path lie in [exp(-80), 1] and [1, exp(80)]
+    assert np.exp(-80.0) > np.finfo(np.float32).tiny and np.exp(80.0) < f32_max
+
+
+def test_oracle_rejects_bad_cu_seqlens():
+    q, k, v, g, beta, _ = _rand_case(4, 4, 4, 1)
+    with pytest.raises(ValueError):
+        oracle.recurrent(q[:, None], k[:, None], v[:, None], g[:, None], beta[:, None],
+                         np.array([0, 3, 2], dtype=np.int32))
+
+
+# ---------------------------------------------------------------- planted mistakes
+ALL_PINS = [pin_delta_invariant, pin_repeated_key_overwrites, pin_bruteforce, pin_chunkwise,
+            pin_closed_form_no_write, pin_closed_form_first_token]
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5])
+def test_each_planted_oracle_mistake_fails_a_pin(mutant, tmp_path):
+    path = oracle.build_oracle(mutant=mutant, out_dir=str(tmp_path))
+    assert oracle.kda_ref._lib(path=path).kda_oracle_mutant() == mutant
+    errs = {}
+    for pin in ALL_PINS:
+        # route the pin through the mutant build
+        saved = oracle.kda_ref._LIBS.get(mutant)
+        oracle.kda_ref._LIBS[mutant] = oracle.kda_ref._lib(path=path)
+        try:
+            errs[pin.__name__] = pin(mutant=mutant)
+        finally:
+            if saved is None:
+                oracle.kda_ref._LIBS.pop(mutant, None)
+            else:
+                oracle.kda_ref._LIBS[mutant] = saved
+    assert max(errs.values()) > 1e-3, errs
