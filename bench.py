@@ -1,0 +1,384 @@
+"""Benchmark of the KDA hot path on GB300: chunkwise prefill (headline) plus fused decode.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+One step = one ``kda_prefill`` call over the prefill workload (B=1, H=96,
+T=8192, dk=dv=128, bf16 q/k/v, fp32 g/beta/state, N(0,0.02) initial state,
+fp32 output): every stage of the chunkwise path.  The decode workload (B=256,
+H=96, dk=dv=128, 64 consecutive in-place steps) is timed in the same run and
+reported in the ``decode`` object.  Inputs are larger than L2 (1.41 GB prefill,
+1.61 GB decode state), so no flush is needed between iterations.
+
+Rank 0 prints one JSON line.  Under torchrun each rank runs its own independent
+copy of the workload (weak scaling, no collective on the data path).
+``--impl reference`` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import kda_workloads as W  # noqa: E402
+
+METRIC = "KDA prefill tokens/s (×tensor-peak %) and decode state GB/s (×HBM-peak %), 1 GB300"
+UNIT = "tokens/s"
+PREFILL_KERNEL_SRC = ("linear_attention_serving_chunkwise_gb300/csrc/kda_prefill_simt.cu",)
+
+
+# --------------------------------------------------------------------------- helpers
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def prefill_algorithmic(cfg: W.PrefillConfig):
+    """Algorithmic bytes and flops of one prefill call: inputs read once, output and
+    final state written once; flops of the chunkwise form with 64-token chunks."""
+    th = cfg.total_tokens * cfg.num_heads
+    e = 2 if cfg.qkv_dtype == torch.bfloat16 else 4
+    dk, dv, C = cfg.dk, cfg.dv, 64
+    per_th_bytes = e * (2 * dk + dv) + 4 * dk + 4 + 4 * dv
+    state_bytes = cfg.num_seqs * cfg.num_heads * dk * dv * 4 * (2 if cfg.init_state != "zero" else 1)
+    per_th_flops = (C - 1) * dk + (C + 1) * dk + (C + 1) * dv + (C + 1) * dk + (C + 1) * dv + 3 * 2 * dk * dv
+    return th * per_th_bytes + state_bytes, th * per_th_flops
+
+
+def decode_algorithmic(cfg: W.DecodeConfig):
+    """Bytes per decode step: state read + write, plus the per-token vectors and output."""
+    bh = cfg.batch * cfg.num_heads
+    e = 2 if cfg.qkv_dtype == torch.bfloat16 else 4
+    state = bh * cfg.dk * cfg.dv * 4 * 2
+    small = bh * (e * (2 * cfg.dk + cfg.dv) + 4 * cfg.dk + 4 + 4 * cfg.dv)
+    return state, state + small
+
+
+def _src_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(kernel_tag: str, src_hash: str):
+    """dram bytes per launch recorded by an ncu capture under profiles/, if the
+    capture was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
+    m_bytes = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", txt)
+    if not m_hash or not m_bytes or m_hash.group(1) != src_hash:
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- distributed plumbing
+def _dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- CPU oracle legs
+def oracle_sample(cfg: W.PrefillConfig, heads: int, tokens: int, seed: int = 0):
+    """Time the oracle, as it stands, on all host cores over a bounded sample of the prefill
+    workload (``heads`` heads x ``tokens`` tokens).  Returns (tokens/s scaled to all H heads,
+    seconds, cores, description)."""
+    import oracle
+    sub = W.PrefillConfig("sample", (tokens,), heads, cfg.dk, cfg.dv, cfg.qkv_dtype, cfg.init_state)
+    d = W.make_prefill_inputs(sub, seed=seed)
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.recurrent(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"], threads=cores)
+    dt = time.perf_counter() - t0
+    rate = tokens * heads / dt / cfg.num_heads
+    desc = (f"{heads} of {cfg.num_heads} heads x {tokens} tokens of the {cfg.name} workload, fp64 oracle, "
+            f"{cores} threads; tokens/s = token-heads/s / {cfg.num_heads}")
+    return rate, dt, cores, desc
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    cfg = W.prefill_config()
+    times, rates = [], []
+    heads, tokens = 16, 2048
+    for i in range(args.warmup + args.steps):
+        rate, dt, cores, desc = oracle_sample(cfg, heads, tokens, seed=i)
+        if i >= args.warmup:
+            times.append(dt)
+            rates.append(rate)
+    value = float(np.mean(rates))
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "global_batch": 1, "seq_len": 8192, "heads": 96, "dk": 128,
+                       "dv": 128, "qkv_dtype": "bf16", "l2": "inputs larger than L2"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- CUDA arm
+def _time_prefill(kda, d, out, fin, stream, steps, warmup):
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])
+    for _ in range(warmup):
+        kda.prefill(*args, out=out, final_state=fin, stream=stream)
+    stream.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    return args, evs
+
+
+def run_cuda(args, world, rank, local):
+    import linear_attention_serving_chunkwise_gb300 as kda
+    from linear_attention_serving_chunkwise_gb300.build import build
+
+    if rank == 0:
+        build()
+    _barrier(world)
+    kda.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = _peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    # ---------------- prefill: the headline step
+    cfg = W.prefill_config()
+    d = W.make_prefill_inputs(cfg, seed=rank, device=dev)   # one independent problem per rank
+    out = torch.empty((cfg.total_tokens, cfg.num_heads, cfg.dv), dtype=torch.float32, device=dev)
+    fin = torch.empty((1, cfg.num_heads, cfg.dk, cfg.dv), dtype=torch.float32, device=dev)
+    desc = kda.make_desc(1, cfg.total_tokens, cfg.num_heads, cfg.dk, cfg.dv, kda.KDA_BF16)
+    plan = kda.prefill_query(desc)
+    pargs, evs = _time_prefill(kda, d, out, fin, stream, args.steps, args.warmup)
+    if kda.last_device_status(stream) != kda.KDA_OK:
+        raise RuntimeError("prefill reported a device error during warm-up")
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        kda.prefill(*pargs, out=out, final_state=fin, stream=stream)
+        evs[i][1].record(stream)
+    end.record(stream)
+    stream.synchronize()
+    clocks = sampler.stop()
+    torch.cuda.synchronize()
+    _barrier(world)
+    if kda.last_device_status(stream) != kda.KDA_OK:
+        raise RuntimeError("prefill reported a device error in the timed region")
+    total_ms = _max_over_ranks(start.elapsed_time(end), world)
+    launch_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = cfg.total_tokens * world
+    value = tokens_per_step / (ms_per_step / 1e3)
+
+    alg_bytes, alg_flops = prefill_algorithmic(cfg)
+    achieved_gbs = alg_bytes / (launch_ms / 1e3) / 1e9
+    achieved_tflops = alg_flops / (launch_ms / 1e3) / 1e12
+    src_hash = _src_hash(PREFILL_KERNEL_SRC)
+    traffic = _profiled_traffic("kda_prefill", src_hash)
+    roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
+                "algorithmic_bytes_per_launch": alg_bytes, "kernel_launches_per_call": plan["kernel_launches"],
+                "launch_ms": launch_ms}
+    tensor = {"achieved": achieved_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+              "frac": achieved_tflops / peaks["bf16_tflops"], "algorithmic_flops_per_launch": alg_flops,
+              "uses_tensor_cores": bool(plan["tensor_cores"])}
+
+    # ---------------- end to end: pinned host inputs in, out + final state back, every step
+    host = {k: (None if v is None else v.to("cpu").pin_memory()) for k, v in d.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    host_fin = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = host_out.numel() * 4 + host_fin.numel() * 4
+    e2e_steps = max(1, min(args.steps, 20))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for k_, v_ in host.items():
+                if v_ is not None:
+                    d[k_].copy_(v_, non_blocking=True)
+            kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"], out=out,
+                        final_state=fin, stream=stream)
+            host_out.copy_(out, non_blocking=True)
+            host_fin.copy_(fin, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    stream.synchronize()
+    _barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    stream.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    e2e = {"value": tokens_per_step / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps}
+    del host, host_out, host_fin
+
+    # ---------------- decode: 64 consecutive in-place steps
+    dcfg = W.decode_config()
+    dd = W.make_decode_inputs(dcfg, seed=rank, device=dev)
+    state = dd["state0"]
+    dout = torch.empty((dcfg.batch, dcfg.num_heads, dcfg.dv), dtype=torch.float32, device=dev)
+    for s in range(3):
+        kda.decode(dd["q"][s], dd["k"][s], dd["v"][s], dd["g"][s], dd["beta"][s], state, out=dout, stream=stream)
+    stream.synchronize()
+    devs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dcfg.steps)]
+    _barrier(world)
+    for s in range(dcfg.steps):
+        devs[s][0].record(stream)
+        kda.decode(dd["q"][s], dd["k"][s], dd["v"][s], dd["g"][s], dd["beta"][s], state, out=dout, stream=stream)
+        devs[s][1].record(stream)
+    stream.synchronize()
+    dstep_ms = float(np.mean([a.elapsed_time(b) for a, b in devs]))
+    dstep_ms = _max_over_ranks(dstep_ms, world)
+    state_bytes, all_bytes = decode_algorithmic(dcfg)
+    decode = {"workload": dcfg.name, "steps": dcfg.steps, "ms_per_step": dstep_ms,
+              "tokens_per_s": dcfg.batch * world / (dstep_ms / 1e3),
+              "state_gbs": state_bytes / (dstep_ms / 1e3) / 1e9,
+              "all_bytes_gbs": all_bytes / (dstep_ms / 1e3) / 1e9,
+              "roofline": {"bound": "hbm", "achieved": all_bytes / (dstep_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": all_bytes / (dstep_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                           "traffic": _profiled_traffic("kda_decode", _src_hash(
+                               ("linear_attention_serving_chunkwise_gb300/csrc/kda_decode.cu",))),
+                           "algorithmic_bytes_per_launch": all_bytes},
+              "gpu_launches": dcfg.steps}
+    del dd, state
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if plan["tensor_cores"] else "f32", "data": "synthetic",
+            "config": {"workload": cfg.name, "global_batch": world, "seq_len": cfg.total_tokens,
+                       "heads": cfg.num_heads, "dk": cfg.dk, "dv": cfg.dv, "qkv_dtype": "bf16",
+                       "init_state": "N(0,0.02)", "l2": "inputs larger than L2 (1.41 GB per step), no flush",
+                       "parallelism": f"independent problem per GPU x{world}"},
+            "roofline": roofline, "tensor": tensor, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": args.steps * plan["kernel_launches"], "decode": decode}
+    if rank == 0 and world == 1:
+        rate, dt, cores, sdesc = oracle_sample(cfg, heads=32, tokens=8192)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sdesc,
+                                "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    world, rank, local = _dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_cuda(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,159 @@
+/*
+ * kda.h -- C ABI of the Kimi Delta Attention (KDA) library for one GB300 (sm_103a).
+ *
+ * KDA is a gated delta rule with channel-wise decay.  Per (sequence, head) it
+ * carries a key-by-value state S (dk x dv, fp32) and, for each token t,
+ *
+ *     S_t = (I - beta_t k_t k_t^T) . Diag(exp g_t) . S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t
+ *
+ * Sources (Kimi K3 report as summarised on the llm-atlas page "K3_RESEARCH.md"):
+ * question ledger Q04 (fixed-shape recurrent state, channel-wise decay,
+ * delta-rule write), Q05 (the write subtracts the state's prediction for the
+ * current key), Q06 and Figure 3 (log-decay bounded below by g_min = -5 so the
+ * diagonal tile can use BF16 tensor-core matmuls), Q07 (chunkwise-parallel
+ * prefill with the state passed between chunks; O(1) state update for decode),
+ * Q10 (attention output kept in FP32), and section 8's device layer ("fused
+ * decode").  The agihunt digest page adds that FlashKDA cuts chunks further into
+ * 16-token tiles for numerical stability.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are caller-owned DEVICE memory of the current CUDA
+ *     device, contiguous, 16-byte aligned (beta and cu_seqlens: 4-byte
+ *     aligned).  The library allocates nothing.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Work is enqueued asynchronously on it; the call returns at once.
+ *   - Argument errors are detected on the host and returned synchronously,
+ *     before anything is enqueued.  A failed launch returns KDA_ERR_CUDA.
+ *   - Errors found on the device (a bad cu_seqlens entry, a bounded wait that
+ *     gave up) are recorded in a per-device status word; the affected work is
+ *     skipped, nothing traps.  kda_last_device_status() reports and clears it.
+ *   - q is not scaled (no 1/sqrt(dk)); callers pre-scale q if they want that.
+ *   - Preconditions not checked on the host: g in [-5, 0] (the bounded
+ *     log-decay; never clamped), beta in [0, 1].  Values outside these ranges
+ *     are unsupported: they are computed, but without the accuracy bound.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_ABI_VERSION 1
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, bad size, aliasing, bad cu_seqlens */
+    KDA_ERR_UNSUPPORTED = -2,   /* head dims other than dk == dv in {64, 128}, unknown dtype */
+    KDA_ERR_WORKSPACE = -3,     /* workspace smaller than kda_prefill_workspace_bytes() */
+    KDA_ERR_CUDA = -4,          /* a CUDA runtime call or kernel launch failed */
+    KDA_ERR_TIMEOUT = -5        /* a bounded on-device wait gave up (work skipped) */
+} kda_status;
+
+/* Storage type of q, k, v.  g, beta, states and outputs are always fp32. */
+typedef enum kda_dtype {
+    KDA_F32 = 0,
+    KDA_BF16 = 1
+} kda_dtype;
+
+/* Shape of one prefill call. */
+typedef struct kda_prefill_desc {
+    int32_t num_seqs;       /* N >= 0 packed sequences */
+    int32_t total_tokens;   /* T >= 0, sum of all sequence lengths */
+    int32_t num_heads;      /* H >= 1 */
+    int32_t dk;             /* key/query channels: 64 or 128 */
+    int32_t dv;             /* value channels: must equal dk */
+    int32_t qkv_dtype;      /* a kda_dtype */
+} kda_prefill_desc;
+
+/* Library ABI version (KDA_ABI_VERSION of the build). */
+int32_t kda_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* kda_status_string(kda_status status);
+
+/*
+ * Bytes of device scratch memory kda_prefill needs for `desc` (may be 0).
+ * Returns 0 for a desc that kda_prefill would reject.
+ */
+size_t kda_prefill_workspace_bytes(const kda_prefill_desc* desc);
+
+/* What one kda_prefill call for a given desc will do (for harnesses and tracing). */
+typedef struct kda_prefill_plan {
+    int32_t kernel_launches;   /* kernels one call enqueues */
+    int32_t tensor_cores;      /* 1: BF16 tcgen05 path; 0: fp32 CUDA-core path */
+    size_t workspace_bytes;    /* same as kda_prefill_workspace_bytes(desc) */
+} kda_prefill_plan;
+
+/*
+ * Fills *plan for `desc`.  Host only, no CUDA call.  KDA_ERR_INVALID_ARG or
+ * KDA_ERR_UNSUPPORTED for a desc that kda_prefill would reject.
+ */
+kda_status kda_prefill_query(const kda_prefill_desc* desc, kda_prefill_plan* plan);
+
+/*
+ * kda_prefill -- chunkwise-parallel KDA over varlen-packed sequences
+ * (llm-atlas K3_RESEARCH.md, Q07: state passed recursively between chunks,
+ * parallel matrix work inside a chunk; agihunt digest: 16-token tiles).
+ *
+ * Layouts (T = total_tokens, H = num_heads, N = num_seqs):
+ *   q, k        [T, H, dk]   qkv_dtype
+ *   v           [T, H, dv]   qkv_dtype
+ *   g           [T, H, dk]   fp32, natural-log decay per key channel
+ *   beta        [T, H]       fp32
+ *   cu_seqlens  [N + 1]      int32, cu[0] = 0, non-decreasing, cu[N] = T;
+ *                            NULL = N equal sequences (T % N must be 0)
+ *   init_state  [N, H, dk, dv] fp32 (row c = key channel c); NULL = zero state
+ *   out         [T, H, dv]   fp32, written for every token
+ *   final_state [N, H, dk, dv] fp32; NULL = not written.  May be the same
+ *                            pointer as init_state (in-place chaining of calls);
+ *                            any other overlap with an input is rejected.
+ *   workspace   device scratch of at least kda_prefill_workspace_bytes(desc)
+ *               (may be NULL when that is 0); its contents need no set-up and
+ *               are clobbered.  Two calls in flight at once need two workspaces.
+ * A cu_seqlens entry that breaks the rules above is found on the device: that
+ * sequence is skipped and kda_last_device_status() returns KDA_ERR_INVALID_ARG.
+ */
+kda_status kda_prefill(const kda_prefill_desc* desc,
+                       const void* q, const void* k, const void* v,
+                       const float* g, const float* beta,
+                       const int32_t* cu_seqlens,
+                       const float* init_state,
+                       float* out, float* final_state,
+                       void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/*
+ * kda_decode -- one token per sequence, as a fused O(1) update of each head's
+ * state: a single read and a single write of S (llm-atlas K3_RESEARCH.md, Q07
+ * "decode keeps the O(1) state update"; section 8 device layer "fused decode").
+ *
+ * Layouts (B = batch):
+ *   q, k   [B, H, dk]  qkv_dtype;     v [B, H, dv] qkv_dtype
+ *   g      [B, H, dk]  fp32;          beta [B, H] fp32
+ *   state  [B, H, dk, dv] fp32, read and overwritten in place
+ *   out    [B, H, dv] fp32 (o = S_new^T q); must not overlap any input or state
+ */
+kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, int32_t qkv_dtype,
+                      const void* q, const void* k, const void* v,
+                      const float* g, const float* beta,
+                      float* state, float* out,
+                      void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of the
+ * current device: KDA_OK, KDA_ERR_INVALID_ARG (bad cu_seqlens seen on the
+ * device) or KDA_ERR_TIMEOUT (a bounded wait gave up).  KDA_ERR_CUDA if the
+ * synchronisation itself fails.
+ */
+kda_status kda_last_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,27 @@
+"""Kimi Delta Attention (KDA) on one GB300: chunkwise prefill and fused decode.
+
+The compute lives in the CUDA library ``libkda_gb300.so`` behind the C ABI in
+``include/kda.h``; this package is the thin ctypes binding over it.
+"""
+from ._lib import (  # noqa: F401
+    EXPORTED,
+    KDA_BF16,
+    KDA_ERR_CUDA,
+    KDA_ERR_INVALID_ARG,
+    KDA_ERR_TIMEOUT,
+    KDA_ERR_UNSUPPORTED,
+    KDA_ERR_WORKSPACE,
+    KDA_F32,
+    KDA_OK,
+    KDAError,
+    LIB_PATH,
+    PrefillDesc,
+    decode,
+    last_device_status,
+    load,
+    make_desc,
+    prefill,
+    prefill_query,
+    prefill_workspace_bytes,
+    status_string,
+)

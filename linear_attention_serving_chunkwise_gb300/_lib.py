@@ -1,0 +1,171 @@
+"""ctypes binding of the KDA C ABI (include/kda.h).
+
+Argument marshalling only: every step of prefill and decode runs in the CUDA
+library ``libkda_gb300.so``.  PyTorch supplies device memory and streams.  There
+is no fallback: if the library is missing or fails to load, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda_gb300.so")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = -1
+KDA_ERR_UNSUPPORTED = -2
+KDA_ERR_WORKSPACE = -3
+KDA_ERR_CUDA = -4
+KDA_ERR_TIMEOUT = -5
+KDA_F32 = 0
+KDA_BF16 = 1
+
+# Every symbol include/kda.h declares.
+EXPORTED = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes", "kda_prefill_query",
+            "kda_prefill", "kda_decode", "kda_last_device_status")
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+class PrefillDesc(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32)]
+
+
+class PrefillPlan(ctypes.Structure):
+    _fields_ = [("kernel_launches", ctypes.c_int32), ("tensor_cores", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the CUDA library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"KDA CUDA library not built ({p} missing): run "
+                           "`python -m linear_attention_serving_chunkwise_gb300.build`")
+    lib = ctypes.CDLL(p)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    lib.kda_abi_version.restype = i32
+    lib.kda_abi_version.argtypes = []
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_prefill_workspace_bytes.restype = sz
+    lib.kda_prefill_workspace_bytes.argtypes = [ctypes.POINTER(PrefillDesc)]
+    lib.kda_prefill_query.restype = ctypes.c_int
+    lib.kda_prefill_query.argtypes = [ctypes.POINTER(PrefillDesc), ctypes.POINTER(PrefillPlan)]
+    lib.kda_prefill.restype = ctypes.c_int
+    lib.kda_prefill.argtypes = [ctypes.POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.kda_decode.restype = ctypes.c_int
+    lib.kda_decode.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.kda_last_device_status.restype = ctypes.c_int
+    lib.kda_last_device_status.argtypes = [vp]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"q/k/v must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("KDA tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() > 0 else None
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_desc(num_seqs: int, total_tokens: int, num_heads: int, dk: int, dv: int, qkv_dtype: int) -> PrefillDesc:
+    return PrefillDesc(int(num_seqs), int(total_tokens), int(num_heads), int(dk), int(dv), int(qkv_dtype))
+
+
+def prefill_workspace_bytes(desc: PrefillDesc) -> int:
+    return int(load().kda_prefill_workspace_bytes(ctypes.byref(desc)))
+
+
+def prefill_query(desc: PrefillDesc) -> dict:
+    """What one kda_prefill call for ``desc`` will launch (host only)."""
+    plan = PrefillPlan()
+    st = load().kda_prefill_query(ctypes.byref(desc), ctypes.byref(plan))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_prefill_query")
+    return {"kernel_launches": plan.kernel_launches, "tensor_cores": plan.tensor_cores,
+            "workspace_bytes": plan.workspace_bytes}
+
+
+def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_state=None, *,
+            num_seqs: Optional[int] = None, want_final: bool = True, workspace=None, stream=None, check=True):
+    """KDA prefill through ``kda_prefill``.
+
+    q, k [T,H,dk], v [T,H,dv] (fp32 or bf16); g [T,H,dk] fp32; beta [T,H] fp32;
+    cu_seqlens [N+1] int32 on the device, or None with ``num_seqs`` equal
+    sequences (default 1); init_state [N,H,dk,dv] fp32 or None.
+    ``out``/``final_state`` are allocated if not given (``final_state`` may be
+    ``init_state`` for in-place chaining).  Returns (out, final_state)."""
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
+    desc = make_desc(N, T, H, dk, dv, _dtype_code(q))
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=torch.float32, device=q.device)
+    if final_state is None and want_final:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    need = prefill_workspace_bytes(desc)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().kda_prefill(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+                            _ptr(init_state), _ptr(out), _ptr(final_state), _ptr(workspace), ws_bytes,
+                            _stream_handle(stream))
+    if check and st != KDA_OK:
+        raise KDAError(st, "kda_prefill")
+    return out, final_state
+
+
+def decode(q, k, v, g, beta, state, out=None, *, stream=None, check=True):
+    """One KDA decode step through ``kda_decode``; ``state`` [B,H,dk,dv] fp32 is updated in place.
+
+    q, k [B,H,dk], v [B,H,dv] (fp32 or bf16); g [B,H,dk] fp32; beta [B,H] fp32.
+    Returns out [B,H,dv] fp32."""
+    B, H, dk = q.shape
+    dv = v.shape[2]
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
+    st = load().kda_decode(B, H, dk, dv, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                           _ptr(state), _ptr(out), _stream_handle(stream))
+    if check and st != KDA_OK:
+        raise KDAError(st, "kda_decode")
+    return out
+
+
+def last_device_status(stream=None) -> int:
+    return int(load().kda_last_device_status(_stream_handle(stream)))

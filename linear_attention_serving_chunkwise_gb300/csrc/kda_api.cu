@@ -1,0 +1,198 @@
+// C ABI of the KDA library: host-side validation, workspace sizing, dispatch
+// and the per-device status word.  Declarations and contracts: include/kda.h.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/kda.h"
+#include "kda_common.cuh"
+#include "kda_launch.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Per-device error word written by kernels (first error wins).
+__device__ int g_kda_device_status;
+
+int* status_ptr_for_current_device()
+{
+    static std::mutex mu;
+    static int* ptrs[kMaxDevices] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_kda_device_status) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int*>(p);
+    }
+    return ptrs[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+Range range_of(const void* p, size_t bytes)
+{
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + bytes};
+}
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo; }
+
+bool supported_dims(int dk, int dv) { return dk == dv && (dk == 64 || dk == 128); }
+
+kda_status validate_prefill(const kda_prefill_desc* d)
+{
+    if (!d) return KDA_ERR_INVALID_ARG;
+    if (d->num_seqs < 0 || d->total_tokens < 0 || d->num_heads < 1 || d->num_heads > 65535)
+        return KDA_ERR_INVALID_ARG;
+    if (d->qkv_dtype != KDA_F32 && d->qkv_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!supported_dims(d->dk, d->dv)) return KDA_ERR_UNSUPPORTED;
+    if (d->num_seqs == 0 && d->total_tokens != 0) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+const char* kda_status_string(kda_status s)
+{
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: unsupported shape or dtype (dk == dv in {64, 128})";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace too small";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime or launch failure";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait gave up";
+    }
+    return "KDA: unknown status";
+}
+
+size_t kda_prefill_workspace_bytes(const kda_prefill_desc* desc)
+{
+    if (validate_prefill(desc) != KDA_OK) return 0;
+    return 0;
+}
+
+kda_status kda_prefill_query(const kda_prefill_desc* desc, kda_prefill_plan* plan)
+{
+    const kda_status st = validate_prefill(desc);
+    if (st != KDA_OK) return st;
+    if (!plan) return KDA_ERR_INVALID_ARG;
+    plan->kernel_launches = desc->num_seqs > 0 ? 1 : 0;
+    plan->tensor_cores = 0;
+    plan->workspace_bytes = kda_prefill_workspace_bytes(desc);
+    return KDA_OK;
+}
+
+kda_status kda_prefill(const kda_prefill_desc* desc, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const int32_t* cu_seqlens,
+                       const float* init_state, float* out, float* final_state,
+                       void* workspace, size_t workspace_bytes, void* stream)
+{
+    kda_status st = validate_prefill(desc);
+    if (st != KDA_OK) return st;
+    const kda_prefill_desc d = *desc;
+    if (!cu_seqlens && d.num_seqs > 0 && d.total_tokens % d.num_seqs != 0) return KDA_ERR_INVALID_ARG;
+    if (workspace_bytes < kda_prefill_workspace_bytes(desc)) return KDA_ERR_WORKSPACE;
+    if (d.num_seqs == 0) return KDA_OK;
+
+    const size_t T = (size_t)d.total_tokens, H = (size_t)d.num_heads, N = (size_t)d.num_seqs;
+    const size_t esz = d.qkv_dtype == KDA_BF16 ? 2 : 4;
+    if (T > 0) {
+        if (!q || !k || !v || !g || !beta || !out) return KDA_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(out))
+            return KDA_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(beta) & 3u) return KDA_ERR_INVALID_ARG;
+    }
+    if (init_state && !aligned16(init_state)) return KDA_ERR_INVALID_ARG;
+    if (final_state && !aligned16(final_state)) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
+
+    // outputs must not overlap inputs (init_state == final_state exactly is allowed)
+    const size_t sbytes = N * H * d.dk * d.dv * sizeof(float);
+    const Range r_out = range_of(out, T * H * d.dv * sizeof(float));
+    const Range r_fin = range_of(final_state, final_state ? sbytes : 0);
+    const Range ins[] = {range_of(q, T * H * d.dk * esz), range_of(k, T * H * d.dk * esz),
+                         range_of(v, T * H * d.dv * esz), range_of(g, T * H * d.dk * sizeof(float)),
+                         range_of(beta, T * H * sizeof(float)),
+                         range_of(cu_seqlens, cu_seqlens ? (N + 1) * sizeof(int32_t) : 0),
+                         range_of(init_state, init_state ? sbytes : 0)};
+    for (const Range& r : ins) {
+        if (T > 0 && overlaps(r_out, r)) return KDA_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < 6; ++i) {
+        if (final_state && overlaps(r_fin, ins[i])) return KDA_ERR_INVALID_ARG;
+    }
+    if (final_state && init_state && final_state != init_state && overlaps(r_fin, ins[6]))
+        return KDA_ERR_INVALID_ARG;
+    if (final_state && T > 0 && overlaps(r_fin, r_out)) return KDA_ERR_INVALID_ARG;
+
+    int* status = status_ptr_for_current_device();
+    if (!status) return KDA_ERR_CUDA;
+
+    kda::PrefillArgs a;
+    a.num_seqs = d.num_seqs; a.total_tokens = d.total_tokens; a.num_heads = d.num_heads;
+    a.dk = d.dk; a.dv = d.dv; a.bf16 = d.qkv_dtype == KDA_BF16;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu_seqlens = cu_seqlens;
+    a.init_state = init_state; a.out = out; a.final_state = final_state;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.status = status;
+    const cudaError_t e = kda::launch_prefill_simt(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, int32_t qkv_dtype,
+                      const void* q, const void* k, const void* v, const float* g, const float* beta,
+                      float* state, float* out, void* stream)
+{
+    if (batch < 0 || num_heads < 1) return KDA_ERR_INVALID_ARG;
+    if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!supported_dims(dk, dv)) return KDA_ERR_UNSUPPORTED;
+    const size_t BH = (size_t)batch * num_heads;
+    if (BH > 0x7fffffffull) return KDA_ERR_INVALID_ARG;
+    if (BH == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(state) || !aligned16(out))
+        return KDA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(beta) & 3u) return KDA_ERR_INVALID_ARG;
+    const size_t esz = qkv_dtype == KDA_BF16 ? 2 : 4;
+    const Range r_state = range_of(state, BH * dk * dv * sizeof(float));
+    const Range r_out = range_of(out, BH * dv * sizeof(float));
+    const Range ins[] = {range_of(q, BH * dk * esz), range_of(k, BH * dk * esz), range_of(v, BH * dv * esz),
+                         range_of(g, BH * dk * sizeof(float)), range_of(beta, BH * sizeof(float))};
+    for (const Range& r : ins) {
+        if (overlaps(r_out, r) || overlaps(r_state, r)) return KDA_ERR_INVALID_ARG;
+    }
+    if (overlaps(r_out, r_state)) return KDA_ERR_INVALID_ARG;
+
+    kda::DecodeArgs a;
+    a.batch = batch; a.num_heads = num_heads; a.dk = dk; a.dv = dv; a.bf16 = qkv_dtype == KDA_BF16;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state = state; a.out = out;
+    const cudaError_t e = kda::launch_decode(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_last_device_status(void* stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
+    int* p = status_ptr_for_current_device();
+    if (!p) return KDA_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return KDA_ERR_CUDA;
+    switch (h) {
+        case kda::kDevOk: return KDA_OK;
+        case kda::kDevBadSeqlens: return KDA_ERR_INVALID_ARG;
+        case kda::kDevTimeout: return KDA_ERR_TIMEOUT;
+        default: return KDA_ERR_CUDA;
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,57 @@
+// Shared device helpers of the KDA library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Device status codes (mirror kda_status in include/kda.h).
+constexpr int kDevOk = 0;
+constexpr int kDevBadSeqlens = -1;
+constexpr int kDevTimeout = -5;
+
+__device__ __forceinline__ void report_status(int* status, int code)
+{
+    // first error wins; later ones are dropped
+    atomicCAS(status, kDevOk, code);
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Read 4 consecutive elements starting at a 4-element-aligned index.
+__device__ __forceinline__ float4 load4(const float* p)
+{
+    return __ldg(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p)
+{
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+    float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+    return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+
+// Sequence bounds [bos, eos) for sequence n, validated against total_tokens.
+// Returns false (and records a device error) for a malformed cu_seqlens entry.
+__device__ __forceinline__ bool seq_bounds(const int32_t* cu_seqlens, int n, int num_seqs, int total_tokens,
+                                           int* status, int& bos, int& eos)
+{
+    if (cu_seqlens == nullptr) {
+        const int len = total_tokens / num_seqs;
+        bos = n * len;
+        eos = bos + len;
+        return true;
+    }
+    bos = cu_seqlens[n];
+    eos = cu_seqlens[n + 1];
+    const bool ok = (bos >= 0) && (eos >= bos) && (eos <= total_tokens) &&
+                    (n != 0 || bos == 0) && (n != num_seqs - 1 || eos == total_tokens);
+    if (!ok) report_status(status, kDevBadSeqlens);
+    return ok;
+}
+
+}  // namespace kda

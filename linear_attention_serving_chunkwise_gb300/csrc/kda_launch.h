@@ -1,0 +1,36 @@
+// Internal launchers of the KDA library (host side).  Not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+
+struct PrefillArgs {
+    int num_seqs, total_tokens, num_heads, dk, dv;
+    bool bf16;
+    const void *q, *k, *v;
+    const float *g, *beta;
+    const int32_t* cu_seqlens;
+    const float* init_state;
+    float *out, *final_state;
+    void* workspace;
+    size_t workspace_bytes;
+    int* status;  // device status word
+};
+
+struct DecodeArgs {
+    int batch, num_heads, dk, dv;
+    bool bf16;
+    const void *q, *k, *v;
+    const float *g, *beta;
+    float *state, *out;
+};
+
+// fp32 CUDA-core chunkwise prefill (any supported shape, fp32 or bf16 inputs)
+cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
+// fused single-pass decode
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace kda

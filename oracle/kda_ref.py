@@ -227,6 +227,8 @@ def rel_err(x, ref) -> float:
     """max |x - ref| / RMS(ref), the error measure of the parity bar."""
     x = _f64(x)
     ref = _f64(ref)
+    if ref.size == 0:
+        return 0.0
     rms = float(np.sqrt(np.mean(ref * ref)))
     if rms == 0.0:
         return float(np.max(np.abs(x - ref))) if x.size else 0.0

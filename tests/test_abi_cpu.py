@@ -1,0 +1,115 @@
+"""The C-ABI library loads and exports every symbol include/kda.h declares; host-side
+argument checks return their codes before anything reaches a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_serving_chunkwise_gb300 as kda
+from linear_attention_serving_chunkwise_gb300 import _lib
+from linear_attention_serving_chunkwise_gb300.build import LIB, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return kda.load()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert {"kda_prefill", "kda_decode", "kda_prefill_workspace_bytes"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(_lib.EXPORTED) == declared
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.kda_abi_version() == 1
+    for code in (0, -1, -2, -3, -4, -5):
+        assert kda.status_string(code).startswith("KDA")
+    assert "unknown" in kda.status_string(-99)
+
+
+def _fake(addr):
+    # host-side validation never dereferences these
+    return ctypes.c_void_p(addr)
+
+
+def _prefill(lib, desc, q=0x10000, k=0x20000, v=0x30000, g=0x40000, beta=0x50000, cu=None, s0=None,
+             out=0x60000, fin=None, ws=None, ws_bytes=0):
+    p = lambda a: None if a is None else _fake(a)
+    return lib.kda_prefill(ctypes.byref(desc) if desc is not None else None, p(q), p(k), p(v), p(g), p(beta),
+                           p(cu), p(s0), p(out), p(fin), p(ws), ws_bytes, None)
+
+
+def test_prefill_rejects_bad_arguments_on_host(lib):
+    d = kda.make_desc(1, 64, 2, 64, 64, kda.KDA_F32)
+    assert _prefill(lib, None) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill(lib, kda.make_desc(1, 64, 2, 96, 96, kda.KDA_F32)) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(lib, kda.make_desc(1, 64, 2, 128, 64, kda.KDA_F32)) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(lib, kda.make_desc(1, 64, 2, 64, 64, 7)) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(lib, kda.make_desc(-1, 64, 2, 64, 64, 0)) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill(lib, kda.make_desc(1, 64, 0, 64, 64, 0)) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill(lib, kda.make_desc(0, 64, 2, 64, 64, 0)) == kda.KDA_ERR_INVALID_ARG
+    # equal split needs T % N == 0
+    assert _prefill(lib, kda.make_desc(3, 64, 2, 64, 64, 0)) == kda.KDA_ERR_INVALID_ARG
+    # null required pointer
+    assert _prefill(lib, d, q=None) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill(lib, d, out=None) == kda.KDA_ERR_INVALID_ARG
+    # misaligned pointer
+    assert _prefill(lib, d, k=0x20008) == kda.KDA_ERR_INVALID_ARG
+    # out aliasing an input
+    assert _prefill(lib, d, out=0x10000) == kda.KDA_ERR_INVALID_ARG
+    # final_state overlapping out
+    assert _prefill(lib, d, fin=0x60000 + 64) == kda.KDA_ERR_INVALID_ARG
+    # nothing to do: zero sequences
+    assert _prefill(lib, kda.make_desc(0, 0, 2, 64, 64, 0)) == kda.KDA_OK
+
+
+def test_workspace_query(lib):
+    d = kda.make_desc(4, 1000, 8, 128, 128, kda.KDA_BF16)
+    n = kda.prefill_workspace_bytes(d)
+    assert n >= 0
+    assert kda.prefill_workspace_bytes(kda.make_desc(4, 1000, 8, 96, 96, kda.KDA_BF16)) == 0
+    if n > 0:
+        assert _prefill(lib, d, ws=0x70000, ws_bytes=n - 1) == kda.KDA_ERR_WORKSPACE
+
+
+def test_prefill_query(lib):
+    plan = kda.prefill_query(kda.make_desc(1, 8192, 96, 128, 128, kda.KDA_BF16))
+    assert plan["kernel_launches"] >= 1 and plan["workspace_bytes"] >= 0
+    assert kda.prefill_query(kda.make_desc(0, 0, 4, 64, 64, kda.KDA_F32))["kernel_launches"] == 0
+    with pytest.raises(kda.KDAError):
+        kda.prefill_query(kda.make_desc(1, 10, 4, 96, 96, kda.KDA_F32))
+
+
+def test_decode_rejects_bad_arguments_on_host(lib):
+    f = _fake
+    args = lambda **kw: [kw.get(n, f(a)) for n, a in
+                         (("q", 0x10000), ("k", 0x20000), ("v", 0x30000), ("g", 0x40000), ("beta", 0x50000),
+                          ("state", 0x100000), ("out", 0x60000))]
+    assert lib.kda_decode(2, 2, 96, 96, 0, *args(), None) == kda.KDA_ERR_UNSUPPORTED
+    assert lib.kda_decode(2, 2, 64, 64, 5, *args(), None) == kda.KDA_ERR_UNSUPPORTED
+    assert lib.kda_decode(-1, 2, 64, 64, 0, *args(), None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode(2, 2, 64, 64, 0, *args(q=None), None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode(2, 2, 64, 64, 0, *args(out=f(0x100000)), None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode(2, 2, 64, 64, 0, *args(g=f(0x40004)), None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode(0, 2, 64, 64, 0, *args(), None) == kda.KDA_OK
+
+
+def test_library_is_in_tree():
+    assert os.path.dirname(LIB) == os.path.dirname(_lib.__file__)
