@@ -361,13 +361,43 @@ def run_cuda(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_ncu_case(case: str):
+    """A small, self-contained launch for ncu captures (no timing, no JSON): the same kernels
+    as the bench on inputs still larger than L2 but only a few hundred MB on the device.
+      prefill: B=1, H=32, T=8192, dk=dv=128, bf16 (470 MB of inputs/outputs)
+      decode:  B=64, H=96, dk=dv=128, bf16, one step (403 MB of state)"""
+    import linear_attention_serving_chunkwise_gb300 as kda
+    from linear_attention_serving_chunkwise_gb300.build import build
+    build()
+    kda.load()
+    if case == "prefill":
+        cfg = W.PrefillConfig("ncu_prefill_h32_t8192", (8192,), 32, 128, 128, torch.bfloat16, "normal")
+        d = W.make_prefill_inputs(cfg, seed=0, device="cuda")
+        for _ in range(2):
+            kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])
+    else:
+        cfg = W.DecodeConfig("ncu_decode_b64_h96", 64, 96, 128, 128, torch.bfloat16, 2)
+        d = W.make_decode_inputs(cfg, seed=0, device="cuda")
+        st = d["state0"]
+        for s in range(2):
+            kda.decode(d["q"][s], d["k"][s], d["v"][s], d["g"][s], d["beta"][s], st)
+    torch.cuda.synchronize()
+    if kda.last_device_status() != kda.KDA_OK:
+        raise SystemExit("device error")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--ncu-case", default=None, choices=["prefill", "decode"],
+                    help="run one small launch pair for an ncu capture and exit")
     args = ap.parse_args()
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+        return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     world, rank, local = _dist_setup(args.gpus)

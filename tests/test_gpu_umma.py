@@ -1,0 +1,49 @@
+"""GPU self-test of the tcgen05 primitives the tensor-core prefill is built from:
+shared-memory descriptors (128-byte swizzle, K-major and MN-major), the bf16
+instruction descriptor, TMEM allocation, tcgen05.mma / commit / ld / st and the
+A-negate bit, against a torch fp32 matmul of the same bf16 values."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def selftest(tmp_path_factory):
+    out = str(tmp_path_factory.mktemp("umma") / "umma_selftest.so")
+    src = os.path.join(ROOT, "tests", "csrc", "umma_selftest.cu")
+    inc = os.path.join(ROOT, "linear_attention_serving_chunkwise_gb300", "csrc")
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-std=c++17", "-shared",
+                    "-Xcompiler", "-fPIC", "-I", inc, src, "-o", out], check=True)
+    lib = ctypes.CDLL(out)
+    lib.umma_selftest.restype = ctypes.c_int
+    lib.umma_selftest.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    return lib
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("K", [64, 128])
+def test_umma_tile(selftest, mode, K):
+    g = torch.Generator(device="cuda").manual_seed(100 * mode + K)
+    A = torch.randn((128, K), generator=g, device="cuda").to(torch.bfloat16)   # math A [M, K]
+    Bm = torch.randn((K, 128), generator=g, device="cuda").to(torch.bfloat16)  # math B [K, N]
+    C = torch.randn((128, 128), generator=g, device="cuda")
+    a_store = A.t().contiguous() if mode == 2 else A.contiguous()
+    b_store = Bm.t().contiguous() if mode == 0 else Bm.contiguous()
+    D = torch.full((128, 128), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = selftest.umma_selftest(a_store.data_ptr(), b_store.data_ptr(), C.data_ptr(), D.data_ptr(), K, mode,
+                                err.data_ptr())
+    assert rc == 0 and int(err.item()) == 0
+    ref = A.float() @ Bm.float()
+    if mode == 3:
+        ref = C - ref
+    assert torch.isfinite(D).all()
+    rel = ((D - ref).abs().max() / ref.abs().max()).item()
+    assert rel < 1e-5, f"mode {mode} K {K}: rel err {rel:.3e}"
