@@ -13,6 +13,9 @@ using namespace kda::sm100;
 // mode 1: A K-major [128][K], B MN-major [K][128]
 // mode 2: A MN-major [K][128], B MN-major [K][128]
 // mode 3: as mode 1, with D preloaded from C through tcgen05.st and A negated: D = C - A*B
+// mode 4: as mode 1, with A read from TMEM (row m in lane m, bf16 pairs per column)
+// mode 5: M = 64, A K-major [64][K], B MN-major; all 128 lanes are read back so the
+//         test can locate the 64 result rows
 __global__ void __launch_bounds__(128, 1) umma_selftest_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B,
                                                                const float* C, float* D, int K, int mode, int* err)
 {
@@ -24,13 +27,16 @@ __global__ void __launch_bounds__(128, 1) umma_selftest_kernel(const __nv_bfloat
     __shared__ uint32_t tslot;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const bool a_mn = (mode == 2), b_mn = (mode != 0);
+    const int M = (mode == 5) ? 64 : 128;
 
     for (int idx = t; idx < 128 * K; idx += 128) {
         // A(m, k)
         const int m = idx / K, k = idx % K;
-        const __nv_bfloat16 av = a_mn ? A[k * 128 + m] : A[m * K + k];
-        const uint32_t aoff = a_mn ? sw128_off(k, m, K) : sw128_off(m, k, 128);
-        *reinterpret_cast<__nv_bfloat16*>(sA + aoff) = av;
+        if (m < M) {
+            const __nv_bfloat16 av = a_mn ? A[k * 128 + m] : A[m * K + k];
+            const uint32_t aoff = a_mn ? sw128_off(k, m, K) : sw128_off(m, k, M);
+            *reinterpret_cast<__nv_bfloat16*>(sA + aoff) = av;
+        }
         // B(n, k)
         const int n = m;
         const __nv_bfloat16 bv = b_mn ? B[k * 128 + n] : B[n * K + k];
@@ -43,7 +49,7 @@ __global__ void __launch_bounds__(128, 1) umma_selftest_kernel(const __nv_bfloat
         mbar_fence_init();
     }
     if (warp == 0) {
-        tmem_alloc(&tslot, 128);
+        tmem_alloc(&tslot, 256);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -61,17 +67,33 @@ __global__ void __launch_bounds__(128, 1) umma_selftest_kernel(const __nv_bfloat
         }
         tmem_wait_st();
     }
+    if (mode == 4) {
+        // A row `row` into TMEM columns [128, 128 + K/2) of lane `row`
+        for (int c0 = 0; c0 < K / 2; c0 += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int k = 2 * (c0 + i);
+                r[i] = pack_bf16x2(__bfloat162float(A[row * K + k]), __bfloat162float(A[row * K + k + 1]));
+            }
+            tmem_st16u(tmem_addr(base, 32 * warp, 128 + c0), r);
+        }
+        tmem_wait_st();
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
 
     if (t == 0) {
-        const uint32_t idesc = idesc_bf16_f32(128, 128, a_mn ? 1 : 0, b_mn ? 1 : 0, mode == 3 ? 1 : 0);
+        const uint32_t idesc = idesc_bf16_f32(M, 128, a_mn ? 1 : 0, b_mn ? 1 : 0, mode == 3 ? 1 : 0);
         const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
         for (int ks = 0; ks < K / 16; ++ks) {
-            const uint64_t ad = a_mn ? desc_mnmajor(a0, K, ks) : desc_kmajor(a0, 128, ks);
+            const uint64_t ad = a_mn ? desc_mnmajor(a0, K, ks) : desc_kmajor(a0, M, ks);
             const uint64_t bd = b_mn ? desc_mnmajor(b0, K, ks) : desc_kmajor(b0, 128, ks);
-            umma_bf16(base, ad, bd, idesc, (ks > 0 || mode == 3) ? 1u : 0u);
+            if (mode == 4)
+                umma_bf16_tmem_a(base, base + 128 + 8 * ks, bd, idesc, ks > 0 ? 1u : 0u);
+            else
+                umma_bf16(base, ad, bd, idesc, (ks > 0 || mode == 3) ? 1u : 0u);
         }
         umma_commit(&bar);
     }
@@ -86,7 +108,7 @@ __global__ void __launch_bounds__(128, 1) umma_selftest_kernel(const __nv_bfloat
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(base, 128);
+    if (warp == 0) tmem_dealloc(base, 256);
 }
 
 extern "C" int umma_selftest(const void* A, const void* B, const void* C, void* D, int K, int mode, int* err)

@@ -27,6 +27,48 @@ def selftest(tmp_path_factory):
     return lib
 
 
+def _run(selftest, A, Bm, C, K, mode, b_kmajor):
+    a_store = A.t().contiguous() if mode == 2 else A.contiguous()
+    b_store = Bm.t().contiguous() if b_kmajor else Bm.contiguous()
+    D = torch.full((128, 128), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = selftest.umma_selftest(a_store.data_ptr(), b_store.data_ptr(), C.data_ptr(), D.data_ptr(), K, mode,
+                                err.data_ptr())
+    assert rc == 0 and int(err.item()) == 0
+    return D
+
+
+@pytest.mark.parametrize("K", [64, 128])
+def test_umma_a_from_tmem(selftest, K):
+    g = torch.Generator(device="cuda").manual_seed(7 + K)
+    A = torch.randn((128, K), generator=g, device="cuda").to(torch.bfloat16)
+    Bm = torch.randn((K, 128), generator=g, device="cuda").to(torch.bfloat16)
+    C = torch.zeros((128, 128), device="cuda")
+    D = _run(selftest, A, Bm, C, K, 4, False)
+    ref = A.float() @ Bm.float()
+    rel = ((D - ref).abs().max() / ref.abs().max()).item()
+    assert rel < 1e-5, f"A from TMEM, K {K}: rel err {rel:.3e}"
+
+
+def test_umma_m64_lane_layout(selftest):
+    """M = 64 accumulator layout: result row i sits in TMEM lane (i % 16) + 32 * (i // 16)."""
+    K = 64
+    g = torch.Generator(device="cuda").manual_seed(3)
+    A = torch.randn((128, K), generator=g, device="cuda").to(torch.bfloat16)
+    A[64:] = 0
+    Bm = torch.randn((K, 128), generator=g, device="cuda").to(torch.bfloat16)
+    C = torch.zeros((128, 128), device="cuda")
+    D = _run(selftest, A, Bm, C, K, 5, False)
+    ref = (A[:64].float() @ Bm.float())
+    lanes = []
+    for i in range(64):
+        diff = (D - ref[i][None, :]).abs().max(dim=1).values
+        lane = int(torch.argmin(diff).item())
+        assert diff[lane].item() < 1e-3 * ref.abs().max().item(), f"row {i} not found"
+        lanes.append(lane)
+    assert lanes == [(i % 16) + 32 * (i // 16) for i in range(64)]
+
+
 @pytest.mark.parametrize("mode", [0, 1, 2, 3])
 @pytest.mark.parametrize("K", [64, 128])
 def test_umma_tile(selftest, mode, K):
