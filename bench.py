@@ -35,7 +35,8 @@ import kda_workloads as W  # noqa: E402
 
 METRIC = "KDA prefill tokens/s (×tensor-peak %) and decode state GB/s (×HBM-peak %), 1 GB300"
 UNIT = "tokens/s"
-PREFILL_KERNEL_SRC = ("linear_attention_serving_chunkwise_gb300/csrc/kda_prefill_simt.cu",)
+PREFILL_KERNEL_SRC = ("linear_attention_serving_chunkwise_gb300/csrc/kda_prefill_tc.cu",
+                      "linear_attention_serving_chunkwise_gb300/csrc/kda_sm100.cuh")
 
 
 # --------------------------------------------------------------------------- helpers

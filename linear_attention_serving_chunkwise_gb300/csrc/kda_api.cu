@@ -44,6 +44,12 @@ bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.
 
 bool supported_dims(int dk, int dv) { return dk == dv && (dk == 64 || dk == 128); }
 
+// bf16 inputs with dk = dv = 128 run on the tcgen05 kernel; everything else on the fp32 CUDA-core kernel.
+bool uses_tensor_cores(const kda_prefill_desc& d)
+{
+    return d.qkv_dtype == KDA_BF16 && d.dk == 128 && d.dv == 128 && d.total_tokens > 0 && d.num_seqs > 0;
+}
+
 kda_status validate_prefill(const kda_prefill_desc* d)
 {
     if (!d) return KDA_ERR_INVALID_ARG;
@@ -86,7 +92,7 @@ kda_status kda_prefill_query(const kda_prefill_desc* desc, kda_prefill_plan* pla
     if (st != KDA_OK) return st;
     if (!plan) return KDA_ERR_INVALID_ARG;
     plan->kernel_launches = desc->num_seqs > 0 ? 1 : 0;
-    plan->tensor_cores = 0;
+    plan->tensor_cores = uses_tensor_cores(*desc) ? 1 : 0;
     plan->workspace_bytes = kda_prefill_workspace_bytes(desc);
     return KDA_OK;
 }
@@ -143,7 +149,8 @@ kda_status kda_prefill(const kda_prefill_desc* desc, const void* q, const void* 
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu_seqlens = cu_seqlens;
     a.init_state = init_state; a.out = out; a.final_state = final_state;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.status = status;
-    const cudaError_t e = kda::launch_prefill_simt(a, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = uses_tensor_cores(d) ? kda::launch_prefill_tc(a, static_cast<cudaStream_t>(stream))
+                                               : kda::launch_prefill_simt(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -30,6 +30,8 @@ struct DecodeArgs {
 
 // fp32 CUDA-core chunkwise prefill (any supported shape, fp32 or bf16 inputs)
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
+// bf16 tcgen05 chunkwise prefill (dk = dv = 128, T > 0)
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
 // fused single-pass decode
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

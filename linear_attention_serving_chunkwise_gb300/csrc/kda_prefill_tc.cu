@@ -1,0 +1,797 @@
+// Chunkwise KDA prefill on the Blackwell tensor cores (tcgen05), bf16 q/k/v,
+// dk = dv = 128, 64-token chunks cut into four 16-token sub-tiles.
+//
+// Method (llm-atlas "K3_RESEARCH.md": Q04/Q05 recurrence and delta-rule write,
+// Q06 + Figure 3 bounded log-decay g >= -5 so the diagonal tile can use BF16
+// tensor-core matmuls, Q07 chunkwise form with the state passed between chunks;
+// agihunt digest: FlashKDA's 16-token tiles).  For a chunk entered with state S,
+// Gamma_r the inclusive prefix sum of g over the chunk (per key channel):
+//   A[r][i] = beta_r <k_r e^{Gamma_r - Gamma_i}, k_i>  (i < r),  P[r][i] = <q_r e^{..}, k_i>  (i <= r)
+//   T = (I + A)^-1,  W = T diag(beta) (V - K_Gamma S),  O = Q_Gamma S + P W,
+//   S <- Diag(e^{Gamma_63}) S + (K e^{Gamma_63 - Gamma})^T W.
+// Intra-chunk decays are split at sub-tile boundaries so that every bf16 operand
+// factor is finite: for row r in sub-tile J with base rho_J (Gamma just before the
+// sub-tile), e^{Gamma_r - Gamma_i} = e^{Gamma_r - rho_J} e^{rho_J - Gamma_i}; the
+// row factor is <= 1 and the column factor is <= e^{5*16} (finite in bf16) on the
+// diagonal tile and <= 1 off it.
+//
+// One CTA owns one (sequence, head) and walks its chunks in order; the fp32 state
+// lives in tensor memory for the whole sequence.  Per chunk:
+//   1  g cumsum per channel; decayed operands written to TMEM (A operands) and
+//      shared memory (B operands); TMA prefetch of the next chunk starts.
+//   2  A and P by four MMAs (one per sub-tile reference).
+//   3  T = (I + A)^-1 in fp32 on CUDA cores (16x16 diagonal inverses, then block levels).
+//   4  Wk = T diag(beta) K_Gamma by MMA.
+//   5  D1 = T diag(beta) V - Wk S  (rows 0-63)  and  Q_Gamma S  (rows 64-127) by MMA;
+//      W to shared memory; D1 += [0; P] W and S += K~^T W by MMA; O rows to HBM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kda_common.cuh"
+#include "kda_launch.h"
+#include "kda_sm100.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm100;
+
+constexpr int kThreads = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;   // bound on every on-device wait
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- shared memory map (bytes)
+constexpr uint32_t OFF_Q = 0;          // q tile  [64 tok][128 ch] bf16, 2 x 8 KB TMA boxes
+constexpr uint32_t OFF_K = 16384;      // k tile
+constexpr uint32_t OFF_G = 32768;      // g tile  [64][128] fp32, 4 x 8 KB boxes; becomes the sub-tile cumsum
+constexpr uint32_t OFF_V0 = 65536;     // v tile, two buffers (the B operand of T diag(beta) V)
+constexpr uint32_t OFF_V1 = 81920;
+constexpr uint32_t OFF_X = 98304;      // 48 KB region shared by phases 1-2 / 3 / 5
+constexpr uint32_t X_SA = 0;           // A fp32 [64][65]
+constexpr uint32_t X_ST = 16640;       // T fp32 [64][65]
+constexpr uint32_t X_SY = 33280;       // level scratch fp32 [3][16][17]
+constexpr uint32_t X_SB = 0;           // S bf16, MN-major B [128 dk][128 dv]
+constexpr uint32_t X_WB = 32768;       // W bf16, MN-major B [64 tok][128 dv]
+constexpr uint32_t OFF_KG = 147456;    // K_Gamma bf16, MN-major B [64 tok][128 ch]
+constexpr uint32_t OFF_VEC = 163840;   // per-channel vectors [23][128] fp32
+constexpr uint32_t OFF_BETA = OFF_VEC + 23 * 512;
+constexpr uint32_t OFF_BAR = OFF_BETA + 256;
+constexpr uint32_t SMEM_USED = OFF_BAR + 64;
+constexpr size_t SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
+constexpr int LDA = 65;
+
+// column operands of the A/P MMAs: reference m has 16(m+1) rows at X + 2048 m (m+1)
+__host__ __device__ constexpr uint32_t x_kc(int m) { return 2048u * m * (m + 1); }
+
+// per-channel vectors (index * 128 floats into OFF_VEC)
+constexpr int V_S = 0;     // s_J: sum of g*log2e over sub-tile J            (4)
+constexpr int V_E = 4;     // E_J = e^{rho_J}                                (4)
+constexpr int V_G = 8;     // G_J = e^{Gamma_63 - rho_{J+1}}                 (4)
+constexpr int V_D = 12;    // D_J = e^{rho_{J+1} - rho_J}                    (4)
+constexpr int V_F = 16;    // F_{m,J} = e^{rho_m - rho_{J+1}}, J < m          (6)
+constexpr int V_GC = 22;   // gamma_C = e^{Gamma_63}                         (1)
+
+__host__ __device__ constexpr int f_index(int m, int J) { return m * (m - 1) / 2 + J; }
+
+// ---------------------------------------------------------------- tensor memory map (columns)
+constexpr uint32_t TM_S = 0;      // state S [128 dk lanes][128 dv] fp32
+constexpr uint32_t TM_D1 = 128;   // chain accumulator (phase 5)
+constexpr uint32_t TM_KQ = 128;   // [K_r; Q_r] A operand, bf16 pairs (phases 1-2)
+constexpr uint32_t TM_WK = 128;   // Wk accumulator (phase 4)
+constexpr uint32_t TM_AP = 256;   // A/P accumulators, sub-tile m at 256 + 16 m (m+1) / 2 (phases 2-3)
+constexpr uint32_t TM_TPA = 256;  // [T diag(beta); 0] A operand (phases 3-5)
+constexpr uint32_t TM_TPB = 288;  // [0; P] A operand (phases 3-5)
+constexpr uint32_t TM_A1 = 416;   // [-Wk; Q_Gamma] A operand (phases 1-5)
+constexpr uint32_t TM_KT = 480;   // K~^T A operand, lane = key channel (phases 1-5)
+constexpr uint32_t TM_COLS = 512;
+
+__host__ __device__ constexpr uint32_t tm_ap(int m) { return TM_AP + 8u * m * (m + 1); }
+
+struct TcParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_g;
+    const float* beta;
+    const int32_t* cu_seqlens;
+    const float* init_state;
+    float* out;
+    float* final_state;
+    int num_seqs, total_tokens, num_heads;
+    int* status;
+};
+
+__device__ __forceinline__ float ex2f(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcpf(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// byte offset of g[r][c] in the fp32 tile (4 boxes of 32 channels, 128-byte swizzle)
+__device__ __forceinline__ uint32_t g_off(int r, int c)
+{
+    return (uint32_t)(c >> 5) * 8192u + (uint32_t)r * 128u + ((((uint32_t)(c & 31) >> 2) ^ (r & 7u)) << 4) +
+           ((uint32_t)(c & 3) << 2);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
+    return v;
+}
+
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u)
+{
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
+    return __bfloat1622float2(h);
+}
+
+// Every thread waits on `bar` (bounded); returns false for all threads if any gave up.
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* s_abort)
+{
+    if (!mbar_wait_bounded(bar, parity, kWaitNs)) atomicExch(s_abort, 1);
+    __syncthreads();
+    return *s_abort == 0;
+}
+
+__device__ __forceinline__ void issue_chunk_loads(const TcParams& p, uint8_t* sm, uint64_t* bar, int vbuf, int t0,
+                                                  int h)
+{
+    mbar_arrive_expect_tx(bar, 81920u);
+    tma_load_3d(sm + OFF_Q, &p.tm_q, bar, 0, h, t0);
+    tma_load_3d(sm + OFF_Q + 8192, &p.tm_q, bar, 64, h, t0);
+    tma_load_3d(sm + OFF_K, &p.tm_k, bar, 0, h, t0);
+    tma_load_3d(sm + OFF_K + 8192, &p.tm_k, bar, 64, h, t0);
+    uint8_t* vb = sm + (vbuf ? OFF_V1 : OFF_V0);
+    tma_load_3d(vb, &p.tm_v, bar, 0, h, t0);
+    tma_load_3d(vb + 8192, &p.tm_v, bar, 64, h, t0);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) tma_load_3d(sm + OFF_G + 8192 * b, &p.tm_g, bar, 32 * b, h, t0);
+}
+
+// ---------------------------------------------------------------- phase 1a: per-channel cumsum
+// Thread c (< 128) turns column c of the g tile into the sub-tile-local cumsum
+// lambda_r = sum_{s = 16J}^{r} g_s log2(e) (rows past the chunk's end count as 0)
+// and writes the per-channel factors.
+__device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int c, int BT)
+{
+    float s[4];
+#pragma unroll
+    for (int J = 0; J < 4; ++J) {
+        float acc = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+            const int r = 16 * J + rr;
+            float* gp = reinterpret_cast<float*>(sm + OFF_G + g_off(r, c));
+            const float gv = (r < BT) ? *gp : 0.f;
+            acc = fmaf(gv, kLog2e, acc);
+            *gp = acc;
+        }
+        s[J] = acc;
+    }
+    const float rho1 = s[0], rho2 = s[0] + s[1], rho3 = rho2 + s[2], lam63 = rho3 + s[3];
+    const float tail0 = s[1] + s[2] + s[3], tail1 = s[2] + s[3], tail2 = s[3];
+#pragma unroll
+    for (int J = 0; J < 4; ++J) vec[(V_S + J) * 128 + c] = s[J];
+    vec[(V_E + 0) * 128 + c] = 1.f;
+    vec[(V_E + 1) * 128 + c] = ex2f(rho1);
+    vec[(V_E + 2) * 128 + c] = ex2f(rho2);
+    vec[(V_E + 3) * 128 + c] = ex2f(rho3);
+    vec[(V_G + 0) * 128 + c] = ex2f(tail0);
+    vec[(V_G + 1) * 128 + c] = ex2f(tail1);
+    vec[(V_G + 2) * 128 + c] = ex2f(tail2);
+    vec[(V_G + 3) * 128 + c] = 1.f;
+#pragma unroll
+    for (int J = 0; J < 4; ++J) vec[(V_D + J) * 128 + c] = ex2f(s[J]);
+    vec[(V_F + f_index(1, 0)) * 128 + c] = 1.f;
+    vec[(V_F + f_index(2, 0)) * 128 + c] = ex2f(s[1]);
+    vec[(V_F + f_index(2, 1)) * 128 + c] = 1.f;
+    vec[(V_F + f_index(3, 0)) * 128 + c] = ex2f(s[1] + s[2]);
+    vec[(V_F + f_index(3, 1)) * 128 + c] = ex2f(s[2]);
+    vec[(V_F + f_index(3, 2)) * 128 + c] = 1.f;
+    vec[V_GC * 128 + c] = ex2f(lam63);
+}
+
+// ---------------------------------------------------------------- phase 1a': K~^T into TMEM
+// Lane c of the K~^T operand holds K~[r][c] = k[r][c] e^{Gamma_63 - Gamma_r} for the
+// 32 tokens r of this warp-group half, two tokens per column.
+__device__ __forceinline__ void phase1_ktilde(uint8_t* sm, const float* vec, uint32_t tm, int c, int half,
+                                              int quarter, int BT)
+{
+    uint32_t packed[16];
+    const uint32_t kbase = smem_u32(sm + OFF_K);
+    const float s1 = vec[(V_S + 1) * 128 + c], s2 = vec[(V_S + 2) * 128 + c], s3 = vec[(V_S + 3) * 128 + c];
+    const float tail0 = s1 + s2 + s3, tail1 = s2 + s3, tail2 = s3;
+#pragma unroll
+    for (int pr = 0; pr < 16; ++pr) {
+        float f2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 32 * half + 2 * pr + e;
+            const int J = r >> 4;
+            const float lam = *reinterpret_cast<const float*>(sm + OFF_G + g_off(r, c));
+            const float sJ = vec[(V_S + J) * 128 + c];
+            const float tailJ = (J == 0) ? tail0 : ((J == 1) ? tail1 : ((J == 2) ? tail2 : 0.f));
+            const float fac = ex2f((sJ - lam) + tailJ);
+            unsigned short kb;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(kb) : "r"(kbase + sw128_off(r, c, 64)));
+            const float kv = (r < BT) ? __uint_as_float(((uint32_t)kb) << 16) : 0.f;
+            f2[e] = kv * fac;
+        }
+        packed[pr] = pack_bf16x2(f2[0], f2[1]);
+    }
+    tmem_st16u(tmem_addr(tm, 32 * quarter, TM_KT + 16 * half), packed);
+}
+
+// ---------------------------------------------------------------- phase 1b: token operands
+// Thread (lane L, half h): token r = L % 64 of the q rows (L >= 64) or k rows (L < 64),
+// channels [64h, 64h + 64).
+__device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uint32_t tm, int L, int half,
+                                              int quarter, int BT)
+{
+    const int r = L & 63, J = r >> 4;
+    const bool isq = L >= 64;
+    const bool valid = r < BT;
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t src = sbase + (isq ? OFF_Q : OFF_K);
+    uint32_t kq[32], q2[32];
+#pragma unroll
+    for (int gi = 0; gi < 8; ++gi) {
+        const int c0 = 64 * half + 8 * gi;
+        const uint4 raw = ld_shared_v4(src + sw128_chunk(r, c0 >> 3, 64));
+        const uint4 la = ld_shared_v4(sbase + OFF_G + g_off(r, c0));
+        const uint4 lb = ld_shared_v4(sbase + OFF_G + g_off(r, c0 + 4));
+        float xv[8], lam[8];
+        {
+            const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
+            xv[0] = a0.x; xv[1] = a0.y; xv[2] = a1.x; xv[3] = a1.y; xv[4] = a2.x; xv[5] = a2.y; xv[6] = a3.x; xv[7] = a3.y;
+            lam[0] = __uint_as_float(la.x); lam[1] = __uint_as_float(la.y); lam[2] = __uint_as_float(la.z);
+            lam[3] = __uint_as_float(la.w); lam[4] = __uint_as_float(lb.x); lam[5] = __uint_as_float(lb.y);
+            lam[6] = __uint_as_float(lb.z); lam[7] = __uint_as_float(lb.w);
+        }
+        float rowv[8], gam[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float v = valid ? xv[e] : 0.f;
+            const float x = ex2f(lam[e]);                      // e^{Gamma_r - rho_J} in (0, 1]
+            rowv[e] = v * x;
+            gam[e] = rowv[e] * vec[(V_E + J) * 128 + c0 + e];  // v e^{Gamma_r}
+            xv[e] = v * rcpf(x);                               // v e^{rho_J - Gamma_r}, <= e^{80} |v|
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            kq[4 * gi + e] = pack_bf16x2(rowv[2 * e], rowv[2 * e + 1]);
+            q2[4 * gi + e] = pack_bf16x2(gam[2 * e], gam[2 * e + 1]);
+        }
+        if (!isq) {
+            // diagonal-tile column operand of reference J and the K_Gamma B operand
+            st_shared_v4(sbase + OFF_X + x_kc(J) + sw128_chunk(r, c0 >> 3, 16 * (J + 1)),
+                         pack_bf16x2(xv[0], xv[1]), pack_bf16x2(xv[2], xv[3]), pack_bf16x2(xv[4], xv[5]),
+                         pack_bf16x2(xv[6], xv[7]));
+            st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), q2[4 * gi], q2[4 * gi + 1], q2[4 * gi + 2],
+                         q2[4 * gi + 3]);
+            // off-diagonal column operands of references m > J: k e^{rho_{J+1} - Gamma_r} e^{rho_m - rho_{J+1}}
+            float ky[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ky[e] = xv[e] * vec[(V_D + J) * 128 + c0 + e];
+            for (int m = J + 1; m < 4; ++m) {
+                const float* F = vec + (V_F + f_index(m, J)) * 128 + c0;
+                st_shared_v4(sbase + OFF_X + x_kc(m) + sw128_chunk(r, c0 >> 3, 16 * (m + 1)),
+                             pack_bf16x2(ky[0] * F[0], ky[1] * F[1]), pack_bf16x2(ky[2] * F[2], ky[3] * F[3]),
+                             pack_bf16x2(ky[4] * F[4], ky[5] * F[5]), pack_bf16x2(ky[6] * F[6], ky[7] * F[7]));
+            }
+        }
+    }
+    tmem_st32u(tmem_addr(tm, 32 * quarter, TM_KQ + 32 * half), kq);
+    if (isq) tmem_st32u(tmem_addr(tm, 32 * quarter, TM_A1 + 32 * half), q2);
+}
+
+// ---------------------------------------------------------------- phase 3: A/P read-out
+// Warp-group 0, lane L: row r = L % 64 of A (L < 64, scaled by beta_r, strictly lower)
+// or of P (L >= 64, lower with diagonal).  A goes to shared memory for the solve; P and
+// the zero halves of the [T diag(beta); 0] and [0; P] operands go to TMEM.
+__device__ __forceinline__ void phase3_readout(uint8_t* sm, uint32_t tm, int L, int quarter, const float* sbeta)
+{
+    const int r = L & 63, J = r >> 4;
+    const bool isP = L >= 64;
+    float row[64];
+    const uint32_t lane0 = 32 * quarter;
+    if ((quarter & 1) == 0) {   // rows of sub-tiles 0 and 1
+        float a0[16], a1[32];
+        tmem_ld16(tmem_addr(tm, lane0, tm_ap(0)), a0);
+        tmem_ld32(tmem_addr(tm, lane0, tm_ap(1)), a1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) row[i] = (J == 0) ? a0[i] : a1[i];
+#pragma unroll
+        for (int i = 16; i < 32; ++i) row[i] = (J == 1) ? a1[i] : 0.f;
+#pragma unroll
+        for (int i = 32; i < 64; ++i) row[i] = 0.f;
+    } else {                    // rows of sub-tiles 2 and 3
+        float b0[32], b1[32];
+        tmem_ld32(tmem_addr(tm, lane0, tm_ap(3)), b0);
+        tmem_ld32(tmem_addr(tm, lane0, tm_ap(3) + 32), b1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            row[i] = b0[i];
+            row[32 + i] = b1[i];
+        }
+        float c0[32], c1[16];
+        tmem_ld32(tmem_addr(tm, lane0, tm_ap(2)), c0);
+        tmem_ld16(tmem_addr(tm, lane0, tm_ap(2) + 32), c1);
+        tmem_wait_ld();
+        if (J == 2) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) row[i] = c0[i];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) row[32 + i] = c1[i];
+#pragma unroll
+            for (int i = 48; i < 64; ++i) row[i] = 0.f;
+        }
+    }
+    uint32_t zero[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) zero[i] = 0u;
+    if (!isP) {
+        float* sA = reinterpret_cast<float*>(sm + OFF_X + X_SA);
+        const float b = sbeta[r];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) sA[r * LDA + i] = (i < r) ? b * row[i] : 0.f;
+        tmem_st32u(tmem_addr(tm, lane0, TM_TPB), zero);
+    } else {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            pk[i] = pack_bf16x2((2 * i <= r) ? row[2 * i] : 0.f, (2 * i + 1 <= r) ? row[2 * i + 1] : 0.f);
+        tmem_st32u(tmem_addr(tm, lane0, TM_TPB), pk);
+        tmem_st32u(tmem_addr(tm, lane0, TM_TPA), zero);
+    }
+}
+
+// ---------------------------------------------------------------- phase 3: T = (I + A)^-1
+// All 256 threads.  sT must be zero on entry.  16x16 diagonal blocks by forward
+// substitution (one thread per column), then block levels d = 1..3:
+//   T_{m,m-d} = -T_{m,m} sum_{p=m-d}^{m-1} A_{m,p} T_{p,m-d}.
+__device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
+{
+    const float* sA = reinterpret_cast<const float*>(sm + OFF_X + X_SA);
+    float* sT = reinterpret_cast<float*>(sm + OFF_X + X_ST);
+    float* sY = reinterpret_cast<float*>(sm + OFF_X + X_SY);
+    if (t < 64) {
+        const int m = t >> 4, j = t & 15, b = 16 * m;
+        float x[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) x[q] = (q == j) ? 1.f : 0.f;
+#pragma unroll
+        for (int rr = 1; rr < 16; ++rr) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < rr; ++i) acc = fmaf(-sA[(b + rr) * LDA + b + i], x[i], acc);
+            if (rr > j) x[rr] = acc;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) sT[(b + q) * LDA + b + j] = x[q];
+    }
+    __syncthreads();
+    for (int d = 1; d < 4; ++d) {
+        const int nblk = 4 - d;
+        for (int idx = t; idx < nblk * 256; idx += kThreads) {
+            const int bk = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+            const int m = bk + d, J = m - d;
+            float acc = 0.f;
+            for (int p = J; p < m; ++p) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    acc = fmaf(sA[(16 * m + i) * LDA + 16 * p + q], sT[(16 * p + q) * LDA + 16 * J + j], acc);
+            }
+            sY[bk * 272 + i * 17 + j] = acc;
+        }
+        __syncthreads();
+        for (int idx = t; idx < nblk * 256; idx += kThreads) {
+            const int bk = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+            const int m = bk + d, J = m - d;
+            float acc = 0.f;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) acc = fmaf(sT[(16 * m + i) * LDA + 16 * m + q], sY[bk * 272 + q * 17 + j], acc);
+            sT[(16 * m + i) * LDA + 16 * J + j] = -acc;
+        }
+        __syncthreads();
+    }
+}
+
+// 64 consecutive fp32 TMEM columns of this thread's lane -> bf16 rows of an MN-major
+// B-operand tile (row `row`, value columns [64 half, 64 half + 64), `rows` rows per block).
+__device__ __forceinline__ void store_row_bf16(uint32_t tile, int row, int half, int rows, const float (&a)[32],
+                                               const float (&b)[32])
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        st_shared_v4(tile + sw128_chunk(row, 8 * half + q, rows), pack_bf16x2(a[8 * q], a[8 * q + 1]),
+                     pack_bf16x2(a[8 * q + 2], a[8 * q + 3]), pack_bf16x2(a[8 * q + 4], a[8 * q + 5]),
+                     pack_bf16x2(a[8 * q + 6], a[8 * q + 7]));
+        st_shared_v4(tile + sw128_chunk(row, 8 * half + 4 + q, rows), pack_bf16x2(b[8 * q], b[8 * q + 1]),
+                     pack_bf16x2(b[8 * q + 2], b[8 * q + 3]), pack_bf16x2(b[8 * q + 4], b[8 * q + 5]),
+                     pack_bf16x2(b[8 * q + 6], b[8 * q + 7]));
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+__global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int L = 32 * quarter + lane;   // the TMEM lane this thread may access
+    float* vec = reinterpret_cast<float*>(sm + OFF_VEC);
+    float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
+    uint64_t* bar_in = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint64_t* bar_mma = bar_in + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_in + 2);
+    int* s_abort = reinterpret_cast<int*>(tslot + 1);
+    const uint32_t sbase = smem_u32(sm);
+
+    const int H = p.num_heads;
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    int bos, eos;
+    if (!seq_bounds(p.cu_seqlens, n, p.num_seqs, p.total_tokens, p.status, bos, eos)) return;
+    const int nchunks = (eos - bos + 63) >> 6;
+    const size_t sbase_g = ((size_t)n * H + h) * 128 * 128;
+
+    if (t == 0) {
+        mbar_init(bar_in, 1);
+        mbar_init(bar_mma, 1);
+        mbar_fence_init();
+        *s_abort = 0;
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_g);
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tm = *tslot;
+
+    bool tma_pending = false;   // meaningful in thread 0 only
+    if (t == 0 && nchunks > 0) {
+        issue_chunk_loads(p, sm, bar_in, 0, bos, h);
+        tma_pending = true;
+    }
+
+    // initial state -> TMEM: lane L = key channel, columns [64 half, 64 half + 64)
+#pragma unroll
+    for (int cb = 0; cb < 2; ++cb) {
+        const int col = 64 * half + 32 * cb;
+        float v[32];
+        if (p.init_state) {
+            const float4* src = reinterpret_cast<const float4*>(p.init_state + sbase_g + (size_t)L * 128 + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 f = __ldg(src + i);
+                v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + col), v);
+    }
+    tmem_wait_st();
+
+    float beta_next = (t < 64 && bos + t < eos) ? __ldg(p.beta + (size_t)(bos + t) * H + h) : 0.f;
+    uint32_t in_par = 0, mma_par = 0;
+    bool ok = true;
+
+    for (int ci = 0; ci < nchunks; ++ci) {
+        const int t0 = bos + 64 * ci;
+        const int BT = min(64, eos - t0);
+        if (t < 64) sbeta[t] = beta_next;
+        tc_fence_before_sync();
+        __syncthreads();
+        tc_fence_after_sync();
+        if (t < 64) {
+            const int tn = t0 + 64 + t;
+            beta_next = (ci + 1 < nchunks && tn < eos) ? __ldg(p.beta + (size_t)tn * H + h) : 0.f;
+        }
+        if (!(ok = wait_all(bar_in, in_par, s_abort))) break;
+        in_par ^= 1u;
+        tma_pending = false;
+
+        // ---- phase 1: decayed operands
+        if (t < 128) phase1_cumsum(sm, vec, t, BT);
+        __syncthreads();
+        phase1_ktilde(sm, vec, tm, L, half, quarter, BT);
+        phase1_tokens(sm, vec, tm, L, half, quarter, BT);
+        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncthreads();
+
+        // ---- next chunk's loads, then phase 2 (A/P MMAs)
+        if (t == 0) {
+            tc_fence_after_sync();
+            if (ci + 1 < nchunks) {
+                issue_chunk_loads(p, sm, bar_in, (ci + 1) & 1, t0 + 64, h);
+                tma_pending = true;
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t idesc = idesc_bf16_f32(128, 16 * (m + 1), 0, 0);
+                const uint32_t kc = sbase + OFF_X + x_kc(m);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    umma_bf16_tmem_a(tm + tm_ap(m), tm + TM_KQ + 8 * ks, desc_kmajor(kc, 16 * (m + 1), ks), idesc,
+                                     ks > 0 ? 1u : 0u);
+            }
+            umma_commit(bar_mma);
+        }
+        if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
+        mma_par ^= 1u;
+        tc_fence_after_sync();
+
+        // ---- phase 3: A/P read-out (warp-group 0) while warp-group 1 clears T, then the solve
+        if (t < 128) {
+            phase3_readout(sm, tm, L, quarter, sbeta);
+        } else {
+            float* sT = reinterpret_cast<float*>(sm + OFF_X + X_ST);
+            for (int idx = t - 128; idx < 64 * LDA; idx += 128) sT[idx] = 0.f;
+        }
+        __syncthreads();
+        phase3_solve(sm, t);
+        if (t < 64) {   // [T diag(beta)] rows 0-63 into TMEM
+            const float* sT = reinterpret_cast<const float*>(sm + OFF_X + X_ST);
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                pk[i] = pack_bf16x2(sT[t * LDA + 2 * i] * sbeta[2 * i], sT[t * LDA + 2 * i + 1] * sbeta[2 * i + 1]);
+            tmem_st32u(tmem_addr(tm, 32 * quarter, TM_TPA), pk);
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncthreads();
+
+        // ---- phase 4: Wk = T diag(beta) K_Gamma, then -Wk into the A1 operand rows 0-63
+        if (t == 0) {
+            tc_fence_after_sync();
+            const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_WK, tm + TM_TPA + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc,
+                                 ks > 0 ? 1u : 0u);
+            umma_commit(bar_mma);
+        }
+        if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
+        mma_par ^= 1u;
+        tc_fence_after_sync();
+        if (quarter < 2) {
+            float a[32], b[32];
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_WK + 64 * half), a);
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_WK + 64 * half + 32), b);
+            tmem_wait_ld();
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
+                pk[16 + i] = pack_bf16x2(-b[2 * i], -b[2 * i + 1]);
+            }
+            tmem_st32u(tmem_addr(tm, 32 * quarter, TM_A1 + 32 * half), pk);
+            tmem_wait_st();
+        }
+        tc_fence_before_sync();
+        __syncthreads();
+
+        // ---- phase 5a: S -> bf16 B operand; S <- Diag(gamma_C) S in place
+        {
+            float a[32], b[32];
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 64 * half), a);
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 64 * half + 32), b);
+            tmem_wait_ld();
+            store_row_bf16(sbase + OFF_X + X_SB, L, half, 128, a, b);
+            const float gc = vec[V_GC * 128 + L];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                a[i] *= gc;
+                b[i] *= gc;
+            }
+            tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + 64 * half), a);
+            tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + 64 * half + 32), b);
+            tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+
+        // ---- phase 5b: D1 = [T diag(beta); 0] V + [-Wk; Q_Gamma] S
+        if (t == 0) {
+            tc_fence_after_sync();
+            const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+            const uint32_t vb = sbase + ((ci & 1) ? OFF_V1 : OFF_V0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPA + 8 * ks, desc_mnmajor(vb, 64, ks), idesc, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1 + 8 * ks, desc_mnmajor(sbase + OFF_X + X_SB, 128, ks), idesc,
+                                 1u);
+            umma_commit(bar_mma);
+        }
+        if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
+        mma_par ^= 1u;
+        tc_fence_after_sync();
+
+        // ---- phase 5c: W = D1 rows 0-63 -> bf16 MN-major B operand
+        if (quarter < 2) {
+            float a[32], b[32];
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half), a);
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half + 32), b);
+            tmem_wait_ld();
+            store_row_bf16(sbase + OFF_X + X_WB, L, half, 64, a, b);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+
+        // ---- phase 5d: D1 += [0; P] W;  S += K~^T W
+        if (t == 0) {
+            tc_fence_after_sync();
+            const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+            const uint32_t wb = sbase + OFF_X + X_WB;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPB + 8 * ks, desc_mnmajor(wb, 64, ks), idesc, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_S, tm + TM_KT + 8 * ks, desc_mnmajor(wb, 64, ks), idesc, 1u);
+            umma_commit(bar_mma);
+        }
+        if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
+        mma_par ^= 1u;
+        tc_fence_after_sync();
+
+        // ---- phase 5e: O = D1 rows 64-127 -> HBM (fp32)
+        if (quarter >= 2) {
+            const int r = L - 64;
+            float a[32], b[32];
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half), a);
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half + 32), b);
+            tmem_wait_ld();
+            if (r < BT) {
+                float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)(t0 + r) * H + h) * 128 + 64 * half);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+                    dst[8 + i] = make_float4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (ok && p.final_state) {
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {
+            const int col = 64 * half + 32 * cb;
+            float v[32];
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + col), v);
+            tmem_wait_ld();
+            float4* dst = reinterpret_cast<float4*>(p.final_state + sbase_g + (size_t)L * 128 + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+    }
+    if (!ok && t == 0) {
+        // a wait gave up: record it, let in-flight copies and MMAs land (bounded), then leave
+        report_status(p.status, kDevTimeout);
+        if (tma_pending) mbar_wait_bounded(bar_in, in_par, kWaitNs);
+        mbar_wait_bounded(bar_mma, mma_par, kWaitNs);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, TM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 3-D map over a [T][H][128] tensor: box = {box_c channels, 1 head, 64 tokens}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz, int H, int T, int box_c)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)128 * esz, (cuuint64_t)H * 128 * esz};
+    cuuint32_t box[3] = {(cuuint32_t)box_c, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream)
+{
+    TcParams p;
+    if (!make_map(&p.tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
+        !make_map(&p.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
+        !make_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
+        !make_map(&p.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32))
+        return cudaErrorInvalidValue;
+    p.beta = a.beta;
+    p.cu_seqlens = a.cu_seqlens;
+    p.init_state = a.init_state;
+    p.out = a.out;
+    p.final_state = a.final_state;
+    p.num_seqs = a.num_seqs;
+    p.total_tokens = a.total_tokens;
+    p.num_heads = a.num_heads;
+    p.status = a.status;
+    cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const long long units = (long long)a.num_seqs * a.num_heads;
+    kda_prefill_tc_kernel<<<(unsigned)units, kThreads, SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -27,7 +27,7 @@ def _as_sequences(d, b_idx, h_idx):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
 def test_decode_small_all_units(cuda_lib, d, dtype):
     cfg = W.DecodeConfig("small", 5, 3, d, d, dtype, 6)
     inp = W.make_decode_inputs(cfg, seed=d)

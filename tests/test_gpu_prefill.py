@@ -28,13 +28,13 @@ def test_tiny_fp32_workload(cuda_lib):
 
 @pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 200])
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
 def test_single_sequence_sweep(cuda_lib, T, d, dtype):
     cfg = W.random_prefill_config([T], 3, d, dtype, init="normal")
     _run_small(cuda_lib, cfg, seed=T * 7 + d)
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 def test_varlen_with_empty_and_ragged_sequences(cuda_lib, dtype, d):
     rng = np.random.default_rng(d)
@@ -66,7 +66,7 @@ def test_equal_split_without_cu_seqlens(cuda_lib):
     check("final_state", fin, ref_s, 1e-4)
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
 def test_in_place_chaining_equals_one_shot(cuda_lib, dtype):
     """init_state and final_state the same buffer; three chained calls vs the one-shot oracle."""
     cfg = W.random_prefill_config([300], 2, 128, dtype, init="normal")
