@@ -216,6 +216,41 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
            | ((uint32_t)(M >> 4) << 24);     // M / 16
 }
 
+// Instruction descriptor, kind::tf32 (fp32 operands read as tf32) with an fp32
+// accumulator; both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N)
+{
+    return (1u << 4)                         // D: fp32
+           | (2u << 7)                       // A: tf32
+           | (2u << 10)                      // B: tf32
+           | ((uint32_t)(N >> 3) << 17)
+           | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[tmem] * B, kind::tf32: one fp32 element of A per TMEM column
+// (8 columns per K-step of 8), B K-major in shared memory (8 fp32 = 32 bytes per K-step).
+__device__ __forceinline__ void umma_tf32_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A * B, issued by one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate)
@@ -263,6 +298,14 @@ __host__ __device__ __forceinline__ uint32_t sw128_chunk(uint32_t row, uint32_t 
 {
     const uint32_t blk = chunk >> 3, c = chunk & 7u;
     return blk * rows * 128u + row * 128u + ((c ^ (row & 7u)) << 4);
+}
+
+// Byte offset of element (row, col) of an fp32 tile stored with the 128-byte swizzle
+// in 32-column blocks of `rows` rows each.
+__host__ __device__ __forceinline__ uint32_t sw128_off_f32(uint32_t row, uint32_t col, uint32_t rows)
+{
+    const uint32_t blk = col >> 5, c = col & 31u;
+    return blk * rows * 128u + row * 128u + ((((c >> 2) ^ (row & 7u))) << 4) + ((c & 3u) << 2);
 }
 
 // Same, for an fp32 tile of 32-column (128-byte) blocks.

@@ -24,6 +24,8 @@ def selftest(tmp_path_factory):
     lib = ctypes.CDLL(out)
     lib.umma_selftest.restype = ctypes.c_int
     lib.umma_selftest.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    lib.umma_tf32_selftest.restype = ctypes.c_int
+    lib.umma_tf32_selftest.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     return lib
 
 
@@ -89,3 +91,20 @@ def test_umma_tile(selftest, mode, K):
     assert torch.isfinite(D).all()
     rel = ((D - ref).abs().max() / ref.abs().max()).item()
     assert rel < 1e-5, f"mode {mode} K {K}: rel err {rel:.3e}"
+
+
+@pytest.mark.parametrize("a_tmem", [0, 1])
+@pytest.mark.parametrize("K", [32, 128])
+def test_umma_tf32(selftest, K, a_tmem):
+    """kind::tf32 with fp32 operands: A from shared memory or TMEM, B K-major; the
+    result must carry tf32 (10-bit mantissa) precision, far better than bf16."""
+    g = torch.Generator(device="cuda").manual_seed(31 + K + a_tmem)
+    A = torch.randn((128, K), generator=g, device="cuda")
+    B = torch.randn((128, K), generator=g, device="cuda")
+    D = torch.full((128, 128), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = selftest.umma_tf32_selftest(A.data_ptr(), B.data_ptr(), D.data_ptr(), K, a_tmem, err.data_ptr())
+    assert rc == 0 and int(err.item()) == 0
+    ref = (A.double() @ B.double().t()).float()
+    rel = ((D - ref).abs().max() / ref.abs().max()).item()
+    assert rel < 2e-3, f"tf32 K {K} a_tmem {a_tmem}: rel err {rel:.3e}"
