@@ -2,28 +2,34 @@
 // dk = dv = 128, 64-token chunks cut into four 16-token sub-tiles.
 //
 // Method (llm-atlas "K3_RESEARCH.md": Q04/Q05 recurrence and delta-rule write,
-// Q06 + Figure 3 bounded log-decay g >= -5 so the diagonal tile can use BF16
-// tensor-core matmuls, Q07 chunkwise form with the state passed between chunks;
-// agihunt digest: FlashKDA's 16-token tiles).  For a chunk entered with state S,
+// Q06 + Figure 3 bounded log-decay g >= -5 so the diagonal tile can use the
+// tensor cores, Q07 chunkwise form with the state passed between chunks; agihunt
+// digest: FlashKDA's 16-token tiles).  For a chunk entered with state S and
 // Gamma_r the inclusive prefix sum of g over the chunk (per key channel):
-//   A[r][i] = beta_r <k_r e^{Gamma_r - Gamma_i}, k_i>  (i < r),  P[r][i] = <q_r e^{..}, k_i>  (i <= r)
-//   T = (I + A)^-1,  W = T diag(beta) (V - K_Gamma S),  O = Q_Gamma S + P W,
-//   S <- Diag(e^{Gamma_63}) S + (K e^{Gamma_63 - Gamma})^T W.
-// Intra-chunk decays are split at sub-tile boundaries so that every bf16 operand
+//   A[r][i] = beta_r <k_r e^{Gamma_r - Gamma_i}, k_i>  (i < r),   P[r][i] = <q_r e^{Gamma_r - Gamma_i}, k_i>  (i <= r)
+//   Tb = (I + A)^-1 diag(beta),   M = P Tb,   Wk = Tb K_Gamma,   Q' = Q_Gamma - M K_Gamma
+//   W = Tb V - Wk S,   O = Q' S + M V,   S <- Diag(e^{Gamma_63}) S + (K e^{Gamma_63 - Gamma})^T W
+// (O = Q_Gamma S + P W rewritten so that the read-out needs no product with W.)
+//
+// Intra-chunk decays are split at sub-tile boundaries so that every operand
 // factor is finite: for row r in sub-tile J with base rho_J (Gamma just before the
 // sub-tile), e^{Gamma_r - Gamma_i} = e^{Gamma_r - rho_J} e^{rho_J - Gamma_i}; the
-// row factor is <= 1 and the column factor is <= e^{5*16} (finite in bf16) on the
-// diagonal tile and <= 1 off it.
+// row factor is <= 1 and the column factor is <= e^{5*16} on the diagonal tile
+// and <= 1 off it.
+//
+// Precision: A and P use tf32 MMAs (fp32 operands); Tb, M and W enter their MMAs as
+// bf16 hi + lo pairs; S, Wk, Q', K_Gamma and K~ are single bf16; accumulation and
+// the carried state are fp32.
 //
 // One CTA owns one (sequence, head) and walks its chunks in order; the fp32 state
 // lives in tensor memory for the whole sequence.  Per chunk:
-//   1  g cumsum per channel; decayed operands written to TMEM (A operands) and
-//      shared memory (B operands); TMA prefetch of the next chunk starts.
-//   2  A and P by four MMAs (one per sub-tile reference).
-//   3  T = (I + A)^-1 in fp32 on CUDA cores (16x16 diagonal inverses, then block levels).
-//   4  Wk = T diag(beta) K_Gamma by MMA.
-//   5  D1 = T diag(beta) V - Wk S  (rows 0-63)  and  Q_Gamma S  (rows 64-127) by MMA;
-//      W to shared memory; D1 += [0; P] W and S += K~^T W by MMA; O rows to HBM.
+//   1  g cumsum per channel; decayed operands to TMEM (A operands) and shared
+//      memory (B operands); TMA prefetch of the next chunk.
+//   2  A and P by four tf32 MMAs (one per sub-tile reference).
+//   3  T = (I + A)^-1 and M = P Tb in fp32 on CUDA cores.
+//   4  [Wk; M K_Gamma] by MMA, then the [-Wk; Q'] operand.
+//   5  D1 = [Tb; M] V + [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O;
+//      O to HBM, W to shared memory; S += K~^T W by MMA.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -46,24 +52,26 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t OFF_Q = 0;          // q tile  [64 tok][128 ch] bf16, 2 x 8 KB TMA boxes
 constexpr uint32_t OFF_K = 16384;      // k tile
 constexpr uint32_t OFF_G = 32768;      // g tile  [64][128] fp32, 4 x 8 KB boxes; becomes the sub-tile cumsum
-constexpr uint32_t OFF_V0 = 65536;     // v tile, two buffers (the B operand of T diag(beta) V)
+constexpr uint32_t OFF_V0 = 65536;     // v tile, two buffers (B operand of [Tb; M] V)
 constexpr uint32_t OFF_V1 = 81920;
-constexpr uint32_t OFF_X = 98304;      // 48 KB region shared by phases 1-2 / 3 / 5
-constexpr uint32_t X_SA = 0;           // A fp32 [64][65]
+constexpr uint32_t OFF_X = 98304;      // 80 KB region shared by phases 1-2 / 3 / 5
+constexpr uint32_t X_SA = 0;           // A fp32 [64][65], then M
 constexpr uint32_t X_ST = 16640;       // T fp32 [64][65]
-constexpr uint32_t X_SY = 33280;       // level scratch fp32 [3][16][17]
+constexpr uint32_t X_SP = 33280;       // P fp32 [64][65]
+constexpr uint32_t X_SY = 49920;       // level scratch fp32 [3][16][17]
 constexpr uint32_t X_SB = 0;           // S bf16, MN-major B [128 dk][128 dv]
-constexpr uint32_t X_WB = 32768;       // W bf16, MN-major B [64 tok][128 dv]
-constexpr uint32_t OFF_KG = 147456;    // K_Gamma bf16, MN-major B [64 tok][128 ch]
-constexpr uint32_t OFF_VEC = 163840;   // per-channel vectors [23][128] fp32
+constexpr uint32_t X_WH = 32768;       // W hi bf16, MN-major B [64 tok][128 dv]
+constexpr uint32_t X_WL = 49152;       // W lo
+constexpr uint32_t OFF_KG = 180224;    // K_Gamma bf16, MN-major B [64 tok][128 ch]
+constexpr uint32_t OFF_VEC = 196608;   // per-channel vectors [23][128] fp32
 constexpr uint32_t OFF_BETA = OFF_VEC + 23 * 512;
 constexpr uint32_t OFF_BAR = OFF_BETA + 256;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr size_t SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
 constexpr int LDA = 65;
 
-// column operands of the A/P MMAs: reference m has 16(m+1) rows at X + 2048 m (m+1)
-__host__ __device__ constexpr uint32_t x_kc(int m) { return 2048u * m * (m + 1); }
+// fp32 column operands of the A/P MMAs: reference m has 16(m+1) rows at X + 4096 m (m+1)
+__host__ __device__ constexpr uint32_t x_kc(int m) { return 4096u * m * (m + 1); }
 
 // per-channel vectors (index * 128 floats into OFF_VEC)
 constexpr int V_S = 0;     // s_J: sum of g*log2e over sub-tile J            (4)
@@ -77,14 +85,14 @@ __host__ __device__ constexpr int f_index(int m, int J) { return m * (m - 1) / 2
 
 // ---------------------------------------------------------------- tensor memory map (columns)
 constexpr uint32_t TM_S = 0;      // state S [128 dk lanes][128 dv] fp32
-constexpr uint32_t TM_D1 = 128;   // chain accumulator (phase 5)
-constexpr uint32_t TM_KQ = 128;   // [K_r; Q_r] A operand, bf16 pairs (phases 1-2)
-constexpr uint32_t TM_WK = 128;   // Wk accumulator (phase 4)
+constexpr uint32_t TM_KQ = 128;   // [K_r; Q_r] tf32 A operand, one fp32 per column (phases 1-2)
+constexpr uint32_t TM_D2 = 128;   // [Wk; M K_Gamma] accumulator (phase 4)
+constexpr uint32_t TM_D1 = 128;   // [W; O] accumulator (phase 5)
 constexpr uint32_t TM_AP = 256;   // A/P accumulators, sub-tile m at 256 + 16 m (m+1) / 2 (phases 2-3)
-constexpr uint32_t TM_TPA = 256;  // [T diag(beta); 0] A operand (phases 3-5)
-constexpr uint32_t TM_TPB = 288;  // [0; P] A operand (phases 3-5)
-constexpr uint32_t TM_A1 = 416;   // [-Wk; Q_Gamma] A operand (phases 1-5)
-constexpr uint32_t TM_KT = 480;   // K~^T A operand, lane = key channel (phases 1-5)
+constexpr uint32_t TM_TPH = 256;  // [Tb; M] hi, bf16 pairs (phases 3-5)
+constexpr uint32_t TM_TPL = 288;  // [Tb; M] lo (phases 3-5)
+constexpr uint32_t TM_A1 = 416;   // [-Wk; Q_Gamma then Q'] bf16 pairs (phases 1-5)
+constexpr uint32_t TM_KT = 480;   // K~^T, lane = key channel, bf16 pairs (phases 1-5)
 constexpr uint32_t TM_COLS = 512;
 
 __host__ __device__ constexpr uint32_t tm_ap(int m) { return TM_AP + 8u * m * (m + 1); }
@@ -115,11 +123,7 @@ __device__ __forceinline__ float rcpf(float x)
 }
 
 // byte offset of g[r][c] in the fp32 tile (4 boxes of 32 channels, 128-byte swizzle)
-__device__ __forceinline__ uint32_t g_off(int r, int c)
-{
-    return (uint32_t)(c >> 5) * 8192u + (uint32_t)r * 128u + ((((uint32_t)(c & 31) >> 2) ^ (r & 7u)) << 4) +
-           ((uint32_t)(c & 3) << 2);
-}
+__device__ __forceinline__ uint32_t g_off(int r, int c) { return sw128_off_f32(r, c, 64); }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 {
@@ -132,6 +136,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
         : "r"(taddr));
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld32u(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32])
@@ -152,6 +169,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+__device__ __forceinline__ void st_shared_f4(uint32_t saddr, float a, float b, float c, float d)
+{
+    st_shared_v4(saddr, __float_as_uint(a), __float_as_uint(b), __float_as_uint(c), __float_as_uint(d));
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr)
 {
     uint4 v;
@@ -163,6 +185,14 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t u)
 {
     __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
     return __bfloat1622float2(h);
+}
+
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): the pair carries ~16 mantissa bits.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo)
+{
+    const float ah = __bfloat162float(__float2bfloat16_rn(a)), bh = __bfloat162float(__float2bfloat16_rn(b));
+    hi = pack_bf16x2(ah, bh);
+    lo = pack_bf16x2(a - ah, b - bh);
 }
 
 // Every thread waits on `bar` (bounded); returns false for all threads if any gave up.
@@ -264,7 +294,9 @@ __device__ __forceinline__ void phase1_ktilde(uint8_t* sm, const float* vec, uin
 
 // ---------------------------------------------------------------- phase 1b: token operands
 // Thread (lane L, half h): token r = L % 64 of the q rows (L >= 64) or k rows (L < 64),
-// channels [64h, 64h + 64).
+// channels [64h, 64h + 64).  Writes the tf32 row operand [K_r; Q_r] (TMEM), Q_Gamma
+// (TMEM, q rows), and for k rows the fp32 column operands of every reference m >= J
+// and the bf16 K_Gamma B operand (shared memory).
 __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uint32_t tm, int L, int half,
                                               int quarter, int BT)
 {
@@ -273,62 +305,64 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
     const bool valid = r < BT;
     const uint32_t sbase = smem_u32(sm);
     const uint32_t src = sbase + (isq ? OFF_Q : OFF_K);
-    uint32_t kq[32], q2[32];
+    uint32_t q2[32];
 #pragma unroll
-    for (int gi = 0; gi < 8; ++gi) {
-        const int c0 = 64 * half + 8 * gi;
-        const uint4 raw = ld_shared_v4(src + sw128_chunk(r, c0 >> 3, 64));
-        const uint4 la = ld_shared_v4(sbase + OFF_G + g_off(r, c0));
-        const uint4 lb = ld_shared_v4(sbase + OFF_G + g_off(r, c0 + 4));
-        float xv[8], lam[8];
-        {
-            const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
-            xv[0] = a0.x; xv[1] = a0.y; xv[2] = a1.x; xv[3] = a1.y; xv[4] = a2.x; xv[5] = a2.y; xv[6] = a3.x; xv[7] = a3.y;
-            lam[0] = __uint_as_float(la.x); lam[1] = __uint_as_float(la.y); lam[2] = __uint_as_float(la.z);
-            lam[3] = __uint_as_float(la.w); lam[4] = __uint_as_float(lb.x); lam[5] = __uint_as_float(lb.y);
-            lam[6] = __uint_as_float(lb.z); lam[7] = __uint_as_float(lb.w);
-        }
-        float rowv[8], gam[8];
+    for (int hb = 0; hb < 2; ++hb) {
+        float kq[32];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float v = valid ? xv[e] : 0.f;
-            const float x = ex2f(lam[e]);                      // e^{Gamma_r - rho_J} in (0, 1]
-            rowv[e] = v * x;
-            gam[e] = rowv[e] * vec[(V_E + J) * 128 + c0 + e];  // v e^{Gamma_r}
-            xv[e] = v * rcpf(x);                               // v e^{rho_J - Gamma_r}, <= e^{80} |v|
-        }
+        for (int gi = 0; gi < 4; ++gi) {
+            const int c0 = 64 * half + 32 * hb + 8 * gi;
+            const uint4 raw = ld_shared_v4(src + sw128_chunk(r, c0 >> 3, 64));
+            const uint4 la = ld_shared_v4(sbase + OFF_G + g_off(r, c0));
+            const uint4 lb = ld_shared_v4(sbase + OFF_G + g_off(r, c0 + 4));
+            float xv[8], lam[8];
+            {
+                const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
+                xv[0] = a0.x; xv[1] = a0.y; xv[2] = a1.x; xv[3] = a1.y; xv[4] = a2.x; xv[5] = a2.y; xv[6] = a3.x; xv[7] = a3.y;
+                lam[0] = __uint_as_float(la.x); lam[1] = __uint_as_float(la.y); lam[2] = __uint_as_float(la.z);
+                lam[3] = __uint_as_float(la.w); lam[4] = __uint_as_float(lb.x); lam[5] = __uint_as_float(lb.y);
+                lam[6] = __uint_as_float(lb.z); lam[7] = __uint_as_float(lb.w);
+            }
+            float gam[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            kq[4 * gi + e] = pack_bf16x2(rowv[2 * e], rowv[2 * e + 1]);
-            q2[4 * gi + e] = pack_bf16x2(gam[2 * e], gam[2 * e + 1]);
-        }
-        if (!isq) {
-            // diagonal-tile column operand of reference J and the K_Gamma B operand
-            st_shared_v4(sbase + OFF_X + x_kc(J) + sw128_chunk(r, c0 >> 3, 16 * (J + 1)),
-                         pack_bf16x2(xv[0], xv[1]), pack_bf16x2(xv[2], xv[3]), pack_bf16x2(xv[4], xv[5]),
-                         pack_bf16x2(xv[6], xv[7]));
-            st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), q2[4 * gi], q2[4 * gi + 1], q2[4 * gi + 2],
-                         q2[4 * gi + 3]);
-            // off-diagonal column operands of references m > J: k e^{rho_{J+1} - Gamma_r} e^{rho_m - rho_{J+1}}
-            float ky[8];
+            for (int e = 0; e < 8; ++e) {
+                const float v = valid ? xv[e] : 0.f;
+                const float x = ex2f(lam[e]);                        // e^{Gamma_r - rho_J} in (0, 1]
+                kq[8 * gi + e] = v * x;
+                gam[e] = kq[8 * gi + e] * vec[(V_E + J) * 128 + c0 + e];  // v e^{Gamma_r}
+                xv[e] = v * rcpf(x);                                 // v e^{rho_J - Gamma_r}, <= e^{80} |v|
+            }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ky[e] = xv[e] * vec[(V_D + J) * 128 + c0 + e];
-            for (int m = J + 1; m < 4; ++m) {
-                const float* F = vec + (V_F + f_index(m, J)) * 128 + c0;
-                st_shared_v4(sbase + OFF_X + x_kc(m) + sw128_chunk(r, c0 >> 3, 16 * (m + 1)),
-                             pack_bf16x2(ky[0] * F[0], ky[1] * F[1]), pack_bf16x2(ky[2] * F[2], ky[3] * F[3]),
-                             pack_bf16x2(ky[4] * F[4], ky[5] * F[5]), pack_bf16x2(ky[6] * F[6], ky[7] * F[7]));
+            for (int e = 0; e < 4; ++e) q2[16 * hb + 4 * gi + e] = pack_bf16x2(gam[2 * e], gam[2 * e + 1]);
+            if (!isq) {
+                const uint32_t kc = sbase + OFF_X + x_kc(J);
+                const int rows = 16 * (J + 1);
+                st_shared_f4(kc + sw128_off_f32(r, c0, rows), xv[0], xv[1], xv[2], xv[3]);
+                st_shared_f4(kc + sw128_off_f32(r, c0 + 4, rows), xv[4], xv[5], xv[6], xv[7]);
+                st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), q2[16 * hb + 4 * gi],
+                             q2[16 * hb + 4 * gi + 1], q2[16 * hb + 4 * gi + 2], q2[16 * hb + 4 * gi + 3]);
+                // references m > J: k e^{rho_{J+1} - Gamma_r} e^{rho_m - rho_{J+1}}
+                float ky[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ky[e] = xv[e] * vec[(V_D + J) * 128 + c0 + e];
+                for (int m = J + 1; m < 4; ++m) {
+                    const float* F = vec + (V_F + f_index(m, J)) * 128 + c0;
+                    const uint32_t km = sbase + OFF_X + x_kc(m);
+                    const int rm = 16 * (m + 1);
+                    st_shared_f4(km + sw128_off_f32(r, c0, rm), ky[0] * F[0], ky[1] * F[1], ky[2] * F[2], ky[3] * F[3]);
+                    st_shared_f4(km + sw128_off_f32(r, c0 + 4, rm), ky[4] * F[4], ky[5] * F[5], ky[6] * F[6],
+                                 ky[7] * F[7]);
+                }
             }
         }
+        tmem_st32(tmem_addr(tm, 32 * quarter, TM_KQ + 64 * half + 32 * hb), kq);
     }
-    tmem_st32u(tmem_addr(tm, 32 * quarter, TM_KQ + 32 * half), kq);
     if (isq) tmem_st32u(tmem_addr(tm, 32 * quarter, TM_A1 + 32 * half), q2);
 }
 
 // ---------------------------------------------------------------- phase 3: A/P read-out
-// Warp-group 0, lane L: row r = L % 64 of A (L < 64, scaled by beta_r, strictly lower)
-// or of P (L >= 64, lower with diagonal).  A goes to shared memory for the solve; P and
-// the zero halves of the [T diag(beta); 0] and [0; P] operands go to TMEM.
+// Warp-group 0, lane L: row r = L % 64 of A (L < 64: scaled by beta_r, strictly
+// lower) or of P (L >= 64: lower with diagonal), fp32 into shared memory.
 __device__ __forceinline__ void phase3_readout(uint8_t* sm, uint32_t tm, int L, int quarter, const float* sbeta)
 {
     const int r = L & 63, J = r >> 4;
@@ -369,22 +403,15 @@ __device__ __forceinline__ void phase3_readout(uint8_t* sm, uint32_t tm, int L, 
             for (int i = 48; i < 64; ++i) row[i] = 0.f;
         }
     }
-    uint32_t zero[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) zero[i] = 0u;
     if (!isP) {
         float* sA = reinterpret_cast<float*>(sm + OFF_X + X_SA);
         const float b = sbeta[r];
 #pragma unroll
         for (int i = 0; i < 64; ++i) sA[r * LDA + i] = (i < r) ? b * row[i] : 0.f;
-        tmem_st32u(tmem_addr(tm, lane0, TM_TPB), zero);
     } else {
-        uint32_t pk[32];
+        float* sP = reinterpret_cast<float*>(sm + OFF_X + X_SP);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            pk[i] = pack_bf16x2((2 * i <= r) ? row[2 * i] : 0.f, (2 * i + 1 <= r) ? row[2 * i + 1] : 0.f);
-        tmem_st32u(tmem_addr(tm, lane0, TM_TPB), pk);
-        tmem_st32u(tmem_addr(tm, lane0, TM_TPA), zero);
+        for (int i = 0; i < 64; ++i) sP[r * LDA + i] = (i <= r) ? row[i] : 0.f;
     }
 }
 
@@ -439,20 +466,41 @@ __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
     }
 }
 
-// 64 consecutive fp32 TMEM columns of this thread's lane -> bf16 rows of an MN-major
-// B-operand tile (row `row`, value columns [64 half, 64 half + 64), `rows` rows per block).
-__device__ __forceinline__ void store_row_bf16(uint32_t tile, int row, int half, int rows, const float (&a)[32],
-                                               const float (&b)[32])
+// ---------------------------------------------------------------- phase 3: M = P T diag(beta)
+// All 256 threads; thread t owns position (t/16, t%16) of every 16x16 block; the
+// result overwrites A (no longer needed).  Blocks above the diagonal are zero.
+__device__ __forceinline__ void phase3_mmat(uint8_t* sm, int t, const float* sbeta)
+{
+    const float* sP = reinterpret_cast<const float*>(sm + OFF_X + X_SP);
+    const float* sT = reinterpret_cast<const float*>(sm + OFF_X + X_ST);
+    float* sM = reinterpret_cast<float*>(sm + OFF_X + X_SA);
+    const int i = t >> 4, j = t & 15;
+#pragma unroll
+    for (int I = 0; I < 4; ++I) {
+#pragma unroll
+        for (int J = 0; J < 4; ++J) {
+            float acc = 0.f;
+            if (J <= I) {
+                for (int p = J; p <= I; ++p) {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        acc = fmaf(sP[(16 * I + i) * LDA + 16 * p + q], sT[(16 * p + q) * LDA + 16 * J + j], acc);
+                }
+                acc *= sbeta[16 * J + j];
+            }
+            sM[(16 * I + i) * LDA + 16 * J + j] = acc;
+        }
+    }
+}
+
+// 64 fp32 values of a row -> bf16 rows of an MN-major B-operand tile (row `row`,
+// value columns [64 half, 64 half + 64), `rows` rows per 64-column block).
+__device__ __forceinline__ void store_row_bf16(uint32_t tile, int row, int half, int rows, const uint32_t (&pk)[32])
 {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        st_shared_v4(tile + sw128_chunk(row, 8 * half + q, rows), pack_bf16x2(a[8 * q], a[8 * q + 1]),
-                     pack_bf16x2(a[8 * q + 2], a[8 * q + 3]), pack_bf16x2(a[8 * q + 4], a[8 * q + 5]),
-                     pack_bf16x2(a[8 * q + 6], a[8 * q + 7]));
-        st_shared_v4(tile + sw128_chunk(row, 8 * half + 4 + q, rows), pack_bf16x2(b[8 * q], b[8 * q + 1]),
-                     pack_bf16x2(b[8 * q + 2], b[8 * q + 3]), pack_bf16x2(b[8 * q + 4], b[8 * q + 5]),
-                     pack_bf16x2(b[8 * q + 6], b[8 * q + 7]));
-    }
+    for (int q = 0; q < 8; ++q)
+        st_shared_v4(tile + sw128_chunk(row, 8 * half + q, rows), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                     pk[4 * q + 3]);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -540,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         }
         if (!(ok = wait_all(bar_in, in_par, s_abort))) break;
         in_par ^= 1u;
-        tma_pending = false;
+        if (t == 0) tma_pending = false;
 
         // ---- phase 1: decayed operands
         if (t < 128) phase1_cumsum(sm, vec, t, BT);
@@ -552,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_before_sync();
         __syncthreads();
 
-        // ---- next chunk's loads, then phase 2 (A/P MMAs)
+        // ---- next chunk's loads, then phase 2: A and P by tf32 MMAs
         if (t == 0) {
             tc_fence_after_sync();
             if (ci + 1 < nchunks) {
@@ -561,11 +609,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             }
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                const uint32_t idesc = idesc_bf16_f32(128, 16 * (m + 1), 0, 0);
+                const uint32_t idesc = idesc_tf32_f32(128, 16 * (m + 1));
                 const uint32_t kc = sbase + OFF_X + x_kc(m);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    umma_bf16_tmem_a(tm + tm_ap(m), tm + TM_KQ + 8 * ks, desc_kmajor(kc, 16 * (m + 1), ks), idesc,
+                for (int ks = 0; ks < 16; ++ks)
+                    umma_tf32_tmem_a(tm + tm_ap(m), tm + TM_KQ + 8 * ks, desc_kmajor(kc, 16 * (m + 1), ks), idesc,
                                      ks > 0 ? 1u : 0u);
             }
             umma_commit(bar_mma);
@@ -574,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         mma_par ^= 1u;
         tc_fence_after_sync();
 
-        // ---- phase 3: A/P read-out (warp-group 0) while warp-group 1 clears T, then the solve
+        // ---- phase 3: A/P read-out (warp-group 0) while warp-group 1 clears T; solve; M
         if (t < 128) {
             phase3_readout(sm, tm, L, quarter, sbeta);
         } else {
@@ -583,41 +631,63 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         }
         __syncthreads();
         phase3_solve(sm, t);
-        if (t < 64) {   // [T diag(beta)] rows 0-63 into TMEM
-            const float* sT = reinterpret_cast<const float*>(sm + OFF_X + X_ST);
-            uint32_t pk[32];
+        phase3_mmat(sm, t, sbeta);
+        __syncthreads();
+        if (t < 128) {   // [Tb; M] rows as bf16 hi + lo pairs into TMEM
+            const int r = L & 63;
+            const float* src = reinterpret_cast<const float*>(sm + OFF_X + (L < 64 ? X_ST : X_SA)) + r * LDA;
+            const bool scale = L < 64;   // T rows take diag(beta) here; M already has it
+            uint32_t hi[32], lo[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                pk[i] = pack_bf16x2(sT[t * LDA + 2 * i] * sbeta[2 * i], sT[t * LDA + 2 * i + 1] * sbeta[2 * i + 1]);
-            tmem_st32u(tmem_addr(tm, 32 * quarter, TM_TPA), pk);
+            for (int i = 0; i < 32; ++i) {
+                const float a = scale ? src[2 * i] * sbeta[2 * i] : src[2 * i];
+                const float b = scale ? src[2 * i + 1] * sbeta[2 * i + 1] : src[2 * i + 1];
+                split_bf16x2(a, b, hi[i], lo[i]);
+            }
+            tmem_st32u(tmem_addr(tm, 32 * quarter, TM_TPH), hi);
+            tmem_st32u(tmem_addr(tm, 32 * quarter, TM_TPL), lo);
         }
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
 
-        // ---- phase 4: Wk = T diag(beta) K_Gamma, then -Wk into the A1 operand rows 0-63
+        // ---- phase 4: D2 = [Tb; M] K_Gamma (hi + lo), then A1 = [-Wk; Q_Gamma - M K_Gamma]
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                umma_bf16_tmem_a(tm + TM_WK, tm + TM_TPA + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc,
+                umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPH + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc,
                                  ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPL + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
             umma_commit(bar_mma);
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        if (quarter < 2) {
+        {
             float a[32], b[32];
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_WK + 64 * half), a);
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_WK + 64 * half + 32), b);
-            tmem_wait_ld();
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 64 * half), a);
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 64 * half + 32), b);
             uint32_t pk[32];
+            if (quarter < 2) {   // rows 0-63: -Wk
+                tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
-                pk[16 + i] = pack_bf16x2(-b[2 * i], -b[2 * i + 1]);
+                for (int i = 0; i < 16; ++i) {
+                    pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
+                    pk[16 + i] = pack_bf16x2(-b[2 * i], -b[2 * i + 1]);
+                }
+            } else {             // rows 64-127: Q' = Q_Gamma - M K_Gamma
+                tmem_ld32u(tmem_addr(tm, 32 * quarter, TM_A1 + 32 * half), pk);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float2 qa = bf2_to_f2(pk[i]), qb = bf2_to_f2(pk[16 + i]);
+                    pk[i] = pack_bf16x2(qa.x - a[2 * i], qa.y - a[2 * i + 1]);
+                    pk[16 + i] = pack_bf16x2(qb.x - b[2 * i], qb.y - b[2 * i + 1]);
+                }
             }
             tmem_st32u(tmem_addr(tm, 32 * quarter, TM_A1 + 32 * half), pk);
             tmem_wait_st();
@@ -631,7 +701,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 64 * half), a);
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 64 * half + 32), b);
             tmem_wait_ld();
-            store_row_bf16(sbase + OFF_X + X_SB, L, half, 128, a, b);
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                pk[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+                pk[16 + i] = pack_bf16x2(b[2 * i], b[2 * i + 1]);
+            }
+            store_row_bf16(sbase + OFF_X + X_SB, L, half, 128, pk);
             const float gc = vec[V_GC * 128 + L];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -646,14 +722,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_before_sync();
         __syncthreads();
 
-        // ---- phase 5b: D1 = [T diag(beta); 0] V + [-Wk; Q_Gamma] S
+        // ---- phase 5b: D1 = [Tb; M] V (hi + lo) + [-Wk; Q'] S
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
             const uint32_t vb = sbase + ((ci & 1) ? OFF_V1 : OFF_V0);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPA + 8 * ks, desc_mnmajor(vb, 64, ks), idesc, ks > 0 ? 1u : 0u);
+                umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPH + 8 * ks, desc_mnmajor(vb, 64, ks), idesc, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPL + 8 * ks, desc_mnmajor(vb, 64, ks), idesc, 1u);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1 + 8 * ks, desc_mnmajor(sbase + OFF_X + X_SB, 128, ks), idesc,
@@ -664,51 +743,53 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         mma_par ^= 1u;
         tc_fence_after_sync();
 
-        // ---- phase 5c: W = D1 rows 0-63 -> bf16 MN-major B operand
-        if (quarter < 2) {
+        // ---- phase 5c: rows 0-63 -> W (hi + lo) B operands; rows 64-127 -> O to HBM
+        {
             float a[32], b[32];
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half), a);
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half + 32), b);
             tmem_wait_ld();
-            store_row_bf16(sbase + OFF_X + X_WB, L, half, 64, a, b);
+            if (quarter < 2) {
+                uint32_t hi[32], lo[32];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
+                    split_bf16x2(b[2 * i], b[2 * i + 1], hi[16 + i], lo[16 + i]);
+                }
+                store_row_bf16(sbase + OFF_X + X_WH, L, half, 64, hi);
+                store_row_bf16(sbase + OFF_X + X_WL, L, half, 64, lo);
+            } else {
+                const int r = L - 64;
+                if (r < BT) {
+                    float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)(t0 + r) * H + h) * 128 + 64 * half);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+                        dst[8 + i] = make_float4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
+                    }
+                }
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
 
-        // ---- phase 5d: D1 += [0; P] W;  S += K~^T W
+        // ---- phase 5d: S += K~^T W (hi + lo)
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
-            const uint32_t wb = sbase + OFF_X + X_WB;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPB + 8 * ks, desc_mnmajor(wb, 64, ks), idesc, 1u);
+                umma_bf16_tmem_a(tm + TM_S, tm + TM_KT + 8 * ks, desc_mnmajor(sbase + OFF_X + X_WH, 64, ks), idesc,
+                                 1u);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                umma_bf16_tmem_a(tm + TM_S, tm + TM_KT + 8 * ks, desc_mnmajor(wb, 64, ks), idesc, 1u);
+                umma_bf16_tmem_a(tm + TM_S, tm + TM_KT + 8 * ks, desc_mnmajor(sbase + OFF_X + X_WL, 64, ks), idesc,
+                                 1u);
             umma_commit(bar_mma);
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
-        tc_fence_after_sync();
-
-        // ---- phase 5e: O = D1 rows 64-127 -> HBM (fp32)
-        if (quarter >= 2) {
-            const int r = L - 64;
-            float a[32], b[32];
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half), a);
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half + 32), b);
-            tmem_wait_ld();
-            if (r < BT) {
-                float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)(t0 + r) * H + h) * 128 + 64 * half);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
-                    dst[8 + i] = make_float4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
-                }
-            }
-        }
     }
 
     tc_fence_before_sync();
