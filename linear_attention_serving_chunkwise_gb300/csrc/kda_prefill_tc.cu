@@ -24,10 +24,11 @@
 // One CTA owns one (sequence, head) and walks its chunks in order; the fp32 state
 // lives in tensor memory for the whole sequence.  Per chunk:
 //   1  g cumsum per channel; decayed operands to TMEM (A operands) and shared
-//      memory (B operands); TMA prefetch of the next chunk.
+//      memory (B operands); TMA prefetch of the next chunk's k and v.
 //   2  A and P by four tf32 MMAs (one per sub-tile reference).
 //   3  T = (I + A)^-1 and M = P Tb in fp32 on CUDA cores.
-//   4  [Wk; M K_Gamma] by MMA, then the [-Wk; Q'] operand.
+//   4  [Wk; M K_Gamma] by MMA, then the [-Wk; Q'] operand; TMA prefetch of the
+//      next chunk's q and g.
 //   5  D1 = [Tb; M] V + [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O;
 //      O to HBM, W to shared memory; S += K~^T W by MMA.
 #include <cuda.h>
@@ -203,17 +204,23 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* s_
     return *s_abort == 0;
 }
 
-__device__ __forceinline__ void issue_chunk_loads(const TcParams& p, uint8_t* sm, uint64_t* bar, int vbuf, int t0,
-                                                  int h)
+// k and v of a chunk (v into one of two buffers); completes on `bar` (32 KB).
+__device__ __forceinline__ void issue_kv_loads(const TcParams& p, uint8_t* sm, uint64_t* bar, int vbuf, int t0, int h)
 {
-    mbar_arrive_expect_tx(bar, 81920u);
-    tma_load_3d(sm + OFF_Q, &p.tm_q, bar, 0, h, t0);
-    tma_load_3d(sm + OFF_Q + 8192, &p.tm_q, bar, 64, h, t0);
+    mbar_arrive_expect_tx(bar, 32768u);
     tma_load_3d(sm + OFF_K, &p.tm_k, bar, 0, h, t0);
     tma_load_3d(sm + OFF_K + 8192, &p.tm_k, bar, 64, h, t0);
     uint8_t* vb = sm + (vbuf ? OFF_V1 : OFF_V0);
     tma_load_3d(vb, &p.tm_v, bar, 0, h, t0);
     tma_load_3d(vb + 8192, &p.tm_v, bar, 64, h, t0);
+}
+
+// q and g of a chunk; completes on `bar` (48 KB).
+__device__ __forceinline__ void issue_qg_loads(const TcParams& p, uint8_t* sm, uint64_t* bar, int t0, int h)
+{
+    mbar_arrive_expect_tx(bar, 49152u);
+    tma_load_3d(sm + OFF_Q, &p.tm_q, bar, 0, h, t0);
+    tma_load_3d(sm + OFF_Q + 8192, &p.tm_q, bar, 64, h, t0);
 #pragma unroll
     for (int b = 0; b < 4; ++b) tma_load_3d(sm + OFF_G + 8192 * b, &p.tm_g, bar, 32 * b, h, t0);
 }
@@ -294,9 +301,9 @@ __device__ __forceinline__ void phase1_ktilde(uint8_t* sm, const float* vec, uin
 
 // ---------------------------------------------------------------- phase 1b: token operands
 // Thread (lane L, half h): token r = L % 64 of the q rows (L >= 64) or k rows (L < 64),
-// channels [64h, 64h + 64).  Writes the tf32 row operand [K_r; Q_r] (TMEM), Q_Gamma
-// (TMEM, q rows), and for k rows the fp32 column operands of every reference m >= J
-// and the bf16 K_Gamma B operand (shared memory).
+// channels [64h, 64h + 64).  Writes the tf32 row operand [K_r; Q_r] (TMEM) and, for
+// k rows, the fp32 column operands of every reference m >= J and the bf16 K_Gamma B
+// operand (shared memory).
 __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uint32_t tm, int L, int half,
                                               int quarter, int BT)
 {
@@ -357,7 +364,6 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
         }
         tmem_st32(tmem_addr(tm, 32 * quarter, TM_KQ + 64 * half + 32 * hb), kq);
     }
-    if (isq) tmem_st32u(tmem_addr(tm, 32 * quarter, TM_A1 + 32 * half), q2);
 }
 
 // ---------------------------------------------------------------- phase 3: A/P read-out
@@ -503,6 +509,45 @@ __device__ __forceinline__ void store_row_bf16(uint32_t tile, int row, int half,
                      pk[4 * q + 3]);
 }
 
+// Q' row = Q_Gamma - M K_Gamma for token r = L - 64 (lanes 64-127), channels [64h, 64h + 64):
+// Q_Gamma is recomputed in fp32 from the q and cumsum tiles so that the one bf16 rounding
+// happens after the (strongly cancelling) subtraction.
+__device__ __forceinline__ void phase4_qprime(uint8_t* sm, const float* vec, uint32_t tm, int L, int half,
+                                              int quarter, int BT)
+{
+    const int r = L - 64, J = r >> 4;
+    const bool valid = r < BT;
+    const uint32_t sbase = smem_u32(sm);
+    uint32_t pk[32];
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+        float mk[32];
+        tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 64 * half + 32 * hb), mk);
+        tmem_wait_ld();
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+            const int c0 = 64 * half + 32 * hb + 8 * gi;
+            const uint4 raw = ld_shared_v4(sbase + OFF_Q + sw128_chunk(r, c0 >> 3, 64));
+            const uint4 la = ld_shared_v4(sbase + OFF_G + g_off(r, c0));
+            const uint4 lb = ld_shared_v4(sbase + OFF_G + g_off(r, c0 + 4));
+            const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
+            const float qv[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
+            const float lam[8] = {__uint_as_float(la.x), __uint_as_float(la.y), __uint_as_float(la.z),
+                                  __uint_as_float(la.w), __uint_as_float(lb.x), __uint_as_float(lb.y),
+                                  __uint_as_float(lb.z), __uint_as_float(lb.w)};
+            float qp[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float qg = valid ? qv[e] * ex2f(lam[e]) * vec[(V_E + J) * 128 + c0 + e] : 0.f;
+                qp[e] = qg - mk[8 * gi + e];
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pk[16 * hb + 4 * gi + e] = pack_bf16x2(qp[2 * e], qp[2 * e + 1]);
+        }
+    }
+    tmem_st32u(tmem_addr(tm, 32 * quarter, TM_A1 + 32 * half), pk);
+}
+
 // ---------------------------------------------------------------- the kernel
 __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcParams p)
 {
@@ -513,9 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     const int L = 32 * quarter + lane;   // the TMEM lane this thread may access
     float* vec = reinterpret_cast<float*>(sm + OFF_VEC);
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
-    uint64_t* bar_in = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-    uint64_t* bar_mma = bar_in + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_in + 2);
+    uint64_t* bar_kv = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint64_t* bar_qg = bar_kv + 1;
+    uint64_t* bar_mma = bar_kv + 2;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_kv + 3);
     int* s_abort = reinterpret_cast<int*>(tslot + 1);
     const uint32_t sbase = smem_u32(sm);
 
@@ -527,7 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     const size_t sbase_g = ((size_t)n * H + h) * 128 * 128;
 
     if (t == 0) {
-        mbar_init(bar_in, 1);
+        mbar_init(bar_kv, 1);
+        mbar_init(bar_qg, 1);
         mbar_init(bar_mma, 1);
         mbar_fence_init();
         *s_abort = 0;
@@ -545,10 +592,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     tc_fence_after_sync();
     const uint32_t tm = *tslot;
 
-    bool tma_pending = false;   // meaningful in thread 0 only
+    bool kv_pending = false, qg_pending = false;   // meaningful in thread 0 only
     if (t == 0 && nchunks > 0) {
-        issue_chunk_loads(p, sm, bar_in, 0, bos, h);
-        tma_pending = true;
+        issue_kv_loads(p, sm, bar_kv, 0, bos, h);
+        issue_qg_loads(p, sm, bar_qg, bos, h);
+        kv_pending = qg_pending = true;
     }
 
     // initial state -> TMEM: lane L = key channel, columns [64 half, 64 half + 64)
@@ -572,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     tmem_wait_st();
 
     float beta_next = (t < 64 && bos + t < eos) ? __ldg(p.beta + (size_t)(bos + t) * H + h) : 0.f;
-    uint32_t in_par = 0, mma_par = 0;
+    uint32_t kv_par = 0, qg_par = 0, mma_par = 0;
     bool ok = true;
 
     for (int ci = 0; ci < nchunks; ++ci) {
@@ -586,9 +634,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             const int tn = t0 + 64 + t;
             beta_next = (ci + 1 < nchunks && tn < eos) ? __ldg(p.beta + (size_t)tn * H + h) : 0.f;
         }
-        if (!(ok = wait_all(bar_in, in_par, s_abort))) break;
-        in_par ^= 1u;
-        if (t == 0) tma_pending = false;
+        if (!(ok = wait_all(bar_kv, kv_par, s_abort))) break;
+        kv_par ^= 1u;
+        if (!(ok = wait_all(bar_qg, qg_par, s_abort))) break;
+        qg_par ^= 1u;
+        if (t == 0) kv_pending = qg_pending = false;
 
         // ---- phase 1: decayed operands
         if (t < 128) phase1_cumsum(sm, vec, t, BT);
@@ -604,8 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (t == 0) {
             tc_fence_after_sync();
             if (ci + 1 < nchunks) {
-                issue_chunk_loads(p, sm, bar_in, (ci + 1) & 1, t0 + 64, h);
-                tma_pending = true;
+                issue_kv_loads(p, sm, bar_kv, (ci + 1) & 1, t0 + 64, h);
+                kv_pending = true;
             }
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -667,33 +717,29 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        {
+        if (quarter < 2) {   // rows 0-63: -Wk
             float a[32], b[32];
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 64 * half), a);
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 64 * half + 32), b);
+            tmem_wait_ld();
             uint32_t pk[32];
-            if (quarter < 2) {   // rows 0-63: -Wk
-                tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
-                    pk[16 + i] = pack_bf16x2(-b[2 * i], -b[2 * i + 1]);
-                }
-            } else {             // rows 64-127: Q' = Q_Gamma - M K_Gamma
-                tmem_ld32u(tmem_addr(tm, 32 * quarter, TM_A1 + 32 * half), pk);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float2 qa = bf2_to_f2(pk[i]), qb = bf2_to_f2(pk[16 + i]);
-                    pk[i] = pack_bf16x2(qa.x - a[2 * i], qa.y - a[2 * i + 1]);
-                    pk[16 + i] = pack_bf16x2(qb.x - b[2 * i], qb.y - b[2 * i + 1]);
-                }
+            for (int i = 0; i < 16; ++i) {
+                pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
+                pk[16 + i] = pack_bf16x2(-b[2 * i], -b[2 * i + 1]);
             }
             tmem_st32u(tmem_addr(tm, 32 * quarter, TM_A1 + 32 * half), pk);
-            tmem_wait_st();
+        } else {             // rows 64-127: Q' = Q_Gamma - M K_Gamma
+            phase4_qprime(sm, vec, tm, L, half, quarter, BT);
         }
+        tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
+        // the q and g tiles of this chunk are no longer read: fetch the next chunk's
+        if (t == 0 && ci + 1 < nchunks) {
+            issue_qg_loads(p, sm, bar_qg, t0 + 64, h);
+            qg_pending = true;
+        }
 
         // ---- phase 5a: S -> bf16 B operand; S <- Diag(gamma_C) S in place
         {
@@ -810,7 +856,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     if (!ok && t == 0) {
         // a wait gave up: record it, let in-flight copies and MMAs land (bounded), then leave
         report_status(p.status, kDevTimeout);
-        if (tma_pending) mbar_wait_bounded(bar_in, in_par, kWaitNs);
+        if (kv_pending) mbar_wait_bounded(bar_kv, kv_par, kWaitNs);
+        if (qg_pending) mbar_wait_bounded(bar_qg, qg_par, kWaitNs);
         mbar_wait_bounded(bar_mma, mma_par, kWaitNs);
     }
     tc_fence_before_sync();
