@@ -17,7 +17,8 @@
 // row factor is <= 1 and the column factor is <= e^{5*16} on the diagonal tile
 // and <= 1 off it.
 //
-// Precision: A and P use tf32 MMAs (fp32 operands); Tb, M and W enter their MMAs as
+// Precision: A and P use tf32 MMAs (operands rounded to nearest tf32 first, since
+// the tensor core truncates); Tb, M and W enter their MMAs as
 // bf16 hi + lo pairs; S, Wk, Q', K_Gamma and K~ are single bf16; accumulation and
 // the carried state are fp32.
 //
@@ -188,6 +189,14 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t u)
     return __bfloat1622float2(h);
 }
 
+// fp32 -> the nearest tf32 value (ties away from zero), kept in fp32 storage.  The
+// tensor core drops the low 13 mantissa bits of a tf32 operand; rounding first halves
+// the operand error and removes its bias.
+__device__ __forceinline__ float tf32_round(float x)
+{
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+}
+
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi): the pair carries ~16 mantissa bits.
 __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo)
 {
@@ -335,8 +344,9 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
             for (int e = 0; e < 8; ++e) {
                 const float v = valid ? xv[e] : 0.f;
                 const float x = ex2f(lam[e]);                        // e^{Gamma_r - rho_J} in (0, 1]
-                kq[8 * gi + e] = v * x;
-                gam[e] = kq[8 * gi + e] * vec[(V_E + J) * 128 + c0 + e];  // v e^{Gamma_r}
+                const float vx = v * x;
+                kq[8 * gi + e] = tf32_round(vx);
+                gam[e] = vx * vec[(V_E + J) * 128 + c0 + e];         // v e^{Gamma_r}
                 xv[e] = v * rcpf(x);                                 // v e^{rho_J - Gamma_r}, <= e^{80} |v|
             }
 #pragma unroll
@@ -344,8 +354,10 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
             if (!isq) {
                 const uint32_t kc = sbase + OFF_X + x_kc(J);
                 const int rows = 16 * (J + 1);
-                st_shared_f4(kc + sw128_off_f32(r, c0, rows), xv[0], xv[1], xv[2], xv[3]);
-                st_shared_f4(kc + sw128_off_f32(r, c0 + 4, rows), xv[4], xv[5], xv[6], xv[7]);
+                st_shared_f4(kc + sw128_off_f32(r, c0, rows), tf32_round(xv[0]), tf32_round(xv[1]),
+                             tf32_round(xv[2]), tf32_round(xv[3]));
+                st_shared_f4(kc + sw128_off_f32(r, c0 + 4, rows), tf32_round(xv[4]), tf32_round(xv[5]),
+                             tf32_round(xv[6]), tf32_round(xv[7]));
                 st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), q2[16 * hb + 4 * gi],
                              q2[16 * hb + 4 * gi + 1], q2[16 * hb + 4 * gi + 2], q2[16 * hb + 4 * gi + 3]);
                 // references m > J: k e^{rho_{J+1} - Gamma_r} e^{rho_m - rho_{J+1}}
@@ -356,9 +368,10 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
                     const float* F = vec + (V_F + f_index(m, J)) * 128 + c0;
                     const uint32_t km = sbase + OFF_X + x_kc(m);
                     const int rm = 16 * (m + 1);
-                    st_shared_f4(km + sw128_off_f32(r, c0, rm), ky[0] * F[0], ky[1] * F[1], ky[2] * F[2], ky[3] * F[3]);
-                    st_shared_f4(km + sw128_off_f32(r, c0 + 4, rm), ky[4] * F[4], ky[5] * F[5], ky[6] * F[6],
-                                 ky[7] * F[7]);
+                    st_shared_f4(km + sw128_off_f32(r, c0, rm), tf32_round(ky[0] * F[0]), tf32_round(ky[1] * F[1]),
+                                 tf32_round(ky[2] * F[2]), tf32_round(ky[3] * F[3]));
+                    st_shared_f4(km + sw128_off_f32(r, c0 + 4, rm), tf32_round(ky[4] * F[4]),
+                                 tf32_round(ky[5] * F[5]), tf32_round(ky[6] * F[6]), tf32_round(ky[7] * F[7]));
                 }
             }
         }
