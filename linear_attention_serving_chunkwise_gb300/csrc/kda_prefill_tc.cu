@@ -19,17 +19,18 @@
 //
 // Precision: A and P use tf32 MMAs (operands rounded to nearest tf32 first, since
 // the tensor core truncates); Tb, M and W enter their MMAs as
-// bf16 hi + lo pairs; S, Wk, Q', K_Gamma and K~ are single bf16; accumulation and
+// bf16 hi + lo pairs, and so does K~ in the state update; S, Wk, Q' and K_Gamma are
+// single bf16; accumulation and
 // the carried state are fp32.
 //
 // One CTA owns one (sequence, head) and walks its chunks in order; the fp32 state
 // lives in tensor memory for the whole sequence.  Per chunk:
 //   1  g cumsum per channel; decayed operands to TMEM (A operands) and shared
-//      memory (B operands); TMA prefetch of the next chunk's k and v.
+//      memory (B operands); TMA prefetch of the next chunk's v.
 //   2  A and P by four tf32 MMAs (one per sub-tile reference).
 //   3  T = (I + A)^-1 and M = P Tb in fp32 on CUDA cores.
-//   4  [Wk; M K_Gamma] by MMA, then the [-Wk; Q'] operand; TMA prefetch of the
-//      next chunk's q and g.
+//   4  [Wk; M K_Gamma] by MMA while K~^T is built, then the [-Wk; Q'] operand;
+//      TMA prefetch of the next chunk's q, k and g.
 //   5  D1 = [Tb; M] V + [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O;
 //      O to HBM, W to shared memory; S += K~^T W by MMA.
 #include <cuda.h>
@@ -93,8 +94,9 @@ constexpr uint32_t TM_D1 = 128;   // [W; O] accumulator (phase 5)
 constexpr uint32_t TM_AP = 256;   // A/P accumulators, sub-tile m at 256 + 16 m (m+1) / 2 (phases 2-3)
 constexpr uint32_t TM_TPH = 256;  // [Tb; M] hi, bf16 pairs (phases 3-5)
 constexpr uint32_t TM_TPL = 288;  // [Tb; M] lo (phases 3-5)
+constexpr uint32_t TM_KTL = 320;  // K~^T lo (phases 4-5)
 constexpr uint32_t TM_A1 = 416;   // [-Wk; Q_Gamma then Q'] bf16 pairs (phases 1-5)
-constexpr uint32_t TM_KT = 480;   // K~^T, lane = key channel, bf16 pairs (phases 1-5)
+constexpr uint32_t TM_KT = 480;   // K~^T hi, lane = key channel, bf16 pairs (phases 4-5)
 constexpr uint32_t TM_COLS = 512;
 
 __host__ __device__ constexpr uint32_t tm_ap(int m) { return TM_AP + 8u * m * (m + 1); }
@@ -213,23 +215,23 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* s_
     return *s_abort == 0;
 }
 
-// k and v of a chunk (v into one of two buffers); completes on `bar` (32 KB).
-__device__ __forceinline__ void issue_kv_loads(const TcParams& p, uint8_t* sm, uint64_t* bar, int vbuf, int t0, int h)
+// v of a chunk into one of two buffers; completes on `bar` (16 KB).
+__device__ __forceinline__ void issue_v_loads(const TcParams& p, uint8_t* sm, uint64_t* bar, int vbuf, int t0, int h)
 {
-    mbar_arrive_expect_tx(bar, 32768u);
-    tma_load_3d(sm + OFF_K, &p.tm_k, bar, 0, h, t0);
-    tma_load_3d(sm + OFF_K + 8192, &p.tm_k, bar, 64, h, t0);
+    mbar_arrive_expect_tx(bar, 16384u);
     uint8_t* vb = sm + (vbuf ? OFF_V1 : OFF_V0);
     tma_load_3d(vb, &p.tm_v, bar, 0, h, t0);
     tma_load_3d(vb + 8192, &p.tm_v, bar, 64, h, t0);
 }
 
-// q and g of a chunk; completes on `bar` (48 KB).
-__device__ __forceinline__ void issue_qg_loads(const TcParams& p, uint8_t* sm, uint64_t* bar, int t0, int h)
+// q, k and g of a chunk; completes on `bar` (64 KB).
+__device__ __forceinline__ void issue_qkg_loads(const TcParams& p, uint8_t* sm, uint64_t* bar, int t0, int h)
 {
-    mbar_arrive_expect_tx(bar, 49152u);
+    mbar_arrive_expect_tx(bar, 65536u);
     tma_load_3d(sm + OFF_Q, &p.tm_q, bar, 0, h, t0);
     tma_load_3d(sm + OFF_Q + 8192, &p.tm_q, bar, 64, h, t0);
+    tma_load_3d(sm + OFF_K, &p.tm_k, bar, 0, h, t0);
+    tma_load_3d(sm + OFF_K + 8192, &p.tm_k, bar, 64, h, t0);
 #pragma unroll
     for (int b = 0; b < 4; ++b) tma_load_3d(sm + OFF_G + 8192 * b, &p.tm_g, bar, 32 * b, h, t0);
 }
@@ -277,13 +279,13 @@ __device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int c, in
     vec[V_GC * 128 + c] = ex2f(lam63);
 }
 
-// ---------------------------------------------------------------- phase 1a': K~^T into TMEM
+// ---------------------------------------------------------------- phase 4: K~^T into TMEM
 // Lane c of the K~^T operand holds K~[r][c] = k[r][c] e^{Gamma_63 - Gamma_r} for the
-// 32 tokens r of this warp-group half, two tokens per column.
-__device__ __forceinline__ void phase1_ktilde(uint8_t* sm, const float* vec, uint32_t tm, int c, int half,
+// 32 tokens r of this warp-group half, two tokens per column, as a bf16 hi + lo pair.
+__device__ __forceinline__ void phase4_ktilde(uint8_t* sm, const float* vec, uint32_t tm, int c, int half,
                                               int quarter, int BT)
 {
-    uint32_t packed[16];
+    uint32_t hi[16], lo[16];
     const uint32_t kbase = smem_u32(sm + OFF_K);
     const float s1 = vec[(V_S + 1) * 128 + c], s2 = vec[(V_S + 2) * 128 + c], s3 = vec[(V_S + 3) * 128 + c];
     const float tail0 = s1 + s2 + s3, tail1 = s2 + s3, tail2 = s3;
@@ -303,9 +305,10 @@ __device__ __forceinline__ void phase1_ktilde(uint8_t* sm, const float* vec, uin
             const float kv = (r < BT) ? __uint_as_float(((uint32_t)kb) << 16) : 0.f;
             f2[e] = kv * fac;
         }
-        packed[pr] = pack_bf16x2(f2[0], f2[1]);
+        split_bf16x2(f2[0], f2[1], hi[pr], lo[pr]);
     }
-    tmem_st16u(tmem_addr(tm, 32 * quarter, TM_KT + 16 * half), packed);
+    tmem_st16u(tmem_addr(tm, 32 * quarter, TM_KT + 16 * half), hi);
+    tmem_st16u(tmem_addr(tm, 32 * quarter, TM_KTL + 16 * half), lo);
 }
 
 // ---------------------------------------------------------------- phase 1b: token operands
@@ -571,10 +574,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     const int L = 32 * quarter + lane;   // the TMEM lane this thread may access
     float* vec = reinterpret_cast<float*>(sm + OFF_VEC);
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
-    uint64_t* bar_kv = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-    uint64_t* bar_qg = bar_kv + 1;
-    uint64_t* bar_mma = bar_kv + 2;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_kv + 3);
+    uint64_t* bar_v = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint64_t* bar_qkg = bar_v + 1;
+    uint64_t* bar_mma = bar_v + 2;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_v + 3);
     int* s_abort = reinterpret_cast<int*>(tslot + 1);
     const uint32_t sbase = smem_u32(sm);
 
@@ -586,8 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     const size_t sbase_g = ((size_t)n * H + h) * 128 * 128;
 
     if (t == 0) {
-        mbar_init(bar_kv, 1);
-        mbar_init(bar_qg, 1);
+        mbar_init(bar_v, 1);
+        mbar_init(bar_qkg, 1);
         mbar_init(bar_mma, 1);
         mbar_fence_init();
         *s_abort = 0;
@@ -605,11 +608,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     tc_fence_after_sync();
     const uint32_t tm = *tslot;
 
-    bool kv_pending = false, qg_pending = false;   // meaningful in thread 0 only
+    bool v_pending = false, qkg_pending = false;   // meaningful in thread 0 only
     if (t == 0 && nchunks > 0) {
-        issue_kv_loads(p, sm, bar_kv, 0, bos, h);
-        issue_qg_loads(p, sm, bar_qg, bos, h);
-        kv_pending = qg_pending = true;
+        issue_v_loads(p, sm, bar_v, 0, bos, h);
+        issue_qkg_loads(p, sm, bar_qkg, bos, h);
+        v_pending = qkg_pending = true;
     }
 
     // initial state -> TMEM: lane L = key channel, columns [64 half, 64 half + 64)
@@ -633,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     tmem_wait_st();
 
     float beta_next = (t < 64 && bos + t < eos) ? __ldg(p.beta + (size_t)(bos + t) * H + h) : 0.f;
-    uint32_t kv_par = 0, qg_par = 0, mma_par = 0;
+    uint32_t v_par = 0, qkg_par = 0, mma_par = 0;
     bool ok = true;
 
     for (int ci = 0; ci < nchunks; ++ci) {
@@ -647,16 +650,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             const int tn = t0 + 64 + t;
             beta_next = (ci + 1 < nchunks && tn < eos) ? __ldg(p.beta + (size_t)tn * H + h) : 0.f;
         }
-        if (!(ok = wait_all(bar_kv, kv_par, s_abort))) break;
-        kv_par ^= 1u;
-        if (!(ok = wait_all(bar_qg, qg_par, s_abort))) break;
-        qg_par ^= 1u;
-        if (t == 0) kv_pending = qg_pending = false;
+        if (!(ok = wait_all(bar_v, v_par, s_abort))) break;
+        v_par ^= 1u;
+        if (!(ok = wait_all(bar_qkg, qkg_par, s_abort))) break;
+        qkg_par ^= 1u;
+        if (t == 0) v_pending = qkg_pending = false;
 
         // ---- phase 1: decayed operands
         if (t < 128) phase1_cumsum(sm, vec, t, BT);
         __syncthreads();
-        phase1_ktilde(sm, vec, tm, L, half, quarter, BT);
         phase1_tokens(sm, vec, tm, L, half, quarter, BT);
         fence_proxy_async_smem();
         tmem_wait_st();
@@ -667,8 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (t == 0) {
             tc_fence_after_sync();
             if (ci + 1 < nchunks) {
-                issue_kv_loads(p, sm, bar_kv, (ci + 1) & 1, t0 + 64, h);
-                kv_pending = true;
+                issue_v_loads(p, sm, bar_v, (ci + 1) & 1, t0 + 64, h);
+                v_pending = true;
             }
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -727,6 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPL + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
             umma_commit(bar_mma);
         }
+        phase4_ktilde(sm, vec, tm, L, half, quarter, BT);   // overlaps the MMA above
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
@@ -748,10 +751,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
-        // the q and g tiles of this chunk are no longer read: fetch the next chunk's
+        // the q, k and g tiles of this chunk are no longer read: fetch the next chunk's
         if (t == 0 && ci + 1 < nchunks) {
-            issue_qg_loads(p, sm, bar_qg, t0 + 64, h);
-            qg_pending = true;
+            issue_qkg_loads(p, sm, bar_qkg, t0 + 64, h);
+            qkg_pending = true;
         }
 
         // ---- phase 5a: S -> bf16 B operand; S <- Diag(gamma_C) S in place
@@ -833,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_before_sync();
         __syncthreads();
 
-        // ---- phase 5d: S += K~^T W (hi + lo)
+        // ---- phase 5d: S += K~^T W (hi hi + hi lo + lo hi)
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
@@ -844,6 +847,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 umma_bf16_tmem_a(tm + TM_S, tm + TM_KT + 8 * ks, desc_mnmajor(sbase + OFF_X + X_WL, 64, ks), idesc,
+                                 1u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_S, tm + TM_KTL + 8 * ks, desc_mnmajor(sbase + OFF_X + X_WH, 64, ks), idesc,
                                  1u);
             umma_commit(bar_mma);
         }
@@ -869,8 +876,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     if (!ok && t == 0) {
         // a wait gave up: record it, let in-flight copies and MMAs land (bounded), then leave
         report_status(p.status, kDevTimeout);
-        if (kv_pending) mbar_wait_bounded(bar_kv, kv_par, kWaitNs);
-        if (qg_pending) mbar_wait_bounded(bar_qg, qg_par, kWaitNs);
+        if (v_pending) mbar_wait_bounded(bar_v, v_par, kWaitNs);
+        if (qkg_pending) mbar_wait_bounded(bar_qkg, qkg_par, kWaitNs);
         mbar_wait_bounded(bar_mma, mma_par, kWaitNs);
     }
     tc_fence_before_sync();
