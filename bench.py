@@ -355,7 +355,7 @@ def run_cuda(args, world, rank, local):
             "roofline": roofline, "tensor": tensor, "e2e": e2e, "clocks": clocks,
             "gpu_launches": args.steps * plan["kernel_launches"], "decode": decode}
     if rank == 0 and world == 1:
-        rate, dt, cores, sdesc = oracle_sample(cfg, heads=32, tokens=8192)
+        rate, dt, cores, sdesc = oracle_sample(cfg, heads=96, tokens=8192)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sdesc,
                                 "seconds": dt}
     if rank == 0:
