@@ -27,7 +27,7 @@
 // lives in tensor memory for the whole sequence.  Per chunk:
 //   1  g cumsum per channel; decayed operands to TMEM (A operands) and shared
 //      memory (B operands); TMA prefetch of the next chunk's v.
-//   2  A and P by four tf32 MMAs (one per sub-tile reference).
+//   2  A and P by one tf32 MMA over the four sub-tile references side by side.
 //   3  T = (I + A)^-1 and M = P Tb in fp32 on CUDA cores.
 //   4  [Wk; M K_Gamma] by MMA while K~^T is built, then the [-Wk; Q'] operand;
 //      TMA prefetch of the next chunk's q, k and g.
@@ -73,8 +73,10 @@ constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr size_t SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
 constexpr int LDA = 65;
 
-// fp32 column operands of the A/P MMAs: reference m has 16(m+1) rows at X + 4096 m (m+1)
-__host__ __device__ constexpr uint32_t x_kc(int m) { return 4096u * m * (m + 1); }
+// fp32 column operand of the A/P MMA: one K-major tile of 160 rows (4 blocks of 32
+// channels, block stride 160 * 128 bytes); reference m owns rows [8 m (m+1), 8 (m+1)(m+2)).
+constexpr uint32_t KC_ROWS = 160;
+__host__ __device__ constexpr uint32_t kc_row(int m) { return 8u * m * (m + 1); }
 
 // per-channel vectors (index * 128 floats into OFF_VEC)
 constexpr int V_S = 0;     // s_J: sum of g*log2e over sub-tile J            (4)
@@ -237,14 +239,15 @@ __device__ __forceinline__ void issue_qkg_loads(const TcParams& p, uint8_t* sm, 
 }
 
 // ---------------------------------------------------------------- phase 1a: per-channel cumsum
-// Thread c (< 128) turns column c of the g tile into the sub-tile-local cumsum
-// lambda_r = sum_{s = 16J}^{r} g_s log2(e) (rows past the chunk's end count as 0)
-// and writes the per-channel factors.
-__device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int c, int BT)
+// Thread (c = t % 128, pair = t / 128) turns sub-tiles 2 pair and 2 pair + 1 of column c
+// of the g tile into the sub-tile-local cumsum lambda_r = sum_{s = 16J}^{r} g_s log2(e)
+// (rows past the chunk's end count as 0) and stores the sub-tile sums s_J.
+__device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, int BT)
 {
-    float s[4];
+    const int c = t & 127, pair = t >> 7;
 #pragma unroll
-    for (int J = 0; J < 4; ++J) {
+    for (int jj = 0; jj < 2; ++jj) {
+        const int J = 2 * pair + jj;
         float acc = 0.f;
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
@@ -254,27 +257,33 @@ __device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int c, in
             acc = fmaf(gv, kLog2e, acc);
             *gp = acc;
         }
-        s[J] = acc;
+        vec[(V_S + J) * 128 + c] = acc;
     }
-    const float rho1 = s[0], rho2 = s[0] + s[1], rho3 = rho2 + s[2], lam63 = rho3 + s[3];
-    const float tail0 = s[1] + s[2] + s[3], tail1 = s[2] + s[3], tail2 = s[3];
-#pragma unroll
-    for (int J = 0; J < 4; ++J) vec[(V_S + J) * 128 + c] = s[J];
+}
+
+// Per-channel factors from the sub-tile sums (thread c < 128, after phase1_cumsum).
+__device__ __forceinline__ void phase1_factors(float* vec, int c)
+{
+    const float s0 = vec[(V_S + 0) * 128 + c], s1 = vec[(V_S + 1) * 128 + c], s2 = vec[(V_S + 2) * 128 + c],
+                s3 = vec[(V_S + 3) * 128 + c];
+    const float rho1 = s0, rho2 = s0 + s1, rho3 = rho2 + s2, lam63 = rho3 + s3;
     vec[(V_E + 0) * 128 + c] = 1.f;
     vec[(V_E + 1) * 128 + c] = ex2f(rho1);
     vec[(V_E + 2) * 128 + c] = ex2f(rho2);
     vec[(V_E + 3) * 128 + c] = ex2f(rho3);
-    vec[(V_G + 0) * 128 + c] = ex2f(tail0);
-    vec[(V_G + 1) * 128 + c] = ex2f(tail1);
-    vec[(V_G + 2) * 128 + c] = ex2f(tail2);
+    vec[(V_G + 0) * 128 + c] = ex2f(s1 + s2 + s3);
+    vec[(V_G + 1) * 128 + c] = ex2f(s2 + s3);
+    vec[(V_G + 2) * 128 + c] = ex2f(s3);
     vec[(V_G + 3) * 128 + c] = 1.f;
-#pragma unroll
-    for (int J = 0; J < 4; ++J) vec[(V_D + J) * 128 + c] = ex2f(s[J]);
+    vec[(V_D + 0) * 128 + c] = ex2f(s0);
+    vec[(V_D + 1) * 128 + c] = ex2f(s1);
+    vec[(V_D + 2) * 128 + c] = ex2f(s2);
+    vec[(V_D + 3) * 128 + c] = ex2f(s3);
     vec[(V_F + f_index(1, 0)) * 128 + c] = 1.f;
-    vec[(V_F + f_index(2, 0)) * 128 + c] = ex2f(s[1]);
+    vec[(V_F + f_index(2, 0)) * 128 + c] = ex2f(s1);
     vec[(V_F + f_index(2, 1)) * 128 + c] = 1.f;
-    vec[(V_F + f_index(3, 0)) * 128 + c] = ex2f(s[1] + s[2]);
-    vec[(V_F + f_index(3, 1)) * 128 + c] = ex2f(s[2]);
+    vec[(V_F + f_index(3, 0)) * 128 + c] = ex2f(s1 + s2);
+    vec[(V_F + f_index(3, 1)) * 128 + c] = ex2f(s2);
     vec[(V_F + f_index(3, 2)) * 128 + c] = 1.f;
     vec[V_GC * 128 + c] = ex2f(lam63);
 }
@@ -355,11 +364,11 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
 #pragma unroll
             for (int e = 0; e < 4; ++e) q2[16 * hb + 4 * gi + e] = pack_bf16x2(gam[2 * e], gam[2 * e + 1]);
             if (!isq) {
-                const uint32_t kc = sbase + OFF_X + x_kc(J);
-                const int rows = 16 * (J + 1);
-                st_shared_f4(kc + sw128_off_f32(r, c0, rows), tf32_round(xv[0]), tf32_round(xv[1]),
+                const uint32_t kc = sbase + OFF_X;
+                const uint32_t rj = kc_row(J) + r;
+                st_shared_f4(kc + sw128_off_f32(rj, c0, KC_ROWS), tf32_round(xv[0]), tf32_round(xv[1]),
                              tf32_round(xv[2]), tf32_round(xv[3]));
-                st_shared_f4(kc + sw128_off_f32(r, c0 + 4, rows), tf32_round(xv[4]), tf32_round(xv[5]),
+                st_shared_f4(kc + sw128_off_f32(rj, c0 + 4, KC_ROWS), tf32_round(xv[4]), tf32_round(xv[5]),
                              tf32_round(xv[6]), tf32_round(xv[7]));
                 st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), q2[16 * hb + 4 * gi],
                              q2[16 * hb + 4 * gi + 1], q2[16 * hb + 4 * gi + 2], q2[16 * hb + 4 * gi + 3]);
@@ -369,11 +378,10 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
                 for (int e = 0; e < 8; ++e) ky[e] = xv[e] * vec[(V_D + J) * 128 + c0 + e];
                 for (int m = J + 1; m < 4; ++m) {
                     const float* F = vec + (V_F + f_index(m, J)) * 128 + c0;
-                    const uint32_t km = sbase + OFF_X + x_kc(m);
-                    const int rm = 16 * (m + 1);
-                    st_shared_f4(km + sw128_off_f32(r, c0, rm), tf32_round(ky[0] * F[0]), tf32_round(ky[1] * F[1]),
-                                 tf32_round(ky[2] * F[2]), tf32_round(ky[3] * F[3]));
-                    st_shared_f4(km + sw128_off_f32(r, c0 + 4, rm), tf32_round(ky[4] * F[4]),
+                    const uint32_t rm = kc_row(m) + r;
+                    st_shared_f4(kc + sw128_off_f32(rm, c0, KC_ROWS), tf32_round(ky[0] * F[0]),
+                                 tf32_round(ky[1] * F[1]), tf32_round(ky[2] * F[2]), tf32_round(ky[3] * F[3]));
+                    st_shared_f4(kc + sw128_off_f32(rm, c0 + 4, KC_ROWS), tf32_round(ky[4] * F[4]),
                                  tf32_round(ky[5] * F[5]), tf32_round(ky[6] * F[6]), tf32_round(ky[7] * F[7]));
                 }
             }
@@ -657,7 +665,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (t == 0) v_pending = qkg_pending = false;
 
         // ---- phase 1: decayed operands
-        if (t < 128) phase1_cumsum(sm, vec, t, BT);
+        phase1_cumsum(sm, vec, t, BT);
+        __syncthreads();
+        if (t < 128) phase1_factors(vec, t);
         __syncthreads();
         phase1_tokens(sm, vec, tm, L, half, quarter, BT);
         fence_proxy_async_smem();
@@ -672,13 +682,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 issue_v_loads(p, sm, bar_v, (ci + 1) & 1, t0 + 64, h);
                 v_pending = true;
             }
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const uint32_t idesc = idesc_tf32_f32(128, 16 * (m + 1));
-                const uint32_t kc = sbase + OFF_X + x_kc(m);
+            {   // all four references at once: N = 160 columns, reference m in columns [8m(m+1), 8(m+1)(m+2))
+                const uint32_t idesc = idesc_tf32_f32(128, KC_ROWS);
+                const uint32_t kc = sbase + OFF_X;
 #pragma unroll
                 for (int ks = 0; ks < 16; ++ks)
-                    umma_tf32_tmem_a(tm + tm_ap(m), tm + TM_KQ + 8 * ks, desc_kmajor(kc, 16 * (m + 1), ks), idesc,
+                    umma_tf32_tmem_a(tm + TM_AP, tm + TM_KQ + 8 * ks, desc_kmajor(kc, KC_ROWS, ks), idesc,
                                      ks > 0 ? 1u : 0u);
             }
             umma_commit(bar_mma);
@@ -805,38 +814,26 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         mma_par ^= 1u;
         tc_fence_after_sync();
 
-        // ---- phase 5c: rows 0-63 -> W (hi + lo) B operands; rows 64-127 -> O to HBM
-        {
+        // ---- phase 5c: rows 0-63 -> W (hi + lo) B operands
+        if (quarter < 2) {
             float a[32], b[32];
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half), a);
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half + 32), b);
             tmem_wait_ld();
-            if (quarter < 2) {
-                uint32_t hi[32], lo[32];
+            uint32_t hi[32], lo[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
-                    split_bf16x2(b[2 * i], b[2 * i + 1], hi[16 + i], lo[16 + i]);
-                }
-                store_row_bf16(sbase + OFF_X + X_WH, L, half, 64, hi);
-                store_row_bf16(sbase + OFF_X + X_WL, L, half, 64, lo);
-            } else {
-                const int r = L - 64;
-                if (r < BT) {
-                    float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)(t0 + r) * H + h) * 128 + 64 * half);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
-                        dst[8 + i] = make_float4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
-                    }
-                }
+            for (int i = 0; i < 16; ++i) {
+                split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
+                split_bf16x2(b[2 * i], b[2 * i + 1], hi[16 + i], lo[16 + i]);
             }
+            store_row_bf16(sbase + OFF_X + X_WH, L, half, 64, hi);
+            store_row_bf16(sbase + OFF_X + X_WL, L, half, 64, lo);
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
 
-        // ---- phase 5d: S += K~^T W (hi hi + hi lo + lo hi)
+        // ---- phase 5d: S += K~^T W (hi hi + hi lo + lo hi), while rows 64-127 (O) go to HBM
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
@@ -853,6 +850,22 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 umma_bf16_tmem_a(tm + TM_S, tm + TM_KTL + 8 * ks, desc_mnmajor(sbase + OFF_X + X_WH, 64, ks), idesc,
                                  1u);
             umma_commit(bar_mma);
+        }
+        if (quarter >= 2) {
+            tc_fence_after_sync();
+            const int r = L - 64;
+            float a[32], b[32];
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half), a);
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half + 32), b);
+            tmem_wait_ld();
+            if (r < BT) {
+                float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)(t0 + r) * H + h) * 128 + 64 * half);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+                    dst[8 + i] = make_float4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
+                }
+            }
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
