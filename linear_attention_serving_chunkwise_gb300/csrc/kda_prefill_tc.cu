@@ -28,7 +28,7 @@
 //   1  g cumsum per channel; decayed operands to TMEM (A operands) and shared
 //      memory (B operands); TMA prefetch of the next chunk's v.
 //   2  A and P by one tf32 MMA over the four sub-tile references side by side.
-//   3  T = (I + A)^-1 and M = P Tb in fp32 on CUDA cores.
+//   3  T = (I + A)^-1 in fp32 on CUDA cores; M = P Tb by three bf16 MMAs (hi/lo splits).
 //   4  [Wk; M K_Gamma] by MMA while K~^T is built, then the [-Wk; Q'] operand;
 //      TMA prefetch of the next chunk's q, k and g.
 //   5  D1 = [Tb; M] V + [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O;
@@ -58,9 +58,10 @@ constexpr uint32_t OFF_G = 32768;      // g tile  [64][128] fp32, 4 x 8 KB boxes
 constexpr uint32_t OFF_V0 = 65536;     // v tile, two buffers (B operand of [Tb; M] V)
 constexpr uint32_t OFF_V1 = 81920;
 constexpr uint32_t OFF_X = 98304;      // 80 KB region shared by phases 1-2 / 3 / 5
-constexpr uint32_t X_SA = 0;           // A fp32 [64][65], then M
+constexpr uint32_t X_SA = 0;           // A fp32 [64][65]; after the solve: Tb hi/lo bf16 B operands
+constexpr uint32_t X_TBH = 0;          // Tb hi, MN-major B [64 i][64 j] bf16 (8 KB)
+constexpr uint32_t X_TBL = 8192;       // Tb lo
 constexpr uint32_t X_ST = 16640;       // T fp32 [64][65]
-constexpr uint32_t X_SP = 33280;       // P fp32 [64][65]
 constexpr uint32_t X_SY = 49920;       // level scratch fp32 [3][16][17]
 constexpr uint32_t X_SB = 0;           // S bf16, MN-major B [128 dk][128 dv]
 constexpr uint32_t X_WH = 32768;       // W hi bf16, MN-major B [64 tok][128 dv]
@@ -91,6 +92,9 @@ __host__ __device__ constexpr int f_index(int m, int J) { return m * (m - 1) / 2
 // ---------------------------------------------------------------- tensor memory map (columns)
 constexpr uint32_t TM_S = 0;      // state S [128 dk lanes][128 dv] fp32
 constexpr uint32_t TM_KQ = 128;   // [K_r; Q_r] tf32 A operand, one fp32 per column (phases 1-2)
+constexpr uint32_t TM_PH = 128;   // [0; P] hi, bf16 pairs (phase 3)
+constexpr uint32_t TM_PL = 160;   // [0; P] lo (phase 3)
+constexpr uint32_t TM_M = 192;    // M = P Tb accumulator, rows 64-127, 64 columns (phase 3)
 constexpr uint32_t TM_D2 = 128;   // [Wk; M K_Gamma] accumulator (phase 4)
 constexpr uint32_t TM_D1 = 128;   // [W; O] accumulator (phase 5)
 constexpr uint32_t TM_AP = 256;   // A/P accumulators, sub-tile m at 256 + 16 m (m+1) / 2 (phases 2-3)
@@ -392,7 +396,8 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
 
 // ---------------------------------------------------------------- phase 3: A/P read-out
 // Warp-group 0, lane L: row r = L % 64 of A (L < 64: scaled by beta_r, strictly
-// lower) or of P (L >= 64: lower with diagonal), fp32 into shared memory.
+// lower) into shared memory in fp32, or of P (L >= 64: lower with diagonal) into
+// TMEM as bf16 hi + lo pairs (the A operand of M = P Tb; lanes 0-63 get zeros).
 __device__ __forceinline__ void phase3_readout(uint8_t* sm, uint32_t tm, int L, int quarter, const float* sbeta)
 {
     const int r = L & 63, J = r >> 4;
@@ -433,22 +438,56 @@ __device__ __forceinline__ void phase3_readout(uint8_t* sm, uint32_t tm, int L, 
             for (int i = 48; i < 64; ++i) row[i] = 0.f;
         }
     }
+    uint32_t hi[32], lo[32];
     if (!isP) {
         float* sA = reinterpret_cast<float*>(sm + OFF_X + X_SA);
         const float b = sbeta[r];
 #pragma unroll
         for (int i = 0; i < 64; ++i) sA[r * LDA + i] = (i < r) ? b * row[i] : 0.f;
-    } else {
-        float* sP = reinterpret_cast<float*>(sm + OFF_X + X_SP);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) sP[r * LDA + i] = (i <= r) ? row[i] : 0.f;
+        for (int i = 0; i < 32; ++i) hi[i] = lo[i] = 0u;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            split_bf16x2((2 * i <= r) ? row[2 * i] : 0.f, (2 * i + 1 <= r) ? row[2 * i + 1] : 0.f, hi[i], lo[i]);
     }
+    tmem_st32u(tmem_addr(tm, lane0, TM_PH), hi);
+    tmem_st32u(tmem_addr(tm, lane0, TM_PL), lo);
 }
 
 // ---------------------------------------------------------------- phase 3: T = (I + A)^-1
 // All 256 threads.  sT must be zero on entry.  16x16 diagonal blocks by forward
 // substitution (one thread per column), then block levels d = 1..3:
 //   T_{m,m-d} = -T_{m,m} sum_{p=m-d}^{m-1} A_{m,p} T_{p,m-d}.
+template <int D>
+__device__ __forceinline__ void solve_level(const float* sA, float* sT, float* sY, int t)
+{
+    constexpr int NBLK = 4 - D;
+    // Y_{m,J} = sum_{p=J}^{m-1} A_{m,p} T_{p,J}, J = m - D; 4 independent partial sums
+    for (int idx = t; idx < NBLK * 256; idx += kThreads) {
+        const int bk = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+        const int m = bk + D, J = m - D;
+        const float* arow = sA + (16 * m + i) * LDA + 16 * J;
+        const float* tcol = sT + (16 * J) * LDA + 16 * J + j;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < 16 * D; ++q) acc[q & 3] = fmaf(arow[q], tcol[q * LDA], acc[q & 3]);
+        sY[bk * 272 + i * 17 + j] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    }
+    __syncthreads();
+    for (int idx = t; idx < NBLK * 256; idx += kThreads) {
+        const int bk = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+        const int m = bk + D, J = m - D;
+        const float* trow = sT + (16 * m + i) * LDA + 16 * m;
+        const float* y = sY + bk * 272 + j;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < 16; ++q) acc[q & 3] = fmaf(trow[q], y[q * 17], acc[q & 3]);
+        sT[(16 * m + i) * LDA + 16 * J + j] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
+    }
+    __syncthreads();
+}
+
 __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
 {
     const float* sA = reinterpret_cast<const float*>(sm + OFF_X + X_SA);
@@ -461,65 +500,40 @@ __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
         for (int q = 0; q < 16; ++q) x[q] = (q == j) ? 1.f : 0.f;
 #pragma unroll
         for (int rr = 1; rr < 16; ++rr) {
-            float acc = 0.f;
+            const float* arow = sA + (b + rr) * LDA + b;
+            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < rr; ++i) acc = fmaf(-sA[(b + rr) * LDA + b + i], x[i], acc);
-            if (rr > j) x[rr] = acc;
+            for (int i = 0; i < rr; ++i) {
+                if (i & 1) a1 = fmaf(-arow[i], x[i], a1);
+                else a0 = fmaf(-arow[i], x[i], a0);
+            }
+            if (rr > j) x[rr] = a0 + a1;
         }
 #pragma unroll
         for (int q = 0; q < 16; ++q) sT[(b + q) * LDA + b + j] = x[q];
     }
     __syncthreads();
-    for (int d = 1; d < 4; ++d) {
-        const int nblk = 4 - d;
-        for (int idx = t; idx < nblk * 256; idx += kThreads) {
-            const int bk = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
-            const int m = bk + d, J = m - d;
-            float acc = 0.f;
-            for (int p = J; p < m; ++p) {
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    acc = fmaf(sA[(16 * m + i) * LDA + 16 * p + q], sT[(16 * p + q) * LDA + 16 * J + j], acc);
-            }
-            sY[bk * 272 + i * 17 + j] = acc;
-        }
-        __syncthreads();
-        for (int idx = t; idx < nblk * 256; idx += kThreads) {
-            const int bk = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
-            const int m = bk + d, J = m - d;
-            float acc = 0.f;
-#pragma unroll
-            for (int q = 0; q < 16; ++q) acc = fmaf(sT[(16 * m + i) * LDA + 16 * m + q], sY[bk * 272 + q * 17 + j], acc);
-            sT[(16 * m + i) * LDA + 16 * J + j] = -acc;
-        }
-        __syncthreads();
-    }
+    solve_level<1>(sA, sT, sY, t);
+    solve_level<2>(sA, sT, sY, t);
+    solve_level<3>(sA, sT, sY, t);
 }
 
-// ---------------------------------------------------------------- phase 3: M = P T diag(beta)
-// All 256 threads; thread t owns position (t/16, t%16) of every 16x16 block; the
-// result overwrites A (no longer needed).  Blocks above the diagonal are zero.
-__device__ __forceinline__ void phase3_mmat(uint8_t* sm, int t, const float* sbeta)
+// Tb = T diag(beta) as bf16 hi + lo MN-major B operands [64 i][64 j] (all 256 threads).
+__device__ __forceinline__ void phase3_tb_operands(uint8_t* sm, int t, const float* sbeta)
 {
-    const float* sP = reinterpret_cast<const float*>(sm + OFF_X + X_SP);
     const float* sT = reinterpret_cast<const float*>(sm + OFF_X + X_ST);
-    float* sM = reinterpret_cast<float*>(sm + OFF_X + X_SA);
-    const int i = t >> 4, j = t & 15;
+    const uint32_t sbase = smem_u32(sm);
 #pragma unroll
-    for (int I = 0; I < 4; ++I) {
+    for (int u = 0; u < 2; ++u) {
+        const int idx = t + 256 * u, i = idx >> 3, ch = idx & 7;   // row i, 8-column chunk ch
+        uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int J = 0; J < 4; ++J) {
-            float acc = 0.f;
-            if (J <= I) {
-                for (int p = J; p <= I; ++p) {
-#pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        acc = fmaf(sP[(16 * I + i) * LDA + 16 * p + q], sT[(16 * p + q) * LDA + 16 * J + j], acc);
-                }
-                acc *= sbeta[16 * J + j];
-            }
-            sM[(16 * I + i) * LDA + 16 * J + j] = acc;
+        for (int e = 0; e < 4; ++e) {
+            const int j = 8 * ch + 2 * e;
+            split_bf16x2(sT[i * LDA + j] * sbeta[j], sT[i * LDA + j + 1] * sbeta[j + 1], hi[e], lo[e]);
         }
+        st_shared_v4(sbase + OFF_X + X_TBH + sw128_chunk(i, ch, 64), hi[0], hi[1], hi[2], hi[3]);
+        st_shared_v4(sbase + OFF_X + X_TBL + sw128_chunk(i, ch, 64), lo[0], lo[1], lo[2], lo[3]);
     }
 }
 
@@ -696,27 +710,61 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         mma_par ^= 1u;
         tc_fence_after_sync();
 
-        // ---- phase 3: A/P read-out (warp-group 0) while warp-group 1 clears T; solve; M
+        // ---- phase 3: A/P read-out (warp-group 0) while warp-group 1 clears T; solve;
+        //      M = P Tb by MMA; [Tb; M] hi/lo rows into TMEM
         if (t < 128) {
             phase3_readout(sm, tm, L, quarter, sbeta);
         } else {
             float* sT = reinterpret_cast<float*>(sm + OFF_X + X_ST);
             for (int idx = t - 128; idx < 64 * LDA; idx += 128) sT[idx] = 0.f;
         }
+        tmem_wait_st();
         __syncthreads();
         phase3_solve(sm, t);
-        phase3_mmat(sm, t, sbeta);
+        phase3_tb_operands(sm, t, sbeta);
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
         __syncthreads();
-        if (t < 128) {   // [Tb; M] rows as bf16 hi + lo pairs into TMEM
-            const int r = L & 63;
-            const float* src = reinterpret_cast<const float*>(sm + OFF_X + (L < 64 ? X_ST : X_SA)) + r * LDA;
-            const bool scale = L < 64;   // T rows take diag(beta) here; M already has it
+        if (t == 0) {
+            tc_fence_after_sync();
+            const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
+            const uint32_t tbh = sbase + OFF_X + X_TBH, tbl = sbase + OFF_X + X_TBL;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_M, tm + TM_PH + 8 * ks, desc_mnmajor(tbh, 64, ks), idesc, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_M, tm + TM_PH + 8 * ks, desc_mnmajor(tbl, 64, ks), idesc, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_M, tm + TM_PL + 8 * ks, desc_mnmajor(tbh, 64, ks), idesc, 1u);
+            umma_commit(bar_mma);
+        }
+        if (t < 64) {   // Tb rows (lanes 0-63) straight from the hi/lo B-operand tiles
             uint32_t hi[32], lo[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float a = scale ? src[2 * i] * sbeta[2 * i] : src[2 * i];
-                const float b = scale ? src[2 * i + 1] * sbeta[2 * i + 1] : src[2 * i + 1];
-                split_bf16x2(a, b, hi[i], lo[i]);
+            for (int ch = 0; ch < 8; ++ch) {
+                const uint4 h4 = ld_shared_v4(sbase + OFF_X + X_TBH + sw128_chunk(t, ch, 64));
+                const uint4 l4 = ld_shared_v4(sbase + OFF_X + X_TBL + sw128_chunk(t, ch, 64));
+                hi[4 * ch] = h4.x; hi[4 * ch + 1] = h4.y; hi[4 * ch + 2] = h4.z; hi[4 * ch + 3] = h4.w;
+                lo[4 * ch] = l4.x; lo[4 * ch + 1] = l4.y; lo[4 * ch + 2] = l4.z; lo[4 * ch + 3] = l4.w;
+            }
+            tmem_st32u(tmem_addr(tm, 32 * quarter, TM_TPH), hi);
+            tmem_st32u(tmem_addr(tm, 32 * quarter, TM_TPL), lo);
+        }
+        if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
+        mma_par ^= 1u;
+        tc_fence_after_sync();
+        if (t >= 64 && t < 128) {   // M rows (lanes 64-127) -> hi/lo
+            float a[32], b[32];
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_M), a);
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_M + 32), b);
+            tmem_wait_ld();
+            uint32_t hi[32], lo[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
+                split_bf16x2(b[2 * i], b[2 * i + 1], hi[16 + i], lo[16 + i]);
             }
             tmem_st32u(tmem_addr(tm, 32 * quarter, TM_TPH), hi);
             tmem_st32u(tmem_addr(tm, 32 * quarter, TM_TPL), lo);
