@@ -32,7 +32,8 @@
 //   4  [Wk; M K_Gamma] by MMA while K~^T is built, then the [-Wk; Q'] operand;
 //      TMA prefetch of the next chunk's q, k and g.
 //   5  D1 = [Tb; M] V + [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O;
-//      O to HBM, W to shared memory; S += K~^T W by MMA.
+//      W to shared memory; S += K~^T W by MMA while O is staged in shared memory and
+//      written by TMA bulk stores (direct stores for a sequence's ragged last chunk).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -58,11 +59,12 @@ constexpr uint32_t OFF_G = 32768;      // g tile  [64][128] fp32, 4 x 8 KB boxes
 constexpr uint32_t OFF_V0 = 65536;     // v tile, two buffers (B operand of [Tb; M] V)
 constexpr uint32_t OFF_V1 = 81920;
 constexpr uint32_t OFF_X = 98304;      // 80 KB region shared by phases 1-2 / 3 / 5
-constexpr uint32_t X_SA = 0;           // A fp32 [64][65]; after the solve: Tb hi/lo bf16 B operands
+constexpr uint32_t X_SA = 0;           // A fp32 [64][68]; after the solve: Tb hi/lo bf16 B operands
 constexpr uint32_t X_TBH = 0;          // Tb hi, MN-major B [64 i][64 j] bf16 (8 KB)
 constexpr uint32_t X_TBL = 8192;       // Tb lo
-constexpr uint32_t X_ST = 16640;       // T fp32 [64][65]
-constexpr uint32_t X_SY = 49920;       // level scratch fp32 [3][16][17]
+constexpr uint32_t X_ST = 17408;       // T fp32 [64][68]
+constexpr uint32_t X_SY = 34816;       // level scratch fp32 [3][16][20]
+constexpr uint32_t X_OST = 65536;      // O staging, dv columns 0-63: 2 x [64 tok][32] fp32 boxes (phase 5)
 constexpr uint32_t X_SB = 0;           // S bf16, MN-major B [128 dk][128 dv]
 constexpr uint32_t X_WH = 32768;       // W hi bf16, MN-major B [64 tok][128 dv]
 constexpr uint32_t X_WL = 49152;       // W lo
@@ -72,7 +74,8 @@ constexpr uint32_t OFF_BETA = OFF_VEC + 23 * 512;
 constexpr uint32_t OFF_BAR = OFF_BETA + 256;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr size_t SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
-constexpr int LDA = 65;
+constexpr int LDA = 68;    // fp32 row stride of A and T: 16-byte aligned rows
+constexpr int LDY = 20;    // row stride of the level scratch
 
 // fp32 column operand of the A/P MMA: one K-major tile of 160 rows (4 blocks of 32
 // channels, block stride 160 * 128 bytes); reference m owns rows [8 m (m+1), 8 (m+1)(m+2)).
@@ -108,7 +111,7 @@ constexpr uint32_t TM_COLS = 512;
 __host__ __device__ constexpr uint32_t tm_ap(int m) { return TM_AP + 8u * m * (m + 1); }
 
 struct TcParams {
-    CUtensorMap tm_q, tm_k, tm_v, tm_g;
+    CUtensorMap tm_q, tm_k, tm_v, tm_g, tm_o;
     const float* beta;
     const int32_t* cu_seqlens;
     const float* init_state;
@@ -326,9 +329,10 @@ __device__ __forceinline__ void phase4_ktilde(uint8_t* sm, const float* vec, uin
 
 // ---------------------------------------------------------------- phase 1b: token operands
 // Thread (lane L, half h): token r = L % 64 of the q rows (L >= 64) or k rows (L < 64),
-// channels [64h, 64h + 64).  Writes the tf32 row operand [K_r; Q_r] (TMEM) and, for
-// k rows, the fp32 column operands of every reference m >= J and the bf16 K_Gamma B
-// operand (shared memory).
+// channels [64h, 64h + 64).  Writes the tf32 row operand [K_r; Q_r] (TMEM).  The k-row
+// thread also writes token r's diagonal-tile column operand and its K_Gamma B operand;
+// the q-row thread of the same token writes that token's column operands for the
+// references m > J (balancing the two halves).
 __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uint32_t tm, int L, int half,
                                               int quarter, int BT)
 {
@@ -355,20 +359,26 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
                 lam[3] = __uint_as_float(la.w); lam[4] = __uint_as_float(lb.x); lam[5] = __uint_as_float(lb.y);
                 lam[6] = __uint_as_float(lb.z); lam[7] = __uint_as_float(lb.w);
             }
-            float gam[8];
+            const float4 e4a = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
+            const float4 e4b = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
+            const float ev[8] = {e4a.x, e4a.y, e4a.z, e4a.w, e4b.x, e4b.y, e4b.z, e4b.w};
+            float gam[8], xr[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float v = valid ? xv[e] : 0.f;
                 const float x = ex2f(lam[e]);                        // e^{Gamma_r - rho_J} in (0, 1]
                 const float vx = v * x;
                 kq[8 * gi + e] = tf32_round(vx);
-                gam[e] = vx * vec[(V_E + J) * 128 + c0 + e];         // v e^{Gamma_r}
-                xv[e] = v * rcpf(x);                                 // v e^{rho_J - Gamma_r}, <= e^{80} |v|
+                gam[e] = vx * ev[e];                                 // v e^{Gamma_r}
+                xr[e] = rcpf(x);                                     // e^{rho_J - Gamma_r} <= e^{80}
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) q2[16 * hb + 4 * gi + e] = pack_bf16x2(gam[2 * e], gam[2 * e + 1]);
+            const uint32_t kc = sbase + OFF_X;
             if (!isq) {
-                const uint32_t kc = sbase + OFF_X;
+                // diagonal-tile column operand of reference J, and the K_Gamma B operand
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xv[e] = (valid ? xv[e] : 0.f) * xr[e];
                 const uint32_t rj = kc_row(J) + r;
                 st_shared_f4(kc + sw128_off_f32(rj, c0, KC_ROWS), tf32_round(xv[0]), tf32_round(xv[1]),
                              tf32_round(xv[2]), tf32_round(xv[3]));
@@ -376,17 +386,27 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
                              tf32_round(xv[6]), tf32_round(xv[7]));
                 st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), q2[16 * hb + 4 * gi],
                              q2[16 * hb + 4 * gi + 1], q2[16 * hb + 4 * gi + 2], q2[16 * hb + 4 * gi + 3]);
-                // references m > J: k e^{rho_{J+1} - Gamma_r} e^{rho_m - rho_{J+1}}
+            } else if (J < 3) {
+                // this token's k, for the column operands of references m > J:
+                // k e^{rho_{J+1} - Gamma_r} e^{rho_m - rho_{J+1}}
+                const uint4 kraw = ld_shared_v4(sbase + OFF_K + sw128_chunk(r, c0 >> 3, 64));
+                const float2 k0 = bf2_to_f2(kraw.x), k1 = bf2_to_f2(kraw.y), k2 = bf2_to_f2(kraw.z),
+                             k3 = bf2_to_f2(kraw.w);
+                const float kvv[8] = {k0.x, k0.y, k1.x, k1.y, k2.x, k2.y, k3.x, k3.y};
+                const float4 d4a = *reinterpret_cast<const float4*>(vec + (V_D + J) * 128 + c0);
+                const float4 d4b = *reinterpret_cast<const float4*>(vec + (V_D + J) * 128 + c0 + 4);
+                const float dv[8] = {d4a.x, d4a.y, d4a.z, d4a.w, d4b.x, d4b.y, d4b.z, d4b.w};
                 float ky[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ky[e] = xv[e] * vec[(V_D + J) * 128 + c0 + e];
+                for (int e = 0; e < 8; ++e) ky[e] = (valid ? kvv[e] : 0.f) * xr[e] * dv[e];
                 for (int m = J + 1; m < 4; ++m) {
-                    const float* F = vec + (V_F + f_index(m, J)) * 128 + c0;
+                    const float4 f4a = *reinterpret_cast<const float4*>(vec + (V_F + f_index(m, J)) * 128 + c0);
+                    const float4 f4b = *reinterpret_cast<const float4*>(vec + (V_F + f_index(m, J)) * 128 + c0 + 4);
                     const uint32_t rm = kc_row(m) + r;
-                    st_shared_f4(kc + sw128_off_f32(rm, c0, KC_ROWS), tf32_round(ky[0] * F[0]),
-                                 tf32_round(ky[1] * F[1]), tf32_round(ky[2] * F[2]), tf32_round(ky[3] * F[3]));
-                    st_shared_f4(kc + sw128_off_f32(rm, c0 + 4, KC_ROWS), tf32_round(ky[4] * F[4]),
-                                 tf32_round(ky[5] * F[5]), tf32_round(ky[6] * F[6]), tf32_round(ky[7] * F[7]));
+                    st_shared_f4(kc + sw128_off_f32(rm, c0, KC_ROWS), tf32_round(ky[0] * f4a.x),
+                                 tf32_round(ky[1] * f4a.y), tf32_round(ky[2] * f4a.z), tf32_round(ky[3] * f4a.w));
+                    st_shared_f4(kc + sw128_off_f32(rm, c0 + 4, KC_ROWS), tf32_round(ky[4] * f4b.x),
+                                 tf32_round(ky[5] * f4b.y), tf32_round(ky[6] * f4b.z), tf32_round(ky[7] * f4b.w));
                 }
             }
         }
@@ -463,27 +483,46 @@ template <int D>
 __device__ __forceinline__ void solve_level(const float* sA, float* sT, float* sY, int t)
 {
     constexpr int NBLK = 4 - D;
-    // Y_{m,J} = sum_{p=J}^{m-1} A_{m,p} T_{p,J}, J = m - D; 4 independent partial sums
-    for (int idx = t; idx < NBLK * 256; idx += kThreads) {
-        const int bk = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+    // Y_{m,J} = sum_{p=J}^{m-1} A_{m,p} T_{p,J}, J = m - D; each thread 4 adjacent columns
+    if (t < NBLK * 64) {
+        const int bk = t >> 6, i = (t >> 2) & 15, j4 = (t & 3) * 4;
         const int m = bk + D, J = m - D;
         const float* arow = sA + (16 * m + i) * LDA + 16 * J;
-        const float* tcol = sT + (16 * J) * LDA + 16 * J + j;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const float* tb = sT + (16 * J) * LDA + 16 * J + j4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acc2 = acc;
 #pragma unroll
-        for (int q = 0; q < 16 * D; ++q) acc[q & 3] = fmaf(arow[q], tcol[q * LDA], acc[q & 3]);
-        sY[bk * 272 + i * 17 + j] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        for (int q = 0; q < 16 * D; q += 2) {
+            const float a0 = arow[q], a1 = arow[q + 1];
+            const float4 t0 = *reinterpret_cast<const float4*>(tb + q * LDA);
+            const float4 t1 = *reinterpret_cast<const float4*>(tb + (q + 1) * LDA);
+            acc.x = fmaf(a0, t0.x, acc.x); acc.y = fmaf(a0, t0.y, acc.y);
+            acc.z = fmaf(a0, t0.z, acc.z); acc.w = fmaf(a0, t0.w, acc.w);
+            acc2.x = fmaf(a1, t1.x, acc2.x); acc2.y = fmaf(a1, t1.y, acc2.y);
+            acc2.z = fmaf(a1, t1.z, acc2.z); acc2.w = fmaf(a1, t1.w, acc2.w);
+        }
+        *reinterpret_cast<float4*>(sY + bk * 16 * LDY + i * LDY + j4) =
+            make_float4(acc.x + acc2.x, acc.y + acc2.y, acc.z + acc2.z, acc.w + acc2.w);
     }
     __syncthreads();
-    for (int idx = t; idx < NBLK * 256; idx += kThreads) {
-        const int bk = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+    // T_{m,J} = -T_{m,m} Y_{m,J}
+    if (t < NBLK * 64) {
+        const int bk = t >> 6, i = (t >> 2) & 15, j4 = (t & 3) * 4;
         const int m = bk + D, J = m - D;
         const float* trow = sT + (16 * m + i) * LDA + 16 * m;
-        const float* y = sY + bk * 272 + j;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const float* y = sY + bk * 16 * LDY + j4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acc2 = acc;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) acc[q & 3] = fmaf(trow[q], y[q * 17], acc[q & 3]);
-        sT[(16 * m + i) * LDA + 16 * J + j] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
+        for (int q = 0; q < 16; q += 2) {
+            const float a0 = trow[q], a1 = trow[q + 1];
+            const float4 y0 = *reinterpret_cast<const float4*>(y + q * LDY);
+            const float4 y1 = *reinterpret_cast<const float4*>(y + (q + 1) * LDY);
+            acc.x = fmaf(a0, y0.x, acc.x); acc.y = fmaf(a0, y0.y, acc.y);
+            acc.z = fmaf(a0, y0.z, acc.z); acc.w = fmaf(a0, y0.w, acc.w);
+            acc2.x = fmaf(a1, y1.x, acc2.x); acc2.y = fmaf(a1, y1.y, acc2.y);
+            acc2.z = fmaf(a1, y1.z, acc2.z); acc2.w = fmaf(a1, y1.w, acc2.w);
+        }
+        *reinterpret_cast<float4*>(sT + (16 * m + i) * LDA + 16 * J + j4) =
+            make_float4(-(acc.x + acc2.x), -(acc.y + acc2.y), -(acc.z + acc2.z), -(acc.w + acc2.w));
     }
     __syncthreads();
 }
@@ -620,6 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
         tma_prefetch_desc(&p.tm_g);
+        tma_prefetch_desc(&p.tm_o);
     }
     if (warp == 0) {
         tmem_alloc(tslot, TM_COLS);
@@ -630,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     tc_fence_after_sync();
     const uint32_t tm = *tslot;
 
-    bool v_pending = false, qkg_pending = false;   // meaningful in thread 0 only
+    bool v_pending = false, qkg_pending = false, o_pending = false;   // meaningful in thread 0 only
     if (t == 0 && nchunks > 0) {
         issue_v_loads(p, sm, bar_v, 0, bos, h);
         issue_qkg_loads(p, sm, bar_qkg, bos, h);
@@ -665,6 +705,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         const int t0 = bos + 64 * ci;
         const int BT = min(64, eos - t0);
         if (t < 64) sbeta[t] = beta_next;
+        if (t == 0 && o_pending) {   // the previous chunk's O staging must be read out before reuse
+            bulk_wait_read();
+            o_pending = false;
+        }
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
@@ -906,7 +950,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half), a);
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half + 32), b);
             tmem_wait_ld();
-            if (r < BT) {
+            if (BT == 64) {
+                // stage in 128-byte-swizzled [64 tok][32] fp32 boxes for one TMA store per box:
+                // columns 0-63 in the free top of the X region, 64-127 in this chunk's v buffer
+                const uint32_t box0 = half ? sbase + ((ci & 1) ? OFF_V1 : OFF_V0) : sbase + OFF_X + X_OST;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    st_shared_f4(box0 + sw128_off_f32(r, 4 * q, 64), a[4 * q], a[4 * q + 1], a[4 * q + 2],
+                                 a[4 * q + 3]);
+                    st_shared_f4(box0 + 8192 + sw128_off_f32(r, 4 * q, 64), b[4 * q], b[4 * q + 1], b[4 * q + 2],
+                                 b[4 * q + 3]);
+                }
+                fence_proxy_async_smem();
+            } else if (r < BT) {
                 float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)(t0 + r) * H + h) * 128 + 64 * half);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -917,7 +973,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
+        if (t == 0 && BT == 64) {
+            const uint8_t* vb = sm + ((ci & 1) ? OFF_V1 : OFF_V0);
+            tma_store_3d(&p.tm_o, sm + OFF_X + X_OST, 0, h, t0);
+            tma_store_3d(&p.tm_o, sm + OFF_X + X_OST + 8192, 32, h, t0);
+            tma_store_3d(&p.tm_o, vb, 64, h, t0);
+            tma_store_3d(&p.tm_o, vb + 8192, 96, h, t0);
+            bulk_commit();
+            o_pending = true;
+        }
     }
+    if (t == 0) bulk_wait_all();   // staged O fully written before the CTA's shared memory goes away
 
     tc_fence_before_sync();
     __syncthreads();
@@ -984,7 +1050,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream)
     if (!make_map(&p.tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
         !make_map(&p.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
         !make_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
-        !make_map(&p.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32))
+        !make_map(&p.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32) ||
+        !make_map(&p.tm_o, a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32))
         return cudaErrorInvalidValue;
     p.beta = a.beta;
     p.cu_seqlens = a.cu_seqlens;
