@@ -48,7 +48,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;   // bound on every on-device wait
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -177,6 +177,13 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[3
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -246,26 +253,22 @@ __device__ __forceinline__ void issue_qkg_loads(const TcParams& p, uint8_t* sm, 
 }
 
 // ---------------------------------------------------------------- phase 1a: per-channel cumsum
-// Thread (c = t % 128, pair = t / 128) turns sub-tiles 2 pair and 2 pair + 1 of column c
-// of the g tile into the sub-tile-local cumsum lambda_r = sum_{s = 16J}^{r} g_s log2(e)
-// (rows past the chunk's end count as 0) and stores the sub-tile sums s_J.
+// Thread (c = t % 128, J = t / 128) turns sub-tile J of column c of the g tile into the
+// sub-tile-local cumsum lambda_r = sum_{s = 16J}^{r} g_s log2(e) (rows past the chunk's
+// end count as 0) and stores the sub-tile sum s_J.
 __device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, int BT)
 {
-    const int c = t & 127, pair = t >> 7;
+    const int c = t & 127, J = t >> 7;
+    float acc = 0.f;
 #pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-        const int J = 2 * pair + jj;
-        float acc = 0.f;
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            const int r = 16 * J + rr;
-            float* gp = reinterpret_cast<float*>(sm + OFF_G + g_off(r, c));
-            const float gv = (r < BT) ? *gp : 0.f;
-            acc = fmaf(gv, kLog2e, acc);
-            *gp = acc;
-        }
-        vec[(V_S + J) * 128 + c] = acc;
+    for (int rr = 0; rr < 16; ++rr) {
+        const int r = 16 * J + rr;
+        float* gp = reinterpret_cast<float*>(sm + OFF_G + g_off(r, c));
+        const float gv = (r < BT) ? *gp : 0.f;
+        acc = fmaf(gv, kLog2e, acc);
+        *gp = acc;
     }
+    vec[(V_S + J) * 128 + c] = acc;
 }
 
 // Per-channel factors from the sub-tile sums (thread c < 128, after phase1_cumsum).
@@ -296,25 +299,24 @@ __device__ __forceinline__ void phase1_factors(float* vec, int c)
 }
 
 // ---------------------------------------------------------------- phase 4: K~^T into TMEM
-// Lane c of the K~^T operand holds K~[r][c] = k[r][c] e^{Gamma_63 - Gamma_r} for the
-// 32 tokens r of this warp-group half, two tokens per column, as a bf16 hi + lo pair.
-__device__ __forceinline__ void phase4_ktilde(uint8_t* sm, const float* vec, uint32_t tm, int c, int half,
+// Lane c of the K~^T operand holds K~[r][c] = k[r][c] e^{Gamma_63 - Gamma_r} for the 16
+// tokens r of this thread's part, two tokens per column, as a bf16 hi + lo pair.
+__device__ __forceinline__ void phase4_ktilde(uint8_t* sm, const float* vec, uint32_t tm, int c, int part,
                                               int quarter, int BT)
 {
-    uint32_t hi[16], lo[16];
+    uint32_t hi[8], lo[8];
     const uint32_t kbase = smem_u32(sm + OFF_K);
+    const int J = part;   // the 16 tokens of part p are sub-tile p
     const float s1 = vec[(V_S + 1) * 128 + c], s2 = vec[(V_S + 2) * 128 + c], s3 = vec[(V_S + 3) * 128 + c];
-    const float tail0 = s1 + s2 + s3, tail1 = s2 + s3, tail2 = s3;
+    const float tailJ = (J == 0) ? s1 + s2 + s3 : ((J == 1) ? s2 + s3 : ((J == 2) ? s3 : 0.f));
+    const float sJ = vec[(V_S + J) * 128 + c];
 #pragma unroll
-    for (int pr = 0; pr < 16; ++pr) {
+    for (int pr = 0; pr < 8; ++pr) {
         float f2[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int r = 32 * half + 2 * pr + e;
-            const int J = r >> 4;
+            const int r = 16 * part + 2 * pr + e;
             const float lam = *reinterpret_cast<const float*>(sm + OFF_G + g_off(r, c));
-            const float sJ = vec[(V_S + J) * 128 + c];
-            const float tailJ = (J == 0) ? tail0 : ((J == 1) ? tail1 : ((J == 2) ? tail2 : 0.f));
             const float fac = ex2f((sJ - lam) + tailJ);
             unsigned short kb;
             asm volatile("ld.shared.u16 %0, [%1];" : "=h"(kb) : "r"(kbase + sw128_off(r, c, 64)));
@@ -323,17 +325,17 @@ __device__ __forceinline__ void phase4_ktilde(uint8_t* sm, const float* vec, uin
         }
         split_bf16x2(f2[0], f2[1], hi[pr], lo[pr]);
     }
-    tmem_st16u(tmem_addr(tm, 32 * quarter, TM_KT + 16 * half), hi);
-    tmem_st16u(tmem_addr(tm, 32 * quarter, TM_KTL + 16 * half), lo);
+    tmem_st8u(tmem_addr(tm, 32 * quarter, TM_KT + 8 * part), hi);
+    tmem_st8u(tmem_addr(tm, 32 * quarter, TM_KTL + 8 * part), lo);
 }
 
 // ---------------------------------------------------------------- phase 1b: token operands
-// Thread (lane L, half h): token r = L % 64 of the q rows (L >= 64) or k rows (L < 64),
-// channels [64h, 64h + 64).  Writes the tf32 row operand [K_r; Q_r] (TMEM).  The k-row
+// Thread (lane L, part p): token r = L % 64 of the q rows (L >= 64) or k rows (L < 64),
+// channels [32p, 32p + 32).  Writes the tf32 row operand [K_r; Q_r] (TMEM).  The k-row
 // thread also writes token r's diagonal-tile column operand and its K_Gamma B operand;
 // the q-row thread of the same token writes that token's column operands for the
 // references m > J (balancing the two halves).
-__device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uint32_t tm, int L, int half,
+__device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uint32_t tm, int L, int part,
                                               int quarter, int BT)
 {
     const int r = L & 63, J = r >> 4;
@@ -341,138 +343,108 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
     const bool valid = r < BT;
     const uint32_t sbase = smem_u32(sm);
     const uint32_t src = sbase + (isq ? OFF_Q : OFF_K);
-    uint32_t q2[32];
+    const uint32_t kc = sbase + OFF_X;
+    float kq[32];
 #pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-        float kq[32];
+    for (int gi = 0; gi < 4; ++gi) {
+        const int c0 = 32 * part + 8 * gi;
+        const uint4 raw = ld_shared_v4(src + sw128_chunk(r, c0 >> 3, 64));
+        const uint4 la = ld_shared_v4(sbase + OFF_G + g_off(r, c0));
+        const uint4 lb = ld_shared_v4(sbase + OFF_G + g_off(r, c0 + 4));
+        float xv[8], lam[8];
+        {
+            const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
+            xv[0] = a0.x; xv[1] = a0.y; xv[2] = a1.x; xv[3] = a1.y; xv[4] = a2.x; xv[5] = a2.y; xv[6] = a3.x; xv[7] = a3.y;
+            lam[0] = __uint_as_float(la.x); lam[1] = __uint_as_float(la.y); lam[2] = __uint_as_float(la.z);
+            lam[3] = __uint_as_float(la.w); lam[4] = __uint_as_float(lb.x); lam[5] = __uint_as_float(lb.y);
+            lam[6] = __uint_as_float(lb.z); lam[7] = __uint_as_float(lb.w);
+        }
+        float xr[8], vx[8];
 #pragma unroll
-        for (int gi = 0; gi < 4; ++gi) {
-            const int c0 = 64 * half + 32 * hb + 8 * gi;
-            const uint4 raw = ld_shared_v4(src + sw128_chunk(r, c0 >> 3, 64));
-            const uint4 la = ld_shared_v4(sbase + OFF_G + g_off(r, c0));
-            const uint4 lb = ld_shared_v4(sbase + OFF_G + g_off(r, c0 + 4));
-            float xv[8], lam[8];
-            {
-                const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
-                xv[0] = a0.x; xv[1] = a0.y; xv[2] = a1.x; xv[3] = a1.y; xv[4] = a2.x; xv[5] = a2.y; xv[6] = a3.x; xv[7] = a3.y;
-                lam[0] = __uint_as_float(la.x); lam[1] = __uint_as_float(la.y); lam[2] = __uint_as_float(la.z);
-                lam[3] = __uint_as_float(la.w); lam[4] = __uint_as_float(lb.x); lam[5] = __uint_as_float(lb.y);
-                lam[6] = __uint_as_float(lb.z); lam[7] = __uint_as_float(lb.w);
-            }
+        for (int e = 0; e < 8; ++e) {
+            const float v = valid ? xv[e] : 0.f;
+            const float x = ex2f(lam[e]);                        // e^{Gamma_r - rho_J} in (0, 1]
+            vx[e] = v * x;
+            kq[8 * gi + e] = tf32_round(vx[e]);
+            xr[e] = rcpf(x);                                     // e^{rho_J - Gamma_r} <= e^{80}
+            xv[e] = v;
+        }
+        if (!isq) {
+            // diagonal-tile column operand of reference J, and the K_Gamma B operand
             const float4 e4a = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
             const float4 e4b = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
-            const float ev[8] = {e4a.x, e4a.y, e4a.z, e4a.w, e4b.x, e4b.y, e4b.z, e4b.w};
-            float gam[8], xr[8];
+            const uint32_t rj = kc_row(J) + r;
+            st_shared_f4(kc + sw128_off_f32(rj, c0, KC_ROWS), tf32_round(xv[0] * xr[0]), tf32_round(xv[1] * xr[1]),
+                         tf32_round(xv[2] * xr[2]), tf32_round(xv[3] * xr[3]));
+            st_shared_f4(kc + sw128_off_f32(rj, c0 + 4, KC_ROWS), tf32_round(xv[4] * xr[4]),
+                         tf32_round(xv[5] * xr[5]), tf32_round(xv[6] * xr[6]), tf32_round(xv[7] * xr[7]));
+            st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), pack_bf16x2(vx[0] * e4a.x, vx[1] * e4a.y),
+                         pack_bf16x2(vx[2] * e4a.z, vx[3] * e4a.w), pack_bf16x2(vx[4] * e4b.x, vx[5] * e4b.y),
+                         pack_bf16x2(vx[6] * e4b.z, vx[7] * e4b.w));
+        } else if (J < 3) {
+            // this token's k, for the column operands of references m > J:
+            // k e^{rho_{J+1} - Gamma_r} e^{rho_m - rho_{J+1}}
+            const uint4 kraw = ld_shared_v4(sbase + OFF_K + sw128_chunk(r, c0 >> 3, 64));
+            const float2 k0 = bf2_to_f2(kraw.x), k1 = bf2_to_f2(kraw.y), k2 = bf2_to_f2(kraw.z), k3 = bf2_to_f2(kraw.w);
+            const float kvv[8] = {k0.x, k0.y, k1.x, k1.y, k2.x, k2.y, k3.x, k3.y};
+            const float4 d4a = *reinterpret_cast<const float4*>(vec + (V_D + J) * 128 + c0);
+            const float4 d4b = *reinterpret_cast<const float4*>(vec + (V_D + J) * 128 + c0 + 4);
+            const float dv[8] = {d4a.x, d4a.y, d4a.z, d4a.w, d4b.x, d4b.y, d4b.z, d4b.w};
+            float ky[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float v = valid ? xv[e] : 0.f;
-                const float x = ex2f(lam[e]);                        // e^{Gamma_r - rho_J} in (0, 1]
-                const float vx = v * x;
-                kq[8 * gi + e] = tf32_round(vx);
-                gam[e] = vx * ev[e];                                 // v e^{Gamma_r}
-                xr[e] = rcpf(x);                                     // e^{rho_J - Gamma_r} <= e^{80}
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) q2[16 * hb + 4 * gi + e] = pack_bf16x2(gam[2 * e], gam[2 * e + 1]);
-            const uint32_t kc = sbase + OFF_X;
-            if (!isq) {
-                // diagonal-tile column operand of reference J, and the K_Gamma B operand
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xv[e] = (valid ? xv[e] : 0.f) * xr[e];
-                const uint32_t rj = kc_row(J) + r;
-                st_shared_f4(kc + sw128_off_f32(rj, c0, KC_ROWS), tf32_round(xv[0]), tf32_round(xv[1]),
-                             tf32_round(xv[2]), tf32_round(xv[3]));
-                st_shared_f4(kc + sw128_off_f32(rj, c0 + 4, KC_ROWS), tf32_round(xv[4]), tf32_round(xv[5]),
-                             tf32_round(xv[6]), tf32_round(xv[7]));
-                st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), q2[16 * hb + 4 * gi],
-                             q2[16 * hb + 4 * gi + 1], q2[16 * hb + 4 * gi + 2], q2[16 * hb + 4 * gi + 3]);
-            } else if (J < 3) {
-                // this token's k, for the column operands of references m > J:
-                // k e^{rho_{J+1} - Gamma_r} e^{rho_m - rho_{J+1}}
-                const uint4 kraw = ld_shared_v4(sbase + OFF_K + sw128_chunk(r, c0 >> 3, 64));
-                const float2 k0 = bf2_to_f2(kraw.x), k1 = bf2_to_f2(kraw.y), k2 = bf2_to_f2(kraw.z),
-                             k3 = bf2_to_f2(kraw.w);
-                const float kvv[8] = {k0.x, k0.y, k1.x, k1.y, k2.x, k2.y, k3.x, k3.y};
-                const float4 d4a = *reinterpret_cast<const float4*>(vec + (V_D + J) * 128 + c0);
-                const float4 d4b = *reinterpret_cast<const float4*>(vec + (V_D + J) * 128 + c0 + 4);
-                const float dv[8] = {d4a.x, d4a.y, d4a.z, d4a.w, d4b.x, d4b.y, d4b.z, d4b.w};
-                float ky[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ky[e] = (valid ? kvv[e] : 0.f) * xr[e] * dv[e];
-                for (int m = J + 1; m < 4; ++m) {
-                    const float4 f4a = *reinterpret_cast<const float4*>(vec + (V_F + f_index(m, J)) * 128 + c0);
-                    const float4 f4b = *reinterpret_cast<const float4*>(vec + (V_F + f_index(m, J)) * 128 + c0 + 4);
-                    const uint32_t rm = kc_row(m) + r;
-                    st_shared_f4(kc + sw128_off_f32(rm, c0, KC_ROWS), tf32_round(ky[0] * f4a.x),
-                                 tf32_round(ky[1] * f4a.y), tf32_round(ky[2] * f4a.z), tf32_round(ky[3] * f4a.w));
-                    st_shared_f4(kc + sw128_off_f32(rm, c0 + 4, KC_ROWS), tf32_round(ky[4] * f4b.x),
-                                 tf32_round(ky[5] * f4b.y), tf32_round(ky[6] * f4b.z), tf32_round(ky[7] * f4b.w));
-                }
+            for (int e = 0; e < 8; ++e) ky[e] = (valid ? kvv[e] : 0.f) * xr[e] * dv[e];
+            for (int m = J + 1; m < 4; ++m) {
+                const float4 f4a = *reinterpret_cast<const float4*>(vec + (V_F + f_index(m, J)) * 128 + c0);
+                const float4 f4b = *reinterpret_cast<const float4*>(vec + (V_F + f_index(m, J)) * 128 + c0 + 4);
+                const uint32_t rm = kc_row(m) + r;
+                st_shared_f4(kc + sw128_off_f32(rm, c0, KC_ROWS), tf32_round(ky[0] * f4a.x),
+                             tf32_round(ky[1] * f4a.y), tf32_round(ky[2] * f4a.z), tf32_round(ky[3] * f4a.w));
+                st_shared_f4(kc + sw128_off_f32(rm, c0 + 4, KC_ROWS), tf32_round(ky[4] * f4b.x),
+                             tf32_round(ky[5] * f4b.y), tf32_round(ky[6] * f4b.z), tf32_round(ky[7] * f4b.w));
             }
         }
-        tmem_st32(tmem_addr(tm, 32 * quarter, TM_KQ + 64 * half + 32 * hb), kq);
     }
+    tmem_st32(tmem_addr(tm, 32 * quarter, TM_KQ + 32 * part), kq);
 }
 
 // ---------------------------------------------------------------- phase 3: A/P read-out
-// Warp-group 0, lane L: row r = L % 64 of A (L < 64: scaled by beta_r, strictly
-// lower) into shared memory in fp32, or of P (L >= 64: lower with diagonal) into
-// TMEM as bf16 hi + lo pairs (the A operand of M = P Tb; lanes 0-63 get zeros).
-__device__ __forceinline__ void phase3_readout(uint8_t* sm, uint32_t tm, int L, int quarter, const float* sbeta)
+// Lane L, part p: columns [16p, 16p + 16) of row r = L % 64 of A (L < 64: scaled by
+// beta_r, strictly lower) into shared memory in fp32, or of P (L >= 64: lower with
+// diagonal) into TMEM as bf16 hi + lo pairs (the A operand of M = P Tb; lanes 0-63
+// get zeros).
+__device__ __forceinline__ void phase3_readout(uint8_t* sm, uint32_t tm, int L, int quarter, int part,
+                                               const float* sbeta)
 {
     const int r = L & 63, J = r >> 4;
     const bool isP = L >= 64;
-    float row[64];
     const uint32_t lane0 = 32 * quarter;
-    if ((quarter & 1) == 0) {   // rows of sub-tiles 0 and 1
-        float a0[16], a1[32];
-        tmem_ld16(tmem_addr(tm, lane0, tm_ap(0)), a0);
-        tmem_ld32(tmem_addr(tm, lane0, tm_ap(1)), a1);
-        tmem_wait_ld();
+    const int j0 = 2 * (quarter & 1);   // the two sub-tiles of this warp's rows: j0, j0 + 1
+    float va[16], vb[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) row[i] = (J == 0) ? a0[i] : a1[i];
+    for (int i = 0; i < 16; ++i) va[i] = vb[i] = 0.f;
+    if (part <= j0) tmem_ld16(tmem_addr(tm, lane0, tm_ap(j0) + 16 * part), va);
+    if (part <= j0 + 1) tmem_ld16(tmem_addr(tm, lane0, tm_ap(j0 + 1) + 16 * part), vb);
+    tmem_wait_ld();
+    float row[16];
 #pragma unroll
-        for (int i = 16; i < 32; ++i) row[i] = (J == 1) ? a1[i] : 0.f;
-#pragma unroll
-        for (int i = 32; i < 64; ++i) row[i] = 0.f;
-    } else {                    // rows of sub-tiles 2 and 3
-        float b0[32], b1[32];
-        tmem_ld32(tmem_addr(tm, lane0, tm_ap(3)), b0);
-        tmem_ld32(tmem_addr(tm, lane0, tm_ap(3) + 32), b1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            row[i] = b0[i];
-            row[32 + i] = b1[i];
-        }
-        float c0[32], c1[16];
-        tmem_ld32(tmem_addr(tm, lane0, tm_ap(2)), c0);
-        tmem_ld16(tmem_addr(tm, lane0, tm_ap(2) + 32), c1);
-        tmem_wait_ld();
-        if (J == 2) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) row[i] = c0[i];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) row[32 + i] = c1[i];
-#pragma unroll
-            for (int i = 48; i < 64; ++i) row[i] = 0.f;
-        }
-    }
-    uint32_t hi[32], lo[32];
+    for (int i = 0; i < 16; ++i) row[i] = (part <= J) ? ((J == j0) ? va[i] : vb[i]) : 0.f;
+    uint32_t hi[8], lo[8];
     if (!isP) {
         float* sA = reinterpret_cast<float*>(sm + OFF_X + X_SA);
         const float b = sbeta[r];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) sA[r * LDA + i] = (i < r) ? b * row[i] : 0.f;
+        for (int i = 0; i < 16; ++i) sA[r * LDA + 16 * part + i] = (16 * part + i < r) ? b * row[i] : 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) hi[i] = lo[i] = 0u;
+        for (int i = 0; i < 8; ++i) hi[i] = lo[i] = 0u;
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            split_bf16x2((2 * i <= r) ? row[2 * i] : 0.f, (2 * i + 1 <= r) ? row[2 * i + 1] : 0.f, hi[i], lo[i]);
+        for (int i = 0; i < 8; ++i) {
+            const int c = 16 * part + 2 * i;
+            split_bf16x2((c <= r) ? row[2 * i] : 0.f, (c + 1 <= r) ? row[2 * i + 1] : 0.f, hi[i], lo[i]);
+        }
     }
-    tmem_st32u(tmem_addr(tm, lane0, TM_PH), hi);
-    tmem_st32u(tmem_addr(tm, lane0, TM_PL), lo);
+    tmem_st8u(tmem_addr(tm, lane0, TM_PH + 8 * part), hi);
+    tmem_st8u(tmem_addr(tm, lane0, TM_PL + 8 * part), lo);
 }
 
 // ---------------------------------------------------------------- phase 3: T = (I + A)^-1
@@ -557,81 +529,77 @@ __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
     solve_level<3>(sA, sT, sY, t);
 }
 
-// Tb = T diag(beta) as bf16 hi + lo MN-major B operands [64 i][64 j] (all 256 threads).
+// Tb = T diag(beta) as bf16 hi + lo MN-major B operands [64 i][64 j] (512 threads,
+// one 8-column chunk each).
 __device__ __forceinline__ void phase3_tb_operands(uint8_t* sm, int t, const float* sbeta)
 {
     const float* sT = reinterpret_cast<const float*>(sm + OFF_X + X_ST);
     const uint32_t sbase = smem_u32(sm);
+    const int i = t >> 3, ch = t & 7;   // row i, 8-column chunk ch
+    uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int idx = t + 256 * u, i = idx >> 3, ch = idx & 7;   // row i, 8-column chunk ch
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int j = 8 * ch + 2 * e;
-            split_bf16x2(sT[i * LDA + j] * sbeta[j], sT[i * LDA + j + 1] * sbeta[j + 1], hi[e], lo[e]);
-        }
-        st_shared_v4(sbase + OFF_X + X_TBH + sw128_chunk(i, ch, 64), hi[0], hi[1], hi[2], hi[3]);
-        st_shared_v4(sbase + OFF_X + X_TBL + sw128_chunk(i, ch, 64), lo[0], lo[1], lo[2], lo[3]);
+    for (int e = 0; e < 4; ++e) {
+        const int j = 8 * ch + 2 * e;
+        split_bf16x2(sT[i * LDA + j] * sbeta[j], sT[i * LDA + j + 1] * sbeta[j + 1], hi[e], lo[e]);
     }
+    st_shared_v4(sbase + OFF_X + X_TBH + sw128_chunk(i, ch, 64), hi[0], hi[1], hi[2], hi[3]);
+    st_shared_v4(sbase + OFF_X + X_TBL + sw128_chunk(i, ch, 64), lo[0], lo[1], lo[2], lo[3]);
 }
 
-// 64 fp32 values of a row -> bf16 rows of an MN-major B-operand tile (row `row`,
-// value columns [64 half, 64 half + 64), `rows` rows per 64-column block).
-__device__ __forceinline__ void store_row_bf16(uint32_t tile, int row, int half, int rows, const uint32_t (&pk)[32])
+// 32 values of a row (as 16 packed bf16 pairs) -> chunks [4 chunk0, 4 chunk0 + 4) of row
+// `row` of a 128-byte-swizzled bf16 tile with `rows` rows per 64-column block.
+__device__ __forceinline__ void store_row32_bf16(uint32_t tile, int row, int chunk0, int rows, const uint32_t (&pk)[16])
 {
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-        st_shared_v4(tile + sw128_chunk(row, 8 * half + q, rows), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+    for (int q = 0; q < 4; ++q)
+        st_shared_v4(tile + sw128_chunk(row, chunk0 + q, rows), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
                      pk[4 * q + 3]);
 }
 
-// Q' row = Q_Gamma - M K_Gamma for token r = L - 64 (lanes 64-127), channels [64h, 64h + 64):
+// Q' row = Q_Gamma - M K_Gamma for token r = L - 64 (lanes 64-127), channels [32p, 32p + 32):
 // Q_Gamma is recomputed in fp32 from the q and cumsum tiles so that the one bf16 rounding
 // happens after the (strongly cancelling) subtraction.
-__device__ __forceinline__ void phase4_qprime(uint8_t* sm, const float* vec, uint32_t tm, int L, int half,
+__device__ __forceinline__ void phase4_qprime(uint8_t* sm, const float* vec, uint32_t tm, int L, int part,
                                               int quarter, int BT)
 {
     const int r = L - 64, J = r >> 4;
     const bool valid = r < BT;
     const uint32_t sbase = smem_u32(sm);
-    uint32_t pk[32];
+    float mk[32];
+    tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 32 * part), mk);
+    tmem_wait_ld();
+    uint32_t pk[16];
 #pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-        float mk[32];
-        tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 64 * half + 32 * hb), mk);
-        tmem_wait_ld();
+    for (int gi = 0; gi < 4; ++gi) {
+        const int c0 = 32 * part + 8 * gi;
+        const uint4 raw = ld_shared_v4(sbase + OFF_Q + sw128_chunk(r, c0 >> 3, 64));
+        const uint4 la = ld_shared_v4(sbase + OFF_G + g_off(r, c0));
+        const uint4 lb = ld_shared_v4(sbase + OFF_G + g_off(r, c0 + 4));
+        const float4 e4a = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
+        const float4 e4b = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
+        const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
+        const float qv[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
+        const float lam[8] = {__uint_as_float(la.x), __uint_as_float(la.y), __uint_as_float(la.z),
+                              __uint_as_float(la.w), __uint_as_float(lb.x), __uint_as_float(lb.y),
+                              __uint_as_float(lb.z), __uint_as_float(lb.w)};
+        const float ev[8] = {e4a.x, e4a.y, e4a.z, e4a.w, e4b.x, e4b.y, e4b.z, e4b.w};
+        float qp[8];
 #pragma unroll
-        for (int gi = 0; gi < 4; ++gi) {
-            const int c0 = 64 * half + 32 * hb + 8 * gi;
-            const uint4 raw = ld_shared_v4(sbase + OFF_Q + sw128_chunk(r, c0 >> 3, 64));
-            const uint4 la = ld_shared_v4(sbase + OFF_G + g_off(r, c0));
-            const uint4 lb = ld_shared_v4(sbase + OFF_G + g_off(r, c0 + 4));
-            const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
-            const float qv[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
-            const float lam[8] = {__uint_as_float(la.x), __uint_as_float(la.y), __uint_as_float(la.z),
-                                  __uint_as_float(la.w), __uint_as_float(lb.x), __uint_as_float(lb.y),
-                                  __uint_as_float(lb.z), __uint_as_float(lb.w)};
-            float qp[8];
+        for (int e = 0; e < 8; ++e) qp[e] = (valid ? qv[e] * ex2f(lam[e]) * ev[e] : 0.f) - mk[8 * gi + e];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float qg = valid ? qv[e] * ex2f(lam[e]) * vec[(V_E + J) * 128 + c0 + e] : 0.f;
-                qp[e] = qg - mk[8 * gi + e];
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) pk[16 * hb + 4 * gi + e] = pack_bf16x2(qp[2 * e], qp[2 * e + 1]);
-        }
+        for (int e = 0; e < 4; ++e) pk[4 * gi + e] = pack_bf16x2(qp[2 * e], qp[2 * e + 1]);
     }
-    tmem_st32u(tmem_addr(tm, 32 * quarter, TM_A1 + 32 * half), pk);
+    tmem_st16u(tmem_addr(tm, 32 * quarter, TM_A1 + 16 * part), pk);
 }
 
 // ---------------------------------------------------------------- the kernel
+// 16 warps: warp w reaches TMEM lanes [32 (w % 4), +32) and works on column part w / 4.
 __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3, part = warp >> 2;
     const int L = 32 * quarter + lane;   // the TMEM lane this thread may access
     float* vec = reinterpret_cast<float*>(sm + OFF_VEC);
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
@@ -677,13 +645,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         v_pending = qkg_pending = true;
     }
 
-    // initial state -> TMEM: lane L = key channel, columns [64 half, 64 half + 64)
-#pragma unroll
-    for (int cb = 0; cb < 2; ++cb) {
-        const int col = 64 * half + 32 * cb;
+    // initial state -> TMEM: lane L = key channel, columns [32 part, 32 part + 32)
+    {
         float v[32];
         if (p.init_state) {
-            const float4* src = reinterpret_cast<const float4*>(p.init_state + sbase_g + (size_t)L * 128 + col);
+            const float4* src = reinterpret_cast<const float4*>(p.init_state + sbase_g + (size_t)L * 128 + 32 * part);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const float4 f = __ldg(src + i);
@@ -693,9 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
-        tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + col), v);
+        tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), v);
+        tmem_wait_st();
     }
-    tmem_wait_st();
 
     float beta_next = (t < 64 && bos + t < eos) ? __ldg(p.beta + (size_t)(bos + t) * H + h) : 0.f;
     uint32_t v_par = 0, qkg_par = 0, mma_par = 0;
@@ -727,41 +693,38 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         __syncthreads();
         if (t < 128) phase1_factors(vec, t);
         __syncthreads();
-        phase1_tokens(sm, vec, tm, L, half, quarter, BT);
+        phase1_tokens(sm, vec, tm, L, part, quarter, BT);
         fence_proxy_async_smem();
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
 
-        // ---- next chunk's loads, then phase 2: A and P by tf32 MMAs
+        // ---- next chunk's v, then phase 2: A and P by one tf32 MMA
         if (t == 0) {
             tc_fence_after_sync();
             if (ci + 1 < nchunks) {
                 issue_v_loads(p, sm, bar_v, (ci + 1) & 1, t0 + 64, h);
                 v_pending = true;
             }
-            {   // all four references at once: N = 160 columns, reference m in columns [8m(m+1), 8(m+1)(m+2))
-                const uint32_t idesc = idesc_tf32_f32(128, KC_ROWS);
-                const uint32_t kc = sbase + OFF_X;
+            // all four references at once: N = 160 columns, reference m in columns [8m(m+1), 8(m+1)(m+2))
+            const uint32_t idesc = idesc_tf32_f32(128, KC_ROWS);
+            const uint32_t kc = sbase + OFF_X;
 #pragma unroll
-                for (int ks = 0; ks < 16; ++ks)
-                    umma_tf32_tmem_a(tm + TM_AP, tm + TM_KQ + 8 * ks, desc_kmajor(kc, KC_ROWS, ks), idesc,
-                                     ks > 0 ? 1u : 0u);
-            }
+            for (int ks = 0; ks < 16; ++ks)
+                umma_tf32_tmem_a(tm + TM_AP, tm + TM_KQ + 8 * ks, desc_kmajor(kc, KC_ROWS, ks), idesc,
+                                 ks > 0 ? 1u : 0u);
             umma_commit(bar_mma);
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
 
-        // ---- phase 3: A/P read-out (warp-group 0) while warp-group 1 clears T; solve;
-        //      M = P Tb by MMA; [Tb; M] hi/lo rows into TMEM
-        if (t < 128) {
-            phase3_readout(sm, tm, L, quarter, sbeta);
-        } else {
+        // ---- phase 3: clear T; A/P read-out; solve; M = P Tb by MMA; [Tb; M] hi/lo into TMEM
+        {
             float* sT = reinterpret_cast<float*>(sm + OFF_X + X_ST);
-            for (int idx = t - 128; idx < 64 * LDA; idx += 128) sT[idx] = 0.f;
+            for (int idx = t; idx < 64 * LDA; idx += kThreads) sT[idx] = 0.f;
         }
+        phase3_readout(sm, tm, L, quarter, part, sbeta);
         tmem_wait_st();
         __syncthreads();
         phase3_solve(sm, t);
@@ -784,40 +747,36 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 umma_bf16_tmem_a(tm + TM_M, tm + TM_PL + 8 * ks, desc_mnmajor(tbh, 64, ks), idesc, 1u);
             umma_commit(bar_mma);
         }
-        if (t < 64) {   // Tb rows (lanes 0-63) straight from the hi/lo B-operand tiles
-            uint32_t hi[32], lo[32];
+        if (quarter < 2) {   // Tb rows (lanes 0-63), columns [16 part, +16), from the hi/lo B-operand tiles
+            uint32_t hi[8], lo[8];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const uint4 h4 = ld_shared_v4(sbase + OFF_X + X_TBH + sw128_chunk(t, ch, 64));
-                const uint4 l4 = ld_shared_v4(sbase + OFF_X + X_TBL + sw128_chunk(t, ch, 64));
-                hi[4 * ch] = h4.x; hi[4 * ch + 1] = h4.y; hi[4 * ch + 2] = h4.z; hi[4 * ch + 3] = h4.w;
-                lo[4 * ch] = l4.x; lo[4 * ch + 1] = l4.y; lo[4 * ch + 2] = l4.z; lo[4 * ch + 3] = l4.w;
+            for (int cc = 0; cc < 2; ++cc) {
+                const uint4 h4 = ld_shared_v4(sbase + OFF_X + X_TBH + sw128_chunk(L, 2 * part + cc, 64));
+                const uint4 l4 = ld_shared_v4(sbase + OFF_X + X_TBL + sw128_chunk(L, 2 * part + cc, 64));
+                hi[4 * cc] = h4.x; hi[4 * cc + 1] = h4.y; hi[4 * cc + 2] = h4.z; hi[4 * cc + 3] = h4.w;
+                lo[4 * cc] = l4.x; lo[4 * cc + 1] = l4.y; lo[4 * cc + 2] = l4.z; lo[4 * cc + 3] = l4.w;
             }
-            tmem_st32u(tmem_addr(tm, 32 * quarter, TM_TPH), hi);
-            tmem_st32u(tmem_addr(tm, 32 * quarter, TM_TPL), lo);
+            tmem_st8u(tmem_addr(tm, 32 * quarter, TM_TPH + 8 * part), hi);
+            tmem_st8u(tmem_addr(tm, 32 * quarter, TM_TPL + 8 * part), lo);
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        if (t >= 64 && t < 128) {   // M rows (lanes 64-127) -> hi/lo
-            float a[32], b[32];
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_M), a);
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_M + 32), b);
+        if (quarter >= 2) {   // M rows (lanes 64-127), columns [16 part, +16) -> hi/lo
+            float a[16];
+            tmem_ld16(tmem_addr(tm, 32 * quarter, TM_M + 16 * part), a);
             tmem_wait_ld();
-            uint32_t hi[32], lo[32];
+            uint32_t hi[8], lo[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
-                split_bf16x2(b[2 * i], b[2 * i + 1], hi[16 + i], lo[16 + i]);
-            }
-            tmem_st32u(tmem_addr(tm, 32 * quarter, TM_TPH), hi);
-            tmem_st32u(tmem_addr(tm, 32 * quarter, TM_TPL), lo);
+            for (int i = 0; i < 8; ++i) split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
+            tmem_st8u(tmem_addr(tm, 32 * quarter, TM_TPH + 8 * part), hi);
+            tmem_st8u(tmem_addr(tm, 32 * quarter, TM_TPL + 8 * part), lo);
         }
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
 
-        // ---- phase 4: D2 = [Tb; M] K_Gamma (hi + lo), then A1 = [-Wk; Q_Gamma - M K_Gamma]
+        // ---- phase 4: D2 = [Tb; M] K_Gamma (hi + lo) while K~^T is built, then A1 = [-Wk; Q']
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
@@ -830,24 +789,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPL + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
             umma_commit(bar_mma);
         }
-        phase4_ktilde(sm, vec, tm, L, half, quarter, BT);   // overlaps the MMA above
+        phase4_ktilde(sm, vec, tm, L, part, quarter, BT);   // overlaps the MMA above
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        if (quarter < 2) {   // rows 0-63: -Wk
-            float a[32], b[32];
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 64 * half), a);
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 64 * half + 32), b);
+        if (quarter < 2) {   // rows 0-63: -Wk, columns [32 part, +32)
+            float a[32];
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 32 * part), a);
             tmem_wait_ld();
-            uint32_t pk[32];
+            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
-                pk[16 + i] = pack_bf16x2(-b[2 * i], -b[2 * i + 1]);
-            }
-            tmem_st32u(tmem_addr(tm, 32 * quarter, TM_A1 + 32 * half), pk);
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
+            tmem_st16u(tmem_addr(tm, 32 * quarter, TM_A1 + 16 * part), pk);
         } else {             // rows 64-127: Q' = Q_Gamma - M K_Gamma
-            phase4_qprime(sm, vec, tm, L, half, quarter, BT);
+            phase4_qprime(sm, vec, tm, L, part, quarter, BT);
         }
         tmem_wait_st();
         tc_fence_before_sync();
@@ -860,25 +815,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
 
         // ---- phase 5a: S -> bf16 B operand; S <- Diag(gamma_C) S in place
         {
-            float a[32], b[32];
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 64 * half), a);
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 64 * half + 32), b);
+            float a[32];
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), a);
             tmem_wait_ld();
-            uint32_t pk[32];
+            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                pk[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
-                pk[16 + i] = pack_bf16x2(b[2 * i], b[2 * i + 1]);
-            }
-            store_row_bf16(sbase + OFF_X + X_SB, L, half, 128, pk);
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+            store_row32_bf16(sbase + OFF_X + X_SB, L, 4 * part, 128, pk);
             const float gc = vec[V_GC * 128 + L];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                a[i] *= gc;
-                b[i] *= gc;
-            }
-            tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + 64 * half), a);
-            tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + 64 * half + 32), b);
+            for (int i = 0; i < 32; ++i) a[i] *= gc;
+            tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), a);
             tmem_wait_st();
         }
         fence_proxy_async_smem();
@@ -908,24 +855,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
 
         // ---- phase 5c: rows 0-63 -> W (hi + lo) B operands
         if (quarter < 2) {
-            float a[32], b[32];
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half), a);
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half + 32), b);
+            float a[32];
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 32 * part), a);
             tmem_wait_ld();
-            uint32_t hi[32], lo[32];
+            uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
-                split_bf16x2(b[2 * i], b[2 * i + 1], hi[16 + i], lo[16 + i]);
-            }
-            store_row_bf16(sbase + OFF_X + X_WH, L, half, 64, hi);
-            store_row_bf16(sbase + OFF_X + X_WL, L, half, 64, lo);
+            for (int i = 0; i < 16; ++i) split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
+            store_row32_bf16(sbase + OFF_X + X_WH, L, 4 * part, 64, hi);
+            store_row32_bf16(sbase + OFF_X + X_WL, L, 4 * part, 64, lo);
             fence_proxy_async_smem();
         }
         tc_fence_before_sync();
         __syncthreads();
 
-        // ---- phase 5d: S += K~^T W (hi hi + hi lo + lo hi), while rows 64-127 (O) go to HBM
+        // ---- phase 5d: S += K~^T W (hi hi + hi lo + lo hi), while rows 64-127 (O) go out
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
@@ -946,29 +889,22 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (quarter >= 2) {
             tc_fence_after_sync();
             const int r = L - 64;
-            float a[32], b[32];
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half), a);
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 64 * half + 32), b);
+            float a[32];
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 32 * part), a);
             tmem_wait_ld();
             if (BT == 64) {
-                // stage in 128-byte-swizzled [64 tok][32] fp32 boxes for one TMA store per box:
-                // columns 0-63 in the free top of the X region, 64-127 in this chunk's v buffer
-                const uint32_t box0 = half ? sbase + ((ci & 1) ? OFF_V1 : OFF_V0) : sbase + OFF_X + X_OST;
+                // stage in 128-byte-swizzled [64 tok][32] fp32 boxes, one TMA store per box:
+                // boxes 0-1 in the free top of the X region, 2-3 in this chunk's v buffer
+                const uint32_t box = (part < 2) ? sbase + OFF_X + X_OST + 8192 * part
+                                                : sbase + ((ci & 1) ? OFF_V1 : OFF_V0) + 8192 * (part - 2);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    st_shared_f4(box0 + sw128_off_f32(r, 4 * q, 64), a[4 * q], a[4 * q + 1], a[4 * q + 2],
-                                 a[4 * q + 3]);
-                    st_shared_f4(box0 + 8192 + sw128_off_f32(r, 4 * q, 64), b[4 * q], b[4 * q + 1], b[4 * q + 2],
-                                 b[4 * q + 3]);
-                }
+                for (int q = 0; q < 8; ++q)
+                    st_shared_f4(box + sw128_off_f32(r, 4 * q, 64), a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
                 fence_proxy_async_smem();
             } else if (r < BT) {
-                float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)(t0 + r) * H + h) * 128 + 64 * half);
+                float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)(t0 + r) * H + h) * 128 + 32 * part);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
-                    dst[8 + i] = make_float4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
-                }
+                for (int i = 0; i < 8; ++i) dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
             }
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
@@ -989,16 +925,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     __syncthreads();
     tc_fence_after_sync();
     if (ok && p.final_state) {
+        float v[32];
+        tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), v);
+        tmem_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(p.final_state + sbase_g + (size_t)L * 128 + 32 * part);
 #pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {
-            const int col = 64 * half + 32 * cb;
-            float v[32];
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + col), v);
-            tmem_wait_ld();
-            float4* dst = reinterpret_cast<float4*>(p.final_state + sbase_g + (size_t)L * 128 + col);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        }
+        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     }
     if (!ok && t == 0) {
         // a wait gave up: record it, let in-flight copies and MMAs land (bounded), then leave
