@@ -28,9 +28,11 @@
 //   1  g cumsum per channel; decayed operands to TMEM (A operands) and shared
 //      memory (B operands); TMA prefetch of the next chunk's v.
 //   2  A and P by one tf32 MMA over the four sub-tile references side by side.
-//   3  T = (I + A)^-1 in fp32 on CUDA cores; M = P Tb by three bf16 MMAs (hi/lo splits).
-//   4  [Wk; M K_Gamma] by MMA while K~^T is built, then the [-Wk; Q'] operand;
-//      TMA prefetch of the next chunk's q, k and g.
+//   3  T = (I + A)^-1 in fp32 on CUDA cores (6 warps) while the other warps build K~^T
+//      and the state's bf16 B operand and apply the chunk decay to S; M = P Tb by
+//      three bf16 MMAs (hi/lo splits).
+//   4  [Wk; M K_Gamma] by MMA, then the [-Wk; Q'] operand; TMA prefetch of the next
+//      chunk's q, k and g.
 //   5  D1 = [Tb; M] V + [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O;
 //      W to shared memory; S += K~^T W by MMA while O is staged in shared memory and
 //      written by TMA bulk stores (direct stores for a sequence's ragged last chunk).
@@ -64,10 +66,11 @@ constexpr uint32_t X_TBH = 0;          // Tb hi, MN-major B [64 i][64 j] bf16 (8
 constexpr uint32_t X_TBL = 8192;       // Tb lo
 constexpr uint32_t X_ST = 17408;       // T fp32 [64][68]
 constexpr uint32_t X_SY = 34816;       // level scratch fp32 [3][16][20]
-constexpr uint32_t X_OST = 65536;      // O staging, dv columns 0-63: 2 x [64 tok][32] fp32 boxes (phase 5)
-constexpr uint32_t X_SB = 0;           // S bf16, MN-major B [128 dk][128 dv]
-constexpr uint32_t X_WH = 32768;       // W hi bf16, MN-major B [64 tok][128 dv]
-constexpr uint32_t X_WL = 49152;       // W lo
+constexpr uint32_t X_OST = 65536;      // O staging, dv columns 0-63: 2 x [64 tok][32] fp32 boxes (phase 5,
+                                       // after the MMA that reads S bf16 has completed)
+constexpr uint32_t X_SB = 40960;       // S bf16, MN-major B [128 dk][128 dv] (written during the solve)
+constexpr uint32_t X_WH = 0;           // W hi bf16, MN-major B [64 tok][128 dv] (phase 5)
+constexpr uint32_t X_WL = 16384;       // W lo
 constexpr uint32_t OFF_KG = 180224;    // K_Gamma bf16, MN-major B [64 tok][128 ch]
 constexpr uint32_t OFF_VEC = 196608;   // per-channel vectors [23][128] fp32
 constexpr uint32_t OFF_BETA = OFF_VEC + 23 * 512;
@@ -223,6 +226,13 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
     lo = pack_bf16x2(a - ah, b - bh);
 }
 
+// Barrier over the first `n` threads of the CTA (named barrier `id`, n a multiple of 32).
+__device__ __forceinline__ void named_sync(int id, int n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+constexpr int kSolveThreads = 192;   // warps 0-5 run the solve
+
 // Every thread waits on `bar` (bounded); returns false for all threads if any gave up.
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* s_abort)
 {
@@ -298,26 +308,25 @@ __device__ __forceinline__ void phase1_factors(float* vec, int c)
     vec[V_GC * 128 + c] = ex2f(lam63);
 }
 
-// ---------------------------------------------------------------- phase 4: K~^T into TMEM
-// Lane c of the K~^T operand holds K~[r][c] = k[r][c] e^{Gamma_63 - Gamma_r} for the 16
-// tokens r of this thread's part, two tokens per column, as a bf16 hi + lo pair.
-__device__ __forceinline__ void phase4_ktilde(uint8_t* sm, const float* vec, uint32_t tm, int c, int part,
-                                              int quarter, int BT)
+// ---------------------------------------------------------------- phase 3 side work: K~^T into TMEM
+// Lane c of the K~^T operand holds K~[r][c] = k[r][c] e^{Gamma_63 - Gamma_r}, two tokens
+// per column, as a bf16 hi + lo pair; this thread covers tokens [32 hh, 32 hh + 32).
+__device__ __forceinline__ void build_ktilde(uint8_t* sm, const float* vec, uint32_t tm, int c, int hh, int quarter,
+                                             int BT)
 {
-    uint32_t hi[8], lo[8];
+    uint32_t hi[16], lo[16];
     const uint32_t kbase = smem_u32(sm + OFF_K);
-    const int J = part;   // the 16 tokens of part p are sub-tile p
     const float s1 = vec[(V_S + 1) * 128 + c], s2 = vec[(V_S + 2) * 128 + c], s3 = vec[(V_S + 3) * 128 + c];
-    const float tailJ = (J == 0) ? s1 + s2 + s3 : ((J == 1) ? s2 + s3 : ((J == 2) ? s3 : 0.f));
-    const float sJ = vec[(V_S + J) * 128 + c];
+    const float tails[2] = {hh ? s3 : s1 + s2 + s3, hh ? 0.f : s2 + s3};   // sub-tiles 2 hh, 2 hh + 1
+    const float sJs[2] = {vec[(V_S + 2 * hh) * 128 + c], vec[(V_S + 2 * hh + 1) * 128 + c]};
 #pragma unroll
-    for (int pr = 0; pr < 8; ++pr) {
+    for (int pr = 0; pr < 16; ++pr) {
         float f2[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int r = 16 * part + 2 * pr + e;
+            const int rr = 2 * pr + e, r = 32 * hh + rr, jj = rr >> 4;
             const float lam = *reinterpret_cast<const float*>(sm + OFF_G + g_off(r, c));
-            const float fac = ex2f((sJ - lam) + tailJ);
+            const float fac = ex2f((sJs[jj] - lam) + tails[jj]);
             unsigned short kb;
             asm volatile("ld.shared.u16 %0, [%1];" : "=h"(kb) : "r"(kbase + sw128_off(r, c, 64)));
             const float kv = (r < BT) ? __uint_as_float(((uint32_t)kb) << 16) : 0.f;
@@ -325,8 +334,35 @@ __device__ __forceinline__ void phase4_ktilde(uint8_t* sm, const float* vec, uin
         }
         split_bf16x2(f2[0], f2[1], hi[pr], lo[pr]);
     }
-    tmem_st8u(tmem_addr(tm, 32 * quarter, TM_KT + 8 * part), hi);
-    tmem_st8u(tmem_addr(tm, 32 * quarter, TM_KTL + 8 * part), lo);
+    tmem_st16u(tmem_addr(tm, 32 * quarter, TM_KT + 16 * hh), hi);
+    tmem_st16u(tmem_addr(tm, 32 * quarter, TM_KTL + 16 * hh), lo);
+}
+
+// ---------------------------------------------------------------- phase 3 side work: S operand
+// Lane c, columns [64 hh, 64 hh + 64): S -> bf16 MN-major B operand, then S <- gamma_C[c] S.
+__device__ __forceinline__ void build_state_operand(uint8_t* sm, const float* vec, uint32_t tm, int c, int hh,
+                                                    int quarter)
+{
+    const uint32_t sbase = smem_u32(sm);
+    const float gc = vec[V_GC * 128 + c];
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+        const int col = 64 * hh + 32 * k2;
+        float a[32];
+        tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + col), a);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            st_shared_v4(sbase + OFF_X + X_SB + sw128_chunk(c, (col >> 3) + q, 128), pk[4 * q], pk[4 * q + 1],
+                         pk[4 * q + 2], pk[4 * q + 3]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] *= gc;
+        tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + col), a);
+    }
+    tmem_wait_st();
 }
 
 // ---------------------------------------------------------------- phase 1b: token operands
@@ -448,11 +484,11 @@ __device__ __forceinline__ void phase3_readout(uint8_t* sm, uint32_t tm, int L, 
 }
 
 // ---------------------------------------------------------------- phase 3: T = (I + A)^-1
-// All 256 threads.  sT must be zero on entry.  16x16 diagonal blocks by forward
+// Threads 0..kSolveThreads-1 (named barrier 1).  sT must be zero on entry.  16x16 diagonal blocks by forward
 // substitution (one thread per column), then block levels d = 1..3:
 //   T_{m,m-d} = -T_{m,m} sum_{p=m-d}^{m-1} A_{m,p} T_{p,m-d}.
 template <int D>
-__device__ __forceinline__ void solve_level(const float* sA, float* sT, float* sY, int t)
+__device__ __forceinline__ void solve_level(const float* sA, float* sT, float* sY, int t)   // t < kSolveThreads
 {
     constexpr int NBLK = 4 - D;
     // Y_{m,J} = sum_{p=J}^{m-1} A_{m,p} T_{p,J}, J = m - D; each thread 4 adjacent columns
@@ -475,7 +511,7 @@ __device__ __forceinline__ void solve_level(const float* sA, float* sT, float* s
         *reinterpret_cast<float4*>(sY + bk * 16 * LDY + i * LDY + j4) =
             make_float4(acc.x + acc2.x, acc.y + acc2.y, acc.z + acc2.z, acc.w + acc2.w);
     }
-    __syncthreads();
+    named_sync(1, kSolveThreads);
     // T_{m,J} = -T_{m,m} Y_{m,J}
     if (t < NBLK * 64) {
         const int bk = t >> 6, i = (t >> 2) & 15, j4 = (t & 3) * 4;
@@ -496,7 +532,7 @@ __device__ __forceinline__ void solve_level(const float* sA, float* sT, float* s
         *reinterpret_cast<float4*>(sT + (16 * m + i) * LDA + 16 * J + j4) =
             make_float4(-(acc.x + acc2.x), -(acc.y + acc2.y), -(acc.z + acc2.z), -(acc.w + acc2.w));
     }
-    __syncthreads();
+    named_sync(1, kSolveThreads);
 }
 
 __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
@@ -523,7 +559,7 @@ __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
 #pragma unroll
         for (int q = 0; q < 16; ++q) sT[(b + q) * LDA + b + j] = x[q];
     }
-    __syncthreads();
+    named_sync(1, kSolveThreads);
     solve_level<1>(sA, sT, sY, t);
     solve_level<2>(sA, sT, sY, t);
     solve_level<3>(sA, sT, sY, t);
@@ -726,8 +762,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         }
         phase3_readout(sm, tm, L, quarter, part, sbeta);
         tmem_wait_st();
+        tc_fence_before_sync();
         __syncthreads();
-        phase3_solve(sm, t);
+        tc_fence_after_sync();
+        if (t < kSolveThreads) {
+            phase3_solve(sm, t);
+        } else if (warp >= 8) {   // meanwhile: K~^T and the state's B operand (+ its decay)
+            const int hh = (warp - 8) >> 2;
+            build_ktilde(sm, vec, tm, L, hh, quarter, BT);
+            build_state_operand(sm, vec, tm, L, hh, quarter);
+            fence_proxy_async_smem();
+        }
+        tc_fence_before_sync();
+        __syncthreads();
+        tc_fence_after_sync();
         phase3_tb_operands(sm, t, sbeta);
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -776,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_before_sync();
         __syncthreads();
 
-        // ---- phase 4: D2 = [Tb; M] K_Gamma (hi + lo) while K~^T is built, then A1 = [-Wk; Q']
+        // ---- phase 4: D2 = [Tb; M] K_Gamma (hi + lo), then A1 = [-Wk; Q']
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
@@ -789,7 +837,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPL + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
             umma_commit(bar_mma);
         }
-        phase4_ktilde(sm, vec, tm, L, part, quarter, BT);   // overlaps the MMA above
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
@@ -812,25 +859,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             issue_qkg_loads(p, sm, bar_qkg, t0 + 64, h);
             qkg_pending = true;
         }
-
-        // ---- phase 5a: S -> bf16 B operand; S <- Diag(gamma_C) S in place
-        {
-            float a[32];
-            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), a);
-            tmem_wait_ld();
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
-            store_row32_bf16(sbase + OFF_X + X_SB, L, 4 * part, 128, pk);
-            const float gc = vec[V_GC * 128 + L];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] *= gc;
-            tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), a);
-            tmem_wait_st();
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
 
         // ---- phase 5b: D1 = [Tb; M] V (hi + lo) + [-Wk; Q'] S
         if (t == 0) {
