@@ -72,8 +72,8 @@ constexpr uint32_t X_SB = 40960;       // S bf16, MN-major B [128 dk][128 dv] (w
 constexpr uint32_t X_WH = 0;           // W hi bf16, MN-major B [64 tok][128 dv] (phase 5)
 constexpr uint32_t X_WL = 16384;       // W lo
 constexpr uint32_t OFF_KG = 180224;    // K_Gamma bf16, MN-major B [64 tok][128 ch]
-constexpr uint32_t OFF_VEC = 196608;   // per-channel vectors [23][128] fp32
-constexpr uint32_t OFF_BETA = OFF_VEC + 23 * 512;
+constexpr uint32_t OFF_VEC = 196608;   // per-channel vectors [29][128] fp32
+constexpr uint32_t OFF_BETA = OFF_VEC + 29 * 512;
 constexpr uint32_t OFF_BAR = OFF_BETA + 256;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr size_t SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
@@ -92,6 +92,7 @@ constexpr int V_G = 8;     // G_J = e^{Gamma_63 - rho_{J+1}}                 (4)
 constexpr int V_D = 12;    // D_J = e^{rho_{J+1} - rho_J}                    (4)
 constexpr int V_F = 16;    // F_{m,J} = e^{rho_m - rho_{J+1}}, J < m          (6)
 constexpr int V_GC = 22;   // gamma_C = e^{Gamma_63}                         (1)
+constexpr int V_DF = 23;   // D_J F_{m,J} = e^{rho_m - rho_J}, J < m          (6)
 
 __host__ __device__ constexpr int f_index(int m, int J) { return m * (m - 1) / 2 + J; }
 
@@ -306,6 +307,35 @@ __device__ __forceinline__ void phase1_factors(float* vec, int c)
     vec[(V_F + f_index(3, 1)) * 128 + c] = ex2f(s2);
     vec[(V_F + f_index(3, 2)) * 128 + c] = 1.f;
     vec[V_GC * 128 + c] = ex2f(lam63);
+    vec[(V_DF + f_index(1, 0)) * 128 + c] = ex2f(s0);
+    vec[(V_DF + f_index(2, 0)) * 128 + c] = ex2f(s0 + s1);
+    vec[(V_DF + f_index(2, 1)) * 128 + c] = ex2f(s1);
+    vec[(V_DF + f_index(3, 0)) * 128 + c] = ex2f(s0 + s1 + s2);
+    vec[(V_DF + f_index(3, 1)) * 128 + c] = ex2f(s1 + s2);
+    vec[(V_DF + f_index(3, 2)) * 128 + c] = ex2f(s2);
+}
+
+// ---------------------------------------------------------------- phase 1c: off-diagonal column rows
+// For reference m and token i of an earlier sub-tile J < m, the column operand is
+// k_i e^{rho_m - Gamma_i} = (k_i e^{rho_J - Gamma_i}) e^{rho_m - rho_J}: the stored
+// diagonal-tile row of token i times a per-channel factor.  3072 tasks of 4 channels
+// (6 (m, J) pairs x 16 tokens x 32 chunks), 6 per thread.
+__device__ __forceinline__ void phase1_offdiag(uint8_t* sm, const float* vec, int t)
+{
+    const uint32_t kc = smem_u32(sm) + OFF_X;
+#pragma unroll
+    for (int u = 0; u < 6; ++u) {
+        const int task = t + kThreads * u;
+        const int b = task >> 9, i16 = (task >> 5) & 15, c0 = 4 * (task & 31);
+        const int m = (b == 0) ? 1 : ((b < 3) ? 2 : 3);
+        const int J = b - m * (m - 1) / 2;
+        const int i = 16 * J + i16;
+        const uint4 d = ld_shared_v4(kc + sw128_off_f32(kc_row(J) + i, c0, KC_ROWS));
+        const float4 f = *reinterpret_cast<const float4*>(vec + (V_DF + b) * 128 + c0);
+        st_shared_f4(kc + sw128_off_f32(kc_row(m) + i, c0, KC_ROWS), tf32_round(__uint_as_float(d.x) * f.x),
+                     tf32_round(__uint_as_float(d.y) * f.y), tf32_round(__uint_as_float(d.z) * f.z),
+                     tf32_round(__uint_as_float(d.w) * f.w));
+    }
 }
 
 // ---------------------------------------------------------------- phase 3 side work: K~^T into TMEM
@@ -367,10 +397,8 @@ __device__ __forceinline__ void build_state_operand(uint8_t* sm, const float* ve
 
 // ---------------------------------------------------------------- phase 1b: token operands
 // Thread (lane L, part p): token r = L % 64 of the q rows (L >= 64) or k rows (L < 64),
-// channels [32p, 32p + 32).  Writes the tf32 row operand [K_r; Q_r] (TMEM).  The k-row
-// thread also writes token r's diagonal-tile column operand and its K_Gamma B operand;
-// the q-row thread of the same token writes that token's column operands for the
-// references m > J (balancing the two halves).
+// channels [32p, 32p + 32).  Writes the tf32 row operand [K_r; Q_r] (TMEM); the k-row
+// thread also writes token r's diagonal-tile column operand and its K_Gamma B operand.
 __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uint32_t tm, int L, int part,
                                               int quarter, int BT)
 {
@@ -395,17 +423,19 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
             lam[3] = __uint_as_float(la.w); lam[4] = __uint_as_float(lb.x); lam[5] = __uint_as_float(lb.y);
             lam[6] = __uint_as_float(lb.z); lam[7] = __uint_as_float(lb.w);
         }
-        float xr[8], vx[8];
+        float xs[8], vx[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const float v = valid ? xv[e] : 0.f;
-            const float x = ex2f(lam[e]);                        // e^{Gamma_r - rho_J} in (0, 1]
-            vx[e] = v * x;
+            xs[e] = ex2f(lam[e]);                                // e^{Gamma_r - rho_J} in (0, 1]
+            vx[e] = v * xs[e];
             kq[8 * gi + e] = tf32_round(vx[e]);
-            xr[e] = rcpf(x);                                     // e^{rho_J - Gamma_r} <= e^{80}
             xv[e] = v;
         }
         if (!isq) {
+            float xr[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xr[e] = rcpf(xs[e]);     // e^{rho_J - Gamma_r} <= e^{80}
             // diagonal-tile column operand of reference J, and the K_Gamma B operand
             const float4 e4a = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
             const float4 e4b = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
@@ -417,27 +447,6 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
             st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), pack_bf16x2(vx[0] * e4a.x, vx[1] * e4a.y),
                          pack_bf16x2(vx[2] * e4a.z, vx[3] * e4a.w), pack_bf16x2(vx[4] * e4b.x, vx[5] * e4b.y),
                          pack_bf16x2(vx[6] * e4b.z, vx[7] * e4b.w));
-        } else if (J < 3) {
-            // this token's k, for the column operands of references m > J:
-            // k e^{rho_{J+1} - Gamma_r} e^{rho_m - rho_{J+1}}
-            const uint4 kraw = ld_shared_v4(sbase + OFF_K + sw128_chunk(r, c0 >> 3, 64));
-            const float2 k0 = bf2_to_f2(kraw.x), k1 = bf2_to_f2(kraw.y), k2 = bf2_to_f2(kraw.z), k3 = bf2_to_f2(kraw.w);
-            const float kvv[8] = {k0.x, k0.y, k1.x, k1.y, k2.x, k2.y, k3.x, k3.y};
-            const float4 d4a = *reinterpret_cast<const float4*>(vec + (V_D + J) * 128 + c0);
-            const float4 d4b = *reinterpret_cast<const float4*>(vec + (V_D + J) * 128 + c0 + 4);
-            const float dv[8] = {d4a.x, d4a.y, d4a.z, d4a.w, d4b.x, d4b.y, d4b.z, d4b.w};
-            float ky[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ky[e] = (valid ? kvv[e] : 0.f) * xr[e] * dv[e];
-            for (int m = J + 1; m < 4; ++m) {
-                const float4 f4a = *reinterpret_cast<const float4*>(vec + (V_F + f_index(m, J)) * 128 + c0);
-                const float4 f4b = *reinterpret_cast<const float4*>(vec + (V_F + f_index(m, J)) * 128 + c0 + 4);
-                const uint32_t rm = kc_row(m) + r;
-                st_shared_f4(kc + sw128_off_f32(rm, c0, KC_ROWS), tf32_round(ky[0] * f4a.x),
-                             tf32_round(ky[1] * f4a.y), tf32_round(ky[2] * f4a.z), tf32_round(ky[3] * f4a.w));
-                st_shared_f4(kc + sw128_off_f32(rm, c0 + 4, KC_ROWS), tf32_round(ky[4] * f4b.x),
-                             tf32_round(ky[5] * f4b.y), tf32_round(ky[6] * f4b.z), tf32_round(ky[7] * f4b.w));
-            }
         }
     }
     tmem_st32(tmem_addr(tm, 32 * quarter, TM_KQ + 32 * part), kq);
@@ -730,6 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (t < 128) phase1_factors(vec, t);
         __syncthreads();
         phase1_tokens(sm, vec, tm, L, part, quarter, BT);
+        __syncthreads();
+        phase1_offdiag(sm, vec, t);
         fence_proxy_async_smem();
         tmem_wait_st();
         tc_fence_before_sync();
