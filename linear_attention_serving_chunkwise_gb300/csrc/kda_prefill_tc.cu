@@ -32,7 +32,7 @@
 //      and the state's bf16 B operand and apply the chunk decay to S; M = P Tb by
 //      three bf16 MMAs (hi/lo splits).
 //   4  [Wk; M K_Gamma] by MMA, then the [-Wk; Q'] operand; TMA prefetch of the next
-//      chunk's q, k and g.
+//      chunk's q and g (its k is fetched at the end of phase 3).
 //   5  D1 = [Tb; M] V + [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O;
 //      W to shared memory; S += K~^T W by MMA while O is staged in shared memory and
 //      written by TMA bulk stores (direct stores for a sequence's ragged last chunk).
@@ -251,14 +251,20 @@ __device__ __forceinline__ void issue_v_loads(const TcParams& p, uint8_t* sm, ui
     tma_load_3d(vb + 8192, &p.tm_v, bar, 64, h, t0);
 }
 
-// q, k and g of a chunk; completes on `bar` (64 KB).
-__device__ __forceinline__ void issue_qkg_loads(const TcParams& p, uint8_t* sm, uint64_t* bar, int t0, int h)
+// k of a chunk; completes on `bar` (16 KB).
+__device__ __forceinline__ void issue_k_loads(const TcParams& p, uint8_t* sm, uint64_t* bar, int t0, int h)
 {
-    mbar_arrive_expect_tx(bar, 65536u);
-    tma_load_3d(sm + OFF_Q, &p.tm_q, bar, 0, h, t0);
-    tma_load_3d(sm + OFF_Q + 8192, &p.tm_q, bar, 64, h, t0);
+    mbar_arrive_expect_tx(bar, 16384u);
     tma_load_3d(sm + OFF_K, &p.tm_k, bar, 0, h, t0);
     tma_load_3d(sm + OFF_K + 8192, &p.tm_k, bar, 64, h, t0);
+}
+
+// q and g of a chunk; completes on `bar` (48 KB).
+__device__ __forceinline__ void issue_qg_loads(const TcParams& p, uint8_t* sm, uint64_t* bar, int t0, int h)
+{
+    mbar_arrive_expect_tx(bar, 49152u);
+    tma_load_3d(sm + OFF_Q, &p.tm_q, bar, 0, h, t0);
+    tma_load_3d(sm + OFF_Q + 8192, &p.tm_q, bar, 64, h, t0);
 #pragma unroll
     for (int b = 0; b < 4; ++b) tma_load_3d(sm + OFF_G + 8192 * b, &p.tm_g, bar, 32 * b, h, t0);
 }
@@ -649,9 +655,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     float* vec = reinterpret_cast<float*>(sm + OFF_VEC);
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
     uint64_t* bar_v = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-    uint64_t* bar_qkg = bar_v + 1;
-    uint64_t* bar_mma = bar_v + 2;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_v + 3);
+    uint64_t* bar_k = bar_v + 1;
+    uint64_t* bar_qg = bar_v + 2;
+    uint64_t* bar_mma = bar_v + 3;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_v + 4);
     int* s_abort = reinterpret_cast<int*>(tslot + 1);
     const uint32_t sbase = smem_u32(sm);
 
@@ -664,7 +671,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
 
     if (t == 0) {
         mbar_init(bar_v, 1);
-        mbar_init(bar_qkg, 1);
+        mbar_init(bar_k, 1);
+        mbar_init(bar_qg, 1);
         mbar_init(bar_mma, 1);
         mbar_fence_init();
         *s_abort = 0;
@@ -683,11 +691,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     tc_fence_after_sync();
     const uint32_t tm = *tslot;
 
-    bool v_pending = false, qkg_pending = false, o_pending = false;   // meaningful in thread 0 only
+    bool v_pending = false, k_pending = false, qg_pending = false, o_pending = false;   // thread 0 only
     if (t == 0 && nchunks > 0) {
         issue_v_loads(p, sm, bar_v, 0, bos, h);
-        issue_qkg_loads(p, sm, bar_qkg, bos, h);
-        v_pending = qkg_pending = true;
+        issue_k_loads(p, sm, bar_k, bos, h);
+        issue_qg_loads(p, sm, bar_qg, bos, h);
+        v_pending = k_pending = qg_pending = true;
     }
 
     // initial state -> TMEM: lane L = key channel, columns [32 part, 32 part + 32)
@@ -709,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     }
 
     float beta_next = (t < 64 && bos + t < eos) ? __ldg(p.beta + (size_t)(bos + t) * H + h) : 0.f;
-    uint32_t v_par = 0, qkg_par = 0, mma_par = 0;
+    uint32_t v_par = 0, k_par = 0, qg_par = 0, mma_par = 0;
     bool ok = true;
 
     for (int ci = 0; ci < nchunks; ++ci) {
@@ -729,9 +738,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         }
         if (!(ok = wait_all(bar_v, v_par, s_abort))) break;
         v_par ^= 1u;
-        if (!(ok = wait_all(bar_qkg, qkg_par, s_abort))) break;
-        qkg_par ^= 1u;
-        if (t == 0) v_pending = qkg_pending = false;
+        if (!(ok = wait_all(bar_k, k_par, s_abort))) break;
+        k_par ^= 1u;
+        if (!(ok = wait_all(bar_qg, qg_par, s_abort))) break;
+        qg_par ^= 1u;
+        if (t == 0) v_pending = k_pending = qg_pending = false;
 
         // ---- phase 1: decayed operands
         phase1_cumsum(sm, vec, t, BT);
@@ -787,6 +798,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
+        // the k tile of this chunk is no longer read: fetch the next chunk's
+        if (t == 0 && ci + 1 < nchunks) {
+            issue_k_loads(p, sm, bar_k, t0 + 64, h);
+            k_pending = true;
+        }
         phase3_tb_operands(sm, t, sbeta);
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -865,10 +881,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
-        // the q, k and g tiles of this chunk are no longer read: fetch the next chunk's
+        // the q and g tiles of this chunk are no longer read: fetch the next chunk's
         if (t == 0 && ci + 1 < nchunks) {
-            issue_qkg_loads(p, sm, bar_qkg, t0 + 64, h);
-            qkg_pending = true;
+            issue_qg_loads(p, sm, bar_qg, t0 + 64, h);
+            qg_pending = true;
         }
 
         // ---- phase 5b: D1 = [Tb; M] V (hi + lo) + [-Wk; Q'] S
@@ -975,7 +991,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         // a wait gave up: record it, let in-flight copies and MMAs land (bounded), then leave
         report_status(p.status, kDevTimeout);
         if (v_pending) mbar_wait_bounded(bar_v, v_par, kWaitNs);
-        if (qkg_pending) mbar_wait_bounded(bar_qkg, qkg_par, kWaitNs);
+        if (k_pending) mbar_wait_bounded(bar_k, k_par, kWaitNs);
+        if (qg_pending) mbar_wait_bounded(bar_qg, qg_par, kWaitNs);
         mbar_wait_bounded(bar_mma, mma_par, kWaitNs);
     }
     tc_fence_before_sync();
