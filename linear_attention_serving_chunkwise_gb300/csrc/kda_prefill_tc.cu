@@ -725,29 +725,34 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         const int t0 = bos + 64 * ci;
         const int BT = min(64, eos - t0);
         if (t < 64) sbeta[t] = beta_next;
-        if (t == 0 && o_pending) {   // the previous chunk's O staging must be read out before reuse
-            bulk_wait_read();
-            o_pending = false;
-        }
+        // this chunk's inputs (one barrier for the three copies)
+        if (!(mbar_wait_bounded(bar_v, v_par, kWaitNs) && mbar_wait_bounded(bar_k, k_par, kWaitNs) &&
+              mbar_wait_bounded(bar_qg, qg_par, kWaitNs)))
+            atomicExch(s_abort, 1);
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
+        if (*s_abort) {
+            ok = false;
+            break;
+        }
+        v_par ^= 1u;
+        k_par ^= 1u;
+        qg_par ^= 1u;
+        if (t == 0) v_pending = k_pending = qg_pending = false;
         if (t < 64) {
             const int tn = t0 + 64 + t;
             beta_next = (ci + 1 < nchunks && tn < eos) ? __ldg(p.beta + (size_t)tn * H + h) : 0.f;
         }
-        if (!(ok = wait_all(bar_v, v_par, s_abort))) break;
-        v_par ^= 1u;
-        if (!(ok = wait_all(bar_k, k_par, s_abort))) break;
-        k_par ^= 1u;
-        if (!(ok = wait_all(bar_qg, qg_par, s_abort))) break;
-        qg_par ^= 1u;
-        if (t == 0) v_pending = k_pending = qg_pending = false;
 
         // ---- phase 1: decayed operands
         phase1_cumsum(sm, vec, t, BT);
         __syncthreads();
         if (t < 128) phase1_factors(vec, t);
+        if (t == 0 && o_pending) {   // the previous chunk's O staging must be read out before reuse
+            bulk_wait_read();
+            o_pending = false;
+        }
         __syncthreads();
         phase1_tokens(sm, vec, tm, L, part, quarter, BT);
         __syncthreads();
