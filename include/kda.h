@@ -128,6 +128,35 @@ kda_status kda_prefill(const kda_prefill_desc* desc,
                        void* stream);
 
 /*
+ * kda_prefill_checkpointed -- kda_prefill that also snapshots each sequence's state at
+ * chunk-aligned positions, for resuming a later request from a cached prefix (llm-atlas
+ * K3_RESEARCH.md, Q31 hybrid prefix cache with sparse KDA checkpoints and 512-token hash
+ * boundaries; section 8 device layer "KDA replay input"; Lab H boundary arithmetic).
+ *
+ * Same arguments and rules as kda_prefill, plus:
+ *   checkpoint_interval  tokens between snapshots: a positive multiple of 64
+ *   checkpoint_slots     snapshots kept per sequence (>= 1)
+ *   checkpoints          [N, H, checkpoint_slots, dk, dv] fp32, device memory; slot j of
+ *                        sequence n receives the state after its first (j + 1) *
+ *                        checkpoint_interval tokens, for every such boundary that lies
+ *                        within the sequence (the state after the whole sequence is
+ *                        final_state).  Slots past a sequence's last boundary are not
+ *                        written.  Must not overlap any other argument.
+ * Resuming from slot j = running kda_prefill on the tokens after that boundary with
+ * init_state = the snapshot.
+ */
+kda_status kda_prefill_checkpointed(const kda_prefill_desc* desc,
+                                    const void* q, const void* k, const void* v,
+                                    const float* g, const float* beta,
+                                    const int32_t* cu_seqlens,
+                                    const float* init_state,
+                                    float* out, float* final_state,
+                                    int32_t checkpoint_interval, int32_t checkpoint_slots,
+                                    float* checkpoints,
+                                    void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/*
  * kda_decode -- one token per sequence, as a fused O(1) update of each head's
  * state: a single read and a single write of S (llm-atlas K3_RESEARCH.md, Q07
  * "decode keeps the O(1) state update"; section 8 device layer "fused decode").

@@ -26,7 +26,7 @@ KDA_BF16 = 1
 
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes", "kda_prefill_query",
-            "kda_prefill", "kda_decode", "kda_last_device_status")
+            "kda_prefill", "kda_prefill_checkpointed", "kda_decode", "kda_last_device_status")
 
 
 class KDAError(RuntimeError):
@@ -69,6 +69,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kda_prefill_query.argtypes = [ctypes.POINTER(PrefillDesc), ctypes.POINTER(PrefillPlan)]
     lib.kda_prefill.restype = ctypes.c_int
     lib.kda_prefill.argtypes = [ctypes.POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.kda_prefill_checkpointed.restype = ctypes.c_int
+    lib.kda_prefill_checkpointed.argtypes = [ctypes.POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                             i32, i32, vp, vp, sz, vp]
     lib.kda_decode.restype = ctypes.c_int
     lib.kda_decode.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.kda_last_device_status.restype = ctypes.c_int
@@ -123,7 +126,8 @@ def prefill_query(desc: PrefillDesc) -> dict:
 
 
 def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_state=None, *,
-            num_seqs: Optional[int] = None, want_final: bool = True, workspace=None, stream=None, check=True):
+            num_seqs: Optional[int] = None, want_final: bool = True, workspace=None, stream=None, check=True,
+            checkpoint_interval: int = 0, checkpoint_slots: int = 0, checkpoints=None):
     """KDA prefill through ``kda_prefill``.
 
     q, k [T,H,dk], v [T,H,dv] (fp32 or bf16); g [T,H,dk] fp32; beta [T,H] fp32;
@@ -143,6 +147,16 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if checkpoint_interval:
+        if checkpoints is None:
+            checkpoints = torch.zeros((N, H, checkpoint_slots, dk, dv), dtype=torch.float32, device=q.device)
+        st = load().kda_prefill_checkpointed(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                             _ptr(cu_seqlens), _ptr(init_state), _ptr(out), _ptr(final_state),
+                                             int(checkpoint_interval), int(checkpoint_slots), _ptr(checkpoints),
+                                             _ptr(workspace), ws_bytes, _stream_handle(stream))
+        if check and st != KDA_OK:
+            raise KDAError(st, "kda_prefill_checkpointed")
+        return out, final_state, checkpoints
     st = load().kda_prefill(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
                             _ptr(init_state), _ptr(out), _ptr(final_state), _ptr(workspace), ws_bytes,
                             _stream_handle(stream))

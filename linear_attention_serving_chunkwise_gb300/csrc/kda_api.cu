@@ -97,10 +97,14 @@ kda_status kda_prefill_query(const kda_prefill_desc* desc, kda_prefill_plan* pla
     return KDA_OK;
 }
 
-kda_status kda_prefill(const kda_prefill_desc* desc, const void* q, const void* k, const void* v,
-                       const float* g, const float* beta, const int32_t* cu_seqlens,
-                       const float* init_state, float* out, float* final_state,
-                       void* workspace, size_t workspace_bytes, void* stream)
+}  // extern "C"
+
+namespace {
+
+kda_status prefill_impl(const kda_prefill_desc* desc, const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, const int32_t* cu_seqlens, const float* init_state, float* out,
+                        float* final_state, int32_t ckpt_interval, int32_t ckpt_slots, float* checkpoints,
+                        void* workspace, size_t workspace_bytes, void* stream)
 {
     kda_status st = validate_prefill(desc);
     if (st != KDA_OK) return st;
@@ -139,6 +143,15 @@ kda_status kda_prefill(const kda_prefill_desc* desc, const void* q, const void* 
     if (final_state && init_state && final_state != init_state && overlaps(r_fin, ins[6]))
         return KDA_ERR_INVALID_ARG;
     if (final_state && T > 0 && overlaps(r_fin, r_out)) return KDA_ERR_INVALID_ARG;
+    if (checkpoints) {
+        if (ckpt_interval <= 0 || ckpt_interval % 64 != 0 || ckpt_slots <= 0 || !aligned16(checkpoints))
+            return KDA_ERR_INVALID_ARG;
+        const Range r_ck = range_of(checkpoints, N * H * (size_t)ckpt_slots * d.dk * d.dv * sizeof(float));
+        for (const Range& r : ins) {
+            if (overlaps(r_ck, r)) return KDA_ERR_INVALID_ARG;
+        }
+        if ((T > 0 && overlaps(r_ck, r_out)) || (final_state && overlaps(r_ck, r_fin))) return KDA_ERR_INVALID_ARG;
+    }
 
     int* status = status_ptr_for_current_device();
     if (!status) return KDA_ERR_CUDA;
@@ -148,10 +161,37 @@ kda_status kda_prefill(const kda_prefill_desc* desc, const void* q, const void* 
     a.dk = d.dk; a.dv = d.dv; a.bf16 = d.qkv_dtype == KDA_BF16;
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu_seqlens = cu_seqlens;
     a.init_state = init_state; a.out = out; a.final_state = final_state;
+    a.ckpt_interval = checkpoints ? ckpt_interval : 0;
+    a.ckpt_slots = checkpoints ? ckpt_slots : 0;
+    a.checkpoints = checkpoints;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.status = status;
     const cudaError_t e = uses_tensor_cores(d) ? kda::launch_prefill_tc(a, static_cast<cudaStream_t>(stream))
                                                : kda::launch_prefill_simt(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill(const kda_prefill_desc* desc, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const int32_t* cu_seqlens,
+                       const float* init_state, float* out, float* final_state,
+                       void* workspace, size_t workspace_bytes, void* stream)
+{
+    return prefill_impl(desc, q, k, v, g, beta, cu_seqlens, init_state, out, final_state, 0, 0, nullptr, workspace,
+                        workspace_bytes, stream);
+}
+
+kda_status kda_prefill_checkpointed(const kda_prefill_desc* desc, const void* q, const void* k, const void* v,
+                                    const float* g, const float* beta, const int32_t* cu_seqlens,
+                                    const float* init_state, float* out, float* final_state,
+                                    int32_t checkpoint_interval, int32_t checkpoint_slots, float* checkpoints,
+                                    void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (!checkpoints) return KDA_ERR_INVALID_ARG;
+    return prefill_impl(desc, q, k, v, g, beta, cu_seqlens, init_state, out, final_state, checkpoint_interval,
+                        checkpoint_slots, checkpoints, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, int32_t qkv_dtype,

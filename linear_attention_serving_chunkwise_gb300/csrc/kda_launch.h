@@ -15,6 +15,10 @@ struct PrefillArgs {
     const int32_t* cu_seqlens;
     const float* init_state;
     float *out, *final_state;
+    // optional state snapshots: every ckpt_interval tokens (multiple of 64) of each
+    // sequence, up to ckpt_slots per sequence, into checkpoints [N, H, ckpt_slots, dk, dv]
+    int ckpt_interval, ckpt_slots;
+    float* checkpoints;
     void* workspace;
     size_t workspace_bytes;
     int* status;  // device status word

@@ -168,6 +168,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
         __syncthreads();
 #pragma unroll
         for (int m = 0; m < D / kWarps; ++m) sS[(warp + kWarps * m) * kSlice + lane] = snew[m];
+        // state snapshot after a full chunk that ends on a checkpoint boundary
+        const int done = c0 + BT - bos;
+        if (a.checkpoints && BT == kChunk && done % a.ckpt_interval == 0 && done / a.ckpt_interval <= a.ckpt_slots) {
+            const int slot = done / a.ckpt_interval - 1;
+            float* dst = a.checkpoints + (((size_t)n * H + h) * a.ckpt_slots + slot) * D * D;
+#pragma unroll
+            for (int m = 0; m < D / kWarps; ++m) dst[(size_t)(warp + kWarps * m) * D + js + lane] = snew[m];
+        }
     }
     __syncthreads();
     if (a.final_state) {

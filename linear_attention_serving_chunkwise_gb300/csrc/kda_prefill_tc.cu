@@ -121,6 +121,8 @@ struct TcParams {
     const float* init_state;
     float* out;
     float* final_state;
+    float* checkpoints;
+    int ckpt_interval, ckpt_slots;
     int num_seqs, total_tokens, num_heads;
     int* status;
 };
@@ -969,6 +971,22 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
+        // state snapshot after a full chunk that ends on a checkpoint boundary
+        {
+            const int done = t0 + 64 - bos;
+            if (p.checkpoints && BT == 64 && done % p.ckpt_interval == 0 && done / p.ckpt_interval <= p.ckpt_slots) {
+                tc_fence_after_sync();
+                const int slot = done / p.ckpt_interval - 1;
+                float v[32];
+                tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), v);
+                tmem_wait_ld();
+                float4* dst = reinterpret_cast<float4*>(
+                    p.checkpoints + (((size_t)n * H + h) * p.ckpt_slots + slot) * 128 * 128 + (size_t)L * 128 + 32 * part);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                tc_fence_before_sync();
+            }
+        }
         if (t == 0 && BT == 64) {
             const uint8_t* vb = sm + ((ci & 1) ? OFF_V1 : OFF_V0);
             tma_store_3d(&p.tm_o, sm + OFF_X + X_OST, 0, h, t0);
@@ -1051,6 +1069,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream)
     p.init_state = a.init_state;
     p.out = a.out;
     p.final_state = a.final_state;
+    p.checkpoints = a.checkpoints;
+    p.ckpt_interval = a.checkpoints ? a.ckpt_interval : 64;
+    p.ckpt_slots = a.ckpt_slots;
     p.num_seqs = a.num_seqs;
     p.total_tokens = a.total_tokens;
     p.num_heads = a.num_heads;
