@@ -28,10 +28,10 @@
 //   1  g cumsum per channel; decayed operands to TMEM (A operands) and shared
 //      memory (B operands); TMA prefetch of the next chunk's v.
 //   2  A and P by one tf32 MMA over the four sub-tile references side by side.
-//   3  T = (I + A)^-1 in fp32 on CUDA cores (6 warps) while the other warps build K~^T
-//      and the state's bf16 B operand and apply the chunk decay to S; M = P Tb by
-//      three bf16 MMAs (hi/lo splits).
-//   4  [Wk; M K_Gamma] by MMA, then the [-Wk; Q'] operand; TMA prefetch of the next
+//   3  T = (I + A)^-1 in fp32 on CUDA cores (6 warps) while 8 other warps build K~^T;
+//      M = P Tb by three bf16 MMAs (hi/lo splits).
+//   4  [Wk; M K_Gamma] by MMA while the state's bf16 B operand is built (and S decayed);
+//      then the [-Wk; Q'] operand; TMA prefetch of the next
 //      chunk's q and g (its k is fetched at the end of phase 3).
 //   5  D1 = [Tb; M] V + [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O;
 //      W to shared memory; S += K~^T W by MMA while O is staged in shared memory and
@@ -68,7 +68,7 @@ constexpr uint32_t X_ST = 17408;       // T fp32 [64][68]
 constexpr uint32_t X_SY = 34816;       // level scratch fp32 [3][16][20]
 constexpr uint32_t X_OST = 65536;      // O staging, dv columns 0-63: 2 x [64 tok][32] fp32 boxes (phase 5,
                                        // after the MMA that reads S bf16 has completed)
-constexpr uint32_t X_SB = 40960;       // S bf16, MN-major B [128 dk][128 dv] (written during the solve)
+constexpr uint32_t X_SB = 40960;       // S bf16, MN-major B [128 dk][128 dv] (phase 4)
 constexpr uint32_t X_WH = 0;           // W hi bf16, MN-major B [64 tok][128 dv] (phase 5)
 constexpr uint32_t X_WL = 16384;       // W lo
 constexpr uint32_t OFF_KG = 180224;    // K_Gamma bf16, MN-major B [64 tok][128 ch]
@@ -376,31 +376,27 @@ __device__ __forceinline__ void build_ktilde(uint8_t* sm, const float* vec, uint
     tmem_st16u(tmem_addr(tm, 32 * quarter, TM_KTL + 16 * hh), lo);
 }
 
-// ---------------------------------------------------------------- phase 3 side work: S operand
-// Lane c, columns [64 hh, 64 hh + 64): S -> bf16 MN-major B operand, then S <- gamma_C[c] S.
-__device__ __forceinline__ void build_state_operand(uint8_t* sm, const float* vec, uint32_t tm, int c, int hh,
+// ---------------------------------------------------------------- phase 4 side work: S operand
+// Lane c, columns [32 part, 32 part + 32): S -> bf16 MN-major B operand, then
+// S <- gamma_C[c] S (the chunk decay, applied before the state update accumulates).
+__device__ __forceinline__ void build_state_operand(uint8_t* sm, const float* vec, uint32_t tm, int c, int part,
                                                     int quarter)
 {
     const uint32_t sbase = smem_u32(sm);
     const float gc = vec[V_GC * 128 + c];
+    float a[32];
+    tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), a);
+    tmem_wait_ld();
+    uint32_t pk[16];
 #pragma unroll
-    for (int k2 = 0; k2 < 2; ++k2) {
-        const int col = 64 * hh + 32 * k2;
-        float a[32];
-        tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + col), a);
-        tmem_wait_ld();
-        uint32_t pk[16];
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+    for (int q = 0; q < 4; ++q)
+        st_shared_v4(sbase + OFF_X + X_SB + sw128_chunk(c, 4 * part + q, 128), pk[4 * q], pk[4 * q + 1],
+                     pk[4 * q + 2], pk[4 * q + 3]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            st_shared_v4(sbase + OFF_X + X_SB + sw128_chunk(c, (col >> 3) + q, 128), pk[4 * q], pk[4 * q + 1],
-                         pk[4 * q + 2], pk[4 * q + 3]);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) a[i] *= gc;
-        tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + col), a);
-    }
-    tmem_wait_st();
+    for (int i = 0; i < 32; ++i) a[i] *= gc;
+    tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), a);
 }
 
 // ---------------------------------------------------------------- phase 1b: token operands
@@ -796,11 +792,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_after_sync();
         if (t < kSolveThreads) {
             phase3_solve(sm, t);
-        } else if (warp >= 8) {   // meanwhile: K~^T and the state's B operand (+ its decay)
-            const int hh = (warp - 8) >> 2;
-            build_ktilde(sm, vec, tm, L, hh, quarter, BT);
-            build_state_operand(sm, vec, tm, L, hh, quarter);
-            fence_proxy_async_smem();
+        } else if (warp >= 8) {   // meanwhile: K~^T
+            build_ktilde(sm, vec, tm, L, (warp - 8) >> 2, quarter, BT);
         }
         tc_fence_before_sync();
         __syncthreads();
@@ -871,6 +864,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPL + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
             umma_commit(bar_mma);
         }
+        build_state_operand(sm, vec, tm, L, part, quarter);   // overlaps the MMA above
+        tmem_wait_st();
+        fence_proxy_async_smem();
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
