@@ -57,7 +57,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---------------------------------------------------------------- shared memory map (bytes)
 constexpr uint32_t OFF_Q = 0;          // q tile  [64 tok][128 ch] bf16, 2 x 8 KB TMA boxes
 constexpr uint32_t OFF_K = 16384;      // k tile
-constexpr uint32_t OFF_G = 32768;      // g tile  [64][128] fp32, 4 x 8 KB boxes; becomes the sub-tile cumsum
+constexpr uint32_t OFF_G = 32768;      // g tile  [64][128] fp32, 4 x 8 KB boxes; becomes x = e^{Gamma_r - rho_J}
 constexpr uint32_t OFF_V0 = 65536;     // v tile, two buffers (B operand of [Tb; M] V)
 constexpr uint32_t OFF_V1 = 81920;
 constexpr uint32_t OFF_X = 98304;      // 80 KB region shared by phases 1-2 / 3 / 5
@@ -272,9 +272,10 @@ __device__ __forceinline__ void issue_qg_loads(const TcParams& p, uint8_t* sm, u
 }
 
 // ---------------------------------------------------------------- phase 1a: per-channel cumsum
-// Thread (c = t % 128, J = t / 128) turns sub-tile J of column c of the g tile into the
-// sub-tile-local cumsum lambda_r = sum_{s = 16J}^{r} g_s log2(e) (rows past the chunk's
-// end count as 0) and stores the sub-tile sum s_J.
+// Thread (c = t % 128, J = t / 128) forms the sub-tile-local cumsum
+// lambda_r = sum_{s = 16J}^{r} g_s log2(e) of sub-tile J of column c (rows past the chunk's
+// end count as 0), replaces g_r in the tile by x_r = 2^{lambda_r} = e^{Gamma_r - rho_J}
+// (in (0, 1], a normal float since g >= -5) and stores the sub-tile sum s_J.
 __device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, int BT)
 {
     const int c = t & 127, J = t >> 7;
@@ -285,7 +286,7 @@ __device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, in
         float* gp = reinterpret_cast<float*>(sm + OFF_G + g_off(r, c));
         const float gv = (r < BT) ? *gp : 0.f;
         acc = fmaf(gv, kLog2e, acc);
-        *gp = acc;
+        *gp = ex2f(acc);
     }
     vec[(V_S + J) * 128 + c] = acc;
 }
@@ -354,17 +355,17 @@ __device__ __forceinline__ void build_ktilde(uint8_t* sm, const float* vec, uint
 {
     uint32_t hi[16], lo[16];
     const uint32_t kbase = smem_u32(sm + OFF_K);
-    const float s1 = vec[(V_S + 1) * 128 + c], s2 = vec[(V_S + 2) * 128 + c], s3 = vec[(V_S + 3) * 128 + c];
-    const float tails[2] = {hh ? s3 : s1 + s2 + s3, hh ? 0.f : s2 + s3};   // sub-tiles 2 hh, 2 hh + 1
-    const float sJs[2] = {vec[(V_S + 2 * hh) * 128 + c], vec[(V_S + 2 * hh + 1) * 128 + c]};
+    // e^{Gamma_63 - Gamma_r} = e^{Gamma_63 - rho_J} / x_r with e^{Gamma_63 - rho_J} = d_J g_J
+    const float fJ[2] = {vec[(V_D + 2 * hh) * 128 + c] * vec[(V_G + 2 * hh) * 128 + c],
+                         vec[(V_D + 2 * hh + 1) * 128 + c] * vec[(V_G + 2 * hh + 1) * 128 + c]};
 #pragma unroll
     for (int pr = 0; pr < 16; ++pr) {
         float f2[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int rr = 2 * pr + e, r = 32 * hh + rr, jj = rr >> 4;
-            const float lam = *reinterpret_cast<const float*>(sm + OFF_G + g_off(r, c));
-            const float fac = ex2f((sJs[jj] - lam) + tails[jj]);
+            const float x = *reinterpret_cast<const float*>(sm + OFF_G + g_off(r, c));
+            const float fac = fJ[jj] * rcpf(x);
             unsigned short kb;
             asm volatile("ld.shared.u16 %0, [%1];" : "=h"(kb) : "r"(kbase + sw128_off(r, c, 64)));
             const float kv = (r < BT) ? __uint_as_float(((uint32_t)kb) << 16) : 0.f;
@@ -419,19 +420,18 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
         const uint4 raw = ld_shared_v4(src + sw128_chunk(r, c0 >> 3, 64));
         const uint4 la = ld_shared_v4(sbase + OFF_G + g_off(r, c0));
         const uint4 lb = ld_shared_v4(sbase + OFF_G + g_off(r, c0 + 4));
-        float xv[8], lam[8];
+        float xv[8], xs[8];
         {
             const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
             xv[0] = a0.x; xv[1] = a0.y; xv[2] = a1.x; xv[3] = a1.y; xv[4] = a2.x; xv[5] = a2.y; xv[6] = a3.x; xv[7] = a3.y;
-            lam[0] = __uint_as_float(la.x); lam[1] = __uint_as_float(la.y); lam[2] = __uint_as_float(la.z);
-            lam[3] = __uint_as_float(la.w); lam[4] = __uint_as_float(lb.x); lam[5] = __uint_as_float(lb.y);
-            lam[6] = __uint_as_float(lb.z); lam[7] = __uint_as_float(lb.w);
+            xs[0] = __uint_as_float(la.x); xs[1] = __uint_as_float(la.y); xs[2] = __uint_as_float(la.z);
+            xs[3] = __uint_as_float(la.w); xs[4] = __uint_as_float(lb.x); xs[5] = __uint_as_float(lb.y);
+            xs[6] = __uint_as_float(lb.z); xs[7] = __uint_as_float(lb.w);   // e^{Gamma_r - rho_J} in (0, 1]
         }
-        float xs[8], vx[8];
+        float vx[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const float v = valid ? xv[e] : 0.f;
-            xs[e] = ex2f(lam[e]);                                // e^{Gamma_r - rho_J} in (0, 1]
             vx[e] = v * xs[e];
             kq[8 * gi + e] = tf32_round(vx[e]);
             xv[e] = v;
@@ -498,7 +498,7 @@ __device__ __forceinline__ void phase3_readout(uint8_t* sm, uint32_t tm, int L, 
 
 // ---------------------------------------------------------------- phase 3: T = (I + A)^-1
 // Threads 0..kSolveThreads-1 (named barrier 1).  sT must be zero on entry.  16x16 diagonal blocks by forward
-// substitution (one thread per column), then block levels d = 1..3:
+// substitution (block m on warp m, one lane per column), then block levels d = 1..3:
 //   T_{m,m-d} = -T_{m,m} sum_{p=m-d}^{m-1} A_{m,p} T_{p,m-d}.
 template <int D>
 __device__ __forceinline__ void solve_level(const float* sA, float* sT, float* sY, int t)   // t < kSolveThreads
@@ -553,8 +553,8 @@ __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
     const float* sA = reinterpret_cast<const float*>(sm + OFF_X + X_SA);
     float* sT = reinterpret_cast<float*>(sm + OFF_X + X_ST);
     float* sY = reinterpret_cast<float*>(sm + OFF_X + X_SY);
-    if (t < 64) {
-        const int m = t >> 4, j = t & 15, b = 16 * m;
+    if (t < 128 && (t & 31) < 16) {   // block m on warp m (one per SMSP), column j on lane j
+        const int m = t >> 5, j = t & 15, b = 16 * m;
         float x[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) x[q] = (q == j) ? 1.f : 0.f;
@@ -628,13 +628,13 @@ __device__ __forceinline__ void phase4_qprime(uint8_t* sm, const float* vec, uin
         const float4 e4b = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
         const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
         const float qv[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
-        const float lam[8] = {__uint_as_float(la.x), __uint_as_float(la.y), __uint_as_float(la.z),
-                              __uint_as_float(la.w), __uint_as_float(lb.x), __uint_as_float(lb.y),
-                              __uint_as_float(lb.z), __uint_as_float(lb.w)};
+        const float xs[8] = {__uint_as_float(la.x), __uint_as_float(la.y), __uint_as_float(la.z),
+                             __uint_as_float(la.w), __uint_as_float(lb.x), __uint_as_float(lb.y),
+                             __uint_as_float(lb.z), __uint_as_float(lb.w)};
         const float ev[8] = {e4a.x, e4a.y, e4a.z, e4a.w, e4b.x, e4b.y, e4b.z, e4b.w};
         float qp[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qp[e] = (valid ? qv[e] * ex2f(lam[e]) * ev[e] : 0.f) - mk[8 * gi + e];
+        for (int e = 0; e < 8; ++e) qp[e] = (valid ? qv[e] * xs[e] * ev[e] : 0.f) - mk[8 * gi + e];
 #pragma unroll
         for (int e = 0; e < 4; ++e) pk[4 * gi + e] = pack_bf16x2(qp[2 * e], qp[2 * e + 1]);
     }
@@ -646,7 +646,9 @@ __device__ __forceinline__ void phase4_qprime(uint8_t* sm, const float* vec, uin
 __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base; offsetting the __shared__ array itself (rather than rounding an
+    // integer address) keeps every access through `sm` in the shared state space
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int quarter = warp & 3, part = warp >> 2;
     const int L = 32 * quarter + lane;   // the TMEM lane this thread may access
