@@ -72,8 +72,8 @@ constexpr uint32_t X_SB = 40960;       // S bf16, MN-major B [128 dk][128 dv] (p
 constexpr uint32_t X_WH = 0;           // W hi bf16, MN-major B [64 tok][128 dv] (phase 5)
 constexpr uint32_t X_WL = 16384;       // W lo
 constexpr uint32_t OFF_KG = 180224;    // K_Gamma bf16, MN-major B [64 tok][128 ch]
-constexpr uint32_t OFF_VEC = 196608;   // per-channel vectors [29][128] fp32
-constexpr uint32_t OFF_BETA = OFF_VEC + 29 * 512;
+constexpr uint32_t OFF_VEC = 196608;   // per-channel vectors [19][128] fp32
+constexpr uint32_t OFF_BETA = OFF_VEC + 19 * 512;
 constexpr uint32_t OFF_BAR = OFF_BETA + 256;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr size_t SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
@@ -86,13 +86,11 @@ constexpr uint32_t KC_ROWS = 160;
 __host__ __device__ constexpr uint32_t kc_row(int m) { return 8u * m * (m + 1); }
 
 // per-channel vectors (index * 128 floats into OFF_VEC)
-constexpr int V_S = 0;     // s_J: sum of g*log2e over sub-tile J            (4)
-constexpr int V_E = 4;     // E_J = e^{rho_J}                                (4)
-constexpr int V_G = 8;     // G_J = e^{Gamma_63 - rho_{J+1}}                 (4)
-constexpr int V_D = 12;    // D_J = e^{rho_{J+1} - rho_J}                    (4)
-constexpr int V_F = 16;    // F_{m,J} = e^{rho_m - rho_{J+1}}, J < m          (6)
-constexpr int V_GC = 22;   // gamma_C = e^{Gamma_63}                         (1)
-constexpr int V_DF = 23;   // D_J F_{m,J} = e^{rho_m - rho_J}, J < m          (6)
+constexpr int V_E = 0;     // E_J = e^{rho_J}                                (4)
+constexpr int V_G = 4;     // G_J = e^{Gamma_63 - rho_{J+1}}                 (4)
+constexpr int V_D = 8;     // D_J = e^{rho_{J+1} - rho_J}                    (4)
+constexpr int V_GC = 12;   // gamma_C = e^{Gamma_63}                         (1)
+constexpr int V_DF = 13;   // e^{rho_m - rho_J}, J < m                       (6)
 
 __host__ __device__ constexpr int f_index(int m, int J) { return m * (m - 1) / 2 + J; }
 
@@ -207,10 +205,22 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr)
     return v;
 }
 
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t saddr)
+{
+    const uint4 v = ld_shared_v4(saddr);
+    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+}
+
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t u)
 {
     __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
     return __bfloat1622float2(h);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 raw, float (&v)[8])
+{
+    const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
+    v[0] = a0.x; v[1] = a0.y; v[2] = a1.x; v[3] = a1.y; v[4] = a2.x; v[5] = a2.y; v[6] = a3.x; v[7] = a3.y;
 }
 
 // fp32 -> the nearest tf32 value (ties away from zero), kept in fp32 storage.  The
@@ -275,73 +285,68 @@ __device__ __forceinline__ void issue_qg_loads(const TcParams& p, uint8_t* sm, u
 // Thread (c = t % 128, J = t / 128) forms the sub-tile-local cumsum
 // lambda_r = sum_{s = 16J}^{r} g_s log2(e) of sub-tile J of column c (rows past the chunk's
 // end count as 0), replaces g_r in the tile by x_r = 2^{lambda_r} = e^{Gamma_r - rho_J}
-// (in (0, 1], a normal float since g >= -5) and stores the sub-tile sum s_J.
+// (in (0, 1], a normal float since g >= -5) and stores D_J = 2^{s_J}, the last x of the
+// sub-tile (s_J: the sub-tile's sum).
 __device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, int BT)
 {
     const int c = t & 127, J = t >> 7;
-    float acc = 0.f;
+    float acc = 0.f, x = 1.f;
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) {
         const int r = 16 * J + rr;
         float* gp = reinterpret_cast<float*>(sm + OFF_G + g_off(r, c));
         const float gv = (r < BT) ? *gp : 0.f;
         acc = fmaf(gv, kLog2e, acc);
-        *gp = ex2f(acc);
+        x = ex2f(acc);
+        *gp = x;
     }
-    vec[(V_S + J) * 128 + c] = acc;
+    vec[(V_D + J) * 128 + c] = x;
 }
 
-// Per-channel factors from the sub-tile sums (thread c < 128, after phase1_cumsum).
+// Per-channel factors (thread c < 128, after phase1_cumsum), all products of the four
+// D_J = e^{rho_{J+1} - rho_J}: a product of factors <= 1 underflows only where the
+// exponential of the summed exponent does.
 __device__ __forceinline__ void phase1_factors(float* vec, int c)
 {
-    const float s0 = vec[(V_S + 0) * 128 + c], s1 = vec[(V_S + 1) * 128 + c], s2 = vec[(V_S + 2) * 128 + c],
-                s3 = vec[(V_S + 3) * 128 + c];
-    const float rho1 = s0, rho2 = s0 + s1, rho3 = rho2 + s2, lam63 = rho3 + s3;
+    const float d0 = vec[(V_D + 0) * 128 + c], d1 = vec[(V_D + 1) * 128 + c], d2 = vec[(V_D + 2) * 128 + c],
+                d3 = vec[(V_D + 3) * 128 + c];
+    const float d01 = d0 * d1, d12 = d1 * d2, d23 = d2 * d3, d012 = d01 * d2, d123 = d1 * d23;
     vec[(V_E + 0) * 128 + c] = 1.f;
-    vec[(V_E + 1) * 128 + c] = ex2f(rho1);
-    vec[(V_E + 2) * 128 + c] = ex2f(rho2);
-    vec[(V_E + 3) * 128 + c] = ex2f(rho3);
-    vec[(V_G + 0) * 128 + c] = ex2f(s1 + s2 + s3);
-    vec[(V_G + 1) * 128 + c] = ex2f(s2 + s3);
-    vec[(V_G + 2) * 128 + c] = ex2f(s3);
+    vec[(V_E + 1) * 128 + c] = d0;
+    vec[(V_E + 2) * 128 + c] = d01;
+    vec[(V_E + 3) * 128 + c] = d012;
+    vec[(V_G + 0) * 128 + c] = d123;
+    vec[(V_G + 1) * 128 + c] = d23;
+    vec[(V_G + 2) * 128 + c] = d3;
     vec[(V_G + 3) * 128 + c] = 1.f;
-    vec[(V_D + 0) * 128 + c] = ex2f(s0);
-    vec[(V_D + 1) * 128 + c] = ex2f(s1);
-    vec[(V_D + 2) * 128 + c] = ex2f(s2);
-    vec[(V_D + 3) * 128 + c] = ex2f(s3);
-    vec[(V_F + f_index(1, 0)) * 128 + c] = 1.f;
-    vec[(V_F + f_index(2, 0)) * 128 + c] = ex2f(s1);
-    vec[(V_F + f_index(2, 1)) * 128 + c] = 1.f;
-    vec[(V_F + f_index(3, 0)) * 128 + c] = ex2f(s1 + s2);
-    vec[(V_F + f_index(3, 1)) * 128 + c] = ex2f(s2);
-    vec[(V_F + f_index(3, 2)) * 128 + c] = 1.f;
-    vec[V_GC * 128 + c] = ex2f(lam63);
-    vec[(V_DF + f_index(1, 0)) * 128 + c] = ex2f(s0);
-    vec[(V_DF + f_index(2, 0)) * 128 + c] = ex2f(s0 + s1);
-    vec[(V_DF + f_index(2, 1)) * 128 + c] = ex2f(s1);
-    vec[(V_DF + f_index(3, 0)) * 128 + c] = ex2f(s0 + s1 + s2);
-    vec[(V_DF + f_index(3, 1)) * 128 + c] = ex2f(s1 + s2);
-    vec[(V_DF + f_index(3, 2)) * 128 + c] = ex2f(s2);
+    vec[V_GC * 128 + c] = d012 * d3;
+    vec[(V_DF + f_index(1, 0)) * 128 + c] = d0;
+    vec[(V_DF + f_index(2, 0)) * 128 + c] = d01;
+    vec[(V_DF + f_index(2, 1)) * 128 + c] = d1;
+    vec[(V_DF + f_index(3, 0)) * 128 + c] = d012;
+    vec[(V_DF + f_index(3, 1)) * 128 + c] = d12;
+    vec[(V_DF + f_index(3, 2)) * 128 + c] = d2;
 }
 
 // ---------------------------------------------------------------- phase 1c: off-diagonal column rows
 // For reference m and token i of an earlier sub-tile J < m, the column operand is
 // k_i e^{rho_m - Gamma_i} = (k_i e^{rho_J - Gamma_i}) e^{rho_m - rho_J}: the stored
-// diagonal-tile row of token i times a per-channel factor.  3072 tasks of 4 channels
-// (6 (m, J) pairs x 16 tokens x 32 chunks), 6 per thread.
+// diagonal-tile row of token i times a per-channel factor.  Thread t covers token offset
+// i16 = (t / 32) % 16 and channels [4 (t % 32), +4) of all six (m, J) pairs; the row of
+// each pair is a compile-time offset from the thread's own swizzled base.
 __device__ __forceinline__ void phase1_offdiag(uint8_t* sm, const float* vec, int t)
 {
-    const uint32_t kc = smem_u32(sm) + OFF_X;
+    const int i16 = (t >> 5) & 15, c0 = 4 * (t & 31);
+    // sw128_off_f32(row, c0, KC_ROWS) with row % 8 == i16 % 8 for every row used below
+    const uint32_t base = smem_u32(sm) + OFF_X + ((t & 31) >> 3) * (KC_ROWS * 128u) + i16 * 128u +
+                          ((uint32_t)((t & 7) ^ (i16 & 7)) << 4);
 #pragma unroll
-    for (int u = 0; u < 6; ++u) {
-        const int task = t + kThreads * u;
-        const int b = task >> 9, i16 = (task >> 5) & 15, c0 = 4 * (task & 31);
+    for (int b = 0; b < 6; ++b) {
         const int m = (b == 0) ? 1 : ((b < 3) ? 2 : 3);
         const int J = b - m * (m - 1) / 2;
-        const int i = 16 * J + i16;
-        const uint4 d = ld_shared_v4(kc + sw128_off_f32(kc_row(J) + i, c0, KC_ROWS));
+        const uint4 d = ld_shared_v4(base + (kc_row(J) + 16 * J) * 128u);
         const float4 f = *reinterpret_cast<const float4*>(vec + (V_DF + b) * 128 + c0);
-        st_shared_f4(kc + sw128_off_f32(kc_row(m) + i, c0, KC_ROWS), tf32_round(__uint_as_float(d.x) * f.x),
+        st_shared_f4(base + (kc_row(m) + 16 * J) * 128u, tf32_round(__uint_as_float(d.x) * f.x),
                      tf32_round(__uint_as_float(d.y) * f.y), tf32_round(__uint_as_float(d.z) * f.z),
                      tf32_round(__uint_as_float(d.w) * f.w));
     }
@@ -402,8 +407,10 @@ __device__ __forceinline__ void build_state_operand(uint8_t* sm, const float* ve
 
 // ---------------------------------------------------------------- phase 1b: token operands
 // Thread (lane L, part p): token r = L % 64 of the q rows (L >= 64) or k rows (L < 64),
-// channels [32p, 32p + 32).  Writes the tf32 row operand [K_r; Q_r] (TMEM); the k-row
-// thread also writes token r's diagonal-tile column operand and its K_Gamma B operand.
+// channels [32p, 32p + 32).  Writes the tf32 row operand [K_r; Q_r] (TMEM).  The k-row
+// thread also writes token r's diagonal-tile column operand (it holds the reciprocal);
+// the q-row thread writes token r's K_Gamma B operand, which balances the two halves
+// (they run on different SMSPs).
 __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uint32_t tm, int L, int part,
                                               int quarter, int BT)
 {
@@ -421,36 +428,34 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
         const uint4 la = ld_shared_v4(sbase + OFF_G + g_off(r, c0));
         const uint4 lb = ld_shared_v4(sbase + OFF_G + g_off(r, c0 + 4));
         float xv[8], xs[8];
-        {
-            const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
-            xv[0] = a0.x; xv[1] = a0.y; xv[2] = a1.x; xv[3] = a1.y; xv[4] = a2.x; xv[5] = a2.y; xv[6] = a3.x; xv[7] = a3.y;
-            xs[0] = __uint_as_float(la.x); xs[1] = __uint_as_float(la.y); xs[2] = __uint_as_float(la.z);
-            xs[3] = __uint_as_float(la.w); xs[4] = __uint_as_float(lb.x); xs[5] = __uint_as_float(lb.y);
-            xs[6] = __uint_as_float(lb.z); xs[7] = __uint_as_float(lb.w);   // e^{Gamma_r - rho_J} in (0, 1]
-        }
-        float vx[8];
+        unpack8(raw, xv);
+        xs[0] = __uint_as_float(la.x); xs[1] = __uint_as_float(la.y); xs[2] = __uint_as_float(la.z);
+        xs[3] = __uint_as_float(la.w); xs[4] = __uint_as_float(lb.x); xs[5] = __uint_as_float(lb.y);
+        xs[6] = __uint_as_float(lb.z); xs[7] = __uint_as_float(lb.w);   // e^{Gamma_r - rho_J} in (0, 1]
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const float v = valid ? xv[e] : 0.f;
-            vx[e] = v * xs[e];
-            kq[8 * gi + e] = tf32_round(vx[e]);
-            xv[e] = v;
+            xv[e] = valid ? xv[e] : 0.f;
+            kq[8 * gi + e] = tf32_round(xv[e] * xs[e]);
         }
-        if (!isq) {
+        if (!isq) {   // diagonal-tile column operand of reference J: k_r e^{rho_J - Gamma_r} <= e^{80} |k_r|
             float xr[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xr[e] = rcpf(xs[e]);     // e^{rho_J - Gamma_r} <= e^{80}
-            // diagonal-tile column operand of reference J, and the K_Gamma B operand
-            const float4 e4a = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
-            const float4 e4b = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
+            for (int e = 0; e < 8; ++e) xr[e] = rcpf(xs[e]);
             const uint32_t rj = kc_row(J) + r;
             st_shared_f4(kc + sw128_off_f32(rj, c0, KC_ROWS), tf32_round(xv[0] * xr[0]), tf32_round(xv[1] * xr[1]),
                          tf32_round(xv[2] * xr[2]), tf32_round(xv[3] * xr[3]));
             st_shared_f4(kc + sw128_off_f32(rj, c0 + 4, KC_ROWS), tf32_round(xv[4] * xr[4]),
                          tf32_round(xv[5] * xr[5]), tf32_round(xv[6] * xr[6]), tf32_round(xv[7] * xr[7]));
-            st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), pack_bf16x2(vx[0] * e4a.x, vx[1] * e4a.y),
-                         pack_bf16x2(vx[2] * e4a.z, vx[3] * e4a.w), pack_bf16x2(vx[4] * e4b.x, vx[5] * e4b.y),
-                         pack_bf16x2(vx[6] * e4b.z, vx[7] * e4b.w));
+        } else {      // K_Gamma B operand: k_r e^{Gamma_r} = k_r x_r E_J (bf16)
+            float kv[8];
+            unpack8(ld_shared_v4(sbase + OFF_K + sw128_chunk(r, c0 >> 3, 64)), kv);
+            const float4 e4a = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
+            const float4 e4b = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
+            const float ev[8] = {e4a.x, e4a.y, e4a.z, e4a.w, e4b.x, e4b.y, e4b.z, e4b.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) kv[e] = valid ? kv[e] * xs[e] * ev[e] : 0.f;
+            st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), pack_bf16x2(kv[0], kv[1]),
+                         pack_bf16x2(kv[2], kv[3]), pack_bf16x2(kv[4], kv[5]), pack_bf16x2(kv[6], kv[7]));
         }
     }
     tmem_st32(tmem_addr(tm, 32 * quarter, TM_KQ + 32 * part), kq);
@@ -479,10 +484,12 @@ __device__ __forceinline__ void phase3_readout(uint8_t* sm, uint32_t tm, int L, 
     for (int i = 0; i < 16; ++i) row[i] = (part <= J) ? ((J == j0) ? va[i] : vb[i]) : 0.f;
     uint32_t hi[8], lo[8];
     if (!isP) {
-        float* sA = reinterpret_cast<float*>(sm + OFF_X + X_SA);
+        const uint32_t arow = smem_u32(sm) + OFF_X + X_SA + 4u * (r * LDA + 16 * part);
         const float b = sbeta[r];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sA[r * LDA + 16 * part + i] = (16 * part + i < r) ? b * row[i] : 0.f;
+        for (int i = 0; i < 16; ++i) row[i] = (16 * part + i < r) ? b * row[i] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_shared_f4(arow + 16u * q, row[4 * q], row[4 * q + 1], row[4 * q + 2], row[4 * q + 3]);
 #pragma unroll
         for (int i = 0; i < 8; ++i) hi[i] = lo[i] = 0u;
     } else {
@@ -497,7 +504,8 @@ __device__ __forceinline__ void phase3_readout(uint8_t* sm, uint32_t tm, int L, 
 }
 
 // ---------------------------------------------------------------- phase 3: T = (I + A)^-1
-// Threads 0..kSolveThreads-1 (named barrier 1).  sT must be zero on entry.  16x16 diagonal blocks by forward
+// Threads 0..kSolveThreads-1 (named barrier 1).  Writes the blocks on and below the block diagonal of sT
+// (the rest is never read).  16x16 diagonal blocks by forward
 // substitution (block m on warp m, one lane per column), then block levels d = 1..3:
 //   T_{m,m-d} = -T_{m,m} sum_{p=m-d}^{m-1} A_{m,p} T_{p,m-d}.
 template <int D>
@@ -579,17 +587,22 @@ __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
 }
 
 // Tb = T diag(beta) as bf16 hi + lo MN-major B operands [64 i][64 j] (512 threads,
-// one 8-column chunk each).
+// one 8-column chunk each).  The solve writes only the blocks on and below the block
+// diagonal; the chunks above it are zeros here.
 __device__ __forceinline__ void phase3_tb_operands(uint8_t* sm, int t, const float* sbeta)
 {
-    const float* sT = reinterpret_cast<const float*>(sm + OFF_X + X_ST);
     const uint32_t sbase = smem_u32(sm);
     const int i = t >> 3, ch = t & 7;   // row i, 8-column chunk ch
-    uint32_t hi[4], lo[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int j = 8 * ch + 2 * e;
-        split_bf16x2(sT[i * LDA + j] * sbeta[j], sT[i * LDA + j + 1] * sbeta[j + 1], hi[e], lo[e]);
+    uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+    if ((ch >> 1) <= (i >> 4)) {
+        const uint32_t trow = sbase + OFF_X + X_ST + 4u * (i * LDA + 8 * ch);
+        const float4 t0 = ld_shared_f4(trow), t1 = ld_shared_f4(trow + 16u);
+        const float4 b0 = *reinterpret_cast<const float4*>(sbeta + 8 * ch);
+        const float4 b1 = *reinterpret_cast<const float4*>(sbeta + 8 * ch + 4);
+        split_bf16x2(t0.x * b0.x, t0.y * b0.y, hi[0], lo[0]);
+        split_bf16x2(t0.z * b0.z, t0.w * b0.w, hi[1], lo[1]);
+        split_bf16x2(t1.x * b1.x, t1.y * b1.y, hi[2], lo[2]);
+        split_bf16x2(t1.z * b1.z, t1.w * b1.w, hi[3], lo[3]);
     }
     st_shared_v4(sbase + OFF_X + X_TBH + sw128_chunk(i, ch, 64), hi[0], hi[1], hi[2], hi[3]);
     st_shared_v4(sbase + OFF_X + X_TBL + sw128_chunk(i, ch, 64), lo[0], lo[1], lo[2], lo[3]);
@@ -782,11 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         mma_par ^= 1u;
         tc_fence_after_sync();
 
-        // ---- phase 3: clear T; A/P read-out; solve; M = P Tb by MMA; [Tb; M] hi/lo into TMEM
-        {
-            float* sT = reinterpret_cast<float*>(sm + OFF_X + X_ST);
-            for (int idx = t; idx < 64 * LDA; idx += kThreads) sT[idx] = 0.f;
-        }
+        // ---- phase 3: A/P read-out; solve; M = P Tb by MMA; [Tb; M] hi/lo into TMEM
         phase3_readout(sm, tm, L, quarter, part, sbeta);
         tmem_wait_st();
         tc_fence_before_sync();
