@@ -76,3 +76,38 @@ def test_multi_token_decode_through_prefill(cuda_lib):
     assert cuda_lib.last_device_status() == cuda_lib.KDA_OK
     check("draft outputs", out, ref_o, 2e-2)
     check("state after drafts", state, ref_s, 2e-2)
+
+
+def test_draft_verify_then_accept_prefix(cuda_lib):
+    """Speculative verification: K drafts per sequence run from the current state into a
+    separate buffer (the current state is untouched, so rejecting is free); accepting
+    a_b <= K drafts of sequence b is one more call over those tokens, a_b = 0 included."""
+    B, H, D, K = 12, 4, 128, 4
+    cfg = W.DecodeConfig("drafts", B, H, D, D, torch.bfloat16, K)
+    inp = W.make_decode_inputs(cfg, seed=24)
+    pack = lambda x: x.transpose(0, 1).reshape(B * K, *x.shape[2:]).contiguous()
+    q, k, v, g, beta = (pack(inp[n]) for n in ("q", "k", "v", "g", "beta"))
+    cu = np.arange(0, B * K + 1, K, dtype=np.int32)
+    ref_o, _ = oracle.recurrent(q, k, v, g, beta, cu, inp["state0"])
+    state = inp["state0"].cuda()
+    scratch = torch.full_like(state, float("nan"))
+    out, _ = cuda_lib.prefill(q.cuda(), k.cuda(), v.cuda(), g.cuda(), beta.cuda(),
+                              torch.from_numpy(cu).cuda(), state, final_state=scratch)
+    torch.cuda.synchronize()
+    check("draft outputs", out, ref_o, 2e-2)
+    assert torch.equal(state.cpu(), inp["state0"]), "the current state must not change while verifying"
+    # accept a_b tokens of sequence b
+    acc = [b % (K + 1) for b in range(B)]
+    rows = np.concatenate([np.arange(b * K, b * K + a) for b, a in enumerate(acc)]).astype(np.int64)
+    cu_a = np.concatenate([[0], np.cumsum(acc)]).astype(np.int32)
+    sel = lambda x: x[torch.from_numpy(rows)].contiguous()
+    qa, ka, va, ga, ba = (sel(x) for x in (q, k, v, g, beta))
+    _, ref_s = oracle.recurrent(qa, ka, va, ga, ba, cu_a, inp["state0"])
+    cuda_lib.prefill(qa.cuda(), ka.cuda(), va.cuda(), ga.cuda(), ba.cuda(), torch.from_numpy(cu_a).cuda(), state,
+                     final_state=state)
+    torch.cuda.synchronize()
+    assert cuda_lib.last_device_status() == cuda_lib.KDA_OK
+    check("state after accepted drafts", state, ref_s, 2e-2)
+    for b, a in enumerate(acc):
+        if a == 0:
+            assert torch.equal(state[b].cpu(), inp["state0"][b]), b
