@@ -27,8 +27,9 @@
 // lives in tensor memory for the whole sequence.  Per chunk:
 //   1  g cumsum per channel; decayed operands to TMEM (A operands) and shared
 //      memory (B operands); TMA prefetch of the next chunk's v.
-//   2  A and P by one tf32 MMA over the four sub-tile references side by side.
-//   3  T = (I + A)^-1 in fp32 on CUDA cores (6 warps) while 8 other warps build K~^T;
+//   2  A and P by one tf32 MMA over the four sub-tile references side by side, while
+//      all warps build K~^T (TMEM).
+//   3  T = (I + A)^-1 in fp32 on CUDA cores (8 warps);
 //      M = P Tb by three bf16 MMAs (hi/lo splits).
 //   4  [Wk; M K_Gamma] by MMA while the state's bf16 B operand is built (and S decayed);
 //      then the [-Wk; Q'] operand; TMA prefetch of the next
@@ -65,7 +66,7 @@ constexpr uint32_t X_SA = 0;           // A fp32 [64][68]; after the solve: Tb h
 constexpr uint32_t X_TBH = 0;          // Tb hi, MN-major B [64 i][64 j] bf16 (8 KB)
 constexpr uint32_t X_TBL = 8192;       // Tb lo
 constexpr uint32_t X_ST = 17408;       // T fp32 [64][68]
-constexpr uint32_t X_SY = 34816;       // level scratch fp32 [3][16][20]
+constexpr uint32_t X_SY = 34816;       // solve scratch fp32 [32][LDY]
 constexpr uint32_t X_OST = 65536;      // O staging, dv columns 0-63: 2 x [64 tok][32] fp32 boxes (phase 5,
                                        // after the MMA that reads S bf16 has completed)
 constexpr uint32_t X_SB = 40960;       // S bf16, MN-major B [128 dk][128 dv] (phase 4)
@@ -78,7 +79,7 @@ constexpr uint32_t OFF_BAR = OFF_BETA + 256;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr size_t SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
 constexpr int LDA = 68;    // fp32 row stride of A and T: 16-byte aligned rows
-constexpr int LDY = 20;    // row stride of the level scratch
+constexpr int LDY = 36;    // row stride of the solve scratch: 16-byte aligned rows
 
 // fp32 column operand of the A/P MMA: one K-major tile of 160 rows (4 blocks of 32
 // channels, block stride 160 * 128 bytes); reference m owns rows [8 m (m+1), 8 (m+1)(m+2)).
@@ -105,9 +106,9 @@ constexpr uint32_t TM_D1 = 128;   // [W; O] accumulator (phase 5)
 constexpr uint32_t TM_AP = 256;   // A/P accumulators, sub-tile m at 256 + 16 m (m+1) / 2 (phases 2-3)
 constexpr uint32_t TM_TPH = 256;  // [Tb; M] hi, bf16 pairs (phases 3-5)
 constexpr uint32_t TM_TPL = 288;  // [Tb; M] lo (phases 3-5)
-constexpr uint32_t TM_KTL = 320;  // K~^T lo (phases 4-5)
-constexpr uint32_t TM_A1 = 416;   // [-Wk; Q_Gamma then Q'] bf16 pairs (phases 1-5)
-constexpr uint32_t TM_KT = 480;   // K~^T hi, lane = key channel, bf16 pairs (phases 4-5)
+constexpr uint32_t TM_A1 = 320;   // [-Wk; Q'] bf16 pairs (phases 4-5)
+constexpr uint32_t TM_KTL = 416;  // K~^T lo (phases 2-5)
+constexpr uint32_t TM_KT = 480;   // K~^T hi, lane = key channel, bf16 pairs (phases 2-5)
 constexpr uint32_t TM_COLS = 512;
 
 __host__ __device__ constexpr uint32_t tm_ap(int m) { return TM_AP + 8u * m * (m + 1); }
@@ -244,7 +245,7 @@ __device__ __forceinline__ void named_sync(int id, int n)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
-constexpr int kSolveThreads = 192;   // warps 0-5 run the solve
+constexpr int kSolveThreads = 256;   // warps 0-7 run the solve
 
 // Every thread waits on `bar` (bounded); returns false for all threads if any gave up.
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* s_abort)
@@ -332,14 +333,15 @@ __device__ __forceinline__ void phase1_factors(float* vec, int c)
 // For reference m and token i of an earlier sub-tile J < m, the column operand is
 // k_i e^{rho_m - Gamma_i} = (k_i e^{rho_J - Gamma_i}) e^{rho_m - rho_J}: the stored
 // diagonal-tile row of token i times a per-channel factor.  Thread t covers token offset
-// i16 = (t / 32) % 16 and channels [4 (t % 32), +4) of all six (m, J) pairs; the row of
-// each pair is a compile-time offset from the thread's own swizzled base.
+// i16 = t % 16 and channels [4 cq, 4 cq + 4), cq = t / 16, of all six (m, J) pairs (a
+// warp: 16 tokens x 2 channel quads, so its factor loads are broadcasts); the row of each
+// pair is a compile-time offset from the thread's own swizzled base.
 __device__ __forceinline__ void phase1_offdiag(uint8_t* sm, const float* vec, int t)
 {
-    const int i16 = (t >> 5) & 15, c0 = 4 * (t & 31);
+    const int i16 = t & 15, cq = (t >> 4) & 31, c0 = 4 * cq;
     // sw128_off_f32(row, c0, KC_ROWS) with row % 8 == i16 % 8 for every row used below
-    const uint32_t base = smem_u32(sm) + OFF_X + ((t & 31) >> 3) * (KC_ROWS * 128u) + i16 * 128u +
-                          ((uint32_t)((t & 7) ^ (i16 & 7)) << 4);
+    const uint32_t base = smem_u32(sm) + OFF_X + (cq >> 3) * (KC_ROWS * 128u) + i16 * 128u +
+                          ((uint32_t)((cq & 7) ^ (i16 & 7)) << 4);
 #pragma unroll
     for (int b = 0; b < 6; ++b) {
         const int m = (b == 0) ? 1 : ((b < 3) ? 2 : 3);
@@ -352,34 +354,32 @@ __device__ __forceinline__ void phase1_offdiag(uint8_t* sm, const float* vec, in
     }
 }
 
-// ---------------------------------------------------------------- phase 3 side work: K~^T into TMEM
+// ---------------------------------------------------------------- phase 2 side work: K~^T into TMEM
 // Lane c of the K~^T operand holds K~[r][c] = k[r][c] e^{Gamma_63 - Gamma_r}, two tokens
-// per column, as a bf16 hi + lo pair; this thread covers tokens [32 hh, 32 hh + 32).
-__device__ __forceinline__ void build_ktilde(uint8_t* sm, const float* vec, uint32_t tm, int c, int hh, int quarter,
+// per column, as a bf16 hi + lo pair; this thread covers sub-tile J = part (tokens
+// [16 J, 16 J + 16)), where e^{Gamma_63 - Gamma_r} = d_J g_J / x_r.
+__device__ __forceinline__ void build_ktilde(uint8_t* sm, const float* vec, uint32_t tm, int c, int part, int quarter,
                                              int BT)
 {
-    uint32_t hi[16], lo[16];
+    uint32_t hi[8], lo[8];
     const uint32_t kbase = smem_u32(sm + OFF_K);
-    // e^{Gamma_63 - Gamma_r} = e^{Gamma_63 - rho_J} / x_r with e^{Gamma_63 - rho_J} = d_J g_J
-    const float fJ[2] = {vec[(V_D + 2 * hh) * 128 + c] * vec[(V_G + 2 * hh) * 128 + c],
-                         vec[(V_D + 2 * hh + 1) * 128 + c] * vec[(V_G + 2 * hh + 1) * 128 + c]};
+    const float fJ = vec[(V_D + part) * 128 + c] * vec[(V_G + part) * 128 + c];
 #pragma unroll
-    for (int pr = 0; pr < 16; ++pr) {
+    for (int pr = 0; pr < 8; ++pr) {
         float f2[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int rr = 2 * pr + e, r = 32 * hh + rr, jj = rr >> 4;
+            const int r = 16 * part + 2 * pr + e;
             const float x = *reinterpret_cast<const float*>(sm + OFF_G + g_off(r, c));
-            const float fac = fJ[jj] * rcpf(x);
             unsigned short kb;
             asm volatile("ld.shared.u16 %0, [%1];" : "=h"(kb) : "r"(kbase + sw128_off(r, c, 64)));
             const float kv = (r < BT) ? __uint_as_float(((uint32_t)kb) << 16) : 0.f;
-            f2[e] = kv * fac;
+            f2[e] = kv * (fJ * rcpf(x));
         }
         split_bf16x2(f2[0], f2[1], hi[pr], lo[pr]);
     }
-    tmem_st16u(tmem_addr(tm, 32 * quarter, TM_KT + 16 * hh), hi);
-    tmem_st16u(tmem_addr(tm, 32 * quarter, TM_KTL + 16 * hh), lo);
+    tmem_st8u(tmem_addr(tm, 32 * quarter, TM_KT + 8 * part), hi);
+    tmem_st8u(tmem_addr(tm, 32 * quarter, TM_KTL + 8 * part), lo);
 }
 
 // ---------------------------------------------------------------- phase 4 side work: S operand
@@ -504,86 +504,129 @@ __device__ __forceinline__ void phase3_readout(uint8_t* sm, uint32_t tm, int L, 
 }
 
 // ---------------------------------------------------------------- phase 3: T = (I + A)^-1
-// Threads 0..kSolveThreads-1 (named barrier 1).  Writes the blocks on and below the block diagonal of sT
-// (the rest is never read).  16x16 diagonal blocks by forward
-// substitution (block m on warp m, one lane per column), then block levels d = 1..3:
-//   T_{m,m-d} = -T_{m,m} sum_{p=m-d}^{m-1} A_{m,p} T_{p,m-d}.
-template <int D>
-__device__ __forceinline__ void solve_level(const float* sA, float* sT, float* sY, int t)   // t < kSolveThreads
-{
-    constexpr int NBLK = 4 - D;
-    // Y_{m,J} = sum_{p=J}^{m-1} A_{m,p} T_{p,J}, J = m - D; each thread 4 adjacent columns
-    if (t < NBLK * 64) {
-        const int bk = t >> 6, i = (t >> 2) & 15, j4 = (t & 3) * 4;
-        const int m = bk + D, J = m - D;
-        const float* arow = sA + (16 * m + i) * LDA + 16 * J;
-        const float* tb = sT + (16 * J) * LDA + 16 * J + j4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acc2 = acc;
-#pragma unroll
-        for (int q = 0; q < 16 * D; q += 2) {
-            const float a0 = arow[q], a1 = arow[q + 1];
-            const float4 t0 = *reinterpret_cast<const float4*>(tb + q * LDA);
-            const float4 t1 = *reinterpret_cast<const float4*>(tb + (q + 1) * LDA);
-            acc.x = fmaf(a0, t0.x, acc.x); acc.y = fmaf(a0, t0.y, acc.y);
-            acc.z = fmaf(a0, t0.z, acc.z); acc.w = fmaf(a0, t0.w, acc.w);
-            acc2.x = fmaf(a1, t1.x, acc2.x); acc2.y = fmaf(a1, t1.y, acc2.y);
-            acc2.z = fmaf(a1, t1.z, acc2.z); acc2.w = fmaf(a1, t1.w, acc2.w);
-        }
-        *reinterpret_cast<float4*>(sY + bk * 16 * LDY + i * LDY + j4) =
-            make_float4(acc.x + acc2.x, acc.y + acc2.y, acc.z + acc2.z, acc.w + acc2.w);
-    }
-    named_sync(1, kSolveThreads);
-    // T_{m,J} = -T_{m,m} Y_{m,J}
-    if (t < NBLK * 64) {
-        const int bk = t >> 6, i = (t >> 2) & 15, j4 = (t & 3) * 4;
-        const int m = bk + D, J = m - D;
-        const float* trow = sT + (16 * m + i) * LDA + 16 * m;
-        const float* y = sY + bk * 16 * LDY + j4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acc2 = acc;
-#pragma unroll
-        for (int q = 0; q < 16; q += 2) {
-            const float a0 = trow[q], a1 = trow[q + 1];
-            const float4 y0 = *reinterpret_cast<const float4*>(y + q * LDY);
-            const float4 y1 = *reinterpret_cast<const float4*>(y + (q + 1) * LDY);
-            acc.x = fmaf(a0, y0.x, acc.x); acc.y = fmaf(a0, y0.y, acc.y);
-            acc.z = fmaf(a0, y0.z, acc.z); acc.w = fmaf(a0, y0.w, acc.w);
-            acc2.x = fmaf(a1, y1.x, acc2.x); acc2.y = fmaf(a1, y1.y, acc2.y);
-            acc2.z = fmaf(a1, y1.z, acc2.z); acc2.w = fmaf(a1, y1.w, acc2.w);
-        }
-        *reinterpret_cast<float4*>(sT + (16 * m + i) * LDA + 16 * J + j4) =
-            make_float4(-(acc.x + acc2.x), -(acc.y + acc2.y), -(acc.z + acc2.z), -(acc.w + acc2.w));
-    }
-    named_sync(1, kSolveThreads);
-}
-
+// Threads 0..kSolveThreads-1 (warps 0-7, named barrier 1).  A is strictly lower triangular
+// (beta folded in), so T is unit lower triangular.  Writes the blocks on and below the
+// block diagonal of sT and zeros in blocks (0,1) and (2,3); nothing else is read.
+//   1  the four 16x16 diagonal blocks by forward substitution (block m on warp m, one lane
+//      per column), while warps 4-7 zero blocks (0,1) and (2,3);
+//   2  the two 32x32 diagonal halves: T_{2b+1,2b} = -T_{2b+1,2b+1} A_{2b+1,2b} T_{2b,2b};
+//   3  the lower half: T[32:64, 0:32] = -H1 A[32:64, 0:32] H0, with H0, H1 the halves.
 __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
 {
     const float* sA = reinterpret_cast<const float*>(sm + OFF_X + X_SA);
     float* sT = reinterpret_cast<float*>(sm + OFF_X + X_ST);
     float* sY = reinterpret_cast<float*>(sm + OFF_X + X_SY);
-    if (t < 128 && (t & 31) < 16) {   // block m on warp m (one per SMSP), column j on lane j
-        const int m = t >> 5, j = t & 15, b = 16 * m;
-        float x[16];
+    if (t < 128) {
+        if ((t & 31) < 16) {
+            const int m = t >> 5, j = t & 15, b = 16 * m;
+            float x[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) x[q] = (q == j) ? 1.f : 0.f;
+            for (int q = 0; q < 16; ++q) x[q] = (q == j) ? 1.f : 0.f;
 #pragma unroll
-        for (int rr = 1; rr < 16; ++rr) {
-            const float* arow = sA + (b + rr) * LDA + b;
-            float a0 = 0.f, a1 = 0.f;
+            for (int rr = 1; rr < 16; ++rr) {
+                const float4* arow4 = reinterpret_cast<const float4*>(sA + (b + rr) * LDA + b);
+                float av[16];
 #pragma unroll
-            for (int i = 0; i < rr; ++i) {
-                if (i & 1) a1 = fmaf(-arow[i], x[i], a1);
-                else a0 = fmaf(-arow[i], x[i], a0);
+                for (int i4 = 0; i4 < 4; ++i4) {
+                    if (4 * i4 < rr) {
+                        const float4 v4 = arow4[i4];
+                        av[4 * i4] = v4.x; av[4 * i4 + 1] = v4.y; av[4 * i4 + 2] = v4.z; av[4 * i4 + 3] = v4.w;
+                    }
+                }
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < rr; ++i) {
+                    if (i & 1) a1 = fmaf(-av[i], x[i], a1);
+                    else a0 = fmaf(-av[i], x[i], a0);
+                }
+                if (rr > j) x[rr] = a0 + a1;
             }
-            if (rr > j) x[rr] = a0 + a1;
-        }
 #pragma unroll
-        for (int q = 0; q < 16; ++q) sT[(b + q) * LDA + b + j] = x[q];
+            for (int q = 0; q < 16; ++q) sT[(b + q) * LDA + b + j] = x[q];
+        }
+    } else {
+        const int u = t - 128, blk = u >> 6, row = (u >> 2) & 15, c4 = 4 * (u & 3);
+        *reinterpret_cast<float4*>(sT + (32 * blk + row) * LDA + 32 * blk + 16 + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     named_sync(1, kSolveThreads);
-    solve_level<1>(sA, sT, sY, t);
-    solve_level<2>(sA, sT, sY, t);
-    solve_level<3>(sA, sT, sY, t);
+    {   // 2a: Y_b = A_{2b+1,2b} T_{2b,2b} (thread: half b, row i, columns j2, j2 + 1)
+        const int b = t >> 7, i = (t >> 3) & 15, j2 = 2 * (t & 7);
+        const int r0 = 32 * b + 16, c0 = 32 * b;
+        const float* arow = sA + (r0 + i) * LDA + c0;
+        const float* tcol = sT + c0 * LDA + c0 + j2;
+        float2 acc = make_float2(0.f, 0.f), acc2 = acc;
+#pragma unroll
+        for (int q = 0; q < 16; q += 2) {
+            const float a0 = arow[q], a1 = arow[q + 1];
+            const float2 t0 = *reinterpret_cast<const float2*>(tcol + q * LDA);
+            const float2 t1 = *reinterpret_cast<const float2*>(tcol + (q + 1) * LDA);
+            acc.x = fmaf(a0, t0.x, acc.x); acc.y = fmaf(a0, t0.y, acc.y);
+            acc2.x = fmaf(a1, t1.x, acc2.x); acc2.y = fmaf(a1, t1.y, acc2.y);
+        }
+        *reinterpret_cast<float2*>(sY + (16 * b + i) * LDY + j2) = make_float2(acc.x + acc2.x, acc.y + acc2.y);
+    }
+    named_sync(1, kSolveThreads);
+    {   // 2b: T_{2b+1,2b} = -T_{2b+1,2b+1} Y_b
+        const int b = t >> 7, i = (t >> 3) & 15, j2 = 2 * (t & 7);
+        const int r0 = 32 * b + 16, c0 = 32 * b;
+        const float* trow = sT + (r0 + i) * LDA + r0;
+        const float* y = sY + 16 * b * LDY + j2;
+        float2 acc = make_float2(0.f, 0.f), acc2 = acc;
+#pragma unroll
+        for (int q = 0; q < 16; q += 2) {
+            const float a0 = trow[q], a1 = trow[q + 1];
+            const float2 y0 = *reinterpret_cast<const float2*>(y + q * LDY);
+            const float2 y1 = *reinterpret_cast<const float2*>(y + (q + 1) * LDY);
+            acc.x = fmaf(a0, y0.x, acc.x); acc.y = fmaf(a0, y0.y, acc.y);
+            acc2.x = fmaf(a1, y1.x, acc2.x); acc2.y = fmaf(a1, y1.y, acc2.y);
+        }
+        *reinterpret_cast<float2*>(sT + (r0 + i) * LDA + c0 + j2) = make_float2(-(acc.x + acc2.x), -(acc.y + acc2.y));
+    }
+    named_sync(1, kSolveThreads);
+    if (t < 128) {   // steps 3a/3b on warps 0-3: row i of the lower half, columns [8 jg, 8 jg + 8)
+        const int i = 8 * (t >> 5) + ((t & 31) >> 2), jg = t & 3;
+        {   // 3a: Y = A[32:64, 0:32] H0
+            const float* arow = sA + (32 + i) * LDA;
+            const float* hcol = sT + 8 * jg;
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const float a = arow[q];
+                const float4 h0 = *reinterpret_cast<const float4*>(hcol + q * LDA);
+                const float4 h1 = *reinterpret_cast<const float4*>(hcol + q * LDA + 4);
+                acc[0] = fmaf(a, h0.x, acc[0]); acc[1] = fmaf(a, h0.y, acc[1]);
+                acc[2] = fmaf(a, h0.z, acc[2]); acc[3] = fmaf(a, h0.w, acc[3]);
+                acc[4] = fmaf(a, h1.x, acc[4]); acc[5] = fmaf(a, h1.y, acc[5]);
+                acc[6] = fmaf(a, h1.z, acc[6]); acc[7] = fmaf(a, h1.w, acc[7]);
+            }
+            *reinterpret_cast<float4*>(sY + i * LDY + 8 * jg) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<float4*>(sY + i * LDY + 8 * jg + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        named_sync(2, 128);
+        {   // 3b: T[32:64, 0:32] = -H1 Y; rows 0-15 of H1 are zero past column 15
+            const float* hrow = sT + (32 + i) * LDA + 32;
+            const float* y = sY + 8 * jg;
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+            const int qn = (i < 16) ? 16 : 32;   // uniform per warp
+#pragma unroll 4
+            for (int q = 0; q < qn; ++q) {
+                const float a = hrow[q];
+                const float4 y0 = *reinterpret_cast<const float4*>(y + q * LDY);
+                const float4 y1 = *reinterpret_cast<const float4*>(y + q * LDY + 4);
+                acc[0] = fmaf(a, y0.x, acc[0]); acc[1] = fmaf(a, y0.y, acc[1]);
+                acc[2] = fmaf(a, y0.z, acc[2]); acc[3] = fmaf(a, y0.w, acc[3]);
+                acc[4] = fmaf(a, y1.x, acc[4]); acc[5] = fmaf(a, y1.y, acc[5]);
+                acc[6] = fmaf(a, y1.z, acc[6]); acc[7] = fmaf(a, y1.w, acc[7]);
+            }
+            *reinterpret_cast<float4*>(sT + (32 + i) * LDA + 8 * jg) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+            *reinterpret_cast<float4*>(sT + (32 + i) * LDA + 8 * jg + 4) =
+                make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
+        }
+    }
 }
 
 // Tb = T diag(beta) as bf16 hi + lo MN-major B operands [64 i][64 j] (512 threads,
@@ -791,6 +834,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                                  ks > 0 ? 1u : 0u);
             umma_commit(bar_mma);
         }
+        build_ktilde(sm, vec, tm, L, part, quarter, BT);   // overlaps the MMA above
+        tmem_wait_st();
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
@@ -801,11 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
-        if (t < kSolveThreads) {
-            phase3_solve(sm, t);
-        } else if (warp >= 8) {   // meanwhile: K~^T
-            build_ktilde(sm, vec, tm, L, (warp - 8) >> 2, quarter, BT);
-        }
+        if (t < kSolveThreads) phase3_solve(sm, t);
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
