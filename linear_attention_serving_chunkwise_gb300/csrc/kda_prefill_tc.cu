@@ -31,9 +31,9 @@
 //      all warps build K~^T (TMEM).
 //   3  T = (I + A)^-1 in fp32 on CUDA cores (8 warps);
 //      M = P Tb by three bf16 MMAs (hi/lo splits).
-//   4  [Wk; M K_Gamma] by MMA while the state's bf16 B operand is built (and S decayed);
-//      then the [-Wk; Q'] operand; TMA prefetch of the next
-//      chunk's q and g (its k is fetched at the end of phase 3).
+//   4  [Wk; -Q'] by MMA onto a -Q_Gamma seed (written at the end of phase 3) while the
+//      state's bf16 B operand is built (and S decayed); then the [-Wk; Q'] operand; TMA
+//      prefetch of the next chunk's q and g (its k is fetched at the end of phase 3).
 //   5  D1 = [Tb; M] V + [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O;
 //      W to shared memory; S += K~^T W by MMA while O is staged in shared memory and
 //      written by TMA bulk stores (direct stores for a sequence's ragged last chunk).
@@ -101,7 +101,7 @@ constexpr uint32_t TM_KQ = 128;   // [K_r; Q_r] tf32 A operand, one fp32 per col
 constexpr uint32_t TM_PH = 128;   // [0; P] hi, bf16 pairs (phase 3)
 constexpr uint32_t TM_PL = 160;   // [0; P] lo (phase 3)
 constexpr uint32_t TM_M = 192;    // M = P Tb accumulator, rows 64-127, 64 columns (phase 3)
-constexpr uint32_t TM_D2 = 128;   // [Wk; M K_Gamma] accumulator (phase 4)
+constexpr uint32_t TM_D2 = 128;   // [Wk; M K_Gamma - Q_Gamma] accumulator (end of phase 3 - phase 4)
 constexpr uint32_t TM_D1 = 128;   // [W; O] accumulator (phase 5)
 constexpr uint32_t TM_AP = 256;   // A/P accumulators, sub-tile m at 256 + 16 m (m+1) / 2 (phases 2-3)
 constexpr uint32_t TM_TPH = 256;  // [Tb; M] hi, bf16 pairs (phases 3-5)
@@ -661,40 +661,38 @@ __device__ __forceinline__ void store_row32_bf16(uint32_t tile, int row, int chu
                      pk[4 * q + 3]);
 }
 
-// Q' row = Q_Gamma - M K_Gamma for token r = L - 64 (lanes 64-127), channels [32p, 32p + 32):
-// Q_Gamma is recomputed in fp32 from the q and cumsum tiles so that the one bf16 rounding
-// happens after the (strongly cancelling) subtraction.
-__device__ __forceinline__ void phase4_qprime(uint8_t* sm, const float* vec, uint32_t tm, int L, int part,
-                                              int quarter, int BT)
+// -Q_Gamma for token r = L - 64 (lanes 64-127) into rows 64-127 of the [Wk; M K_Gamma]
+// accumulator, channels [16p, 16p + 16) and [64 + 16p, 64 + 16p + 16): the MMA then adds
+// M K_Gamma on top, so the strongly cancelling Q' = Q_Gamma - M K_Gamma is formed in fp32
+// and rounded to bf16 once.  Those columns hold only the (consumed) P operands and this
+// thread's own M columns, already read; rows 0-63 of the region are exact zeros (the
+// zero rows of [0; P] and of the M accumulator), so the MMA accumulates onto them.
+__device__ __forceinline__ void phase3_seed_qgamma(uint8_t* sm, const float* vec, uint32_t tm, int L, int part,
+                                                   int quarter, int BT)
 {
     const int r = L - 64, J = r >> 4;
     const bool valid = r < BT;
     const uint32_t sbase = smem_u32(sm);
-    float mk[32];
-    tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 32 * part), mk);
-    tmem_wait_ld();
-    uint32_t pk[16];
 #pragma unroll
-    for (int gi = 0; gi < 4; ++gi) {
-        const int c0 = 32 * part + 8 * gi;
-        const uint4 raw = ld_shared_v4(sbase + OFF_Q + sw128_chunk(r, c0 >> 3, 64));
-        const uint4 la = ld_shared_v4(sbase + OFF_G + g_off(r, c0));
-        const uint4 lb = ld_shared_v4(sbase + OFF_G + g_off(r, c0 + 4));
-        const float4 e4a = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
-        const float4 e4b = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
-        const float2 a0 = bf2_to_f2(raw.x), a1 = bf2_to_f2(raw.y), a2 = bf2_to_f2(raw.z), a3 = bf2_to_f2(raw.w);
-        const float qv[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
-        const float xs[8] = {__uint_as_float(la.x), __uint_as_float(la.y), __uint_as_float(la.z),
-                             __uint_as_float(la.w), __uint_as_float(lb.x), __uint_as_float(lb.y),
-                             __uint_as_float(lb.z), __uint_as_float(lb.w)};
-        const float ev[8] = {e4a.x, e4a.y, e4a.z, e4a.w, e4b.x, e4b.y, e4b.z, e4b.w};
-        float qp[8];
+    for (int g = 0; g < 2; ++g) {
+        const int c0 = 16 * part + 64 * g;
+        uint32_t v[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qp[e] = (valid ? qv[e] * xs[e] * ev[e] : 0.f) - mk[8 * gi + e];
+        for (int h = 0; h < 2; ++h) {
+            const int c = c0 + 8 * h;
+            float qv[8];
+            unpack8(ld_shared_v4(sbase + OFF_Q + sw128_chunk(r, c >> 3, 64)), qv);
+            const float4 xa = ld_shared_f4(sbase + OFF_G + g_off(r, c));
+            const float4 xb = ld_shared_f4(sbase + OFF_G + g_off(r, c + 4));
+            const float4 ea = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c);
+            const float4 eb = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c + 4);
+            const float xe[8] = {xa.x * ea.x, xa.y * ea.y, xa.z * ea.z, xa.w * ea.w,
+                                 xb.x * eb.x, xb.y * eb.y, xb.z * eb.z, xb.w * eb.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) pk[4 * gi + e] = pack_bf16x2(qp[2 * e], qp[2 * e + 1]);
+            for (int e = 0; e < 8; ++e) v[8 * h + e] = __float_as_uint(valid ? -(qv[e] * xe[e]) : 0.f);
+        }
+        tmem_st16u(tmem_addr(tm, 32 * quarter, TM_D2 + c0), v);
     }
-    tmem_st16u(tmem_addr(tm, 32 * quarter, TM_A1 + 16 * part), pk);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -898,19 +896,24 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             for (int i = 0; i < 8; ++i) split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
             tmem_st8u(tmem_addr(tm, 32 * quarter, TM_TPH + 8 * part), hi);
             tmem_st8u(tmem_addr(tm, 32 * quarter, TM_TPL + 8 * part), lo);
+            phase3_seed_qgamma(sm, vec, tm, L, part, quarter, BT);
         }
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
 
-        // ---- phase 4: D2 = [Tb; M] K_Gamma (hi + lo), then A1 = [-Wk; Q']
+        // ---- phase 4: D2 = [0; -Q_Gamma] + [Tb; M] K_Gamma (hi + lo) = [Wk; -Q'], A1 = -D2
         if (t == 0) {
             tc_fence_after_sync();
+            // the q and g tiles of this chunk are no longer read: fetch the next chunk's
+            if (ci + 1 < nchunks) {
+                issue_qg_loads(p, sm, bar_qg, t0 + 64, h);
+                qg_pending = true;
+            }
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPH + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc,
-                                 ks > 0 ? 1u : 0u);
+                umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPH + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPL + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
@@ -922,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        if (quarter < 2) {   // rows 0-63: -Wk, columns [32 part, +32)
+        {   // A1 = -D2 = [-Wk; Q'], columns [32 part, +32)
             float a[32];
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 32 * part), a);
             tmem_wait_ld();
@@ -930,17 +933,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
             tmem_st16u(tmem_addr(tm, 32 * quarter, TM_A1 + 16 * part), pk);
-        } else {             // rows 64-127: Q' = Q_Gamma - M K_Gamma
-            phase4_qprime(sm, vec, tm, L, part, quarter, BT);
         }
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
-        // the q and g tiles of this chunk are no longer read: fetch the next chunk's
-        if (t == 0 && ci + 1 < nchunks) {
-            issue_qg_loads(p, sm, bar_qg, t0 + 64, h);
-            qg_pending = true;
-        }
 
         // ---- phase 5b: D1 = [Tb; M] V (hi + lo) + [-Wk; Q'] S
         if (t == 0) {
