@@ -29,11 +29,12 @@
 //      memory (B operands); TMA prefetch of the next chunk's v.
 //   2  A and P by one tf32 MMA over the four sub-tile references side by side, while
 //      all warps build K~^T (TMEM).
-//   3  T = (I + A)^-1 in fp32 on CUDA cores (8 warps);
+//   3  T = (I + A)^-1 in fp32 on CUDA cores (8 warps) while the other 8 build the
+//      state's bf16 B operand and apply the chunk decay to S;
 //      M = P Tb by three bf16 MMAs (hi/lo splits).
-//   4  [Wk; -Q'] by MMA onto a -Q_Gamma seed (written at the end of phase 3) while the
-//      state's bf16 B operand is built (and S decayed); then the [-Wk; Q'] operand; TMA
-//      prefetch of the next chunk's q and g (its k is fetched at the end of phase 3).
+//   4  [Wk; -Q'] by MMA onto a -Q_Gamma seed (written at the end of phase 3); then the
+//      [-Wk; Q'] operand; TMA prefetch of the next chunk's q and g (its k is fetched at
+//      the end of phase 3).
 //   5  D1 = [Tb; M] V + [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O;
 //      W to shared memory; S += K~^T W by MMA while O is staged in shared memory and
 //      written by TMA bulk stores (direct stores for a sequence's ragged last chunk).
@@ -69,7 +70,7 @@ constexpr uint32_t X_ST = 17408;       // T fp32 [64][68]
 constexpr uint32_t X_SY = 34816;       // solve scratch fp32 [32][LDY]
 constexpr uint32_t X_OST = 65536;      // O staging, dv columns 0-63: 2 x [64 tok][32] fp32 boxes (phase 5,
                                        // after the MMA that reads S bf16 has completed)
-constexpr uint32_t X_SB = 40960;       // S bf16, MN-major B [128 dk][128 dv] (phase 4)
+constexpr uint32_t X_SB = 40960;       // S bf16, MN-major B [128 dk][128 dv] (phases 3-5b)
 constexpr uint32_t X_WH = 0;           // W hi bf16, MN-major B [64 tok][128 dv] (phase 5)
 constexpr uint32_t X_WL = 16384;       // W lo
 constexpr uint32_t OFF_KG = 180224;    // K_Gamma bf16, MN-major B [64 tok][128 ch]
@@ -382,7 +383,7 @@ __device__ __forceinline__ void build_ktilde(uint8_t* sm, const float* vec, uint
     tmem_st8u(tmem_addr(tm, 32 * quarter, TM_KTL + 8 * part), lo);
 }
 
-// ---------------------------------------------------------------- phase 4 side work: S operand
+// ---------------------------------------------------------------- phase 3 side work: S operand
 // Lane c, columns [32 part, 32 part + 32): S -> bf16 MN-major B operand, then
 // S <- gamma_C[c] S (the chunk decay, applied before the state update accumulates).
 __device__ __forceinline__ void build_state_operand(uint8_t* sm, const float* vec, uint32_t tm, int c, int part,
@@ -583,45 +584,58 @@ __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
         *reinterpret_cast<float2*>(sT + (r0 + i) * LDA + c0 + j2) = make_float2(-(acc.x + acc2.x), -(acc.y + acc2.y));
     }
     named_sync(1, kSolveThreads);
-    if (t < 128) {   // steps 3a/3b on warps 0-3: row i of the lower half, columns [8 jg, 8 jg + 8)
-        const int i = 8 * (t >> 5) + ((t & 31) >> 2), jg = t & 3;
-        {   // 3a: Y = A[32:64, 0:32] H0
-            const float* arow = sA + (32 + i) * LDA;
-            const float* hcol = sT + 8 * jg;
-            float acc[8];
+    // steps 3a/3b: thread (row i of the lower half, columns [8 jg, 8 jg + 8), q parity qh); the
+    // two q parities of an output sit 16 lanes apart and are summed with one shuffle.
+    const int lane = t & 31, w = t >> 5;
+    const int jg = lane & 3, i = 4 * w + ((lane >> 2) & 3), qh = lane >> 4;
+    float acc[8];
+    {   // 3a: Y = A[32:64, 0:32] H0
+        const float* arow = sA + (32 + i) * LDA + qh;
+        const float* hcol = sT + qh * LDA + 8 * jg;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const float a = arow[q];
-                const float4 h0 = *reinterpret_cast<const float4*>(hcol + q * LDA);
-                const float4 h1 = *reinterpret_cast<const float4*>(hcol + q * LDA + 4);
-                acc[0] = fmaf(a, h0.x, acc[0]); acc[1] = fmaf(a, h0.y, acc[1]);
-                acc[2] = fmaf(a, h0.z, acc[2]); acc[3] = fmaf(a, h0.w, acc[3]);
-                acc[4] = fmaf(a, h1.x, acc[4]); acc[5] = fmaf(a, h1.y, acc[5]);
-                acc[6] = fmaf(a, h1.z, acc[6]); acc[7] = fmaf(a, h1.w, acc[7]);
-            }
+        for (int k = 0; k < 16; ++k) {
+            const float a = arow[2 * k];
+            const float4 h0 = *reinterpret_cast<const float4*>(hcol + 2 * k * LDA);
+            const float4 h1 = *reinterpret_cast<const float4*>(hcol + 2 * k * LDA + 4);
+            acc[0] = fmaf(a, h0.x, acc[0]); acc[1] = fmaf(a, h0.y, acc[1]);
+            acc[2] = fmaf(a, h0.z, acc[2]); acc[3] = fmaf(a, h0.w, acc[3]);
+            acc[4] = fmaf(a, h1.x, acc[4]); acc[5] = fmaf(a, h1.y, acc[5]);
+            acc[6] = fmaf(a, h1.z, acc[6]); acc[7] = fmaf(a, h1.w, acc[7]);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
+        if (qh == 0) {
             *reinterpret_cast<float4*>(sY + i * LDY + 8 * jg) = make_float4(acc[0], acc[1], acc[2], acc[3]);
             *reinterpret_cast<float4*>(sY + i * LDY + 8 * jg + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
         }
-        named_sync(2, 128);
-        {   // 3b: T[32:64, 0:32] = -H1 Y; rows 0-15 of H1 are zero past column 15
-            const float* hrow = sT + (32 + i) * LDA + 32;
-            const float* y = sY + 8 * jg;
-            float acc[8];
+    }
+    named_sync(1, kSolveThreads);
+    {   // 3b: T[32:64, 0:32] = -H1 Y; rows 0-15 of H1 are zero past column 15
+        const float* hrow = sT + (32 + i) * LDA + 32 + qh;
+        const float* y = sY + qh * LDY + 8 * jg;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-            const int qn = (i < 16) ? 16 : 32;   // uniform per warp
-#pragma unroll 4
-            for (int q = 0; q < qn; ++q) {
-                const float a = hrow[q];
-                const float4 y0 = *reinterpret_cast<const float4*>(y + q * LDY);
-                const float4 y1 = *reinterpret_cast<const float4*>(y + q * LDY + 4);
-                acc[0] = fmaf(a, y0.x, acc[0]); acc[1] = fmaf(a, y0.y, acc[1]);
-                acc[2] = fmaf(a, y0.z, acc[2]); acc[3] = fmaf(a, y0.w, acc[3]);
-                acc[4] = fmaf(a, y1.x, acc[4]); acc[5] = fmaf(a, y1.y, acc[5]);
-                acc[6] = fmaf(a, y1.z, acc[6]); acc[7] = fmaf(a, y1.w, acc[7]);
-            }
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        auto step = [&](int k) {
+            const float a = hrow[2 * k];
+            const float4 y0 = *reinterpret_cast<const float4*>(y + 2 * k * LDY);
+            const float4 y1 = *reinterpret_cast<const float4*>(y + 2 * k * LDY + 4);
+            acc[0] = fmaf(a, y0.x, acc[0]); acc[1] = fmaf(a, y0.y, acc[1]);
+            acc[2] = fmaf(a, y0.z, acc[2]); acc[3] = fmaf(a, y0.w, acc[3]);
+            acc[4] = fmaf(a, y1.x, acc[4]); acc[5] = fmaf(a, y1.y, acc[5]);
+            acc[6] = fmaf(a, y1.z, acc[6]); acc[7] = fmaf(a, y1.w, acc[7]);
+        };
+        if (w < 4) {   // i < 16
+#pragma unroll
+            for (int k = 0; k < 8; ++k) step(k);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) step(k);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
+        if (qh == 0) {
             *reinterpret_cast<float4*>(sT + (32 + i) * LDA + 8 * jg) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
             *reinterpret_cast<float4*>(sT + (32 + i) * LDA + 8 * jg + 4) =
                 make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
@@ -844,7 +858,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
-        if (t < kSolveThreads) phase3_solve(sm, t);
+        if (t < kSolveThreads) {
+            phase3_solve(sm, t);
+        } else {   // meanwhile warps 8-15: the state's bf16 B operand, then S <- gamma_C S
+            build_state_operand(sm, vec, tm, L, 2 * (part - 2), quarter);
+            build_state_operand(sm, vec, tm, L, 2 * (part - 2) + 1, quarter);
+            tmem_wait_st();
+            fence_proxy_async_smem();
+        }
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
@@ -919,9 +940,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPL + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
             umma_commit(bar_mma);
         }
-        build_state_operand(sm, vec, tm, L, part, quarter);   // overlaps the MMA above
-        tmem_wait_st();
-        fence_proxy_async_smem();
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
