@@ -408,10 +408,10 @@ __device__ __forceinline__ void build_state_operand(uint8_t* sm, const float* ve
 
 // ---------------------------------------------------------------- phase 1b: token operands
 // Thread (lane L, part p): token r = L % 64 of the q rows (L >= 64) or k rows (L < 64),
-// channels [32p, 32p + 32).  Writes the tf32 row operand [K_r; Q_r] (TMEM).  The k-row
-// thread also writes token r's diagonal-tile column operand (it holds the reciprocal);
-// the q-row thread writes token r's K_Gamma B operand, which balances the two halves
-// (they run on different SMSPs).
+// channels [32p, 32p + 32).  Writes the tf32 row operand [K_r; Q_r] (TMEM).  Token r's
+// diagonal-tile column operand is split between the k-row and the q-row thread, and the
+// q-row thread also writes its K_Gamma B operand, so that the two halves (which run on
+// different SMSPs) carry the same number of reciprocals.
 __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uint32_t tm, int L, int part,
                                               int quarter, int BT)
 {
@@ -438,23 +438,26 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
             xv[e] = valid ? xv[e] : 0.f;
             kq[8 * gi + e] = tf32_round(xv[e] * xs[e]);
         }
-        if (!isq) {   // diagonal-tile column operand of reference J: k_r e^{rho_J - Gamma_r} <= e^{80} |k_r|
-            float xr[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xr[e] = rcpf(xs[e]);
-            const uint32_t rj = kc_row(J) + r;
-            st_shared_f4(kc + sw128_off_f32(rj, c0, KC_ROWS), tf32_round(xv[0] * xr[0]), tf32_round(xv[1] * xr[1]),
-                         tf32_round(xv[2] * xr[2]), tf32_round(xv[3] * xr[3]));
-            st_shared_f4(kc + sw128_off_f32(rj, c0 + 4, KC_ROWS), tf32_round(xv[4] * xr[4]),
-                         tf32_round(xv[5] * xr[5]), tf32_round(xv[6] * xr[6]), tf32_round(xv[7] * xr[7]));
-        } else {      // K_Gamma B operand: k_r e^{Gamma_r} = k_r x_r E_J (bf16)
+        // diagonal-tile column operand of reference J, k_r e^{rho_J - Gamma_r} <= e^{80} |k_r|:
+        // channels [c0, c0 + 4) from the k-row thread, [c0 + 4, c0 + 8) from the q-row thread
+        const uint32_t rj = kc_row(J) + r;
+        if (!isq) {
+            st_shared_f4(kc + sw128_off_f32(rj, c0, KC_ROWS), tf32_round(xv[0] * rcpf(xs[0])),
+                         tf32_round(xv[1] * rcpf(xs[1])), tf32_round(xv[2] * rcpf(xs[2])),
+                         tf32_round(xv[3] * rcpf(xs[3])));
+        } else {      // and the K_Gamma B operand: k_r e^{Gamma_r} = k_r x_r E_J (bf16)
             float kv[8];
             unpack8(ld_shared_v4(sbase + OFF_K + sw128_chunk(r, c0 >> 3, 64)), kv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) kv[e] = valid ? kv[e] : 0.f;
+            st_shared_f4(kc + sw128_off_f32(rj, c0 + 4, KC_ROWS), tf32_round(kv[4] * rcpf(xs[4])),
+                         tf32_round(kv[5] * rcpf(xs[5])), tf32_round(kv[6] * rcpf(xs[6])),
+                         tf32_round(kv[7] * rcpf(xs[7])));
             const float4 e4a = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
             const float4 e4b = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
             const float ev[8] = {e4a.x, e4a.y, e4a.z, e4a.w, e4b.x, e4b.y, e4b.z, e4b.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) kv[e] = valid ? kv[e] * xs[e] * ev[e] : 0.f;
+            for (int e = 0; e < 8; ++e) kv[e] = kv[e] * xs[e] * ev[e];
             st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), pack_bf16x2(kv[0], kv[1]),
                          pack_bf16x2(kv[2], kv[3]), pack_bf16x2(kv[4], kv[5]), pack_bf16x2(kv[6], kv[7]));
         }
