@@ -7,7 +7,9 @@ T=8192, dk=dv=128, bf16 q/k/v, fp32 g/beta/state, N(0,0.02) initial state,
 fp32 output): every stage of the chunkwise path.  The decode workload (B=256,
 H=96, dk=dv=128, 64 consecutive in-place steps) is timed in the same run and
 reported in the ``decode`` object.  Inputs are larger than L2 (1.41 GB prefill,
-1.61 GB decode state), so no flush is needed between iterations.
+1.61 GB decode state), so no flush is needed between iterations.  ``e2e`` times
+``kda_prefill_host`` from pinned host inputs to pinned host outputs (out and final
+state) every step.
 
 Rank 0 prints one JSON line.  Under torchrun each rank runs its own independent
 copy of the workload (weak scaling, no collective on the data path).
@@ -35,6 +37,7 @@ import kda_workloads as W  # noqa: E402
 
 METRIC = "KDA prefill tokens/s (×tensor-peak %) and decode state GB/s (×HBM-peak %), 1 GB300"
 UNIT = "tokens/s"
+E2E_SEGMENT_TOKENS = 1024
 PREFILL_KERNEL_SRC = ("linear_attention_serving_chunkwise_gb300/csrc/kda_prefill_tc.cu",
                       "linear_attention_serving_chunkwise_gb300/csrc/kda_sm100.cuh")
 
@@ -282,23 +285,24 @@ def run_cuda(args, world, rank, local):
               "frac": achieved_tflops / peaks["bf16_tflops"], "algorithmic_flops_per_launch": alg_flops,
               "uses_tensor_cores": bool(plan["tensor_cores"])}
 
-    # ---------------- end to end: pinned host inputs in, out + final state back, every step
+    # ---------------- end to end: kda_prefill_host from pinned host inputs to pinned host
+    # outputs (out + final state), every step; the library pipelines the copies over
+    # 1024-token rounds against the kernels
     host = {k: (None if v is None else v.to("cpu").pin_memory()) for k, v in d.items()}
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     host_fin = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = host_out.numel() * 4 + host_fin.numel() * 4
     e2e_steps = max(1, min(args.steps, 20))
+    seg = E2E_SEGMENT_TOKENS
+    hdesc = kda.make_desc(cfg.num_seqs, cfg.total_tokens, cfg.num_heads, cfg.dk, cfg.dv,
+                          kda.KDA_BF16 if cfg.qkv_dtype == torch.bfloat16 else kda.KDA_F32)
+    ws = torch.empty(kda.prefill_host_workspace_bytes(hdesc, seg), dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        with torch.cuda.stream(stream):
-            for k_, v_ in host.items():
-                if v_ is not None:
-                    d[k_].copy_(v_, non_blocking=True)
-            kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"], out=out,
-                        final_state=fin, stream=stream)
-            host_out.copy_(out, non_blocking=True)
-            host_fin.copy_(fin, non_blocking=True)
+        kda.prefill_host(host["q"], host["k"], host["v"], host["g"], host["beta"], host["cu_seqlens"],
+                         host["init_state"], out=host_out, final_state=host_fin, segment_tokens=seg,
+                         num_seqs=cfg.num_seqs, workspace=ws, stream=stream)
 
     for _ in range(2):
         e2e_step()
@@ -312,8 +316,9 @@ def run_cuda(args, world, rank, local):
     stream.synchronize()
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
     e2e = {"value": tokens_per_step / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps}
-    del host, host_out, host_fin
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
+           "api": "kda_prefill_host", "segment_tokens": seg}
+    del host, host_out, host_fin, ws
 
     # ---------------- decode: 64 consecutive in-place steps
     dcfg = W.decode_config()

@@ -157,6 +157,41 @@ kda_status kda_prefill_checkpointed(const kda_prefill_desc* desc,
                                     void* stream);
 
 /*
+ * kda_prefill_host -- kda_prefill with q, k, v, g, beta, cu_seqlens, init_state, out and
+ * final_state in HOST memory (same layouts and rules as kda_prefill; the chunkwise form
+ * is the one of llm-atlas K3_RESEARCH.md, Q07).  The call walks the sequences in rounds of
+ * `segment_tokens` tokens per sequence and keeps the state on the device between rounds:
+ * round r's inputs are copied into one of two device staging sets on an upload stream
+ * while round r-1 runs on `stream`, and round r-1's outputs are copied back on a
+ * download stream (streams and events of the library, ordered after prior work on
+ * `stream`).  segment_tokens is a positive multiple of 64, so the chunk boundaries, and
+ * every output and final-state value, equal those of one kda_prefill call.
+ *
+ *   workspace   DEVICE memory of at least kda_prefill_host_workspace_bytes(desc,
+ *               segment_tokens) bytes, 256-byte aligned; clobbered.
+ *   stream      compute stream; when the call returns, `stream` has been made to wait for
+ *               all of its copies and kernels: synchronise it before reading out or
+ *               final_state, or reusing the host inputs.
+ * Host buffers should be pinned (cudaHostAlloc / cudaHostRegister) for the copies to
+ * overlap the kernels; pageable memory gives the same results more slowly.  Calls on one
+ * device are serialised by the library while they enqueue.
+ * Errors: as kda_prefill (cu_seqlens is checked on the host); KDA_ERR_INVALID_ARG for a
+ * segment_tokens that is not a positive multiple of 64 or a misaligned workspace;
+ * KDA_ERR_WORKSPACE for a short one.  Nothing is enqueued when an argument is rejected.
+ */
+size_t kda_prefill_host_workspace_bytes(const kda_prefill_desc* desc, int32_t segment_tokens);
+
+kda_status kda_prefill_host(const kda_prefill_desc* desc,
+                            const void* q, const void* k, const void* v,
+                            const float* g, const float* beta,
+                            const int32_t* cu_seqlens,
+                            const float* init_state,
+                            float* out, float* final_state,
+                            int32_t segment_tokens,
+                            void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
  * kda_decode -- one token per sequence, as a fused O(1) update of each head's
  * state: a single read and a single write of S (llm-atlas K3_RESEARCH.md, Q07
  * "decode keeps the O(1) state update"; section 8 device layer "fused decode").

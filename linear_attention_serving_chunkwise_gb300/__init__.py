@@ -21,6 +21,8 @@ from ._lib import (  # noqa: F401
     load,
     make_desc,
     prefill,
+    prefill_host,
+    prefill_host_workspace_bytes,
     prefill_query,
     prefill_workspace_bytes,
     status_string,

@@ -26,7 +26,8 @@ KDA_BF16 = 1
 
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes", "kda_prefill_query",
-            "kda_prefill", "kda_prefill_checkpointed", "kda_decode", "kda_last_device_status")
+            "kda_prefill", "kda_prefill_checkpointed", "kda_prefill_host_workspace_bytes", "kda_prefill_host",
+            "kda_decode", "kda_last_device_status")
 
 
 class KDAError(RuntimeError):
@@ -72,6 +73,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kda_prefill_checkpointed.restype = ctypes.c_int
     lib.kda_prefill_checkpointed.argtypes = [ctypes.POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                              i32, i32, vp, vp, sz, vp]
+    lib.kda_prefill_host_workspace_bytes.restype = sz
+    lib.kda_prefill_host_workspace_bytes.argtypes = [ctypes.POINTER(PrefillDesc), i32]
+    lib.kda_prefill_host.restype = ctypes.c_int
+    lib.kda_prefill_host.argtypes = [ctypes.POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz,
+                                     vp]
     lib.kda_decode.restype = ctypes.c_int
     lib.kda_decode.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.kda_last_device_status.restype = ctypes.c_int
@@ -162,6 +168,41 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_
                             _stream_handle(stream))
     if check and st != KDA_OK:
         raise KDAError(st, "kda_prefill")
+    return out, final_state
+
+
+def prefill_host_workspace_bytes(desc: PrefillDesc, segment_tokens: int) -> int:
+    return int(load().kda_prefill_host_workspace_bytes(ctypes.byref(desc), int(segment_tokens)))
+
+
+def prefill_host(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_state=None, *,
+                 segment_tokens: int = 1024, num_seqs: Optional[int] = None, want_final: bool = True,
+                 workspace=None, stream=None, check=True, device=None):
+    """KDA prefill through ``kda_prefill_host``: every tensor is a CPU tensor (pinned for
+    the copies to overlap the kernels); ``workspace`` is a CUDA uint8 tensor, allocated if
+    not given.  Asynchronous like the other entry points: the results are in ``out`` /
+    ``final_state`` once ``stream`` (default: the current stream) has been synchronised.
+    Returns (out, final_state)."""
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
+    desc = make_desc(N, T, H, dk, dv, _dtype_code(q))
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=torch.float32, pin_memory=pin)
+    if final_state is None and want_final:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, pin_memory=pin)
+    if workspace is None:
+        need = prefill_host_workspace_bytes(desc, segment_tokens)
+        dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().kda_prefill_host(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                 _ptr(cu_seqlens), _ptr(init_state), _ptr(out), _ptr(final_state),
+                                 int(segment_tokens), ctypes.c_void_p(workspace.data_ptr()), ws_bytes,
+                                 _stream_handle(stream))
+    if check and st != KDA_OK:
+        raise KDAError(st, "kda_prefill_host")
     return out, final_state
 
 

@@ -113,3 +113,51 @@ def test_decode_rejects_bad_arguments_on_host(lib):
 
 def test_library_is_in_tree():
     assert os.path.dirname(LIB) == os.path.dirname(_lib.__file__)
+
+
+def _host_call(lib, desc, seg, cu=None, ws=0x100000, ws_bytes=1 << 40, init=None, fin=None):
+    import numpy as np
+    T, H, dk, dv = desc.total_tokens, desc.num_heads, desc.dk, desc.dv
+    arrs = {n: np.zeros(max(T, 1) * H * d, dtype=np.float32) for n, d in
+            (("q", dk), ("k", dk), ("v", dv), ("g", dk), ("out", dv))}
+    beta = np.zeros(max(T, 1) * H, dtype=np.float32)
+    p = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    return lib.kda_prefill_host(ctypes.byref(desc), p(arrs["q"]), p(arrs["k"]), p(arrs["v"]), p(arrs["g"]), p(beta),
+                                p(cu), p(init), p(arrs["out"]), p(fin), seg, _fake(ws), ws_bytes, None)
+
+
+def test_prefill_host_rejects_bad_arguments_on_host(lib):
+    """kda_prefill_host checks everything on the host before its first CUDA call."""
+    import numpy as np
+    d = kda.make_desc(2, 256, 2, 64, 64, kda.KDA_F32)
+    need = kda.prefill_host_workspace_bytes(d, 128)
+    assert need > 0
+    for seg in (0, -64, 100, 65):
+        assert _host_call(lib, d, seg, ws_bytes=need) == kda.KDA_ERR_INVALID_ARG
+    assert _host_call(lib, d, 128, ws_bytes=need - 1) == kda.KDA_ERR_WORKSPACE
+    assert _host_call(lib, d, 128, ws=0x100010, ws_bytes=need) == kda.KDA_ERR_INVALID_ARG   # misaligned
+    bad_cu = [np.array([0, 200, 100], dtype=np.int32), np.array([1, 100, 256], dtype=np.int32),
+              np.array([0, 100, 255], dtype=np.int32)]
+    for cu in bad_cu:
+        assert _host_call(lib, d, 128, cu=cu, ws_bytes=need) == kda.KDA_ERR_INVALID_ARG
+    assert _host_call(lib, kda.make_desc(3, 256, 2, 64, 64, kda.KDA_F32), 128, ws_bytes=1 << 40) == \
+        kda.KDA_ERR_INVALID_ARG   # equal split needs T % N == 0
+    assert _host_call(lib, kda.make_desc(1, 64, 2, 96, 96, kda.KDA_F32), 128) == kda.KDA_ERR_UNSUPPORTED
+    # final_state overlapping the initial state (but not identical) is rejected
+    st = np.zeros(2 * 2 * 64 * 64 + 16, dtype=np.float32)
+    init = st[:2 * 2 * 64 * 64]
+    fin = st[16:]
+    assert _host_call(lib, d, 128, ws_bytes=need, init=init, fin=fin) == kda.KDA_ERR_INVALID_ARG
+    assert _host_call(lib, kda.make_desc(0, 0, 2, 64, 64, kda.KDA_F32), 128) == kda.KDA_OK
+
+
+def test_prefill_host_workspace_bytes():
+    d = kda.make_desc(2, 1000, 4, 128, 128, kda.KDA_BF16)
+    state = 2 * 4 * 128 * 128 * 4
+    per_token = 4 * (2 * 128 * 2 + 128 * 2 + 128 * 4 + 4 + 128 * 4)
+    w64, w128, w4k = (kda.prefill_host_workspace_bytes(d, s) for s in (64, 128, 4096))
+    assert w64 >= state + 2 * 128 * per_token and w128 >= state + 2 * 256 * per_token
+    assert w64 < w128 < w4k
+    assert w4k >= state + 2 * 1000 * per_token          # a round never holds more than all tokens
+    assert w4k < state + 2 * 1000 * per_token + 64 * 1024
+    assert kda.prefill_host_workspace_bytes(d, 100) == 0
