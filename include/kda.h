@@ -192,6 +192,30 @@ kda_status kda_prefill_host(const kda_prefill_desc* desc,
                             void* stream);
 
 /*
+ * kda_prefill_host_static -- kda_prefill_host without a caller workspace.  The pages have
+ * no counterpart to this entry point: it is a convenience of this library's host-buffer
+ * path.  The device staging lives in a fixed scratch array inside the library,
+ * KDA_STATIC_SCRATCH_BYTES per device, so the call allocates nothing (no device memory,
+ * no caller buffer).  Same arguments, layouts, results and stream semantics as
+ * kda_prefill_host.  Calls on one device share the scratch, so each call's copies and
+ * kernels run after those of the previous call on that device (whatever its stream).
+ * Errors: as kda_prefill_host, and KDA_ERR_WORKSPACE when
+ * kda_prefill_host_workspace_bytes(desc, segment_tokens) exceeds the scratch (a smaller
+ * segment_tokens, or kda_prefill_host with a workspace, serves larger problems); nothing
+ * is enqueued then.
+ */
+#define KDA_STATIC_SCRATCH_BYTES (64u << 20)
+
+kda_status kda_prefill_host_static(const kda_prefill_desc* desc,
+                                   const void* q, const void* k, const void* v,
+                                   const float* g, const float* beta,
+                                   const int32_t* cu_seqlens,
+                                   const float* init_state,
+                                   float* out, float* final_state,
+                                   int32_t segment_tokens,
+                                   void* stream);
+
+/*
  * kda_decode -- one token per sequence, as a fused O(1) update of each head's
  * state: a single read and a single write of S (llm-atlas K3_RESEARCH.md, Q07
  * "decode keeps the O(1) state update"; section 8 device layer "fused decode").

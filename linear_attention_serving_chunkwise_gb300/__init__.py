@@ -13,6 +13,7 @@ from ._lib import (  # noqa: F401
     KDA_ERR_WORKSPACE,
     KDA_F32,
     KDA_OK,
+    KDA_STATIC_SCRATCH_BYTES,
     KDAError,
     LIB_PATH,
     PrefillDesc,
@@ -22,6 +23,7 @@ from ._lib import (  # noqa: F401
     make_desc,
     prefill,
     prefill_host,
+    prefill_host_static,
     prefill_host_workspace_bytes,
     prefill_query,
     prefill_workspace_bytes,

@@ -27,7 +27,8 @@ KDA_BF16 = 1
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes", "kda_prefill_query",
             "kda_prefill", "kda_prefill_checkpointed", "kda_prefill_host_workspace_bytes", "kda_prefill_host",
-            "kda_decode", "kda_last_device_status")
+            "kda_prefill_host_static", "kda_decode", "kda_last_device_status")
+KDA_STATIC_SCRATCH_BYTES = 64 << 20
 
 
 class KDAError(RuntimeError):
@@ -78,6 +79,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kda_prefill_host.restype = ctypes.c_int
     lib.kda_prefill_host.argtypes = [ctypes.POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz,
                                      vp]
+    lib.kda_prefill_host_static.restype = ctypes.c_int
+    lib.kda_prefill_host_static.argtypes = [ctypes.POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                            vp]
     lib.kda_decode.restype = ctypes.c_int
     lib.kda_decode.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.kda_last_device_status.restype = ctypes.c_int
@@ -203,6 +207,28 @@ def prefill_host(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, f
                                  _stream_handle(stream))
     if check and st != KDA_OK:
         raise KDAError(st, "kda_prefill_host")
+    return out, final_state
+
+
+def prefill_host_static(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_state=None, *,
+                        segment_tokens: int = 128, num_seqs: Optional[int] = None, want_final: bool = True,
+                        stream=None, check=True):
+    """``prefill_host`` through ``kda_prefill_host_static``: the device staging is the
+    library's own scratch (no workspace, no device allocation).  Returns (out, final_state)."""
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
+    desc = make_desc(N, T, H, dk, dv, _dtype_code(q))
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=torch.float32, pin_memory=pin)
+    if final_state is None and want_final:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, pin_memory=pin)
+    st = load().kda_prefill_host_static(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                        _ptr(cu_seqlens), _ptr(init_state), _ptr(out), _ptr(final_state),
+                                        int(segment_tokens), _stream_handle(stream))
+    if check and st != KDA_OK:
+        raise KDAError(st, "kda_prefill_host_static")
     return out, final_state
 
 
