@@ -151,3 +151,44 @@ def test_long_context_chained_calls_sampled(cuda_lib):
     torch.cuda.synchronize()
     assert cuda_lib.last_device_status() == cuda_lib.KDA_OK
     _sampled_check(cuda_lib, cfg, d, out, state, [(0, 3), (0, 50), (0, 95)], 2e-2)
+
+
+@pytest.mark.parametrize("case", ["g_at_bound", "no_decay_beta_one", "beta_zero", "channel_extremes"])
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)], ids=["bf16-128", "fp32-64"])
+def test_decay_and_beta_extremes(cuda_lib, case, dtype, d):
+    """The degenerate corners of the recurrence against the oracle: every g at the bound
+    g_min = -5 (the largest in-tile factors, e^75 within a 16-token sub-tile), no decay with
+    beta = 1 (pure overwrite), beta = 0 (the state only decays; decay scaled down so that it
+    stays within fp32's range), and channels alternating between -5 and 0."""
+    cfg = W.random_prefill_config([200, 77], 3, d, dtype, init="normal")
+    inp = W.make_prefill_inputs(cfg, seed=51)
+    g, beta = inp["g"], inp["beta"]
+    if case == "g_at_bound":
+        g = torch.full_like(g, -5.0)
+    elif case == "no_decay_beta_one":
+        g, beta = torch.zeros_like(g), torch.ones_like(beta)
+    elif case == "beta_zero":
+        # the state only decays: keep the total decay over 200 tokens (~e^-25) inside
+        # fp32's range, or both sides would compare values the GPU cannot represent
+        g, beta = 0.05 * g, torch.zeros_like(beta)
+    else:
+        g = torch.zeros_like(g)
+        g[..., 0::2] = -5.0
+    inp = dict(inp, g=g.contiguous(), beta=beta.contiguous())
+    ref_o, ref_s = oracle_full(inp)
+    dv = to_device(inp)
+    out, fin = cuda_lib.prefill(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"], dv["cu_seqlens"], dv["init_state"])
+    torch.cuda.synchronize()
+    assert cuda_lib.last_device_status() == cuda_lib.KDA_OK
+    tol = tol_for(dtype)
+    if case == "beta_zero" and dtype == torch.bfloat16:
+        # every output is the bf16 read-out of the decayed initial state and the outputs span
+        # ~20x (a sequence's first tokens see the undecayed state): the bar is checked per
+        # output vector o_t, max_j |err| <= 2e-2 * RMS(o_t); the tensor-wide ratio is recorded
+        got = out.detach().cpu().double().numpy()
+        err = np.abs(got - ref_o).max(axis=(1, 2))
+        tok_rms = np.sqrt((ref_o ** 2).mean(axis=(1, 2)))
+        assert np.isfinite(got).all() and (err <= tol * tok_rms).all(), (err / tok_rms).max()
+    else:
+        check(f"{case} out", out, ref_o, tol)
+    check(f"{case} final_state", fin, ref_s, tol)
