@@ -30,10 +30,10 @@
 //   2  A and P by one tf32 MMA over the four sub-tile references side by side, while
 //      all warps build K~^T (TMEM).
 //   3  T = (I + A)^-1 in fp32 on CUDA cores (8 warps) while the other 8 build the
-//      state's bf16 B operand and apply the chunk decay to S;
+//      state's bf16 B operand, apply the chunk decay to S and seed the next
+//      accumulator with [0; -Q_Gamma];
 //      M = P Tb by three bf16 MMAs (hi/lo splits).
-//   4  [Wk; -Q'] by MMA onto a -Q_Gamma seed (written at the end of phase 3); then the
-//      [-Wk; Q'] operand; TMA prefetch of the next chunk's q and g (its k is fetched at
+//   4  [Wk; -Q'] by MMA onto the seed; then the [-Wk; Q'] operand; TMA prefetch of the next chunk's q and g (its k is fetched at
 //      the end of phase 3).
 //   5  D1 = [Tb; M] V + [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O;
 //      W to shared memory; S += K~^T W by MMA while O is staged in shared memory and
@@ -102,13 +102,13 @@ constexpr uint32_t TM_KQ = 128;   // [K_r; Q_r] tf32 A operand, one fp32 per col
 constexpr uint32_t TM_PH = 128;   // [0; P] hi, bf16 pairs (phase 3)
 constexpr uint32_t TM_PL = 160;   // [0; P] lo (phase 3)
 constexpr uint32_t TM_M = 192;    // M = P Tb accumulator, rows 64-127, 64 columns (phase 3)
-constexpr uint32_t TM_D2 = 128;   // [Wk; M K_Gamma - Q_Gamma] accumulator (end of phase 3 - phase 4)
-constexpr uint32_t TM_D1 = 128;   // [W; O] accumulator (phase 5)
+constexpr uint32_t TM_A1 = 128;   // [-Wk; Q'] bf16 pairs (phases 4-5b)
 constexpr uint32_t TM_AP = 256;   // A/P accumulators, sub-tile m at 256 + 16 m (m+1) / 2 (phases 2-3)
 constexpr uint32_t TM_TPH = 256;  // [Tb; M] hi, bf16 pairs (phases 3-5)
 constexpr uint32_t TM_TPL = 288;  // [Tb; M] lo (phases 3-5)
-constexpr uint32_t TM_A1 = 320;   // [-Wk; Q'] bf16 pairs (phases 4-5)
-constexpr uint32_t TM_KTL = 416;  // K~^T lo (phases 2-5)
+constexpr uint32_t TM_D2 = 320;   // [0; -Q_Gamma] seed, then [Wk; M K_Gamma - Q_Gamma] (phases 3-4)
+constexpr uint32_t TM_D1 = 320;   // [W; O] accumulator (phase 5)
+constexpr uint32_t TM_KTL = 448;  // K~^T lo (phases 2-5)
 constexpr uint32_t TM_KT = 480;   // K~^T hi, lane = key channel, bf16 pairs (phases 2-5)
 constexpr uint32_t TM_COLS = 512;
 
@@ -652,37 +652,44 @@ __device__ __forceinline__ void store_row32_bf16(uint32_t tile, int row, int chu
                      pk[4 * q + 3]);
 }
 
-// -Q_Gamma for token r = L - 64 (lanes 64-127) into rows 64-127 of the [Wk; M K_Gamma]
-// accumulator, channels [16p, 16p + 16) and [64 + 16p, 64 + 16p + 16): the MMA then adds
-// M K_Gamma on top, so the strongly cancelling Q' = Q_Gamma - M K_Gamma is formed in fp32
-// and rounded to bf16 once.  Those columns hold only the (consumed) P operands and this
-// thread's own M columns, already read; rows 0-63 of the region are exact zeros (the
-// zero rows of [0; P] and of the M accumulator), so the MMA accumulates onto them.
-__device__ __forceinline__ void phase3_seed_qgamma(uint8_t* sm, const float* vec, uint32_t tm, int L, int part,
-                                                   int quarter, int BT)
+// Seed of the [Wk; M K_Gamma] accumulator, columns [32p, 32p + 32): zeros in rows 0-63
+// (lanes L < 64) and -Q_Gamma in rows 64-127 (token r = L - 64; rows past the chunk's end
+// stay 0).  The MMA then adds [Tb; M] K_Gamma on top, so the strongly cancelling
+// Q' = Q_Gamma - M K_Gamma is formed in fp32 and rounded to bf16 once.  The seed's
+// columns are free from the A/P read-out on, so it is written during the solve.
+__device__ __forceinline__ void phase3_seed(uint8_t* sm, const float* vec, uint32_t tm, int L, int p, int quarter,
+                                            int BT)
 {
-    const int r = L - 64, J = r >> 4;
-    const bool valid = r < BT;
+    const int r = L - 64, J = (r >> 4) & 3;
+    const bool valid = L >= 64 && r < BT;
     const uint32_t sbase = smem_u32(sm);
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        const int c0 = 16 * part + 64 * g;
+    for (int half = 0; half < 2; ++half) {
         uint32_t v[16];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int c = c0 + 8 * h;
-            float qv[8];
-            unpack8(ld_shared_v4(sbase + OFF_Q + sw128_chunk(r, c >> 3, 64)), qv);
-            const float4 xa = ld_shared_f4(sbase + OFF_G + g_off(r, c));
-            const float4 xb = ld_shared_f4(sbase + OFF_G + g_off(r, c + 4));
-            const float4 ea = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c);
-            const float4 eb = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c + 4);
-            const float xe[8] = {xa.x * ea.x, xa.y * ea.y, xa.z * ea.z, xa.w * ea.w,
-                                 xb.x * eb.x, xb.y * eb.y, xb.z * eb.z, xb.w * eb.w};
+            const int c = 32 * p + 16 * half + 8 * h;
+            if (valid) {
+                float qv[8];
+                unpack8(ld_shared_v4(sbase + OFF_Q + sw128_chunk(r, c >> 3, 64)), qv);
+                const float4 xa = ld_shared_f4(sbase + OFF_G + g_off(r, c));
+                const float4 xb = ld_shared_f4(sbase + OFF_G + g_off(r, c + 4));
+                const float4 ea = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c);
+                const float4 eb = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c + 4);
+                v[8 * h + 0] = __float_as_uint(-(qv[0] * (xa.x * ea.x)));
+                v[8 * h + 1] = __float_as_uint(-(qv[1] * (xa.y * ea.y)));
+                v[8 * h + 2] = __float_as_uint(-(qv[2] * (xa.z * ea.z)));
+                v[8 * h + 3] = __float_as_uint(-(qv[3] * (xa.w * ea.w)));
+                v[8 * h + 4] = __float_as_uint(-(qv[4] * (xb.x * eb.x)));
+                v[8 * h + 5] = __float_as_uint(-(qv[5] * (xb.y * eb.y)));
+                v[8 * h + 6] = __float_as_uint(-(qv[6] * (xb.z * eb.z)));
+                v[8 * h + 7] = __float_as_uint(-(qv[7] * (xb.w * eb.w)));
+            } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[8 * h + e] = __float_as_uint(valid ? -(qv[e] * xe[e]) : 0.f);
+                for (int e = 0; e < 8; ++e) v[8 * h + e] = 0u;
+            }
         }
-        tmem_st16u(tmem_addr(tm, 32 * quarter, TM_D2 + c0), v);
+        tmem_st16u(tmem_addr(tm, 32 * quarter, TM_D2 + 32 * p + 16 * half), v);
     }
 }
 
@@ -837,9 +844,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_after_sync();
         if (t < kSolveThreads) {
             phase3_solve(sm, t);
-        } else {   // meanwhile warps 8-15: the state's bf16 B operand, then S <- gamma_C S
+        } else {   // meanwhile warps 8-15: the state's bf16 B operand, S <- gamma_C S, and the seed
             build_state_operand(sm, vec, tm, L, 2 * (part - 2), quarter);
             build_state_operand(sm, vec, tm, L, 2 * (part - 2) + 1, quarter);
+            phase3_seed(sm, vec, tm, L, 2 * (part - 2), quarter, BT);
+            phase3_seed(sm, vec, tm, L, 2 * (part - 2) + 1, quarter, BT);
             tmem_wait_st();
             fence_proxy_async_smem();
         }
@@ -894,7 +903,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             for (int i = 0; i < 8; ++i) split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
             tmem_st8u(tmem_addr(tm, 32 * quarter, TM_TPH + 8 * part), hi);
             tmem_st8u(tmem_addr(tm, 32 * quarter, TM_TPL + 8 * part), lo);
-            phase3_seed_qgamma(sm, vec, tm, L, part, quarter, BT);
         }
         tmem_wait_st();
         tc_fence_before_sync();
