@@ -102,12 +102,12 @@ constexpr uint32_t TM_KQ = 128;   // [K_r; Q_r] tf32 A operand, one fp32 per col
 constexpr uint32_t TM_PH = 128;   // [0; P] hi, bf16 pairs (phase 3)
 constexpr uint32_t TM_PL = 160;   // [0; P] lo (phase 3)
 constexpr uint32_t TM_M = 192;    // M = P Tb accumulator, rows 64-127, 64 columns (phase 3)
-constexpr uint32_t TM_A1 = 128;   // [-Wk; Q'] bf16 pairs (phases 4-5b)
+constexpr uint32_t TM_D1 = 128;   // [W; O] accumulator: [Tb; M] V from phase 4, + [-Wk; Q'] S in phase 5
 constexpr uint32_t TM_AP = 256;   // A/P accumulators, sub-tile m at 256 + 16 m (m+1) / 2 (phases 2-3)
 constexpr uint32_t TM_TPH = 256;  // [Tb; M] hi, bf16 pairs (phases 3-5)
 constexpr uint32_t TM_TPL = 288;  // [Tb; M] lo (phases 3-5)
 constexpr uint32_t TM_D2 = 320;   // [0; -Q_Gamma] seed, then [Wk; M K_Gamma - Q_Gamma] (phases 3-4)
-constexpr uint32_t TM_D1 = 320;   // [W; O] accumulator (phase 5)
+constexpr uint32_t TM_A1 = 320;   // [-Wk; Q'] bf16 pairs, over the read D2 (phases 4-5b)
 constexpr uint32_t TM_KTL = 448;  // K~^T lo (phases 2-5)
 constexpr uint32_t TM_KT = 480;   // K~^T hi, lane = key channel, bf16 pairs (phases 2-5)
 constexpr uint32_t TM_COLS = 512;
@@ -744,6 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     const uint32_t tm = *tslot;
 
     bool v_pending = false, k_pending = false, qg_pending = false, o_pending = false;   // thread 0 only
+    bool mma_open = false;   // thread 0: MMAs issued after the last commit
     if (t == 0 && nchunks > 0) {
         issue_v_loads(p, sm, bar_v, 0, bos, h);
         issue_k_loads(p, sm, bar_k, bos, h);
@@ -908,7 +909,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_before_sync();
         __syncthreads();
 
-        // ---- phase 4: D2 = [0; -Q_Gamma] + [Tb; M] K_Gamma (hi + lo) = [Wk; -Q'], A1 = -D2
+        // ---- phase 4: D2 = [0; -Q_Gamma] + [Tb; M] K_Gamma (hi + lo) = [Wk; -Q'], A1 = -D2; the
+        // state-independent half of D1, [Tb; M] V (hi + lo), queued right behind it
         if (t == 0) {
             tc_fence_after_sync();
             // the q and g tiles of this chunk are no longer read: fetch the next chunk's
@@ -924,14 +926,25 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             for (int ks = 0; ks < 4; ++ks)
                 umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPL + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
             umma_commit(bar_mma);
+            const uint32_t vb = sbase + ((ci & 1) ? OFF_V1 : OFF_V0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPH + 8 * ks, desc_mnmajor(vb, 64, ks), idesc, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPL + 8 * ks, desc_mnmajor(vb, 64, ks), idesc, 1u);
+            mma_open = true;   // committed with phase 5b's MMAs
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        {   // A1 = -D2 = [-Wk; Q'], columns [32 part, +32)
+        {   // A1 = -D2 = [-Wk; Q'], columns [16 part, +16), written over D2 once every thread has read it
             float a[32];
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 32 * part), a);
             tmem_wait_ld();
+            tc_fence_before_sync();
+            __syncthreads();
+            tc_fence_after_sync();
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
@@ -940,23 +953,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
-
-        // ---- phase 5b: D1 = [Tb; M] V (hi + lo) + [-Wk; Q'] S
+        // ---- phase 5b: D1 += [-Wk; Q'] S (the [Tb; M] V half was queued in phase 4)
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
-            const uint32_t vb = sbase + ((ci & 1) ? OFF_V1 : OFF_V0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPH + 8 * ks, desc_mnmajor(vb, 64, ks), idesc, ks > 0 ? 1u : 0u);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPL + 8 * ks, desc_mnmajor(vb, 64, ks), idesc, 1u);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1 + 8 * ks, desc_mnmajor(sbase + OFF_X + X_SB, 128, ks), idesc,
                                  1u);
             umma_commit(bar_mma);
+            mma_open = false;
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
@@ -1064,6 +1070,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (k_pending) mbar_wait_bounded(bar_k, k_par, kWaitNs);
         if (qg_pending) mbar_wait_bounded(bar_qg, qg_par, kWaitNs);
         mbar_wait_bounded(bar_mma, mma_par, kWaitNs);
+        if (mma_open) {   // MMAs queued behind that commit: commit and wait for them too
+            umma_commit(bar_mma);
+            mbar_wait_bounded(bar_mma, mma_par ^ 1u, kWaitNs);
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
