@@ -6,7 +6,8 @@ One step = one ``kda_prefill`` call over the prefill workload (B=1, H=96,
 T=8192, dk=dv=128, bf16 q/k/v, fp32 g/beta/state, N(0,0.02) initial state,
 fp32 output): every stage of the chunkwise path.  The decode workload (B=256,
 H=96, dk=dv=128, 64 consecutive in-place steps) is timed in the same run and
-reported in the ``decode`` object.  Inputs are larger than L2 (1.41 GB prefill,
+reported in the ``decode`` object, and K = 4 tokens per sequence through one
+``kda_decode_multi`` call in the ``decode_multi`` object.  Inputs are larger than L2 (1.41 GB prefill,
 1.61 GB decode state), so no flush is needed between iterations.  ``e2e`` times
 ``kda_prefill_host`` from pinned host inputs to pinned host outputs (out and final
 state) every step.
@@ -350,6 +351,38 @@ def run_cuda(args, world, rank, local):
               "gpu_launches": dcfg.steps}
     del dd, state
 
+    # ---------------- multi-token decode: K = 4 draft tokens per sequence, same B and H
+    K = 4
+    mm = W.make_decode_inputs(dcfg, seed=rank, device=dev, steps=K)
+    mx = {n: mm[n].transpose(0, 1).contiguous() for n in ("q", "k", "v", "g", "beta")}
+    mstate = mm["state0"]
+    mout = torch.empty((dcfg.batch, K, dcfg.num_heads, dcfg.dv), dtype=torch.float32, device=dev)
+    mcalls = 16
+    for _ in range(3):
+        kda.decode_multi(mx["q"], mx["k"], mx["v"], mx["g"], mx["beta"], mstate, out=mout, stream=stream)
+    stream.synchronize()
+    _barrier(world)
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    m0.record(stream)
+    for _ in range(mcalls):
+        kda.decode_multi(mx["q"], mx["k"], mx["v"], mx["g"], mx["beta"], mstate, out=mout, stream=stream)
+    m1.record(stream)
+    stream.synchronize()
+    mcall_ms = _max_over_ranks(m0.elapsed_time(m1) / mcalls, world)
+    e_in = 2 if dcfg.qkv_dtype == torch.bfloat16 else 4
+    per_head_token = e_in * (2 * dcfg.dk + dcfg.dv) + 4 * dcfg.dk + 4 + 4 * dcfg.dv
+    m_bytes = dcfg.batch * dcfg.num_heads * (2 * dcfg.dk * dcfg.dv * 4 + K * per_head_token)
+    decode_multi = {"workload": f"decode_multi_bf16_b{dcfg.batch}_h{dcfg.num_heads}_k{K}_d{dcfg.dk}",
+                    "tokens_per_call": K, "calls": mcalls, "ms_per_call": mcall_ms,
+                    "tokens_per_s": dcfg.batch * K * world / (mcall_ms / 1e3),
+                    "vs_k_single_steps": (K * dstep_ms) / mcall_ms,
+                    "roofline": {"bound": "hbm", "achieved": m_bytes / (mcall_ms / 1e3) / 1e9,
+                                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                 "frac": m_bytes / (mcall_ms / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                                 "algorithmic_bytes_per_launch": m_bytes},
+                    "gpu_launches": mcalls}
+    del mm, mx, mstate, mout
+
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if plan["tensor_cores"] else "f32", "data": "synthetic",
@@ -358,7 +391,7 @@ def run_cuda(args, world, rank, local):
                        "init_state": "N(0,0.02)", "l2": "inputs larger than L2 (1.41 GB per step), no flush",
                        "parallelism": f"independent problem per GPU x{world}"},
             "roofline": roofline, "tensor": tensor, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": args.steps * plan["kernel_launches"], "decode": decode}
+            "gpu_launches": args.steps * plan["kernel_launches"], "decode": decode, "decode_multi": decode_multi}
     if rank == 0 and world == 1:
         rate, dt, cores, sdesc = oracle_sample(cfg, heads=96, tokens=8192)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sdesc,

@@ -233,6 +233,36 @@ kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, 
                       void* stream);
 
 /*
+ * kda_decode_multi -- K consecutive tokens of each sequence in one pass over each head's
+ * state, for verifying K draft tokens (llm-atlas K3_RESEARCH.md, Q28: the MTP layer tuned
+ * into an EAGLE-3 draft; Q07: O(1) decode update).  Per token the same fused update as
+ * kda_decode; the state stays in registers across the K tokens, so HBM sees one read of
+ * S and at most one write.
+ *
+ * Layouts (B = batch, K = tokens, 1 <= K <= KDA_DECODE_MULTI_MAX_TOKENS):
+ *   q, k     [B, K, H, dk] qkv_dtype;   v [B, K, H, dv] qkv_dtype
+ *   g        [B, K, H, dk] fp32;        beta [B, K, H] fp32
+ *   n_apply  [B] int32 device memory, or NULL (= K for every sequence): the state of
+ *            sequence b is replaced by the state after its first n_apply[b] tokens
+ *            (0 leaves it untouched).  A value outside [0, K] leaves that state untouched
+ *            and makes kda_last_device_status() return KDA_ERR_INVALID_ARG.
+ *   state    [B, H, dk, dv] fp32, read, and written where n_apply[b] > 0
+ *   out      [B, K, H, dv] fp32, o for every token (whatever n_apply says), or NULL
+ * Verification: one call with n_apply = 0 (outputs for all K drafts, state untouched),
+ * then one with n_apply = the accepted count per sequence and out = NULL.
+ * Errors: as kda_decode, plus KDA_ERR_INVALID_ARG for K out of range.
+ */
+#define KDA_DECODE_MULTI_MAX_TOKENS 64
+
+kda_status kda_decode_multi(int32_t batch, int32_t tokens, int32_t num_heads, int32_t dk, int32_t dv,
+                            int32_t qkv_dtype,
+                            const void* q, const void* k, const void* v,
+                            const float* g, const float* beta,
+                            const int32_t* n_apply,
+                            float* state, float* out,
+                            void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of the
  * current device: KDA_OK, KDA_ERR_INVALID_ARG (bad cu_seqlens seen on the
  * device) or KDA_ERR_TIMEOUT (a bounded wait gave up).  KDA_ERR_CUDA if the

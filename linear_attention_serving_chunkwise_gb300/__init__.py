@@ -6,6 +6,7 @@ The compute lives in the CUDA library ``libkda_gb300.so`` behind the C ABI in
 from ._lib import (  # noqa: F401
     EXPORTED,
     KDA_BF16,
+    KDA_DECODE_MULTI_MAX_TOKENS,
     KDA_ERR_CUDA,
     KDA_ERR_INVALID_ARG,
     KDA_ERR_TIMEOUT,
@@ -18,6 +19,7 @@ from ._lib import (  # noqa: F401
     LIB_PATH,
     PrefillDesc,
     decode,
+    decode_multi,
     last_device_status,
     load,
     make_desc,

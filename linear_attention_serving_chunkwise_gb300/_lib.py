@@ -27,7 +27,8 @@ KDA_BF16 = 1
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes", "kda_prefill_query",
             "kda_prefill", "kda_prefill_checkpointed", "kda_prefill_host_workspace_bytes", "kda_prefill_host",
-            "kda_prefill_host_static", "kda_decode", "kda_last_device_status")
+            "kda_prefill_host_static", "kda_decode", "kda_decode_multi", "kda_last_device_status")
+KDA_DECODE_MULTI_MAX_TOKENS = 64
 KDA_STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -84,6 +85,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                             vp]
     lib.kda_decode.restype = ctypes.c_int
     lib.kda_decode.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.kda_decode_multi.restype = ctypes.c_int
+    lib.kda_decode_multi.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.kda_last_device_status.restype = ctypes.c_int
     lib.kda_last_device_status.argtypes = [vp]
     if path is None:
@@ -245,6 +248,22 @@ def decode(q, k, v, g, beta, state, out=None, *, stream=None, check=True):
                            _ptr(state), _ptr(out), _stream_handle(stream))
     if check and st != KDA_OK:
         raise KDAError(st, "kda_decode")
+    return out
+
+
+def decode_multi(q, k, v, g, beta, state, out=None, n_apply=None, *, want_out=True, stream=None, check=True):
+    """K tokens per sequence through ``kda_decode_multi``: q, k [B,K,H,dk], v [B,K,H,dv]
+    (fp32 or bf16); g [B,K,H,dk] fp32; beta [B,K,H] fp32; ``state`` [B,H,dk,dv] fp32 is
+    replaced by the state after the first ``n_apply[b]`` tokens (int32 [B] on the device;
+    None = all K).  Returns out [B,K,H,dv] fp32 (None when ``want_out`` is False)."""
+    B, K, H, dk = q.shape
+    dv = v.shape[3]
+    if out is None and want_out:
+        out = torch.empty((B, K, H, dv), dtype=torch.float32, device=q.device)
+    st = load().kda_decode_multi(B, K, H, dk, dv, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                 _ptr(n_apply), _ptr(state), _ptr(out), _stream_handle(stream))
+    if check and st != KDA_OK:
+        raise KDAError(st, "kda_decode_multi")
     return out
 
 

@@ -225,6 +225,45 @@ kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, 
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status kda_decode_multi(int32_t batch, int32_t tokens, int32_t num_heads, int32_t dk, int32_t dv,
+                            int32_t qkv_dtype, const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const int32_t* n_apply, float* state, float* out, void* stream)
+{
+    if (batch < 0 || num_heads < 1 || tokens < 1 || tokens > KDA_DECODE_MULTI_MAX_TOKENS) return KDA_ERR_INVALID_ARG;
+    if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!supported_dims(dk, dv)) return KDA_ERR_UNSUPPORTED;
+    const size_t BH = (size_t)batch * num_heads;
+    if (BH > 0x7fffffffull || (size_t)batch * tokens * num_heads > 0x7fffffffull) return KDA_ERR_INVALID_ARG;
+    if (BH == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !state) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(state) ||
+        (out && !aligned16(out)))
+        return KDA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(beta) & 3u) || (reinterpret_cast<uintptr_t>(n_apply) & 3u))
+        return KDA_ERR_INVALID_ARG;
+    const size_t BKH = BH * (size_t)tokens;
+    const size_t esz = qkv_dtype == KDA_BF16 ? 2 : 4;
+    const Range r_state = range_of(state, BH * dk * dv * sizeof(float));
+    const Range r_out = range_of(out, out ? BKH * dv * sizeof(float) : 0);
+    const Range ins[] = {range_of(q, BKH * dk * esz), range_of(k, BKH * dk * esz), range_of(v, BKH * dv * esz),
+                         range_of(g, BKH * dk * sizeof(float)), range_of(beta, BKH * sizeof(float)),
+                         range_of(n_apply, n_apply ? (size_t)batch * sizeof(int32_t) : 0)};
+    for (const Range& r : ins) {
+        if (overlaps(r_out, r) || overlaps(r_state, r)) return KDA_ERR_INVALID_ARG;
+    }
+    if (overlaps(r_out, r_state)) return KDA_ERR_INVALID_ARG;
+    int* status = status_ptr_for_current_device();
+    if (!status) return KDA_ERR_CUDA;
+
+    kda::DecodeMultiArgs a;
+    a.batch = batch; a.tokens = tokens; a.num_heads = num_heads; a.dk = dk; a.dv = dv;
+    a.bf16 = qkv_dtype == KDA_BF16;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.n_apply = n_apply;
+    a.state = state; a.out = out; a.status = status;
+    const cudaError_t e = kda::launch_decode_multi(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status kda_last_device_status(void* stream)
 {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;

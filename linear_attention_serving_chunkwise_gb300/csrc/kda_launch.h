@@ -32,11 +32,23 @@ struct DecodeArgs {
     float *state, *out;
 };
 
+struct DecodeMultiArgs {
+    int batch, tokens, num_heads, dk, dv;
+    bool bf16;
+    const void *q, *k, *v;       // [B, K, H, d]
+    const float *g, *beta;       // [B, K, H, dk], [B, K, H]
+    const int32_t* n_apply;      // [B] tokens whose update is kept, or nullptr (= K)
+    float *state, *out;          // [B, H, dk, dv] in place; [B, K, H, dv] or nullptr
+    int* status;                 // device status word
+};
+
 // fp32 CUDA-core chunkwise prefill (any supported shape, fp32 or bf16 inputs)
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 // bf16 tcgen05 chunkwise prefill (dk = dv = 128, T > 0)
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
 // fused single-pass decode
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// K tokens per sequence in one pass over the state
+cudaError_t launch_decode_multi(const DecodeMultiArgs& a, cudaStream_t stream);
 
 }  // namespace kda

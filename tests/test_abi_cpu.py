@@ -161,3 +161,20 @@ def test_prefill_host_workspace_bytes():
     assert w4k >= state + 2 * 1000 * per_token          # a round never holds more than all tokens
     assert w4k < state + 2 * 1000 * per_token + 64 * 1024
     assert kda.prefill_host_workspace_bytes(d, 100) == 0
+
+
+def test_decode_multi_rejects_bad_arguments_on_host(lib):
+    f = _fake
+    base = dict(q=f(0x10000), k=f(0x20000), v=f(0x30000), g=f(0x40000), beta=f(0x50000), n=None,
+                state=f(0x100000), out=f(0x60000))
+    call = lambda B=2, K=2, H=2, d=64, dt=0, **kw: lib.kda_decode_multi(
+        B, K, H, d, d, dt, *[kw.get(n, base[n]) for n in ("q", "k", "v", "g", "beta", "n", "state", "out")], None)
+    assert call(K=0) == kda.KDA_ERR_INVALID_ARG
+    assert call(K=kda.KDA_DECODE_MULTI_MAX_TOKENS + 1) == kda.KDA_ERR_INVALID_ARG
+    assert call(d=96) == kda.KDA_ERR_UNSUPPORTED
+    assert call(dt=5) == kda.KDA_ERR_UNSUPPORTED
+    assert call(q=None) == kda.KDA_ERR_INVALID_ARG
+    assert call(n=f(0x70002)) == kda.KDA_ERR_INVALID_ARG          # misaligned counts
+    assert call(out=f(0x100000)) == kda.KDA_ERR_INVALID_ARG       # out over the state
+    assert call(state=f(0x10000 + 64)) == kda.KDA_ERR_INVALID_ARG  # state over q
+    assert call(B=0) == kda.KDA_OK
