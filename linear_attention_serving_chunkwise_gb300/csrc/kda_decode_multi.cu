@@ -3,138 +3,144 @@
 // "K3_RESEARCH.md", Q28: the MTP layer tuned into an EAGLE-3 draft model; Q07: decode
 // keeps the O(1) state update).
 //
-// The CTAs of one (sequence, head) hold its state in registers for all K tokens: per token
-// the same fused step as single-token decode (S' = Diag(exp g) S; r = S'^T k, p = S'^T q
-// from one pass; w = beta (v - r); S <- S' + k w^T; o = p + (k . q) w).  Outputs are
-// written for every token; the state written back is the one after the first
-// n_apply[b] tokens (0 leaves it untouched), so a verify pass followed by an apply pass
-// for the accepted prefix reads the state twice and writes it once.
+// One CTA per (sequence, head).  Warp w owns the state columns [16 w, 16 w + 16) over all
+// dk rows; lane (rs = lane / 4, cq = lane % 4) holds rows [rs D/8, (rs + 1) D/8) of the
+// float4 column 4 cq in registers for the whole call.  Per token the fused step of
+// single-token decode (S' = Diag(exp g) S; r = S'^T k, p = S'^T q; w = beta (v - r);
+// S <- S' + k w^T; o = p + (k . q) w): every sum runs over dk, i.e. over the 8 lanes of
+// one column, so a step is three shuffle rounds and no CTA barrier.  The K tokens'
+// vectors are staged in shared memory once, behind the only barrier of the kernel.
+// Outputs are written for every token; the state written back is the one after the
+// first n_apply[b] tokens (0 leaves it untouched).
 #include "kda_common.cuh"
 #include "kda_launch.h"
 
 namespace kda {
 namespace {
 
-constexpr int kMultiThreads = 256;
+// shared staging of one token: k, q, e^g in padded 16-row blocks (stride 20 floats, so the
+// 8 row blocks read by one warp fall in different banks), then v, then beta
+template <int D>
+struct MultiLayout {
+    static constexpr int kBlk = 20;                    // floats per 16-row block
+    static constexpr int kVec = D / 16 * kBlk;         // floats of one padded dk vector
+    static constexpr int kTok = 3 * kVec + D + 4;      // floats per token (16-byte multiple)
+    __device__ static int row(int r) { return (r >> 4) * kBlk + (r & 15); }
+};
 
-// SPLIT CTAs share one (sequence, head): CTA `half` owns the dv columns
-// [half D / SPLIT, (half + 1) D / SPLIT) of the state.  Every reduction of the step runs
-// over dk (rows), so the column blocks never exchange data; k . q is formed in each.
-template <typename Tin, int D, int SPLIT>
-__global__ void __launch_bounds__(kMultiThreads, SPLIT == 1 ? 2 : 3) kda_decode_multi_kernel(DecodeMultiArgs a)
+template <typename Tin, int D>
+__global__ void __launch_bounds__(2 * D, 2) kda_decode_multi_kernel(DecodeMultiArgs a)
 {
-    constexpr int DV = D / SPLIT;             // state columns of this CTA
-    constexpr int C4 = DV / 4;                // float4 columns per state row
-    constexpr int RG = kMultiThreads / C4;    // row groups
-    constexpr int RP = D / RG;                // rows per thread
-    static_assert(RG * C4 == kMultiThreads && RP * RG == D, "decode tiling");
+    using Lay = MultiLayout<D>;
+    constexpr int R = D / 8;                  // state rows per lane
+    constexpr int kThreads = 2 * D;           // D / 16 warps of 16 columns
+    extern __shared__ __align__(16) float smv[];
 
-    const int bh = blockIdx.x / SPLIT, half = blockIdx.x % SPLIT;   // bh = b * H + h
+    const int bh = blockIdx.x;                // b * H + h
     const int b = bh / a.num_heads, h = bh % a.num_heads;
-    const int t = threadIdx.x;
-    const int cg = t % C4, rg = t / C4;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int rs = lane >> 2, cq = lane & 3;
     const int K = a.tokens;
-    const int c0 = half * DV;                 // first state column of this CTA
-
-    // token vectors double-buffered by step parity: step j + 1 fills one buffer while no
-    // thread can still read it (three barriers separate it from step j - 1)
-    __shared__ float sk[2][D], sq[2][D], sdec[2][D], sv[2][DV], sw[DV];
-    __shared__ float4 red_r[RG][C4], red_p[RG][C4];
-    __shared__ float s_kq[2], s_beta[2];
+    const int col = 16 * w + 4 * cq;          // first of this lane's 4 state columns
+    const int r0 = rs * R;                    // first of this lane's R rows
 
     int n_apply = K;
     if (a.n_apply) {
         n_apply = a.n_apply[b];
         if (n_apply < 0 || n_apply > K) {
-            if (t == 0 && h == 0 && half == 0) report_status(a.status, kDevBadSeqlens);
+            if (t == 0 && h == 0) report_status(a.status, kDevBadSeqlens);
             n_apply = 0;   // an invalid count leaves the state untouched
         }
     }
 
-    float* S = a.state + (size_t)bh * D * D + c0;
-    float4 s[RP];
+    float* S = a.state + (size_t)bh * D * D + col;
+    float4 s[R];
 #pragma unroll
-    for (int i = 0; i < RP; ++i) s[i] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(rg * RP + i) * D) + cg);
+    for (int i = 0; i < R; ++i) s[i] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(r0 + i) * D));
 
-    // token j's vectors are loaded into registers during step j - 1
-    auto tok_index = [&](int j) { return ((size_t)b * K + j) * a.num_heads + h; };   // [B, K, H, .]
-    float nk = 0.f, nq = 0.f, nv = 0.f, ng = 0.f, nb = 0.f;
-    auto fetch = [&](int j) {
-        const size_t tok = tok_index(j);
-        if (t < D) {
-            nk = to_f32(static_cast<const Tin*>(a.k)[tok * D + t]);
-            nq = to_f32(static_cast<const Tin*>(a.q)[tok * D + t]);
-            ng = a.g[tok * D + t];
-        }
-        if (t < DV) nv = to_f32(static_cast<const Tin*>(a.v)[tok * D + c0 + t]);
-        if (t == 0) nb = a.beta[tok];
-    };
-    fetch(0);
+    // stage every token's vectors (plain loads, all issued before the one barrier)
+    for (int idx = t; idx < K * D; idx += kThreads) {
+        const int j = idx / D, c = idx - j * D;
+        const size_t tok = ((size_t)b * K + j) * a.num_heads + h;   // [B, K, H, .]
+        float* base = smv + j * Lay::kTok;
+        base[Lay::row(c)] = to_f32(static_cast<const Tin*>(a.k)[tok * D + c]);
+        base[Lay::kVec + Lay::row(c)] = to_f32(static_cast<const Tin*>(a.q)[tok * D + c]);
+        base[2 * Lay::kVec + Lay::row(c)] = expf(a.g[tok * D + c]);
+        base[3 * Lay::kVec + c] = to_f32(static_cast<const Tin*>(a.v)[tok * D + c]);
+        if (c == 0) base[3 * Lay::kVec + D] = a.beta[tok];
+    }
+    __syncthreads();
 
     for (int j = 0; j < K; ++j) {
-        const int buf = j & 1;
-        const size_t tok = tok_index(j);
-        if (t < D) {
-            sk[buf][t] = nk;
-            sq[buf][t] = nq;
-            sdec[buf][t] = expf(ng);
-        }
-        if (t < DV) sv[buf][t] = nv;
-        if (t == 0) s_beta[buf] = nb;
-        if (j + 1 < K) fetch(j + 1);
-        __syncthreads();
-        if (t < 32) {
-            float kq = 0.f;
-            for (int c = t; c < D; c += 32) kq += sk[buf][c] * sq[buf][c];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
-            if (t == 0) s_kq[buf] = kq;
-        }
+        const float* base = smv + j * Lay::kTok;
+        const float* kv = base + Lay::row(r0);
+        const float* qv = base + Lay::kVec + Lay::row(r0);
+        const float* dv = base + 2 * Lay::kVec + Lay::row(r0);
         float4 r = make_float4(0.f, 0.f, 0.f, 0.f), p = r;
+        float kq = 0.f;
 #pragma unroll
-        for (int i = 0; i < RP; ++i) {
-            const int row = rg * RP + i;
-            const float d = sdec[buf][row], kc = sk[buf][row], qc = sq[buf][row];
-            s[i].x *= d; s[i].y *= d; s[i].z *= d; s[i].w *= d;
-            r.x += s[i].x * kc; r.y += s[i].y * kc; r.z += s[i].z * kc; r.w += s[i].w * kc;
-            p.x += s[i].x * qc; p.y += s[i].y * qc; p.z += s[i].z * qc; p.w += s[i].w * qc;
-        }
-        red_r[rg][cg] = r;
-        red_p[rg][cg] = p;
-        __syncthreads();
-        if (t < DV) {
-            const float* rr = reinterpret_cast<const float*>(&red_r[0][0]);
-            const float* pp = reinterpret_cast<const float*>(&red_p[0][0]);
-            float rs = 0.f, ps = 0.f;
+        for (int i4 = 0; i4 < R / 4; ++i4) {
+            const float4 k4 = *reinterpret_cast<const float4*>(kv + 4 * i4);
+            const float4 q4 = *reinterpret_cast<const float4*>(qv + 4 * i4);
+            const float4 d4 = *reinterpret_cast<const float4*>(dv + 4 * i4);
+            const float kk[4] = {k4.x, k4.y, k4.z, k4.w}, qq[4] = {q4.x, q4.y, q4.z, q4.w},
+                        dd[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-            for (int gI = 0; gI < RG; ++gI) {
-                rs += rr[gI * DV + t];
-                ps += pp[gI * DV + t];
+            for (int e = 0; e < 4; ++e) {
+                float4& x = s[4 * i4 + e];
+                x.x *= dd[e]; x.y *= dd[e]; x.z *= dd[e]; x.w *= dd[e];
+                r.x += x.x * kk[e]; r.y += x.y * kk[e]; r.z += x.z * kk[e]; r.w += x.w * kk[e];
+                p.x += x.x * qq[e]; p.y += x.y * qq[e]; p.z += x.z * qq[e]; p.w += x.w * qq[e];
+                kq += kk[e] * qq[e];
             }
-            const float w = s_beta[buf] * (sv[buf][t] - rs);
-            sw[t] = w;
-            if (a.out) a.out[tok * D + c0 + t] = ps + s_kq[buf] * w;
         }
-        __syncthreads();
-        const float4 w4 = reinterpret_cast<const float4*>(sw)[cg];
+        // sums over the 8 lanes of each column (lane bits 2-4)
 #pragma unroll
-        for (int i = 0; i < RP; ++i) {
-            const float kc = sk[buf][rg * RP + i];
-            s[i].x += kc * w4.x; s[i].y += kc * w4.y; s[i].z += kc * w4.z; s[i].w += kc * w4.w;
+        for (int o = 4; o < 32; o <<= 1) {
+            r.x += __shfl_xor_sync(0xffffffffu, r.x, o); r.y += __shfl_xor_sync(0xffffffffu, r.y, o);
+            r.z += __shfl_xor_sync(0xffffffffu, r.z, o); r.w += __shfl_xor_sync(0xffffffffu, r.w, o);
+            p.x += __shfl_xor_sync(0xffffffffu, p.x, o); p.y += __shfl_xor_sync(0xffffffffu, p.y, o);
+            p.z += __shfl_xor_sync(0xffffffffu, p.z, o); p.w += __shfl_xor_sync(0xffffffffu, p.w, o);
+            kq += __shfl_xor_sync(0xffffffffu, kq, o);
+        }
+        const float4 v4 = *reinterpret_cast<const float4*>(base + 3 * Lay::kVec + col);
+        const float beta = base[3 * Lay::kVec + D];
+        const float4 w4 = make_float4(beta * (v4.x - r.x), beta * (v4.y - r.y), beta * (v4.z - r.z),
+                                      beta * (v4.w - r.w));
+        if (a.out && rs == 0) {
+            const size_t tok = ((size_t)b * K + j) * a.num_heads + h;
+            *reinterpret_cast<float4*>(a.out + tok * D + col) =
+                make_float4(p.x + kq * w4.x, p.y + kq * w4.y, p.z + kq * w4.z, p.w + kq * w4.w);
+        }
+#pragma unroll
+        for (int i4 = 0; i4 < R / 4; ++i4) {
+            const float4 k4 = *reinterpret_cast<const float4*>(kv + 4 * i4);
+            const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float4& x = s[4 * i4 + e];
+                x.x += kk[e] * w4.x; x.y += kk[e] * w4.y; x.z += kk[e] * w4.z; x.w += kk[e] * w4.w;
+            }
         }
         if (j + 1 == n_apply) {   // the state after the applied prefix
 #pragma unroll
-            for (int i = 0; i < RP; ++i) __stcs(reinterpret_cast<float4*>(S + (size_t)(rg * RP + i) * D) + cg, s[i]);
+            for (int i = 0; i < R; ++i) __stcs(reinterpret_cast<float4*>(S + (size_t)(r0 + i) * D), s[i]);
         }
     }
 }
 
-template <typename Tin, int D, int SPLIT>
+template <typename Tin, int D>
 cudaError_t launch_t(const DecodeMultiArgs& a, cudaStream_t stream)
 {
-    const long long blocks = (long long)a.batch * a.num_heads * SPLIT;
+    const long long blocks = (long long)a.batch * a.num_heads;
     if (blocks == 0) return cudaSuccess;
-    kda_decode_multi_kernel<Tin, D, SPLIT><<<(unsigned)blocks, kMultiThreads, 0, stream>>>(a);
+    const size_t smem = (size_t)a.tokens * MultiLayout<D>::kTok * sizeof(float);
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(kda_decode_multi_kernel<Tin, D>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    kda_decode_multi_kernel<Tin, D><<<(unsigned)blocks, 2 * D, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -142,10 +148,8 @@ cudaError_t launch_t(const DecodeMultiArgs& a, cudaStream_t stream)
 
 cudaError_t launch_decode_multi(const DecodeMultiArgs& a, cudaStream_t stream)
 {
-    // one CTA per (sequence, head): splitting the columns over two CTAs measured slower on
-    // GB300 (0.93 vs 0.83 ms for B = 256, H = 96, K = 4), the per-step barriers dominate
-    if (a.dk == 128) return a.bf16 ? launch_t<__nv_bfloat16, 128, 1>(a, stream) : launch_t<float, 128, 1>(a, stream);
-    return a.bf16 ? launch_t<__nv_bfloat16, 64, 1>(a, stream) : launch_t<float, 64, 1>(a, stream);
+    if (a.dk == 128) return a.bf16 ? launch_t<__nv_bfloat16, 128>(a, stream) : launch_t<float, 128>(a, stream);
+    return a.bf16 ? launch_t<__nv_bfloat16, 64>(a, stream) : launch_t<float, 64>(a, stream);
 }
 
 }  // namespace kda

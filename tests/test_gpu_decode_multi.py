@@ -87,7 +87,8 @@ def test_decode_multi_verify_then_apply(cuda_lib):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
 @pytest.mark.parametrize("D", [64, 128])
 def test_decode_multi_single_token_equals_decode(cuda_lib, dtype, D):
-    """K = 1 is the single-token decode step, bit for bit (same tiling and arithmetic)."""
+    """K = 1 is the single-token decode step up to fp32 summation order (the two kernels
+    split the dk sums differently: per-lane rows then shuffles here, row groups there)."""
     B, H = 16, 4
     x, s0 = _inputs(B, H, D, dtype, 1, seed=72)
     dev = {n: x[n].cuda() for n in x}
@@ -95,7 +96,8 @@ def test_decode_multi_single_token_equals_decode(cuda_lib, dtype, D):
     o_multi = cuda_lib.decode_multi(*(dev[n] for n in ("q", "k", "v", "g", "beta")), s_multi)
     o_one = cuda_lib.decode(*(dev[n][:, 0].contiguous() for n in ("q", "k", "v", "g", "beta")), s_one)
     torch.cuda.synchronize()
-    assert torch.equal(o_multi[:, 0], o_one) and torch.equal(s_multi, s_one)
+    rel = lambda x, y: ((x - y).abs().max() / y.pow(2).mean().sqrt()).item()
+    assert rel(o_multi[:, 0], o_one) < 2e-6 and rel(s_multi, s_one) < 2e-6
 
 
 def test_decode_multi_bad_count_leaves_state(cuda_lib):
