@@ -18,10 +18,9 @@
 // and <= 1 off it.
 //
 // Precision: A and P use tf32 MMAs (operands rounded to nearest tf32 first, since
-// the tensor core truncates); Tb, M and W enter their MMAs as
-// bf16 hi + lo pairs, and so does K~ in the state update; S, Wk, Q' and K_Gamma are
-// single bf16; accumulation and
-// the carried state are fp32.
+// the tensor core truncates); Tb, M and W enter their MMAs as bf16 hi + lo pairs, and
+// so does K~ in the state update; S, Wk, Q' and K_Gamma are single bf16 (Q' rounded
+// once, after its fp32 subtraction); accumulation and the carried state are fp32.
 //
 // One CTA owns one (sequence, head) and walks its chunks in order; the fp32 state
 // lives in tensor memory for the whole sequence.  Per chunk:
@@ -31,13 +30,14 @@
 //      all warps build K~^T (TMEM).
 //   3  T = (I + A)^-1 in fp32 on CUDA cores (8 warps) while the other 8 build the
 //      state's bf16 B operand, apply the chunk decay to S and seed the next
-//      accumulator with [0; -Q_Gamma];
-//      M = P Tb by three bf16 MMAs (hi/lo splits).
-//   4  [Wk; -Q'] by MMA onto the seed; then the [-Wk; Q'] operand; TMA prefetch of the next chunk's q and g (its k is fetched at
-//      the end of phase 3).
-//   5  D1 = [Tb; M] V + [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O;
-//      W to shared memory; S += K~^T W by MMA while O is staged in shared memory and
-//      written by TMA bulk stores (direct stores for a sequence's ragged last chunk).
+//      accumulator with [0; -Q_Gamma]; M = P Tb by three bf16 MMAs (hi/lo splits);
+//      TMA prefetch of the next chunk's k.
+//   4  [Wk; -Q'] by MMA onto the seed, and the state-independent half of D1,
+//      [Tb; M] V, queued behind it; then the [-Wk; Q'] operand over the read
+//      accumulator; TMA prefetch of the next chunk's q and g.
+//   5  D1 += [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O; W to shared
+//      memory; S += K~^T W by MMA while O is staged in shared memory and written by
+//      TMA bulk stores (direct stores for a sequence's ragged last chunk).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -104,8 +104,8 @@ constexpr uint32_t TM_PL = 160;   // [0; P] lo (phase 3)
 constexpr uint32_t TM_M = 192;    // M = P Tb accumulator, rows 64-127, 64 columns (phase 3)
 constexpr uint32_t TM_D1 = 128;   // [W; O] accumulator: [Tb; M] V from phase 4, + [-Wk; Q'] S in phase 5
 constexpr uint32_t TM_AP = 256;   // A/P accumulators, sub-tile m at 256 + 16 m (m+1) / 2 (phases 2-3)
-constexpr uint32_t TM_TPH = 256;  // [Tb; M] hi, bf16 pairs (phases 3-5)
-constexpr uint32_t TM_TPL = 288;  // [Tb; M] lo (phases 3-5)
+constexpr uint32_t TM_TPH = 256;  // [Tb; M] hi, bf16 pairs (phases 3-4)
+constexpr uint32_t TM_TPL = 288;  // [Tb; M] lo (phases 3-4)
 constexpr uint32_t TM_D2 = 320;   // [0; -Q_Gamma] seed, then [Wk; M K_Gamma - Q_Gamma] (phases 3-4)
 constexpr uint32_t TM_A1 = 320;   // [-Wk; Q'] bf16 pairs, over the read D2 (phases 4-5b)
 constexpr uint32_t TM_KTL = 448;  // K~^T lo (phases 2-5)
