@@ -404,7 +404,8 @@ def run_ncu_case(case: str):
     """A small, self-contained launch for ncu captures (no timing, no JSON): the same kernels
     as the bench on inputs still larger than L2 but only a few hundred MB on the device.
       prefill: B=1, H=32, T=8192, dk=dv=128, bf16 (470 MB of inputs/outputs)
-      decode:  B=64, H=96, dk=dv=128, bf16, one step (403 MB of state)"""
+      decode:  B=64, H=96, dk=dv=128, bf16, one step (403 MB of state)
+      decode_multi: the same B, H with K = 4 tokens per sequence in one call"""
     import linear_attention_serving_chunkwise_gb300 as kda
     from linear_attention_serving_chunkwise_gb300.build import build
     build()
@@ -414,12 +415,19 @@ def run_ncu_case(case: str):
         d = W.make_prefill_inputs(cfg, seed=0, device="cuda")
         for _ in range(2):
             kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])
-    else:
+    elif case == "decode":
         cfg = W.DecodeConfig("ncu_decode_b64_h96", 64, 96, 128, 128, torch.bfloat16, 2)
         d = W.make_decode_inputs(cfg, seed=0, device="cuda")
         st = d["state0"]
         for s in range(2):
             kda.decode(d["q"][s], d["k"][s], d["v"][s], d["g"][s], d["beta"][s], st)
+    else:
+        cfg = W.DecodeConfig("ncu_decode_multi_b64_h96_k4", 64, 96, 128, 128, torch.bfloat16, 4)
+        d = W.make_decode_inputs(cfg, seed=0, device="cuda")
+        x = {n: d[n].transpose(0, 1).contiguous() for n in ("q", "k", "v", "g", "beta")}
+        st = d["state0"]
+        for _ in range(2):
+            kda.decode_multi(x["q"], x["k"], x["v"], x["g"], x["beta"], st)
     torch.cuda.synchronize()
     if kda.last_device_status() != kda.KDA_OK:
         raise SystemExit("device error")
@@ -431,7 +439,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--ncu-case", default=None, choices=["prefill", "decode"],
+    ap.add_argument("--ncu-case", default=None, choices=["prefill", "decode", "decode_multi"],
                     help="run one small launch pair for an ncu capture and exit")
     args = ap.parse_args()
     if args.ncu_case:

@@ -13,7 +13,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <cstring>
 #include <mutex>
 #include <vector>
 
@@ -65,7 +64,6 @@ struct Sizes {
     size_t esz, in_row_q, in_row_v, row_g, row_beta, row_out;   // bytes per token of each tensor
     size_t round_tokens;                                         // tokens of the largest round
     size_t state_bytes, cu_bytes;
-    size_t per_token() const { return 2 * in_row_q + in_row_v + row_g + row_beta + row_out; }
 };
 
 bool sizes_of(const kda_prefill_desc& d, int32_t L, Sizes* s)
