@@ -20,7 +20,10 @@
  * Conventions for every entry point:
  *   - All tensor pointers are caller-owned DEVICE memory of the current CUDA
  *     device, contiguous, 16-byte aligned (beta and cu_seqlens: 4-byte
- *     aligned).  The library allocates nothing.
+ *     aligned) -- except for kda_prefill_host and kda_prefill_host_static, whose
+ *     tensors are HOST memory.  The library allocates no memory per call: the
+ *     host-buffer path creates its streams and events once per device, and
+ *     kda_prefill_host_static's scratch is a fixed array in the library's image.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Work is enqueued asynchronously on it; the call returns at once.
  *   - Argument errors are detected on the host and returned synchronously,
