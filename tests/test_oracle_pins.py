@@ -144,6 +144,33 @@ def test_closed_forms():
     assert rel_err(o, q.astype(np.float64) @ S0.astype(np.float64)) < 1e-12
 
 
+def test_linear_in_values_and_initial_state():
+    """For fixed q, k, g, beta the recurrence is linear in (v, S_0): the outputs and the
+    final state of a*(v1, S01) + b*(v2, S02) are a*(run 1) + b*(run 2).  Inputs are
+    chosen exactly representable in fp32 so that the combination is exact."""
+    q, k, v1, g, beta, S01 = _rand_case(12, 8, 6, 21)
+    _, _, v2, _, _, S02 = _rand_case(12, 8, 6, 22)
+    dy = lambda x: (np.round(x * 64.0) / 64.0).astype(np.float32)   # dyadic: sums below stay exact
+    v1, v2, S01, S02 = dy(v1), dy(v2), dy(S01), dy(S02)
+    a, b = 0.5, -2.0
+    o1, f1 = _run1(q, k, v1, g, beta, S01)
+    o2, f2 = _run1(q, k, v2, g, beta, S02)
+    o, f = _run1(q, k, (a * v1 + b * v2).astype(np.float32), g, beta, (a * S01 + b * S02).astype(np.float32))
+    assert rel_err(o, a * o1 + b * o2) < 1e-12 and rel_err(f, a * f1 + b * f2) < 1e-12
+
+
+def test_query_only_reads():
+    """q enters only the read-out: scaling q scales every output and leaves the state
+    trajectory (hence the final state) untouched; a zero q gives zero outputs."""
+    q, k, v, g, beta, S0 = _rand_case(10, 8, 8, 23)
+    o1, f1 = _run1(q, k, v, g, beta, S0)
+    o2, f2 = _run1((4.0 * q).astype(np.float32), k, v, g, beta, S0)
+    o0, f0 = _run1(np.zeros_like(q), k, v, g, beta, S0)
+    assert rel_err(o2, 4.0 * o1) < 1e-12
+    assert np.array_equal(f2, f1) and np.array_equal(f0, f1)
+    assert np.all(o0 == 0)
+
+
 def test_norm_bound():
     """||k|| = 1, beta in [0,1], g <= 0 make (I - beta k k^T) Diag(e^g) a contraction:
     ||S_t||_2 <= ||S_{t-1}||_2 + beta_t ||v_t||."""
