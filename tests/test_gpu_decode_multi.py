@@ -1,5 +1,7 @@
 """GPU parity of kda_decode_multi (K tokens per sequence in one pass over the state) against
-the oracle, and its apply-count semantics for verifying draft tokens."""
+the oracle, and its apply-count semantics for verifying draft tokens.  Up to 8 tokens the
+library runs its persistent kernel (resident CTAs walking the (sequence, head) units, the next
+unit's state prefetched into shared memory); longer drafts run one CTA per unit."""
 import numpy as np
 import pytest
 import torch
@@ -25,7 +27,7 @@ def _oracle(x, state0, lens):
     return oracle.recurrent(pick(x["q"]), pick(x["k"]), pick(x["v"]), pick(x["g"]), pick(x["beta"]), cu, state0)
 
 
-@pytest.mark.parametrize("K", [1, 3, 8])
+@pytest.mark.parametrize("K", [1, 3, 8, 12])
 @pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 128), (torch.float32, 64), (torch.float32, 128)],
                          ids=["bf16-128", "fp32-64", "fp32-128"])
 def test_decode_multi_matches_oracle(cuda_lib, K, dtype, D):
@@ -131,3 +133,39 @@ def test_decode_multi_serving_size(cuda_lib):
                                   np.array([0, K], dtype=np.int32), s0[b:b + 1, hs].cpu().contiguous())
         check(f"seq {b} out", out[b][:, hs].cpu(), ro, 2e-2)
         check(f"seq {b} state", state[b, hs].cpu(), rs[0], 2e-2)
+
+
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 128), (torch.float32, 64)], ids=["bf16-128", "fp32-64"])
+def test_decode_multi_units_beyond_resident_ctas(cuda_lib, dtype, D):
+    """More (sequence, head) units than resident CTAs, not a multiple of them: every CTA walks
+    several units, so every unit after the first comes from the prefetched copy; all checked."""
+    B, H, K = 97, 7, 4                       # 679 units
+    x, s0 = _inputs(B, H, D, dtype, K, seed=75)
+    n_apply = [(3 * b) % (K + 1) for b in range(B)]
+    ref_o, _ = _oracle(x, s0, [K] * B)
+    _, ref_s = _oracle(x, s0, n_apply)
+    state = s0.cuda()
+    out = cuda_lib.decode_multi(*(x[n].cuda() for n in ("q", "k", "v", "g", "beta")), state,
+                                n_apply=torch.tensor(n_apply, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert cuda_lib.last_device_status() == cuda_lib.KDA_OK
+    tol = tol_for(dtype)
+    check("outputs", out.reshape(B * K, H, D), ref_o, tol)
+    check("state", state, ref_s, tol)
+    for b in range(B):
+        if n_apply[b] == 0:
+            assert torch.equal(state[b].cpu(), s0[b])
+
+
+def test_decode_multi_persistent_equals_per_unit_arithmetic(cuda_lib):
+    """The two kernels run the same per-token arithmetic: the first 8 tokens of a 9-token call
+    (per-unit kernel) and an 8-token call (persistent kernel) give bit-identical outputs."""
+    B, H, D = 40, 12, 128
+    x, s0 = _inputs(B, H, D, torch.bfloat16, 9, seed=76)
+    dev = {n: x[n].cuda() for n in x}
+    s9, s8 = s0.cuda(), s0.cuda()
+    o9 = cuda_lib.decode_multi(*(dev[n] for n in ("q", "k", "v", "g", "beta")), s9,
+                               n_apply=torch.full((B,), 8, dtype=torch.int32, device="cuda"))
+    o8 = cuda_lib.decode_multi(*(dev[n][:, :8].contiguous() for n in ("q", "k", "v", "g", "beta")), s8)
+    torch.cuda.synchronize()
+    assert torch.equal(o9[:, :8], o8) and torch.equal(s9, s8)
