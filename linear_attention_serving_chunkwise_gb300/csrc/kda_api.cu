@@ -50,6 +50,21 @@ bool uses_tensor_cores(const kda_prefill_desc& d)
     return d.qkv_dtype == KDA_BF16 && d.dk == 128 && d.dv == 128 && d.total_tokens > 0 && d.num_seqs > 0;
 }
 
+// The chunk-parallel split (per-chunk operands for all chunks at once through the workspace,
+// then the state scan) runs when few (sequence, head) units would leave most SMs idle under
+// the one-CTA-per-head kernel, and its operand workspace (98,816 bytes per (chunk, head))
+// stays within kSplitMaxItems items; otherwise the one-CTA-per-head kernel runs.
+constexpr long long kSplitMaxUnits = 128;
+constexpr long long kSplitMaxItems = 16384;
+
+bool uses_split(const kda_prefill_desc& d)
+{
+    if (!uses_tensor_cores(d)) return false;
+    const long long units = (long long)d.num_seqs * d.num_heads;
+    const long long items = ((long long)d.total_tokens / 64 + d.num_seqs) * d.num_heads;
+    return units <= kSplitMaxUnits && items <= kSplitMaxItems;
+}
+
 kda_status validate_prefill(const kda_prefill_desc* d)
 {
     if (!d) return KDA_ERR_INVALID_ARG;
@@ -83,7 +98,8 @@ const char* kda_status_string(kda_status s)
 size_t kda_prefill_workspace_bytes(const kda_prefill_desc* desc)
 {
     if (validate_prefill(desc) != KDA_OK) return 0;
-    return 0;
+    if (!uses_split(*desc)) return 0;
+    return kda::prefill_split_workspace_bytes(desc->num_seqs, desc->total_tokens, desc->num_heads);
 }
 
 kda_status kda_prefill_query(const kda_prefill_desc* desc, kda_prefill_plan* plan)
@@ -91,7 +107,7 @@ kda_status kda_prefill_query(const kda_prefill_desc* desc, kda_prefill_plan* pla
     const kda_status st = validate_prefill(desc);
     if (st != KDA_OK) return st;
     if (!plan) return KDA_ERR_INVALID_ARG;
-    plan->kernel_launches = desc->num_seqs > 0 ? 1 : 0;
+    plan->kernel_launches = desc->num_seqs > 0 ? (uses_split(*desc) ? 3 : 1) : 0;
     plan->tensor_cores = uses_tensor_cores(*desc) ? 1 : 0;
     plan->workspace_bytes = kda_prefill_workspace_bytes(desc);
     return KDA_OK;
@@ -104,13 +120,16 @@ namespace {
 kda_status prefill_impl(const kda_prefill_desc* desc, const void* q, const void* k, const void* v, const float* g,
                         const float* beta, const int32_t* cu_seqlens, const float* init_state, float* out,
                         float* final_state, int32_t ckpt_interval, int32_t ckpt_slots, float* checkpoints,
-                        void* workspace, size_t workspace_bytes, void* stream)
+                        void* workspace, size_t workspace_bytes, void* stream, bool allow_split)
 {
     kda_status st = validate_prefill(desc);
     if (st != KDA_OK) return st;
     const kda_prefill_desc d = *desc;
     if (!cu_seqlens && d.num_seqs > 0 && d.total_tokens % d.num_seqs != 0) return KDA_ERR_INVALID_ARG;
-    if (workspace_bytes < kda_prefill_workspace_bytes(desc)) return KDA_ERR_WORKSPACE;
+    const bool split = allow_split && uses_split(d);
+    const size_t ws_need = split ? kda_prefill_workspace_bytes(desc) : 0;
+    if (workspace_bytes < ws_need) return KDA_ERR_WORKSPACE;
+    if (split && (!workspace || !aligned16(workspace))) return KDA_ERR_INVALID_ARG;
     if (d.num_seqs == 0) return KDA_OK;
 
     const size_t T = (size_t)d.total_tokens, H = (size_t)d.num_heads, N = (size_t)d.num_seqs;
@@ -143,6 +162,13 @@ kda_status prefill_impl(const kda_prefill_desc* desc, const void* q, const void*
     if (final_state && init_state && final_state != init_state && overlaps(r_fin, ins[6]))
         return KDA_ERR_INVALID_ARG;
     if (final_state && T > 0 && overlaps(r_fin, r_out)) return KDA_ERR_INVALID_ARG;
+    const Range r_ws = range_of(workspace, ws_need);
+    if (split) {   // the workspace is written: it must not overlap anything else
+        for (const Range& r : ins) {
+            if (overlaps(r_ws, r)) return KDA_ERR_INVALID_ARG;
+        }
+        if (overlaps(r_ws, r_out) || (final_state && overlaps(r_ws, r_fin))) return KDA_ERR_INVALID_ARG;
+    }
     if (checkpoints) {
         if (ckpt_interval <= 0 || ckpt_interval % 64 != 0 || ckpt_slots <= 0 || !aligned16(checkpoints))
             return KDA_ERR_INVALID_ARG;
@@ -150,7 +176,8 @@ kda_status prefill_impl(const kda_prefill_desc* desc, const void* q, const void*
         for (const Range& r : ins) {
             if (overlaps(r_ck, r)) return KDA_ERR_INVALID_ARG;
         }
-        if ((T > 0 && overlaps(r_ck, r_out)) || (final_state && overlaps(r_ck, r_fin))) return KDA_ERR_INVALID_ARG;
+        if ((T > 0 && overlaps(r_ck, r_out)) || (final_state && overlaps(r_ck, r_fin)) || overlaps(r_ck, r_ws))
+            return KDA_ERR_INVALID_ARG;
     }
 
     int* status = status_ptr_for_current_device();
@@ -165,12 +192,27 @@ kda_status prefill_impl(const kda_prefill_desc* desc, const void* q, const void*
     a.ckpt_slots = checkpoints ? ckpt_slots : 0;
     a.checkpoints = checkpoints;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.status = status;
-    const cudaError_t e = uses_tensor_cores(d) ? kda::launch_prefill_tc(a, static_cast<cudaStream_t>(stream))
-                                               : kda::launch_prefill_simt(a, static_cast<cudaStream_t>(stream));
+    const cudaStream_t sm = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = split                  ? kda::launch_prefill_split(a, sm)
+                          : uses_tensor_cores(d) ? kda::launch_prefill_tc(a, sm)
+                                                 : kda::launch_prefill_simt(a, sm);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 }  // namespace
+
+namespace kda {
+
+// kda_prefill restricted to the kernels that need no workspace (the host-buffer path's rounds)
+kda_status prefill_no_workspace(const kda_prefill_desc* desc, const void* q, const void* k, const void* v,
+                                const float* g, const float* beta, const int32_t* cu_seqlens, const float* init_state,
+                                float* out, float* final_state, void* stream)
+{
+    return prefill_impl(desc, q, k, v, g, beta, cu_seqlens, init_state, out, final_state, 0, 0, nullptr, nullptr, 0,
+                        stream, false);
+}
+
+}  // namespace kda
 
 extern "C" {
 
@@ -180,7 +222,7 @@ kda_status kda_prefill(const kda_prefill_desc* desc, const void* q, const void* 
                        void* workspace, size_t workspace_bytes, void* stream)
 {
     return prefill_impl(desc, q, k, v, g, beta, cu_seqlens, init_state, out, final_state, 0, 0, nullptr, workspace,
-                        workspace_bytes, stream);
+                        workspace_bytes, stream, true);
 }
 
 kda_status kda_prefill_checkpointed(const kda_prefill_desc* desc, const void* q, const void* k, const void* v,
@@ -191,7 +233,7 @@ kda_status kda_prefill_checkpointed(const kda_prefill_desc* desc, const void* q,
 {
     if (!checkpoints) return KDA_ERR_INVALID_ARG;
     return prefill_impl(desc, q, k, v, g, beta, cu_seqlens, init_state, out, final_state, checkpoint_interval,
-                        checkpoint_slots, checkpoints, workspace, workspace_bytes, stream);
+                        checkpoint_slots, checkpoints, workspace, workspace_bytes, stream, true);
 }
 
 kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, int32_t qkv_dtype,

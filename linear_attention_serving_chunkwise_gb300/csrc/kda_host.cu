@@ -18,6 +18,13 @@
 
 #include "../../include/kda.h"
 
+namespace kda {
+// kda_prefill on the kernels that need no workspace (defined with the C ABI)
+kda_status prefill_no_workspace(const kda_prefill_desc* desc, const void* q, const void* k, const void* v,
+                                const float* g, const float* beta, const int32_t* cu_seqlens, const float* init_state,
+                                float* out, float* final_state, void* stream);
+}  // namespace kda
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -255,9 +262,9 @@ kda_status kda_prefill_host(const kda_prefill_desc* desc, const void* q, const v
         for (int u = 0; u < kUp; ++u) KDA_CK(cudaStreamWaitEvent(comp, hp->staged[b][u], 0));
         kda_prefill_desc rd = d;
         rd.total_tokens = cu[N];
-        st = kda_prefill(&rd, sg.q, sg.k, sg.v, reinterpret_cast<const float*>(sg.g),
-                         reinterpret_cast<const float*>(sg.beta), sg.cu, dstate, reinterpret_cast<float*>(sg.out),
-                         dstate, nullptr, 0, comp);
+        st = kda::prefill_no_workspace(&rd, sg.q, sg.k, sg.v, reinterpret_cast<const float*>(sg.g),
+                                       reinterpret_cast<const float*>(sg.beta), sg.cu, dstate,
+                                       reinterpret_cast<float*>(sg.out), dstate, comp);
         if (st != KDA_OK) return st;
         KDA_CK(cudaEventRecord(hp->computed[b], comp));
         // outputs of round r

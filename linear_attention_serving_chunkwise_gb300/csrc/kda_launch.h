@@ -46,6 +46,10 @@ struct DecodeMultiArgs {
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 // bf16 tcgen05 chunkwise prefill (dk = dv = 128, T > 0)
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
+// the same, chunk-parallel: per-chunk operands for every chunk at once (workspace), then
+// the state scan; needs prefill_split_workspace_bytes of workspace, 16-byte aligned
+cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream);
+size_t prefill_split_workspace_bytes(int num_seqs, int total_tokens, int num_heads);
 // fused single-pass decode
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // K tokens per sequence in one pass over the state

@@ -1,0 +1,781 @@
+// Chunk-parallel KDA prefill on the tcgen05 tensor cores (bf16 q/k/v, dk = dv = 128):
+// the chunkwise form of llm-atlas "K3_RESEARCH.md" Q07 split at the one place where it
+// is sequential.  Everything a chunk needs that does not depend on the state entering it
+// (the g cumsum, A and P, T = (I + A)^-1, Tb = T diag(beta), M = P Tb, Wk = Tb K_Gamma,
+// Q' = Q_Gamma - M K_Gamma and K~ = K e^{Gamma_63 - Gamma}) depends only on that chunk's
+// q, k, g and beta, so it is computed for all (sequence, head, chunk) items at once; the
+// state recurrence
+//   W = Tb V - Wk S,   O = Q' S + M V,   S <- Diag(gamma_C) S + K~^T W
+// then walks each (sequence, head)'s chunks in order.  Three launches per call:
+//   1  kda_chunk_offsets_kernel: per-sequence chunk offsets (prefix sums of ceil(len / 64))
+//      and the cu_seqlens check, into the workspace;
+//   2  kda_chunk_prep_kernel: persistent CTAs over the items.  Each item runs the phases
+//      of the one-CTA-per-head kernel up to [Wk; -Q'] (same functions, same arithmetic) and
+//      writes the operands of its state step -- [-Wk; Q'] bf16, [Tb; M] and K~^T as bf16
+//      hi + lo, gamma_C -- to the workspace as the byte images of 128-byte-swizzled K-major
+//      tiles, so that they can be copied into shared memory as they are;
+//   3  kda_state_scan_kernel: one CTA per (sequence, head), the state in tensor memory.
+//      Per chunk: the state's bf16 operand and S <- gamma_C S; D1 = [Tb; M] V + [-Wk; Q'] S
+//      by MMAs with the A operands in shared memory; W (hi + lo) to shared memory and O to
+//      HBM; S += K~^T W by MMAs.  The item's images arrive by bulk asynchronous copies one
+//      step ahead, v by TMA two chunks ahead.
+// The tensor-core instructions and their operands are those of the one-CTA-per-head
+// kernel, so the results are the same; the work of steps 1-2 spreads over every SM
+// instead of one SM per (sequence, head), at the price of 96.5 KB of operands per item
+// written and read back through HBM.
+#include <algorithm>
+#include <cstring>
+
+#include "kda_prefill_tc_phases.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm100;
+
+// ---------------------------------------------------------------- one item's operand images (bytes)
+constexpr uint32_t IMG_A1 = 0;          // [-Wk; Q'] bf16, K-major [128 rows][128 K] (2 x 16 KB)
+constexpr uint32_t IMG_TBH = 32768;     // [Tb; M] hi bf16, K-major [128 rows][64 K]
+constexpr uint32_t IMG_TBL = 49152;     // [Tb; M] lo
+constexpr uint32_t IMG_GAM = 65536;     // gamma_C fp32 [128]
+constexpr uint32_t IMG_FRONT = 66048;   // bytes [0, IMG_FRONT): read at the start of a chunk step
+constexpr uint32_t IMG_KTH = 66048;     // K~^T hi bf16, K-major [128 dk rows][64 K tokens]
+constexpr uint32_t IMG_KTL = 82432;     // K~^T lo
+constexpr uint32_t IMG_BACK = 32768;    // bytes [IMG_KTH, IMG_KTH + IMG_BACK): read for the state update
+constexpr uint32_t IMG_BYTES = 98816;
+
+// ---------------------------------------------------------------- state-scan shared memory (bytes)
+constexpr uint32_t B_A1 = 0;            // the front image, copied whole
+constexpr uint32_t B_TBH = IMG_TBH;
+constexpr uint32_t B_TBL = IMG_TBL;
+constexpr uint32_t B_GAM = IMG_GAM;
+constexpr uint32_t B_KTH = 66560;       // the back image (1024-byte aligned)
+constexpr uint32_t B_KTL = B_KTH + 16384;
+constexpr uint32_t B_V0 = 99328;        // v tiles [64 tok][128 ch] bf16, two buffers
+constexpr uint32_t B_V1 = 115712;
+constexpr uint32_t B_SB = 132096;       // S bf16, MN-major B [128 dk][128 dv]
+constexpr uint32_t B_WH = 164864;       // W hi bf16, MN-major B [64 tok][128 dv]
+constexpr uint32_t B_WL = 181248;       // W lo
+constexpr uint32_t B_OST = 197632;      // O staging: 4 x [64 tok][32 dv] fp32 boxes, 128-byte swizzle
+constexpr uint32_t B_BAR = 230400;
+constexpr size_t B_SMEM_BYTES = B_BAR + 64 + 1024;
+constexpr uint32_t B_TM_S = 0;          // tensor memory: state [128 dk lanes][128 dv] fp32
+constexpr uint32_t B_TM_D1 = 128;       // [W; O] accumulator
+constexpr uint32_t B_TM_COLS = 256;
+
+static_assert(B_KTH % 1024 == 0 && B_V0 % 1024 == 0 && B_SB % 1024 == 0 && B_WH % 1024 == 0, "tile alignment");
+static_assert(B_KTH >= IMG_FRONT && B_V0 >= B_KTH + IMG_BACK && B_V1 == B_V0 + 16384 && B_SB >= B_V1 + 16384 &&
+                  B_WH >= B_SB + 32768 && B_WL == B_WH + 16384 && B_OST >= B_WL + 16384 &&
+                  B_OST % 1024 == 0 && B_BAR >= B_OST + 32768 && B_SMEM_BYTES <= 232448,
+              "state-scan map overlaps");
+static_assert(IMG_KTL == IMG_KTH + 16384 && IMG_BYTES == IMG_KTH + IMG_BACK, "image map");
+
+struct SplitParams {
+    TcParams p;                 // inputs, outputs, tensor maps, status (as the one-CTA-per-head kernel)
+    uint8_t* ops;               // operand images, item (global chunk gc, head h) at ((gc * H) + h) * IMG_BYTES
+    int32_t* chunk_off;         // [num_seqs + 1]: first global chunk of each sequence
+};
+
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// contiguous shared -> global copy (bulk-group completion); both 16-byte aligned, size % 16 == 0
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(smem_src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// start moving [gsrc, gsrc + bytes) into L2 (no completion to wait for)
+__device__ __forceinline__ void prefetch_l2(const void* gsrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
+}
+
+// the prep kernel stages each 32 KB piece of an item's image here (the v buffers of the
+// shared map, which it does not use) and writes it with one bulk store
+constexpr uint32_t A_STAGE = OFF_V0;
+static_assert(OFF_V1 + 16384 == A_STAGE + 32768, "staging buffer");
+
+// ---------------------------------------------------------------- step 1: chunk offsets
+// One CTA of 1024 threads: chunk_off[n] = sum over m < n of ceil(len_m / 64), lengths of
+// sequences that fail the cu_seqlens check counted as 0 (and the failure reported).
+__global__ void __launch_bounds__(1024) kda_chunk_offsets_kernel(const int32_t* cu_seqlens, int num_seqs,
+                                                                 int total_tokens, int32_t* chunk_off, int* status)
+{
+    __shared__ int warp_sums[32];
+    __shared__ int carry;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    if (t == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < num_seqs; base += 1024) {
+        const int n = base + t;
+        int cnt = 0;
+        if (n < num_seqs) {
+            int bos, eos;
+            if (seq_bounds(cu_seqlens, n, num_seqs, total_tokens, status, bos, eos)) cnt = (eos - bos + 63) >> 6;
+        }
+        int x = cnt;   // inclusive warp scan
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sums[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int s = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += y;
+            }
+            warp_sums[lane] = s;   // inclusive over warps
+        }
+        __syncthreads();
+        const int before = carry + (w > 0 ? warp_sums[w - 1] : 0) + x - cnt;
+        if (n < num_seqs) chunk_off[n] = before;
+        __syncthreads();
+        if (t == 1023) carry = before + cnt;
+        __syncthreads();
+    }
+    if (t == 0) chunk_off[num_seqs] = carry;
+}
+
+// Sequence of global chunk gc: the last n with chunk_off[n] <= gc (binary search).
+__device__ __forceinline__ int seq_of_chunk(const int32_t* chunk_off, int num_seqs, int gc)
+{
+    int lo = 0, hi = num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(chunk_off + mid) <= gc) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ---------------------------------------------------------------- step 2: per-item operands
+struct Item {
+    int h, t0, eos, gc;
+};
+
+__device__ __forceinline__ Item item_at(const SplitParams& sp, int item)
+{
+    const int H = sp.p.num_heads;
+    Item it;
+    it.gc = item / H;
+    it.h = item - it.gc * H;
+    const int n = seq_of_chunk(sp.chunk_off, sp.p.num_seqs, it.gc);
+    int bos, eos;
+    seq_bounds(sp.p.cu_seqlens, n, sp.p.num_seqs, sp.p.total_tokens, sp.p.status, bos, eos);   // valid: it has chunks
+    it.t0 = bos + 64 * (it.gc - __ldg(sp.chunk_off + n));
+    it.eos = eos;
+    return it;
+}
+
+// Persistent: CTA b takes items b, b + gridDim.x, ...; the next item's q, k and g tiles are
+// fetched by TMA while the current one is worked on (k once phase 3 no longer reads it,
+// q and g once phase 4 starts), its beta into a register.  16 warps; warp w reaches TMEM
+// lanes [32 (w % 4), +32) and works on column part w / 4, as in the one-CTA-per-head kernel.
+__global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __grid_constant__ SplitParams sp)
+{
+    const TcParams& p = sp.p;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int quarter = warp & 3, part = warp >> 2;
+    const int L = 32 * quarter + lane;
+    float* vec = reinterpret_cast<float*>(sm + OFF_VEC);
+    float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
+    uint64_t* bar_k = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint64_t* bar_qg = bar_k + 1;
+    uint64_t* bar_mma = bar_k + 2;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_k + 4);
+    int* s_abort = reinterpret_cast<int*>(tslot + 1);
+    const uint32_t sbase = smem_u32(sm);
+    const int H = p.num_heads;
+    const int items = __ldg(sp.chunk_off + p.num_seqs) * H;
+
+    if (t == 0) {
+        mbar_init(bar_k, 1);
+        mbar_init(bar_qg, 1);
+        mbar_init(bar_mma, 1);
+        mbar_fence_init();
+        *s_abort = 0;
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_g);
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tm = *tslot;
+
+    bool k_pending = false, qg_pending = false;   // thread 0 only
+    int item = blockIdx.x;
+    Item cur{};
+    if (item < items) {
+        cur = item_at(sp, item);
+        if (t == 0) {
+            issue_k_loads(p, sm, bar_k, cur.t0, cur.h);
+            issue_qg_loads(p, sm, bar_qg, cur.t0, cur.h);
+            k_pending = qg_pending = true;
+        }
+    }
+    float beta_next = (item < items && t < 64 && cur.t0 + t < cur.eos)
+                          ? __ldg(p.beta + (size_t)(cur.t0 + t) * H + cur.h)
+                          : 0.f;
+    uint32_t k_par = 0, qg_par = 0, mma_par = 0;
+    bool ok = true;
+
+    for (; item < items; item += gridDim.x) {
+        const int h = cur.h, t0 = cur.t0;
+        const int BT = min(64, cur.eos - t0);
+        uint8_t* img = sp.ops + ((size_t)cur.gc * H + h) * IMG_BYTES;
+        const bool has_next = item + (int)gridDim.x < items;
+        const Item nxt = has_next ? item_at(sp, item + gridDim.x) : cur;
+        if (t < 64) sbeta[t] = beta_next;
+        if (t == 0) bulk_wait_read();   // the previous item's last piece has left the staging buffer
+        if (!(mbar_wait_bounded(bar_k, k_par, kWaitNs) && mbar_wait_bounded(bar_qg, qg_par, kWaitNs)))
+            atomicExch(s_abort, 1);
+        tc_fence_before_sync();
+        __syncthreads();
+        tc_fence_after_sync();
+        if (*s_abort) {
+            ok = false;
+            break;
+        }
+        k_par ^= 1u;
+        qg_par ^= 1u;
+        if (t == 0) k_pending = qg_pending = false;
+        if (t < 64)
+            beta_next = (has_next && nxt.t0 + t < nxt.eos) ? __ldg(p.beta + (size_t)(nxt.t0 + t) * H + nxt.h) : 0.f;
+
+        // ---- phase 1: decayed operands
+        phase1_cumsum(sm, vec, t, BT);
+        __syncthreads();
+        if (t < 128) phase1_factors(vec, t);
+        __syncthreads();
+        phase1_tokens(sm, vec, tm, L, part, quarter, BT);
+        __syncthreads();
+        phase1_offdiag(sm, vec, t);
+        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncthreads();
+
+        // ---- phase 2: A and P by one tf32 MMA, while K~^T goes to the image
+        if (t == 0) {
+            tc_fence_after_sync();
+            const uint32_t idesc = idesc_tf32_f32(128, KC_ROWS);
+            const uint32_t kc = sbase + OFF_X;
+#pragma unroll
+            for (int ks = 0; ks < 16; ++ks)
+                umma_tf32_tmem_a(tm + TM_AP, tm + TM_KQ + 8 * ks, desc_kmajor(kc, KC_ROWS, ks), idesc,
+                                 ks > 0 ? 1u : 0u);
+            umma_commit(bar_mma);
+        }
+        {
+            uint32_t hi[8], lo[8];
+            ktilde_pairs(sm, vec, L, part, BT, hi, lo);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                st_shared_v4(sbase + A_STAGE + sw128_chunk(L, 2 * part + cc, 128), hi[4 * cc], hi[4 * cc + 1],
+                             hi[4 * cc + 2], hi[4 * cc + 3]);
+                st_shared_v4(sbase + A_STAGE + 16384 + sw128_chunk(L, 2 * part + cc, 128), lo[4 * cc],
+                             lo[4 * cc + 1], lo[4 * cc + 2], lo[4 * cc + 3]);
+            }
+            fence_proxy_async_smem();
+        }
+        if (t < 128) reinterpret_cast<float*>(img + IMG_GAM)[t] = vec[V_GC * 128 + t];
+        if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
+        mma_par ^= 1u;
+        tc_fence_after_sync();
+        if (t == 0) {
+            bulk_store(img + IMG_KTH, sm + A_STAGE, IMG_BACK);
+            bulk_commit();
+        }
+
+        // ---- phase 3: A/P read-out; solve while warps 8-15 seed D2; M = P Tb; [Tb; M] hi/lo
+        phase3_readout(sm, tm, L, quarter, part, sbeta);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncthreads();
+        tc_fence_after_sync();
+        if (t < kSolveThreads) {
+            phase3_solve(sm, t);
+        } else {
+            phase3_seed(sm, vec, tm, L, 2 * (part - 2), quarter, BT);
+            phase3_seed(sm, vec, tm, L, 2 * (part - 2) + 1, quarter, BT);
+            tmem_wait_st();
+        }
+        tc_fence_before_sync();
+        __syncthreads();
+        tc_fence_after_sync();
+        if (t == 0 && has_next) {   // the k tile is no longer read
+            issue_k_loads(p, sm, bar_k, nxt.t0, nxt.h);
+            k_pending = true;
+        }
+        phase3_tb_operands(sm, t, sbeta);
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+        if (t == 0) {
+            tc_fence_after_sync();
+            const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
+            const uint32_t tbh = sbase + OFF_X + X_TBH, tbl = sbase + OFF_X + X_TBL;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_M, tm + TM_PH + 8 * ks, desc_mnmajor(tbh, 64, ks), idesc, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_M, tm + TM_PH + 8 * ks, desc_mnmajor(tbl, 64, ks), idesc, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_M, tm + TM_PL + 8 * ks, desc_mnmajor(tbh, 64, ks), idesc, 1u);
+            umma_commit(bar_mma);
+            bulk_wait_read();   // the K~ piece has left the staging buffer
+        }
+        // [Tb; M] hi/lo: row L, K = tokens [16 part, +16), to TMEM (the D2 MMA) and the staging buffer
+        uint32_t hi[8], lo[8];
+        if (quarter < 2) {   // Tb rows (lanes 0-63) from the hi/lo B-operand tiles
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const uint4 h4 = ld_shared_v4(sbase + OFF_X + X_TBH + sw128_chunk(L, 2 * part + cc, 64));
+                const uint4 l4 = ld_shared_v4(sbase + OFF_X + X_TBL + sw128_chunk(L, 2 * part + cc, 64));
+                hi[4 * cc] = h4.x; hi[4 * cc + 1] = h4.y; hi[4 * cc + 2] = h4.z; hi[4 * cc + 3] = h4.w;
+                lo[4 * cc] = l4.x; lo[4 * cc + 1] = l4.y; lo[4 * cc + 2] = l4.z; lo[4 * cc + 3] = l4.w;
+            }
+            tmem_st8u(tmem_addr(tm, 32 * quarter, TM_TPH + 8 * part), hi);
+            tmem_st8u(tmem_addr(tm, 32 * quarter, TM_TPL + 8 * part), lo);
+        }
+        if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
+        mma_par ^= 1u;
+        tc_fence_after_sync();
+        if (quarter >= 2) {   // M rows (lanes 64-127), split into hi/lo
+            float a[16];
+            tmem_ld16(tmem_addr(tm, 32 * quarter, TM_M + 16 * part), a);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
+            tmem_st8u(tmem_addr(tm, 32 * quarter, TM_TPH + 8 * part), hi);
+            tmem_st8u(tmem_addr(tm, 32 * quarter, TM_TPL + 8 * part), lo);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            st_shared_v4(sbase + A_STAGE + sw128_chunk(L, 2 * part + cc, 128), hi[4 * cc], hi[4 * cc + 1],
+                         hi[4 * cc + 2], hi[4 * cc + 3]);
+            st_shared_v4(sbase + A_STAGE + 16384 + sw128_chunk(L, 2 * part + cc, 128), lo[4 * cc], lo[4 * cc + 1],
+                         lo[4 * cc + 2], lo[4 * cc + 3]);
+        }
+        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncthreads();
+
+        // ---- phase 4: D2 = [0; -Q_Gamma] + [Tb; M] K_Gamma (hi + lo) = [Wk; -Q']; A1 = -D2 to the image
+        if (t == 0) {
+            tc_fence_after_sync();
+            bulk_store(img + IMG_TBH, sm + A_STAGE, 32768);
+            bulk_commit();
+            if (has_next) {   // the q and g tiles are no longer read
+                issue_qg_loads(p, sm, bar_qg, nxt.t0, nxt.h);
+                qg_pending = true;
+            }
+            const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPH + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPL + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
+            umma_commit(bar_mma);
+            bulk_wait_read();   // the [Tb; M] piece has left the staging buffer
+        }
+        if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
+        mma_par ^= 1u;
+        tc_fence_after_sync();
+        {   // row L, K = dk columns [32 part, +32)
+            float a[32];
+            tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 32 * part), a);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st_shared_v4(sbase + A_STAGE + sw128_chunk(L, 4 * part + q, 128), pk[4 * q], pk[4 * q + 1],
+                             pk[4 * q + 2], pk[4 * q + 3]);
+            fence_proxy_async_smem();
+        }
+        __syncthreads();
+        if (t == 0) {
+            bulk_store(img + IMG_A1, sm + A_STAGE, 32768);
+            bulk_commit();
+        }
+        cur = nxt;   // the next item's first barrier orders these TMEM reads before its writes
+    }
+
+    if (t == 0) bulk_wait_all();   // the images are written before the CTA's shared memory goes away
+    if (!ok && t == 0) {
+        report_status(p.status, kDevTimeout);
+        if (k_pending) mbar_wait_bounded(bar_k, k_par, kWaitNs);
+        if (qg_pending) mbar_wait_bounded(bar_qg, qg_par, kWaitNs);
+        mbar_wait_bounded(bar_mma, mma_par, kWaitNs);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, TM_COLS);
+}
+
+// ---------------------------------------------------------------- step 3: the state scan
+// One CTA per (sequence, head), 16 warps (warp w: TMEM lanes [32 (w % 4), +32), column part
+// w / 4).  The front image of chunk c+1 is fetched once chunk c's D1 MMAs have read theirs,
+// the back image once its state update has; v two chunks ahead into the freed buffer, and
+// the images of chunk c+2 are prefetched into L2 at the same time.
+__global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __grid_constant__ SplitParams sp)
+{
+    const TcParams& p = sp.p;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int quarter = warp & 3, part = warp >> 2;
+    const int L = 32 * quarter + lane;
+    uint64_t* bar_f = reinterpret_cast<uint64_t*>(sm + B_BAR);
+    uint64_t* bar_b = bar_f + 1;
+    uint64_t* bar_v = bar_f + 2;   // two, one per v buffer
+    uint64_t* bar_mma = bar_f + 4;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_f + 5);
+    int* s_abort = reinterpret_cast<int*>(tslot + 1);
+    const uint32_t sbase = smem_u32(sm);
+    const float* sgam = reinterpret_cast<const float*>(sm + B_GAM);
+
+    const int H = p.num_heads;
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    int bos, eos;
+    if (!seq_bounds(p.cu_seqlens, n, p.num_seqs, p.total_tokens, p.status, bos, eos)) return;
+    const int nchunks = (eos - bos + 63) >> 6;
+    const int gc0 = __ldg(sp.chunk_off + n);
+    const size_t sbase_g = ((size_t)n * H + h) * 128 * 128;
+    auto image = [&](int c) { return sp.ops + ((size_t)(gc0 + c) * H + h) * IMG_BYTES; };
+
+    if (t == 0) {
+        for (int i = 0; i < 5; ++i) mbar_init(bar_f + i, 1);
+        mbar_fence_init();
+        *s_abort = 0;
+        tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_o);
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, B_TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tm = *tslot;
+
+    // thread 0's copies in flight, for the bounded clean-up on abort
+    bool f_pending = false, b_pending = false, o_pending = false, mma_open = false;
+    uint32_t v_pending = 0;   // bit b: a v copy into buffer b in flight
+    auto fetch_front = [&](int c) {
+        mbar_arrive_expect_tx(bar_f, IMG_FRONT);
+        bulk_load(sm + B_A1, image(c), IMG_FRONT, bar_f);
+        f_pending = true;
+    };
+    auto fetch_back = [&](int c) {
+        mbar_arrive_expect_tx(bar_b, IMG_BACK);
+        bulk_load(sm + B_KTH, image(c) + IMG_KTH, IMG_BACK, bar_b);
+        b_pending = true;
+    };
+    auto fetch_v = [&](int c) {   // [64 tok][128 ch] as two 64-channel TMA boxes
+        uint64_t* bar = bar_v + (c & 1);
+        uint8_t* dst = sm + ((c & 1) ? B_V1 : B_V0);
+        mbar_arrive_expect_tx(bar, 16384u);
+        tma_load_3d(dst, &p.tm_v, bar, 0, h, bos + 64 * c);
+        tma_load_3d(dst + 8192, &p.tm_v, bar, 64, h, bos + 64 * c);
+        v_pending |= 1u << (c & 1);
+    };
+    if (t == 0 && nchunks > 0) {
+        fetch_front(0);
+        fetch_back(0);
+        fetch_v(0);
+        if (nchunks > 1) {
+            fetch_v(1);
+            prefetch_l2(image(1), IMG_BYTES);
+        }
+    }
+
+    // initial state -> TMEM: lane L = key channel, columns [32 part, 32 part + 32)
+    {
+        float v[32];
+        if (p.init_state) {
+            const float4* src = reinterpret_cast<const float4*>(p.init_state + sbase_g + (size_t)L * 128 + 32 * part);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 f = __ldg(src + i);
+                v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        tmem_st32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), v);
+        tmem_wait_st();
+    }
+
+    uint32_t f_par = 0, b_par = 0, v_par = 0, mma_par = 0;   // v_par: bit b = buffer b's parity
+    bool ok = true;
+    for (int ci = 0; ci < nchunks; ++ci) {
+        const int t0 = bos + 64 * ci;
+        const int BT = min(64, eos - t0);
+        const int vb = ci & 1;
+        if (t == 0 && o_pending) {   // the previous chunk's O staging has been read out
+            bulk_wait_read();
+            o_pending = false;
+        }
+        if (!mbar_wait_bounded(bar_f, f_par, kWaitNs)) atomicExch(s_abort, 1);
+        tc_fence_before_sync();
+        __syncthreads();
+        tc_fence_after_sync();
+        if (*s_abort) {
+            ok = false;
+            break;
+        }
+        f_par ^= 1u;
+        if (t == 0) f_pending = false;
+
+        // the state's bf16 B operand; S <- gamma_C S (this chunk's decay, before its update)
+        // runs while the D1 MMAs, which read only the bf16 copy, execute
+        float a[32];
+        tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), a);
+        tmem_wait_ld();
+        {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st_shared_v4(sbase + B_SB + sw128_chunk(L, 4 * part + q, 128), pk[4 * q], pk[4 * q + 1],
+                             pk[4 * q + 2], pk[4 * q + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+
+        // D1 = [Tb; M] V (hi + lo) + [-Wk; Q'] S
+        if (t == 0) {
+            tc_fence_after_sync();
+            if (!mbar_wait_bounded(bar_v + vb, (v_par >> vb) & 1u, kWaitNs)) {
+                atomicExch(s_abort, 1);
+            } else {
+                v_par ^= 1u << vb;
+                v_pending &= ~(1u << vb);
+                const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+                const uint32_t vt = sbase + (vb ? B_V1 : B_V0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_TBH, 128, ks), desc_mnmajor(vt, 64, ks), idesc,
+                              ks > 0 ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_TBL, 128, ks), desc_mnmajor(vt, 64, ks), idesc, 1u);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_A1, 128, ks), desc_mnmajor(sbase + B_SB, 128, ks),
+                              idesc, 1u);
+                umma_commit(bar_mma);
+                mma_open = true;
+            }
+        }
+        {
+            const float gc = sgam[L];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] *= gc;
+            tmem_st32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), a);
+            tmem_wait_st();
+        }
+        if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
+        mma_par ^= 1u;
+        tc_fence_after_sync();
+        if (t == 0) {   // the front image and this v buffer have been read
+            mma_open = false;
+            if (ci + 1 < nchunks) fetch_front(ci + 1);
+            if (ci + 2 < nchunks) {
+                fetch_v(ci + 2);
+                prefetch_l2(image(ci + 2), IMG_BYTES);   // so that the next fetches come from L2
+            }
+        }
+
+        // rows 0-63 -> W (hi + lo) B operands, and S += K~^T W as soon as the 8 warps holding
+        // them are done; rows 64-127 = O staged for TMA stores meanwhile
+        tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_D1 + 32 * part), a);
+        tmem_wait_ld();
+        if (quarter < 2) {
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
+            store_row32_bf16(sbase + B_WH, L, 4 * part, 64, hi);
+            store_row32_bf16(sbase + B_WL, L, 4 * part, 64, lo);
+            fence_proxy_async_smem();
+            named_sync(1, 256);
+            if (t == 0) {   // S += K~^T W (hi hi + hi lo + lo hi)
+                tc_fence_after_sync();
+                if (!mbar_wait_bounded(bar_b, b_par, kWaitNs)) {
+                    atomicExch(s_abort, 1);
+                } else {
+                    b_par ^= 1u;
+                    b_pending = false;
+                    const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_bf16(tm + B_TM_S, desc_kmajor(sbase + B_KTH, 128, ks),
+                                  desc_mnmajor(sbase + B_WH, 64, ks), idesc, 1u);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_bf16(tm + B_TM_S, desc_kmajor(sbase + B_KTH, 128, ks),
+                                  desc_mnmajor(sbase + B_WL, 64, ks), idesc, 1u);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_bf16(tm + B_TM_S, desc_kmajor(sbase + B_KTL, 128, ks),
+                                  desc_mnmajor(sbase + B_WH, 64, ks), idesc, 1u);
+                    umma_commit(bar_mma);
+                    mma_open = true;
+                }
+            }
+        } else {
+            const int r = L - 64;
+            if (BT == 64) {   // box `part` = dv columns [32 part, +32)
+                const uint32_t box = sbase + B_OST + 8192 * part;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_shared_f4(box + sw128_off_f32(r, 4 * q, 64), a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+                fence_proxy_async_smem();
+            } else if (r < BT) {   // a sequence's ragged last chunk: direct stores
+                float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)(t0 + r) * H + h) * 128 + 32 * part);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+            }
+        }
+        if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
+        mma_par ^= 1u;
+        if (t == 0) {
+            mma_open = false;
+            if (ci + 1 < nchunks) fetch_back(ci + 1);
+            if (BT == 64) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tma_store_3d(&p.tm_o, sm + B_OST + 8192 * j, 32 * j, h, t0);
+                bulk_commit();
+                o_pending = true;
+            }
+        }
+        // state snapshot after a full chunk that ends on a checkpoint boundary
+        {
+            const int done = t0 + 64 - bos;
+            if (p.checkpoints && BT == 64 && done % p.ckpt_interval == 0 && done / p.ckpt_interval <= p.ckpt_slots) {
+                tc_fence_after_sync();
+                const int slot = done / p.ckpt_interval - 1;
+                float v[32];
+                tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), v);
+                tmem_wait_ld();
+                float4* dst = reinterpret_cast<float4*>(
+                    p.checkpoints + (((size_t)n * H + h) * p.ckpt_slots + slot) * 128 * 128 + (size_t)L * 128 + 32 * part);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                tc_fence_before_sync();
+            }
+        }
+    }
+
+    if (t == 0) bulk_wait_all();   // staged O fully written before the CTA's shared memory goes away
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (ok && p.final_state) {
+        float v[32];
+        tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), v);
+        tmem_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(p.final_state + sbase_g + (size_t)L * 128 + 32 * part);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
+    if (!ok && t == 0) {
+        // a wait gave up: record it, let in-flight copies and MMAs land (bounded), then leave
+        report_status(p.status, kDevTimeout);
+        if (f_pending) mbar_wait_bounded(bar_f, f_par, kWaitNs);
+        if (b_pending) mbar_wait_bounded(bar_b, b_par, kWaitNs);
+        for (int i = 0; i < 2; ++i)
+            if ((v_pending >> i) & 1u) mbar_wait_bounded(bar_v + i, (v_par >> i) & 1u, kWaitNs);
+        if (mma_open) mbar_wait_bounded(bar_mma, mma_par, kWaitNs);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, B_TM_COLS);
+}
+
+}  // namespace
+
+size_t prefill_split_workspace_bytes(int num_seqs, int total_tokens, int num_heads)
+{
+    const size_t chunks = (size_t)total_tokens / 64 + (size_t)num_seqs;   // >= the sum of ceil(len / 64)
+    const size_t offs = ((size_t)(num_seqs + 1) * sizeof(int32_t) + 255) & ~(size_t)255;
+    return offs + chunks * (size_t)num_heads * IMG_BYTES;
+}
+
+cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream)
+{
+    SplitParams sp;
+    memset(&sp, 0, sizeof(sp));
+    TcParams& p = sp.p;
+    if (!make_map(&p.tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
+        !make_map(&p.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
+        !make_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
+        !make_map(&p.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32) ||
+        !make_map(&p.tm_o, a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32))
+        return cudaErrorInvalidValue;
+    p.beta = a.beta;
+    p.cu_seqlens = a.cu_seqlens;
+    p.init_state = a.init_state;
+    p.out = a.out;
+    p.final_state = a.final_state;
+    p.checkpoints = a.checkpoints;
+    p.ckpt_interval = a.checkpoints ? a.ckpt_interval : 64;
+    p.ckpt_slots = a.ckpt_slots;
+    p.num_seqs = a.num_seqs;
+    p.total_tokens = a.total_tokens;
+    p.num_heads = a.num_heads;
+    p.status = a.status;
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    sp.chunk_off = reinterpret_cast<int32_t*>(ws);
+    sp.ops = ws + (((size_t)(a.num_seqs + 1) * sizeof(int32_t) + 255) & ~(size_t)255);
+
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kda_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kda_state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)B_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+
+    kda_chunk_offsets_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.num_seqs, a.total_tokens, sp.chunk_off,
+                                                      a.status);
+    const long long items_max = ((long long)a.total_tokens / 64 + a.num_seqs) * a.num_heads;
+    const long long prep_grid = std::max(1LL, std::min<long long>(sms, items_max));
+    kda_chunk_prep_kernel<<<(unsigned)prep_grid, kThreads, SMEM_BYTES, stream>>>(sp);
+    kda_state_scan_kernel<<<(unsigned)((long long)a.num_seqs * a.num_heads), kThreads, B_SMEM_BYTES, stream>>>(sp);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

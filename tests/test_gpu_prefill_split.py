@@ -1,0 +1,121 @@
+"""GPU tests of the chunk-parallel prefill path: per-chunk operands for every (sequence, head,
+chunk) at once, then the state scan.  kda_prefill takes it for bf16, dk = dv = 128 calls with
+at most 128 (sequence, head) units; more units run the one-CTA-per-head kernel.  The two
+issue the same tensor-core instructions on the same operands, so their results are compared
+bit for bit, and each is compared with the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import kda_workloads as W
+from _parity import check, oracle_full, to_device, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _plan(kda, N, T, H):
+    return kda.prefill_query(kda.make_desc(N, T, H, 128, 128, kda.KDA_BF16))
+
+
+def _run(kda, d):
+    g = to_device(d)
+    out, fin = kda.prefill(g["q"], g["k"], g["v"], g["g"], g["beta"], g["cu_seqlens"], g["init_state"])
+    torch.cuda.synchronize()
+    assert kda.last_device_status() == kda.KDA_OK
+    return out.cpu(), fin.cpu()
+
+
+def _padded(d, extra_lens, seed):
+    """d with extra sequences appended (their own random inputs): same leading tokens and states."""
+    H = d["q"].shape[1]
+    cfg = W.random_prefill_config(extra_lens, H, 128, torch.bfloat16, init="normal")
+    e = W.make_prefill_inputs(cfg, seed=seed)
+    cat = lambda n: torch.cat([d[n], e[n]])
+    cu = torch.cat([d["cu_seqlens"], e["cu_seqlens"][1:] + d["cu_seqlens"][-1]])
+    return {"q": cat("q"), "k": cat("k"), "v": cat("v"), "g": cat("g"), "beta": cat("beta"),
+            "cu_seqlens": cu, "init_state": cat("init_state")}
+
+
+def test_plan_selects_the_path(cuda_lib):
+    split = _plan(cuda_lib, 1, 8192, 96)
+    assert split["kernel_launches"] == 3 and split["tensor_cores"] == 1
+    assert split["workspace_bytes"] >= (8192 // 64) * 96 * 98816
+    one = _plan(cuda_lib, 2, 8192, 96)          # 192 units: one CTA per (sequence, head)
+    assert one["kernel_launches"] == 1 and one["workspace_bytes"] == 0
+    long = _plan(cuda_lib, 1, 64 * 200, 96)     # 19,296 items: over the workspace cap
+    assert long["kernel_launches"] == 1 and long["workspace_bytes"] == 0
+
+
+@pytest.mark.parametrize("lens", [[300, 0, 641, 129], [64], [1], [0, 0, 100, 0, 64, 1], [17, 64, 65, 128, 191]],
+                         ids=["ragged", "one-chunk", "one-token", "empties", "boundaries"])
+def test_split_matches_oracle(cuda_lib, lens):
+    cfg = W.random_prefill_config(lens, 3, 128, torch.bfloat16, init="normal")
+    assert _plan(cuda_lib, len(lens), cfg.total_tokens, 3)["kernel_launches"] == 3
+    d = W.make_prefill_inputs(cfg, seed=sum(lens) + 5)
+    out, fin = _run(cuda_lib, d)
+    ref_o, ref_s = oracle_full(d)
+    check("split out", out, ref_o, tol_for(torch.bfloat16))
+    check("split final state", fin, ref_s, tol_for(torch.bfloat16))
+
+
+def test_split_and_one_cta_per_head_agree_bitwise(cuda_lib):
+    H = 4
+    lens = [300, 0, 641, 129]
+    cfg = W.random_prefill_config(lens, H, 128, torch.bfloat16, init="normal")
+    d = W.make_prefill_inputs(cfg, seed=90)
+    extra = [64 + 3 * i for i in range(30)]                       # 34 x 4 = 136 units
+    p = _padded(d, extra, seed=91)
+    T0 = cfg.total_tokens
+    assert _plan(cuda_lib, len(lens), T0, H)["kernel_launches"] == 3
+    assert _plan(cuda_lib, len(lens) + len(extra), p["q"].shape[0], H)["kernel_launches"] == 1
+    o_split, s_split = _run(cuda_lib, d)
+    o_one, s_one = _run(cuda_lib, p)
+    diff_o = (o_split - o_one[:T0]).abs().max().item()
+    diff_s = (s_split - s_one[:len(lens)]).abs().max().item()
+    assert torch.equal(o_split, o_one[:T0]) and torch.equal(s_split, s_one[:len(lens)]), (diff_o, diff_s)
+    # and the one-CTA-per-head run against the oracle, padding sequences included
+    ref_o, ref_s = oracle_full(p)
+    check("one-CTA-per-head out", o_one, ref_o, tol_for(torch.bfloat16))
+    check("one-CTA-per-head final state", s_one, ref_s, tol_for(torch.bfloat16))
+
+
+def test_split_checkpoints_and_in_place_state(cuda_lib):
+    """Checkpoints from the state scan equal the state after each prefix; in-place chaining."""
+    H, L = 2, 512
+    cfg = W.random_prefill_config([L], H, 128, torch.bfloat16, init="normal")
+    d = W.make_prefill_inputs(cfg, seed=92)
+    g = to_device(d)
+    state = g["init_state"].clone()
+    out, fin, ck = cuda_lib.prefill(g["q"], g["k"], g["v"], g["g"], g["beta"], g["cu_seqlens"], state,
+                                    final_state=state, checkpoint_interval=128, checkpoint_slots=4)
+    torch.cuda.synchronize()
+    assert cuda_lib.last_device_status() == cuda_lib.KDA_OK and fin.data_ptr() == state.data_ptr()
+    for j in range(4):
+        sub = {n: d[n][:128 * (j + 1)] for n in ("q", "k", "v", "g", "beta")}
+        sub["cu_seqlens"] = torch.tensor([0, 128 * (j + 1)], dtype=torch.int32)
+        sub["init_state"] = d["init_state"]
+        _, ref_s = oracle_full(sub)
+        check(f"checkpoint {j}", ck[:, :, j].cpu(), ref_s, tol_for(torch.bfloat16))
+    _, ref_final = oracle_full(d)
+    check("in-place final", state.cpu(), ref_final, tol_for(torch.bfloat16))
+
+
+def test_split_workspace_rules(cuda_lib):
+    cfg = W.random_prefill_config([200], 2, 128, torch.bfloat16, init="zero")
+    g = to_device(W.make_prefill_inputs(cfg, seed=93))
+    desc = cuda_lib.make_desc(1, 200, 2, 128, 128, cuda_lib.KDA_BF16)
+    need = cuda_lib.prefill_workspace_bytes(desc)
+    assert need > 0
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(cuda_lib.KDAError) as e:
+        cuda_lib.prefill(g["q"], g["k"], g["v"], g["g"], g["beta"], g["cu_seqlens"], None, workspace=small)
+    assert e.value.status == cuda_lib.KDA_ERR_WORKSPACE
+    ws = torch.empty(need + 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(cuda_lib.KDAError) as e:   # not 16-byte aligned
+        cuda_lib.prefill(g["q"], g["k"], g["v"], g["g"], g["beta"], g["cu_seqlens"], None, workspace=ws[8:])
+    assert e.value.status == cuda_lib.KDA_ERR_INVALID_ARG
+    # a reused workspace gives the same bits
+    o1, _ = cuda_lib.prefill(g["q"], g["k"], g["v"], g["g"], g["beta"], g["cu_seqlens"], None, workspace=ws)
+    o2, _ = cuda_lib.prefill(g["q"], g["k"], g["v"], g["g"], g["beta"], g["cu_seqlens"], None, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
