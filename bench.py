@@ -39,8 +39,12 @@ import kda_workloads as W  # noqa: E402
 METRIC = "KDA prefill tokens/s (×tensor-peak %) and decode state GB/s (×HBM-peak %), 1 GB300"
 UNIT = "tokens/s"
 E2E_SEGMENT_TOKENS = 1024
-PREFILL_KERNEL_SRC = ("linear_attention_serving_chunkwise_gb300/csrc/kda_prefill_tc.cu",
+# the kernels one bench-size kda_prefill call runs (the chunk-parallel split path)
+PREFILL_KERNEL_SRC = ("linear_attention_serving_chunkwise_gb300/csrc/kda_prefill_split.cu",
+                      "linear_attention_serving_chunkwise_gb300/csrc/kda_prefill_tc_phases.cuh",
                       "linear_attention_serving_chunkwise_gb300/csrc/kda_sm100.cuh")
+PREFILL_KERNELS = "kda_chunk_offsets_kernel + kda_chunk_prep_kernel + kda_state_scan_kernel"
+
 
 
 # --------------------------------------------------------------------------- helpers
@@ -217,10 +221,10 @@ def run_reference(args, world, rank):
 
 
 # --------------------------------------------------------------------------- CUDA arm
-def _time_prefill(kda, d, out, fin, stream, steps, warmup):
+def _time_prefill(kda, d, out, fin, ws, stream, steps, warmup):
     args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])
     for _ in range(warmup):
-        kda.prefill(*args, out=out, final_state=fin, stream=stream)
+        kda.prefill(*args, out=out, final_state=fin, workspace=ws, stream=stream)
     stream.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     return args, evs
@@ -246,7 +250,8 @@ def run_cuda(args, world, rank, local):
     fin = torch.empty((1, cfg.num_heads, cfg.dk, cfg.dv), dtype=torch.float32, device=dev)
     desc = kda.make_desc(1, cfg.total_tokens, cfg.num_heads, cfg.dk, cfg.dv, kda.KDA_BF16)
     plan = kda.prefill_query(desc)
-    pargs, evs = _time_prefill(kda, d, out, fin, stream, args.steps, args.warmup)
+    ws = torch.empty(max(plan["workspace_bytes"], 16), dtype=torch.uint8, device=dev)   # allocated once
+    pargs, evs = _time_prefill(kda, d, out, fin, ws, stream, args.steps, args.warmup)
     if kda.last_device_status(stream) != kda.KDA_OK:
         raise RuntimeError("prefill reported a device error during warm-up")
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -257,7 +262,7 @@ def run_cuda(args, world, rank, local):
     start.record(stream)
     for i in range(args.steps):
         evs[i][0].record(stream)
-        kda.prefill(*pargs, out=out, final_state=fin, stream=stream)
+        kda.prefill(*pargs, out=out, final_state=fin, workspace=ws, stream=stream)
         evs[i][1].record(stream)
     end.record(stream)
     stream.synchronize()
@@ -281,7 +286,11 @@ def run_cuda(args, world, rank, local):
                 "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
                 "algorithmic_bytes_per_launch": alg_bytes, "kernel_launches_per_call": plan["kernel_launches"],
-                "launch_ms": launch_ms}
+                "launch_ms": launch_ms,
+                "kernels": PREFILL_KERNELS if plan["kernel_launches"] == 3 else "kda_prefill_tc_kernel",
+                "timed": "CUDA events on the launching stream around each kda_prefill call (all its launches); "
+                         "per-kernel shares in profiles/bench_launch_list_prefill_decode.md",
+                "workspace_bytes": plan["workspace_bytes"]}
     tensor = {"achieved": achieved_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
               "frac": achieved_tflops / peaks["bf16_tflops"], "algorithmic_flops_per_launch": alg_flops,
               "uses_tensor_cores": bool(plan["tensor_cores"])}
@@ -403,7 +412,9 @@ def run_cuda(args, world, rank, local):
 def run_ncu_case(case: str):
     """A small, self-contained launch for ncu captures (no timing, no JSON): the same kernels
     as the bench on inputs still larger than L2 but only a few hundred MB on the device.
-      prefill: B=1, H=32, T=8192, dk=dv=128, bf16 (470 MB of inputs/outputs)
+      prefill: B=1, H=32, T=8192, dk=dv=128, bf16 (470 MB of inputs/outputs; the
+               chunk-parallel split path: offsets, chunk prep, state scan)
+      prefill_one_cta: 5 sequences of 2048 tokens, H=32 (160 units: one CTA per (sequence, head))
       decode:  B=64, H=96, dk=dv=128, bf16, one step (403 MB of state)
       decode_multi: the same B, H with K = 4 tokens per sequence in one call"""
     import linear_attention_serving_chunkwise_gb300 as kda
@@ -412,6 +423,11 @@ def run_ncu_case(case: str):
     kda.load()
     if case == "prefill":
         cfg = W.PrefillConfig("ncu_prefill_h32_t8192", (8192,), 32, 128, 128, torch.bfloat16, "normal")
+        d = W.make_prefill_inputs(cfg, seed=0, device="cuda")
+        for _ in range(2):
+            kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])
+    elif case == "prefill_one_cta":
+        cfg = W.PrefillConfig("ncu_prefill_one_cta_5x2048_h32", (2048,) * 5, 32, 128, 128, torch.bfloat16, "normal")
         d = W.make_prefill_inputs(cfg, seed=0, device="cuda")
         for _ in range(2):
             kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])
@@ -439,7 +455,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--ncu-case", default=None, choices=["prefill", "decode", "decode_multi"],
+    ap.add_argument("--ncu-case", default=None, choices=["prefill", "prefill_one_cta", "decode", "decode_multi"],
                     help="run one small launch pair for an ncu capture and exit")
     args = ap.parse_args()
     if args.ncu_case:

@@ -81,7 +81,11 @@ const char* kda_status_string(kda_status status);
 
 /*
  * Bytes of device scratch memory kda_prefill needs for `desc` (may be 0).
- * Returns 0 for a desc that kda_prefill would reject.
+ * Returns 0 for a desc that kda_prefill would reject.  Non-zero exactly when the
+ * chunkwise form runs chunk-parallel: bf16, dk = dv = 128, num_seqs * num_heads <= 120
+ * and (total_tokens / 64 + num_seqs) * num_heads <= 16384.  The workspace then holds
+ * the chunk offsets and, per (64-token chunk, head), the operands of that chunk's state
+ * step: 98,816 bytes each, for (total_tokens / 64 + num_seqs) * num_heads chunks.
  */
 size_t kda_prefill_workspace_bytes(const kda_prefill_desc* desc);
 
@@ -116,8 +120,12 @@ kda_status kda_prefill_query(const kda_prefill_desc* desc, kda_prefill_plan* pla
  *                            pointer as init_state (in-place chaining of calls);
  *                            any other overlap with an input is rejected.
  *   workspace   device scratch of at least kda_prefill_workspace_bytes(desc)
- *               (may be NULL when that is 0); its contents need no set-up and
- *               are clobbered.  Two calls in flight at once need two workspaces.
+ *               (may be NULL when that is 0), 16-byte aligned, overlapping no
+ *               input or output; its contents need no set-up and are clobbered.
+ *               Two calls in flight at once need two workspaces.  With a
+ *               workspace the call runs three kernels (chunk offsets; the
+ *               state-independent operands of every (chunk, head) at once; the
+ *               state scan), otherwise one; both give bit-identical results.
  * A cu_seqlens entry that breaks the rules above is found on the device: that
  * sequence is skipped and kda_last_device_status() returns KDA_ERR_INVALID_ARG.
  */

@@ -51,10 +51,12 @@ bool uses_tensor_cores(const kda_prefill_desc& d)
 }
 
 // The chunk-parallel split (per-chunk operands for all chunks at once through the workspace,
-// then the state scan) runs when few (sequence, head) units would leave most SMs idle under
-// the one-CTA-per-head kernel, and its operand workspace (98,816 bytes per (chunk, head))
-// stays within kSplitMaxItems items; otherwise the one-CTA-per-head kernel runs.
-constexpr long long kSplitMaxUnits = 128;
+// then the state scan) runs when few (sequence, head) units would leave SMs idle under the
+// one-CTA-per-head kernel, and its operand workspace (98,816 bytes per (chunk, head)) stays
+// within kSplitMaxItems items; otherwise the one-CTA-per-head kernel runs.  On a 152-SM
+// GB300 with 8192-token sequences the two take the same time at about 120 units (split:
+// 1.199 ms at 96, 1.406 ms at 120; one CTA per unit: 1.41 ms up to 152 units).
+constexpr long long kSplitMaxUnits = 120;
 constexpr long long kSplitMaxItems = 16384;
 
 bool uses_split(const kda_prefill_desc& d)

@@ -74,6 +74,7 @@ struct SplitParams {
     TcParams p;                 // inputs, outputs, tensor maps, status (as the one-CTA-per-head kernel)
     uint8_t* ops;               // operand images, item (global chunk gc, head h) at ((gc * H) + h) * IMG_BYTES
     int32_t* chunk_off;         // [num_seqs + 1]: first global chunk of each sequence
+    int2* chunk_info;           // [chunks]: (first token, end of its sequence) of each global chunk
 };
 
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar)
@@ -98,16 +99,36 @@ __device__ __forceinline__ void prefetch_l2(const void* gsrc, uint32_t bytes)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
 }
 
-// the prep kernel stages each 32 KB piece of an item's image here (the v buffers of the
-// shared map, which it does not use) and writes it with one bulk store
+// the prep kernel stages each 32 KB piece of an item's image in shared memory and writes it
+// with one bulk store: K~ and [Tb; M] in the v buffers of the shared map (which it does not
+// use), [-Wk; Q'] in the part of the X region that holds the state operand in the
+// one-CTA-per-head kernel (free here from phase 3 on), so that its staging need not wait
+// for the [Tb; M] store to leave.  beta comes by cp.async into two buffers, one item ahead.
 constexpr uint32_t A_STAGE = OFF_V0;
+constexpr uint32_t A_STAGE2 = OFF_X + X_SB;
+constexpr uint32_t A_BETA2 = (uint32_t)SMEM_USED;
+constexpr size_t A_SMEM_BYTES = SMEM_BYTES + 256;
 static_assert(OFF_V1 + 16384 == A_STAGE + 32768, "staging buffer");
+static_assert(A_STAGE2 % 1024 == 0 && X_SB >= X_SY + 32 * LDY * 4 && X_SB + 32768 <= 81920, "second staging buffer");
+static_assert(A_BETA2 % 16 == 0, "beta buffer");
+
+__device__ __forceinline__ void cp_async4_zfill(void* smem_dst, const void* gsrc, bool valid)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_prev() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // ---------------------------------------------------------------- step 1: chunk offsets
 // One CTA of 1024 threads: chunk_off[n] = sum over m < n of ceil(len_m / 64), lengths of
-// sequences that fail the cu_seqlens check counted as 0 (and the failure reported).
+// sequences that fail the cu_seqlens check counted as 0 (and the failure reported); then
+// chunk_info[gc] = (first token, end of the sequence) of every global chunk, so that a
+// chunk's item needs one load and no search.
 __global__ void __launch_bounds__(1024) kda_chunk_offsets_kernel(const int32_t* cu_seqlens, int num_seqs,
-                                                                 int total_tokens, int32_t* chunk_off, int* status)
+                                                                 int total_tokens, int32_t* chunk_off,
+                                                                 int2* chunk_info, int* status)
 {
     __shared__ int warp_sums[32];
     __shared__ int carry;
@@ -146,18 +167,21 @@ __global__ void __launch_bounds__(1024) kda_chunk_offsets_kernel(const int32_t* 
         __syncthreads();
     }
     if (t == 0) chunk_off[num_seqs] = carry;
-}
-
-// Sequence of global chunk gc: the last n with chunk_off[n] <= gc (binary search).
-__device__ __forceinline__ int seq_of_chunk(const int32_t* chunk_off, int num_seqs, int gc)
-{
-    int lo = 0, hi = num_seqs - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(chunk_off + mid) <= gc) lo = mid;
-        else hi = mid - 1;
+    __syncthreads();
+    // chunk gc belongs to the last n with chunk_off[n] <= gc (chunk_off written above by this
+    // CTA: plain loads)
+    const int total = carry;
+    for (int gc = t; gc < total; gc += 1024) {
+        int lo = 0, hi = num_seqs - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (chunk_off[mid] <= gc) lo = mid;
+            else hi = mid - 1;
+        }
+        int bos, eos;
+        seq_bounds(cu_seqlens, lo, num_seqs, total_tokens, status, bos, eos);   // valid: it has chunks
+        chunk_info[gc] = make_int2(bos + 64 * (gc - chunk_off[lo]), eos);
     }
-    return lo;
 }
 
 // ---------------------------------------------------------------- step 2: per-item operands
@@ -165,17 +189,16 @@ struct Item {
     int h, t0, eos, gc;
 };
 
+// item = gc * H + h; the (t0, eos) load is first used an item later
 __device__ __forceinline__ Item item_at(const SplitParams& sp, int item)
 {
     const int H = sp.p.num_heads;
     Item it;
     it.gc = item / H;
     it.h = item - it.gc * H;
-    const int n = seq_of_chunk(sp.chunk_off, sp.p.num_seqs, it.gc);
-    int bos, eos;
-    seq_bounds(sp.p.cu_seqlens, n, sp.p.num_seqs, sp.p.total_tokens, sp.p.status, bos, eos);   // valid: it has chunks
-    it.t0 = bos + 64 * (it.gc - __ldg(sp.chunk_off + n));
-    it.eos = eos;
+    const int2 info = __ldg(sp.chunk_info + it.gc);
+    it.t0 = info.x;
+    it.eos = info.y;
     return it;
 }
 
@@ -192,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     const int quarter = warp & 3, part = warp >> 2;
     const int L = 32 * quarter + lane;
     float* vec = reinterpret_cast<float*>(sm + OFF_VEC);
-    float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
+    auto sbeta_buf = [&](int b) { return reinterpret_cast<float*>(sm + (b ? A_BETA2 : OFF_BETA)); };
     uint64_t* bar_k = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint64_t* bar_qg = bar_k + 1;
     uint64_t* bar_mma = bar_k + 2;
@@ -223,7 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
 
     bool k_pending = false, qg_pending = false;   // thread 0 only
     int item = blockIdx.x;
-    Item cur{};
+    // the current and next items; the one after is looked up an item ahead of its use, so
+    // that its dependent loads (chunk offsets, then cu_seqlens) are never waited for
+    Item cur{}, nxt{};
+    if (item + (int)gridDim.x < items) nxt = item_at(sp, item + gridDim.x);
     if (item < items) {
         cur = item_at(sp, item);
         if (t == 0) {
@@ -232,20 +258,27 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
             k_pending = qg_pending = true;
         }
     }
-    float beta_next = (item < items && t < 64 && cur.t0 + t < cur.eos)
-                          ? __ldg(p.beta + (size_t)(cur.t0 + t) * H + cur.h)
-                          : 0.f;
+    // beta of an item (tokens t0 .. t0 + 63, zero past the sequence's end) into buffer b
+    auto fetch_beta = [&](const Item& it, int b) {
+        if (t < 64) {
+            const bool valid = it.t0 + t < it.eos;
+            cp_async4_zfill(sbeta_buf(b) + t, valid ? p.beta + (size_t)(it.t0 + t) * H + it.h : p.beta, valid);
+            cp_async_commit_wait_prev();
+        }
+    };
+    if (item < items) fetch_beta(cur, 0);
     uint32_t k_par = 0, qg_par = 0, mma_par = 0;
     bool ok = true;
 
-    for (; item < items; item += gridDim.x) {
+    for (int li = 0; item < items; item += gridDim.x, ++li) {
+        const float* sbeta = sbeta_buf(li & 1);
         const int h = cur.h, t0 = cur.t0;
         const int BT = min(64, cur.eos - t0);
         uint8_t* img = sp.ops + ((size_t)cur.gc * H + h) * IMG_BYTES;
         const bool has_next = item + (int)gridDim.x < items;
-        const Item nxt = has_next ? item_at(sp, item + gridDim.x) : cur;
-        if (t < 64) sbeta[t] = beta_next;
-        if (t == 0) bulk_wait_read();   // the previous item's last piece has left the staging buffer
+        const Item nxt2 = (item + 2LL * gridDim.x < items) ? item_at(sp, item + 2 * gridDim.x) : nxt;
+        if (t < 64) cp_async_wait_all();   // this item's beta
+        if (t == 0) bulk_wait_read();   // the previous item's pieces have left the staging buffers
         if (!(mbar_wait_bounded(bar_k, k_par, kWaitNs) && mbar_wait_bounded(bar_qg, qg_par, kWaitNs)))
             atomicExch(s_abort, 1);
         tc_fence_before_sync();
@@ -258,8 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         k_par ^= 1u;
         qg_par ^= 1u;
         if (t == 0) k_pending = qg_pending = false;
-        if (t < 64)
-            beta_next = (has_next && nxt.t0 + t < nxt.eos) ? __ldg(p.beta + (size_t)(nxt.t0 + t) * H + nxt.h) : 0.f;
+        if (has_next) fetch_beta(nxt, (li + 1) & 1);   // the buffer the previous item used
 
         // ---- phase 1: decayed operands
         phase1_cumsum(sm, vec, t, BT);
@@ -400,7 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
             for (int ks = 0; ks < 4; ++ks)
                 umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPL + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
             umma_commit(bar_mma);
-            bulk_wait_read();   // the [Tb; M] piece has left the staging buffer
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
@@ -414,16 +445,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
             for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                st_shared_v4(sbase + A_STAGE + sw128_chunk(L, 4 * part + q, 128), pk[4 * q], pk[4 * q + 1],
+                st_shared_v4(sbase + A_STAGE2 + sw128_chunk(L, 4 * part + q, 128), pk[4 * q], pk[4 * q + 1],
                              pk[4 * q + 2], pk[4 * q + 3]);
             fence_proxy_async_smem();
         }
         __syncthreads();
         if (t == 0) {
-            bulk_store(img + IMG_A1, sm + A_STAGE, 32768);
+            bulk_store(img + IMG_A1, sm + A_STAGE2, 32768);
             bulk_commit();
         }
         cur = nxt;   // the next item's first barrier orders these TMEM reads before its writes
+        nxt = nxt2;
     }
 
     if (t == 0) bulk_wait_all();   // the images are written before the CTA's shared memory goes away
@@ -485,18 +517,22 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
     tc_fence_after_sync();
     const uint32_t tm = *tslot;
 
-    // thread 0's copies in flight, for the bounded clean-up on abort
-    bool f_pending = false, b_pending = false, o_pending = false, mma_open = false;
-    uint32_t v_pending = 0;   // bit b: a v copy into buffer b in flight
+    // The copies into shared memory are issued by one producer thread (kProducer, in a warp
+    // of the O half, which has slack when they are due); it counts what it issued so that,
+    // on abort, it can wait for the last copy on each barrier.  Thread 0 issues the MMAs and
+    // the O stores.
+    constexpr int kProducer = 64;
+    bool o_pending = false, mma_open = false;   // thread 0
+    int n_front = 0, n_back = 0, n_v[2] = {0, 0};   // producer
     auto fetch_front = [&](int c) {
         mbar_arrive_expect_tx(bar_f, IMG_FRONT);
         bulk_load(sm + B_A1, image(c), IMG_FRONT, bar_f);
-        f_pending = true;
+        ++n_front;
     };
     auto fetch_back = [&](int c) {
         mbar_arrive_expect_tx(bar_b, IMG_BACK);
         bulk_load(sm + B_KTH, image(c) + IMG_KTH, IMG_BACK, bar_b);
-        b_pending = true;
+        ++n_back;
     };
     auto fetch_v = [&](int c) {   // [64 tok][128 ch] as two 64-channel TMA boxes
         uint64_t* bar = bar_v + (c & 1);
@@ -504,9 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
         mbar_arrive_expect_tx(bar, 16384u);
         tma_load_3d(dst, &p.tm_v, bar, 0, h, bos + 64 * c);
         tma_load_3d(dst + 8192, &p.tm_v, bar, 64, h, bos + 64 * c);
-        v_pending |= 1u << (c & 1);
+        if (c & 1) ++n_v[1];
+        else ++n_v[0];
     };
-    if (t == 0 && nchunks > 0) {
+    if (t == kProducer && nchunks > 0) {
         fetch_front(0);
         fetch_back(0);
         fetch_v(0);
@@ -540,10 +577,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
         const int t0 = bos + 64 * ci;
         const int BT = min(64, eos - t0);
         const int vb = ci & 1;
-        if (t == 0 && o_pending) {   // the previous chunk's O staging has been read out
-            bulk_wait_read();
-            o_pending = false;
-        }
         if (!mbar_wait_bounded(bar_f, f_par, kWaitNs)) atomicExch(s_abort, 1);
         tc_fence_before_sync();
         __syncthreads();
@@ -553,7 +586,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
             break;
         }
         f_par ^= 1u;
-        if (t == 0) f_pending = false;
 
         // the state's bf16 B operand; S <- gamma_C S (this chunk's decay, before its update)
         // runs while the D1 MMAs, which read only the bf16 copy, execute
@@ -580,7 +612,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
                 atomicExch(s_abort, 1);
             } else {
                 v_par ^= 1u << vb;
-                v_pending &= ~(1u << vb);
                 const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
                 const uint32_t vt = sbase + (vb ? B_V1 : B_V0);
 #pragma unroll
@@ -597,6 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
                 umma_commit(bar_mma);
                 mma_open = true;
             }
+            if (o_pending) {   // the previous chunk's O staging has been read out (rewritten below)
+                bulk_wait_read();
+                o_pending = false;
+            }
         }
         {
             const float gc = sgam[L];
@@ -608,8 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        if (t == 0) {   // the front image and this v buffer have been read
-            mma_open = false;
+        if (t == 0) mma_open = false;
+        if (t == kProducer) {   // the front image and this v buffer have been read
             if (ci + 1 < nchunks) fetch_front(ci + 1);
             if (ci + 2 < nchunks) {
                 fetch_v(ci + 2);
@@ -635,7 +670,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
                     atomicExch(s_abort, 1);
                 } else {
                     b_par ^= 1u;
-                    b_pending = false;
                     const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
@@ -669,9 +703,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
+        if (t == kProducer && ci + 1 < nchunks) fetch_back(ci + 1);
         if (t == 0) {
             mma_open = false;
-            if (ci + 1 < nchunks) fetch_back(ci + 1);
             if (BT == 64) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) tma_store_3d(&p.tm_o, sm + B_OST + 8192 * j, 32 * j, h, t0);
@@ -710,26 +744,41 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
         for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     }
     if (!ok && t == 0) {
-        // a wait gave up: record it, let in-flight copies and MMAs land (bounded), then leave
+        // a wait gave up: record it, let in-flight MMAs land (bounded), then leave
         report_status(p.status, kDevTimeout);
-        if (f_pending) mbar_wait_bounded(bar_f, f_par, kWaitNs);
-        if (b_pending) mbar_wait_bounded(bar_b, b_par, kWaitNs);
-        for (int i = 0; i < 2; ++i)
-            if ((v_pending >> i) & 1u) mbar_wait_bounded(bar_v + i, (v_par >> i) & 1u, kWaitNs);
         if (mma_open) mbar_wait_bounded(bar_mma, mma_par, kWaitNs);
+    }
+    if (!ok && t == kProducer) {   // and the copies: the last one issued on each barrier (bounded)
+        if (n_front > 0) mbar_wait_bounded(bar_f, (uint32_t)(n_front - 1) & 1u, kWaitNs);
+        if (n_back > 0) mbar_wait_bounded(bar_b, (uint32_t)(n_back - 1) & 1u, kWaitNs);
+        for (int i = 0; i < 2; ++i)
+            if (n_v[i] > 0) mbar_wait_bounded(bar_v + i, (uint32_t)(n_v[i] - 1) & 1u, kWaitNs);
     }
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, B_TM_COLS);
 }
 
+// workspace: chunk_off [N + 1] int32, chunk_info [chunks] int2, then the operand images
+struct SplitWorkspace {
+    size_t chunks, off_bytes, info_bytes, total;
+};
+
+SplitWorkspace split_workspace(int num_seqs, int total_tokens, int num_heads)
+{
+    SplitWorkspace w;
+    w.chunks = (size_t)total_tokens / 64 + (size_t)num_seqs;   // >= the sum of ceil(len / 64)
+    w.off_bytes = ((size_t)(num_seqs + 1) * sizeof(int32_t) + 255) & ~(size_t)255;
+    w.info_bytes = (w.chunks * sizeof(int2) + 255) & ~(size_t)255;
+    w.total = w.off_bytes + w.info_bytes + w.chunks * (size_t)num_heads * IMG_BYTES;
+    return w;
+}
+
 }  // namespace
 
 size_t prefill_split_workspace_bytes(int num_seqs, int total_tokens, int num_heads)
 {
-    const size_t chunks = (size_t)total_tokens / 64 + (size_t)num_seqs;   // >= the sum of ceil(len / 64)
-    const size_t offs = ((size_t)(num_seqs + 1) * sizeof(int32_t) + 255) & ~(size_t)255;
-    return offs + chunks * (size_t)num_heads * IMG_BYTES;
+    return split_workspace(num_seqs, total_tokens, num_heads).total;
 }
 
 cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream)
@@ -756,24 +805,26 @@ cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream)
     p.num_heads = a.num_heads;
     p.status = a.status;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    const SplitWorkspace wl = split_workspace(a.num_seqs, a.total_tokens, a.num_heads);
     sp.chunk_off = reinterpret_cast<int32_t*>(ws);
-    sp.ops = ws + (((size_t)(a.num_seqs + 1) * sizeof(int32_t) + 255) & ~(size_t)255);
+    sp.chunk_info = reinterpret_cast<int2*>(ws + wl.off_bytes);
+    sp.ops = ws + wl.off_bytes + wl.info_bytes;
 
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kda_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        e = cudaFuncSetAttribute(kda_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)A_SMEM_BYTES);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kda_state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)B_SMEM_BYTES);
     if (e != cudaSuccess) return e;
 
     kda_chunk_offsets_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.num_seqs, a.total_tokens, sp.chunk_off,
-                                                      a.status);
+                                                      sp.chunk_info, a.status);
     const long long items_max = ((long long)a.total_tokens / 64 + a.num_seqs) * a.num_heads;
     const long long prep_grid = std::max(1LL, std::min<long long>(sms, items_max));
-    kda_chunk_prep_kernel<<<(unsigned)prep_grid, kThreads, SMEM_BYTES, stream>>>(sp);
+    kda_chunk_prep_kernel<<<(unsigned)prep_grid, kThreads, A_SMEM_BYTES, stream>>>(sp);
     kda_state_scan_kernel<<<(unsigned)((long long)a.num_seqs * a.num_heads), kThreads, B_SMEM_BYTES, stream>>>(sp);
     return cudaGetLastError();
 }

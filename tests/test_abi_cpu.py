@@ -97,6 +97,34 @@ def test_prefill_query(lib):
         kda.prefill_query(kda.make_desc(1, 10, 4, 96, 96, kda.KDA_F32))
 
 
+def test_prefill_path_selection_and_split_workspace(lib):
+    """bf16, dk = dv = 128 with at most 120 (sequence, head) units and at most 16384 (chunk, head)
+    items: the three-launch chunk-parallel path, whose workspace holds the chunk offsets, the
+    chunk table and 98,816 bytes of operands per item; otherwise one launch, no workspace."""
+    def plan(N, T, H, dt=kda.KDA_BF16, d=128):
+        return kda.prefill_query(kda.make_desc(N, T, H, d, d, dt))
+    p = plan(1, 8192, 96)
+    items = (8192 // 64 + 1) * 96
+    assert p["kernel_launches"] == 3 and p["tensor_cores"] == 1
+    assert items * 98816 <= p["workspace_bytes"] <= items * 98816 + 4096
+    assert plan(1, 8192, 120)["kernel_launches"] == 3
+    assert plan(1, 8192, 121)["kernel_launches"] == 1 and plan(1, 8192, 121)["workspace_bytes"] == 0
+    assert plan(2, 8192, 64)["kernel_launches"] == 1                 # 128 units
+    assert plan(1, 64 * 200, 96)["kernel_launches"] == 1             # 19,296 items
+    assert plan(1, 8192, 96, kda.KDA_F32)["kernel_launches"] == 1    # fp32 inputs: CUDA-core kernel
+    assert plan(1, 8192, 96, d=64)["kernel_launches"] == 1
+
+
+def test_split_workspace_rejected_on_host(lib):
+    d = kda.make_desc(1, 200, 2, 128, 128, kda.KDA_BF16)
+    n = kda.prefill_workspace_bytes(d)
+    assert n > 0
+    assert _prefill(lib, d, ws=None, ws_bytes=n) == kda.KDA_ERR_INVALID_ARG           # missing
+    assert _prefill(lib, d, ws=0x1000008, ws_bytes=n) == kda.KDA_ERR_INVALID_ARG      # misaligned
+    assert _prefill(lib, d, ws=0x10000, ws_bytes=n) == kda.KDA_ERR_INVALID_ARG        # over q
+    assert _prefill(lib, d, ws=0x60000 - 256, ws_bytes=n) == kda.KDA_ERR_INVALID_ARG  # over out
+
+
 def test_decode_rejects_bad_arguments_on_host(lib):
     f = _fake
     args = lambda **kw: [kw.get(n, f(a)) for n, a in

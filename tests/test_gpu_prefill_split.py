@@ -1,6 +1,6 @@
 """GPU tests of the chunk-parallel prefill path: per-chunk operands for every (sequence, head,
 chunk) at once, then the state scan.  kda_prefill takes it for bf16, dk = dv = 128 calls with
-at most 128 (sequence, head) units; more units run the one-CTA-per-head kernel.  The two
+at most 120 (sequence, head) units; more units run the one-CTA-per-head kernel.  The two
 issue the same tensor-core instructions on the same operands, so their results are compared
 bit for bit, and each is compared with the oracle."""
 import numpy as np
@@ -42,6 +42,8 @@ def test_plan_selects_the_path(cuda_lib):
     assert split["workspace_bytes"] >= (8192 // 64) * 96 * 98816
     one = _plan(cuda_lib, 2, 8192, 96)          # 192 units: one CTA per (sequence, head)
     assert one["kernel_launches"] == 1 and one["workspace_bytes"] == 0
+    assert _plan(cuda_lib, 1, 8192, 120)["kernel_launches"] == 3
+    assert _plan(cuda_lib, 1, 8192, 121)["kernel_launches"] == 1
     long = _plan(cuda_lib, 1, 64 * 200, 96)     # 19,296 items: over the workspace cap
     assert long["kernel_launches"] == 1 and long["workspace_bytes"] == 0
 
@@ -63,7 +65,7 @@ def test_split_and_one_cta_per_head_agree_bitwise(cuda_lib):
     lens = [300, 0, 641, 129]
     cfg = W.random_prefill_config(lens, H, 128, torch.bfloat16, init="normal")
     d = W.make_prefill_inputs(cfg, seed=90)
-    extra = [64 + 3 * i for i in range(30)]                       # 34 x 4 = 136 units
+    extra = [64 + 3 * i for i in range(30)]                       # 34 x 4 = 136 units (> 120)
     p = _padded(d, extra, seed=91)
     T0 = cfg.total_tokens
     assert _plan(cuda_lib, len(lens), T0, H)["kernel_launches"] == 3
