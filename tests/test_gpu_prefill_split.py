@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import kda_workloads as W
-from _parity import check, oracle_full, to_device, tol_for
+from _parity import check, oracle_full, oracle_heads, to_device, tol_for
 
 pytestmark = pytest.mark.gpu
 
@@ -121,3 +121,37 @@ def test_split_workspace_rules(cuda_lib):
     o2, _ = cuda_lib.prefill(g["q"], g["k"], g["v"], g["g"], g["beta"], g["cu_seqlens"], None, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2)
+
+
+def test_split_many_sequences_at_the_unit_limit(cuda_lib):
+    """40 sequences x 3 heads = 120 units (the split's limit), lengths 0..400 with empties:
+    every chunk's (first token, sequence end) comes from the chunk table."""
+    rng = np.random.default_rng(94)
+    lens = [int(x) for x in rng.integers(0, 401, size=40)]
+    lens[5] = lens[17] = 0
+    lens[23] = 64
+    cfg = W.random_prefill_config(lens, 3, 128, torch.bfloat16, init="normal")
+    assert _plan(cuda_lib, 40, cfg.total_tokens, 3)["kernel_launches"] == 3
+    d = W.make_prefill_inputs(cfg, seed=95)
+    out, fin = _run(cuda_lib, d)
+    ref_o, ref_s = oracle_full(d)
+    check("many-sequence split out", out, ref_o, tol_for(torch.bfloat16))
+    check("many-sequence split final state", fin, ref_s, tol_for(torch.bfloat16))
+
+
+def test_split_at_the_item_cap_sampled(cuda_lib):
+    """T = 16320, H = 64: (255 + 1) x 64 = 16384 items, the most the split takes (16384 tokens
+    would take the one-CTA-per-unit kernel).  Sampled heads against the oracle."""
+    H, T = 64, 16320
+    assert _plan(cuda_lib, 1, T, H)["kernel_launches"] == 3
+    assert _plan(cuda_lib, 1, T + 64, H)["kernel_launches"] == 1
+    cfg = W.PrefillConfig("cap", (T,), H, 128, 128, torch.bfloat16, "normal")
+    d = W.make_prefill_inputs(cfg, seed=96, device="cuda")
+    out, fin = cuda_lib.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])
+    torch.cuda.synchronize()
+    assert cuda_lib.last_device_status() == cuda_lib.KDA_OK
+    heads = [0, 37, 63]
+    host = {k: (None if v is None else v.cpu()) for k, v in d.items()}
+    ro, rs = oracle_heads(host, 0, heads, host["cu_seqlens"].numpy())
+    check("cap split out", out[:, heads].cpu(), ro, tol_for(torch.bfloat16))
+    check("cap split final state", fin[0, heads].cpu(), rs, tol_for(torch.bfloat16))
