@@ -414,7 +414,8 @@ def run_ncu_case(case: str):
     as the bench on inputs still larger than L2 but only a few hundred MB on the device.
       prefill: B=1, H=32, T=8192, dk=dv=128, bf16 (470 MB of inputs/outputs; the
                chunk-parallel split path: offsets, chunk prep, state scan)
-      prefill_one_cta: 5 sequences of 2048 tokens, H=32 (160 units: one CTA per (sequence, head))
+      prefill_one_cta: 4 sequences of 2048 tokens, H=38 (152 units, one full wave: one CTA
+               per (sequence, head))
       decode:  B=64, H=96, dk=dv=128, bf16, one step (403 MB of state)
       decode_multi: the same B, H with K = 4 tokens per sequence in one call"""
     import linear_attention_serving_chunkwise_gb300 as kda
@@ -427,7 +428,7 @@ def run_ncu_case(case: str):
         for _ in range(2):
             kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])
     elif case == "prefill_one_cta":
-        cfg = W.PrefillConfig("ncu_prefill_one_cta_5x2048_h32", (2048,) * 5, 32, 128, 128, torch.bfloat16, "normal")
+        cfg = W.PrefillConfig("ncu_prefill_one_cta_4x2048_h38", (2048,) * 4, 38, 128, 128, torch.bfloat16, "normal")
         d = W.make_prefill_inputs(cfg, seed=0, device="cuda")
         for _ in range(2):
             kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])

@@ -50,21 +50,33 @@ bool uses_tensor_cores(const kda_prefill_desc& d)
     return d.qkv_dtype == KDA_BF16 && d.dk == 128 && d.dv == 128 && d.total_tokens > 0 && d.num_seqs > 0;
 }
 
-// The chunk-parallel split (per-chunk operands for all chunks at once through the workspace,
-// then the state scan) runs when few (sequence, head) units would leave SMs idle under the
-// one-CTA-per-head kernel, and its operand workspace (98,816 bytes per (chunk, head)) stays
-// within kSplitMaxItems items; otherwise the one-CTA-per-head kernel runs.  On a 152-SM
-// GB300 with 8192-token sequences the two take the same time at about 120 units (split:
-// 1.199 ms at 96, 1.406 ms at 120; one CTA per unit: 1.41 ms up to 152 units).
-constexpr long long kSplitMaxUnits = 120;
-constexpr long long kSplitMaxItems = 16384;
+// Which tensor-core path a bf16, dk = dv = 128 call takes, from its shape alone.  One CTA per
+// (sequence, head) unit walks that unit's chunks; with U units on the GB300's 152 SMs that is
+// ceil(U / 152) waves of about 22.7 K cycles per chunk.  The chunk-parallel split runs the
+// state-independent work of every (chunk, head) item on all SMs (about 21 K cycles per
+// item) and then the state scan, again in ceil(U / 152) waves but of about 6.0 K cycles per
+// chunk; its workspace holds 98,816 bytes per item, at most kSplitMaxItems of them.  The
+// split is taken when its estimate is lower.  For 8192-token sequences that is up to 120
+// units (measured: 1.199 ms at 96 units and 1.38 ms at 117, against 1.42 ms for one CTA
+// per unit), and again from 153 to about 235 units, where one CTA per unit would run a
+// mostly idle second wave (160 units: 2.14 against 2.80 ms; 192: 2.42 against 2.81 ms).
+constexpr long long kGpuSMs = 152;
+constexpr long long kSplitMaxItems = 32768;
+constexpr long long kCyclesPerChunkOneCta = 227;     // hundreds of cycles
+constexpr long long kCyclesPerItemPrep = 210;
+constexpr long long kCyclesPerChunkScan = 60;
 
 bool uses_split(const kda_prefill_desc& d)
 {
     if (!uses_tensor_cores(d)) return false;
     const long long units = (long long)d.num_seqs * d.num_heads;
     const long long items = ((long long)d.total_tokens / 64 + d.num_seqs) * d.num_heads;
-    return units <= kSplitMaxUnits && items <= kSplitMaxItems;
+    if (items > kSplitMaxItems) return false;
+    const long long chunks = ((long long)d.total_tokens / d.num_seqs + 63) / 64;   // of an average sequence
+    const long long waves = (units + kGpuSMs - 1) / kGpuSMs;
+    const long long one_cta = waves * chunks * kCyclesPerChunkOneCta;
+    const long long split = items * kCyclesPerItemPrep / kGpuSMs + waves * chunks * kCyclesPerChunkScan;
+    return split < one_cta;
 }
 
 kda_status validate_prefill(const kda_prefill_desc* d)

@@ -98,19 +98,24 @@ def test_prefill_query(lib):
 
 
 def test_prefill_path_selection_and_split_workspace(lib):
-    """bf16, dk = dv = 128 with at most 120 (sequence, head) units and at most 16384 (chunk, head)
-    items: the three-launch chunk-parallel path, whose workspace holds the chunk offsets, the
-    chunk table and 98,816 bytes of operands per item; otherwise one launch, no workspace."""
+    """bf16, dk = dv = 128: the three-launch chunk-parallel path where its cost estimate beats
+    one CTA per (sequence, head) and its items fit the workspace cap (32768); its workspace
+    holds the chunk offsets, the chunk table and 98,816 bytes of operands per item.
+    Otherwise one launch, no workspace."""
     def plan(N, T, H, dt=kda.KDA_BF16, d=128):
         return kda.prefill_query(kda.make_desc(N, T, H, d, d, dt))
     p = plan(1, 8192, 96)
     items = (8192 // 64 + 1) * 96
     assert p["kernel_launches"] == 3 and p["tensor_cores"] == 1
     assert items * 98816 <= p["workspace_bytes"] <= items * 98816 + 4096
-    assert plan(1, 8192, 120)["kernel_launches"] == 3
-    assert plan(1, 8192, 121)["kernel_launches"] == 1 and plan(1, 8192, 121)["workspace_bytes"] == 0
-    assert plan(2, 8192, 64)["kernel_launches"] == 1                 # 128 units
-    assert plan(1, 64 * 200, 96)["kernel_launches"] == 1             # 19,296 items
+    assert plan(1, 8192, 112)["kernel_launches"] == 3
+    assert plan(1, 8192, 124)["kernel_launches"] == 1 and plan(1, 8192, 124)["workspace_bytes"] == 0
+    assert plan(2, 8192, 64)["kernel_launches"] == 1                 # 128 units of 4096 tokens
+    assert plan(1, 8192, 152)["kernel_launches"] == 1                # one full wave
+    assert plan(1, 8192, 160)["kernel_launches"] == 3                # a second wave of 8
+    assert plan(1, 8192, 240)["kernel_launches"] == 1                # a second wave of 88
+    assert plan(40, 8000, 3)["kernel_launches"] == 1                 # 120 short sequences
+    assert plan(1, 64 * 400, 96)["kernel_launches"] == 1             # 38,496 items: over the cap
     assert plan(1, 8192, 96, kda.KDA_F32)["kernel_launches"] == 1    # fp32 inputs: CUDA-core kernel
     assert plan(1, 8192, 96, d=64)["kernel_launches"] == 1
 

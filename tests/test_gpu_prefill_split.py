@@ -1,6 +1,6 @@
 """GPU tests of the chunk-parallel prefill path: per-chunk operands for every (sequence, head,
-chunk) at once, then the state scan.  kda_prefill takes it for bf16, dk = dv = 128 calls with
-at most 120 (sequence, head) units; more units run the one-CTA-per-head kernel.  The two
+chunk) at once, then the state scan.  kda_prefill picks it for bf16, dk = dv = 128 calls by a
+cost estimate from the shape (few units, or a partial second wave of one CTA per unit).  The two
 issue the same tensor-core instructions on the same operands, so their results are compared
 bit for bit, and each is compared with the oracle."""
 import numpy as np
@@ -40,11 +40,12 @@ def test_plan_selects_the_path(cuda_lib):
     split = _plan(cuda_lib, 1, 8192, 96)
     assert split["kernel_launches"] == 3 and split["tensor_cores"] == 1
     assert split["workspace_bytes"] >= (8192 // 64) * 96 * 98816
-    one = _plan(cuda_lib, 2, 8192, 96)          # 192 units: one CTA per (sequence, head)
+    one = _plan(cuda_lib, 2, 8192, 76)          # 152 units: one full wave of one CTA per unit
     assert one["kernel_launches"] == 1 and one["workspace_bytes"] == 0
-    assert _plan(cuda_lib, 1, 8192, 120)["kernel_launches"] == 3
-    assert _plan(cuda_lib, 1, 8192, 121)["kernel_launches"] == 1
-    long = _plan(cuda_lib, 1, 64 * 200, 96)     # 19,296 items: over the workspace cap
+    assert _plan(cuda_lib, 1, 8192, 112)["kernel_launches"] == 3
+    assert _plan(cuda_lib, 1, 8192, 124)["kernel_launches"] == 1
+    assert _plan(cuda_lib, 2, 8192, 96)["kernel_launches"] == 3   # 192 units: a second wave of 40
+    long = _plan(cuda_lib, 1, 64 * 400, 96)     # 38,496 items: over the workspace cap
     assert long["kernel_launches"] == 1 and long["workspace_bytes"] == 0
 
 
@@ -65,7 +66,7 @@ def test_split_and_one_cta_per_head_agree_bitwise(cuda_lib):
     lens = [300, 0, 641, 129]
     cfg = W.random_prefill_config(lens, H, 128, torch.bfloat16, init="normal")
     d = W.make_prefill_inputs(cfg, seed=90)
-    extra = [64 + 3 * i for i in range(30)]                       # 34 x 4 = 136 units (> 120)
+    extra = [64 + 3 * i for i in range(30)]                       # 34 x 4 = 136 short units
     p = _padded(d, extra, seed=91)
     T0 = cfg.total_tokens
     assert _plan(cuda_lib, len(lens), T0, H)["kernel_launches"] == 3
@@ -123,15 +124,15 @@ def test_split_workspace_rules(cuda_lib):
     assert torch.equal(o1, o2)
 
 
-def test_split_many_sequences_at_the_unit_limit(cuda_lib):
-    """40 sequences x 3 heads = 120 units (the split's limit), lengths 0..400 with empties:
-    every chunk's (first token, sequence end) comes from the chunk table."""
+def test_split_many_sequences(cuda_lib):
+    """30 sequences x 2 heads, lengths 0..400 with empties: every chunk's (first token,
+    sequence end) comes from the chunk table."""
     rng = np.random.default_rng(94)
-    lens = [int(x) for x in rng.integers(0, 401, size=40)]
+    lens = [int(x) for x in rng.integers(0, 401, size=30)]
     lens[5] = lens[17] = 0
     lens[23] = 64
-    cfg = W.random_prefill_config(lens, 3, 128, torch.bfloat16, init="normal")
-    assert _plan(cuda_lib, 40, cfg.total_tokens, 3)["kernel_launches"] == 3
+    cfg = W.random_prefill_config(lens, 2, 128, torch.bfloat16, init="normal")
+    assert _plan(cuda_lib, 30, cfg.total_tokens, 2)["kernel_launches"] == 3
     d = W.make_prefill_inputs(cfg, seed=95)
     out, fin = _run(cuda_lib, d)
     ref_o, ref_s = oracle_full(d)
@@ -140,9 +141,9 @@ def test_split_many_sequences_at_the_unit_limit(cuda_lib):
 
 
 def test_split_at_the_item_cap_sampled(cuda_lib):
-    """T = 16320, H = 64: (255 + 1) x 64 = 16384 items, the most the split takes (16384 tokens
-    would take the one-CTA-per-unit kernel).  Sampled heads against the oracle."""
-    H, T = 64, 16320
+    """T = 32704, H = 64: (511 + 1) x 64 = 32768 items, the most the split takes (64 more
+    tokens would take the one-CTA-per-unit kernel).  Sampled heads against the oracle."""
+    H, T = 64, 32704
     assert _plan(cuda_lib, 1, T, H)["kernel_launches"] == 3
     assert _plan(cuda_lib, 1, T + 64, H)["kernel_launches"] == 1
     cfg = W.PrefillConfig("cap", (T,), H, 128, 128, torch.bfloat16, "normal")
