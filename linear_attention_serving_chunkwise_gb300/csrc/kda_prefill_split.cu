@@ -7,8 +7,9 @@
 // state recurrence
 //   W = Tb V - Wk S,   O = Q' S + M V,   S <- Diag(gamma_C) S + K~^T W
 // then walks each (sequence, head)'s chunks in order.  Three launches per call:
-//   1  kda_chunk_offsets_kernel: per-sequence chunk offsets (prefix sums of ceil(len / 64))
-//      and the cu_seqlens check, into the workspace;
+//   1  kda_chunk_offsets_kernel: per-sequence chunk offsets (prefix sums of ceil(len / 64)),
+//      the cu_seqlens check, and a table of every chunk's (first token, sequence end), into
+//      the workspace;
 //   2  kda_chunk_prep_kernel: persistent CTAs over the items.  Each item runs the phases
 //      of the one-CTA-per-head kernel up to [Wk; -Q'] (same functions, same arithmetic) and
 //      writes the operands of its state step -- [-Wk; Q'] bf16, [Tb; M] and K~^T as bf16
@@ -204,8 +205,9 @@ __device__ __forceinline__ Item item_at(const SplitParams& sp, int item)
 
 // Persistent: CTA b takes items b, b + gridDim.x, ...; the next item's q, k and g tiles are
 // fetched by TMA while the current one is worked on (k once phase 3 no longer reads it,
-// q and g once phase 4 starts), its beta into a register.  16 warps; warp w reaches TMEM
-// lanes [32 (w % 4), +32) and works on column part w / 4, as in the one-CTA-per-head kernel.
+// q and g once phase 4 starts), its beta by cp.async into the other of two buffers.  16
+// warps; warp w reaches TMEM lanes [32 (w % 4), +32) and works on column part w / 4, as in
+// the one-CTA-per-head kernel.
 __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __grid_constant__ SplitParams sp)
 {
     const TcParams& p = sp.p;
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     bool k_pending = false, qg_pending = false;   // thread 0 only
     int item = blockIdx.x;
     // the current and next items; the one after is looked up an item ahead of its use, so
-    // that its dependent loads (chunk offsets, then cu_seqlens) are never waited for
+    // that its chunk-table load is never waited for
     Item cur{}, nxt{};
     if (item + (int)gridDim.x < items) nxt = item_at(sp, item + gridDim.x);
     if (item < items) {
