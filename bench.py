@@ -43,7 +43,9 @@ E2E_SEGMENT_TOKENS = 1024
 PREFILL_KERNEL_SRC = ("linear_attention_serving_chunkwise_gb300/csrc/kda_prefill_split.cu",
                       "linear_attention_serving_chunkwise_gb300/csrc/kda_prefill_tc_phases.cuh",
                       "linear_attention_serving_chunkwise_gb300/csrc/kda_sm100.cuh")
-PREFILL_KERNELS = "kda_chunk_offsets_kernel + kda_chunk_prep_kernel + kda_state_scan_kernel"
+PREFILL_KERNELS = {1: "kda_prefill_tc_kernel",
+                   2: "kda_chunk_offsets_kernel + kda_prep_scan_kernel (cooperative: chunk prep, then the state scan)",
+                   3: "kda_chunk_offsets_kernel + kda_chunk_prep_kernel + kda_state_scan_kernel"}
 
 
 
@@ -287,7 +289,7 @@ def run_cuda(args, world, rank, local):
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
                 "algorithmic_bytes_per_launch": alg_bytes, "kernel_launches_per_call": plan["kernel_launches"],
                 "launch_ms": launch_ms,
-                "kernels": PREFILL_KERNELS if plan["kernel_launches"] == 3 else "kda_prefill_tc_kernel",
+                "kernels": PREFILL_KERNELS.get(plan["kernel_launches"], "?"),
                 "timed": "CUDA events on the launching stream around each kda_prefill call (all its launches); "
                          "per-kernel shares in profiles/bench_launch_list_prefill_decode.md",
                 "workspace_bytes": plan["workspace_bytes"]}
@@ -413,7 +415,7 @@ def run_ncu_case(case: str):
     """A small, self-contained launch for ncu captures (no timing, no JSON): the same kernels
     as the bench on inputs still larger than L2 but only a few hundred MB on the device.
       prefill: B=1, H=32, T=8192, dk=dv=128, bf16 (470 MB of inputs/outputs; the
-               chunk-parallel split path: offsets, chunk prep, state scan)
+               chunk-parallel path: chunk offsets, then the cooperative prep-and-scan kernel)
       prefill_one_cta: 4 sequences of 2048 tokens, H=38 (152 units, one full wave: one CTA
                per (sequence, head))
       decode:  B=64, H=96, dk=dv=128, bf16, one step (403 MB of state)

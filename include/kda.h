@@ -125,9 +125,12 @@ kda_status kda_prefill_query(const kda_prefill_desc* desc, kda_prefill_plan* pla
  *               (may be NULL when that is 0), 16-byte aligned, overlapping no
  *               input or output; its contents need no set-up and are clobbered.
  *               Two calls in flight at once need two workspaces.  With a
- *               workspace the call runs three kernels (chunk offsets; the
- *               state-independent operands of every (chunk, head) at once; the
- *               state scan), otherwise one; both give bit-identical results.
+ *               workspace the call computes chunk offsets, then the
+ *               state-independent operands of every (chunk, head) at once and
+ *               the state scan, in one cooperative launch at up to 120
+ *               (sequence, head) units (two launches in all) or in two
+ *               separate ones above that (three in all).  Without one, one
+ *               launch.  All forms give bit-identical results.
  * A cu_seqlens entry that breaks the rules above is found on the device: that
  * sequence is skipped and kda_last_device_status() returns KDA_ERR_INVALID_ARG.
  */

@@ -79,6 +79,15 @@ bool uses_split(const kda_prefill_desc& d)
     return split < one_cta;
 }
 
+// Launches of one call: the chunk-parallel path is one launch of chunk offsets plus either
+// the single cooperative prep-and-scan launch (while at least 32 of the 152 SMs' CTAs never
+// scan) or the separate prep and scan launches; otherwise one launch.
+int split_launches(const kda_prefill_desc& d)
+{
+    if (!uses_split(d)) return 1;
+    return (long long)d.num_seqs * d.num_heads + 32 <= kGpuSMs ? 2 : 3;
+}
+
 kda_status validate_prefill(const kda_prefill_desc* d)
 {
     if (!d) return KDA_ERR_INVALID_ARG;
@@ -121,7 +130,7 @@ kda_status kda_prefill_query(const kda_prefill_desc* desc, kda_prefill_plan* pla
     const kda_status st = validate_prefill(desc);
     if (st != KDA_OK) return st;
     if (!plan) return KDA_ERR_INVALID_ARG;
-    plan->kernel_launches = desc->num_seqs > 0 ? (uses_split(*desc) ? 3 : 1) : 0;
+    plan->kernel_launches = desc->num_seqs > 0 ? split_launches(*desc) : 0;
     plan->tensor_cores = uses_tensor_cores(*desc) ? 1 : 0;
     plan->workspace_bytes = kda_prefill_workspace_bytes(desc);
     return KDA_OK;

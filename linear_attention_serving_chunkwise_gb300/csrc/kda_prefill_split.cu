@@ -26,6 +26,7 @@
 // written and read back through HBM.
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 #include "kda_prefill_tc_phases.cuh"
 
@@ -64,6 +65,12 @@ constexpr uint32_t B_TM_S = 0;          // tensor memory: state [128 dk lanes][1
 constexpr uint32_t B_TM_D1 = 128;       // [W; O] accumulator
 constexpr uint32_t B_TM_COLS = 256;
 
+// single-launch form: at least this many CTAs never scan (they finish the prep items), and
+// the switch point uses these per-chunk costs (cycles, measured on GB300)
+constexpr long long kSingleMinProducers = 32;
+constexpr long long kScanCyclesPerChunk = 6000;
+constexpr long long kPrepCyclesPerItem = 21000;
+
 static_assert(B_KTH % 1024 == 0 && B_V0 % 1024 == 0 && B_SB % 1024 == 0 && B_WH % 1024 == 0, "tile alignment");
 static_assert(B_KTH >= IMG_FRONT && B_V0 >= B_KTH + IMG_BACK && B_V1 == B_V0 + 16384 && B_SB >= B_V1 + 16384 &&
                   B_WH >= B_SB + 32768 && B_WL == B_WH + 16384 && B_OST >= B_WL + 16384 &&
@@ -76,6 +83,9 @@ struct SplitParams {
     uint8_t* ops;               // operand images, item (global chunk gc, head h) at ((gc * H) + h) * IMG_BYTES
     int32_t* chunk_off;         // [num_seqs + 1]: first global chunk of each sequence
     int2* chunk_info;           // [chunks]: (first token, end of its sequence) of each global chunk
+    int* counter;               // next unclaimed item (the single-launch form claims items from it)
+    int* flags;                 // [items]: 1 once the item's images are in memory (single-launch form)
+    int num_flags;              // entries of flags (an upper bound on the items)
 };
 
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar)
@@ -92,6 +102,69 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uin
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(smem_src)),
                  "r"(bytes)
                  : "memory");
+}
+
+// Items are claimed from the global counter with one fetch-and-add each (handed out in
+// increasing order).  A claim's raw index is resolved here: -1 once all `items` are taken;
+// an index at or past `limit` is still this CTA's to do (so no item is ever dropped), but
+// stops its further claims.
+__device__ __forceinline__ int resolve_claim(int v, int items, int limit, bool& stop)
+{
+    if (v < 0 || v >= items) {
+        stop = true;
+        return -1;
+    }
+    if (v >= limit) stop = true;
+    return v;
+}
+
+// acquire fence at GPU scope (after relaxed reads of flags that were set by release stores)
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p)
+{
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// wait until at most N committed bulk stores are incomplete (their writes not yet performed)
+template <int N>
+__device__ __forceinline__ void bulk_wait_group()
+{
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// order this thread's generic-proxy and async-proxy accesses to global memory
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v)
+{
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// wait (bounded by kWaitNs of wall time) until *flag != 0; false if it gave up
+__device__ __forceinline__ bool wait_flag(const int* flag)
+{
+    if (ld_acquire_gpu(flag)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!ld_acquire_gpu(flag)) {
+        if (globaltimer_ns() - t0 > kWaitNs) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
+__device__ __forceinline__ void mbar_inval(uint64_t* bar)
+{
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // start moving [gsrc, gsrc + bytes) into L2 (no completion to wait for)
@@ -126,15 +199,22 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // One CTA of 1024 threads: chunk_off[n] = sum over m < n of ceil(len_m / 64), lengths of
 // sequences that fail the cu_seqlens check counted as 0 (and the failure reported); then
 // chunk_info[gc] = (first token, end of the sequence) of every global chunk, so that a
-// chunk's item needs one load and no search.
+// chunk's item needs one load and no search.  Also zeroes the item counter and flags that
+// the single-launch form claims and publishes items with.
 __global__ void __launch_bounds__(1024) kda_chunk_offsets_kernel(const int32_t* cu_seqlens, int num_seqs,
                                                                  int total_tokens, int32_t* chunk_off,
-                                                                 int2* chunk_info, int* status)
+                                                                 int2* chunk_info, int* counter, int* flags,
+                                                                 int num_flags, int* status)
 {
     __shared__ int warp_sums[32];
     __shared__ int carry;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    if (t == 0) carry = 0;
+    // the single-launch form's claim counter and item flags start from zero on every call
+    for (int i = t; i < num_flags; i += 1024) flags[i] = 0;
+    if (t == 0) {
+        *counter = 0;
+        carry = 0;
+    }
     __syncthreads();
     for (int base = 0; base < num_seqs; base += 1024) {
         const int n = base + t;
@@ -203,16 +283,19 @@ __device__ __forceinline__ Item item_at(const SplitParams& sp, int item)
     return it;
 }
 
-// Persistent: CTA b takes items b, b + gridDim.x, ...; the next item's q, k and g tiles are
+// The chunk-prep work of one CTA.  Items come either in a fixed order (kDyn = false: CTA b
+// takes b, b + gridDim.x, ...) or claimed one at a time from the global counter below
+// `limit` (kDyn = true), in which case each item's flag is set once its three image pieces
+// are in memory (two items later, or at the end).  The next item's q, k and g tiles are
 // fetched by TMA while the current one is worked on (k once phase 3 no longer reads it,
 // q and g once phase 4 starts), its beta by cp.async into the other of two buffers.  16
 // warps; warp w reaches TMEM lanes [32 (w % 4), +32) and works on column part w / 4, as in
-// the one-CTA-per-head kernel.
-__global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __grid_constant__ SplitParams sp)
+// the one-CTA-per-head kernel.  `tm`: 512 allocated TMEM columns.  On return the CTA's
+// barriers are invalidated and its copies complete, so shared memory can be reused.
+template <bool kDyn>
+__device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, uint32_t tm, int limit)
 {
     const TcParams& p = sp.p;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int quarter = warp & 3, part = warp >> 2;
     const int L = 32 * quarter + lane;
@@ -221,11 +304,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     uint64_t* bar_k = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint64_t* bar_qg = bar_k + 1;
     uint64_t* bar_mma = bar_k + 2;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_k + 4);
-    int* s_abort = reinterpret_cast<int*>(tslot + 1);
+    int* s_abort = reinterpret_cast<int*>(sm + OFF_BAR + 36);
+    int* s_seq = reinterpret_cast<int*>(sm + OFF_BAR + 40);   // item indices claimed by thread 0
     const uint32_t sbase = smem_u32(sm);
     const int H = p.num_heads;
     const int items = __ldg(sp.chunk_off + p.num_seqs) * H;
+    const int G = gridDim.x;
+    bool stop = false;                   // thread 0 (kDyn): no more claims
+    int claim_raw = -1;                  // thread 0 (kDyn): a claim issued an item ago, unresolved
+    int* s_pub = reinterpret_cast<int*>(sm + OFF_BAR + 52);   // item to publish this iteration
 
     if (t == 0) {
         mbar_init(bar_k, 1);
@@ -236,23 +323,32 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_g);
-    }
-    if (warp == 0) {
-        tmem_alloc(tslot, TM_COLS);
-        tmem_relinquish();
+        if constexpr (kDyn) {
+            s_seq[0] = resolve_claim(atomicAdd(sp.counter, 1), items, limit, stop);
+            s_seq[1] = stop ? -1 : resolve_claim(atomicAdd(sp.counter, 1), items, limit, stop);
+            claim_raw = stop ? -1 : atomicAdd(sp.counter, 1);   // resolved at the first item
+            *s_pub = -1;
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    const uint32_t tm = *tslot;
 
+    // the current and next items (index -1: none); the one after is looked up an item ahead
+    // of its use, so that its chunk-table load is never waited for
+    int item, nidx;
+    if constexpr (kDyn) {
+        item = s_seq[0];
+        nidx = s_seq[1];
+    } else {
+        item = (int)blockIdx.x < items ? (int)blockIdx.x : -1;
+        nidx = (item >= 0 && item + G < items) ? item + G : -1;
+    }
     bool k_pending = false, qg_pending = false;   // thread 0 only
-    int item = blockIdx.x;
-    // the current and next items; the one after is looked up an item ahead of its use, so
-    // that its chunk-table load is never waited for
+    int pub2 = -1, pub1 = -1;                     // thread 0 (kDyn): done, not yet published
     Item cur{}, nxt{};
-    if (item + (int)gridDim.x < items) nxt = item_at(sp, item + gridDim.x);
-    if (item < items) {
+    if (nidx >= 0) nxt = item_at(sp, nidx);
+    if (item >= 0) {
         cur = item_at(sp, item);
         if (t == 0) {
             issue_k_loads(p, sm, bar_k, cur.t0, cur.h);
@@ -268,19 +364,34 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
             cp_async_commit_wait_prev();
         }
     };
-    if (item < items) fetch_beta(cur, 0);
+    if (item >= 0) fetch_beta(cur, 0);
     uint32_t k_par = 0, qg_par = 0, mma_par = 0;
     bool ok = true;
 
-    for (int li = 0; item < items; item += gridDim.x, ++li) {
+    for (int li = 0; item >= 0; ++li) {
         const float* sbeta = sbeta_buf(li & 1);
         const int h = cur.h, t0 = cur.t0;
         const int BT = min(64, cur.eos - t0);
         uint8_t* img = sp.ops + ((size_t)cur.gc * H + h) * IMG_BYTES;
-        const bool has_next = item + (int)gridDim.x < items;
-        const Item nxt2 = (item + 2LL * gridDim.x < items) ? item_at(sp, item + 2 * gridDim.x) : nxt;
+        const bool has_next = nidx >= 0;
         if (t < 64) cp_async_wait_all();   // this item's beta
-        if (t == 0) bulk_wait_read();   // the previous item's pieces have left the staging buffers
+        if (t == 0) {
+            bulk_wait_read();   // the previous item's pieces have left the staging buffers
+            if constexpr (kDyn) {
+                *s_pub = -1;
+                if (pub2 >= 0) {   // the item two back: its pieces are older than the last three
+                    bulk_wait_group<3>();
+                    fence_proxy_async_global();
+                    *s_pub = pub2;   // released after the barrier below, by a thread with no copies in flight
+                }
+                pub2 = pub1;
+                pub1 = item;
+                // the item after next: the claim issued an item ago (its latency hidden by that
+                // item's work); then the next claim, resolved at the next item
+                s_seq[2] = has_next ? resolve_claim(claim_raw, items, limit, stop) : -1;
+                claim_raw = (has_next && !stop && s_seq[2] >= 0) ? atomicAdd(sp.counter, 1) : -1;
+            }
+        }
         if (!(mbar_wait_bounded(bar_k, k_par, kWaitNs) && mbar_wait_bounded(bar_qg, qg_par, kWaitNs)))
             atomicExch(s_abort, 1);
         tc_fence_before_sync();
@@ -290,11 +401,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
             ok = false;
             break;
         }
+        int n2;   // the item after next
+        if constexpr (kDyn) {
+            n2 = s_seq[2];
+            if (t == kThreads - 32 && *s_pub >= 0) st_release_gpu(sp.flags + *s_pub, 1);
+        }
+        else n2 = (has_next && nidx + G < items) ? nidx + G : -1;
+        const Item nxt2 = n2 >= 0 ? item_at(sp, n2) : nxt;
         k_par ^= 1u;
         qg_par ^= 1u;
         if (t == 0) k_pending = qg_pending = false;
         if (has_next) fetch_beta(nxt, (li + 1) & 1);   // the buffer the previous item used
-
         // ---- phase 1: decayed operands
         phase1_cumsum(sm, vec, t, BT);
         __syncthreads();
@@ -458,9 +575,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
         }
         cur = nxt;   // the next item's first barrier orders these TMEM reads before its writes
         nxt = nxt2;
+        item = nidx;
+        nidx = n2;
     }
 
-    if (t == 0) bulk_wait_all();   // the images are written before the CTA's shared memory goes away
+    if (t == 0) {
+        bulk_wait_all();   // the images are written before the CTA's shared memory is reused
+        if constexpr (kDyn) {
+            if (ok) {
+                fence_proxy_async_global();
+                if (pub2 >= 0) st_release_gpu(sp.flags + pub2, 1);
+                if (pub1 >= 0) st_release_gpu(sp.flags + pub1, 1);
+            }
+        }
+    }
     if (!ok && t == 0) {
         report_status(p.status, kDevTimeout);
         if (k_pending) mbar_wait_bounded(bar_k, k_par, kWaitNs);
@@ -469,19 +597,44 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, TM_COLS);
+    if (t == 0) {
+        mbar_inval(bar_k);
+        mbar_inval(bar_qg);
+        mbar_inval(bar_mma);
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __grid_constant__ SplitParams sp)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 32);
+    if ((threadIdx.x >> 5) == 0) {
+        tmem_alloc(tslot, TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tm = *tslot;
+    prep_items<false>(sp, sm, tm, 0x7fffffff);
+    tc_fence_before_sync();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 0) tmem_dealloc(tm, TM_COLS);
 }
 
 // ---------------------------------------------------------------- step 3: the state scan
-// One CTA per (sequence, head), 16 warps (warp w: TMEM lanes [32 (w % 4), +32), column part
-// w / 4).  The front image of chunk c+1 is fetched once chunk c's D1 MMAs have read theirs,
-// the back image once its state update has; v two chunks ahead into the freed buffer, and
-// the images of chunk c+2 are prefetched into L2 at the same time.
-__global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __grid_constant__ SplitParams sp)
+// The scan of one (sequence, head) unit by one CTA, 16 warps (warp w: TMEM lanes
+// [32 (w % 4), +32), column part w / 4).  The front image of chunk c+1 is fetched once chunk
+// c's D1 MMAs have read theirs, the back image once its state update has; v two chunks ahead
+// into the freed buffer, and the images of chunk c+2 are prefetched into L2 at the same time.
+// With kFlags (the single-launch form) each image is fetched only once its item's flag is
+// set.  `tm`: at least 256 allocated TMEM columns.
+template <bool kFlags>
+__device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, uint32_t tm, int unit)
 {
     const TcParams& p = sp.p;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int quarter = warp & 3, part = warp >> 2;
     const int L = 32 * quarter + lane;
@@ -489,19 +642,41 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
     uint64_t* bar_b = bar_f + 1;
     uint64_t* bar_v = bar_f + 2;   // two, one per v buffer
     uint64_t* bar_mma = bar_f + 4;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_f + 5);
-    int* s_abort = reinterpret_cast<int*>(tslot + 1);
+    int* s_abort = reinterpret_cast<int*>(sm + B_BAR + 44);
     const uint32_t sbase = smem_u32(sm);
     const float* sgam = reinterpret_cast<const float*>(sm + B_GAM);
 
     const int H = p.num_heads;
-    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    const int n = unit / H, h = unit % H;
     int bos, eos;
     if (!seq_bounds(p.cu_seqlens, n, p.num_seqs, p.total_tokens, p.status, bos, eos)) return;
     const int nchunks = (eos - bos + 63) >> 6;
     const int gc0 = __ldg(sp.chunk_off + n);
     const size_t sbase_g = ((size_t)n * H + h) * 128 * 128;
     auto image = [&](int c) { return sp.ops + ((size_t)(gc0 + c) * H + h) * IMG_BYTES; };
+    // kFlags: the producer fetches chunk c's images only once its item is published.  It reads
+    // the flags of up to 16 chunks ahead with relaxed loads and takes one acquire (and proxy)
+    // fence for all that are set, so that a fence is paid per batch, not per fetch; it blocks
+    // (bounded) only when chunk c itself is not yet published.
+    int known = -1;   // producer: chunks <= known are published and acquired
+    auto ready = [&](int c) {
+        if constexpr (kFlags) {
+            if (c <= known) return true;
+            const int* f = sp.flags + (size_t)gc0 * H + h;
+            if (!ld_relaxed_gpu(f + (size_t)c * H) && !wait_flag(f + (size_t)c * H)) return false;
+            int fl[15];   // the next 15 chunks' flags, loaded together
+#pragma unroll
+            for (int i = 0; i < 15; ++i) fl[i] = (c + 1 + i < nchunks) ? ld_relaxed_gpu(f + (size_t)(c + 1 + i) * H) : 0;
+            int k = c;
+#pragma unroll
+            for (int i = 0; i < 15; ++i)
+                if (k == c + i && fl[i]) k = c + 1 + i;
+            fence_acquire_gpu();
+            fence_proxy_async_global();
+            known = k;
+        }
+        return true;
+    };
 
     if (t == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(bar_f + i, 1);
@@ -510,14 +685,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
         tma_prefetch_desc(&p.tm_v);
         tma_prefetch_desc(&p.tm_o);
     }
-    if (warp == 0) {
-        tmem_alloc(tslot, B_TM_COLS);
-        tmem_relinquish();
-    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    const uint32_t tm = *tslot;
 
     // The copies into shared memory are issued by one producer thread (kProducer, in a warp
     // of the O half, which has slack when they are due); it counts what it issued so that,
@@ -527,11 +697,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
     bool o_pending = false, mma_open = false;   // thread 0
     int n_front = 0, n_back = 0, n_v[2] = {0, 0};   // producer
     auto fetch_front = [&](int c) {
+        if (!ready(c)) {   // never published: give up (the waits on bar_f then run out)
+            atomicExch(s_abort, 1);
+            return;
+        }
         mbar_arrive_expect_tx(bar_f, IMG_FRONT);
         bulk_load(sm + B_A1, image(c), IMG_FRONT, bar_f);
         ++n_front;
     };
     auto fetch_back = [&](int c) {
+        if (!ready(c)) {
+            atomicExch(s_abort, 1);
+            return;
+        }
         mbar_arrive_expect_tx(bar_b, IMG_BACK);
         bulk_load(sm + B_KTH, image(c) + IMG_KTH, IMG_BACK, bar_b);
         ++n_back;
@@ -758,12 +936,59 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, B_TM_COLS);
 }
 
-// workspace: chunk_off [N + 1] int32, chunk_info [chunks] int2, then the operand images
+__global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __grid_constant__ SplitParams sp)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_BAR + 40);
+    if ((threadIdx.x >> 5) == 0) {
+        tmem_alloc(tslot, B_TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tm = *tslot;
+    scan_unit<false>(sp, sm, tm, blockIdx.x);
+    tc_fence_before_sync();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 0) tmem_dealloc(tm, B_TM_COLS);
+}
+
+// The single-launch form (cooperative: every CTA resident, one per SM).  Every CTA claims
+// chunk-prep items in increasing order; CTAs b < units stop claiming at `switch_item` and
+// then scan unit b, fetching each chunk's images once its flag is set, while the others
+// keep claiming until the items run out.  A CTA waits only on items that other CTAs have
+// already claimed or will claim, and the CTAs that never scan finish every item left, so
+// every wait ends.
+__global__ void __launch_bounds__(kThreads, 1) kda_prep_scan_kernel(const __grid_constant__ SplitParams sp, int units,
+                                                                    int switch_item)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_BAR + 120);   // used by neither layout
+    if ((threadIdx.x >> 5) == 0) {
+        tmem_alloc(tslot, TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tm = *tslot;
+    const bool scans = (int)blockIdx.x < units;
+    prep_items<true>(sp, sm, tm, scans ? switch_item : 0x7fffffff);
+    if (scans) scan_unit<true>(sp, sm, tm, blockIdx.x);
+    tc_fence_before_sync();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 0) tmem_dealloc(tm, TM_COLS);
+}
+
+// workspace: chunk_off [N + 1] int32, chunk_info [chunks] int2, the claim counter, the item
+// flags [chunks * H] int32, then the operand images
 struct SplitWorkspace {
-    size_t chunks, off_bytes, info_bytes, total;
+    size_t chunks, off_bytes, info_bytes, ctr_bytes, flag_bytes, total;
 };
 
 SplitWorkspace split_workspace(int num_seqs, int total_tokens, int num_heads)
@@ -772,7 +997,9 @@ SplitWorkspace split_workspace(int num_seqs, int total_tokens, int num_heads)
     w.chunks = (size_t)total_tokens / 64 + (size_t)num_seqs;   // >= the sum of ceil(len / 64)
     w.off_bytes = ((size_t)(num_seqs + 1) * sizeof(int32_t) + 255) & ~(size_t)255;
     w.info_bytes = (w.chunks * sizeof(int2) + 255) & ~(size_t)255;
-    w.total = w.off_bytes + w.info_bytes + w.chunks * (size_t)num_heads * IMG_BYTES;
+    w.ctr_bytes = 256;
+    w.flag_bytes = (w.chunks * (size_t)num_heads * sizeof(int) + 255) & ~(size_t)255;
+    w.total = w.off_bytes + w.info_bytes + w.ctr_bytes + w.flag_bytes + w.chunks * (size_t)num_heads * IMG_BYTES;
     return w;
 }
 
@@ -781,6 +1008,42 @@ SplitWorkspace split_workspace(int num_seqs, int total_tokens, int num_heads)
 size_t prefill_split_workspace_bytes(int num_seqs, int total_tokens, int num_heads)
 {
     return split_workspace(num_seqs, total_tokens, num_heads).total;
+}
+
+// Per-device facts the launch needs, found once: SM count and whether the single-launch
+// form can run (cooperative launch, one resident CTA per SM).
+struct SplitDevice {
+    int sms = 0;
+    bool single = false;
+};
+
+cudaError_t split_device(SplitDevice* out)
+{
+    static SplitDevice cache[64];
+    static std::once_flag once[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev] {
+        SplitDevice d;
+        int coop = 0, per_sm = 0;
+        bool ok = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess &&
+                  cudaFuncSetAttribute(kda_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)A_SMEM_BYTES) == cudaSuccess &&
+                  cudaFuncSetAttribute(kda_state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)B_SMEM_BYTES) == cudaSuccess &&
+                  cudaFuncSetAttribute(kda_prep_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)B_SMEM_BYTES) == cudaSuccess &&
+                  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_prep_scan_kernel, kThreads,
+                                                                B_SMEM_BYTES) == cudaSuccess;
+        d.single = ok && coop && per_sm >= 1;
+        if (!ok) d.sms = 0;
+        cache[dev] = d;
+    });
+    *out = cache[dev];
+    return out->sms > 0 ? cudaSuccess : cudaErrorUnknown;
 }
 
 cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream)
@@ -810,24 +1073,35 @@ cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream)
     const SplitWorkspace wl = split_workspace(a.num_seqs, a.total_tokens, a.num_heads);
     sp.chunk_off = reinterpret_cast<int32_t*>(ws);
     sp.chunk_info = reinterpret_cast<int2*>(ws + wl.off_bytes);
-    sp.ops = ws + wl.off_bytes + wl.info_bytes;
+    sp.counter = reinterpret_cast<int*>(ws + wl.off_bytes + wl.info_bytes);
+    sp.flags = reinterpret_cast<int*>(ws + wl.off_bytes + wl.info_bytes + wl.ctr_bytes);
+    sp.num_flags = (int)(wl.chunks * (size_t)a.num_heads);
+    sp.ops = ws + wl.off_bytes + wl.info_bytes + wl.ctr_bytes + wl.flag_bytes;
 
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kda_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)A_SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kda_state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)B_SMEM_BYTES);
+    SplitDevice dv;
+    cudaError_t e = split_device(&dv);
     if (e != cudaSuccess) return e;
 
     kda_chunk_offsets_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.num_seqs, a.total_tokens, sp.chunk_off,
-                                                      sp.chunk_info, a.status);
+                                                      sp.chunk_info, sp.counter, sp.flags, sp.num_flags, a.status);
+    const long long units = (long long)a.num_seqs * a.num_heads;
+    if (dv.single && units + kSingleMinProducers <= dv.sms) {
+        // Scanning CTAs stop claiming items once (grid - units) producers alone can finish the
+        // rest in the time the scan takes: rest = (grid - units) x chunks x scan / prep per item.
+        const long long chunks = ((long long)a.total_tokens / a.num_seqs + 63) / 64;
+        const long long items = chunks * a.num_seqs * a.num_heads;
+        const long long rest = (dv.sms - units) * chunks * kScanCyclesPerChunk / kPrepCyclesPerItem;
+        int units_i = (int)units, switch_item = (int)std::max(0LL, items - rest);
+        void* args[] = {&sp, &units_i, &switch_item};
+        e = cudaLaunchCooperativeKernel((const void*)kda_prep_scan_kernel, dim3((unsigned)dv.sms), dim3(kThreads),
+                                        args, B_SMEM_BYTES, stream);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     const long long items_max = ((long long)a.total_tokens / 64 + a.num_seqs) * a.num_heads;
-    const long long prep_grid = std::max(1LL, std::min<long long>(sms, items_max));
+    const long long prep_grid = std::max(1LL, std::min<long long>(dv.sms, items_max));
     kda_chunk_prep_kernel<<<(unsigned)prep_grid, kThreads, A_SMEM_BYTES, stream>>>(sp);
-    kda_state_scan_kernel<<<(unsigned)((long long)a.num_seqs * a.num_heads), kThreads, B_SMEM_BYTES, stream>>>(sp);
+    kda_state_scan_kernel<<<(unsigned)units, kThreads, B_SMEM_BYTES, stream>>>(sp);
     return cudaGetLastError();
 }
 
