@@ -312,7 +312,6 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
     const int G = gridDim.x;
     bool stop = false;                   // thread 0 (kDyn): no more claims
     int claim_raw = -1;                  // thread 0 (kDyn): a claim issued an item ago, unresolved
-    int* s_pub = reinterpret_cast<int*>(sm + OFF_BAR + 52);   // item to publish this iteration
 
     if (t == 0) {
         mbar_init(bar_k, 1);
@@ -327,7 +326,6 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             s_seq[0] = resolve_claim(atomicAdd(sp.counter, 1), items, limit, stop);
             s_seq[1] = stop ? -1 : resolve_claim(atomicAdd(sp.counter, 1), items, limit, stop);
             claim_raw = stop ? -1 : atomicAdd(sp.counter, 1);   // resolved at the first item
-            *s_pub = -1;
         }
     }
     tc_fence_before_sync();
@@ -345,7 +343,11 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         nidx = (item >= 0 && item + G < items) ? item + G : -1;
     }
     bool k_pending = false, qg_pending = false;   // thread 0 only
-    int pub2 = -1, pub1 = -1;                     // thread 0 (kDyn): done, not yet published
+    // The image pieces are stored, waited for and published by kStorer, a thread of the warps
+    // that only write the seed during the solve, so that this work fits in their idle time
+    // there instead of delaying thread 0 (which issues the loads and MMAs).
+    constexpr int kStorer = kSolveThreads;
+    int pub2 = -1, pub1 = -1;                     // kStorer (kDyn): done, not yet published
     Item cur{}, nxt{};
     if (nidx >= 0) nxt = item_at(sp, nidx);
     if (item >= 0) {
@@ -375,17 +377,9 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         uint8_t* img = sp.ops + ((size_t)cur.gc * H + h) * IMG_BYTES;
         const bool has_next = nidx >= 0;
         if (t < 64) cp_async_wait_all();   // this item's beta
-        if (t == 0) {
-            bulk_wait_read();   // the previous item's pieces have left the staging buffers
-            if constexpr (kDyn) {
-                *s_pub = -1;
-                if (pub2 >= 0) {   // the item two back: its pieces are older than the last three
-                    bulk_wait_group<3>();
-                    fence_proxy_async_global();
-                    *s_pub = pub2;   // released after the barrier below, by a thread with no copies in flight
-                }
-                pub2 = pub1;
-                pub1 = item;
+        if (t == kStorer) bulk_wait_read();   // the previous item's pieces have left the staging buffers
+        if constexpr (kDyn) {
+            if (t == 0) {
                 // the item after next: the claim issued an item ago (its latency hidden by that
                 // item's work); then the next claim, resolved at the next item
                 s_seq[2] = has_next ? resolve_claim(claim_raw, items, limit, stop) : -1;
@@ -402,10 +396,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             break;
         }
         int n2;   // the item after next
-        if constexpr (kDyn) {
-            n2 = s_seq[2];
-            if (t == kThreads - 32 && *s_pub >= 0) st_release_gpu(sp.flags + *s_pub, 1);
-        }
+        if constexpr (kDyn) n2 = s_seq[2];
         else n2 = (has_next && nidx + G < items) ? nidx + G : -1;
         const Item nxt2 = n2 >= 0 ? item_at(sp, n2) : nxt;
         k_par ^= 1u;
@@ -452,7 +443,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        if (t == 0) {
+        if (t == kStorer) {
             bulk_store(img + IMG_KTH, sm + A_STAGE, IMG_BACK);
             bulk_commit();
         }
@@ -469,6 +460,18 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             phase3_seed(sm, vec, tm, L, 2 * (part - 2), quarter, BT);
             phase3_seed(sm, vec, tm, L, 2 * (part - 2) + 1, quarter, BT);
             tmem_wait_st();
+            if (t == kStorer) {
+                bulk_wait_read();   // the K~ piece has left the staging buffer ([Tb; M] goes there next)
+                if constexpr (kDyn) {
+                    if (pub2 >= 0) {   // the item two back: its pieces are older than the last three
+                        bulk_wait_group<3>();
+                        fence_proxy_async_global();
+                        st_release_gpu(sp.flags + pub2, 1);
+                    }
+                    pub2 = pub1;
+                    pub1 = item;
+                }
+            }
         }
         tc_fence_before_sync();
         __syncthreads();
@@ -495,7 +498,6 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             for (int ks = 0; ks < 4; ++ks)
                 umma_bf16_tmem_a(tm + TM_M, tm + TM_PL + 8 * ks, desc_mnmajor(tbh, 64, ks), idesc, 1u);
             umma_commit(bar_mma);
-            bulk_wait_read();   // the K~ piece has left the staging buffer
         }
         // [Tb; M] hi/lo: row L, K = tokens [16 part, +16), to TMEM (the D2 MMA) and the staging buffer
         uint32_t hi[8], lo[8];
@@ -535,10 +537,12 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         __syncthreads();
 
         // ---- phase 4: D2 = [0; -Q_Gamma] + [Tb; M] K_Gamma (hi + lo) = [Wk; -Q']; A1 = -D2 to the image
-        if (t == 0) {
-            tc_fence_after_sync();
+        if (t == kStorer) {
             bulk_store(img + IMG_TBH, sm + A_STAGE, 32768);
             bulk_commit();
+        }
+        if (t == 0) {
+            tc_fence_after_sync();
             if (has_next) {   // the q and g tiles are no longer read
                 issue_qg_loads(p, sm, bar_qg, nxt.t0, nxt.h);
                 qg_pending = true;
@@ -569,7 +573,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             fence_proxy_async_smem();
         }
         __syncthreads();
-        if (t == 0) {
+        if (t == kStorer) {
             bulk_store(img + IMG_A1, sm + A_STAGE2, 32768);
             bulk_commit();
         }
@@ -579,7 +583,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         nidx = n2;
     }
 
-    if (t == 0) {
+    if (t == kStorer) {
         bulk_wait_all();   // the images are written before the CTA's shared memory is reused
         if constexpr (kDyn) {
             if (ok) {
