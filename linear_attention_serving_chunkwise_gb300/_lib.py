@@ -120,6 +120,14 @@ def _stream_handle(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _keep_until_done(tensor: torch.Tensor, stream) -> None:
+    """A scratch tensor this module allocated on the current stream and the library uses on
+    ``stream``: tell the caching allocator, so that the memory is not handed to another
+    allocation before that stream's work is done."""
+    if stream is not None and stream != torch.cuda.current_stream(tensor.device):
+        tensor.record_stream(stream)
+
+
 def make_desc(num_seqs: int, total_tokens: int, num_heads: int, dk: int, dv: int, qkv_dtype: int) -> PrefillDesc:
     return PrefillDesc(int(num_seqs), int(total_tokens), int(num_heads), int(dk), int(dv), int(qkv_dtype))
 
@@ -154,15 +162,19 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_
     desc = make_desc(N, T, H, dk, dv, _dtype_code(q))
     if out is None:
         out = torch.empty((T, H, dv), dtype=torch.float32, device=q.device)
+        _keep_until_done(out, stream)
     if final_state is None and want_final:
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+        _keep_until_done(final_state, stream)
     need = prefill_workspace_bytes(desc)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        _keep_until_done(workspace, stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if checkpoint_interval:
         if checkpoints is None:
             checkpoints = torch.zeros((N, H, checkpoint_slots, dk, dv), dtype=torch.float32, device=q.device)
+            _keep_until_done(checkpoints, stream)
         st = load().kda_prefill_checkpointed(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                              _ptr(cu_seqlens), _ptr(init_state), _ptr(out), _ptr(final_state),
                                              int(checkpoint_interval), int(checkpoint_slots), _ptr(checkpoints),
@@ -203,6 +215,7 @@ def prefill_host(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, f
         need = prefill_host_workspace_bytes(desc, segment_tokens)
         dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        _keep_until_done(workspace, stream)
     ws_bytes = workspace.numel() * workspace.element_size()
     st = load().kda_prefill_host(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                  _ptr(cu_seqlens), _ptr(init_state), _ptr(out), _ptr(final_state),
@@ -244,6 +257,7 @@ def decode(q, k, v, g, beta, state, out=None, *, stream=None, check=True):
     dv = v.shape[2]
     if out is None:
         out = torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
+        _keep_until_done(out, stream)
     st = load().kda_decode(B, H, dk, dv, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                            _ptr(state), _ptr(out), _stream_handle(stream))
     if check and st != KDA_OK:
@@ -260,6 +274,7 @@ def decode_multi(q, k, v, g, beta, state, out=None, n_apply=None, *, want_out=Tr
     dv = v.shape[3]
     if out is None and want_out:
         out = torch.empty((B, K, H, dv), dtype=torch.float32, device=q.device)
+        _keep_until_done(out, stream)
     st = load().kda_decode_multi(B, K, H, dk, dv, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                  _ptr(n_apply), _ptr(state), _ptr(out), _stream_handle(stream))
     if check and st != KDA_OK:

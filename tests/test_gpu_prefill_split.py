@@ -174,3 +174,54 @@ def test_split_separate_launches_sampled(cuda_lib):
     ro, rs = oracle_heads(host, 0, heads, host["cu_seqlens"].numpy())
     check("separate-launch split out", out[:, heads].cpu(), ro, tol_for(torch.bfloat16))
     check("separate-launch split final state", fin[0, heads].cpu(), rs, tol_for(torch.bfloat16))
+
+
+def test_concurrent_calls_on_two_streams(cuda_lib):
+    """Two single-launch prefills on two streams with their own workspaces, and a decode on a
+    third stream, in flight together: each equals its run alone, bit for bit (cooperative
+    launches take the whole GPU, so the runtime orders them; nothing waits across calls)."""
+    runs = []
+    for i, (lens, H) in enumerate([([700, 333], 8), ([1024], 12)]):
+        cfg = W.random_prefill_config(lens, H, 128, torch.bfloat16, init="normal")
+        assert _plan(cuda_lib, len(lens), cfg.total_tokens, H)["kernel_launches"] == 2
+        runs.append(to_device(W.make_prefill_inputs(cfg, seed=98 + i)))
+    solo = []
+    for g in runs:
+        o, f = cuda_lib.prefill(g["q"], g["k"], g["v"], g["g"], g["beta"], g["cu_seqlens"], g["init_state"])
+        solo.append((o.clone(), f.clone()))
+    torch.cuda.synchronize()
+    dcfg = W.DecodeConfig("side", 64, 16, 128, 128, torch.bfloat16, 1)
+    di = W.make_decode_inputs(dcfg, seed=99, device="cuda")
+    dstate, dstate_ref = di["state0"].clone(), di["state0"].clone()
+    dref = cuda_lib.decode(di["q"][0], di["k"][0], di["v"][0], di["g"][0], di["beta"][0], dstate_ref)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    outs = []
+    for _ in range(3):   # several rounds, so that the calls overlap in different ways
+        outs.clear()
+        for g, s in zip(runs, streams):
+            outs.append(cuda_lib.prefill(g["q"], g["k"], g["v"], g["g"], g["beta"], g["cu_seqlens"], g["init_state"],
+                                         stream=s))
+        dstate.copy_(di["state0"])
+        dout = cuda_lib.decode(di["q"][0], di["k"][0], di["v"][0], di["g"][0], di["beta"][0], dstate, stream=streams[2])
+        torch.cuda.synchronize()
+        assert cuda_lib.last_device_status() == cuda_lib.KDA_OK
+        for (o, f), (ro, rf) in zip(outs, solo):
+            assert torch.equal(o, ro) and torch.equal(f, rf)
+        assert torch.equal(dout, dref) and torch.equal(dstate, dstate_ref)
+
+
+def test_single_launch_uneven_sequences_near_the_limit(cuda_lib):
+    """112 units of uneven sequences (7 sequences x 16 heads, one of a single token): items are
+    claimed and published across all CTAs, and the scans of the long sequences run well past
+    the short ones'."""
+    rng = np.random.default_rng(100)
+    lens = [int(x) for x in rng.integers(700, 2200, size=7)]
+    lens[3] = 1
+    cfg = W.random_prefill_config(lens, 16, 128, torch.bfloat16, init="normal")
+    assert _plan(cuda_lib, 7, cfg.total_tokens, 16)["kernel_launches"] == 2
+    d = W.make_prefill_inputs(cfg, seed=101)
+    out, fin = _run(cuda_lib, d)
+    ref_o, ref_s = oracle_full(d)
+    check("near-limit out", out, ref_o, tol_for(torch.bfloat16))
+    check("near-limit final state", fin, ref_s, tol_for(torch.bfloat16))
