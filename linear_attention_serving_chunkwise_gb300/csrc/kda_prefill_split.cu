@@ -61,6 +61,10 @@ constexpr uint32_t B_WL = 181248;       // W lo
 constexpr uint32_t B_OST = 197632;      // O staging: 4 x [64 tok][32 dv] fp32 boxes, 128-byte swizzle
 constexpr uint32_t B_BAR = 230400;
 constexpr size_t B_SMEM_BYTES = B_BAR + 64 + 1024;
+// words of the 64-byte block at B_BAR: the scan's 5 barriers (0-39), the separate scan
+// kernel's TMEM slot (40), the scan's abort word (44), the single launch's TMEM slot (48)
+constexpr uint32_t B_WORD_TSLOT = 40, B_WORD_ABORT = 44, B_WORD_TSLOT1 = 48;
+static_assert(B_WORD_TSLOT1 + 4 <= 64, "scan word block");
 constexpr uint32_t B_TM_S = 0;          // tensor memory: state [128 dk lanes][128 dv] fp32
 constexpr uint32_t B_TM_D1 = 128;       // [W; O] accumulator
 constexpr uint32_t B_TM_COLS = 256;
@@ -182,6 +186,8 @@ constexpr uint32_t A_STAGE = OFF_V0;
 constexpr uint32_t A_STAGE2 = OFF_X + X_SB;
 constexpr uint32_t A_BETA2 = (uint32_t)SMEM_USED;
 constexpr size_t A_SMEM_BYTES = SMEM_BYTES + 256;
+static_assert(SMEM_USED + 256 <= B_BAR, "the prep layout ends below the scan's word block, which the single launch's "
+                                        "TMEM slot occupies from the start");
 static_assert(OFF_V1 + 16384 == A_STAGE + 32768, "staging buffer");
 static_assert(A_STAGE2 % 1024 == 0 && X_SB >= X_SY + 32 * LDY * 4 && X_SB + 32768 <= 81920, "second staging buffer");
 static_assert(A_BETA2 % 16 == 0, "beta buffer");
@@ -646,7 +652,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
     uint64_t* bar_b = bar_f + 1;
     uint64_t* bar_v = bar_f + 2;   // two, one per v buffer
     uint64_t* bar_mma = bar_f + 4;
-    int* s_abort = reinterpret_cast<int*>(sm + B_BAR + 44);
+    int* s_abort = reinterpret_cast<int*>(sm + B_BAR + B_WORD_ABORT);
     const uint32_t sbase = smem_u32(sm);
     const float* sgam = reinterpret_cast<const float*>(sm + B_GAM);
 
@@ -946,7 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_BAR + 40);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_BAR + B_WORD_TSLOT);
     if ((threadIdx.x >> 5) == 0) {
         tmem_alloc(tslot, B_TM_COLS);
         tmem_relinquish();
@@ -972,7 +978,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_scan_kernel(const __grid
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_BAR + 120);   // used by neither layout
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_BAR + B_WORD_TSLOT1);   // used by neither layout
     if ((threadIdx.x >> 5) == 0) {
         tmem_alloc(tslot, TM_COLS);
         tmem_relinquish();
