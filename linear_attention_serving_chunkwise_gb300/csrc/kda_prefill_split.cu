@@ -1105,8 +1105,9 @@ cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream)
         void* args[] = {&sp, &units_i, &switch_item};
         e = cudaLaunchCooperativeKernel((const void*)kda_prep_scan_kernel, dim3((unsigned)dv.sms), dim3(kThreads),
                                         args, B_SMEM_BYTES, stream);
-        if (e != cudaSuccess) return e;
-        return cudaGetLastError();
+        if (e == cudaSuccess) return cudaGetLastError();
+        if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+        (void)cudaGetLastError();   // not all CTAs can be resident here: the separate launches below
     }
     const long long items_max = ((long long)a.total_tokens / 64 + a.num_seqs) * a.num_heads;
     const long long prep_grid = std::max(1LL, std::min<long long>(dv.sms, items_max));
