@@ -178,19 +178,20 @@ __device__ __forceinline__ void prefetch_l2(const void* gsrc, uint32_t bytes)
 }
 
 // the prep kernel stages each 32 KB piece of an item's image in shared memory and writes it
-// with one bulk store: K~ and [Tb; M] in the v buffers of the shared map (which it does not
-// use), [-Wk; Q'] in the part of the X region that holds the state operand in the
-// one-CTA-per-head kernel (free here from phase 3 on), so that its staging need not wait
-// for the [Tb; M] store to leave.  beta comes by cp.async into two buffers, one item ahead.
+// with one bulk store, all three in turn in the v buffers of the shared map (which it does
+// not use).  K_Gamma, the B operand of the item's last MMA, has two buffers (the shared
+// map's and A_KG2), so that the next item's token phase can write its own while that MMA
+// runs.  beta comes by cp.async into two buffers, one item ahead.
 constexpr uint32_t A_STAGE = OFF_V0;
-constexpr uint32_t A_STAGE2 = OFF_X + X_SB;
-constexpr uint32_t A_BETA2 = (uint32_t)SMEM_USED;
-constexpr size_t A_SMEM_BYTES = SMEM_BYTES + 256;
-static_assert(SMEM_USED + 256 <= B_BAR, "the prep layout ends below the scan's word block, which the single launch's "
-                                        "TMEM slot occupies from the start");
+constexpr uint32_t A_KG2 = ((uint32_t)SMEM_USED + 1023u) & ~1023u;
+constexpr uint32_t A_BETA2 = A_KG2 + 16384;
+constexpr uint32_t A_USED = A_BETA2 + 256;
+constexpr size_t A_SMEM_BYTES = A_USED + 1024;   // slack for 1024-byte alignment
+static_assert(A_USED <= B_BAR, "the prep layout ends below the scan's word block, which the single launch's "
+                                "TMEM slot occupies from the start");
+static_assert(A_SMEM_BYTES <= 232448, "prep shared memory");
 static_assert(OFF_V1 + 16384 == A_STAGE + 32768, "staging buffer");
-static_assert(A_STAGE2 % 1024 == 0 && X_SB >= X_SY + 32 * LDY * 4 && X_SB + 32768 <= 81920, "second staging buffer");
-static_assert(A_BETA2 % 16 == 0, "beta buffer");
+static_assert(A_KG2 % 1024 == 0 && A_BETA2 % 16 == 0, "second K_Gamma and beta buffers");
 
 __device__ __forceinline__ void cp_async4_zfill(void* smem_dst, const void* gsrc, bool valid)
 {
@@ -293,9 +294,9 @@ __device__ __forceinline__ Item item_at(const SplitParams& sp, int item)
 // takes b, b + gridDim.x, ...) or claimed one at a time from the global counter below
 // `limit` (kDyn = true), in which case each item's flag is set once its three image pieces
 // are in memory (two items later, or at the end).  The next item's q, k and g tiles are
-// fetched by TMA while the current one is worked on (k once phase 3 no longer reads it,
-// q and g once phase 4 starts), its beta by cp.async into the other of two buffers.  16
-// warps; warp w reaches TMEM lanes [32 (w % 4), +32) and works on column part w / 4, as in
+// fetched by TMA while the current one is worked on (k once the A/P MMA is done, q and g
+// once the seed of phase 3 is), its beta by cp.async into the other of two buffers.  Its
+// phase 1 up to the off-diagonal rows runs while the current item's last MMA does.  16 warps; warp w reaches TMEM lanes [32 (w % 4), +32) and works on column part w / 4, as in
 // the one-CTA-per-head kernel.  `tm`: 512 allocated TMEM columns.  On return the CTA's
 // barriers are invalidated and its copies complete, so shared memory can be reused.
 template <bool kDyn>
@@ -307,6 +308,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
     const int L = 32 * quarter + lane;
     float* vec = reinterpret_cast<float*>(sm + OFF_VEC);
     auto sbeta_buf = [&](int b) { return reinterpret_cast<float*>(sm + (b ? A_BETA2 : OFF_BETA)); };
+    auto kg_buf = [](int b) { return b ? A_KG2 : OFF_KG; };
     uint64_t* bar_k = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint64_t* bar_qg = bar_k + 1;
     uint64_t* bar_mma = bar_k + 2;
@@ -348,17 +350,17 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         item = (int)blockIdx.x < items ? (int)blockIdx.x : -1;
         nidx = (item >= 0 && item + G < items) ? item + G : -1;
     }
-    bool k_pending = false, qg_pending = false;   // thread 0 only
-    // The image pieces are stored, waited for and published by kStorer, a thread of the warps
-    // that only write the seed during the solve, so that this work fits in their idle time
-    // there instead of delaying thread 0 (which issues the loads and MMAs).
+    // The tile loads are issued, and the image pieces stored, waited for and published, by
+    // kStorer, a thread of the warps that only write the seed during the solve, so that this
+    // work fits in their idle time instead of delaying thread 0 (which issues the MMAs).
     constexpr int kStorer = kSolveThreads;
+    bool k_pending = false, qg_pending = false;   // kStorer: a load issued, not yet waited for
     int pub2 = -1, pub1 = -1;                     // kStorer (kDyn): done, not yet published
     Item cur{}, nxt{};
     if (nidx >= 0) nxt = item_at(sp, nidx);
     if (item >= 0) {
         cur = item_at(sp, item);
-        if (t == 0) {
+        if (t == kStorer) {
             issue_k_loads(p, sm, bar_k, cur.t0, cur.h);
             issue_qg_loads(p, sm, bar_qg, cur.t0, cur.h);
             k_pending = qg_pending = true;
@@ -374,16 +376,38 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
     };
     if (item >= 0) fetch_beta(cur, 0);
     uint32_t k_par = 0, qg_par = 0, mma_par = 0;
-    bool ok = true;
+    // phase 1 of an item up to the off-diagonal rows, once its tiles are in: per-channel
+    // cumsums (g becomes x in place) and factors into vec, then the token rows into TMEM,
+    // the [K; Q] operand in the X region and K_Gamma into buffer b.  The item's first
+    // barrier orders these writes before they are read.
+    auto phase1ab = [&](const Item& it, int b) -> bool {
+        const int BTn = min(64, it.eos - it.t0);
+        if (!mbar_wait_bounded(bar_qg, qg_par, kWaitNs)) atomicExch(s_abort, 1);
+        __syncthreads();
+        if (*s_abort) return false;
+        qg_par ^= 1u;
+        if (t == kStorer) qg_pending = false;
+        phase1_cumsum(sm, vec, t, BTn);
+        __syncthreads();
+        if (t < 128) phase1_factors(vec, t);
+        if (!mbar_wait_bounded(bar_k, k_par, kWaitNs)) atomicExch(s_abort, 1);
+        __syncthreads();
+        if (*s_abort) return false;
+        k_par ^= 1u;
+        if (t == kStorer) k_pending = false;
+        phase1_tokens(sm, vec, tm, L, part, quarter, BTn, kg_buf(b));
+        return true;
+    };
+    bool ok = item < 0 || phase1ab(cur, 0);
 
-    for (int li = 0; item >= 0; ++li) {
+    for (int li = 0; ok && item >= 0; ++li) {
         const float* sbeta = sbeta_buf(li & 1);
         const int h = cur.h, t0 = cur.t0;
         const int BT = min(64, cur.eos - t0);
         uint8_t* img = sp.ops + ((size_t)cur.gc * H + h) * IMG_BYTES;
         const bool has_next = nidx >= 0;
+        const uint32_t kg = kg_buf(li & 1);
         if (t < 64) cp_async_wait_all();   // this item's beta
-        if (t == kStorer) bulk_wait_read();   // the previous item's pieces have left the staging buffers
         if constexpr (kDyn) {
             if (t == 0) {
                 // the item after next: the claim issued an item ago (its latency hidden by that
@@ -392,33 +416,19 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
                 claim_raw = (has_next && !stop && s_seq[2] >= 0) ? atomicAdd(sp.counter, 1) : -1;
             }
         }
-        if (!(mbar_wait_bounded(bar_k, k_par, kWaitNs) && mbar_wait_bounded(bar_qg, qg_par, kWaitNs)))
-            atomicExch(s_abort, 1);
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
-        if (*s_abort) {
-            ok = false;
-            break;
-        }
         int n2;   // the item after next
         if constexpr (kDyn) n2 = s_seq[2];
         else n2 = (has_next && nidx + G < items) ? nidx + G : -1;
         const Item nxt2 = n2 >= 0 ? item_at(sp, n2) : nxt;
-        k_par ^= 1u;
-        qg_par ^= 1u;
-        if (t == 0) k_pending = qg_pending = false;
         if (has_next) fetch_beta(nxt, (li + 1) & 1);   // the buffer the previous item used
-        // ---- phase 1: decayed operands
-        phase1_cumsum(sm, vec, t, BT);
-        __syncthreads();
-        if (t < 128) phase1_factors(vec, t);
-        __syncthreads();
-        phase1_tokens(sm, vec, tm, L, part, quarter, BT);
-        __syncthreads();
+        // ---- phase 1: decayed operands (all but the off-diagonal rows are done)
         phase1_offdiag(sm, vec, t);
         fence_proxy_async_smem();
         tmem_wait_st();
+        if (t == kStorer) bulk_wait_read();   // the previous item's pieces have left the staging buffer
         tc_fence_before_sync();
         __syncthreads();
 
@@ -450,6 +460,10 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         mma_par ^= 1u;
         tc_fence_after_sync();
         if (t == kStorer) {
+            if (has_next) {   // the k tile is no longer read
+                issue_k_loads(p, sm, bar_k, nxt.t0, nxt.h);
+                k_pending = true;
+            }
             bulk_store(img + IMG_KTH, sm + A_STAGE, IMG_BACK);
             bulk_commit();
         }
@@ -478,14 +492,17 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
                     pub1 = item;
                 }
             }
+            if (has_next) {
+                named_sync(2, kThreads - kSolveThreads);   // every seed has read this item's q and x
+                if (t == kStorer) {
+                    issue_qg_loads(p, sm, bar_qg, nxt.t0, nxt.h);
+                    qg_pending = true;
+                }
+            }
         }
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
-        if (t == 0 && has_next) {   // the k tile is no longer read
-            issue_k_loads(p, sm, bar_k, nxt.t0, nxt.h);
-            k_pending = true;
-        }
         phase3_tb_operands(sm, t, sbeta);
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -549,19 +566,19 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         }
         if (t == 0) {
             tc_fence_after_sync();
-            if (has_next) {   // the q and g tiles are no longer read
-                issue_qg_loads(p, sm, bar_qg, nxt.t0, nxt.h);
-                qg_pending = true;
-            }
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPH + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
+                umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPH + 8 * ks, desc_mnmajor(sbase + kg, 64, ks), idesc, 1u);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPL + 8 * ks, desc_mnmajor(sbase + OFF_KG, 64, ks), idesc, 1u);
+                umma_bf16_tmem_a(tm + TM_D2, tm + TM_TPL + 8 * ks, desc_mnmajor(sbase + kg, 64, ks), idesc, 1u);
             umma_commit(bar_mma);
         }
+        // the next item's phase 1 meanwhile.  It writes the g tile, vec, the X region, TMEM
+        // columns [128, 256) and the other K_Gamma buffer, none of which this item still reads.
+        if (has_next && !(ok = phase1ab(nxt, (li + 1) & 1))) break;
+        if (t == kStorer) bulk_wait_read();   // the [Tb; M] piece has left the staging buffer
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
@@ -574,13 +591,13 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                st_shared_v4(sbase + A_STAGE2 + sw128_chunk(L, 4 * part + q, 128), pk[4 * q], pk[4 * q + 1],
+                st_shared_v4(sbase + A_STAGE + sw128_chunk(L, 4 * part + q, 128), pk[4 * q], pk[4 * q + 1],
                              pk[4 * q + 2], pk[4 * q + 3]);
             fence_proxy_async_smem();
         }
         __syncthreads();
         if (t == kStorer) {
-            bulk_store(img + IMG_A1, sm + A_STAGE2, 32768);
+            bulk_store(img + IMG_A1, sm + A_STAGE, 32768);
             bulk_commit();
         }
         cur = nxt;   // the next item's first barrier orders these TMEM reads before its writes
@@ -601,9 +618,11 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
     }
     if (!ok && t == 0) {
         report_status(p.status, kDevTimeout);
+        mbar_wait_bounded(bar_mma, mma_par, kWaitNs);
+    }
+    if (!ok && t == kStorer) {
         if (k_pending) mbar_wait_bounded(bar_k, k_par, kWaitNs);
         if (qg_pending) mbar_wait_bounded(bar_qg, qg_par, kWaitNs);
-        mbar_wait_bounded(bar_mma, mma_par, kWaitNs);
     }
     tc_fence_before_sync();
     __syncthreads();

@@ -362,7 +362,7 @@ __device__ __forceinline__ void build_state_operand(uint8_t* sm, const float* ve
 // q-row thread also writes its K_Gamma B operand, so that the two halves (which run on
 // different SMSPs) carry the same number of reciprocals.
 __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uint32_t tm, int L, int part,
-                                              int quarter, int BT)
+                                              int quarter, int BT, uint32_t kg_off = OFF_KG)
 {
     const int r = L & 63, J = r >> 4;
     const bool isq = L >= 64;
@@ -407,7 +407,7 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
             const float ev[8] = {e4a.x, e4a.y, e4a.z, e4a.w, e4b.x, e4b.y, e4b.z, e4b.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) kv[e] = kv[e] * xs[e] * ev[e];
-            st_shared_v4(sbase + OFF_KG + sw128_chunk(r, c0 >> 3, 64), pack_bf16x2(kv[0], kv[1]),
+            st_shared_v4(sbase + kg_off + sw128_chunk(r, c0 >> 3, 64), pack_bf16x2(kv[0], kv[1]),
                          pack_bf16x2(kv[2], kv[3]), pack_bf16x2(kv[4], kv[5]), pack_bf16x2(kv[6], kv[7]));
         }
     }
