@@ -395,7 +395,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if (*s_abort) return false;
         k_par ^= 1u;
         if (t == kStorer) k_pending = false;
-        phase1_tokens(sm, vec, tm, L, part, quarter, BTn, kg_buf(b));
+        phase1_tokens<true>(sm, vec, tm, L, part, quarter, BTn, kg_buf(b));
         return true;
     };
     bool ok = item < 0 || phase1ab(cur, 0);

@@ -137,6 +137,10 @@ __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+__device__ __forceinline__ void st_shared_v2(uint32_t saddr, uint32_t a, uint32_t b)
+{
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(saddr), "r"(a), "r"(b) : "memory");
+}
 __device__ __forceinline__ void st_shared_f4(uint32_t saddr, float a, float b, float c, float d)
 {
     st_shared_v4(saddr, __float_as_uint(a), __float_as_uint(b), __float_as_uint(c), __float_as_uint(d));
@@ -358,9 +362,12 @@ __device__ __forceinline__ void build_state_operand(uint8_t* sm, const float* ve
 // ---------------------------------------------------------------- phase 1b: token operands
 // Thread (lane L, part p): token r = L % 64 of the q rows (L >= 64) or k rows (L < 64),
 // channels [32p, 32p + 32).  Writes the tf32 row operand [K_r; Q_r] (TMEM).  Token r's
-// diagonal-tile column operand is split between the k-row and the q-row thread, and the
-// q-row thread also writes its K_Gamma B operand, so that the two halves (which run on
-// different SMSPs) carry the same number of reciprocals.
+// diagonal-tile column operand is split between the k-row and the q-row thread (channels
+// c0..c0+3 and c0+4..c0+7 of each group of 8), so that the two halves, which run on
+// different SMSPs, carry the same number of reciprocals.  Its K_Gamma B operand is
+// written by the q-row thread, or with kSplitKG split the same way (the same values; more
+// registers, which the one-CTA-per-head kernel cannot spare).
+template <bool kSplitKG = false>
 __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uint32_t tm, int L, int part,
                                               int quarter, int BT, uint32_t kg_off = OFF_KG)
 {
@@ -389,12 +396,19 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
         }
         // diagonal-tile column operand of reference J, k_r e^{rho_J - Gamma_r} <= e^{80} |k_r|:
         // channels [c0, c0 + 4) from the k-row thread, [c0 + 4, c0 + 8) from the q-row thread
+        // K_Gamma B operand: k_r e^{Gamma_r} = k_r x_r E_J (bf16)
         const uint32_t rj = kc_row(J) + r;
-        if (!isq) {
+        const uint32_t kg = sbase + kg_off + sw128_chunk(r, c0 >> 3, 64);
+        if (!isq) {   // xv holds k_r here
             st_shared_f4(kc + sw128_off_f32(rj, c0, KC_ROWS), tf32_round(xv[0] * rcpf(xs[0])),
                          tf32_round(xv[1] * rcpf(xs[1])), tf32_round(xv[2] * rcpf(xs[2])),
                          tf32_round(xv[3] * rcpf(xs[3])));
-        } else {      // and the K_Gamma B operand: k_r e^{Gamma_r} = k_r x_r E_J (bf16)
+            if constexpr (kSplitKG) {
+                const float4 e4 = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
+                st_shared_v2(kg, pack_bf16x2(xv[0] * xs[0] * e4.x, xv[1] * xs[1] * e4.y),
+                             pack_bf16x2(xv[2] * xs[2] * e4.z, xv[3] * xs[3] * e4.w));
+            }
+        } else {
             float kv[8];
             unpack8(ld_shared_v4(sbase + OFF_K + sw128_chunk(r, c0 >> 3, 64)), kv);
 #pragma unroll
@@ -402,13 +416,19 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
             st_shared_f4(kc + sw128_off_f32(rj, c0 + 4, KC_ROWS), tf32_round(kv[4] * rcpf(xs[4])),
                          tf32_round(kv[5] * rcpf(xs[5])), tf32_round(kv[6] * rcpf(xs[6])),
                          tf32_round(kv[7] * rcpf(xs[7])));
-            const float4 e4a = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
-            const float4 e4b = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
-            const float ev[8] = {e4a.x, e4a.y, e4a.z, e4a.w, e4b.x, e4b.y, e4b.z, e4b.w};
+            if constexpr (kSplitKG) {
+                const float4 e4 = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
+                st_shared_v2(kg + 8u, pack_bf16x2(kv[4] * xs[4] * e4.x, kv[5] * xs[5] * e4.y),
+                             pack_bf16x2(kv[6] * xs[6] * e4.z, kv[7] * xs[7] * e4.w));
+            } else {
+                const float4 e4a = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
+                const float4 e4b = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
+                const float ev[8] = {e4a.x, e4a.y, e4a.z, e4a.w, e4b.x, e4b.y, e4b.z, e4b.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) kv[e] = kv[e] * xs[e] * ev[e];
-            st_shared_v4(sbase + kg_off + sw128_chunk(r, c0 >> 3, 64), pack_bf16x2(kv[0], kv[1]),
-                         pack_bf16x2(kv[2], kv[3]), pack_bf16x2(kv[4], kv[5]), pack_bf16x2(kv[6], kv[7]));
+                for (int e = 0; e < 8; ++e) kv[e] = kv[e] * xs[e] * ev[e];
+                st_shared_v4(kg, pack_bf16x2(kv[0], kv[1]), pack_bf16x2(kv[2], kv[3]), pack_bf16x2(kv[4], kv[5]),
+                             pack_bf16x2(kv[6], kv[7]));
+            }
         }
     }
     tmem_st32(tmem_addr(tm, 32 * quarter, TM_KQ + 32 * part), kq);
