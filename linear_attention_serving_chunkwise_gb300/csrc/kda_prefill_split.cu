@@ -185,13 +185,14 @@ __device__ __forceinline__ void prefetch_l2(const void* gsrc, uint32_t bytes)
 constexpr uint32_t A_STAGE = OFF_V0;
 constexpr uint32_t A_KG2 = ((uint32_t)SMEM_USED + 1023u) & ~1023u;
 constexpr uint32_t A_BETA2 = A_KG2 + 16384;
-constexpr uint32_t A_USED = A_BETA2 + 256;
+constexpr uint32_t A_INFO = A_BETA2 + 256;   // two chunk-table entries (int2), see prep_items
+constexpr uint32_t A_USED = A_INFO + 16;
 constexpr size_t A_SMEM_BYTES = A_USED + 1024;   // slack for 1024-byte alignment
 static_assert(A_USED <= B_BAR, "the prep layout ends below the scan's word block, which the single launch's "
                                 "TMEM slot occupies from the start");
 static_assert(A_SMEM_BYTES <= 232448, "prep shared memory");
 static_assert(OFF_V1 + 16384 == A_STAGE + 32768, "staging buffer");
-static_assert(A_KG2 % 1024 == 0 && A_BETA2 % 16 == 0, "second K_Gamma and beta buffers");
+static_assert(A_KG2 % 1024 == 0 && A_BETA2 % 16 == 0 && A_INFO % 8 == 0, "second K_Gamma, beta, info buffers");
 
 __device__ __forceinline__ void cp_async4_zfill(void* smem_dst, const void* gsrc, bool valid)
 {
@@ -199,7 +200,11 @@ __device__ __forceinline__ void cp_async4_zfill(void* smem_dst, const void* gsrc
                  "r"(valid ? 4 : 0)
                  : "memory");
 }
-__device__ __forceinline__ void cp_async_commit_wait_prev() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async8(void* smem_dst, const void* gsrc)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // ---------------------------------------------------------------- step 1: chunk offsets
@@ -277,7 +282,7 @@ struct Item {
     int h, t0, eos, gc;
 };
 
-// item = gc * H + h; the (t0, eos) load is first used an item later
+// item = gc * H + h, with its (t0, eos) entry of the chunk table (read now: the prologue only)
 __device__ __forceinline__ Item item_at(const SplitParams& sp, int item)
 {
     const int H = sp.p.num_heads;
@@ -314,6 +319,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
     uint64_t* bar_mma = bar_k + 2;
     int* s_abort = reinterpret_cast<int*>(sm + OFF_BAR + 36);
     int* s_seq = reinterpret_cast<int*>(sm + OFF_BAR + 40);   // item indices claimed by thread 0
+    int2* s_info = reinterpret_cast<int2*>(sm + A_INFO);
     const uint32_t sbase = smem_u32(sm);
     const int H = p.num_heads;
     const int items = __ldg(sp.chunk_off + p.num_seqs) * H;
@@ -371,7 +377,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if (t < 64) {
             const bool valid = it.t0 + t < it.eos;
             cp_async4_zfill(sbeta_buf(b) + t, valid ? p.beta + (size_t)(it.t0 + t) * H + it.h : p.beta, valid);
-            cp_async_commit_wait_prev();
+            cp_async_commit();
         }
     };
     if (item >= 0) fetch_beta(cur, 0);
@@ -387,7 +393,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if (*s_abort) return false;
         qg_par ^= 1u;
         if (t == kStorer) qg_pending = false;
-        phase1_cumsum(sm, vec, t, BTn);
+        phase1_cumsum<true>(sm, vec, t, BTn);
         __syncthreads();
         if (t < 128) phase1_factors(vec, t);
         if (!mbar_wait_bounded(bar_k, k_par, kWaitNs)) atomicExch(s_abort, 1);
@@ -407,7 +413,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         uint8_t* img = sp.ops + ((size_t)cur.gc * H + h) * IMG_BYTES;
         const bool has_next = nidx >= 0;
         const uint32_t kg = kg_buf(li & 1);
-        if (t < 64) cp_async_wait_all();   // this item's beta
+        if (t < 64) cp_async_wait_all();   // this item's beta; thread 0: the next item's entry
         if constexpr (kDyn) {
             if (t == 0) {
                 // the item after next: the claim issued an item ago (its latency hidden by that
@@ -422,10 +428,20 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         int n2;   // the item after next
         if constexpr (kDyn) n2 = s_seq[2];
         else n2 = (has_next && nidx + G < items) ? nidx + G : -1;
-        const Item nxt2 = n2 >= 0 ? item_at(sp, n2) : nxt;
+        if (li > 0 && has_next) {   // the next item's chunk-table entry, copied an item ago
+            const int2 inf = s_info[(li + 1) & 1];
+            nxt.t0 = inf.x;
+            nxt.eos = inf.y;
+        }
         if (has_next) fetch_beta(nxt, (li + 1) & 1);   // the buffer the previous item used
+        // the chunk-table entry of the item after next, copied by thread 0 and read from shared
+        // memory at the next item's top, so that no thread waits for the load
+        if (t == 0 && n2 >= 0) {
+            cp_async8(s_info + (li & 1), sp.chunk_info + n2 / H);
+            cp_async_commit();
+        }
         // ---- phase 1: decayed operands (all but the off-diagonal rows are done)
-        phase1_offdiag(sm, vec, t);
+        phase1_offdiag<true>(sm, vec, t);
         fence_proxy_async_smem();
         tmem_wait_st();
         if (t == kStorer) bulk_wait_read();   // the previous item's pieces have left the staging buffer
@@ -601,7 +617,10 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             bulk_commit();
         }
         cur = nxt;   // the next item's first barrier orders these TMEM reads before its writes
-        nxt = nxt2;
+        if (n2 >= 0) {   // its t0 and eos are read at the next item's top
+            nxt.gc = n2 / H;
+            nxt.h = n2 - nxt.gc * H;
+        }
         item = nidx;
         nidx = n2;
     }

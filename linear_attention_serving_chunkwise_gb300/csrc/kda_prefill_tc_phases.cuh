@@ -235,18 +235,34 @@ __device__ __forceinline__ void issue_qg_loads(const TcParams& p, uint8_t* sm, u
 // end count as 0), replaces g_r in the tile by x_r = 2^{lambda_r} = e^{Gamma_r - rho_J}
 // (in (0, 1], a normal float since g >= -5) and stores D_J = 2^{s_J}, the last x of the
 // sub-tile (s_J: the sub-tile's sum).
+template <bool kHoist = false>
 __device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, int BT)
 {
     const int c = t & 127, J = t >> 7;
     float acc = 0.f, x = 1.f;
+    if constexpr (kHoist) {   // the 16 loads first (16 more registers live)
+        float gv[16];
 #pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-        const int r = 16 * J + rr;
-        float* gp = reinterpret_cast<float*>(sm + OFF_G + g_off(r, c));
-        const float gv = (r < BT) ? *gp : 0.f;
-        acc = fmaf(gv, kLog2e, acc);
-        x = ex2f(acc);
-        *gp = x;
+        for (int rr = 0; rr < 16; ++rr) {
+            const int r = 16 * J + rr;
+            gv[rr] = (r < BT) ? *reinterpret_cast<const float*>(sm + OFF_G + g_off(r, c)) : 0.f;
+        }
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+            acc = fmaf(gv[rr], kLog2e, acc);
+            x = ex2f(acc);
+            *reinterpret_cast<float*>(sm + OFF_G + g_off(16 * J + rr, c)) = x;
+        }
+    } else {
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+            const int r = 16 * J + rr;
+            float* gp = reinterpret_cast<float*>(sm + OFF_G + g_off(r, c));
+            const float gv = (r < BT) ? *gp : 0.f;
+            acc = fmaf(gv, kLog2e, acc);
+            x = ex2f(acc);
+            *gp = x;
+        }
     }
     vec[(V_D + J) * 128 + c] = x;
 }
@@ -283,21 +299,41 @@ __device__ __forceinline__ void phase1_factors(float* vec, int c)
 // i16 = t % 16 and channels [4 cq, 4 cq + 4), cq = t / 16, of all six (m, J) pairs (a
 // warp: 16 tokens x 2 channel quads, so its factor loads are broadcasts); the row of each
 // pair is a compile-time offset from the thread's own swizzled base.
+template <bool kHoist = false>
 __device__ __forceinline__ void phase1_offdiag(uint8_t* sm, const float* vec, int t)
 {
     const int i16 = t & 15, cq = (t >> 4) & 31, c0 = 4 * cq;
     // sw128_off_f32(row, c0, KC_ROWS) with row % 8 == i16 % 8 for every row used below
     const uint32_t base = smem_u32(sm) + OFF_X + (cq >> 3) * (KC_ROWS * 128u) + i16 * 128u +
                           ((uint32_t)((cq & 7) ^ (i16 & 7)) << 4);
+    if constexpr (kHoist) {
+        // the rows read (diagonal tiles) and written (off-diagonal ones) are disjoint: all
+        // loads first, so that their latencies overlap (more registers live at once)
+        uint4 d[3];
+        float4 f[6];
 #pragma unroll
-    for (int b = 0; b < 6; ++b) {
-        const int m = (b == 0) ? 1 : ((b < 3) ? 2 : 3);
-        const int J = b - m * (m - 1) / 2;
-        const uint4 d = ld_shared_v4(base + (kc_row(J) + 16 * J) * 128u);
-        const float4 f = *reinterpret_cast<const float4*>(vec + (V_DF + b) * 128 + c0);
-        st_shared_f4(base + (kc_row(m) + 16 * J) * 128u, tf32_round(__uint_as_float(d.x) * f.x),
-                     tf32_round(__uint_as_float(d.y) * f.y), tf32_round(__uint_as_float(d.z) * f.z),
-                     tf32_round(__uint_as_float(d.w) * f.w));
+        for (int J = 0; J < 3; ++J) d[J] = ld_shared_v4(base + (kc_row(J) + 16 * J) * 128u);
+#pragma unroll
+        for (int b = 0; b < 6; ++b) f[b] = *reinterpret_cast<const float4*>(vec + (V_DF + b) * 128 + c0);
+#pragma unroll
+        for (int b = 0; b < 6; ++b) {
+            const int m = (b == 0) ? 1 : ((b < 3) ? 2 : 3);
+            const int J = b - m * (m - 1) / 2;
+            st_shared_f4(base + (kc_row(m) + 16 * J) * 128u, tf32_round(__uint_as_float(d[J].x) * f[b].x),
+                         tf32_round(__uint_as_float(d[J].y) * f[b].y), tf32_round(__uint_as_float(d[J].z) * f[b].z),
+                         tf32_round(__uint_as_float(d[J].w) * f[b].w));
+        }
+    } else {
+#pragma unroll
+        for (int b = 0; b < 6; ++b) {
+            const int m = (b == 0) ? 1 : ((b < 3) ? 2 : 3);
+            const int J = b - m * (m - 1) / 2;
+            const uint4 d = ld_shared_v4(base + (kc_row(J) + 16 * J) * 128u);
+            const float4 f = *reinterpret_cast<const float4*>(vec + (V_DF + b) * 128 + c0);
+            st_shared_f4(base + (kc_row(m) + 16 * J) * 128u, tf32_round(__uint_as_float(d.x) * f.x),
+                         tf32_round(__uint_as_float(d.y) * f.y), tf32_round(__uint_as_float(d.z) * f.z),
+                         tf32_round(__uint_as_float(d.w) * f.w));
+        }
     }
 }
 
