@@ -84,7 +84,7 @@ const char* kda_status_string(kda_status status);
  * Returns 0 for a desc that kda_prefill would reject.  Non-zero exactly when the
  * chunkwise form runs chunk-parallel: bf16, dk = dv = 128, at most 32768 (chunk, head)
  * items ((total_tokens / 64 + num_seqs) * num_heads), and a cost estimate from the shape
- * favours it over one CTA per (sequence, head): few units (up to ~120 for 8192-token
+ * favours it over one CTA per (sequence, head): few units (up to ~130 for 8192-token
  * sequences), or a partial second wave on the 152 SMs.  The workspace then holds
  * the chunk offsets and, per (64-token chunk, head), the operands of that chunk's state
  * step: 98,816 bytes each, for (total_tokens / 64 + num_seqs) * num_heads chunks.

@@ -70,10 +70,12 @@ constexpr uint32_t B_TM_D1 = 128;       // [W; O] accumulator
 constexpr uint32_t B_TM_COLS = 256;
 
 // single-launch form: at least this many CTAs never scan (they finish the prep items), and
-// the switch point uses these per-chunk costs (cycles, measured on GB300)
+// the switch point uses these costs (cycles on GB300: a scan's 6.0 K per chunk as measured,
+// the prep's 19.4 K per item less an allowance for the scans' start and flag waits, tuned
+// at 64 and 96 units)
 constexpr long long kSingleMinProducers = 32;
 constexpr long long kScanCyclesPerChunk = 6000;
-constexpr long long kPrepCyclesPerItem = 21000;
+constexpr long long kPrepCyclesPerItem = 18400;
 
 static_assert(B_KTH % 1024 == 0 && B_V0 % 1024 == 0 && B_SB % 1024 == 0 && B_WH % 1024 == 0, "tile alignment");
 static_assert(B_KTH >= IMG_FRONT && B_V0 >= B_KTH + IMG_BACK && B_V1 == B_V0 + 16384 && B_SB >= B_V1 + 16384 &&

@@ -109,11 +109,14 @@ def test_prefill_path_selection_and_split_workspace(lib):
     assert p["kernel_launches"] == 2 and p["tensor_cores"] == 1   # offsets + one cooperative launch
     assert items * 98816 <= p["workspace_bytes"] <= items * 98816 + items * 4 + 4096
     assert plan(1, 8192, 112)["kernel_launches"] == 2
-    assert plan(1, 8192, 124)["kernel_launches"] == 1 and plan(1, 8192, 124)["workspace_bytes"] == 0
-    assert plan(2, 8192, 64)["kernel_launches"] == 1                 # 128 units of 4096 tokens
+    assert plan(1, 8192, 120)["kernel_launches"] == 2                # the last single launch
+    assert plan(1, 8192, 124)["kernel_launches"] == 3                # split, separate launches
+    assert plan(1, 8192, 136)["kernel_launches"] == 1 and plan(1, 8192, 136)["workspace_bytes"] == 0
+    assert plan(2, 8192, 64)["kernel_launches"] == 3                 # 128 units of 4096 tokens
     assert plan(1, 8192, 152)["kernel_launches"] == 1                # one full wave
     assert plan(1, 8192, 160)["kernel_launches"] == 3                # a second wave of 8: separate launches
-    assert plan(1, 8192, 240)["kernel_launches"] == 1                # a second wave of 88
+    assert plan(1, 8192, 240)["kernel_launches"] == 3                # a second wave of 88
+    assert plan(2, 8192, 76)["kernel_launches"] == 1                 # one full wave
     assert plan(40, 8000, 3)["kernel_launches"] == 1                 # 120 short sequences
     assert plan(1, 64 * 400, 96)["kernel_launches"] == 1             # 38,496 items: over the cap
     assert plan(1, 8192, 96, kda.KDA_F32)["kernel_launches"] == 1    # fp32 inputs: CUDA-core kernel
