@@ -32,6 +32,18 @@
  *     gave up) are recorded in a per-device status word; the affected work is
  *     skipped, nothing traps.  kda_last_device_status() reports and clears it.
  *   - q is not scaled (no 1/sqrt(dk)); callers pre-scale q if they want that.
+ *   - Input prologue (the `prologue` word of kda_prefill_desc, kda_decode and
+ *     kda_decode_multi; 0 = the inputs are used as given).  The workloads'
+ *     input recipe -- q and k L2-normalised per (token, head), g = g_min *
+ *     sigmoid(.), beta = sigmoid(.) -- can run inside the kernels' loads instead
+ *     of as separate passes over HBM:
+ *       KDA_PROLOGUE_QK_L2NORM   q and k are replaced by x / max(||x||_2, 1e-12)
+ *                                over the dk channels of each (token, head),
+ *                                computed in fp32 and rounded to qkv_dtype;
+ *       KDA_PROLOGUE_G_LOGITS    g holds logits z; the decay used is -5 * sigmoid(z);
+ *       KDA_PROLOGUE_BETA_LOGITS beta holds logits y; the write used is sigmoid(y).
+ *     The output gate that the pages pair with KDA (llm-atlas Q08) is not part
+ *     of this: its form is not given there.
  *   - Preconditions not checked on the host: g in [-5, 0] (the bounded
  *     log-decay; never clamped), beta in [0, 1].  Values outside these ranges
  *     are unsupported: they are computed, but without the accuracy bound.
@@ -46,7 +58,12 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 1
+#define KDA_ABI_VERSION 2
+
+#define KDA_PROLOGUE_QK_L2NORM 1
+#define KDA_PROLOGUE_G_LOGITS 2
+#define KDA_PROLOGUE_BETA_LOGITS 4
+#define KDA_PROLOGUE_ALL 7
 
 typedef enum kda_status {
     KDA_OK = 0,
@@ -71,6 +88,7 @@ typedef struct kda_prefill_desc {
     int32_t dk;             /* key/query channels: 64 or 128 */
     int32_t dv;             /* value channels: must equal dk */
     int32_t qkv_dtype;      /* a kda_dtype */
+    int32_t prologue;       /* KDA_PROLOGUE_* bits (0: inputs as given); others rejected */
 } kda_prefill_desc;
 
 /* Library ABI version (KDA_ABI_VERSION of the build). */
@@ -241,8 +259,10 @@ kda_status kda_prefill_host_static(const kda_prefill_desc* desc,
  *   g      [B, H, dk]  fp32;          beta [B, H] fp32
  *   state  [B, H, dk, dv] fp32, read and overwritten in place
  *   out    [B, H, dv] fp32 (o = S_new^T q); must not overlap any input or state
+ *   prologue  KDA_PROLOGUE_* bits applied to this token's inputs (see the top)
  */
 kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, int32_t qkv_dtype,
+                      int32_t prologue,
                       const void* q, const void* k, const void* v,
                       const float* g, const float* beta,
                       float* state, float* out,
@@ -266,12 +286,13 @@ kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, 
  *   out      [B, K, H, dv] fp32, o for every token (whatever n_apply says), or NULL
  * Verification: one call with n_apply = 0 (outputs for all K drafts, state untouched),
  * then one with n_apply = the accepted count per sequence and out = NULL.
+ * prologue: KDA_PROLOGUE_* bits applied to every token's inputs (see the top).
  * Errors: as kda_decode, plus KDA_ERR_INVALID_ARG for K out of range.
  */
 #define KDA_DECODE_MULTI_MAX_TOKENS 64
 
 kda_status kda_decode_multi(int32_t batch, int32_t tokens, int32_t num_heads, int32_t dk, int32_t dv,
-                            int32_t qkv_dtype,
+                            int32_t qkv_dtype, int32_t prologue,
                             const void* q, const void* k, const void* v,
                             const float* g, const float* beta,
                             const int32_t* n_apply,

@@ -123,20 +123,31 @@ def _l2_normalised(shape, seed, stream, device, out_dtype):
     return (x / n).to(out_dtype)
 
 
-def make_prefill_inputs(cfg: PrefillConfig, seed: int = 0, device="cpu") -> dict:
+def _qkgb(shape_qk, shape_b, seed, device, dtype, raw):
+    """q, k, g, beta of the recipe, or with ``raw`` the same draws before it: q and k not
+    normalised (the N(0,1) draws in the storage type), g and beta as the N(0,1) logits."""
+    if raw:
+        q = _normal(shape_qk, seed, _S_Q, device, dtype=torch.float64).to(dtype)
+        k = _normal(shape_qk, seed, _S_K, device, dtype=torch.float64).to(dtype)
+        return q, k, _normal(shape_qk, seed, _S_G, device), _normal(shape_b, seed, _S_B, device)
+    q = _l2_normalised(shape_qk, seed, _S_Q, device, dtype)
+    k = _l2_normalised(shape_qk, seed, _S_K, device, dtype)
+    g = (G_MIN * torch.sigmoid(_normal(shape_qk, seed, _S_G, device))).contiguous()
+    return q, k, g, torch.sigmoid(_normal(shape_b, seed, _S_B, device)).contiguous()
+
+
+def make_prefill_inputs(cfg: PrefillConfig, seed: int = 0, device="cpu", raw: bool = False) -> dict:
     """Seeded prefill inputs in the library layouts.
 
     q, k: [T, H, dk]; v: [T, H, dv] (cfg.qkv_dtype); g: [T, H, dk] fp32;
     beta: [T, H] fp32; cu_seqlens: [N+1] int32; init_state: [N, H, dk, dv]
-    fp32 or None.  All tensors are contiguous on ``device``.
+    fp32 or None.  All tensors are contiguous on ``device``.  With ``raw`` q, k, g and
+    beta are the draws before the recipe (for the library's input prologue).
     """
     T, H, dk, dv = cfg.total_tokens, cfg.num_heads, cfg.dk, cfg.dv
     d = {}
-    d["q"] = _l2_normalised((T, H, dk), seed, _S_Q, device, cfg.qkv_dtype)
-    d["k"] = _l2_normalised((T, H, dk), seed, _S_K, device, cfg.qkv_dtype)
+    d["q"], d["k"], d["g"], d["beta"] = _qkgb((T, H, dk), (T, H), seed, device, cfg.qkv_dtype, raw)
     d["v"] = _normal((T, H, dv), seed, _S_V, device).to(cfg.qkv_dtype)
-    d["g"] = (G_MIN * torch.sigmoid(_normal((T, H, dk), seed, _S_G, device))).contiguous()
-    d["beta"] = torch.sigmoid(_normal((T, H), seed, _S_B, device)).contiguous()
     d["cu_seqlens"] = torch.from_numpy(cfg.cu_seqlens()).to(device)
     if cfg.init_state == "normal":
         d["init_state"] = _normal((cfg.num_seqs, H, dk, dv), seed, _S_S0, device, std=0.02)
@@ -145,17 +156,15 @@ def make_prefill_inputs(cfg: PrefillConfig, seed: int = 0, device="cpu") -> dict
     return d
 
 
-def make_decode_inputs(cfg: DecodeConfig, seed: int = 0, device="cpu", steps: Optional[int] = None) -> dict:
+def make_decode_inputs(cfg: DecodeConfig, seed: int = 0, device="cpu", steps: Optional[int] = None,
+                       raw: bool = False) -> dict:
     """Seeded decode inputs: per step q,k [S,B,H,dk], v [S,B,H,dv], g [S,B,H,dk], beta [S,B,H];
-    state0 [B,H,dk,dv] ~ N(0, 0.02)."""
+    state0 [B,H,dk,dv] ~ N(0, 0.02).  ``raw`` as for make_prefill_inputs."""
     S = cfg.steps if steps is None else steps
     B, H, dk, dv = cfg.batch, cfg.num_heads, cfg.dk, cfg.dv
     d = {}
-    d["q"] = _l2_normalised((S, B, H, dk), seed, _S_Q, device, cfg.qkv_dtype)
-    d["k"] = _l2_normalised((S, B, H, dk), seed, _S_K, device, cfg.qkv_dtype)
+    d["q"], d["k"], d["g"], d["beta"] = _qkgb((S, B, H, dk), (S, B, H), seed, device, cfg.qkv_dtype, raw)
     d["v"] = _normal((S, B, H, dv), seed, _S_V, device).to(cfg.qkv_dtype)
-    d["g"] = (G_MIN * torch.sigmoid(_normal((S, B, H, dk), seed, _S_G, device))).contiguous()
-    d["beta"] = torch.sigmoid(_normal((S, B, H), seed, _S_B, device)).contiguous()
     d["state0"] = _normal((B, H, dk, dv), seed, _S_S0, device, std=0.02)
     return d
 

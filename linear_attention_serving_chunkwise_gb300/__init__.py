@@ -5,6 +5,7 @@ The compute lives in the CUDA library ``libkda_gb300.so`` behind the C ABI in
 """
 from ._lib import (  # noqa: F401
     EXPORTED,
+    KDA_ABI_VERSION,
     KDA_BF16,
     KDA_DECODE_MULTI_MAX_TOKENS,
     KDA_ERR_CUDA,
@@ -14,6 +15,10 @@ from ._lib import (  # noqa: F401
     KDA_ERR_WORKSPACE,
     KDA_F32,
     KDA_OK,
+    KDA_PROLOGUE_ALL,
+    KDA_PROLOGUE_BETA_LOGITS,
+    KDA_PROLOGUE_G_LOGITS,
+    KDA_PROLOGUE_QK_L2NORM,
     KDA_STATIC_SCRATCH_BYTES,
     KDAError,
     LIB_PATH,

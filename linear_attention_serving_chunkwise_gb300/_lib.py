@@ -23,6 +23,12 @@ KDA_ERR_CUDA = -4
 KDA_ERR_TIMEOUT = -5
 KDA_F32 = 0
 KDA_BF16 = 1
+KDA_ABI_VERSION = 2
+# input prologue bits (include/kda.h): q/k L2 normalisation, g = -5 sigmoid(z), beta = sigmoid(y)
+KDA_PROLOGUE_QK_L2NORM = 1
+KDA_PROLOGUE_G_LOGITS = 2
+KDA_PROLOGUE_BETA_LOGITS = 4
+KDA_PROLOGUE_ALL = 7
 
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes", "kda_prefill_query",
@@ -40,7 +46,8 @@ class KDAError(RuntimeError):
 
 class PrefillDesc(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32), ("num_heads", ctypes.c_int32),
-                ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32)]
+                ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32),
+                ("prologue", ctypes.c_int32)]
 
 
 class PrefillPlan(ctypes.Structure):
@@ -84,9 +91,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kda_prefill_host_static.argtypes = [ctypes.POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
                                             vp]
     lib.kda_decode.restype = ctypes.c_int
-    lib.kda_decode.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.kda_decode.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.kda_decode_multi.restype = ctypes.c_int
-    lib.kda_decode_multi.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.kda_decode_multi.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.kda_last_device_status.restype = ctypes.c_int
     lib.kda_last_device_status.argtypes = [vp]
     if path is None:
@@ -128,8 +135,10 @@ def _keep_until_done(tensor: torch.Tensor, stream) -> None:
         tensor.record_stream(stream)
 
 
-def make_desc(num_seqs: int, total_tokens: int, num_heads: int, dk: int, dv: int, qkv_dtype: int) -> PrefillDesc:
-    return PrefillDesc(int(num_seqs), int(total_tokens), int(num_heads), int(dk), int(dv), int(qkv_dtype))
+def make_desc(num_seqs: int, total_tokens: int, num_heads: int, dk: int, dv: int, qkv_dtype: int,
+              prologue: int = 0) -> PrefillDesc:
+    return PrefillDesc(int(num_seqs), int(total_tokens), int(num_heads), int(dk), int(dv), int(qkv_dtype),
+                       int(prologue))
 
 
 def prefill_workspace_bytes(desc: PrefillDesc) -> int:
@@ -148,18 +157,19 @@ def prefill_query(desc: PrefillDesc) -> dict:
 
 def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_state=None, *,
             num_seqs: Optional[int] = None, want_final: bool = True, workspace=None, stream=None, check=True,
-            checkpoint_interval: int = 0, checkpoint_slots: int = 0, checkpoints=None):
+            checkpoint_interval: int = 0, checkpoint_slots: int = 0, checkpoints=None, prologue: int = 0):
     """KDA prefill through ``kda_prefill``.
 
     q, k [T,H,dk], v [T,H,dv] (fp32 or bf16); g [T,H,dk] fp32; beta [T,H] fp32;
     cu_seqlens [N+1] int32 on the device, or None with ``num_seqs`` equal
     sequences (default 1); init_state [N,H,dk,dv] fp32 or None.
     ``out``/``final_state`` are allocated if not given (``final_state`` may be
-    ``init_state`` for in-place chaining).  Returns (out, final_state)."""
+    ``init_state`` for in-place chaining).  ``prologue``: KDA_PROLOGUE_* bits (q, k, g and
+    beta then hold the raw values of the input recipe).  Returns (out, final_state)."""
     T, H, dk = q.shape
     dv = v.shape[2]
     N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
-    desc = make_desc(N, T, H, dk, dv, _dtype_code(q))
+    desc = make_desc(N, T, H, dk, dv, _dtype_code(q), prologue)
     if out is None:
         out = torch.empty((T, H, dv), dtype=torch.float32, device=q.device)
         _keep_until_done(out, stream)
@@ -196,7 +206,7 @@ def prefill_host_workspace_bytes(desc: PrefillDesc, segment_tokens: int) -> int:
 
 def prefill_host(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_state=None, *,
                  segment_tokens: int = 1024, num_seqs: Optional[int] = None, want_final: bool = True,
-                 workspace=None, stream=None, check=True, device=None):
+                 workspace=None, stream=None, check=True, device=None, prologue: int = 0):
     """KDA prefill through ``kda_prefill_host``: every tensor is a CPU tensor (pinned for
     the copies to overlap the kernels); ``workspace`` is a CUDA uint8 tensor, allocated if
     not given.  Asynchronous like the other entry points: the results are in ``out`` /
@@ -205,7 +215,7 @@ def prefill_host(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, f
     T, H, dk = q.shape
     dv = v.shape[2]
     N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
-    desc = make_desc(N, T, H, dk, dv, _dtype_code(q))
+    desc = make_desc(N, T, H, dk, dv, _dtype_code(q), prologue)
     pin = q.is_pinned()
     if out is None:
         out = torch.empty((T, H, dv), dtype=torch.float32, pin_memory=pin)
@@ -228,13 +238,13 @@ def prefill_host(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, f
 
 def prefill_host_static(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_state=None, *,
                         segment_tokens: int = 128, num_seqs: Optional[int] = None, want_final: bool = True,
-                        stream=None, check=True):
+                        stream=None, check=True, prologue: int = 0):
     """``prefill_host`` through ``kda_prefill_host_static``: the device staging is the
     library's own scratch (no workspace, no device allocation).  Returns (out, final_state)."""
     T, H, dk = q.shape
     dv = v.shape[2]
     N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
-    desc = make_desc(N, T, H, dk, dv, _dtype_code(q))
+    desc = make_desc(N, T, H, dk, dv, _dtype_code(q), prologue)
     pin = q.is_pinned()
     if out is None:
         out = torch.empty((T, H, dv), dtype=torch.float32, pin_memory=pin)
@@ -248,34 +258,37 @@ def prefill_host_static(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=
     return out, final_state
 
 
-def decode(q, k, v, g, beta, state, out=None, *, stream=None, check=True):
+def decode(q, k, v, g, beta, state, out=None, *, stream=None, check=True, prologue: int = 0):
     """One KDA decode step through ``kda_decode``; ``state`` [B,H,dk,dv] fp32 is updated in place.
 
-    q, k [B,H,dk], v [B,H,dv] (fp32 or bf16); g [B,H,dk] fp32; beta [B,H] fp32.
-    Returns out [B,H,dv] fp32."""
+    q, k [B,H,dk], v [B,H,dv] (fp32 or bf16); g [B,H,dk] fp32; beta [B,H] fp32;
+    ``prologue``: KDA_PROLOGUE_* bits.  Returns out [B,H,dv] fp32."""
     B, H, dk = q.shape
     dv = v.shape[2]
     if out is None:
         out = torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
         _keep_until_done(out, stream)
-    st = load().kda_decode(B, H, dk, dv, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+    st = load().kda_decode(B, H, dk, dv, _dtype_code(q), int(prologue), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                            _ptr(state), _ptr(out), _stream_handle(stream))
     if check and st != KDA_OK:
         raise KDAError(st, "kda_decode")
     return out
 
 
-def decode_multi(q, k, v, g, beta, state, out=None, n_apply=None, *, want_out=True, stream=None, check=True):
+def decode_multi(q, k, v, g, beta, state, out=None, n_apply=None, *, want_out=True, stream=None, check=True,
+                 prologue: int = 0):
     """K tokens per sequence through ``kda_decode_multi``: q, k [B,K,H,dk], v [B,K,H,dv]
     (fp32 or bf16); g [B,K,H,dk] fp32; beta [B,K,H] fp32; ``state`` [B,H,dk,dv] fp32 is
     replaced by the state after the first ``n_apply[b]`` tokens (int32 [B] on the device;
-    None = all K).  Returns out [B,K,H,dv] fp32 (None when ``want_out`` is False)."""
+    None = all K); ``prologue``: KDA_PROLOGUE_* bits.  Returns out [B,K,H,dv] fp32 (None
+    when ``want_out`` is False)."""
     B, K, H, dk = q.shape
     dv = v.shape[3]
     if out is None and want_out:
         out = torch.empty((B, K, H, dv), dtype=torch.float32, device=q.device)
         _keep_until_done(out, stream)
-    st = load().kda_decode_multi(B, K, H, dk, dv, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+    st = load().kda_decode_multi(B, K, H, dk, dv, _dtype_code(q), int(prologue), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                 _ptr(beta),
                                  _ptr(n_apply), _ptr(state), _ptr(out), _stream_handle(stream))
     if check and st != KDA_OK:
         raise KDAError(st, "kda_decode_multi")

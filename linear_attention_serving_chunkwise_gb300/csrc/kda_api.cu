@@ -99,6 +99,7 @@ kda_status validate_prefill(const kda_prefill_desc* d)
     if (d->qkv_dtype != KDA_F32 && d->qkv_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
     if (!supported_dims(d->dk, d->dv)) return KDA_ERR_UNSUPPORTED;
     if (d->num_seqs == 0 && d->total_tokens != 0) return KDA_ERR_INVALID_ARG;
+    if (d->prologue & ~KDA_PROLOGUE_ALL) return KDA_ERR_INVALID_ARG;
     return KDA_OK;
 }
 
@@ -218,6 +219,7 @@ kda_status prefill_impl(const kda_prefill_desc* desc, const void* q, const void*
     a.ckpt_slots = checkpoints ? ckpt_slots : 0;
     a.checkpoints = checkpoints;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.status = status;
+    a.prologue = d.prologue;
     const cudaStream_t sm = static_cast<cudaStream_t>(stream);
     const cudaError_t e = split                  ? kda::launch_prefill_split(a, sm)
                           : uses_tensor_cores(d) ? kda::launch_prefill_tc(a, sm)
@@ -263,10 +265,10 @@ kda_status kda_prefill_checkpointed(const kda_prefill_desc* desc, const void* q,
 }
 
 kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, int32_t qkv_dtype,
-                      const void* q, const void* k, const void* v, const float* g, const float* beta,
-                      float* state, float* out, void* stream)
+                      int32_t prologue, const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, float* state, float* out, void* stream)
 {
-    if (batch < 0 || num_heads < 1) return KDA_ERR_INVALID_ARG;
+    if (batch < 0 || num_heads < 1 || (prologue & ~KDA_PROLOGUE_ALL)) return KDA_ERR_INVALID_ARG;
     if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
     if (!supported_dims(dk, dv)) return KDA_ERR_UNSUPPORTED;
     const size_t BH = (size_t)batch * num_heads;
@@ -289,15 +291,18 @@ kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, 
     kda::DecodeArgs a;
     a.batch = batch; a.num_heads = num_heads; a.dk = dk; a.dv = dv; a.bf16 = qkv_dtype == KDA_BF16;
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state = state; a.out = out;
+    a.prologue = prologue;
     const cudaError_t e = kda::launch_decode(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 kda_status kda_decode_multi(int32_t batch, int32_t tokens, int32_t num_heads, int32_t dk, int32_t dv,
-                            int32_t qkv_dtype, const void* q, const void* k, const void* v, const float* g,
-                            const float* beta, const int32_t* n_apply, float* state, float* out, void* stream)
+                            int32_t qkv_dtype, int32_t prologue, const void* q, const void* k, const void* v,
+                            const float* g, const float* beta, const int32_t* n_apply, float* state, float* out,
+                            void* stream)
 {
     if (batch < 0 || num_heads < 1 || tokens < 1 || tokens > KDA_DECODE_MULTI_MAX_TOKENS) return KDA_ERR_INVALID_ARG;
+    if (prologue & ~KDA_PROLOGUE_ALL) return KDA_ERR_INVALID_ARG;
     if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
     if (!supported_dims(dk, dv)) return KDA_ERR_UNSUPPORTED;
     const size_t BH = (size_t)batch * num_heads;
@@ -327,7 +332,7 @@ kda_status kda_decode_multi(int32_t batch, int32_t tokens, int32_t num_heads, in
     a.batch = batch; a.tokens = tokens; a.num_heads = num_heads; a.dk = dk; a.dv = dv;
     a.bf16 = qkv_dtype == KDA_BF16;
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.n_apply = n_apply;
-    a.state = state; a.out = out; a.status = status;
+    a.state = state; a.out = out; a.status = status; a.prologue = prologue;
     const cudaError_t e = kda::launch_decode_multi(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

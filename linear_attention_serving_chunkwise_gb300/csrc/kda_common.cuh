@@ -21,6 +21,23 @@ __device__ __forceinline__ void report_status(int* status, int code)
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// Input prologue (bits of KDA_PROLOGUE_* in include/kda.h): the workloads' recipe for q, k,
+// g and beta, applied as the kernels load them.  g_min = -5 is the pages' bound on the
+// log-decay (llm-atlas Q06).
+constexpr int kProQK = 1, kProG = 2, kProBeta = 4;
+constexpr float kGMin = -5.f;
+constexpr float kL2Eps = 1e-12f;
+__device__ __forceinline__ float sigmoid_f(float y) { return 1.f / (1.f + expf(-y)); }
+__device__ __forceinline__ float g_of(float g, int prologue) { return (prologue & kProG) ? kGMin * sigmoid_f(g) : g; }
+__device__ __forceinline__ float beta_of(float b, int prologue) { return (prologue & kProBeta) ? sigmoid_f(b) : b; }
+// x / max(||x||, eps) rounded to the storage type of q and k
+__device__ __forceinline__ float l2_scale(float x, float den, float) { return x / den; }
+__device__ __forceinline__ float l2_scale(float x, float den, __nv_bfloat16)
+{
+    return __bfloat162float(__float2bfloat16_rn(x / den));
+}
+__device__ __forceinline__ float l2_den(float sumsq) { return fmaxf(sqrtf(sumsq), kL2Eps); }
+
 // Read 4 consecutive elements starting at a 4-element-aligned index.
 __device__ __forceinline__ float4 load4(const float* p)
 {

@@ -15,9 +15,11 @@ namespace {
 
 constexpr int kDecodeThreads = 256;
 
-template <typename Tin, int D>
+// kPro: the input prologue is compiled in (its own instance; the common one is unchanged).
+template <typename Tin, int D, bool kPro>
 __global__ void __launch_bounds__(kDecodeThreads, 2) kda_decode_kernel(DecodeArgs a)
 {
+    const int pro = kPro ? a.prologue : 0;
     constexpr int C4 = D / 4;                  // float4 columns per state row
     constexpr int RG = kDecodeThreads / C4;    // row groups
     constexpr int RP = D / RG;                 // rows per thread
@@ -48,10 +50,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) kda_decode_kernel(DecodeArg
         sk[t] = to_f32(k[t]);
         sq[t] = to_f32(q[t]);
         sv[t] = to_f32(v[t]);
-        sdec[t] = expf(g[t]);
+        sdec[t] = expf(g_of(g[t], pro));
     }
-    if (t == 0) s_beta = a.beta[bh];
+    if (t == 0) s_beta = beta_of(a.beta[bh], pro);
     __syncthreads();
+    if (pro & kProQK) {   // warp 0 normalises k, warp 1 q
+        if (t < 64) {
+            float* x = t < 32 ? sk : sq;
+            const int lane = t & 31;
+            float ss = 0.f;
+            for (int c = lane; c < D; c += 32) ss += x[c] * x[c];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float den = l2_den(ss);
+            for (int c = lane; c < D; c += 32) x[c] = l2_scale(x[c], den, Tin{});
+        }
+        __syncthreads();
+    }
     if (t < 32) {
         float kq = 0.f;
         for (int c = t; c < D; c += 32) kq += sk[c] * sq[c];
@@ -105,7 +120,10 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream)
 {
     const long long blocks = (long long)a.batch * a.num_heads;
     if (blocks == 0) return cudaSuccess;
-    kda_decode_kernel<Tin, D><<<(unsigned)blocks, kDecodeThreads, 0, stream>>>(a);
+    if (a.prologue)
+        kda_decode_kernel<Tin, D, true><<<(unsigned)blocks, kDecodeThreads, 0, stream>>>(a);
+    else
+        kda_decode_kernel<Tin, D, false><<<(unsigned)blocks, kDecodeThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -107,9 +107,30 @@ __device__ __forceinline__ void split4(float2 (&s)[2 * R], int i, float4 x)
     s[2 * i + 1] = make_float2(x.z, x.w);
 }
 
+// The prologue's q/k L2 normalisation on the staged tokens (tokb: K tokens in
+// MultiLayout<D>): warp w of the 2D / 32 takes vectors w, w + D / 16, ... of the 2K (k then
+// q of each token).
 template <typename Tin, int D>
+__device__ __forceinline__ void normalise_tokens(float* tokb, int K, int w, int lane)
+{
+    using Lay = MultiLayout<D>;
+    for (int vi = w; vi < 2 * K; vi += D / 16) {
+        float* x = tokb + (vi >> 1) * Lay::kTok + (vi & 1) * Lay::kVec;
+        float ss = 0.f;
+        for (int c = lane; c < D; c += 32) ss += x[Lay::row(c)] * x[Lay::row(c)];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float den = l2_den(ss);
+        for (int c = lane; c < D; c += 32) x[Lay::row(c)] = l2_scale(x[Lay::row(c)], den, Tin{});
+    }
+}
+
+// kPro (both kernels): the input prologue is compiled in (own instances; the common ones
+// are unchanged).
+template <typename Tin, int D, bool kPro>
 __global__ void __launch_bounds__(2 * D, 2) kda_decode_multi_kernel(DecodeMultiArgs a)
 {
+    const int pro = kPro ? a.prologue : 0;
     using Lay = MultiLayout<D>;
     constexpr int R = D / 8;                  // state rows per lane
     constexpr int kThreads = 2 * D;           // D / 16 warps of 16 columns
@@ -144,11 +165,15 @@ __global__ void __launch_bounds__(2 * D, 2) kda_decode_multi_kernel(DecodeMultiA
         float* base = smv + j * Lay::kTok;
         base[Lay::row(c)] = to_f32(static_cast<const Tin*>(a.k)[tok * D + c]);
         base[Lay::kVec + Lay::row(c)] = to_f32(static_cast<const Tin*>(a.q)[tok * D + c]);
-        base[2 * Lay::kVec + Lay::row(c)] = expf(a.g[tok * D + c]);
+        base[2 * Lay::kVec + Lay::row(c)] = expf(g_of(a.g[tok * D + c], pro));
         base[3 * Lay::kVec + c] = to_f32(static_cast<const Tin*>(a.v)[tok * D + c]);
-        if (c == 0) base[3 * Lay::kVec + D] = a.beta[tok];
+        if (c == 0) base[3 * Lay::kVec + D] = beta_of(a.beta[tok], pro);
     }
     __syncthreads();
+    if (pro & kProQK) {
+        normalise_tokens<Tin, D>(smv, K, t >> 5, lane);
+        __syncthreads();
+    }
 
     for (int j = 0; j < K; ++j) {
         const float* base = smv + j * Lay::kTok;
@@ -203,9 +228,10 @@ struct PersistLayout {
     static constexpr size_t smem(int K) { return kStateBytes + (size_t)K * MultiLayout<D>::kTok * 4 + (size_t)K * kRawTok; }
 };
 
-template <typename Tin, int D>
+template <typename Tin, int D, bool kPro>
 __global__ void __launch_bounds__(2 * D, 2) kda_decode_multi_persistent_kernel(DecodeMultiArgs a, int units)
 {
+    const int pro = kPro ? a.prologue : 0;
     using Lay = MultiLayout<D>;
     using PL = PersistLayout<Tin, D>;
     constexpr int R = D / 8;
@@ -273,11 +299,16 @@ __global__ void __launch_bounds__(2 * D, 2) kda_decode_multi_persistent_kernel(D
             float* base = tokb + j * Lay::kTok;
             base[Lay::row(c)] = to_f32(rv[c]);
             base[Lay::kVec + Lay::row(c)] = to_f32(rv[D + c]);
-            base[2 * Lay::kVec + Lay::row(c)] = expf(reinterpret_cast<const float*>(rt + 3 * D * sizeof(Tin))[c]);
+            base[2 * Lay::kVec + Lay::row(c)] =
+                expf(g_of(reinterpret_cast<const float*>(rt + 3 * D * sizeof(Tin))[c], pro));
             base[3 * Lay::kVec + c] = to_f32(rv[2 * D + c]);
-            if (c == 0) base[3 * Lay::kVec + D] = *reinterpret_cast<const float*>(rt + 16 * PL::kTokChunks);
+            if (c == 0) base[3 * Lay::kVec + D] = beta_of(*reinterpret_cast<const float*>(rt + 16 * PL::kTokChunks), pro);
         }
         __syncthreads();
+        if (pro & kProQK) {
+            normalise_tokens<Tin, D>(tokb, K, t >> 5, lane);
+            __syncthreads();
+        }
         if ((long long)u + gridDim.x < units) prefetch(u + gridDim.x);
 
         float* S = a.state + (size_t)u * D * D + col;
@@ -301,38 +332,39 @@ __global__ void __launch_bounds__(2 * D, 2) kda_decode_multi_persistent_kernel(D
     }
 }
 
-template <typename Tin, int D>
+template <typename Tin, int D, bool kPro>
 cudaError_t launch_t(const DecodeMultiArgs& a, cudaStream_t stream)
 {
     const long long blocks = (long long)a.batch * a.num_heads;
     if (blocks == 0) return cudaSuccess;
     const size_t smem = (size_t)a.tokens * MultiLayout<D>::kTok * sizeof(float);
     if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(kda_decode_multi_kernel<Tin, D>,
+        const cudaError_t e = cudaFuncSetAttribute(kda_decode_multi_kernel<Tin, D, kPro>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    kda_decode_multi_kernel<Tin, D><<<(unsigned)blocks, 2 * D, smem, stream>>>(a);
+    kda_decode_multi_kernel<Tin, D, kPro><<<(unsigned)blocks, 2 * D, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
 // resident CTAs per SM of one persistent variant at K tokens, and the device's SM count:
 // found once per device (cached as value + 1, 0 = not yet known)
 constexpr int kMaxDevices = 64;
+constexpr int kVariants = 8;   // (dtype, dk, prologue)
 std::atomic<int> g_sm_count[kMaxDevices];
-std::atomic<int> g_resident[kMaxDevices][4][kPersistMaxTokens + 1];
+std::atomic<int> g_resident[kMaxDevices][kVariants][kPersistMaxTokens + 1];
 
-template <typename Tin, int D>
+template <typename Tin, int D, bool kPro>
 cudaError_t launch_persistent(const DecodeMultiArgs& a, int variant, cudaStream_t stream)
 {
     const long long units = (long long)a.batch * a.num_heads;
     if (units == 0) return cudaSuccess;
-    auto kern = kda_decode_multi_persistent_kernel<Tin, D>;
+    auto kern = kda_decode_multi_persistent_kernel<Tin, D, kPro>;
     const size_t smem = PersistLayout<Tin, D>::smem(a.tokens);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return launch_t<Tin, D>(a, stream);
+    if (dev < 0 || dev >= kMaxDevices) return launch_t<Tin, D, kPro>(a, stream);
     int sms = g_sm_count[dev].load(std::memory_order_relaxed) - 1;
     if (sms < 0) {
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -350,23 +382,33 @@ cudaError_t launch_persistent(const DecodeMultiArgs& a, int variant, cudaStream_
         if (e != cudaSuccess) return e;
         slot.store(per_sm + 1, std::memory_order_relaxed);
     }
-    if (per_sm < 1) return launch_t<Tin, D>(a, stream);
+    if (per_sm < 1) return launch_t<Tin, D, kPro>(a, stream);
     const long long grid = std::min(units, (long long)sms * per_sm);
     kern<<<(unsigned)grid, 2 * D, smem, stream>>>(a, (int)units);
     return cudaGetLastError();
+}
+
+template <bool kPro>
+cudaError_t launch_multi(const DecodeMultiArgs& a, cudaStream_t stream)
+{
+    constexpr int v0 = kPro ? 4 : 0;
+    if (a.tokens <= kPersistMaxTokens) {
+        if (a.dk == 128)
+            return a.bf16 ? launch_persistent<__nv_bfloat16, 128, kPro>(a, v0, stream)
+                          : launch_persistent<float, 128, kPro>(a, v0 + 1, stream);
+        return a.bf16 ? launch_persistent<__nv_bfloat16, 64, kPro>(a, v0 + 2, stream)
+                      : launch_persistent<float, 64, kPro>(a, v0 + 3, stream);
+    }
+    if (a.dk == 128)
+        return a.bf16 ? launch_t<__nv_bfloat16, 128, kPro>(a, stream) : launch_t<float, 128, kPro>(a, stream);
+    return a.bf16 ? launch_t<__nv_bfloat16, 64, kPro>(a, stream) : launch_t<float, 64, kPro>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_multi(const DecodeMultiArgs& a, cudaStream_t stream)
 {
-    if (a.tokens <= kPersistMaxTokens) {
-        if (a.dk == 128)
-            return a.bf16 ? launch_persistent<__nv_bfloat16, 128>(a, 0, stream) : launch_persistent<float, 128>(a, 1, stream);
-        return a.bf16 ? launch_persistent<__nv_bfloat16, 64>(a, 2, stream) : launch_persistent<float, 64>(a, 3, stream);
-    }
-    if (a.dk == 128) return a.bf16 ? launch_t<__nv_bfloat16, 128>(a, stream) : launch_t<float, 128>(a, stream);
-    return a.bf16 ? launch_t<__nv_bfloat16, 64>(a, stream) : launch_t<float, 64>(a, stream);
+    return a.prologue ? launch_multi<true>(a, stream) : launch_multi<false>(a, stream);
 }
 
 }  // namespace kda

@@ -22,6 +22,7 @@ struct PrefillArgs {
     void* workspace;
     size_t workspace_bytes;
     int* status;  // device status word
+    int prologue; // KDA_PROLOGUE_* bits
 };
 
 struct DecodeArgs {
@@ -30,6 +31,7 @@ struct DecodeArgs {
     const void *q, *k, *v;
     const float *g, *beta;
     float *state, *out;
+    int prologue; // KDA_PROLOGUE_* bits
 };
 
 struct DecodeMultiArgs {
@@ -40,6 +42,7 @@ struct DecodeMultiArgs {
     const int32_t* n_apply;      // [B] tokens whose update is kept, or nullptr (= K)
     float *state, *out;          // [B, H, dk, dv] in place; [B, K, H, dv] or nullptr
     int* status;                 // device status word
+    int prologue;                // KDA_PROLOGUE_* bits
 };
 
 // fp32 CUDA-core chunkwise prefill (any supported shape, fp32 or bf16 inputs)

@@ -69,14 +69,26 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
             const size_t gi = ((size_t)(c0 + r) * H + h) * D + c;
             sQ[idx] = to_f32(q[gi]);
             sK[idx] = to_f32(k[gi]);
-            sG[idx] = a.g[gi];
+            sG[idx] = g_of(a.g[gi], a.prologue);
         }
         for (int idx = t; idx < BT * kSlice; idx += kThreads) {
             const int r = idx / kSlice, j = idx % kSlice;
             sV[idx] = to_f32(v[((size_t)(c0 + r) * H + h) * D + js + j]);
         }
-        if (t < BT) sB[t] = a.beta[(size_t)(c0 + t) * H + h];
+        if (t < BT) sB[t] = beta_of(a.beta[(size_t)(c0 + t) * H + h], a.prologue);
         __syncthreads();
+        if (a.prologue & kProQK) {   // one warp per token row of q or k
+            for (int vi = warp; vi < 2 * BT; vi += kWarps) {
+                float* x = (vi & 1 ? sQ : sK) + (vi >> 1) * D;
+                float ss = 0.f;
+                for (int c = lane; c < D; c += 32) ss += x[c] * x[c];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float den = l2_den(ss);
+                for (int c = lane; c < D; c += 32) x[c] = l2_scale(x[c], den, Tin{});
+            }
+            __syncthreads();
+        }
 
         // Gamma: inclusive prefix sum of g down the chunk, per key channel
         if (t < D) {

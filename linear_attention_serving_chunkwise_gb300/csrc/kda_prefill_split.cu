@@ -306,10 +306,13 @@ __device__ __forceinline__ Item item_at(const SplitParams& sp, int item)
 // phase 1 up to the off-diagonal rows runs while the current item's last MMA does.  16 warps; warp w reaches TMEM lanes [32 (w % 4), +32) and works on column part w / 4, as in
 // the one-CTA-per-head kernel.  `tm`: 512 allocated TMEM columns.  On return the CTA's
 // barriers are invalidated and its copies complete, so shared memory can be reused.
-template <bool kDyn>
+// kPro: the input prologue is compiled in (instances of their own, so that the common ones
+// keep their registers and schedule).
+template <bool kDyn, bool kPro>
 __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, uint32_t tm, int limit)
 {
     const TcParams& p = sp.p;
+    const int pro = kPro ? p.prologue : 0;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int quarter = warp & 3, part = warp >> 2;
     const int L = 32 * quarter + lane;
@@ -395,7 +398,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if (*s_abort) return false;
         qg_par ^= 1u;
         if (t == kStorer) qg_pending = false;
-        phase1_cumsum<true>(sm, vec, t, BTn);
+        phase1_cumsum<true>(sm, vec, t, BTn, pro);
         __syncthreads();
         if (t < 128) phase1_factors(vec, t);
         if (!mbar_wait_bounded(bar_k, k_par, kWaitNs)) atomicExch(s_abort, 1);
@@ -403,6 +406,10 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if (*s_abort) return false;
         k_par ^= 1u;
         if (t == kStorer) k_pending = false;
+        if (pro & kProQK) {
+            phase0_normalise_qk(sm, t);
+            __syncthreads();
+        }
         phase1_tokens<true>(sm, vec, tm, L, part, quarter, BTn, kg_buf(b));
         return true;
     };
@@ -415,7 +422,10 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         uint8_t* img = sp.ops + ((size_t)cur.gc * H + h) * IMG_BYTES;
         const bool has_next = nidx >= 0;
         const uint32_t kg = kg_buf(li & 1);
-        if (t < 64) cp_async_wait_all();   // this item's beta; thread 0: the next item's entry
+        if (t < 64) {
+            cp_async_wait_all();   // this item's beta; thread 0: the next item's entry
+            if ((pro & kProBeta) && t < BT) sbeta_buf(li & 1)[t] = sigmoid_f(sbeta_buf(li & 1)[t]);
+        }
         if constexpr (kDyn) {
             if (t == 0) {
                 // the item after next: the claim issued an item ago (its latency hidden by that
@@ -655,6 +665,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
     __syncthreads();
 }
 
+template <bool kPro>
 __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __grid_constant__ SplitParams sp)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -668,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tm = *tslot;
-    prep_items<false>(sp, sm, tm, 0x7fffffff);
+    prep_items<false, kPro>(sp, sm, tm, 0x7fffffff);
     tc_fence_before_sync();
     __syncthreads();
     if ((threadIdx.x >> 5) == 0) tmem_dealloc(tm, TM_COLS);
@@ -1013,6 +1024,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
 // keep claiming until the items run out.  A CTA waits only on items that other CTAs have
 // already claimed or will claim, and the CTAs that never scan finish every item left, so
 // every wait ends.
+template <bool kPro>
 __global__ void __launch_bounds__(kThreads, 1) kda_prep_scan_kernel(const __grid_constant__ SplitParams sp, int units,
                                                                     int switch_item)
 {
@@ -1028,7 +1040,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_scan_kernel(const __grid
     tc_fence_after_sync();
     const uint32_t tm = *tslot;
     const bool scans = (int)blockIdx.x < units;
-    prep_items<true>(sp, sm, tm, scans ? switch_item : 0x7fffffff);
+    prep_items<true, kPro>(sp, sm, tm, scans ? switch_item : 0x7fffffff);
     if (scans) scan_unit<true>(sp, sm, tm, blockIdx.x);
     tc_fence_before_sync();
     __syncthreads();
@@ -1077,18 +1089,24 @@ cudaError_t split_device(SplitDevice* out)
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::call_once(once[dev], [dev] {
         SplitDevice d;
-        int coop = 0, per_sm = 0;
+        int coop = 0, per_sm = 0, per_sm_pro = 0;
         bool ok = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
                   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess &&
-                  cudaFuncSetAttribute(kda_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                  cudaFuncSetAttribute(kda_chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)A_SMEM_BYTES) == cudaSuccess &&
+                  cudaFuncSetAttribute(kda_chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)A_SMEM_BYTES) == cudaSuccess &&
                   cudaFuncSetAttribute(kda_state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)B_SMEM_BYTES) == cudaSuccess &&
-                  cudaFuncSetAttribute(kda_prep_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                  cudaFuncSetAttribute(kda_prep_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)B_SMEM_BYTES) == cudaSuccess &&
-                  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_prep_scan_kernel, kThreads,
+                  cudaFuncSetAttribute(kda_prep_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)B_SMEM_BYTES) == cudaSuccess &&
+                  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_prep_scan_kernel<false>, kThreads,
+                                                                B_SMEM_BYTES) == cudaSuccess &&
+                  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_pro, kda_prep_scan_kernel<true>, kThreads,
                                                                 B_SMEM_BYTES) == cudaSuccess;
-        d.single = ok && coop && per_sm >= 1;
+        d.single = ok && coop && per_sm >= 1 && per_sm_pro >= 1;
         if (!ok) d.sms = 0;
         cache[dev] = d;
     });
@@ -1119,6 +1137,7 @@ cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream)
     p.total_tokens = a.total_tokens;
     p.num_heads = a.num_heads;
     p.status = a.status;
+    p.prologue = a.prologue;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     const SplitWorkspace wl = split_workspace(a.num_seqs, a.total_tokens, a.num_heads);
     sp.chunk_off = reinterpret_cast<int32_t*>(ws);
@@ -1143,15 +1162,18 @@ cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream)
         const long long rest = (dv.sms - units) * chunks * kScanCyclesPerChunk / kPrepCyclesPerItem;
         int units_i = (int)units, switch_item = (int)std::max(0LL, items - rest);
         void* args[] = {&sp, &units_i, &switch_item};
-        e = cudaLaunchCooperativeKernel((const void*)kda_prep_scan_kernel, dim3((unsigned)dv.sms), dim3(kThreads),
-                                        args, B_SMEM_BYTES, stream);
+        const void* kern = a.prologue ? (const void*)kda_prep_scan_kernel<true> : (const void*)kda_prep_scan_kernel<false>;
+        e = cudaLaunchCooperativeKernel(kern, dim3((unsigned)dv.sms), dim3(kThreads), args, B_SMEM_BYTES, stream);
         if (e == cudaSuccess) return cudaGetLastError();
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         (void)cudaGetLastError();   // not all CTAs can be resident here: the separate launches below
     }
     const long long items_max = ((long long)a.total_tokens / 64 + a.num_seqs) * a.num_heads;
     const long long prep_grid = std::max(1LL, std::min<long long>(dv.sms, items_max));
-    kda_chunk_prep_kernel<<<(unsigned)prep_grid, kThreads, A_SMEM_BYTES, stream>>>(sp);
+    if (a.prologue)
+        kda_chunk_prep_kernel<true><<<(unsigned)prep_grid, kThreads, A_SMEM_BYTES, stream>>>(sp);
+    else
+        kda_chunk_prep_kernel<false><<<(unsigned)prep_grid, kThreads, A_SMEM_BYTES, stream>>>(sp);
     kda_state_scan_kernel<<<(unsigned)units, kThreads, B_SMEM_BYTES, stream>>>(sp);
     return cudaGetLastError();
 }

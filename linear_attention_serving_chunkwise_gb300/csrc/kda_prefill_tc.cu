@@ -47,8 +47,12 @@ using namespace sm100;
 
 // ---------------------------------------------------------------- the kernel
 // 16 warps: warp w reaches TMEM lanes [32 (w % 4), +32) and works on column part w / 4.
+// kPro: the input prologue is compiled in (a separate instance, so that the common one
+// keeps its registers).
+template <bool kPro>
 __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcParams p)
 {
+    const int pro = kPro ? p.prologue : 0;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base; offsetting the __shared__ array itself (rather than rounding an
     // integer address) keeps every access through `sm` in the shared state space
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tmem_wait_st();
     }
 
-    float beta_next = (t < 64 && bos + t < eos) ? __ldg(p.beta + (size_t)(bos + t) * H + h) : 0.f;
+    float beta_next = (t < 64 && bos + t < eos) ? beta_of(__ldg(p.beta + (size_t)(bos + t) * H + h), pro) : 0.f;
     uint32_t v_par = 0, k_par = 0, qg_par = 0, mma_par = 0;
     bool ok = true;
 
@@ -147,11 +151,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (t == 0) v_pending = k_pending = qg_pending = false;
         if (t < 64) {
             const int tn = t0 + 64 + t;
-            beta_next = (ci + 1 < nchunks && tn < eos) ? __ldg(p.beta + (size_t)tn * H + h) : 0.f;
+            beta_next = (ci + 1 < nchunks && tn < eos) ? beta_of(__ldg(p.beta + (size_t)tn * H + h), pro) : 0.f;
         }
 
+        if (pro & kProQK) {
+            phase0_normalise_qk(sm, t);
+            __syncthreads();
+        }
         // ---- phase 1: decayed operands
-        phase1_cumsum(sm, vec, t, BT);
+        phase1_cumsum(sm, vec, t, BT, pro);
         __syncthreads();
         if (t < 128) phase1_factors(vec, t);
         if (t == 0 && o_pending) {   // the previous chunk's O staging must be read out before reuse
@@ -455,11 +463,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream)
     p.total_tokens = a.total_tokens;
     p.num_heads = a.num_heads;
     p.status = a.status;
-    cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    p.prologue = a.prologue;
+    auto kern = a.prologue ? kda_prefill_tc_kernel<true> : kda_prefill_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const long long units = (long long)a.num_seqs * a.num_heads;
-    kda_prefill_tc_kernel<<<(unsigned)units, kThreads, SMEM_BYTES, stream>>>(p);
+    kern<<<(unsigned)units, kThreads, SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -93,6 +93,7 @@ struct TcParams {
     int ckpt_interval, ckpt_slots;
     int num_seqs, total_tokens, num_heads;
     int* status;
+    int prologue;   // KDA_PROLOGUE_* bits
 };
 
 __device__ __forceinline__ float ex2f(float x)
@@ -235,8 +236,9 @@ __device__ __forceinline__ void issue_qg_loads(const TcParams& p, uint8_t* sm, u
 // end count as 0), replaces g_r in the tile by x_r = 2^{lambda_r} = e^{Gamma_r - rho_J}
 // (in (0, 1], a normal float since g >= -5) and stores D_J = 2^{s_J}, the last x of the
 // sub-tile (s_J: the sub-tile's sum).
+// With the prologue's kProG bit the tile holds logits z and g = -5 sigmoid(z) is used.
 template <bool kHoist = false>
-__device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, int BT)
+__device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, int BT, int prologue = 0)
 {
     const int c = t & 127, J = t >> 7;
     float acc = 0.f, x = 1.f;
@@ -245,7 +247,7 @@ __device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, in
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
             const int r = 16 * J + rr;
-            gv[rr] = (r < BT) ? *reinterpret_cast<const float*>(sm + OFF_G + g_off(r, c)) : 0.f;
+            gv[rr] = (r < BT) ? g_of(*reinterpret_cast<const float*>(sm + OFF_G + g_off(r, c)), prologue) : 0.f;
         }
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
@@ -258,13 +260,44 @@ __device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, in
         for (int rr = 0; rr < 16; ++rr) {
             const int r = 16 * J + rr;
             float* gp = reinterpret_cast<float*>(sm + OFF_G + g_off(r, c));
-            const float gv = (r < BT) ? *gp : 0.f;
+            const float gv = (r < BT) ? g_of(*gp, prologue) : 0.f;
             acc = fmaf(gv, kLog2e, acc);
             x = ex2f(acc);
             *gp = x;
         }
     }
     vec[(V_D + J) * 128 + c] = x;
+}
+
+// The prologue's L2 normalisation of the q and k tiles in place (512 threads): thread t
+// takes row t / 4 of [k; q] (token r = that row mod 64) and channels [32 (t % 4), +32), the
+// row's sum of squares closing over the 4 neighbouring lanes; x / max(||x||, 1e-12) in fp32
+// goes back as bf16.
+__device__ __forceinline__ void phase0_normalise_qk(uint8_t* sm, int t)
+{
+    const int row = t >> 2, qtr = t & 3, r = row & 63;
+    const uint32_t tile = smem_u32(sm) + (row < 64 ? OFF_K : OFF_Q);
+    float x[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float v8[8];
+        unpack8(ld_shared_v4(tile + sw128_chunk(r, 4 * qtr + i, 64)), v8);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[8 * i + e] = v8[e];
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) ss = fmaf(x[e], x[e], ss);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    const float den = l2_den(ss);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(x[8 * i + 2 * e] / den, x[8 * i + 2 * e + 1] / den);
+        st_shared_v4(tile + sw128_chunk(r, 4 * qtr + i, 64), w[0], w[1], w[2], w[3]);
+    }
 }
 
 // Per-channel factors (thread c < 128, after phase1_cumsum), all products of the four

@@ -12,4 +12,10 @@ from .kda_ref import (  # noqa: F401
     chunkwise_naive,
     delta_invariant_keys,
     rel_err,
+    prologue,
+    sigmoid64,
+    l2_normalise64,
+    PROLOGUE_QK_L2NORM,
+    PROLOGUE_G_LOGITS,
+    PROLOGUE_BETA_LOGITS,
 )

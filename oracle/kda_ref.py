@@ -216,6 +216,54 @@ def chunkwise_naive(q, k, v, g, beta, S0=None, chunk: int = 64):
     return out, S
 
 
+# Input prologue bits, as in the C ABI's KDA_PROLOGUE_* (restated here: the oracle shares
+# no header with the library).
+PROLOGUE_QK_L2NORM = 1
+PROLOGUE_G_LOGITS = 2
+PROLOGUE_BETA_LOGITS = 4
+G_MIN = -5.0          # the bound on the log-decay (llm-atlas Q06 and Figure 3)
+L2_EPS = 1e-12
+
+
+def sigmoid64(y) -> np.ndarray:
+    """1 / (1 + e^-y) in fp64, without overflow for large |y|."""
+    y = np.asarray(y, dtype=np.float64)
+    e = np.exp(-np.abs(y))
+    return np.where(y >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def l2_normalise64(x) -> np.ndarray:
+    """x / max(||x||_2, 1e-12) over the last axis, in fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    n = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+    return x / np.maximum(n, L2_EPS)
+
+
+def prologue(inputs: dict, flags: int) -> dict:
+    """The workloads' input recipe applied to raw inputs, as the library's prologue bits ask:
+    q and k L2-normalised per (token, head) over dk in fp64 and rounded to their storage
+    type (bf16 stays bf16, fp32 stays fp32); g = g_min * sigmoid(z); beta = sigmoid(y), both
+    in fp64 and then stored as fp32 like every g and beta.  Returns a new dict of CPU torch
+    tensors in the storage types.  The recipe is the benchmark workloads' (q, k ~ N(0,1)
+    then L2-normalised per (token, head), beta = sigmoid(N(0,1)), g = -5 sigmoid(N(0,1)));
+    -5 is the pages' bound on the log-decay.  Test infrastructure: the oracle side of the
+    prologue parity tests."""
+    import torch
+    out = dict(inputs)
+    if flags & PROLOGUE_QK_L2NORM:
+        for name in ("q", "k"):
+            t = inputs[name].detach().to("cpu")
+            n64 = l2_normalise64(t.to(torch.float64).numpy())
+            out[name] = torch.from_numpy(n64).to(t.dtype)
+    if flags & PROLOGUE_G_LOGITS:
+        z = inputs["g"].detach().to("cpu", torch.float64).numpy()
+        out["g"] = torch.from_numpy(G_MIN * sigmoid64(z)).to(torch.float32)
+    if flags & PROLOGUE_BETA_LOGITS:
+        y = inputs["beta"].detach().to("cpu", torch.float64).numpy()
+        out["beta"] = torch.from_numpy(sigmoid64(y)).to(torch.float32)
+    return out
+
+
 def delta_invariant_keys(dk: int, n: int, seed: int = 0) -> np.ndarray:
     """n <= dk orthonormal keys (rows), from a QR factorisation of a seeded Gaussian matrix."""
     rng = np.random.default_rng(seed)

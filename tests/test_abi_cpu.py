@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.kda_abi_version() == 1
+    assert lib.kda_abi_version() == kda.KDA_ABI_VERSION == 2
     for code in (0, -1, -2, -3, -4, -5):
         assert kda.status_string(code).startswith("KDA")
     assert "unknown" in kda.status_string(-99)
@@ -78,6 +78,16 @@ def test_prefill_rejects_bad_arguments_on_host(lib):
     assert _prefill(lib, d, fin=0x60000 + 64) == kda.KDA_ERR_INVALID_ARG
     # nothing to do: zero sequences
     assert _prefill(lib, kda.make_desc(0, 0, 2, 64, 64, 0)) == kda.KDA_OK
+    # the input prologue: any of its three bits, nothing else
+    assert _prefill(lib, kda.make_desc(0, 0, 2, 64, 64, 0, kda.KDA_PROLOGUE_ALL)) == kda.KDA_OK
+    assert _prefill(lib, kda.make_desc(1, 64, 2, 64, 64, 0, 8)) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill(lib, kda.make_desc(1, 64, 2, 64, 64, 0, -1)) == kda.KDA_ERR_INVALID_ARG
+    with pytest.raises(kda.KDAError):
+        kda.prefill_query(kda.make_desc(1, 64, 2, 64, 64, 0, 16))
+    # the prologue does not change the plan
+    for dt, d in ((kda.KDA_BF16, 128), (kda.KDA_F32, 64)):
+        assert kda.prefill_query(kda.make_desc(1, 8192, 96, d, d, dt)) == \
+            kda.prefill_query(kda.make_desc(1, 8192, 96, d, d, dt, kda.KDA_PROLOGUE_ALL))
 
 
 def test_workspace_query(lib):
@@ -138,13 +148,15 @@ def test_decode_rejects_bad_arguments_on_host(lib):
     args = lambda **kw: [kw.get(n, f(a)) for n, a in
                          (("q", 0x10000), ("k", 0x20000), ("v", 0x30000), ("g", 0x40000), ("beta", 0x50000),
                           ("state", 0x100000), ("out", 0x60000))]
-    assert lib.kda_decode(2, 2, 96, 96, 0, *args(), None) == kda.KDA_ERR_UNSUPPORTED
-    assert lib.kda_decode(2, 2, 64, 64, 5, *args(), None) == kda.KDA_ERR_UNSUPPORTED
-    assert lib.kda_decode(-1, 2, 64, 64, 0, *args(), None) == kda.KDA_ERR_INVALID_ARG
-    assert lib.kda_decode(2, 2, 64, 64, 0, *args(q=None), None) == kda.KDA_ERR_INVALID_ARG
-    assert lib.kda_decode(2, 2, 64, 64, 0, *args(out=f(0x100000)), None) == kda.KDA_ERR_INVALID_ARG
-    assert lib.kda_decode(2, 2, 64, 64, 0, *args(g=f(0x40004)), None) == kda.KDA_ERR_INVALID_ARG
-    assert lib.kda_decode(0, 2, 64, 64, 0, *args(), None) == kda.KDA_OK
+    assert lib.kda_decode(2, 2, 96, 96, 0, 0, *args(), None) == kda.KDA_ERR_UNSUPPORTED
+    assert lib.kda_decode(2, 2, 64, 64, 5, 0, *args(), None) == kda.KDA_ERR_UNSUPPORTED
+    assert lib.kda_decode(-1, 2, 64, 64, 0, 0, *args(), None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode(2, 2, 64, 64, 0, 0, *args(q=None), None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode(2, 2, 64, 64, 0, 0, *args(out=f(0x100000)), None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode(2, 2, 64, 64, 0, 0, *args(g=f(0x40004)), None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode(0, 2, 64, 64, 0, 0, *args(), None) == kda.KDA_OK
+    assert lib.kda_decode(2, 2, 64, 64, 0, 8, *args(), None) == kda.KDA_ERR_INVALID_ARG   # unknown prologue bit
+    assert lib.kda_decode(0, 2, 64, 64, 0, kda.KDA_PROLOGUE_ALL, *args(), None) == kda.KDA_OK
 
 
 def test_library_is_in_tree():
@@ -203,8 +215,9 @@ def test_decode_multi_rejects_bad_arguments_on_host(lib):
     f = _fake
     base = dict(q=f(0x10000), k=f(0x20000), v=f(0x30000), g=f(0x40000), beta=f(0x50000), n=None,
                 state=f(0x100000), out=f(0x60000))
-    call = lambda B=2, K=2, H=2, d=64, dt=0, **kw: lib.kda_decode_multi(
-        B, K, H, d, d, dt, *[kw.get(n, base[n]) for n in ("q", "k", "v", "g", "beta", "n", "state", "out")], None)
+    call = lambda B=2, K=2, H=2, d=64, dt=0, pro=0, **kw: lib.kda_decode_multi(
+        B, K, H, d, d, dt, pro, *[kw.get(n, base[n]) for n in ("q", "k", "v", "g", "beta", "n", "state", "out")],
+        None)
     assert call(K=0) == kda.KDA_ERR_INVALID_ARG
     assert call(K=kda.KDA_DECODE_MULTI_MAX_TOKENS + 1) == kda.KDA_ERR_INVALID_ARG
     assert call(d=96) == kda.KDA_ERR_UNSUPPORTED
@@ -214,3 +227,5 @@ def test_decode_multi_rejects_bad_arguments_on_host(lib):
     assert call(out=f(0x100000)) == kda.KDA_ERR_INVALID_ARG       # out over the state
     assert call(state=f(0x10000 + 64)) == kda.KDA_ERR_INVALID_ARG  # state over q
     assert call(B=0) == kda.KDA_OK
+    assert call(pro=-1) == kda.KDA_ERR_INVALID_ARG                 # unknown prologue bits
+    assert call(B=0, pro=kda.KDA_PROLOGUE_ALL) == kda.KDA_OK

@@ -265,3 +265,69 @@ def test_each_planted_oracle_mistake_fails_a_pin(mutant, tmp_path):
             else:
                 oracle.kda_ref._LIBS[mutant] = saved
     assert max(errs.values()) > 1e-3, errs
+
+
+# ---------------------------------------------------------------- the input prologue
+def test_prologue_closed_forms():
+    """The oracle's input prologue against values its definition fixes: a 3-4-5 row becomes
+    (0.6, 0.8), exactly in fp32 and as the nearest bf16 values (0.6015625, 0.80078125) in
+    bf16; a zero row stays zero (the 1e-12 floor); sigmoid(0) = 1/2 and sigmoid(ln 3) = 3/4
+    give g = -2.5, -3.75 and beta = 0.5, 0.75; logits of +-1e4 give the limits without NaN."""
+    import torch
+    raw = torch.zeros(2, 1, 8)
+    raw[0, 0, 0], raw[0, 0, 1] = 3.0, 4.0
+    z = torch.tensor([[0.0], [float(np.log(3.0))]]).repeat(1, 4).reshape(2, 1, 4)
+    y = torch.tensor([[0.0], [float(np.log(3.0))]])
+    d = {"q": raw.clone(), "k": raw.clone(), "g": z, "beta": y}
+    p = oracle.prologue(d, oracle.PROLOGUE_QK_L2NORM | oracle.PROLOGUE_G_LOGITS | oracle.PROLOGUE_BETA_LOGITS)
+    for name in ("q", "k"):
+        assert p[name].dtype == torch.float32
+        assert p[name][0, 0, 0].item() == np.float32(0.6) and p[name][0, 0, 1].item() == np.float32(0.8)
+        assert torch.count_nonzero(p[name][0, 0, 2:]) == 0 and torch.count_nonzero(p[name][1]) == 0
+    assert np.allclose(p["g"][:, 0, 0].numpy(), [-2.5, -3.75], rtol=0, atol=1e-6)
+    assert np.allclose(p["beta"][:, 0].numpy(), [0.5, 0.75], rtol=0, atol=1e-7)
+    pb = oracle.prologue({"q": raw.to(torch.bfloat16), "k": raw.to(torch.bfloat16)}, oracle.PROLOGUE_QK_L2NORM)
+    assert pb["q"].dtype == torch.bfloat16
+    assert pb["q"][0, 0, 0].item() == 0.6015625 and pb["q"][0, 0, 1].item() == 0.80078125
+    lim = oracle.prologue({"g": torch.tensor([[[1e4, -1e4]]]), "beta": torch.tensor([[1e4], [-1e4]])},
+                          oracle.PROLOGUE_G_LOGITS | oracle.PROLOGUE_BETA_LOGITS)
+    assert lim["g"].flatten().tolist() == [-5.0, -0.0] and lim["beta"].flatten().tolist() == [1.0, 0.0]
+    # only the asked-for bits act
+    only_g = oracle.prologue(d, oracle.PROLOGUE_G_LOGITS)
+    assert torch.equal(only_g["q"], d["q"]) and torch.equal(only_g["beta"], d["beta"])
+
+
+def test_prologue_scale_invariance_and_unit_norm():
+    """Normalisation ignores a positive scale of the row, and every non-zero row comes out
+    with norm 1 (to fp32 rounding)."""
+    import torch
+    rng = np.random.default_rng(31)
+    x = torch.from_numpy(rng.standard_normal((40, 3, 64)).astype(np.float32))
+    a = oracle.prologue({"q": x, "k": x}, oracle.PROLOGUE_QK_L2NORM)["q"]
+    b = oracle.prologue({"q": 8.0 * x, "k": x}, oracle.PROLOGUE_QK_L2NORM)["q"]
+    assert torch.equal(a, b)   # scaling by a power of two is exact
+    c = oracle.prologue({"q": 3.7 * x, "k": x}, oracle.PROLOGUE_QK_L2NORM)["q"]
+    assert float((a - c).abs().max()) < 1e-6
+    n = torch.linalg.vector_norm(a.double(), dim=-1)
+    assert float((n - 1).abs().max()) < 1e-6
+
+
+def test_prologue_keeps_the_delta_invariant():
+    """Raw keys = orthonormal keys times arbitrary positive scales, g logits of -1e4 (g = 0)
+    and beta logits of +1e4 (beta = 1): after the prologue the keys are orthonormal again,
+    so the recurrence returns each written value (the invariant of the delta rule)."""
+    import torch
+    dk = dv = 16
+    K = oracle.delta_invariant_keys(dk, dk, seed=5)
+    rng = np.random.default_rng(6)
+    scales = rng.uniform(0.1, 20.0, size=(dk, 1))
+    raw = torch.from_numpy((K * scales)[:, None, :].astype(np.float32))
+    V = rng.standard_normal((dk, dv)).astype(np.float32)
+    d = {"q": raw, "k": raw, "g": torch.full((dk, 1, dk), -1e4), "beta": torch.full((dk, 1), 1e4)}
+    p = oracle.prologue(d, oracle.PROLOGUE_QK_L2NORM | oracle.PROLOGUE_G_LOGITS | oracle.PROLOGUE_BETA_LOGITS)
+    assert torch.count_nonzero(p["g"]) == 0 and bool((p["beta"] == 1).all())
+    Kn = p["k"][:, 0].numpy()
+    _, S = _run1(Kn, Kn, V, p["g"][:, 0].numpy(), p["beta"][:, 0].numpy(), None)
+    Kd = Kn.astype(np.float64)
+    assert np.max(np.abs(Kd @ Kd.T - np.eye(dk))) < 1e-6
+    assert np.max(np.abs(S.T @ Kd.T - V.astype(np.float64).T)) < 1e-5
