@@ -394,6 +394,43 @@ def run_cuda(args, world, rank, local):
                     "gpu_launches": mcalls}
     del mm, mx, mstate, mout
 
+    # ---------------- the input prologue: the same prefill from the recipe's raw draws, with q/k
+    # normalisation and the g and beta parametrisations inside the kernels' loads (its own
+    # workspace: the headline one was released above).  A failure here is reported in the line.
+    prologue = {"workload": cfg.name + "_raw_inputs", "bits": "q/k L2 norm, g = -5 sigmoid(z), beta = sigmoid(y)"}
+    try:
+        draw = W.make_prefill_inputs(cfg, seed=rank, device=dev, raw=True)
+        pws = torch.empty(max(plan["workspace_bytes"], 16), dtype=torch.uint8, device=dev)
+        rargs = (draw["q"], draw["k"], draw["v"], draw["g"], draw["beta"], draw["cu_seqlens"], draw["init_state"])
+
+        def pro_call():
+            kda.prefill(*rargs, out=out, final_state=fin, workspace=pws, stream=stream,
+                        prologue=kda.KDA_PROLOGUE_ALL)
+
+        for _ in range(args.warmup):
+            pro_call()
+        stream.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _barrier(world)
+        p0.record(stream)
+        for _ in range(args.steps):
+            pro_call()
+        p1.record(stream)
+        stream.synchronize()
+        if kda.last_device_status(stream) != kda.KDA_OK:
+            raise RuntimeError("prefill with the prologue reported a device error")
+        pro_ms = _max_over_ranks(p0.elapsed_time(p1) / args.steps, world)
+        prologue.update({"ms_per_call": pro_ms, "tokens_per_s": tokens_per_step / (pro_ms / 1e3),
+                         "vs_plain_call": ms_per_step / pro_ms,
+                         "roofline": {"bound": "hbm", "achieved": alg_bytes / (pro_ms / 1e3) / 1e9,
+                                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                      "frac": alg_bytes / (pro_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                      "traffic": None, "algorithmic_bytes_per_launch": alg_bytes},
+                         "gpu_launches": args.steps * plan["kernel_launches"]})
+        del draw, rargs, pws
+    except Exception as exc:   # noqa: BLE001 -- recorded in the line instead of ending the run
+        prologue["error"] = f"{type(exc).__name__}: {exc}"
+
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if plan["tensor_cores"] else "f32", "data": "synthetic",
@@ -402,7 +439,8 @@ def run_cuda(args, world, rank, local):
                        "init_state": "N(0,0.02)", "l2": "inputs larger than L2 (1.41 GB per step), no flush",
                        "parallelism": f"independent problem per GPU x{world}"},
             "roofline": roofline, "tensor": tensor, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": args.steps * plan["kernel_launches"], "decode": decode, "decode_multi": decode_multi}
+            "gpu_launches": args.steps * plan["kernel_launches"], "decode": decode, "decode_multi": decode_multi,
+            "prologue": prologue}
     if rank == 0 and world == 1:
         rate, dt, cores, sdesc = oracle_sample(cfg, heads=96, tokens=8192)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sdesc,
