@@ -197,6 +197,12 @@ def test_prefill_host_rejects_bad_arguments_on_host(lib):
     fin = st[16:]
     assert _host_call(lib, d, 128, ws_bytes=need, init=init, fin=fin) == kda.KDA_ERR_INVALID_ARG
     assert _host_call(lib, kda.make_desc(0, 0, 2, 64, 64, kda.KDA_F32), 128) == kda.KDA_OK
+    # unknown prologue bits are rejected before any copy; the known ones pass the checks
+    assert _host_call(lib, kda.make_desc(2, 256, 2, 64, 64, kda.KDA_F32, 8), 128, ws_bytes=need) == \
+        kda.KDA_ERR_INVALID_ARG
+    assert kda.prefill_host_workspace_bytes(kda.make_desc(2, 256, 2, 64, 64, kda.KDA_F32, kda.KDA_PROLOGUE_ALL),
+                                            128) == need
+    assert _host_call(lib, kda.make_desc(0, 0, 2, 64, 64, kda.KDA_F32, kda.KDA_PROLOGUE_ALL), 128) == kda.KDA_OK
 
 
 def test_prefill_host_workspace_bytes():
