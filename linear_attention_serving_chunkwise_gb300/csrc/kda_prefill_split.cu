@@ -6,7 +6,9 @@
 // q, k, g and beta, so it is computed for all (sequence, head, chunk) items at once; the
 // state recurrence
 //   W = Tb V - Wk S,   O = Q' S + M V,   S <- Diag(gamma_C) S + K~^T W
-// then walks each (sequence, head)'s chunks in order.  Three launches per call:
+// then walks each (sequence, head)'s chunks in order.  Three launches per call, or two when
+// at least 32 SMs' CTAs are left over from the scans: then steps 2 and 3 share one
+// cooperative launch (kda_prep_scan_kernel) and the scans overlap the last prep items:
 //   1  kda_chunk_offsets_kernel: per-sequence chunk offsets (prefix sums of ceil(len / 64)),
 //      the cu_seqlens check, and a table of every chunk's (first token, sequence end), into
 //      the workspace;
@@ -23,7 +25,8 @@
 // The tensor-core instructions and their operands are those of the one-CTA-per-head
 // kernel, so the results are the same; the work of steps 1-2 spreads over every SM
 // instead of one SM per (sequence, head), at the price of 96.5 KB of operands per item
-// written and read back through HBM.
+// written and read back through HBM.  The prep kernels come in two instances: with the
+// input prologue (q/k normalisation, g and beta from logits) compiled in, and without.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
