@@ -56,7 +56,7 @@ bool uses_tensor_cores(const kda_prefill_desc& d)
 // state-independent work of every (chunk, head) item on all SMs (about 19.2 K cycles per
 // item) and then the state scan, again in ceil(U / 152) waves but of about 6.0 K cycles per
 // chunk, plus a fixed 10 K cycles (the extra launch, the pipeline's fill); its workspace
-// holds 98,816 bytes per item, at most kSplitMaxItems of them.  The split is taken when its
+// holds 115,200 bytes per item, at most kSplitMaxItems of them.  The split is taken when its
 // estimate is lower.  For 8192-token sequences that is up to 130 units (measured: 1.17 ms at
 // 112 units, 1.25 at 120 and 1.36 at 128, against 1.41 ms for one CTA per unit; 1.44 at
 // 136), and again from 153 units to the item cap, where one CTA per unit would run a mostly

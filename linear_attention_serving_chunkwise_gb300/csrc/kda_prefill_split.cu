@@ -24,7 +24,7 @@
 //      step ahead, v by TMA two chunks ahead.
 // The tensor-core instructions and their operands are those of the one-CTA-per-head
 // kernel, so the results are the same; the work of steps 1-2 spreads over every SM
-// instead of one SM per (sequence, head), at the price of 96.5 KB of operands per item
+// instead of one SM per (sequence, head), at the price of 112.5 KB of operands per item
 // written and read back through HBM.  The prep kernels come in two instances: with the
 // input prologue (q/k normalisation, g and beta from logits) compiled in, and without.
 #include <algorithm>
@@ -47,7 +47,9 @@ constexpr uint32_t IMG_FRONT = 66048;   // bytes [0, IMG_FRONT): read at the sta
 constexpr uint32_t IMG_KTH = 66048;     // K~^T hi bf16, K-major [128 dk rows][64 K tokens]
 constexpr uint32_t IMG_KTL = 82432;     // K~^T lo
 constexpr uint32_t IMG_BACK = 32768;    // bytes [IMG_KTH, IMG_KTH + IMG_BACK): read for the state update
-constexpr uint32_t IMG_BYTES = 98816;
+constexpr uint32_t IMG_QLO = 98816;     // Q' lo = bf16(Q' - bf16(Q')), K-major [64 rows][128 K] (2 x 8 KB),
+                                        // read at the start of a chunk step with the front
+constexpr uint32_t IMG_BYTES = 115200;
 
 // ---------------------------------------------------------------- state-scan shared memory (bytes)
 constexpr uint32_t B_A1 = 0;            // the front image, copied whole
@@ -58,10 +60,12 @@ constexpr uint32_t B_KTH = 66560;       // the back image (1024-byte aligned)
 constexpr uint32_t B_KTL = B_KTH + 16384;
 constexpr uint32_t B_V0 = 99328;        // v tiles [64 tok][128 ch] bf16, two buffers
 constexpr uint32_t B_V1 = 115712;
-constexpr uint32_t B_SB = 132096;       // S bf16, MN-major B [128 dk][128 dv]
+constexpr uint32_t B_SB = 132096;       // S hi bf16, MN-major B [128 dk][128 dv]
+constexpr uint32_t B_SL = 164864;       // S lo bf16, same layout, until D1 has read it; then:
 constexpr uint32_t B_WH = 164864;       // W hi bf16, MN-major B [64 tok][128 dv]
 constexpr uint32_t B_WL = 181248;       // W lo
-constexpr uint32_t B_OST = 197632;      // O staging: 4 x [64 tok][32 dv] fp32 boxes, 128-byte swizzle
+constexpr uint32_t B_A1L = 197632;      // [0; Q' lo] K-major A [128 rows][128 K]: in each 16 KB K block, rows
+                                        // 0-63 are zeros written once, rows 64-127 the image's Q' lo
 constexpr uint32_t B_BAR = 230400;
 constexpr size_t B_SMEM_BYTES = B_BAR + 64 + 1024;
 // words of the 64-byte block at B_BAR: the scan's 5 barriers (0-39), the separate scan
@@ -82,10 +86,12 @@ constexpr long long kPrepCyclesPerItem = 18400;
 
 static_assert(B_KTH % 1024 == 0 && B_V0 % 1024 == 0 && B_SB % 1024 == 0 && B_WH % 1024 == 0, "tile alignment");
 static_assert(B_KTH >= IMG_FRONT && B_V0 >= B_KTH + IMG_BACK && B_V1 == B_V0 + 16384 && B_SB >= B_V1 + 16384 &&
-                  B_WH >= B_SB + 32768 && B_WL == B_WH + 16384 && B_OST >= B_WL + 16384 &&
-                  B_OST % 1024 == 0 && B_BAR >= B_OST + 32768 && B_SMEM_BYTES <= 232448,
+                  B_SL >= B_SB + 32768 && B_WH == B_SL && B_WL == B_WH + 16384 && B_A1L >= B_SL + 32768 &&
+                  B_A1L % 1024 == 0 && B_BAR >= B_A1L + 32768 && B_SMEM_BYTES <= 232448,
               "state-scan map overlaps");
-static_assert(IMG_KTL == IMG_KTH + 16384 && IMG_BYTES == IMG_KTH + IMG_BACK, "image map");
+static_assert(IMG_KTL == IMG_KTH + 16384 && IMG_QLO == IMG_KTH + IMG_BACK && IMG_BYTES == IMG_QLO + 16384 &&
+                  IMG_BYTES % 16 == 0,
+              "image map");
 
 struct SplitParams {
     TcParams p;                 // inputs, outputs, tensor maps, status (as the one-CTA-per-head kernel)
@@ -613,18 +619,24 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        {   // row L, K = dk columns [32 part, +32)
+        {   // row L, K = dk columns [32 part, +32); the Q' rows' lo halves go to the image directly
             float a[32];
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 32 * part), a);
             tmem_wait_ld();
-            uint32_t pk[16];
+            uint32_t pk[16], pl[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
+            for (int i = 0; i < 16; ++i) split_bf16x2(-a[2 * i], -a[2 * i + 1], pk[i], pl[i]);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 st_shared_v4(sbase + A_STAGE + sw128_chunk(L, 4 * part + q, 128), pk[4 * q], pk[4 * q + 1],
                              pk[4 * q + 2], pk[4 * q + 3]);
             fence_proxy_async_smem();
+            if (quarter >= 2) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(img + IMG_QLO + sw128_chunk(L - 64, 4 * part + q, 64)) =
+                        make_uint4(pl[4 * q], pl[4 * q + 1], pl[4 * q + 2], pl[4 * q + 3]);
+            }
         }
         __syncthreads();
         if (t == kStorer) {
@@ -747,26 +759,30 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         mbar_fence_init();
         *s_abort = 0;
         tma_prefetch_desc(&p.tm_v);
-        tma_prefetch_desc(&p.tm_o);
     }
+    // rows 0-63 of the [0; Q' lo] operand: zeros in both K blocks, written once
+    st_shared_v4(sbase + B_A1L + ((t >> 8) << 14) + 16 * (t & 255), 0u, 0u, 0u, 0u);
+    st_shared_v4(sbase + B_A1L + ((t >> 8) << 14) + 16 * (t & 255) + 4096, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
 
     // The copies into shared memory are issued by one producer thread (kProducer, in a warp
     // of the O half, which has slack when they are due); it counts what it issued so that,
-    // on abort, it can wait for the last copy on each barrier.  Thread 0 issues the MMAs and
-    // the O stores.
+    // on abort, it can wait for the last copy on each barrier.  Thread 0 issues the MMAs.
     constexpr int kProducer = 64;
-    bool o_pending = false, mma_open = false;   // thread 0
+    bool mma_open = false;   // thread 0
     int n_front = 0, n_back = 0, n_v[2] = {0, 0};   // producer
     auto fetch_front = [&](int c) {
         if (!ready(c)) {   // never published: give up (the waits on bar_f then run out)
             atomicExch(s_abort, 1);
             return;
         }
-        mbar_arrive_expect_tx(bar_f, IMG_FRONT);
+        mbar_arrive_expect_tx(bar_f, IMG_FRONT + 16384u);
         bulk_load(sm + B_A1, image(c), IMG_FRONT, bar_f);
+        bulk_load(sm + B_A1L + 8192, image(c) + IMG_QLO, 8192u, bar_f);    // rows 64-127, K block 0
+        bulk_load(sm + B_A1L + 24576, image(c) + IMG_QLO + 8192, 8192u, bar_f);   // K block 1
         ++n_front;
     };
     auto fetch_back = [&](int c) {
@@ -831,25 +847,28 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         }
         f_par ^= 1u;
 
-        // the state's bf16 B operand; S <- gamma_C S (this chunk's decay, before its update)
-        // runs while the D1 MMAs, which read only the bf16 copy, execute
+        // the state's bf16 hi and lo B operands; S <- gamma_C S (this chunk's decay, before its
+        // update) runs while the D1 MMAs, which read only the bf16 copies, execute
         float a[32];
         tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), a);
         tmem_wait_ld();
         {
-            uint32_t pk[16];
+            uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+            for (int i = 0; i < 16; ++i) split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                st_shared_v4(sbase + B_SB + sw128_chunk(L, 4 * part + q, 128), pk[4 * q], pk[4 * q + 1],
-                             pk[4 * q + 2], pk[4 * q + 3]);
+            for (int q = 0; q < 4; ++q) {
+                st_shared_v4(sbase + B_SB + sw128_chunk(L, 4 * part + q, 128), hi[4 * q], hi[4 * q + 1],
+                             hi[4 * q + 2], hi[4 * q + 3]);
+                st_shared_v4(sbase + B_SL + sw128_chunk(L, 4 * part + q, 128), lo[4 * q], lo[4 * q + 1],
+                             lo[4 * q + 2], lo[4 * q + 3]);
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
 
-        // D1 = [Tb; M] V (hi + lo) + [-Wk; Q'] S
+        // D1 = [Tb; M] V (hi + lo) + [-Wk; Q'] S_hi + [-Wk; Q'] S_lo + [0; Q' lo] S_hi
         if (t == 0) {
             tc_fence_after_sync();
             if (!mbar_wait_bounded(bar_v + vb, (v_par >> vb) & 1u, kWaitNs)) {
@@ -869,12 +888,16 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
                 for (int ks = 0; ks < 8; ++ks)
                     umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_A1, 128, ks), desc_mnmajor(sbase + B_SB, 128, ks),
                               idesc, 1u);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_A1, 128, ks), desc_mnmajor(sbase + B_SL, 128, ks),
+                              idesc, 1u);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_A1L, 128, ks), desc_mnmajor(sbase + B_SB, 128, ks),
+                              idesc, 1u);
                 umma_commit(bar_mma);
                 mma_open = true;
-            }
-            if (o_pending) {   // the previous chunk's O staging has been read out (rewritten below)
-                bulk_wait_read();
-                o_pending = false;
             }
         }
         {
@@ -896,8 +919,8 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
             }
         }
 
-        // rows 0-63 -> W (hi + lo) B operands, and S += K~^T W as soon as the 8 warps holding
-        // them are done; rows 64-127 = O staged for TMA stores meanwhile
+        // rows 0-63 -> W (hi + lo) B operands (over S lo, which D1 has read), and S += K~^T W as
+        // soon as the 8 warps holding them are done; rows 64-127 = O, stored meanwhile
         tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_D1 + 32 * part), a);
         tmem_wait_ld();
         if (quarter < 2) {
@@ -931,15 +954,9 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
                     mma_open = true;
                 }
             }
-        } else {
+        } else {   // O row r = token t0 + r, dv columns [32 part, +32): 128 contiguous bytes
             const int r = L - 64;
-            if (BT == 64) {   // box `part` = dv columns [32 part, +32)
-                const uint32_t box = sbase + B_OST + 8192 * part;
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_f4(box + sw128_off_f32(r, 4 * q, 64), a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
-                fence_proxy_async_smem();
-            } else if (r < BT) {   // a sequence's ragged last chunk: direct stores
+            if (r < BT) {
                 float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)(t0 + r) * H + h) * 128 + 32 * part);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
@@ -948,15 +965,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         if (t == kProducer && ci + 1 < nchunks) fetch_back(ci + 1);
-        if (t == 0) {
-            mma_open = false;
-            if (BT == 64) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) tma_store_3d(&p.tm_o, sm + B_OST + 8192 * j, 32 * j, h, t0);
-                bulk_commit();
-                o_pending = true;
-            }
-        }
+        if (t == 0) mma_open = false;
         // state snapshot after a full chunk that ends on a checkpoint boundary
         {
             const int done = t0 + 64 - bos;
@@ -975,7 +984,6 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         }
     }
 
-    if (t == 0) bulk_wait_all();   // staged O fully written before the CTA's shared memory goes away
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();

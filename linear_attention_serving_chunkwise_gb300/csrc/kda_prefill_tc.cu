@@ -206,8 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (t < kSolveThreads) {
             phase3_solve(sm, t);
         } else {   // meanwhile warps 8-15: the state's bf16 B operand, S <- gamma_C S, and the seed
-            build_state_operand(sm, vec, tm, L, 2 * (part - 2), quarter);
-            build_state_operand(sm, vec, tm, L, 2 * (part - 2) + 1, quarter);
+            build_state_operand(sm, tm, L, 2 * (part - 2), quarter);
+            build_state_operand(sm, tm, L, 2 * (part - 2) + 1, quarter);
             phase3_seed(sm, vec, tm, L, 2 * (part - 2), quarter, BT);
             phase3_seed(sm, vec, tm, L, 2 * (part - 2) + 1, quarter, BT);
             tmem_wait_st();
@@ -295,32 +295,48 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPL + 8 * ks, desc_mnmajor(vb, 64, ks), idesc, 1u);
             mma_open = true;   // committed with phase 5b's MMAs
         }
+        // meanwhile: the state's lo operand, and S <- gamma_C S
+        state_lo_and_decay(sm, vec, tm, L, part, quarter);
+        fence_proxy_async_smem();
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        {   // A1 = -D2 = [-Wk; Q'], columns [16 part, +16), written over D2 once every thread has read it
+        {   // A1 = -D2 = [-Wk; Q'] (hi) and [0; Q' lo], columns [16 part, +16), written over D2 once
+            // every thread has read it
             float a[32];
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 32 * part), a);
             tmem_wait_ld();
             tc_fence_before_sync();
             __syncthreads();
             tc_fence_after_sync();
-            uint32_t pk[16];
+            uint32_t pk[16], pl[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(-a[2 * i], -a[2 * i + 1]);
+            for (int i = 0; i < 16; ++i) split_bf16x2(-a[2 * i], -a[2 * i + 1], pk[i], pl[i]);
+            if (quarter < 2) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pl[i] = 0u;
+            }
             tmem_st16u(tmem_addr(tm, 32 * quarter, TM_A1 + 16 * part), pk);
+            tmem_st16u(tmem_addr(tm, 32 * quarter, TM_A1L + 16 * part), pl);
         }
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
-        // ---- phase 5b: D1 += [-Wk; Q'] S (the [Tb; M] V half was queued in phase 4)
+        // ---- phase 5b: D1 += [-Wk; Q'] S_hi + [-Wk; Q'] S_lo + [0; Q' lo] S_hi (the [Tb; M] V half
+        // was queued in phase 4)
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+            const uint32_t sh = sbase + OFF_X + X_SB, sl = sbase + OFF_X + X_SL;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1 + 8 * ks, desc_mnmajor(sbase + OFF_X + X_SB, 128, ks), idesc,
-                                 1u);
+                umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1 + 8 * ks, desc_mnmajor(sh, 128, ks), idesc, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1 + 8 * ks, desc_mnmajor(sl, 128, ks), idesc, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1L + 8 * ks, desc_mnmajor(sh, 128, ks), idesc, 1u);
             umma_commit(bar_mma);
             mma_open = false;
         }

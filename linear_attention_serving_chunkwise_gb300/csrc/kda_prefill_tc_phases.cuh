@@ -38,7 +38,8 @@ constexpr uint32_t X_ST = 17408;       // T fp32 [64][68]
 constexpr uint32_t X_SY = 34816;       // solve scratch fp32 [32][LDY]
 constexpr uint32_t X_OST = 65536;      // O staging, dv columns 0-63: 2 x [64 tok][32] fp32 boxes (phase 5,
                                        // after the MMA that reads S bf16 has completed)
-constexpr uint32_t X_SB = 40960;       // S bf16, MN-major B [128 dk][128 dv] (phases 3-5b)
+constexpr uint32_t X_SB = 40960;       // S hi bf16, MN-major B [128 dk][128 dv] (phases 3-5b)
+constexpr uint32_t X_SL = 0;           // S lo bf16, same layout (phases 4-5b; the W tiles take it over in 5c)
 constexpr uint32_t X_WH = 0;           // W hi bf16, MN-major B [64 tok][128 dv] (phase 5)
 constexpr uint32_t X_WL = 16384;       // W lo
 constexpr uint32_t OFF_KG = 180224;    // K_Gamma bf16, MN-major B [64 tok][128 ch]
@@ -76,6 +77,7 @@ constexpr uint32_t TM_TPH = 256;  // [Tb; M] hi, bf16 pairs (phases 3-4)
 constexpr uint32_t TM_TPL = 288;  // [Tb; M] lo (phases 3-4)
 constexpr uint32_t TM_D2 = 320;   // [0; -Q_Gamma] seed, then [Wk; M K_Gamma - Q_Gamma] (phases 3-4)
 constexpr uint32_t TM_A1 = 320;   // [-Wk; Q'] bf16 pairs, over the read D2 (phases 4-5b)
+constexpr uint32_t TM_A1L = 384;  // [0; Q' - bf16(Q')] bf16 pairs, over the read D2 (phases 4-5b)
 constexpr uint32_t TM_KTL = 448;  // K~^T lo (phases 2-5)
 constexpr uint32_t TM_KT = 480;   // K~^T hi, lane = key channel, bf16 pairs (phases 2-5)
 constexpr uint32_t TM_COLS = 512;
@@ -406,13 +408,11 @@ __device__ __forceinline__ void build_ktilde(uint8_t* sm, const float* vec, uint
 }
 
 // ---------------------------------------------------------------- phase 3 side work: S operand
-// Lane c, columns [32 part, 32 part + 32): S -> bf16 MN-major B operand, then
-// S <- gamma_C[c] S (the chunk decay, applied before the state update accumulates).
-__device__ __forceinline__ void build_state_operand(uint8_t* sm, const float* vec, uint32_t tm, int c, int part,
-                                                    int quarter)
+// Lane c, columns [32 part, 32 part + 32): S -> its bf16 rounding S_hi as an MN-major B
+// operand.  The state is left as it is; state_lo_and_decay (phase 4) completes the split.
+__device__ __forceinline__ void build_state_operand(uint8_t* sm, uint32_t tm, int c, int part, int quarter)
 {
     const uint32_t sbase = smem_u32(sm);
-    const float gc = vec[V_GC * 128 + c];
     float a[32];
     tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), a);
     tmem_wait_ld();
@@ -423,6 +423,28 @@ __device__ __forceinline__ void build_state_operand(uint8_t* sm, const float* ve
     for (int q = 0; q < 4; ++q)
         st_shared_v4(sbase + OFF_X + X_SB + sw128_chunk(c, 4 * part + q, 128), pk[4 * q], pk[4 * q + 1],
                      pk[4 * q + 2], pk[4 * q + 3]);
+}
+
+// ---------------------------------------------------------------- phase 4 side work: S lo, decay
+// Lane c, columns [32 part, 32 part + 32): S_lo = bf16(S - S_hi) as a second B operand of
+// the same layout (the history read-out Q' S is formed as Q'_hi S_hi + Q'_hi S_lo +
+// Q'_lo S_hi, so that its operands carry ~16 mantissa bits), then S <- gamma_C[c] S (the
+// chunk decay, applied before the state update accumulates).
+__device__ __forceinline__ void state_lo_and_decay(uint8_t* sm, const float* vec, uint32_t tm, int c, int part,
+                                                   int quarter)
+{
+    const uint32_t sbase = smem_u32(sm);
+    const float gc = vec[V_GC * 128 + c];
+    float a[32];
+    tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), a);
+    tmem_wait_ld();
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        st_shared_v4(sbase + OFF_X + X_SL + sw128_chunk(c, 4 * part + q, 128), lo[4 * q], lo[4 * q + 1],
+                     lo[4 * q + 2], lo[4 * q + 3]);
 #pragma unroll
     for (int i = 0; i < 32; ++i) a[i] *= gc;
     tmem_st32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), a);

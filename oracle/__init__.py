@@ -7,7 +7,6 @@ it, and the two share no code.
 from .kda_ref import (  # noqa: F401
     build_oracle,
     recurrent,
-    recurrent_seq_head,
     unrolled_bruteforce,
     chunkwise_naive,
     delta_invariant_keys,

@@ -118,21 +118,6 @@ def recurrent(q, k, v, g, beta, cu_seqlens, init_state=None, threads: Optional[i
     return out, fin
 
 
-def recurrent_seq_head(inputs: dict, seq: int, head: int, cu_host=None, threads: int = 1):
-    """Oracle for one (sequence, head) of a packed workload whose tensors may live on a GPU.
-
-    Copies only that slice to the host.  Returns (out [L, dv], final [dk, dv]) in fp64."""
-    cu = np.asarray(_host(inputs["cu_seqlens"])[0] if cu_host is None else cu_host, dtype=np.int64)
-    b, e = int(cu[seq]), int(cu[seq + 1])
-    sl = lambda x: x[b:e, head:head + 1]
-    s0 = inputs.get("init_state")
-    s0 = None if s0 is None else s0[seq:seq + 1, head:head + 1]
-    o, f = recurrent(sl(inputs["q"]), sl(inputs["k"]), sl(inputs["v"]), sl(inputs["g"]),
-                     inputs["beta"][b:e, head:head + 1], np.array([0, e - b], dtype=np.int32), s0,
-                     threads=threads)
-    return o[:, 0, :], f[0, 0]
-
-
 def _f64(x):
     if x is None:
         return None

@@ -110,14 +110,14 @@ def test_prefill_query(lib):
 def test_prefill_path_selection_and_split_workspace(lib):
     """bf16, dk = dv = 128: the three-launch chunk-parallel path where its cost estimate beats
     one CTA per (sequence, head) and its items fit the workspace cap (32768); its workspace
-    holds the chunk offsets, the chunk table and 98,816 bytes of operands per item.
+    holds the chunk offsets, the chunk table and 115,200 bytes of operands per item.
     Otherwise one launch, no workspace."""
     def plan(N, T, H, dt=kda.KDA_BF16, d=128):
         return kda.prefill_query(kda.make_desc(N, T, H, d, d, dt))
     p = plan(1, 8192, 96)
     items = (8192 // 64 + 1) * 96
     assert p["kernel_launches"] == 2 and p["tensor_cores"] == 1   # offsets + one cooperative launch
-    assert items * 98816 <= p["workspace_bytes"] <= items * 98816 + items * 4 + 4096
+    assert items * 115200 <= p["workspace_bytes"] <= items * 115200 + items * 4 + 4096
     assert plan(1, 8192, 112)["kernel_launches"] == 2
     assert plan(1, 8192, 120)["kernel_launches"] == 2                # the last single launch
     assert plan(1, 8192, 124)["kernel_launches"] == 3                # split, separate launches

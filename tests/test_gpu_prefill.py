@@ -181,14 +181,5 @@ def test_decay_and_beta_extremes(cuda_lib, case, dtype, d):
     torch.cuda.synchronize()
     assert cuda_lib.last_device_status() == cuda_lib.KDA_OK
     tol = tol_for(dtype)
-    if case == "beta_zero" and dtype == torch.bfloat16:
-        # every output is the bf16 read-out of the decayed initial state and the outputs span
-        # ~20x (a sequence's first tokens see the undecayed state): the bar is checked per
-        # output vector o_t, max_j |err| <= 2e-2 * RMS(o_t); the tensor-wide ratio is recorded
-        got = out.detach().cpu().double().numpy()
-        err = np.abs(got - ref_o).max(axis=(1, 2))
-        tok_rms = np.sqrt((ref_o ** 2).mean(axis=(1, 2)))
-        assert np.isfinite(got).all() and (err <= tol * tok_rms).all(), (err / tok_rms).max()
-    else:
-        check(f"{case} out", out, ref_o, tol)
+    check(f"{case} out", out, ref_o, tol)
     check(f"{case} final_state", fin, ref_s, tol)

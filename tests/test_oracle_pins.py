@@ -331,3 +331,25 @@ def test_prologue_keeps_the_delta_invariant():
     Kd = Kn.astype(np.float64)
     assert np.max(np.abs(Kd @ Kd.T - np.eye(dk))) < 1e-6
     assert np.max(np.abs(S.T @ Kd.T - V.astype(np.float64).T)) < 1e-5
+
+
+def test_rel_err_hand_worked_values():
+    """The parity bar's measure, max |x - ref| / RMS(ref), on values worked out by hand.
+    Each case tells it apart from a plausible slip: the mean instead of the max of |x - ref|,
+    the L2 norm or the standard deviation of ref instead of its RMS, the RMS over the
+    non-zero entries only, or a sign taken one way."""
+    ref = np.array([1.0, -1.0, 1.0, -1.0])           # RMS 1, L2 norm 2
+    x = ref + np.array([0.0, 0.5, -0.25, 0.0])       # max |d| 0.5, mean |d| 0.1875
+    assert rel_err(x, ref) == 0.5
+    assert rel_err(ref - (x - ref), ref) == 0.5      # errors of the other sign
+    ref = np.array([2.0, 2.0, 2.0, 2.0, 0.0, 0.0, 0.0, 0.0])   # RMS sqrt(2); std 1; RMS of non-zeros 2
+    x = ref.copy()
+    x[7] = 1.0
+    assert abs(rel_err(x, ref) - 1.0 / np.sqrt(2.0)) < 1e-15
+    ref2 = np.array([[3.0, 4.0, 0.0], [0.0, 0.0, 5.0]])        # RMS sqrt(50 / 6) = 5 / sqrt(3)
+    x2 = ref2 + np.array([[0.0, 0.0, 0.0], [0.0, -2.5, 0.0]])
+    assert abs(rel_err(x2, ref2) - 2.5 * np.sqrt(3.0) / 5.0) < 1e-15
+    # an all-zero reference: the bar falls back to the absolute error
+    assert rel_err(np.array([0.0, 0.25, -0.5]), np.zeros(3)) == 0.5
+    assert rel_err(np.zeros(0), np.zeros(0)) == 0.0
+    assert rel_err(ref2, ref2) == 0.0
