@@ -203,9 +203,21 @@ kda_status kda_prefill_host(const kda_prefill_desc* desc, const void* q, const v
     Stage stage[2] = {carve(ws + align_up(s.state_bytes), s),
                       carve(ws + align_up(s.state_bytes) + stage_bytes(s), s)};
 
+    // On an error after work has been enqueued, the caller's stream is still made to wait for
+    // every copy already queued on the library's streams (best effort), so that the contract
+    // holds on failure too: once `stream` has drained, no copy reads the host inputs or the
+    // workspace, or writes out or final_state.
+    auto join = [&]() {
+        for (int u = 0; u < kUp; ++u)
+            if (cudaEventRecord(hp->end, hp->up[u]) == cudaSuccess) (void)cudaStreamWaitEvent(comp, hp->end, 0);
+        if (cudaEventRecord(hp->end, hp->down) == cudaSuccess) (void)cudaStreamWaitEvent(comp, hp->end, 0);
+    };
 #define KDA_CK(x) \
     do { \
-        if ((x) != cudaSuccess) return KDA_ERR_CUDA; \
+        if ((x) != cudaSuccess) { \
+            join(); \
+            return KDA_ERR_CUDA; \
+        } \
     } while (0)
     // everything after prior work on the caller's stream
     KDA_CK(cudaEventRecord(hp->start, comp));
@@ -254,8 +266,10 @@ kda_status kda_prefill_host(const kda_prefill_desc* desc, const void* q, const v
             !copy_rows(sg.k, static_cast<const char*>(k), s.in_row_q, cu, r, h2d, true) ||
             !copy_rows(sg.v, static_cast<const char*>(v), s.in_row_v, cu, r, h2d, true) ||
             !copy_rows(sg.g, reinterpret_cast<const char*>(g), s.row_g, cu, r, h2d, true) ||
-            !copy_rows(sg.beta, reinterpret_cast<const char*>(beta), s.row_beta, cu, r, h2d, true))
+            !copy_rows(sg.beta, reinterpret_cast<const char*>(beta), s.row_beta, cu, r, h2d, true)) {
+            join();
             return KDA_ERR_CUDA;
+        }
         KDA_CK(cudaMemcpyAsync(sg.cu, cu, s.cu_bytes, h2d, hp->up[0]));
         for (int u = 0; u < kUp; ++u) KDA_CK(cudaEventRecord(hp->staged[b][u], hp->up[u]));
         // round r on the caller's stream, continuing the device state in place
@@ -265,12 +279,17 @@ kda_status kda_prefill_host(const kda_prefill_desc* desc, const void* q, const v
         st = kda::prefill_no_workspace(&rd, sg.q, sg.k, sg.v, reinterpret_cast<const float*>(sg.g),
                                        reinterpret_cast<const float*>(sg.beta), sg.cu, dstate,
                                        reinterpret_cast<float*>(sg.out), dstate, comp);
-        if (st != KDA_OK) return st;
+        if (st != KDA_OK) {
+            join();
+            return st;
+        }
         KDA_CK(cudaEventRecord(hp->computed[b], comp));
         // outputs of round r
         KDA_CK(cudaStreamWaitEvent(hp->down, hp->computed[b], 0));
-        if (!copy_rows(reinterpret_cast<char*>(out), sg.out, s.row_out, cu, r, cudaMemcpyDeviceToHost, false))
+        if (!copy_rows(reinterpret_cast<char*>(out), sg.out, s.row_out, cu, r, cudaMemcpyDeviceToHost, false)) {
+            join();
             return KDA_ERR_CUDA;
+        }
         KDA_CK(cudaEventRecord(hp->drained[b], hp->down));
     }
     if (final_state) {

@@ -1,12 +1,19 @@
 // kda_prefill_host_static: the host-buffer prefill with its device staging in a fixed
 // scratch array of this library, so that a call allocates nothing and needs no device
-// buffer from the caller.  Declarations and contracts: include/kda.h.
+// buffer from the caller.  It serves callers that cannot call cudaMalloc when a request
+// arrives: a process whose device memory already belongs to its own pool, or a loop that
+// cannot take the synchronisation a cudaMalloc may cause.  Declarations and contracts:
+// include/kda.h.
 //
-// The scratch is one file-scope __device__ array per device (its address taken once per
-// device with cudaGetSymbolAddress).  Calls share it, so each call's work on the device is
-// ordered after the previous call's: the caller's stream waits for an event that the
+// The scratch is one file-scope __device__ array, KDA_STATIC_SCRATCH_BYTES (64 MiB) on every
+// device that loads the library, held until exit.  In host code its name is only a host-side
+// stand-in, so the device address is taken once per device, on the first call with that
+// device current, with cudaGetSymbolAddress (the first call also creates one event; it should
+// come before any stream capture).  Calls share the array, so each call's work on the device
+// is ordered after the previous call's: the caller's stream waits for an event that the
 // previous call recorded on its own stream behind all of its copies and kernels, and the
-// call records that event anew behind its own.
+// call records that event anew behind its own.  Each call writes all of the scratch it reads
+// (the state is copied in or zeroed first), so nothing left by the previous call is used.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -66,8 +73,12 @@ extern "C" kda_status kda_prefill_host_static(const kda_prefill_desc* desc, cons
     if (s->used && cudaStreamWaitEvent(strm, s->done, 0) != cudaSuccess) return KDA_ERR_CUDA;
     const kda_status r = kda_prefill_host(desc, q, k, v, g, beta, cu_seqlens, init_state, out, final_state,
                                           segment_tokens, s->base, (size_t)KDA_STATIC_SCRATCH_BYTES, stream);
+    // Whatever the outcome, the event is recorded behind this call's work: kda_prefill_host
+    // leaves `strm` waiting for every copy and kernel it enqueued, on failure too, so the next
+    // call cannot reuse the scratch while a failed call's partial work still runs.  (After an
+    // argument error nothing was enqueued; the event then marks the previous call's end.)
+    const bool recorded = cudaEventRecord(s->done, strm) == cudaSuccess;
+    if (recorded) s->used = true;
     if (r != KDA_OK) return r;
-    if (cudaEventRecord(s->done, strm) != cudaSuccess) return KDA_ERR_CUDA;
-    s->used = true;
-    return KDA_OK;
+    return recorded ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -1,6 +1,10 @@
-"""GPU tests of kda_prefill_host_static: the host-buffer prefill whose device staging is the
-library's own fixed scratch array (no workspace from the caller, no device allocation).
-Collected last so that its scratch is first touched after every other GPU test."""
+"""GPU tests of kda_prefill_host_static, the entry point for callers that cannot allocate
+device memory when a request arrives (their device memory already belongs to their own pool,
+or their loop cannot take a cudaMalloc's synchronisation): the host-buffer prefill with its
+device staging in the library's own fixed scratch array, no workspace from the caller and no
+device allocation.  Its results must equal those of kda_prefill_host with a workspace, on
+consecutive calls too.  Collected last (the file sorts last) so that a run stopping at the
+first failure has run every other test first; it also passes alone in a fresh process."""
 import numpy as np
 import pytest
 import torch
