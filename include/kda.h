@@ -42,8 +42,13 @@
  *                                computed in fp32 and rounded to qkv_dtype;
  *       KDA_PROLOGUE_G_LOGITS    g holds logits z; the decay used is -5 * sigmoid(z);
  *       KDA_PROLOGUE_BETA_LOGITS beta holds logits y; the write used is sigmoid(y).
- *     The output gate that the pages pair with KDA (llm-atlas Q08) is not part
- *     of this: its form is not given there.
+ *   - Output gate (kda_prefill_gated, kda_decode_gated, kda_decode_multi_gated):
+ *     the pages give KDA an input-dependent, full-rank gate over the read-out
+ *     channels (llm-atlas Q08) but not its formula.  This library reads it as an
+ *     elementwise sigmoid gate applied to the fp32 output, out = o * sigmoid(z),
+ *     with the logits z [.., H, dv] fp32 computed by the caller (the projection
+ *     that produces them is outside the attention kernel).  The gate changes only
+ *     the written output, never the state.
  *   - Preconditions not checked on the host: g in [-5, 0] (the bounded
  *     log-decay; never clamped), beta in [0, 1].  Values outside these ranges
  *     are unsupported: they are computed, but without the accuracy bound.
@@ -58,7 +63,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 2
+#define KDA_ABI_VERSION 3
 
 #define KDA_PROLOGUE_QK_L2NORM 1
 #define KDA_PROLOGUE_G_LOGITS 2
@@ -105,7 +110,7 @@ const char* kda_status_string(kda_status status);
  * favours it over one CTA per (sequence, head): few units (up to ~130 for 8192-token
  * sequences), or a partial second wave on the 152 SMs.  The workspace then holds
  * the chunk offsets and, per (64-token chunk, head), the operands of that chunk's state
- * step: 98,816 bytes each, for (total_tokens / 64 + num_seqs) * num_heads chunks.
+ * step: 115,200 bytes each, for (total_tokens / 64 + num_seqs) * num_heads chunks.
  */
 size_t kda_prefill_workspace_bytes(const kda_prefill_desc* desc);
 
@@ -162,6 +167,24 @@ kda_status kda_prefill(const kda_prefill_desc* desc,
                        void* stream);
 
 /*
+ * kda_prefill_gated -- kda_prefill with the output gate (see the top): every output
+ * element is written as o * sigmoid(z), z = gate[t][h][j] (llm-atlas K3_RESEARCH.md, Q08,
+ * read as an elementwise sigmoid gate on the read-out channels).
+ *   gate  [T, H, dv] fp32 logits, device memory, 16-byte aligned; must not overlap out,
+ *         final_state or the workspace.  NULL makes the call identical to kda_prefill.
+ * Everything else (layouts, workspace, paths, errors) as kda_prefill; final_state is the
+ * ungated recurrence's, bit for bit.
+ */
+kda_status kda_prefill_gated(const kda_prefill_desc* desc,
+                             const void* q, const void* k, const void* v,
+                             const float* g, const float* beta, const float* gate,
+                             const int32_t* cu_seqlens,
+                             const float* init_state,
+                             float* out, float* final_state,
+                             void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/*
  * kda_prefill_checkpointed -- kda_prefill that also snapshots each sequence's state at
  * chunk-aligned positions, for resuming a later request from a cached prefix (llm-atlas
  * K3_RESEARCH.md, Q31 hybrid prefix cache with sparse KDA checkpoints and 512-token hash
@@ -211,7 +234,10 @@ kda_status kda_prefill_checkpointed(const kda_prefill_desc* desc,
  * device are serialised by the library while they enqueue.
  * Errors: as kda_prefill (cu_seqlens is checked on the host); KDA_ERR_INVALID_ARG for a
  * segment_tokens that is not a positive multiple of 64 or a misaligned workspace;
- * KDA_ERR_WORKSPACE for a short one.  Nothing is enqueued when an argument is rejected.
+ * KDA_ERR_WORKSPACE for a short one.  Nothing is enqueued when an argument is rejected.  When
+ * a CUDA call fails after work has been enqueued, the error is returned with `stream` made to
+ * wait (as far as the runtime still allows) for the copies and kernels already enqueued, so
+ * that synchronising it still marks the point after which no copy touches the buffers.
  */
 size_t kda_prefill_host_workspace_bytes(const kda_prefill_desc* desc, int32_t segment_tokens);
 
@@ -227,12 +253,23 @@ kda_status kda_prefill_host(const kda_prefill_desc* desc,
 
 /*
  * kda_prefill_host_static -- kda_prefill_host without a caller workspace.  The pages have
- * no counterpart to this entry point: it is a convenience of this library's host-buffer
- * path.  The device staging lives in a fixed scratch array inside the library,
- * KDA_STATIC_SCRATCH_BYTES per device, so the call allocates nothing (no device memory,
- * no caller buffer).  Same arguments, layouts, results and stream semantics as
- * kda_prefill_host.  Calls on one device share the scratch, so each call's copies and
- * kernels run after those of the previous call on that device (whatever its stream).
+ * no counterpart to this entry point.  It is for callers that cannot call cudaMalloc when
+ * a request arrives: a serving process that has already handed all of the device's memory
+ * to its own pool (a fresh cudaMalloc would fail or fragment it), or a latency-bound loop
+ * that cannot take the device-wide synchronisation a cudaMalloc may cause, and has no
+ * device buffer of its own to lend.  The device staging then lives in a fixed scratch
+ * array inside the library, KDA_STATIC_SCRATCH_BYTES per device, which every device that
+ * loads the library holds until the process exits; the call itself calls no cudaMalloc,
+ * cudaFree or allocating library routine.  Same arguments, layouts, results and stream
+ * semantics as kda_prefill_host.
+ *   - The first call on a device sets that device up (the scratch's device address, taken
+ *     with cudaGetSymbolAddress while that device is current, and one event); make that
+ *     first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps whatever the last call left
+ *     in it; each call writes every part of it that it reads (the state is copied in or
+ *     zeroed first).  Two calls that ran on the GPU at the same time would race on it, so
+ *     the library orders them: each call's copies and kernels run after those of the
+ *     previous call on that device, whatever streams they were given.
  * Errors: as kda_prefill_host, and KDA_ERR_WORKSPACE when
  * kda_prefill_host_workspace_bytes(desc, segment_tokens) exceeds the scratch (a smaller
  * segment_tokens, or kda_prefill_host with a workspace, serves larger problems); nothing
@@ -269,6 +306,19 @@ kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, 
                       void* stream);
 
 /*
+ * kda_decode_gated -- kda_decode with the output gate: out = o * sigmoid(gate) elementwise
+ * (llm-atlas K3_RESEARCH.md, Q08; see the top).  gate [B, H, dv] fp32 logits, device memory,
+ * 16-byte aligned, overlapping neither out nor state; NULL = kda_decode.  The state update
+ * is that of kda_decode, bit for bit.
+ */
+kda_status kda_decode_gated(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, int32_t qkv_dtype,
+                            int32_t prologue,
+                            const void* q, const void* k, const void* v,
+                            const float* g, const float* beta, const float* gate,
+                            float* state, float* out,
+                            void* stream);
+
+/*
  * kda_decode_multi -- K consecutive tokens of each sequence in one pass over each head's
  * state, for verifying K draft tokens (llm-atlas K3_RESEARCH.md, Q28: the MTP layer tuned
  * into an EAGLE-3 draft; Q07: O(1) decode update).  Per token the same fused update as
@@ -298,6 +348,46 @@ kda_status kda_decode_multi(int32_t batch, int32_t tokens, int32_t num_heads, in
                             const int32_t* n_apply,
                             float* state, float* out,
                             void* stream);
+
+/*
+ * kda_decode_multi_gated -- kda_decode_multi with the output gate on every token's output:
+ * out = o * sigmoid(gate) (llm-atlas K3_RESEARCH.md, Q08; see the top).  gate [B, K, H, dv]
+ * fp32 logits, device memory, 16-byte aligned, overlapping neither out nor state; ignored
+ * when out is NULL; NULL = kda_decode_multi.  States as kda_decode_multi, bit for bit.
+ */
+kda_status kda_decode_multi_gated(int32_t batch, int32_t tokens, int32_t num_heads, int32_t dk, int32_t dv,
+                                  int32_t qkv_dtype, int32_t prologue,
+                                  const void* q, const void* k, const void* v,
+                                  const float* g, const float* beta, const float* gate,
+                                  const int32_t* n_apply,
+                                  float* state, float* out,
+                                  void* stream);
+
+/*
+ * kda_state_combine -- the fold step of context-parallel prefill over one long sequence
+ * (llm-atlas K3_RESEARCH.md, section 8 system-state table: "KCP" in the pretraining row; Q07:
+ * the state passed from chunk to chunk).  When consecutive token ranges of a sequence run on
+ * different ranks, range r maps the state entering it as S_after = M_r S_before + S_r, where
+ * M_r is the dk x dk product of its chunks' transitions (the state after the range from
+ * initial state I with v = 0: kda_prefill with a zero v and an identity init_state) and S_r
+ * is the state after the range from a zero start.  The state entering range r is then the
+ * fold S <- M_j S + S_j over the ranges j < r, one call per step:
+ *
+ *   state_out[i] = transition[i] . state_in[i] + state_add[i]     for i < count (fp32)
+ *
+ *   count       number of (sequence, head) states, >= 0
+ *   dk, dv      must be equal, 64 or 128 (else KDA_ERR_UNSUPPORTED)
+ *   transition  [count, dk, dk] fp32, row-major (may be NULL when state_in is NULL)
+ *   state_in    [count, dk, dv] fp32, row c = key channel c; NULL = zero
+ *   state_add   [count, dk, dv] fp32; NULL = zero
+ *   state_out   [count, dk, dv] fp32; may be state_add itself (in place), must not overlap
+ *               state_in or transition (KDA_ERR_INVALID_ARG)
+ * All pointers are device memory, 16-byte aligned; asynchronous on `stream`.
+ */
+kda_status kda_state_combine(int32_t count, int32_t dk, int32_t dv,
+                             const float* transition, const float* state_in,
+                             const float* state_add, float* state_out,
+                             void* stream);
 
 /*
  * Synchronises `stream`, then returns and clears the device status word of the

@@ -15,7 +15,9 @@ Input recipe (the five workloads named by the library's headline benchmark):
   (llm-atlas "K3_RESEARCH.md", question ledger Q06 and Figure 3);
 * initial state ~ N(0, 0.02) (standard deviation 0.02) where the workload has
   one, zero otherwise;
-* varlen lengths uniform in [512, 16384] inclusive.
+* varlen lengths uniform in [512, 16384] inclusive;
+* output-gate logits z ~ N(0, 1) per output element, fp32 (for the gated entry points:
+  out = o * sigmoid(z)).
 
 Random draws come from a ``torch.Generator`` seeded per tensor with
 ``seed * 1000 + stream`` on the device the tensors are made on, so a large
@@ -33,7 +35,7 @@ import torch
 G_MIN = -5.0
 
 # stream ids: one independent generator per tensor kind
-_S_Q, _S_K, _S_V, _S_G, _S_B, _S_S0, _S_LEN = 1, 2, 3, 4, 5, 6, 7
+_S_Q, _S_K, _S_V, _S_G, _S_B, _S_S0, _S_LEN, _S_Z = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 @dataclasses.dataclass(frozen=True)
@@ -167,6 +169,12 @@ def make_decode_inputs(cfg: DecodeConfig, seed: int = 0, device="cpu", steps: Op
     d["v"] = _normal((S, B, H, dv), seed, _S_V, device).to(cfg.qkv_dtype)
     d["state0"] = _normal((B, H, dk, dv), seed, _S_S0, device, std=0.02)
     return d
+
+
+def make_gate_logits(shape, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Seeded output-gate logits z ~ N(0, 1), fp32, of the output's shape ([T, H, dv] for
+    prefill, [B, H, dv] or [B, K, H, dv] for decode)."""
+    return _normal(tuple(shape), seed, _S_Z, device).contiguous()
 
 
 def random_prefill_config(seqlens: List[int], num_heads: int, d: int, qkv_dtype, init: str = "normal",

@@ -34,5 +34,6 @@ from ._lib import (  # noqa: F401
     prefill_host_workspace_bytes,
     prefill_query,
     prefill_workspace_bytes,
+    state_combine,
     status_string,
 )

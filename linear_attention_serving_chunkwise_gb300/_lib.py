@@ -23,7 +23,7 @@ KDA_ERR_CUDA = -4
 KDA_ERR_TIMEOUT = -5
 KDA_F32 = 0
 KDA_BF16 = 1
-KDA_ABI_VERSION = 2
+KDA_ABI_VERSION = 3
 # input prologue bits (include/kda.h): q/k L2 normalisation, g = -5 sigmoid(z), beta = sigmoid(y)
 KDA_PROLOGUE_QK_L2NORM = 1
 KDA_PROLOGUE_G_LOGITS = 2
@@ -32,8 +32,9 @@ KDA_PROLOGUE_ALL = 7
 
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes", "kda_prefill_query",
-            "kda_prefill", "kda_prefill_checkpointed", "kda_prefill_host_workspace_bytes", "kda_prefill_host",
-            "kda_prefill_host_static", "kda_decode", "kda_decode_multi", "kda_last_device_status")
+            "kda_prefill", "kda_prefill_gated", "kda_prefill_checkpointed", "kda_prefill_host_workspace_bytes",
+            "kda_prefill_host", "kda_prefill_host_static", "kda_decode", "kda_decode_gated", "kda_decode_multi",
+            "kda_decode_multi_gated", "kda_state_combine", "kda_last_device_status")
 KDA_DECODE_MULTI_MAX_TOKENS = 64
 KDA_STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -79,6 +80,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.kda_prefill_query.argtypes = [ctypes.POINTER(PrefillDesc), ctypes.POINTER(PrefillPlan)]
     lib.kda_prefill.restype = ctypes.c_int
     lib.kda_prefill.argtypes = [ctypes.POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.kda_prefill_gated.restype = ctypes.c_int
+    lib.kda_prefill_gated.argtypes = [ctypes.POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.kda_prefill_checkpointed.restype = ctypes.c_int
     lib.kda_prefill_checkpointed.argtypes = [ctypes.POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                              i32, i32, vp, vp, sz, vp]
@@ -92,8 +95,15 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                             vp]
     lib.kda_decode.restype = ctypes.c_int
     lib.kda_decode.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.kda_decode_gated.restype = ctypes.c_int
+    lib.kda_decode_gated.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.kda_decode_multi.restype = ctypes.c_int
     lib.kda_decode_multi.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.kda_decode_multi_gated.restype = ctypes.c_int
+    lib.kda_decode_multi_gated.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                           vp]
+    lib.kda_state_combine.restype = ctypes.c_int
+    lib.kda_state_combine.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp]
     lib.kda_last_device_status.restype = ctypes.c_int
     lib.kda_last_device_status.argtypes = [vp]
     if path is None:
@@ -157,15 +167,18 @@ def prefill_query(desc: PrefillDesc) -> dict:
 
 def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_state=None, *,
             num_seqs: Optional[int] = None, want_final: bool = True, workspace=None, stream=None, check=True,
-            checkpoint_interval: int = 0, checkpoint_slots: int = 0, checkpoints=None, prologue: int = 0):
-    """KDA prefill through ``kda_prefill``.
+            checkpoint_interval: int = 0, checkpoint_slots: int = 0, checkpoints=None, prologue: int = 0,
+            gate=None):
+    """KDA prefill through ``kda_prefill`` (``kda_prefill_gated`` when ``gate`` is given).
 
     q, k [T,H,dk], v [T,H,dv] (fp32 or bf16); g [T,H,dk] fp32; beta [T,H] fp32;
     cu_seqlens [N+1] int32 on the device, or None with ``num_seqs`` equal
     sequences (default 1); init_state [N,H,dk,dv] fp32 or None.
     ``out``/``final_state`` are allocated if not given (``final_state`` may be
     ``init_state`` for in-place chaining).  ``prologue``: KDA_PROLOGUE_* bits (q, k, g and
-    beta then hold the raw values of the input recipe).  Returns (out, final_state)."""
+    beta then hold the raw values of the input recipe).  ``gate``: output gate logits
+    [T,H,dv] fp32 (out = o * sigmoid(gate)), not combined with checkpoints.  Returns
+    (out, final_state)."""
     T, H, dk = q.shape
     dv = v.shape[2]
     N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
@@ -182,6 +195,8 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_
         _keep_until_done(workspace, stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if checkpoint_interval:
+        if gate is not None:
+            raise ValueError("the output gate is not offered with checkpoints")
         if checkpoints is None:
             checkpoints = torch.zeros((N, H, checkpoint_slots, dk, dv), dtype=torch.float32, device=q.device)
             _keep_until_done(checkpoints, stream)
@@ -192,6 +207,13 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=None, final_
         if check and st != KDA_OK:
             raise KDAError(st, "kda_prefill_checkpointed")
         return out, final_state, checkpoints
+    if gate is not None:
+        st = load().kda_prefill_gated(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(gate),
+                                      _ptr(cu_seqlens), _ptr(init_state), _ptr(out), _ptr(final_state),
+                                      _ptr(workspace), ws_bytes, _stream_handle(stream))
+        if check and st != KDA_OK:
+            raise KDAError(st, "kda_prefill_gated")
+        return out, final_state
     st = load().kda_prefill(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
                             _ptr(init_state), _ptr(out), _ptr(final_state), _ptr(workspace), ws_bytes,
                             _stream_handle(stream))
@@ -258,16 +280,24 @@ def prefill_host_static(q, k, v, g, beta, cu_seqlens=None, init_state=None, out=
     return out, final_state
 
 
-def decode(q, k, v, g, beta, state, out=None, *, stream=None, check=True, prologue: int = 0):
-    """One KDA decode step through ``kda_decode``; ``state`` [B,H,dk,dv] fp32 is updated in place.
+def decode(q, k, v, g, beta, state, out=None, *, stream=None, check=True, prologue: int = 0, gate=None):
+    """One KDA decode step through ``kda_decode`` (``kda_decode_gated`` with ``gate``);
+    ``state`` [B,H,dk,dv] fp32 is updated in place.
 
     q, k [B,H,dk], v [B,H,dv] (fp32 or bf16); g [B,H,dk] fp32; beta [B,H] fp32;
-    ``prologue``: KDA_PROLOGUE_* bits.  Returns out [B,H,dv] fp32."""
+    ``prologue``: KDA_PROLOGUE_* bits; ``gate``: output gate logits [B,H,dv] fp32.
+    Returns out [B,H,dv] fp32."""
     B, H, dk = q.shape
     dv = v.shape[2]
     if out is None:
         out = torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
         _keep_until_done(out, stream)
+    if gate is not None:
+        st = load().kda_decode_gated(B, H, dk, dv, _dtype_code(q), int(prologue), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                     _ptr(beta), _ptr(gate), _ptr(state), _ptr(out), _stream_handle(stream))
+        if check and st != KDA_OK:
+            raise KDAError(st, "kda_decode_gated")
+        return out
     st = load().kda_decode(B, H, dk, dv, _dtype_code(q), int(prologue), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                            _ptr(state), _ptr(out), _stream_handle(stream))
     if check and st != KDA_OK:
@@ -276,22 +306,47 @@ def decode(q, k, v, g, beta, state, out=None, *, stream=None, check=True, prolog
 
 
 def decode_multi(q, k, v, g, beta, state, out=None, n_apply=None, *, want_out=True, stream=None, check=True,
-                 prologue: int = 0):
+                 prologue: int = 0, gate=None):
     """K tokens per sequence through ``kda_decode_multi``: q, k [B,K,H,dk], v [B,K,H,dv]
     (fp32 or bf16); g [B,K,H,dk] fp32; beta [B,K,H] fp32; ``state`` [B,H,dk,dv] fp32 is
     replaced by the state after the first ``n_apply[b]`` tokens (int32 [B] on the device;
     None = all K); ``prologue``: KDA_PROLOGUE_* bits.  Returns out [B,K,H,dv] fp32 (None
-    when ``want_out`` is False)."""
+    when ``want_out`` is False).  ``gate``: output gate logits [B,K,H,dv] fp32 (through
+    ``kda_decode_multi_gated``)."""
     B, K, H, dk = q.shape
     dv = v.shape[3]
     if out is None and want_out:
         out = torch.empty((B, K, H, dv), dtype=torch.float32, device=q.device)
         _keep_until_done(out, stream)
+    if gate is not None:
+        st = load().kda_decode_multi_gated(B, K, H, dk, dv, _dtype_code(q), int(prologue), _ptr(q), _ptr(k), _ptr(v),
+                                           _ptr(g), _ptr(beta), _ptr(gate), _ptr(n_apply), _ptr(state), _ptr(out),
+                                           _stream_handle(stream))
+        if check and st != KDA_OK:
+            raise KDAError(st, "kda_decode_multi_gated")
+        return out
     st = load().kda_decode_multi(B, K, H, dk, dv, _dtype_code(q), int(prologue), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                  _ptr(beta),
                                  _ptr(n_apply), _ptr(state), _ptr(out), _stream_handle(stream))
     if check and st != KDA_OK:
         raise KDAError(st, "kda_decode_multi")
+    return out
+
+
+def state_combine(transition, state_in, state_add, out=None, *, stream=None, check=True):
+    """out = transition @ state_in + state_add per (sequence, head), through
+    ``kda_state_combine``: transition [..., dk, dk], states [..., dk, dv] fp32 on the device
+    (state_in or state_add may be None = zero; ``out`` may be ``state_add``).  Returns out."""
+    ref = state_add if state_add is not None else state_in
+    dk, dv = ref.shape[-2], ref.shape[-1]
+    count = ref.numel() // (dk * dv)
+    if out is None:
+        out = torch.empty_like(ref)
+        _keep_until_done(out, stream)
+    st = load().kda_state_combine(count, dk, dv, _ptr(transition), _ptr(state_in), _ptr(state_add), _ptr(out),
+                                  _stream_handle(stream))
+    if check and st != KDA_OK:
+        raise KDAError(st, "kda_state_combine")
     return out
 
 

@@ -147,7 +147,8 @@ namespace {
 kda_status prefill_impl(const kda_prefill_desc* desc, const void* q, const void* k, const void* v, const float* g,
                         const float* beta, const int32_t* cu_seqlens, const float* init_state, float* out,
                         float* final_state, int32_t ckpt_interval, int32_t ckpt_slots, float* checkpoints,
-                        void* workspace, size_t workspace_bytes, void* stream, bool allow_split)
+                        void* workspace, size_t workspace_bytes, void* stream, bool allow_split,
+                        const float* gate = nullptr)
 {
     kda_status st = validate_prefill(desc);
     if (st != KDA_OK) return st;
@@ -170,6 +171,7 @@ kda_status prefill_impl(const kda_prefill_desc* desc, const void* q, const void*
     if (init_state && !aligned16(init_state)) return KDA_ERR_INVALID_ARG;
     if (final_state && !aligned16(final_state)) return KDA_ERR_INVALID_ARG;
     if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
+    if (gate && !aligned16(gate)) return KDA_ERR_INVALID_ARG;
 
     // outputs must not overlap inputs (init_state == final_state exactly is allowed)
     const size_t sbytes = N * H * d.dk * d.dv * sizeof(float);
@@ -189,12 +191,15 @@ kda_status prefill_impl(const kda_prefill_desc* desc, const void* q, const void*
     if (final_state && init_state && final_state != init_state && overlaps(r_fin, ins[6]))
         return KDA_ERR_INVALID_ARG;
     if (final_state && T > 0 && overlaps(r_fin, r_out)) return KDA_ERR_INVALID_ARG;
+    const Range r_gate = range_of(gate, gate ? T * H * d.dv * sizeof(float) : 0);
+    if (overlaps(r_gate, r_out) || overlaps(r_gate, r_fin)) return KDA_ERR_INVALID_ARG;
     const Range r_ws = range_of(workspace, ws_need);
     if (split) {   // the workspace is written: it must not overlap anything else
         for (const Range& r : ins) {
             if (overlaps(r_ws, r)) return KDA_ERR_INVALID_ARG;
         }
-        if (overlaps(r_ws, r_out) || (final_state && overlaps(r_ws, r_fin))) return KDA_ERR_INVALID_ARG;
+        if (overlaps(r_ws, r_out) || (final_state && overlaps(r_ws, r_fin)) || overlaps(r_ws, r_gate))
+            return KDA_ERR_INVALID_ARG;
     }
     if (checkpoints) {
         if (ckpt_interval <= 0 || ckpt_interval % 64 != 0 || ckpt_slots <= 0 || !aligned16(checkpoints))
@@ -220,6 +225,7 @@ kda_status prefill_impl(const kda_prefill_desc* desc, const void* q, const void*
     a.checkpoints = checkpoints;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.status = status;
     a.prologue = d.prologue;
+    a.gate = T > 0 ? gate : nullptr;
     const cudaStream_t sm = static_cast<cudaStream_t>(stream);
     const cudaError_t e = split                  ? kda::launch_prefill_split(a, sm)
                           : uses_tensor_cores(d) ? kda::launch_prefill_tc(a, sm)
@@ -253,6 +259,15 @@ kda_status kda_prefill(const kda_prefill_desc* desc, const void* q, const void* 
                         workspace_bytes, stream, true);
 }
 
+kda_status kda_prefill_gated(const kda_prefill_desc* desc, const void* q, const void* k, const void* v,
+                             const float* g, const float* beta, const float* gate, const int32_t* cu_seqlens,
+                             const float* init_state, float* out, float* final_state, void* workspace,
+                             size_t workspace_bytes, void* stream)
+{
+    return prefill_impl(desc, q, k, v, g, beta, cu_seqlens, init_state, out, final_state, 0, 0, nullptr, workspace,
+                        workspace_bytes, stream, true, gate);
+}
+
 kda_status kda_prefill_checkpointed(const kda_prefill_desc* desc, const void* q, const void* k, const void* v,
                                     const float* g, const float* beta, const int32_t* cu_seqlens,
                                     const float* init_state, float* out, float* final_state,
@@ -264,9 +279,9 @@ kda_status kda_prefill_checkpointed(const kda_prefill_desc* desc, const void* q,
                         checkpoint_slots, checkpoints, workspace, workspace_bytes, stream, true);
 }
 
-kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, int32_t qkv_dtype,
-                      int32_t prologue, const void* q, const void* k, const void* v, const float* g,
-                      const float* beta, float* state, float* out, void* stream)
+kda_status kda_decode_gated(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, int32_t qkv_dtype,
+                            int32_t prologue, const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const float* gate, float* state, float* out, void* stream)
 {
     if (batch < 0 || num_heads < 1 || (prologue & ~KDA_PROLOGUE_ALL)) return KDA_ERR_INVALID_ARG;
     if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
@@ -287,19 +302,33 @@ kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, 
         if (overlaps(r_out, r) || overlaps(r_state, r)) return KDA_ERR_INVALID_ARG;
     }
     if (overlaps(r_out, r_state)) return KDA_ERR_INVALID_ARG;
+    if (gate) {
+        if (!aligned16(gate)) return KDA_ERR_INVALID_ARG;
+        const Range r_gate = range_of(gate, BH * dv * sizeof(float));
+        if (overlaps(r_gate, r_out) || overlaps(r_gate, r_state)) return KDA_ERR_INVALID_ARG;
+    }
 
     kda::DecodeArgs a;
     a.batch = batch; a.num_heads = num_heads; a.dk = dk; a.dv = dv; a.bf16 = qkv_dtype == KDA_BF16;
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state = state; a.out = out;
     a.prologue = prologue;
+    a.gate = gate;
     const cudaError_t e = kda::launch_decode(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-kda_status kda_decode_multi(int32_t batch, int32_t tokens, int32_t num_heads, int32_t dk, int32_t dv,
-                            int32_t qkv_dtype, int32_t prologue, const void* q, const void* k, const void* v,
-                            const float* g, const float* beta, const int32_t* n_apply, float* state, float* out,
-                            void* stream)
+kda_status kda_decode(int32_t batch, int32_t num_heads, int32_t dk, int32_t dv, int32_t qkv_dtype,
+                      int32_t prologue, const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, float* state, float* out, void* stream)
+{
+    return kda_decode_gated(batch, num_heads, dk, dv, qkv_dtype, prologue, q, k, v, g, beta, nullptr, state, out,
+                            stream);
+}
+
+kda_status kda_decode_multi_gated(int32_t batch, int32_t tokens, int32_t num_heads, int32_t dk, int32_t dv,
+                                  int32_t qkv_dtype, int32_t prologue, const void* q, const void* k, const void* v,
+                                  const float* g, const float* beta, const float* gate, const int32_t* n_apply,
+                                  float* state, float* out, void* stream)
 {
     if (batch < 0 || num_heads < 1 || tokens < 1 || tokens > KDA_DECODE_MULTI_MAX_TOKENS) return KDA_ERR_INVALID_ARG;
     if (prologue & ~KDA_PROLOGUE_ALL) return KDA_ERR_INVALID_ARG;
@@ -325,6 +354,12 @@ kda_status kda_decode_multi(int32_t batch, int32_t tokens, int32_t num_heads, in
         if (overlaps(r_out, r) || overlaps(r_state, r)) return KDA_ERR_INVALID_ARG;
     }
     if (overlaps(r_out, r_state)) return KDA_ERR_INVALID_ARG;
+    if (!out) gate = nullptr;
+    if (gate) {
+        if (!aligned16(gate)) return KDA_ERR_INVALID_ARG;
+        const Range r_gate = range_of(gate, BKH * dv * sizeof(float));
+        if (overlaps(r_gate, r_out) || overlaps(r_gate, r_state)) return KDA_ERR_INVALID_ARG;
+    }
     int* status = status_ptr_for_current_device();
     if (!status) return KDA_ERR_CUDA;
 
@@ -333,8 +368,18 @@ kda_status kda_decode_multi(int32_t batch, int32_t tokens, int32_t num_heads, in
     a.bf16 = qkv_dtype == KDA_BF16;
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.n_apply = n_apply;
     a.state = state; a.out = out; a.status = status; a.prologue = prologue;
+    a.gate = gate;
     const cudaError_t e = kda::launch_decode_multi(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_decode_multi(int32_t batch, int32_t tokens, int32_t num_heads, int32_t dk, int32_t dv,
+                            int32_t qkv_dtype, int32_t prologue, const void* q, const void* k, const void* v,
+                            const float* g, const float* beta, const int32_t* n_apply, float* state, float* out,
+                            void* stream)
+{
+    return kda_decode_multi_gated(batch, tokens, num_heads, dk, dv, qkv_dtype, prologue, q, k, v, g, beta, nullptr,
+                                  n_apply, state, out, stream);
 }
 
 kda_status kda_last_device_status(void* stream)

@@ -28,15 +28,27 @@ constexpr int kProQK = 1, kProG = 2, kProBeta = 4;
 constexpr float kGMin = -5.f;
 constexpr float kL2Eps = 1e-12f;
 __device__ __forceinline__ float sigmoid_f(float y) { return 1.f / (1.f + expf(-y)); }
-__device__ __forceinline__ float g_of(float g, int prologue) { return (prologue & kProG) ? kGMin * sigmoid_f(g) : g; }
-__device__ __forceinline__ float beta_of(float b, int prologue) { return (prologue & kProBeta) ? sigmoid_f(b) : b; }
-// x / max(||x||, eps) rounded to the storage type of q and k
-__device__ __forceinline__ float l2_scale(float x, float den, float) { return x / den; }
-__device__ __forceinline__ float l2_scale(float x, float den, __nv_bfloat16)
+// The same with the fast exponential and division (a few ulp of fp32 from the exact value;
+// 0 and 1 at the ends), for the prologue's parametrisations, which run on every g element
+// on the prefill's critical path.  Parity against the oracle's fp64 sigmoid is tested.
+__device__ __forceinline__ float sigmoid_fast(float y) { return __fdividef(1.f, 1.f + __expf(-y)); }
+__device__ __forceinline__ float g_of(float g, int prologue) { return (prologue & kProG) ? kGMin * sigmoid_fast(g) : g; }
+__device__ __forceinline__ float beta_of(float b, int prologue) { return (prologue & kProBeta) ? sigmoid_fast(b) : b; }
+// x / max(||x||, eps) as x times the row's reciprocal norm, rounded to the storage type of q and k
+__device__ __forceinline__ float l2_scale(float x, float inv, float) { return x * inv; }
+__device__ __forceinline__ float l2_scale(float x, float inv, __nv_bfloat16)
 {
-    return __bfloat162float(__float2bfloat16_rn(x / den));
+    return __bfloat162float(__float2bfloat16_rn(x * inv));
 }
-__device__ __forceinline__ float l2_den(float sumsq) { return fmaxf(sqrtf(sumsq), kL2Eps); }
+__device__ __forceinline__ float l2_inv(float sumsq) { return 1.f / fmaxf(sqrtf(sumsq), kL2Eps); }
+
+// Output gate (llm-atlas Q08, read as an elementwise sigmoid over the read-out channels):
+// o <- o * sigmoid(z) for 4 consecutive outputs and their logits (16-byte aligned).
+__device__ __forceinline__ float4 gate4(float4 o, const float* z)
+{
+    const float4 zz = __ldg(reinterpret_cast<const float4*>(z));
+    return make_float4(o.x * sigmoid_f(zz.x), o.y * sigmoid_f(zz.y), o.z * sigmoid_f(zz.z), o.w * sigmoid_f(zz.w));
+}
 
 // Read 4 consecutive elements starting at a 4-element-aligned index.
 __device__ __forceinline__ float4 load4(const float* p)

@@ -62,8 +62,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) kda_decode_kernel(DecodeArg
             for (int c = lane; c < D; c += 32) ss += x[c] * x[c];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float den = l2_den(ss);
-            for (int c = lane; c < D; c += 32) x[c] = l2_scale(x[c], den, Tin{});
+            const float inv = l2_inv(ss);
+            for (int c = lane; c < D; c += 32) x[c] = l2_scale(x[c], inv, Tin{});
         }
         __syncthreads();
     }
@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) kda_decode_kernel(DecodeArg
         }
         const float w = s_beta * (sv[t] - rs);
         sw[t] = w;
-        a.out[bh * D + t] = ps + s_kq * w;
+        const float o = ps + s_kq * w;
+        a.out[bh * D + t] = a.gate ? o * sigmoid_f(__ldg(a.gate + bh * D + t)) : o;
     }
     __syncthreads();
 

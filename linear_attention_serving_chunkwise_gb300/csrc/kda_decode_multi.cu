@@ -120,8 +120,8 @@ __device__ __forceinline__ void normalise_tokens(float* tokb, int K, int w, int 
         for (int c = lane; c < D; c += 32) ss += x[Lay::row(c)] * x[Lay::row(c)];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float den = l2_den(ss);
-        for (int c = lane; c < D; c += 32) x[Lay::row(c)] = l2_scale(x[Lay::row(c)], den, Tin{});
+        const float inv = l2_inv(ss);
+        for (int c = lane; c < D; c += 32) x[Lay::row(c)] = l2_scale(x[Lay::row(c)], inv, Tin{});
     }
 }
 
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(2 * D, 2) kda_decode_multi_kernel(DecodeMultiA
                                         base[3 * Lay::kVec + D]);
         if (a.out && rs == 0) {
             const size_t tok = ((size_t)b * K + j) * a.num_heads + h;
-            *reinterpret_cast<float4*>(a.out + tok * D + col) = o4;
+            *reinterpret_cast<float4*>(a.out + tok * D + col) = a.gate ? gate4(o4, a.gate + tok * D + col) : o4;
         }
         if (j + 1 == n_apply) {   // the state after the applied prefix
 #pragma unroll
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(2 * D, 2) kda_decode_multi_persistent_kernel(D
                                             base[3 * Lay::kVec + D]);
             if (a.out && rs == 0) {
                 const size_t tok = ((size_t)b * K + j) * H + h;
-                *reinterpret_cast<float4*>(a.out + tok * D + col) = o4;
+                *reinterpret_cast<float4*>(a.out + tok * D + col) = a.gate ? gate4(o4, a.gate + tok * D + col) : o4;
             }
             if (j + 1 == n_apply) {
 #pragma unroll

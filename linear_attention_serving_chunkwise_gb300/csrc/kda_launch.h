@@ -23,6 +23,7 @@ struct PrefillArgs {
     size_t workspace_bytes;
     int* status;  // device status word
     int prologue; // KDA_PROLOGUE_* bits
+    const float* gate;  // output gate logits [T, H, dv] (out = o * sigmoid(gate)), or nullptr
 };
 
 struct DecodeArgs {
@@ -32,6 +33,7 @@ struct DecodeArgs {
     const float *g, *beta;
     float *state, *out;
     int prologue; // KDA_PROLOGUE_* bits
+    const float* gate;  // output gate logits [B, H, dv], or nullptr
 };
 
 struct DecodeMultiArgs {
@@ -43,6 +45,7 @@ struct DecodeMultiArgs {
     float *state, *out;          // [B, H, dk, dv] in place; [B, K, H, dv] or nullptr
     int* status;                 // device status word
     int prologue;                // KDA_PROLOGUE_* bits
+    const float* gate;           // output gate logits [B, K, H, dv], or nullptr
 };
 
 // fp32 CUDA-core chunkwise prefill (any supported shape, fp32 or bf16 inputs)

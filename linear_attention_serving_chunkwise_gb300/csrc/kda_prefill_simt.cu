@@ -84,8 +84,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
                 for (int c = lane; c < D; c += 32) ss += x[c] * x[c];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                const float den = l2_den(ss);
-                for (int c = lane; c < D; c += 32) x[c] = l2_scale(x[c], den, Tin{});
+                const float inv = l2_inv(ss);
+                for (int c = lane; c < D; c += 32) x[c] = l2_scale(x[c], inv, Tin{});
             }
             __syncthreads();
         }
@@ -166,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
             float acc = 0.f;
             for (int c = 0; c < D; ++c) acc += sQ[r * D + c] * sS[c * kSlice + lane];
             for (int i = 0; i <= r; ++i) acc += sP[r * kAld + i] * sV[i * kSlice + lane];
-            a.out[((size_t)(c0 + r) * H + h) * D + js + lane] = acc;
+            const size_t oi = ((size_t)(c0 + r) * H + h) * D + js + lane;
+            a.out[oi] = a.gate ? acc * sigmoid_f(__ldg(a.gate + oi)) : acc;
         }
         // S <- Diag(exp Gamma_n) S + K~^T W
         float snew[D / kWarps];

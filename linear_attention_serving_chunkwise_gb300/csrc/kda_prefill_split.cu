@@ -60,7 +60,9 @@ constexpr uint32_t B_KTH = 66560;       // the back image (1024-byte aligned)
 constexpr uint32_t B_KTL = B_KTH + 16384;
 constexpr uint32_t B_V0 = 99328;        // v tiles [64 tok][128 ch] bf16, two buffers
 constexpr uint32_t B_V1 = 115712;
-constexpr uint32_t B_SB = 132096;       // S hi bf16, MN-major B [128 dk][128 dv]
+constexpr uint32_t B_SB = 132096;       // S hi bf16, MN-major B [128 dk][128 dv], until D1 has read it; then
+                                        // O staging: 4 x [64 tok][32 dv] fp32 boxes, 128-byte swizzle
+constexpr uint32_t B_OST = B_SB;
 constexpr uint32_t B_SL = 164864;       // S lo bf16, same layout, until D1 has read it; then:
 constexpr uint32_t B_WH = 164864;       // W hi bf16, MN-major B [64 tok][128 dv]
 constexpr uint32_t B_WL = 181248;       // W lo
@@ -433,7 +435,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         const uint32_t kg = kg_buf(li & 1);
         if (t < 64) {
             cp_async_wait_all();   // this item's beta; thread 0: the next item's entry
-            if ((pro & kProBeta) && t < BT) sbeta_buf(li & 1)[t] = sigmoid_f(sbeta_buf(li & 1)[t]);
+            if ((pro & kProBeta) && t < BT) sbeta_buf(li & 1)[t] = sigmoid_fast(sbeta_buf(li & 1)[t]);
         }
         if constexpr (kDyn) {
             if (t == 0) {
@@ -619,7 +621,10 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        {   // row L, K = dk columns [32 part, +32); the Q' rows' lo halves go to the image directly
+        {   // row L, K = dk columns [32 part, +32).  The Q' rows' lo halves are staged in this
+            // item's K_Gamma buffer, which the D2 MMA has finished reading (the next item's phase 1
+            // wrote the other one); the buffer's next writer runs after the next item's first
+            // bulk_wait_read, so the store below has left it by then.
             float a[32];
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D2 + 32 * part), a);
             tmem_wait_ld();
@@ -630,17 +635,18 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             for (int q = 0; q < 4; ++q)
                 st_shared_v4(sbase + A_STAGE + sw128_chunk(L, 4 * part + q, 128), pk[4 * q], pk[4 * q + 1],
                              pk[4 * q + 2], pk[4 * q + 3]);
-            fence_proxy_async_smem();
             if (quarter >= 2) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4*>(img + IMG_QLO + sw128_chunk(L - 64, 4 * part + q, 64)) =
-                        make_uint4(pl[4 * q], pl[4 * q + 1], pl[4 * q + 2], pl[4 * q + 3]);
+                    st_shared_v4(sbase + kg + sw128_chunk(L - 64, 4 * part + q, 64), pl[4 * q], pl[4 * q + 1],
+                                 pl[4 * q + 2], pl[4 * q + 3]);
             }
+            fence_proxy_async_smem();
         }
         __syncthreads();
-        if (t == kStorer) {
+        if (t == kStorer) {   // one bulk group, as the publication count expects three per item
             bulk_store(img + IMG_A1, sm + A_STAGE, 32768);
+            bulk_store(img + IMG_QLO, sm + kg, 16384);
             bulk_commit();
         }
         cur = nxt;   // the next item's first barrier orders these TMEM reads before its writes
@@ -759,6 +765,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         mbar_fence_init();
         *s_abort = 0;
         tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_o);
     }
     // rows 0-63 of the [0; Q' lo] operand: zeros in both K blocks, written once
     st_shared_v4(sbase + B_A1L + ((t >> 8) << 14) + 16 * (t & 255), 0u, 0u, 0u, 0u);
@@ -770,9 +777,11 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
 
     // The copies into shared memory are issued by one producer thread (kProducer, in a warp
     // of the O half, which has slack when they are due); it counts what it issued so that,
-    // on abort, it can wait for the last copy on each barrier.  Thread 0 issues the MMAs.
+    // on abort, it can wait for the last copy on each barrier.  It also issues the O stores,
+    // once the O warps have staged them.  Thread 0 issues the MMAs.
     constexpr int kProducer = 64;
-    bool mma_open = false;   // thread 0
+    bool o_pending = false;   // producer
+    bool mma_open = false;    // thread 0
     int n_front = 0, n_back = 0, n_v[2] = {0, 0};   // producer
     auto fetch_front = [&](int c) {
         if (!ready(c)) {   // never published: give up (the waits on bar_f then run out)
@@ -838,6 +847,10 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         const int BT = min(64, eos - t0);
         const int vb = ci & 1;
         if (!mbar_wait_bounded(bar_f, f_par, kWaitNs)) atomicExch(s_abort, 1);
+        if (t == kProducer && o_pending) {   // the previous chunk's O staging (over S hi) has been read out
+            bulk_wait_read();
+            o_pending = false;
+        }
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
@@ -847,32 +860,13 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         }
         f_par ^= 1u;
 
-        // the state's bf16 hi and lo B operands; S <- gamma_C S (this chunk's decay, before its
-        // update) runs while the D1 MMAs, which read only the bf16 copies, execute
-        float a[32];
-        tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), a);
-        tmem_wait_ld();
-        {
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                st_shared_v4(sbase + B_SB + sw128_chunk(L, 4 * part + q, 128), hi[4 * q], hi[4 * q + 1],
-                             hi[4 * q + 2], hi[4 * q + 3]);
-                st_shared_v4(sbase + B_SL + sw128_chunk(L, 4 * part + q, 128), lo[4 * q], lo[4 * q + 1],
-                             lo[4 * q + 2], lo[4 * q + 3]);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-
-        // D1 = [Tb; M] V (hi + lo) + [-Wk; Q'] S_hi + [-Wk; Q'] S_lo + [0; Q' lo] S_hi
+        // D1 = [Tb; M] V (hi + lo), the half that does not depend on the state, at once
+        bool v_ok = true;   // thread 0
         if (t == 0) {
             tc_fence_after_sync();
             if (!mbar_wait_bounded(bar_v + vb, (v_par >> vb) & 1u, kWaitNs)) {
                 atomicExch(s_abort, 1);
+                v_ok = false;
             } else {
                 v_par ^= 1u << vb;
                 const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
@@ -884,17 +878,58 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_TBL, 128, ks), desc_mnmajor(vt, 64, ks), idesc, 1u);
+                mma_open = true;
+            }
+        }
+
+        // the state's bf16 B operands: S_hi first, so that the MMAs that read it start while
+        // S_lo = bf16(S - S_hi) is formed; S <- gamma_C S (this chunk's decay, before its update)
+        // then runs while the D1 MMAs, which read only the bf16 copies, execute
+        float a[32];
+        tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), a);
+        tmem_wait_ld();
+        uint32_t hi[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) hi[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+        store_row32_bf16(sbase + B_SB, L, 4 * part, 128, hi);
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+        // D1 += [-Wk; Q'] S_hi + [0; Q' lo] S_hi
+        if (t == 0) {
+            tc_fence_after_sync();
+            if (v_ok) {
+                const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_A1, 128, ks), desc_mnmajor(sbase + B_SB, 128, ks),
                               idesc, 1u);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_A1, 128, ks), desc_mnmajor(sbase + B_SL, 128, ks),
+                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_A1L, 128, ks), desc_mnmajor(sbase + B_SB, 128, ks),
                               idesc, 1u);
+            }
+        }
+        {
+            uint32_t lo[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float2 h2 = bf2_to_f2(hi[i]);
+                lo[i] = pack_bf16x2(a[2 * i] - h2.x, a[2 * i + 1] - h2.y);
+            }
+            store_row32_bf16(sbase + B_SL, L, 4 * part, 128, lo);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+        // D1 += [-Wk; Q'] S_lo
+        if (t == 0) {
+            tc_fence_after_sync();
+            if (v_ok) {
+                const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_A1L, 128, ks), desc_mnmajor(sbase + B_SB, 128, ks),
+                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_A1, 128, ks), desc_mnmajor(sbase + B_SL, 128, ks),
                               idesc, 1u);
                 umma_commit(bar_mma);
                 mma_open = true;
@@ -920,7 +955,8 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         }
 
         // rows 0-63 -> W (hi + lo) B operands (over S lo, which D1 has read), and S += K~^T W as
-        // soon as the 8 warps holding them are done; rows 64-127 = O, stored meanwhile
+        // soon as the 8 warps holding them are done; rows 64-127 = O staged (over S hi) for TMA
+        // stores meanwhile
         tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_D1 + 32 * part), a);
         tmem_wait_ld();
         if (quarter < 2) {
@@ -954,10 +990,32 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
                     mma_open = true;
                 }
             }
-        } else {   // O row r = token t0 + r, dv columns [32 part, +32): 128 contiguous bytes
+        } else {   // O row r = token t0 + r, dv columns [32 part, +32)
             const int r = L - 64;
-            if (r < BT) {
-                float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)(t0 + r) * H + h) * 128 + 32 * part);
+            const size_t o0 = ((size_t)(t0 + r) * H + h) * 128 + 32 * part;
+            if (p.gate && r < BT) {   // the output gate, o * sigmoid(z)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 o = gate4(make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]),
+                                           p.gate + o0 + 4 * i);
+                    a[4 * i] = o.x; a[4 * i + 1] = o.y; a[4 * i + 2] = o.z; a[4 * i + 3] = o.w;
+                }
+            }
+            if (BT == 64) {   // box `part` = dv columns [32 part, +32)
+                const uint32_t box = sbase + B_OST + 8192 * part;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_shared_f4(box + sw128_off_f32(r, 4 * q, 64), a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+                fence_proxy_async_smem();
+                named_sync(3, 256);   // the 8 O warps: the boxes are complete
+                if (t == kProducer) {   // stored now, so that they are read out before the next S build
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) tma_store_3d(&p.tm_o, sm + B_OST + 8192 * j, 32 * j, h, t0);
+                    bulk_commit();
+                    o_pending = true;
+                }
+            } else if (r < BT) {   // a sequence's ragged last chunk: direct stores
+                float4* dst = reinterpret_cast<float4*>(p.out + o0);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
             }
@@ -984,6 +1042,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         }
     }
 
+    if (t == kProducer) bulk_wait_all();   // staged O fully written before the CTA's shared memory goes away
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -1149,6 +1208,7 @@ cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream)
     p.num_heads = a.num_heads;
     p.status = a.status;
     p.prologue = a.prologue;
+    p.gate = a.gate;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     const SplitWorkspace wl = split_workspace(a.num_seqs, a.total_tokens, a.num_heads);
     sp.chunk_off = reinterpret_cast<int32_t*>(ws);

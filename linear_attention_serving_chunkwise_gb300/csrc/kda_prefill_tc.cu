@@ -322,8 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
-        // ---- phase 5b: D1 += [-Wk; Q'] S_hi + [-Wk; Q'] S_lo + [0; Q' lo] S_hi (the [Tb; M] V half
-        // was queued in phase 4)
+        // ---- phase 5b: D1 += [-Wk; Q'] S_hi + [0; Q' lo] S_hi + [-Wk; Q'] S_lo (the [Tb; M] V half
+        // was queued in phase 4; the order is the chunk-parallel scan's)
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
@@ -333,10 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1 + 8 * ks, desc_mnmajor(sh, 128, ks), idesc, 1u);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1 + 8 * ks, desc_mnmajor(sl, 128, ks), idesc, 1u);
+                umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1L + 8 * ks, desc_mnmajor(sh, 128, ks), idesc, 1u);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1L + 8 * ks, desc_mnmajor(sh, 128, ks), idesc, 1u);
+                umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1 + 8 * ks, desc_mnmajor(sl, 128, ks), idesc, 1u);
             umma_commit(bar_mma);
             mma_open = false;
         }
@@ -383,6 +383,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             float a[32];
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 32 * part), a);
             tmem_wait_ld();
+            if (p.gate && r < BT) {   // the output gate, o * sigmoid(z)
+                const float* z = p.gate + ((size_t)(t0 + r) * H + h) * 128 + 32 * part;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 o = gate4(make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]), z + 4 * i);
+                    a[4 * i] = o.x; a[4 * i + 1] = o.y; a[4 * i + 2] = o.z; a[4 * i + 3] = o.w;
+                }
+            }
             if (BT == 64) {
                 // stage in 128-byte-swizzled [64 tok][32] fp32 boxes, one TMA store per box:
                 // boxes 0-1 in the free top of the X region, 2-3 in this chunk's v buffer
@@ -480,6 +488,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream)
     p.num_heads = a.num_heads;
     p.status = a.status;
     p.prologue = a.prologue;
+    p.gate = a.gate;
     auto kern = a.prologue ? kda_prefill_tc_kernel<true> : kda_prefill_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;

@@ -96,6 +96,7 @@ struct TcParams {
     int num_seqs, total_tokens, num_heads;
     int* status;
     int prologue;   // KDA_PROLOGUE_* bits
+    const float* gate;   // output gate logits [T, H, 128]: out = o * sigmoid(gate); nullptr = none
 };
 
 __device__ __forceinline__ float ex2f(float x)
@@ -274,7 +275,7 @@ __device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, in
 // The prologue's L2 normalisation of the q and k tiles in place (512 threads): thread t
 // takes row t / 4 of [k; q] (token r = that row mod 64) and channels [32 (t % 4), +32), the
 // row's sum of squares closing over the 4 neighbouring lanes; x / max(||x||, 1e-12) in fp32
-// goes back as bf16.
+// (x times the reciprocal norm) goes back as bf16.
 __device__ __forceinline__ void phase0_normalise_qk(uint8_t* sm, int t)
 {
     const int row = t >> 2, qtr = t & 3, r = row & 63;
@@ -292,12 +293,12 @@ __device__ __forceinline__ void phase0_normalise_qk(uint8_t* sm, int t)
     for (int e = 0; e < 32; ++e) ss = fmaf(x[e], x[e], ss);
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-    const float den = l2_den(ss);
+    const float inv = l2_inv(ss);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(x[8 * i + 2 * e] / den, x[8 * i + 2 * e + 1] / den);
+        for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(x[8 * i + 2 * e] * inv, x[8 * i + 2 * e + 1] * inv);
         st_shared_v4(tile + sw128_chunk(r, 4 * qtr + i, 64), w[0], w[1], w[2], w[3]);
     }
 }

@@ -12,6 +12,7 @@ from .kda_ref import (  # noqa: F401
     delta_invariant_keys,
     rel_err,
     prologue,
+    output_gate,
     sigmoid64,
     l2_normalise64,
     PROLOGUE_QK_L2NORM,

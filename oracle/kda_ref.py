@@ -249,6 +249,17 @@ def prologue(inputs: dict, flags: int) -> dict:
     return out
 
 
+def output_gate(out, z) -> np.ndarray:
+    """The output gate: o * sigmoid(z) elementwise over the read-out channels, in fp64.
+
+    llm-atlas "K3_RESEARCH.md", question ledger Q08: KDA's output gate is input-dependent and
+    full-rank over the read-out channels; the pages give no formula.  Read here as an
+    elementwise sigmoid gate on the fp32 attention output o (the recurrence's o_t = S_t^T q_t),
+    with the logits z of the same shape supplied by the caller (their projection is outside
+    the attention).  The state is not touched."""
+    return _f64(out) * sigmoid64(_f64(z))
+
+
 def delta_invariant_keys(dk: int, n: int, seed: int = 0) -> np.ndarray:
     """n <= dk orthonormal keys (rows), from a QR factorisation of a seeded Gaussian matrix."""
     rng = np.random.default_rng(seed)

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.kda_abi_version() == kda.KDA_ABI_VERSION == 2
+    assert lib.kda_abi_version() == kda.KDA_ABI_VERSION == 3
     for code in (0, -1, -2, -3, -4, -5):
         assert kda.status_string(code).startswith("KDA")
     assert "unknown" in kda.status_string(-99)
@@ -235,3 +235,27 @@ def test_decode_multi_rejects_bad_arguments_on_host(lib):
     assert call(B=0) == kda.KDA_OK
     assert call(pro=-1) == kda.KDA_ERR_INVALID_ARG                 # unknown prologue bits
     assert call(B=0, pro=kda.KDA_PROLOGUE_ALL) == kda.KDA_OK
+
+
+def test_gated_entry_points_reject_bad_gates_on_host(lib):
+    """The output gate's pointer is checked like the other inputs before anything runs:
+    16-byte alignment, and no overlap with out, final_state or the state."""
+    d = kda.make_desc(1, 64, 2, 64, 64, kda.KDA_F32)
+    p = _fake
+    args = lambda gate, out=0x60000, fin=None: (ctypes.byref(d), p(0x10000), p(0x20000), p(0x30000), p(0x40000),
+                                                 p(0x50000), None if gate is None else p(gate), None, None, p(out),
+                                                 None if fin is None else p(fin), None, 0, None)
+    assert lib.kda_prefill_gated(*args(0x70008)) == kda.KDA_ERR_INVALID_ARG            # misaligned
+    assert lib.kda_prefill_gated(*args(0x60000 + 256)) == kda.KDA_ERR_INVALID_ARG      # inside out
+    assert lib.kda_prefill_gated(*args(0x80000, fin=0x80000)) == kda.KDA_ERR_INVALID_ARG
+    # decode: B=2, H=2, d=64 fp32; out at 0x60000 (1 KB), state at 0x90000 (64 KB)
+    dec = lambda gate: lib.kda_decode_gated(2, 2, 64, 64, kda.KDA_F32, 0, p(0x10000), p(0x20000), p(0x30000),
+                                            p(0x40000), p(0x50000), p(gate), p(0x90000), p(0x60000), None)
+    assert dec(0x70004) == kda.KDA_ERR_INVALID_ARG
+    assert dec(0x60000) == kda.KDA_ERR_INVALID_ARG
+    assert dec(0x90000 + 4096) == kda.KDA_ERR_INVALID_ARG
+    mul = lambda gate: lib.kda_decode_multi_gated(2, 3, 2, 64, 64, kda.KDA_F32, 0, p(0x10000), p(0x20000),
+                                                  p(0x30000), p(0x40000), p(0x50000), p(gate), None, p(0x90000),
+                                                  p(0x60000), None)
+    assert mul(0x70004) == kda.KDA_ERR_INVALID_ARG
+    assert mul(0x60000 + 512) == kda.KDA_ERR_INVALID_ARG

@@ -353,3 +353,49 @@ def test_rel_err_hand_worked_values():
     assert rel_err(np.array([0.0, 0.25, -0.5]), np.zeros(3)) == 0.5
     assert rel_err(np.zeros(0), np.zeros(0)) == 0.0
     assert rel_err(ref2, ref2) == 0.0
+
+
+def test_output_gate_closed_forms():
+    """The oracle's output gate o * sigmoid(z) at points where sigmoid is known exactly:
+    z = 0 halves o, z = ln 3 gives 3/4, z = +-1e4 gives o and 0, sigmoid(z) + sigmoid(-z) = 1,
+    and it acts channel by channel.  Catches tanh for sigmoid, a sign flip of z, o and z
+    swapped, or a reduction over the channels."""
+    rng = np.random.default_rng(41)
+    o = rng.standard_normal((5, 3, 16))
+    z = rng.standard_normal((5, 3, 16))
+    assert np.array_equal(oracle.output_gate(o, np.zeros_like(o)), 0.5 * o)
+    assert np.max(np.abs(oracle.output_gate(o, np.full_like(o, np.log(3.0))) - 0.75 * o)) < 1e-15
+    assert np.array_equal(oracle.output_gate(o, np.full_like(o, 1e4)), o)
+    assert np.array_equal(oracle.output_gate(o, np.full_like(o, -1e4)), np.zeros_like(o))
+    assert np.max(np.abs(oracle.output_gate(o, z) + oracle.output_gate(o, -z) - o)) < 1e-15
+    z2 = z.copy()
+    z2[2, 1, 7] += 3.0
+    diff = oracle.output_gate(o, z2) != oracle.output_gate(o, z)
+    assert diff.sum() == 1 and diff[2, 1, 7]
+
+
+def test_range_transition_and_split_identity():
+    """Context-parallel prefill rests on the recurrence being affine in its initial state: a
+    token range maps the state entering it to M S + S_r.  M, the state after the range from
+    S_0 = I with v = 0, equals the explicit product of the per-token transitions
+    (I - beta_t k_t k_t^T) Diag(e^{g_t}) (written out here, T = 7); and splitting a sequence at
+    any token, then combining, reproduces the one-shot final state and the later outputs."""
+    dk = 6
+    q, k, v, g, beta, _ = _rand_case(7, dk, dk, 31, g_scale=1.0)
+    eye = np.eye(dk, dtype=np.float32)
+    _, M = _run1(q, k, np.zeros_like(v), g, beta, eye)
+    P = np.eye(dk)
+    for t in range(7):
+        kt = k[t].astype(np.float64)
+        P = (np.eye(dk) - float(beta[t]) * np.outer(kt, kt)) @ np.diag(np.exp(g[t].astype(np.float64))) @ P
+    assert np.max(np.abs(M - P)) < 1e-12
+    q, k, v, g, beta, S0 = _rand_case(40, 8, 8, 32, g_scale=0.5)
+    o_full, f_full = _run1(q, k, v, g, beta, S0)
+    eye8, zv = np.eye(8, dtype=np.float32), np.zeros_like(v)
+    for m in (1, 17, 39):
+        _, S_m = _run1(q[:m], k[:m], v[:m], g[:m], beta[:m], S0)
+        _, M = _run1(q[m:], k[m:], zv[m:], g[m:], beta[m:], eye8)
+        _, S_r = _run1(q[m:], k[m:], v[m:], g[m:], beta[m:], None)
+        assert rel_err(M @ S_m + S_r, f_full) < 1e-12
+        o_tail, _ = _run1(q[m:], k[m:], v[m:], g[m:], beta[m:], S_m.astype(np.float32))
+        assert rel_err(o_tail, o_full[m:]) < 1e-6   # S_m re-enters as fp32
