@@ -40,6 +40,10 @@ import kda_workloads as W  # noqa: E402
 METRIC = "KDA prefill tokens/s (×tensor-peak %) and decode state GB/s (×HBM-peak %), 1 GB300"
 UNIT = "tokens/s"
 E2E_SEGMENT_TOKENS = 1024
+# GB300's nominal HBM3e bandwidth.  The roofline's `peak` is the measured copy bandwidth (a
+# plain copy reaches less than a read-modify-write stream does, so a kernel can pass it); each
+# roofline object also carries its fraction of this nominal figure.
+NOMINAL_HBM_GBS = 7900.0
 # the kernels one bench-size kda_prefill call runs (the chunk-parallel split path)
 PREFILL_KERNEL_SRC = ("linear_attention_serving_chunkwise_gb300/csrc/kda_prefill_split.cu",
                       "linear_attention_serving_chunkwise_gb300/csrc/kda_prefill_tc_phases.cuh",
@@ -91,6 +95,25 @@ def _src_hash(paths):
     return h.hexdigest()[:16]
 
 
+def _profiled_tensor_pipe(src_hash: str):
+    """Tensor-pipe activity of the chunk prep (sm__pipe_tensor_cycles_active, percent of the
+    kernel's cycles) recorded by an ncu capture under profiles/, if taken on the current
+    kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "kda_prefill_tensor_pipe.txt")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
+    if not m_hash or m_hash.group(1) != src_hash:
+        return None
+    out = {}
+    for key in ("prep_pct", "scan_pct", "prep_scan_pct"):
+        m = re.search(key + r":\s*([0-9.]+)", txt)
+        if m:
+            out[key] = float(m.group(1))
+    return out or None
+
+
 def _profiled_traffic(kernel_tag: str, src_hash: str):
     """dram bytes per launch recorded by an ncu capture under profiles/, if the
     capture was taken on the current kernel source; else None."""
@@ -106,14 +129,19 @@ def _profiled_traffic(kernel_tag: str, src_hash: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock/throttle samples (every 20 ms, each with its timestamp) from before the
+    first timed leg to after the last.  Each timed leg marks its window (host wall clock from
+    the synchronize before its first event to the synchronize after its last), and only the
+    samples inside a window count: between legs the GPU idles while the host sets up."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
+        self.windows = []   # (leg, t0, t1), host wall clock
         self.path = os.path.join(tempfile.gettempdir(), f"kda_clocks_bench_{os.getpid()}.csv")
 
     def start(self):
@@ -121,10 +149,21 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def window(self, leg: str, t0: float, t1: float):
+        self.windows.append((leg, t0, t1))
+
+    @staticmethod
+    def _stamp(txt: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(txt.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self):
         if self.proc is None:
@@ -135,22 +174,29 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons, per_leg, total = [], [], set(), {}, 0
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
+                continue
+            total += 1
+            ts = self._stamp(f[0])
+            legs = [w[0] for w in self.windows if ts is not None and w[1] <= ts <= w[2]]
+            if not legs:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                sm.append(float(f[2]))
+                smax.append(float(f[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            per_leg[legs[0]] = per_leg.get(legs[0], 0) + 1
+            for n, v in zip(self.NAMES, f[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "sm_mhz_min": min(sm) if sm else None, "reasons": sorted(reasons), "samples": len(sm),
+                "samples_per_leg": per_leg, "samples_total": total, "interval_ms": 20,
+                "legs": [w[0] for w in self.windows]}
 
 
 # --------------------------------------------------------------------------- distributed plumbing
@@ -261,7 +307,9 @@ def run_cuda(args, world, rank, local):
     _barrier(world)
     torch.cuda.synchronize()
     sampler = ClockSampler(torch.cuda.current_device())
-    sampler.start()
+    sampler.start()   # runs until the last leg; only samples inside the legs' windows count
+    time.sleep(0.1)
+    w0 = time.time()
     start.record(stream)
     for i in range(args.steps):
         evs[i][0].record(stream)
@@ -269,7 +317,7 @@ def run_cuda(args, world, rank, local):
         evs[i][1].record(stream)
     end.record(stream)
     stream.synchronize()
-    clocks = sampler.stop()
+    sampler.window("prefill", w0, time.time())
     torch.cuda.synchronize()
     _barrier(world)
     if kda.last_device_status(stream) != kda.KDA_OK:
@@ -287,6 +335,7 @@ def run_cuda(args, world, rank, local):
     traffic = _profiled_traffic("kda_prefill", src_hash)
     roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                "frac_of_nominal": achieved_gbs / NOMINAL_HBM_GBS, "nominal_gbs": NOMINAL_HBM_GBS,
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
                 "algorithmic_bytes_per_launch": alg_bytes, "kernel_launches_per_call": plan["kernel_launches"],
                 "launch_ms": launch_ms,
@@ -296,7 +345,11 @@ def run_cuda(args, world, rank, local):
                 "workspace_bytes": plan["workspace_bytes"]}
     tensor = {"achieved": achieved_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
               "frac": achieved_tflops / peaks["bf16_tflops"], "algorithmic_flops_per_launch": alg_flops,
-              "uses_tensor_cores": bool(plan["tensor_cores"])}
+              "uses_tensor_cores": bool(plan["tensor_cores"]),
+              "pipe_active_pct_ncu": _profiled_tensor_pipe(src_hash),
+              "pipe_target_pct": 50.0,
+              "pipe_note": "sm__pipe_tensor_cycles_active of the intra-chunk MMA kernels (ncu, small case, "
+                           "profiles/kda_prefill_tensor_pipe.txt); null when the capture is not of this source"}
 
     # ---------------- end to end: kda_prefill_host from pinned host inputs to pinned host
     # outputs (out + final state), every step; the library pipelines the copies over
@@ -322,11 +375,13 @@ def run_cuda(args, world, rank, local):
     stream.synchronize()
     _barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
     e0.record(stream)
     for _ in range(e2e_steps):
         e2e_step()
     e1.record(stream)
     stream.synchronize()
+    sampler.window("e2e", w0, time.time())
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
     e2e = {"value": tokens_per_step / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
@@ -343,11 +398,13 @@ def run_cuda(args, world, rank, local):
     stream.synchronize()
     devs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dcfg.steps)]
     _barrier(world)
+    w0 = time.time()
     for s in range(dcfg.steps):
         devs[s][0].record(stream)
         kda.decode(dd["q"][s], dd["k"][s], dd["v"][s], dd["g"][s], dd["beta"][s], state, out=dout, stream=stream)
         devs[s][1].record(stream)
     stream.synchronize()
+    sampler.window("decode", w0, time.time())
     dstep_ms = float(np.mean([a.elapsed_time(b) for a, b in devs]))
     dstep_ms = _max_over_ranks(dstep_ms, world)
     state_bytes, all_bytes = decode_algorithmic(dcfg)
@@ -357,6 +414,7 @@ def run_cuda(args, world, rank, local):
               "all_bytes_gbs": all_bytes / (dstep_ms / 1e3) / 1e9,
               "roofline": {"bound": "hbm", "achieved": all_bytes / (dstep_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                            "unit": "GB/s", "frac": all_bytes / (dstep_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                           "frac_of_nominal": all_bytes / (dstep_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
                            "traffic": _profiled_traffic("kda_decode", _src_hash(
                                ("linear_attention_serving_chunkwise_gb300/csrc/kda_decode.cu",))),
                            "algorithmic_bytes_per_launch": all_bytes},
@@ -375,11 +433,13 @@ def run_cuda(args, world, rank, local):
     stream.synchronize()
     _barrier(world)
     m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
     m0.record(stream)
     for _ in range(mcalls):
         kda.decode_multi(mx["q"], mx["k"], mx["v"], mx["g"], mx["beta"], mstate, out=mout, stream=stream)
     m1.record(stream)
     stream.synchronize()
+    sampler.window("decode_multi", w0, time.time())
     mcall_ms = _max_over_ranks(m0.elapsed_time(m1) / mcalls, world)
     e_in = 2 if dcfg.qkv_dtype == torch.bfloat16 else 4
     per_head_token = e_in * (2 * dcfg.dk + dcfg.dv) + 4 * dcfg.dk + 4 + 4 * dcfg.dv
@@ -391,6 +451,7 @@ def run_cuda(args, world, rank, local):
                     "roofline": {"bound": "hbm", "achieved": m_bytes / (mcall_ms / 1e3) / 1e9,
                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                  "frac": m_bytes / (mcall_ms / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                                 "frac_of_nominal": m_bytes / (mcall_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
                                  "algorithmic_bytes_per_launch": m_bytes},
                     "gpu_launches": mcalls}
     del mm, mx, mstate, mout
@@ -413,11 +474,13 @@ def run_cuda(args, world, rank, local):
         stream.synchronize()
         p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         _barrier(world)
+        w0 = time.time()
         p0.record(stream)
         for _ in range(args.steps):
             pro_call()
         p1.record(stream)
         stream.synchronize()
+        sampler.window("prologue", w0, time.time())
         if kda.last_device_status(stream) != kda.KDA_OK:
             raise RuntimeError("prefill with the prologue reported a device error")
         pro_ms = _max_over_ranks(p0.elapsed_time(p1) / args.steps, world)
@@ -426,11 +489,13 @@ def run_cuda(args, world, rank, local):
                          "roofline": {"bound": "hbm", "achieved": alg_bytes / (pro_ms / 1e3) / 1e9,
                                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": alg_bytes / (pro_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                      "frac_of_nominal": alg_bytes / (pro_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
                                       "traffic": None, "algorithmic_bytes_per_launch": alg_bytes},
                          "gpu_launches": args.steps * plan["kernel_launches"]})
         del draw, rargs, pws
     except Exception as exc:   # noqa: BLE001 -- recorded in the line instead of ending the run
         prologue["error"] = f"{type(exc).__name__}: {exc}"
+    clocks = sampler.stop()
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -455,6 +520,8 @@ def run_ncu_case(case: str):
     as the bench on inputs still larger than L2 but only a few hundred MB on the device.
       prefill: B=1, H=32, T=8192, dk=dv=128, bf16 (470 MB of inputs/outputs; the
                chunk-parallel path: chunk offsets, then the cooperative prep-and-scan kernel)
+      prefill_sep: 2 sequences of 4096 tokens, H=64 (128 units: the chunk-parallel path as
+               separate chunk-prep and state-scan launches, so each can be captured alone)
       prefill_one_cta: 4 sequences of 2048 tokens, H=38 (152 units, one full wave: one CTA
                per (sequence, head))
       decode:  B=64, H=96, dk=dv=128, bf16, one step (403 MB of state)
@@ -466,6 +533,14 @@ def run_ncu_case(case: str):
     if case == "prefill":
         cfg = W.PrefillConfig("ncu_prefill_h32_t8192", (8192,), 32, 128, 128, torch.bfloat16, "normal")
         d = W.make_prefill_inputs(cfg, seed=0, device="cuda")
+        for _ in range(2):
+            kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])
+    elif case == "prefill_sep":
+        cfg = W.PrefillConfig("ncu_prefill_sep_2x4096_h64", (4096,) * 2, 64, 128, 128, torch.bfloat16, "normal")
+        d = W.make_prefill_inputs(cfg, seed=0, device="cuda")
+        plan = kda.prefill_query(kda.make_desc(2, 8192, 64, 128, 128, kda.KDA_BF16))
+        if plan["kernel_launches"] != 3:
+            raise SystemExit(f"prefill_sep expected the separate launches, got {plan}")
         for _ in range(2):
             kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])
     elif case == "prefill_one_cta":
@@ -497,7 +572,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--ncu-case", default=None, choices=["prefill", "prefill_one_cta", "decode", "decode_multi"],
+    ap.add_argument("--ncu-case", default=None,
+                    choices=["prefill", "prefill_sep", "prefill_one_cta", "decode", "decode_multi"],
                     help="run one small launch pair for an ncu capture and exit")
     args = ap.parse_args()
     if args.ncu_case:
