@@ -2,6 +2,9 @@
 
 ``python -m linear_attention_serving_chunkwise_gb300.build`` or ``build()`` compiles each
 ``csrc/*.cu`` translation unit in parallel and links ``libkda_gb300.so`` beside this file.
+``build(phase_clocks=True)`` builds a separate instrumented library,
+``libkda_gb300_clocks.so``, with the per-phase cycle marks compiled in (see phase_clocks.py);
+the library everything else loads never has them.
 """
 from __future__ import annotations
 
@@ -16,6 +19,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkda_gb300.so")
+OBJ_CLOCKS = os.path.join(PKG, "_build_clocks")
+LIB_CLOCKS = os.path.join(PKG, "libkda_gb300_clocks.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -39,25 +44,28 @@ def _deps():
         [os.path.join(os.path.dirname(PKG), "include", "kda.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, phase_clocks: bool = False) -> str:
+    lib_path, obj_dir = (LIB_CLOCKS, OBJ_CLOCKS) if phase_clocks else (LIB, OBJ)
+    if not force and up_to_date(lib_path):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(OBJ, exist_ok=True)
+    os.makedirs(obj_dir, exist_ok=True)
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                      "--expt-relaxed-constexpr", "-I", os.path.join(os.path.dirname(PKG), "include")]
+    if phase_clocks:
+        common += ["-DKDA_PHASE_CLOCKS"]
     if ptxas_v:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc] + common + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0 or verbose or ptxas_v:
@@ -69,14 +77,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(_sources()))) as ex:
         objs = list(ex.map(compile_one, _sources()))
     libdir = _cuda_lib_dir(nvcc)
-    cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", LIB + ".tmp"] + objs + \
+    cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", lib_path + ".tmp"] + objs + \
         ["-Xlinker", f"-rpath,{libdir}", "-L", libdir]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("linking libkda_gb300.so failed")
-    os.replace(LIB + ".tmp", LIB)
-    return LIB
+        raise RuntimeError(f"linking {os.path.basename(lib_path)} failed")
+    os.replace(lib_path + ".tmp", lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -52,20 +52,20 @@ bool uses_tensor_cores(const kda_prefill_desc& d)
 
 // Which tensor-core path a bf16, dk = dv = 128 call takes, from its shape alone.  One CTA per
 // (sequence, head) unit walks that unit's chunks; with U units on the GB300's 152 SMs that is
-// ceil(U / 152) waves of about 22.7 K cycles per chunk.  The chunk-parallel split runs the
-// state-independent work of every (chunk, head) item on all SMs (about 19.2 K cycles per
-// item) and then the state scan, again in ceil(U / 152) waves but of about 6.0 K cycles per
+// ceil(U / 152) waves of about 25.8 K cycles per chunk.  The chunk-parallel split runs the
+// state-independent work of every (chunk, head) item on all SMs (about 19.8 K cycles per
+// item) and then the state scan, again in ceil(U / 152) waves but of about 7.2 K cycles per
 // chunk, plus a fixed 10 K cycles (the extra launch, the pipeline's fill); its workspace
 // holds 115,200 bytes per item, at most kSplitMaxItems of them.  The split is taken when its
-// estimate is lower.  For 8192-token sequences that is up to 130 units (measured: 1.17 ms at
-// 112 units, 1.25 at 120 and 1.36 at 128, against 1.41 ms for one CTA per unit; 1.44 at
-// 136), and again from 153 units to the item cap, where one CTA per unit would run a mostly
-// idle second wave (192 units: 2.24 against 2.80 ms; 240: 2.61 against 2.81 ms).
+// estimate is lower.  For 8192-token sequences that is up to about 140 units (measured: 1.10 ms
+// at 96 units and 1.46 ms at 124 with the split, 1.59 ms at 136 with one CTA per unit), and
+// again from 153 units to the item cap, where one CTA per unit would run a mostly idle second
+// wave.
 constexpr long long kGpuSMs = 152;
 constexpr long long kSplitMaxItems = 32768;
-constexpr long long kCyclesPerChunkOneCta = 227;     // hundreds of cycles
-constexpr long long kCyclesPerItemPrep = 192;
-constexpr long long kCyclesPerChunkScan = 60;
+constexpr long long kCyclesPerChunkOneCta = 258;     // hundreds of cycles
+constexpr long long kCyclesPerItemPrep = 198;
+constexpr long long kCyclesPerChunkScan = 72;
 constexpr long long kCyclesSplitFixed = 100;
 
 bool uses_split(const kda_prefill_desc& d)

@@ -83,8 +83,8 @@ constexpr uint32_t B_TM_COLS = 256;
 // the prep's 19.4 K per item less an allowance for the scans' start and flag waits, tuned
 // at 64 and 96 units)
 constexpr long long kSingleMinProducers = 32;
-constexpr long long kScanCyclesPerChunk = 6000;
-constexpr long long kPrepCyclesPerItem = 18400;
+constexpr long long kScanCyclesPerChunk = 7200;
+constexpr long long kPrepCyclesPerItem = 18800;
 
 static_assert(B_KTH % 1024 == 0 && B_V0 % 1024 == 0 && B_SB % 1024 == 0 && B_WH % 1024 == 0, "tile alignment");
 static_assert(B_KTH >= IMG_FRONT && B_V0 >= B_KTH + IMG_BACK && B_V1 == B_V0 + 16384 && B_SB >= B_V1 + 16384 &&
@@ -425,6 +425,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         return true;
     };
     bool ok = item < 0 || phase1ab(cur, 0);
+    KDA_CLK_DECL(clk);
 
     for (int li = 0; ok && item >= 0; ++li) {
         const float* sbeta = sbeta_buf(li & 1);
@@ -448,6 +449,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
+        KDA_CLK(clk, 0);   // loop top: claims, beta
         int n2;   // the item after next
         if constexpr (kDyn) n2 = s_seq[2];
         else n2 = (has_next && nidx + G < items) ? nidx + G : -1;
@@ -470,6 +472,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if (t == kStorer) bulk_wait_read();   // the previous item's pieces have left the staging buffer
         tc_fence_before_sync();
         __syncthreads();
+        KDA_CLK(clk, 1);   // off-diagonal rows
 
         // ---- phase 2: A and P by one tf32 MMA, while K~^T goes to the image
         if (t == 0) {
@@ -498,6 +501,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
+        KDA_CLK(clk, 2);   // A/P MMA with K~ staged alongside
         if (t == kStorer) {
             if (has_next) {   // the k tile is no longer read
                 issue_k_loads(p, sm, bar_k, nxt.t0, nxt.h);
@@ -513,6 +517,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
+        KDA_CLK(clk, 3);   // A/P read-out
         if (t < kSolveThreads) {
             phase3_solve(sm, t);
         } else {
@@ -542,10 +547,12 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
+        KDA_CLK(clk, 4);   // solve, with the seed, stores and publication alongside
         phase3_tb_operands(sm, t, sbeta);
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
+        KDA_CLK(clk, 5);   // Tb operands
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
@@ -577,6 +584,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
+        KDA_CLK(clk, 6);   // M = P Tb, Tb rows to TMEM
         if (quarter >= 2) {   // M rows (lanes 64-127), split into hi/lo
             float a[16];
             tmem_ld16(tmem_addr(tm, 32 * quarter, TM_M + 16 * part), a);
@@ -597,6 +605,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
+        KDA_CLK(clk, 7);   // M rows, [Tb; M] staged
 
         // ---- phase 4: D2 = [0; -Q_Gamma] + [Tb; M] K_Gamma (hi + lo) = [Wk; -Q']; A1 = -D2 to the image
         if (t == kStorer) {
@@ -617,10 +626,12 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         // the next item's phase 1 meanwhile.  It writes the g tile, vec, the X region, TMEM
         // columns [128, 256) and the other K_Gamma buffer, none of which this item still reads.
         if (has_next && !(ok = phase1ab(nxt, (li + 1) & 1))) break;
+        KDA_CLK(clk, 8);   // the next item's phase 1 under the [Wk; -Q'] MMA
         if (t == kStorer) bulk_wait_read();   // the [Tb; M] piece has left the staging buffer
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
+        KDA_CLK(clk, 9);   // wait for it
         {   // row L, K = dk columns [32 part, +32).  The Q' rows' lo halves are staged in this
             // item's K_Gamma buffer, which the D2 MMA has finished reading (the next item's phase 1
             // wrote the other one); the buffer's next writer runs after the next item's first
@@ -649,6 +660,8 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             bulk_store(img + IMG_QLO, sm + kg, 16384);
             bulk_commit();
         }
+        KDA_CLK(clk, 10);   // [-Wk; Q'] hi and Q' lo staged
+        KDA_CLK_COUNT(clk, 31);
         cur = nxt;   // the next item's first barrier orders these TMEM reads before its writes
         if (n2 >= 0) {   // its t0 and eos are read at the next item's top
             nxt.gc = n2 / H;
@@ -842,6 +855,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
 
     uint32_t f_par = 0, b_par = 0, v_par = 0, mma_par = 0;   // v_par: bit b = buffer b's parity
     bool ok = true;
+    KDA_CLK_DECL(clk);
     for (int ci = 0; ci < nchunks; ++ci) {
         const int t0 = bos + 64 * ci;
         const int BT = min(64, eos - t0);
@@ -859,6 +873,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
             break;
         }
         f_par ^= 1u;
+        KDA_CLK(clk, 16);   // front image in, last O staging read out
 
         // D1 = [Tb; M] V (hi + lo), the half that does not depend on the state, at once
         bool v_ok = true;   // thread 0
@@ -895,6 +910,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
+        KDA_CLK(clk, 17);   // V half of D1 issued, S_hi
         // D1 += [-Wk; Q'] S_hi + [0; Q' lo] S_hi
         if (t == 0) {
             tc_fence_after_sync();
@@ -922,6 +938,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
+        KDA_CLK(clk, 18);   // S_lo (under the S_hi MMAs)
         // D1 += [-Wk; Q'] S_lo
         if (t == 0) {
             tc_fence_after_sync();
@@ -945,6 +962,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
+        KDA_CLK(clk, 19);   // decay, D1 complete
         if (t == 0) mma_open = false;
         if (t == kProducer) {   // the front image and this v buffer have been read
             if (ci + 1 < nchunks) fetch_front(ci + 1);
@@ -1022,6 +1040,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
+        KDA_CLK(clk, 20);   // W split, state update (O staged alongside)
         if (t == kProducer && ci + 1 < nchunks) fetch_back(ci + 1);
         if (t == 0) mma_open = false;
         // state snapshot after a full chunk that ends on a checkpoint boundary
@@ -1040,6 +1059,8 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
                 tc_fence_before_sync();
             }
         }
+        KDA_CLK(clk, 21);   // checkpoint
+        KDA_CLK_COUNT(clk, 30);
     }
 
     if (t == kProducer) bulk_wait_all();   // staged O fully written before the CTA's shared memory goes away
@@ -1250,3 +1271,13 @@ cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream)
 }
 
 }  // namespace kda
+
+#ifdef KDA_PHASE_CLOCKS
+// Instrumented build only: copy out and clear this file's cycle marks (kClockSlots values).
+extern "C" int kda_phase_clocks_split(unsigned long long* out)
+{
+    if (cudaMemcpyFromSymbol(out, kda::phase_clock_slots, sizeof(kda::phase_clock_slots)) != cudaSuccess) return -1;
+    static const unsigned long long zero[kda::kClockSlots] = {};
+    return cudaMemcpyToSymbol(kda::phase_clock_slots, zero, sizeof(zero)) == cudaSuccess ? 0 : -1;
+}
+#endif

@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     float beta_next = (t < 64 && bos + t < eos) ? beta_of(__ldg(p.beta + (size_t)(bos + t) * H + h), pro) : 0.f;
     uint32_t v_par = 0, k_par = 0, qg_par = 0, mma_par = 0;
     bool ok = true;
+    KDA_CLK_DECL(clk);
 
     for (int ci = 0; ci < nchunks; ++ci) {
         const int t0 = bos + 64 * ci;
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             ok = false;
             break;
         }
+        KDA_CLK(clk, 0);   // this chunk's inputs in
         v_par ^= 1u;
         k_par ^= 1u;
         qg_par ^= 1u;
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
+        KDA_CLK(clk, 1);   // phase 1
 
         // ---- next chunk's v, then phase 2: A and P by one tf32 MMA
         if (t == 0) {
@@ -196,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
+        KDA_CLK(clk, 2);   // A/P MMA with K~ alongside
 
         // ---- phase 3: A/P read-out; solve; M = P Tb by MMA; [Tb; M] hi/lo into TMEM
         phase3_readout(sm, tm, L, quarter, part, sbeta);
@@ -203,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
+        KDA_CLK(clk, 3);   // A/P read-out
         if (t < kSolveThreads) {
             phase3_solve(sm, t);
         } else {   // meanwhile warps 8-15: the state's bf16 B operand, S <- gamma_C S, and the seed
@@ -216,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
+        KDA_CLK(clk, 4);   // solve, with the state operand and the seed alongside
         // the k tile of this chunk is no longer read: fetch the next chunk's
         if (t == 0 && ci + 1 < nchunks) {
             issue_k_loads(p, sm, bar_k, t0 + 64, h);
@@ -268,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
+        KDA_CLK(clk, 5);   // Tb operands, M = P Tb, [Tb; M] hi/lo
 
         // ---- phase 4: D2 = [0; -Q_Gamma] + [Tb; M] K_Gamma (hi + lo) = [Wk; -Q'], A1 = -D2; the
         // state-independent half of D1, [Tb; M] V (hi + lo), queued right behind it
@@ -301,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
+        KDA_CLK(clk, 6);   // [Wk; -Q'] MMA with the state's lo operand and decay alongside
         {   // A1 = -D2 = [-Wk; Q'] (hi) and [0; Q' lo], columns [16 part, +16), written over D2 once
             // every thread has read it
             float a[32];
@@ -322,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tmem_wait_st();
         tc_fence_before_sync();
         __syncthreads();
+        KDA_CLK(clk, 7);   // [-Wk; Q'] hi/lo operands
         // ---- phase 5b: D1 += [-Wk; Q'] S_hi + [0; Q' lo] S_hi + [-Wk; Q'] S_lo (the [Tb; M] V half
         // was queued in phase 4; the order is the chunk-parallel scan's)
         if (t == 0) {
@@ -343,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
+        KDA_CLK(clk, 8);   // the S half of D1
 
         // ---- phase 5c: rows 0-63 -> W (hi + lo) B operands
         if (quarter < 2) {
@@ -358,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         }
         tc_fence_before_sync();
         __syncthreads();
+        KDA_CLK(clk, 9);   // W hi/lo
 
         // ---- phase 5d: S += K~^T W (hi hi + hi lo + lo hi), while rows 64-127 (O) go out
         if (t == 0) {
@@ -408,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
+        KDA_CLK(clk, 10);   // state update, O staged
         // state snapshot after a full chunk that ends on a checkpoint boundary
         {
             const int done = t0 + 64 - bos;
@@ -433,6 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             bulk_commit();
             o_pending = true;
         }
+        KDA_CLK(clk, 11);   // checkpoint, O stores issued
+        KDA_CLK_COUNT(clk, 31);
     }
     if (t == 0) bulk_wait_all();   // staged O fully written before the CTA's shared memory goes away
 
@@ -498,3 +512,13 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream)
 }
 
 }  // namespace kda
+
+#ifdef KDA_PHASE_CLOCKS
+// Instrumented build only: copy out and clear this file's cycle marks (kClockSlots values).
+extern "C" int kda_phase_clocks_tc(unsigned long long* out)
+{
+    if (cudaMemcpyFromSymbol(out, kda::phase_clock_slots, sizeof(kda::phase_clock_slots)) != cudaSuccess) return -1;
+    static const unsigned long long zero[kda::kClockSlots] = {};
+    return cudaMemcpyToSymbol(kda::phase_clock_slots, zero, sizeof(zero)) == cudaSuccess ? 0 : -1;
+}
+#endif

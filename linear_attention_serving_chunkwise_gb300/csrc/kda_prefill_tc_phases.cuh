@@ -20,6 +20,38 @@ namespace {
 
 using namespace sm100;
 
+// ---------------------------------------------------------------- per-phase cycle marks
+// Compile-time option KDA_PHASE_CLOCKS (off in the library build; phase_clocks.py builds a
+// separate instrumented library with it): thread 0 of CTA 0 adds the clock64() cycles since
+// its previous mark to slot `id` of its file's phase_clock_slots array, by a reduction that
+// does not wait for the memory, and counts the items or chunks it ran in the two last slots.
+#ifdef KDA_PHASE_CLOCKS
+constexpr int kClockSlots = 32;
+struct PhaseClock {
+    long long prev;
+    __device__ __forceinline__ void mark(unsigned long long* slots, int id)
+    {
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            const long long now = clock64();
+            atomicAdd(slots + id, (unsigned long long)(now - prev));
+            prev = now;
+        }
+    }
+    __device__ __forceinline__ void count(unsigned long long* slots, int id)
+    {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(slots + id, 1ull);
+    }
+};
+__device__ unsigned long long phase_clock_slots[kClockSlots];   // one array per translation unit
+#define KDA_CLK_DECL(v) PhaseClock v{clock64()}
+#define KDA_CLK(v, id) v.mark(phase_clock_slots, id)
+#define KDA_CLK_COUNT(v, id) v.count(phase_clock_slots, id)
+#else
+#define KDA_CLK_DECL(v)
+#define KDA_CLK(v, id)
+#define KDA_CLK_COUNT(v, id)
+#endif
+
 constexpr int kThreads = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;   // bound on every on-device wait
 constexpr float kLog2e = 1.4426950408889634f;
