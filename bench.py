@@ -10,7 +10,10 @@ reported in the ``decode`` object, and K = 4 tokens per sequence through one
 ``kda_decode_multi`` call in the ``decode_multi`` object.  Inputs are larger than L2 (1.41 GB prefill,
 1.61 GB decode state), so no flush is needed between iterations.  ``e2e`` times
 ``kda_prefill_host`` from pinned host inputs to pinned host outputs (out and final
-state) every step.
+state) every step.  ``prologue`` times the same prefill from the recipe's raw draws with the
+input prologue in the kernels, ``gate`` the same prefill through ``kda_prefill_gated`` (the
+output gate o * sigmoid(z)).  nvidia-smi clock samples are kept for the timed windows of
+every leg.
 
 Rank 0 prints one JSON line.  Under torchrun each rank runs its own independent
 copy of the workload (weak scaling, no collective on the data path).
@@ -495,6 +498,44 @@ def run_cuda(args, world, rank, local):
         del draw, rargs, pws
     except Exception as exc:   # noqa: BLE001 -- recorded in the line instead of ending the run
         prologue["error"] = f"{type(exc).__name__}: {exc}"
+
+    # ---------------- the output gate: the headline call with gate logits z [T, H, dv] fp32
+    # (out = o * sigmoid(z)), through kda_prefill_gated; 512 more bytes read per token-head
+    gate = {"workload": cfg.name + "_gated", "api": "kda_prefill_gated"}
+    try:
+        z = W.make_gate_logits((cfg.total_tokens, cfg.num_heads, cfg.dv), seed=rank, device=dev)
+        gws = torch.empty(max(plan["workspace_bytes"], 16), dtype=torch.uint8, device=dev)
+
+        def gate_call():
+            kda.prefill(*pargs, out=out, final_state=fin, workspace=gws, stream=stream, gate=z)
+
+        for _ in range(args.warmup):
+            gate_call()
+        stream.synchronize()
+        q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _barrier(world)
+        w0 = time.time()
+        q0.record(stream)
+        for _ in range(args.steps):
+            gate_call()
+        q1.record(stream)
+        stream.synchronize()
+        sampler.window("gate", w0, time.time())
+        if kda.last_device_status(stream) != kda.KDA_OK:
+            raise RuntimeError("the gated prefill reported a device error")
+        gate_ms = _max_over_ranks(q0.elapsed_time(q1) / args.steps, world)
+        gate_bytes = alg_bytes + cfg.total_tokens * cfg.num_heads * cfg.dv * 4
+        gate.update({"ms_per_call": gate_ms, "tokens_per_s": tokens_per_step / (gate_ms / 1e3),
+                     "vs_plain_call": ms_per_step / gate_ms,
+                     "roofline": {"bound": "hbm", "achieved": gate_bytes / (gate_ms / 1e3) / 1e9,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": gate_bytes / (gate_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                  "frac_of_nominal": gate_bytes / (gate_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                                  "traffic": None, "algorithmic_bytes_per_launch": gate_bytes},
+                     "gpu_launches": args.steps * plan["kernel_launches"]})
+        del z, gws
+    except Exception as exc:   # noqa: BLE001 -- recorded in the line instead of ending the run
+        gate["error"] = f"{type(exc).__name__}: {exc}"
     clocks = sampler.stop()
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -506,7 +547,7 @@ def run_cuda(args, world, rank, local):
                        "parallelism": f"independent problem per GPU x{world}"},
             "roofline": roofline, "tensor": tensor, "e2e": e2e, "clocks": clocks,
             "gpu_launches": args.steps * plan["kernel_launches"], "decode": decode, "decode_multi": decode_multi,
-            "prologue": prologue}
+            "prologue": prologue, "gate": gate}
     if rank == 0 and world == 1:
         rate, dt, cores, sdesc = oracle_sample(cfg, heads=96, tokens=8192)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sdesc,
