@@ -71,20 +71,22 @@ constexpr uint32_t B_A1L = 197632;      // [0; Q' lo] K-major A [128 rows][128 K
 constexpr uint32_t B_BAR = 230400;
 constexpr size_t B_SMEM_BYTES = B_BAR + 64 + 1024;
 // words of the 64-byte block at B_BAR: the scan's 5 barriers (0-39), the separate scan
-// kernel's TMEM slot (40), the scan's abort word (44), the single launch's TMEM slot (48)
-constexpr uint32_t B_WORD_TSLOT = 40, B_WORD_ABORT = 44, B_WORD_TSLOT1 = 48;
-static_assert(B_WORD_TSLOT1 + 4 <= 64, "scan word block");
+// kernel's TMEM slot (40), the scan's abort word (44), the single launch's TMEM slot (48), the
+// gate logits' barrier (56)
+constexpr uint32_t B_WORD_TSLOT = 40, B_WORD_ABORT = 44, B_WORD_TSLOT1 = 48, B_WORD_BARZ = 56;
+static_assert(B_WORD_TSLOT1 + 4 <= B_WORD_BARZ && B_WORD_BARZ + 8 <= 64, "scan word block");
 constexpr uint32_t B_TM_S = 0;          // tensor memory: state [128 dk lanes][128 dv] fp32
 constexpr uint32_t B_TM_D1 = 128;       // [W; O] accumulator
 constexpr uint32_t B_TM_COLS = 256;
 
 // single-launch form: at least this many CTAs never scan (they finish the prep items), and
-// the switch point uses these costs (cycles on GB300: a scan's 6.0 K per chunk as measured,
-// the prep's 19.4 K per item less an allowance for the scans' start and flag waits, tuned
-// at 64 and 96 units)
+// the switch point uses these costs (cycles on GB300: a scan's 7.2 K per chunk as measured,
+// the prep's 19.8 K per item (23.1 K with the input prologue) less an allowance for the
+// scans' start and flag waits; swept on the B=1, H=96, T=8192 shape)
 constexpr long long kSingleMinProducers = 32;
 constexpr long long kScanCyclesPerChunk = 7200;
 constexpr long long kPrepCyclesPerItem = 18800;
+constexpr long long kPrepCyclesPerItemPrologue = 22100;   // the prologue instances' prep (23.1 K per item)
 
 static_assert(B_KTH % 1024 == 0 && B_V0 % 1024 == 0 && B_SB % 1024 == 0 && B_WH % 1024 == 0, "tile alignment");
 static_assert(B_KTH >= IMG_FRONT && B_V0 >= B_KTH + IMG_BACK && B_V1 == B_V0 + 16384 && B_SB >= B_V1 + 16384 &&
@@ -737,6 +739,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
     uint64_t* bar_b = bar_f + 1;
     uint64_t* bar_v = bar_f + 2;   // two, one per v buffer
     uint64_t* bar_mma = bar_f + 4;
+    uint64_t* bar_z = reinterpret_cast<uint64_t*>(sm + B_BAR + B_WORD_BARZ);   // the gate's logits
     int* s_abort = reinterpret_cast<int*>(sm + B_BAR + B_WORD_ABORT);
     const uint32_t sbase = smem_u32(sm);
     const float* sgam = reinterpret_cast<const float*>(sm + B_GAM);
@@ -775,10 +778,12 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
 
     if (t == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(bar_f + i, 1);
+        mbar_init(bar_z, 1);
         mbar_fence_init();
         *s_abort = 0;
         tma_prefetch_desc(&p.tm_v);
         tma_prefetch_desc(&p.tm_o);
+        if (p.gate) tma_prefetch_desc(&p.tm_z);
     }
     // rows 0-63 of the [0; Q' lo] operand: zeros in both K blocks, written once
     st_shared_v4(sbase + B_A1L + ((t >> 8) << 14) + 16 * (t & 255), 0u, 0u, 0u, 0u);
@@ -795,7 +800,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
     constexpr int kProducer = 64;
     bool o_pending = false;   // producer
     bool mma_open = false;    // thread 0
-    int n_front = 0, n_back = 0, n_v[2] = {0, 0};   // producer
+    int n_front = 0, n_back = 0, n_v[2] = {0, 0}, n_z = 0;   // producer
     auto fetch_front = [&](int c) {
         if (!ready(c)) {   // never published: give up (the waits on bar_f then run out)
             atomicExch(s_abort, 1);
@@ -829,6 +834,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         fetch_front(0);
         fetch_back(0);
         fetch_v(0);
+        if (p.gate) tma_prefetch_3d(&p.tm_z, 0, h, bos);   // the first chunk's logits into L2
         if (nchunks > 1) {
             fetch_v(1);
             prefetch_l2(image(1), IMG_BYTES);
@@ -853,7 +859,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         tmem_wait_st();
     }
 
-    uint32_t f_par = 0, b_par = 0, v_par = 0, mma_par = 0;   // v_par: bit b = buffer b's parity
+    uint32_t f_par = 0, b_par = 0, v_par = 0, mma_par = 0, z_par = 0;   // v_par: bit b = buffer b's parity
     bool ok = true;
     KDA_CLK_DECL(clk);
     for (int ci = 0; ci < nchunks; ++ci) {
@@ -965,6 +971,16 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         KDA_CLK(clk, 19);   // decay, D1 complete
         if (t == 0) mma_open = false;
         if (t == kProducer) {   // the front image and this v buffer have been read
+            if (p.gate && BT == 64) {   // this chunk's gate logits into the O staging boxes (S_hi is read)
+                mbar_arrive_expect_tx(bar_z, 32768u);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tma_load_3d(sm + B_OST + 8192 * j, &p.tm_z, bar_z, 32 * j, h, t0);
+                ++n_z;
+                if (ci + 1 < nchunks) {   // and the next chunk's into L2
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) tma_prefetch_3d(&p.tm_z, 32 * j, h, t0 + 64);
+                }
+            }
             if (ci + 1 < nchunks) fetch_front(ci + 1);
             if (ci + 2 < nchunks) {
                 fetch_v(ci + 2);
@@ -1011,19 +1027,18 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         } else {   // O row r = token t0 + r, dv columns [32 part, +32)
             const int r = L - 64;
             const size_t o0 = ((size_t)(t0 + r) * H + h) * 128 + 32 * part;
-            if (p.gate && r < BT) {   // the output gate, o * sigmoid(z)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 o = gate4(make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]),
-                                           p.gate + o0 + 4 * i);
-                    a[4 * i] = o.x; a[4 * i + 1] = o.y; a[4 * i + 2] = o.z; a[4 * i + 3] = o.w;
-                }
-            }
             if (BT == 64) {   // box `part` = dv columns [32 part, +32)
                 const uint32_t box = sbase + B_OST + 8192 * part;
+                if (p.gate) {   // the output gate, o * sigmoid(z), on the logits TMA put in the boxes
+                    if (!mbar_wait_bounded(bar_z, z_par, kWaitNs)) atomicExch(s_abort, 1);
+                    z_par ^= 1u;
+                    stage_gated_row(box, r, a);
+                } else {
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_f4(box + sw128_off_f32(r, 4 * q, 64), a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+                    for (int q = 0; q < 8; ++q)
+                        st_shared_f4(box + sw128_off_f32(r, 4 * q, 64), a[4 * q], a[4 * q + 1], a[4 * q + 2],
+                                     a[4 * q + 3]);
+                }
                 fence_proxy_async_smem();
                 named_sync(3, 256);   // the 8 O warps: the boxes are complete
                 if (t == kProducer) {   // stored now, so that they are read out before the next S build
@@ -1035,7 +1050,10 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
             } else if (r < BT) {   // a sequence's ragged last chunk: direct stores
                 float4* dst = reinterpret_cast<float4*>(p.out + o0);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+                for (int i = 0; i < 8; ++i) {
+                    const float4 o = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+                    dst[i] = p.gate ? gate4(o, p.gate + o0 + 4 * i) : o;
+                }
             }
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
@@ -1085,6 +1103,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         if (n_back > 0) mbar_wait_bounded(bar_b, (uint32_t)(n_back - 1) & 1u, kWaitNs);
         for (int i = 0; i < 2; ++i)
             if (n_v[i] > 0) mbar_wait_bounded(bar_v + i, (uint32_t)(n_v[i] - 1) & 1u, kWaitNs);
+        if (n_z > 0) mbar_wait_bounded(bar_z, (uint32_t)(n_z - 1) & 1u, kWaitNs);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -1214,7 +1233,8 @@ cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream)
         !make_map(&p.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
         !make_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
         !make_map(&p.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32) ||
-        !make_map(&p.tm_o, a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32))
+        !make_map(&p.tm_o, a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32) ||
+        (a.gate && !make_map(&p.tm_z, a.gate, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32)))
         return cudaErrorInvalidValue;
     p.beta = a.beta;
     p.cu_seqlens = a.cu_seqlens;
@@ -1251,7 +1271,8 @@ cudaError_t launch_prefill_split(const PrefillArgs& a, cudaStream_t stream)
         // rest in the time the scan takes: rest = (grid - units) x chunks x scan / prep per item.
         const long long chunks = ((long long)a.total_tokens / a.num_seqs + 63) / 64;
         const long long items = chunks * a.num_seqs * a.num_heads;
-        const long long rest = (dv.sms - units) * chunks * kScanCyclesPerChunk / kPrepCyclesPerItem;
+        const long long prep = a.prologue ? kPrepCyclesPerItemPrologue : kPrepCyclesPerItem;
+        const long long rest = (dv.sms - units) * chunks * kScanCyclesPerChunk / prep;
         int units_i = (int)units, switch_item = (int)std::max(0LL, items - rest);
         void* args[] = {&sp, &units_i, &switch_item};
         const void* kern = a.prologue ? (const void*)kda_prep_scan_kernel<true> : (const void*)kda_prep_scan_kernel<false>;

@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     uint64_t* bar_mma = bar_v + 3;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_v + 4);
     int* s_abort = reinterpret_cast<int*>(tslot + 1);
+    uint64_t* bar_z = bar_v + 5;   // the gate's logits (bytes 40-47 of the barrier block)
     const uint32_t sbase = smem_u32(sm);
 
     const int H = p.num_heads;
@@ -82,8 +83,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         mbar_init(bar_k, 1);
         mbar_init(bar_qg, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(bar_z, 1);
         mbar_fence_init();
         *s_abort = 0;
+        if (p.gate) tma_prefetch_desc(&p.tm_z);
         tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     tc_fence_after_sync();
     const uint32_t tm = *tslot;
 
-    bool v_pending = false, k_pending = false, qg_pending = false, o_pending = false;   // thread 0 only
+    bool v_pending = false, k_pending = false, qg_pending = false, o_pending = false, z_pending = false;   // thread 0
     bool mma_open = false;   // thread 0: MMAs issued after the last commit
     if (t == 0 && nchunks > 0) {
         issue_v_loads(p, sm, bar_v, 0, bos, h);
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     }
 
     float beta_next = (t < 64 && bos + t < eos) ? beta_of(__ldg(p.beta + (size_t)(bos + t) * H + h), pro) : 0.f;
-    uint32_t v_par = 0, k_par = 0, qg_par = 0, mma_par = 0;
+    uint32_t v_par = 0, k_par = 0, qg_par = 0, mma_par = 0, z_par = 0;
     bool ok = true;
     KDA_CLK_DECL(clk);
 
@@ -302,13 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPL + 8 * ks, desc_mnmajor(vb, 64, ks), idesc, 1u);
             mma_open = true;   // committed with phase 5b's MMAs
         }
-        // meanwhile: the state's lo operand, and S <- gamma_C S
-        state_lo_and_decay(sm, vec, tm, L, part, quarter);
-        fence_proxy_async_smem();
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        KDA_CLK(clk, 6);   // [Wk; -Q'] MMA with the state's lo operand and decay alongside
+        KDA_CLK(clk, 6);   // [Wk; -Q'] MMA
         {   // A1 = -D2 = [-Wk; Q'] (hi) and [0; Q' lo], columns [16 part, +16), written over D2 once
             // every thread has read it
             float a[32];
@@ -331,18 +331,29 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         tc_fence_before_sync();
         __syncthreads();
         KDA_CLK(clk, 7);   // [-Wk; Q'] hi/lo operands
-        // ---- phase 5b: D1 += [-Wk; Q'] S_hi + [0; Q' lo] S_hi + [-Wk; Q'] S_lo (the [Tb; M] V half
-        // was queued in phase 4; the order is the chunk-parallel scan's)
+        // ---- phase 5b: D1 += [-Wk; Q'] S_hi + [0; Q' lo] S_hi, then + [-Wk; Q'] S_lo once the
+        // state's lo operand, formed while the first two run, is in (the [Tb; M] V half was
+        // queued in phase 4; the order is the chunk-parallel scan's)
         if (t == 0) {
             tc_fence_after_sync();
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
-            const uint32_t sh = sbase + OFF_X + X_SB, sl = sbase + OFF_X + X_SL;
+            const uint32_t sh = sbase + OFF_X + X_SB;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1 + 8 * ks, desc_mnmajor(sh, 128, ks), idesc, 1u);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1L + 8 * ks, desc_mnmajor(sh, 128, ks), idesc, 1u);
+        }
+        state_lo_and_decay(sm, vec, tm, L, part, quarter);   // and S <- gamma_C S
+        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncthreads();
+        if (t == 0) {
+            tc_fence_after_sync();
+            const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+            const uint32_t sl = sbase + OFF_X + X_SL;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1 + 8 * ks, desc_mnmajor(sl, 128, ks), idesc, 1u);
@@ -352,7 +363,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();
-        KDA_CLK(clk, 8);   // the S half of D1
+        KDA_CLK(clk, 8);   // the S half of D1, the state's lo operand and decay alongside
+        if (t == 0 && p.gate && BT == 64) {   // the gate's logits into the O staging boxes (now free)
+            const uint8_t* vbz = sm + ((ci & 1) ? OFF_V1 : OFF_V0);
+            mbar_arrive_expect_tx(bar_z, 32768u);
+            tma_load_3d(sm + OFF_X + X_OST, &p.tm_z, bar_z, 0, h, t0);
+            tma_load_3d(sm + OFF_X + X_OST + 8192, &p.tm_z, bar_z, 32, h, t0);
+            tma_load_3d(const_cast<uint8_t*>(vbz), &p.tm_z, bar_z, 64, h, t0);
+            tma_load_3d(const_cast<uint8_t*>(vbz) + 8192, &p.tm_z, bar_z, 96, h, t0);
+            z_pending = true;
+            if (ci + 1 < nchunks) {   // and the next chunk's into L2
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tma_prefetch_3d(&p.tm_z, 32 * j, h, t0 + 64);
+            }
+        }
 
         // ---- phase 5c: rows 0-63 -> W (hi + lo) B operands
         if (quarter < 2) {
@@ -394,31 +418,38 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             float a[32];
             tmem_ld32(tmem_addr(tm, 32 * quarter, TM_D1 + 32 * part), a);
             tmem_wait_ld();
-            if (p.gate && r < BT) {   // the output gate, o * sigmoid(z)
-                const float* z = p.gate + ((size_t)(t0 + r) * H + h) * 128 + 32 * part;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 o = gate4(make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]), z + 4 * i);
-                    a[4 * i] = o.x; a[4 * i + 1] = o.y; a[4 * i + 2] = o.z; a[4 * i + 3] = o.w;
-                }
-            }
             if (BT == 64) {
                 // stage in 128-byte-swizzled [64 tok][32] fp32 boxes, one TMA store per box:
                 // boxes 0-1 in the free top of the X region, 2-3 in this chunk's v buffer
                 const uint32_t box = (part < 2) ? sbase + OFF_X + X_OST + 8192 * part
                                                 : sbase + ((ci & 1) ? OFF_V1 : OFF_V0) + 8192 * (part - 2);
+                if (p.gate) {   // the output gate, o * sigmoid(z), on the logits TMA put in the boxes
+                    if (!mbar_wait_bounded(bar_z, z_par, kWaitNs)) atomicExch(s_abort, 1);
+                    z_par ^= 1u;
+                    stage_gated_row(box, r, a);
+                } else {
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_f4(box + sw128_off_f32(r, 4 * q, 64), a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+                    for (int q = 0; q < 8; ++q)
+                        st_shared_f4(box + sw128_off_f32(r, 4 * q, 64), a[4 * q], a[4 * q + 1], a[4 * q + 2],
+                                     a[4 * q + 3]);
+                }
                 fence_proxy_async_smem();
             } else if (r < BT) {
-                float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)(t0 + r) * H + h) * 128 + 32 * part);
+                const size_t o0 = ((size_t)(t0 + r) * H + h) * 128 + 32 * part;
+                float4* dst = reinterpret_cast<float4*>(p.out + o0);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) dst[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+                for (int i = 0; i < 8; ++i) {
+                    const float4 o = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+                    dst[i] = p.gate ? gate4(o, p.gate + o0 + 4 * i) : o;
+                }
             }
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
+        if (t == 0 && z_pending) {   // the O warps have waited on it: the logits are in
+            z_par ^= 1u;
+            z_pending = false;
+        }
         KDA_CLK(clk, 10);   // state update, O staged
         // state snapshot after a full chunk that ends on a checkpoint boundary
         {
@@ -472,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             umma_commit(bar_mma);
             mbar_wait_bounded(bar_mma, mma_par ^ 1u, kWaitNs);
         }
+        if (z_pending) mbar_wait_bounded(bar_z, z_par, kWaitNs);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -487,7 +519,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream)
         !make_map(&p.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
         !make_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.num_heads, a.total_tokens, 64) ||
         !make_map(&p.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32) ||
-        !make_map(&p.tm_o, a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32))
+        !make_map(&p.tm_o, a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32) ||
+        (a.gate && !make_map(&p.tm_z, a.gate, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.num_heads, a.total_tokens, 32)))
         return cudaErrorInvalidValue;
     p.beta = a.beta;
     p.cu_seqlens = a.cu_seqlens;

@@ -118,6 +118,7 @@ __host__ __device__ constexpr uint32_t tm_ap(int m) { return TM_AP + 8u * m * (m
 
 struct TcParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_g, tm_o;
+    CUtensorMap tm_z;   // the output gate's logits, laid out as O (set when gate != nullptr)
     const float* beta;
     const int32_t* cu_seqlens;
     const float* init_state;
@@ -263,6 +264,20 @@ __device__ __forceinline__ void issue_qg_loads(const TcParams& p, uint8_t* sm, u
     tma_load_3d(sm + OFF_Q + 8192, &p.tm_q, bar, 64, h, t0);
 #pragma unroll
     for (int b = 0; b < 4; ++b) tma_load_3d(sm + OFF_G + 8192 * b, &p.tm_g, bar, 32 * b, h, t0);
+}
+
+// The output gate on an O row staged in shared memory: the row's 32 logits were loaded by
+// TMA into the same positions of the same [64 tok][32] fp32 box (128-byte swizzle), so each
+// value is read, multiplied by sigmoid(z) and stored back where the O value goes.
+__device__ __forceinline__ void stage_gated_row(uint32_t box, int r, const float (&a)[32])
+{
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint32_t at = box + sw128_off_f32(r, 4 * q, 64);
+        const float4 z = ld_shared_f4(at);
+        st_shared_f4(at, a[4 * q] * sigmoid_f(z.x), a[4 * q + 1] * sigmoid_f(z.y), a[4 * q + 2] * sigmoid_f(z.z),
+                     a[4 * q + 3] * sigmoid_f(z.w));
+    }
 }
 
 // ---------------------------------------------------------------- phase 1a: per-channel cumsum

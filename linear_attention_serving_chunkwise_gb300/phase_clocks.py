@@ -3,7 +3,8 @@
 ``python -m linear_attention_serving_chunkwise_gb300.phase_clocks`` builds
 ``libkda_gb300_clocks.so`` (the library with KDA_PHASE_CLOCKS defined: thread 0 of CTA 0
 adds clock64() cycles between marks in its loop to a device array), runs a prefill shape on
-each tensor-core path twice, and prints the cycles of each span per item (chunk prep), per
+each tensor-core path twice (``--prologue``: also the chunk-parallel path's prologue
+instances on raw draws), and prints the cycles of each span per item (chunk prep), per
 chunk (state scan) and per chunk (one CTA per (sequence, head)), averaged over what CTA 0 ran
 in the second call.  CTA 0 of the single cooperative launch preps items, then scans its unit,
 so both of its tables come from one CTA.  The instrumented library is a measuring tool only;
@@ -21,8 +22,9 @@ from .build import build
 
 TC_SPANS = ["inputs in (loop top)", "phase 1: cumsum, factors, token rows, off-diagonal rows",
             "A/P tf32 MMA, K~ alongside", "A/P read-out", "solve (state operand and seed alongside)",
-            "Tb operands, M = P Tb, [Tb; M] hi/lo", "[Wk; -Q'] MMA (state lo and decay alongside)",
-            "[-Wk; Q'] hi/lo operands", "S half of D1", "W hi/lo", "state update, O staged",
+            "Tb operands, M = P Tb, [Tb; M] hi/lo", "[Wk; -Q'] MMA",
+            "[-Wk; Q'] hi/lo operands", "S half of D1 (state lo and decay alongside)", "W hi/lo",
+            "state update, O staged",
             "checkpoint, O stores issued"]
 PREP_SPANS = ["loop top: claims, beta", "off-diagonal rows", "A/P tf32 MMA, K~ staged alongside", "A/P read-out",
               "solve (seed, image stores, publication alongside)", "Tb operands", "M = P Tb, Tb rows",
@@ -32,16 +34,17 @@ SCAN_SPANS = ["front image in, last O staging read", "V half of D1 issued, S_hi"
               "decay, D1 complete", "W split, state update (O staged alongside)", "checkpoint"]
 
 
-def _measure(lib, reader, seqlens, heads):
-    """The marks of the second of two calls on one shape."""
+def _measure(lib, reader, seqlens, heads, prologue=0):
+    """The marks of the second of two calls on one shape (with `prologue`, on the recipe's raw
+    draws and the kernels' prologue instances)."""
     import kda_workloads as W
     cfg = W.PrefillConfig("clocks", tuple(seqlens), heads, 128, 128, torch.bfloat16, "normal")
-    d = W.make_prefill_inputs(cfg, seed=0, device="cuda")
+    d = W.make_prefill_inputs(cfg, seed=0, device="cuda", raw=bool(prologue))
     args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])
-    out, fin = _lib.prefill(*args)
+    out, fin = _lib.prefill(*args, prologue=prologue)
     torch.cuda.synchronize()
     _read(lib, reader)
-    _lib.prefill(*args, out=out, final_state=fin)
+    _lib.prefill(*args, out=out, final_state=fin, prologue=prologue)
     torch.cuda.synchronize()
     if _lib.last_device_status() != _lib.KDA_OK:
         raise RuntimeError("the instrumented prefill reported a device error")
@@ -82,6 +85,11 @@ def main(argv=None):
     print("chunk-parallel path, B=1 H=96 T=8192, dk=dv=128 bf16 (single cooperative launch, CTA 0)")
     _table("chunk prep, per item", v, PREP_SPANS, 0, 31)
     _table("state scan, per chunk", v, SCAN_SPANS, 16, 30)
+    if "--prologue" in (argv if argv is not None else sys.argv[1:]):
+        v = _measure(lib, "kda_phase_clocks_split", [8192], 96, prologue=_lib.KDA_PROLOGUE_ALL)
+        print("the same with the input prologue (raw draws, every prologue bit)")
+        _table("chunk prep, per item", v, PREP_SPANS, 0, 31)
+        _table("state scan, per chunk", v, SCAN_SPANS, 16, 30)
     # one CTA per unit: 4 sequences x 2048 tokens, H=38 (152 units, one wave)
     v = _measure(lib, "kda_phase_clocks_tc", [2048] * 4, 38)
     print("one CTA per (sequence, head), 4 x 2048 tokens, H=38, dk=dv=128 bf16 (CTA 0)")
