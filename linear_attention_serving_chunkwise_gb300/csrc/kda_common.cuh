@@ -27,10 +27,10 @@ __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162flo
 constexpr int kProQK = 1, kProG = 2, kProBeta = 4;
 constexpr float kGMin = -5.f;
 constexpr float kL2Eps = 1e-12f;
-__device__ __forceinline__ float sigmoid_f(float y) { return 1.f / (1.f + expf(-y)); }
-// The same with the fast exponential and division (a few ulp of fp32 from the exact value;
-// 0 and 1 at the ends), for the prologue's parametrisations, which run on every g element
-// on the prefill's critical path.  Parity against the oracle's fp64 sigmoid is tested.
+// sigmoid(y) = 1 / (1 + e^-y) with the fast exponential and division (a few ulp of fp32 from
+// the exact value; 0 and 1 at the ends), for the prologue's parametrisations, which run on
+// every g element on the prefill's critical path, and the output gate.  Parity against the
+// oracle's fp64 sigmoid is tested.
 __device__ __forceinline__ float sigmoid_fast(float y) { return __fdividef(1.f, 1.f + __expf(-y)); }
 __device__ __forceinline__ float g_of(float g, int prologue) { return (prologue & kProG) ? kGMin * sigmoid_fast(g) : g; }
 __device__ __forceinline__ float beta_of(float b, int prologue) { return (prologue & kProBeta) ? sigmoid_fast(b) : b; }
@@ -43,11 +43,14 @@ __device__ __forceinline__ float l2_scale(float x, float inv, __nv_bfloat16)
 __device__ __forceinline__ float l2_inv(float sumsq) { return 1.f / fmaxf(sqrtf(sumsq), kL2Eps); }
 
 // Output gate (llm-atlas Q08, read as an elementwise sigmoid over the read-out channels):
-// o <- o * sigmoid(z) for 4 consecutive outputs and their logits (16-byte aligned).
+// o <- o * sigmoid(z), with the fast sigmoid (it runs on every output element, in the O
+// warps of the tensor-core kernels alongside the state update).
+__device__ __forceinline__ float gate1(float o, float z) { return o * sigmoid_fast(z); }
+// for 4 consecutive outputs and their logits in global memory (16-byte aligned)
 __device__ __forceinline__ float4 gate4(float4 o, const float* z)
 {
     const float4 zz = __ldg(reinterpret_cast<const float4*>(z));
-    return make_float4(o.x * sigmoid_f(zz.x), o.y * sigmoid_f(zz.y), o.z * sigmoid_f(zz.z), o.w * sigmoid_f(zz.w));
+    return make_float4(gate1(o.x, zz.x), gate1(o.y, zz.y), gate1(o.z, zz.z), gate1(o.w, zz.w));
 }
 
 // Read 4 consecutive elements starting at a 4-element-aligned index.

@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) kda_decode_kernel(DecodeArg
         const float w = s_beta * (sv[t] - rs);
         sw[t] = w;
         const float o = ps + s_kq * w;
-        a.out[bh * D + t] = a.gate ? o * sigmoid_f(__ldg(a.gate + bh * D + t)) : o;
+        a.out[bh * D + t] = a.gate ? gate1(o, __ldg(a.gate + bh * D + t)) : o;
     }
     __syncthreads();
 

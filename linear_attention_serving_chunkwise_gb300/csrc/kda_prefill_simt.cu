@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
             for (int c = 0; c < D; ++c) acc += sQ[r * D + c] * sS[c * kSlice + lane];
             for (int i = 0; i <= r; ++i) acc += sP[r * kAld + i] * sV[i * kSlice + lane];
             const size_t oi = ((size_t)(c0 + r) * H + h) * D + js + lane;
-            a.out[oi] = a.gate ? acc * sigmoid_f(__ldg(a.gate + oi)) : acc;
+            a.out[oi] = a.gate ? gate1(acc, __ldg(a.gate + oi)) : acc;
         }
         // S <- Diag(exp Gamma_n) S + K~^T W
         float snew[D / kWarps];

@@ -275,8 +275,8 @@ __device__ __forceinline__ void stage_gated_row(uint32_t box, int r, const float
     for (int q = 0; q < 8; ++q) {
         const uint32_t at = box + sw128_off_f32(r, 4 * q, 64);
         const float4 z = ld_shared_f4(at);
-        st_shared_f4(at, a[4 * q] * sigmoid_f(z.x), a[4 * q + 1] * sigmoid_f(z.y), a[4 * q + 2] * sigmoid_f(z.z),
-                     a[4 * q + 3] * sigmoid_f(z.w));
+        st_shared_f4(at, gate1(a[4 * q], z.x), gate1(a[4 * q + 1], z.y), gate1(a[4 * q + 2], z.z),
+                     gate1(a[4 * q + 3], z.w));
     }
 }
 
