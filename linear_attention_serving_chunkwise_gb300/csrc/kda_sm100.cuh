@@ -340,20 +340,33 @@ __host__ __device__ __forceinline__ uint32_t sw128_chunk_f32(uint32_t row, uint3
     return blk * rows * 128u + row * 128u + ((c ^ (row & 7u)) << 4);
 }
 
+
+// The same descriptors from a tile's base descriptor plus a constant byte offset: the start
+// address field (bits 0-13) holds the shared-memory address / 16, every operand lies below
+// 256 KB, so adding offset / 16 to the base never carries out of the field, and
+// desc_off(desc of tile, off) is the descriptor of tile + off.  With the K-steps unrolled the
+// offsets are immediates: one add per descriptor instead of rebuilding it.
+__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile_saddr) { return sdesc_sw128(tile_saddr, 16u, 1024u); }
+__device__ __forceinline__ uint64_t mnmajor_base(uint32_t tile_saddr, uint32_t krows)
+{
+    return sdesc_sw128(tile_saddr, krows * 128u, 1024u);
+}
+__host__ __device__ constexpr uint32_t kmajor_off(uint32_t rows, uint32_t ks) { return (ks >> 2) * rows * 128u + (ks & 3u) * 32u; }
+__host__ __device__ constexpr uint32_t mnmajor_off(uint32_t ks) { return ks * 2048u; }
+__device__ __forceinline__ uint64_t desc_off(uint64_t base, uint32_t bytes) { return base + (uint64_t)(bytes >> 4); }
+
 // Descriptor of K-step `ks` (16 bf16 of K) of a K-major operand with `rows` rows
 // (M or N) and K stored in 64-column blocks.
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_saddr, uint32_t rows, uint32_t ks)
 {
-    const uint32_t addr = tile_saddr + (ks >> 2) * rows * 128u + (ks & 3u) * 32u;
-    return sdesc_sw128(addr, 16u, 1024u);
+    return desc_off(kmajor_base(tile_saddr), kmajor_off(rows, ks));
 }
 
 // Descriptor of K-step `ks` of an MN-major operand stored with K as rows and
 // MN in 64-column blocks of `krows` rows (block stride krows * 128 bytes).
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_saddr, uint32_t krows, uint32_t ks)
 {
-    const uint32_t addr = tile_saddr + ks * 2048u;
-    return sdesc_sw128(addr, krows * 128u, 1024u);
+    return desc_off(mnmajor_base(tile_saddr, krows), mnmajor_off(ks));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
