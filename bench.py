@@ -12,7 +12,9 @@ reported in the ``decode`` object, and K = 4 tokens per sequence through one
 ``kda_prefill_host`` from pinned host inputs to pinned host outputs (out and final
 state) every step.  ``prologue`` times the same prefill from the recipe's raw draws with the
 input prologue in the kernels, ``gate`` the same prefill through ``kda_prefill_gated`` (the
-output gate o * sigmoid(z)).  nvidia-smi clock samples are kept for the timed windows of
+output gate o * sigmoid(z)), ``checkpoints`` through ``kda_prefill_checkpointed`` (a state
+snapshot every 512 tokens) and ``context_parallel`` the same sequence as two token ranges
+emulated on this GPU (local passes, one fold, the rerun).  nvidia-smi clock samples are kept for the timed windows of
 every leg.
 
 Rank 0 prints one JSON line.  Under torchrun each rank runs its own independent
@@ -536,6 +538,78 @@ def run_cuda(args, world, rank, local):
         del z, gws
     except Exception as exc:   # noqa: BLE001 -- recorded in the line instead of ending the run
         gate["error"] = f"{type(exc).__name__}: {exc}"
+
+    # ---------------- state checkpoints: the headline call with a snapshot of every (sequence,
+    # head)'s state after each 512 tokens (16 slots, 100.7 MB more written per call)
+    ckpt = {"workload": cfg.name + "_checkpoints", "api": "kda_prefill_checkpointed", "interval": 512, "slots": 16}
+    try:
+        cws = torch.empty(max(plan["workspace_bytes"], 16), dtype=torch.uint8, device=dev)
+        slots = torch.empty((1, cfg.num_heads, 16, cfg.dk, cfg.dv), dtype=torch.float32, device=dev)
+
+        def ckpt_call():
+            kda.prefill(*pargs, out=out, final_state=fin, workspace=cws, stream=stream, checkpoint_interval=512,
+                        checkpoint_slots=16, checkpoints=slots)
+
+        for _ in range(args.warmup):
+            ckpt_call()
+        stream.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _barrier(world)
+        w0 = time.time()
+        c0.record(stream)
+        for _ in range(args.steps):
+            ckpt_call()
+        c1.record(stream)
+        stream.synchronize()
+        sampler.window("checkpoints", w0, time.time())
+        if kda.last_device_status(stream) != kda.KDA_OK:
+            raise RuntimeError("the checkpointed prefill reported a device error")
+        ck_ms = _max_over_ranks(c0.elapsed_time(c1) / args.steps, world)
+        ck_bytes = alg_bytes + slots.numel() * 4
+        ckpt.update({"ms_per_call": ck_ms, "tokens_per_s": tokens_per_step / (ck_ms / 1e3),
+                     "vs_plain_call": ms_per_step / ck_ms,
+                     "roofline": {"bound": "hbm", "achieved": ck_bytes / (ck_ms / 1e3) / 1e9,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": ck_bytes / (ck_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                  "frac_of_nominal": ck_bytes / (ck_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                                  "traffic": None, "algorithmic_bytes_per_launch": ck_bytes},
+                     "gpu_launches": args.steps * plan["kernel_launches"]})
+        del cws, slots
+    except Exception as exc:   # noqa: BLE001 -- recorded in the line instead of ending the run
+        ckpt["error"] = f"{type(exc).__name__}: {exc}"
+
+    # ---------------- context parallelism emulated on this GPU: the headline sequence as two
+    # token ranges (local transition and zero-start passes of both as one varlen call each, the
+    # fold, the rerun from the folded states).  Three prefill passes, so slower than one call on
+    # one GPU by design: it measures the scheme's cost, not a speedup.
+    cp = {"workload": cfg.name + "_two_ranges", "api": "kcp.virtual_ranks_prefill", "ranks": 2}
+    try:
+        from linear_attention_serving_chunkwise_gb300 import kcp
+
+        def cp_call():
+            return kcp.virtual_ranks_prefill(*pargs[:5], pargs[6], ranks=2, stream=stream)
+
+        for _ in range(3):
+            cp_call()
+        stream.synchronize()
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cp_steps = max(3, min(args.steps, 20))
+        _barrier(world)
+        w0 = time.time()
+        k0.record(stream)
+        for _ in range(cp_steps):
+            cp_call()
+        k1.record(stream)
+        stream.synchronize()
+        sampler.window("context_parallel", w0, time.time())
+        if kda.last_device_status(stream) != kda.KDA_OK:
+            raise RuntimeError("the context-parallel prefill reported a device error")
+        cp_ms = _max_over_ranks(k0.elapsed_time(k1) / cp_steps, world)
+        cp.update({"ms_per_call": cp_ms, "tokens_per_s": tokens_per_step / (cp_ms / 1e3),
+                   "vs_plain_call": ms_per_step / cp_ms, "steps": cp_steps,
+                   "gpu_launches_per_call": "3 prefill calls (2 launches each at these 192 units), 1 kda_state_combine"})
+    except Exception as exc:   # noqa: BLE001 -- recorded in the line instead of ending the run
+        cp["error"] = f"{type(exc).__name__}: {exc}"
     clocks = sampler.stop()
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -547,7 +621,7 @@ def run_cuda(args, world, rank, local):
                        "parallelism": f"independent problem per GPU x{world}"},
             "roofline": roofline, "tensor": tensor, "e2e": e2e, "clocks": clocks,
             "gpu_launches": args.steps * plan["kernel_launches"], "decode": decode, "decode_multi": decode_multi,
-            "prologue": prologue, "gate": gate}
+            "prologue": prologue, "gate": gate, "checkpoints": ckpt, "context_parallel": cp}
     if rank == 0 and world == 1:
         rate, dt, cores, sdesc = oracle_sample(cfg, heads=96, tokens=8192)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sdesc,
