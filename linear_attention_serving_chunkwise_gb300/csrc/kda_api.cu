@@ -53,20 +53,20 @@ bool uses_tensor_cores(const kda_prefill_desc& d)
 // Which tensor-core path a bf16, dk = dv = 128 call takes, from its shape alone.  One CTA per
 // (sequence, head) unit walks that unit's chunks; with U units on the GB300's 152 SMs that is
 // ceil(U / 152) waves of about 25.8 K cycles per chunk.  The chunk-parallel split runs the
-// state-independent work of every (chunk, head) item on all SMs (about 19.8 K cycles per
+// state-independent work of every (chunk, head) item on all SMs (about 19.5 K cycles per
 // item, counted as 21.0 K: at over 120 units its separate launches overlap less) and then the
-// state scan, again in ceil(U / 152) waves but of about 7.2 K cycles per chunk, plus a fixed
-// 10 K cycles (the extra launch, the pipeline's fill); its workspace holds 115,200 bytes per
-// item, at most kSplitMaxItems of them.  The split is taken when its estimate is lower.  For
-// 8192-token sequences that is up to about 130 units (measured: 1.10 ms at 96 units and
-// 1.46 ms at 124 with the split; at 136, 1.64 ms with the split against 1.59 ms with one CTA
-// per unit), and again from 153 units to the item cap, where one CTA per unit would run a
+// state scan, again in ceil(U / 152) waves but of about 5 K cycles per chunk (counted as
+// 6.4 K, which also keeps many short sequences, e.g. 120 of 200 tokens, on one CTA each), plus a fixed 10 K cycles (the extra launch, the pipeline's fill); its workspace holds
+// 115,200 bytes per item, at most kSplitMaxItems of them.  The split is taken when its
+// estimate is lower.  For 8192-token sequences that is up to about 140 units (measured: at 136
+// units 1.55 ms with the split against 1.58 ms with one CTA per unit; at 144, 1.64 ms against
+// 1.58 ms), and again from 153 units to the item cap, where one CTA per unit would run a
 // mostly idle second wave.
 constexpr long long kGpuSMs = 152;
 constexpr long long kSplitMaxItems = 32768;
 constexpr long long kCyclesPerChunkOneCta = 258;     // hundreds of cycles
 constexpr long long kCyclesPerItemPrep = 210;
-constexpr long long kCyclesPerChunkScan = 72;
+constexpr long long kCyclesPerChunkScan = 64;
 constexpr long long kCyclesSplitFixed = 100;
 
 bool uses_split(const kda_prefill_desc& d)

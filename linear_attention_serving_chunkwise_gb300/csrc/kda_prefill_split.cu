@@ -17,12 +17,14 @@
 //      writes the operands of its state step -- [-Wk; Q'] bf16, [Tb; M] and K~^T as bf16
 //      hi + lo, gamma_C -- to the workspace as the byte images of 128-byte-swizzled K-major
 //      tiles, so that they can be copied into shared memory as they are;
-//   3  kda_state_scan_kernel: one CTA per (sequence, head), the state in tensor memory.
-//      Per chunk: the state's bf16 operand and S <- gamma_C S; D1 = [Tb; M] V + [-Wk; Q'] S
-//      by MMAs with the A operands in shared memory; W (hi + lo) to shared memory and O to
-//      HBM; S += K~^T W by MMAs.  The item's images arrive by bulk asynchronous copies one
-//      step ahead, v by TMA two chunks ahead.
-// The tensor-core instructions and their operands are those of the one-CTA-per-head
+//   3  kda_state_scan_kernel: one CTA per (sequence, head), the state transposed (S^T, dv on
+//      the lanes) in tensor memory, the CTA split into CUDA warps, an MMA-issuing thread and
+//      a copy-issuing thread (see scan_unit).  Per chunk: S^T's bf16 operands (hi, lo) into
+//      tensor memory and S^T <- S^T gamma_C; D1^T = V^T [Tb; M]^T + S^T [-Wk; Q']^T by MMAs
+//      whose A operands are v and S^T and whose B operands are the images as they are; W^T
+//      (hi + lo) into tensor memory and O out through shared memory by TMA; S^T += W^T K~.
+//      The item's images arrive by bulk asynchronous copies ahead of their use, v by TMA.
+// Each output element is the same sum of the same products as in the one-CTA-per-head
 // kernel, so the results are the same; the work of steps 1-2 spreads over every SM
 // instead of one SM per (sequence, head), at the price of 112.5 KB of operands per item
 // written and read back through HBM.  The prep kernels come in two instances: with the
@@ -60,38 +62,52 @@ constexpr uint32_t B_KTH = 66560;       // the back image (1024-byte aligned)
 constexpr uint32_t B_KTL = B_KTH + 16384;
 constexpr uint32_t B_V0 = 99328;        // v tiles [64 tok][128 ch] bf16, two buffers
 constexpr uint32_t B_V1 = 115712;
-constexpr uint32_t B_SB = 132096;       // S hi bf16, MN-major B [128 dk][128 dv], until D1 has read it; then
-                                        // O staging: 4 x [64 tok][32 dv] fp32 boxes, 128-byte swizzle
-constexpr uint32_t B_OST = B_SB;
-constexpr uint32_t B_SL = 164864;       // S lo bf16, same layout, until D1 has read it; then:
-constexpr uint32_t B_WH = 164864;       // W hi bf16, MN-major B [64 tok][128 dv]
-constexpr uint32_t B_WL = 181248;       // W lo
-constexpr uint32_t B_A1L = 197632;      // [0; Q' lo] K-major A [128 rows][128 K]: in each 16 KB K block, rows
-                                        // 0-63 are zeros written once, rows 64-127 the image's Q' lo
-constexpr uint32_t B_BAR = 230400;
-constexpr size_t B_SMEM_BYTES = B_BAR + 64 + 1024;
-// words of the 64-byte block at B_BAR: the scan's 5 barriers (0-39), the separate scan
-// kernel's TMEM slot (40), the scan's abort word (44), the single launch's TMEM slot (48), the
-// gate logits' barrier (56)
-constexpr uint32_t B_WORD_TSLOT = 40, B_WORD_ABORT = 44, B_WORD_TSLOT1 = 48, B_WORD_BARZ = 56;
-static_assert(B_WORD_TSLOT1 + 4 <= B_WORD_BARZ && B_WORD_BARZ + 8 <= 64, "scan word block");
-constexpr uint32_t B_TM_S = 0;          // tensor memory: state [128 dk lanes][128 dv] fp32
-constexpr uint32_t B_TM_D1 = 128;       // [W; O] accumulator
-constexpr uint32_t B_TM_COLS = 256;
+constexpr uint32_t B_QLO = 132096;      // Q' lo, K-major [64 rows][128 K] (2 x 8 KB), as the image holds it
+constexpr uint32_t B_OST = 148480;      // O staging, two buffers of 4 x [64 tok][32 dv] fp32 boxes, 128-byte
+                                        // swizzle (32 KB each), for the TMA store
+constexpr uint32_t B_BAR = 230400;      // past the chunk prep's shared memory (the single launch runs both)
+constexpr size_t B_SMEM_BYTES = B_BAR + 256 + 1024;
+// the 256-byte block at B_BAR: the separate scan kernel's TMEM slot (word 40), the scan's abort
+// word (44), the single launch's TMEM slot (48); from byte 64 the scan's mbarriers, by index:
+constexpr uint32_t B_WORD_TSLOT = 40, B_WORD_ABORT = 44, B_WORD_TSLOT1 = 48, B_BARS = 64;
+constexpr int B_BAR_FRONT = 0;     // [-Wk; Q'] and Q' lo of a chunk are in
+constexpr int B_BAR_TB = 1;        // [Tb; M] hi + lo of a chunk are in
+constexpr int B_BAR_BACK = 2;      // the back image (K~^T) is in
+constexpr int B_BAR_V = 3;         // v of a chunk is in, one per buffer (2)
+constexpr int B_BAR_GAMMA = 5;     // gamma_C of a chunk is in
+constexpr int B_BAR_MMA = 6;       // D1's MMAs are done, then the state update's
+constexpr int B_BAR_VDONE = 7;     // the V^T [Tb; M]^T MMAs are done
+constexpr int B_BAR_SHI = 8;       // S^T_hi is written (the 14 CUDA warps arrive)
+constexpr int B_BAR_SLO = 9;       // S^T_lo is written and S^T decayed (14 warps)
+constexpr int B_BAR_WREADY = 10;   // W^T is written (14 warps)
+constexpr int B_BAR_DREAD = 11;    // D1 is read out (14 warps)
+constexpr int B_BAR_END = 12;      // the MMA issuer's last commit
+constexpr int B_BAR_OSTAGED = 13;  // O of a chunk is staged (14 warps)
+constexpr int B_BAR_SFREE = 14;    // the O store of a chunk has read its staging buffer
+constexpr int B_BAR_Z = 15;        // the gate logits of a chunk are in its O staging buffer, one per buffer (2)
+constexpr int B_BAR_COUNT = 17;
+static_assert(B_WORD_TSLOT1 + 4 <= B_BARS && B_BARS + 8 * B_BAR_COUNT <= 256, "scan word block");
+// tensor memory (columns), everything transposed: lane = dv
+constexpr uint32_t B_TM_S = 0;          // S^T [128 dv][128 dk] fp32
+constexpr uint32_t B_TM_D1 = 128;       // D1^T [128 dv][W^T: tokens 0-63 | O^T: tokens 0-63] fp32
+constexpr uint32_t B_TM_SH = 256;       // S^T_hi, bf16 pairs along dk (64 columns)
+constexpr uint32_t B_TM_SL = 320;       // S^T_lo
+constexpr uint32_t B_TM_WH = 384;       // W^T_hi, bf16 pairs along the tokens (32 columns)
+constexpr uint32_t B_TM_WL = 416;       // W^T_lo
+constexpr uint32_t B_TM_COLS = 512;
 
 // single-launch form: at least this many CTAs never scan (they finish the prep items), and
 // the switch point uses these costs (cycles on GB300: a scan's 7.2 K per chunk as measured,
 // the prep's 19.8 K per item (23.1 K with the input prologue) less an allowance for the
 // scans' start and flag waits; swept on the B=1, H=96, T=8192 shape)
 constexpr long long kSingleMinProducers = 32;
-constexpr long long kScanCyclesPerChunk = 7200;
-constexpr long long kPrepCyclesPerItem = 18800;
-constexpr long long kPrepCyclesPerItemPrologue = 22100;   // the prologue instances' prep (23.1 K per item)
+constexpr long long kScanCyclesPerChunk = 6000;
+constexpr long long kPrepCyclesPerItem = 19600;
+constexpr long long kPrepCyclesPerItemPrologue = 22900;   // the prologue instances' prep
 
-static_assert(B_KTH % 1024 == 0 && B_V0 % 1024 == 0 && B_SB % 1024 == 0 && B_WH % 1024 == 0, "tile alignment");
-static_assert(B_KTH >= IMG_FRONT && B_V0 >= B_KTH + IMG_BACK && B_V1 == B_V0 + 16384 && B_SB >= B_V1 + 16384 &&
-                  B_SL >= B_SB + 32768 && B_WH == B_SL && B_WL == B_WH + 16384 && B_A1L >= B_SL + 32768 &&
-                  B_A1L % 1024 == 0 && B_BAR >= B_A1L + 32768 && B_SMEM_BYTES <= 232448,
+static_assert(B_KTH % 1024 == 0 && B_V0 % 1024 == 0 && B_QLO % 1024 == 0, "tile alignment");
+static_assert(B_KTH >= IMG_FRONT && B_V0 >= B_KTH + IMG_BACK && B_V1 == B_V0 + 16384 && B_QLO >= B_V1 + 16384 &&
+                  B_OST >= B_QLO + 16384 && B_OST % 1024 == 0 && B_BAR >= B_OST + 65536 && B_SMEM_BYTES <= 232448 && B_TM_WL + 32 <= B_TM_COLS,
               "state-scan map overlaps");
 static_assert(IMG_KTL == IMG_KTH + 16384 && IMG_QLO == IMG_KTH + IMG_BACK && IMG_BYTES == IMG_QLO + 16384 &&
                   IMG_BYTES % 16 == 0,
@@ -137,6 +153,19 @@ __device__ __forceinline__ int resolve_claim(int v, int items, int limit, bool& 
     return v;
 }
 
+// The next claim: the counter's old value when `want`, else -1.  The fetch-and-add is
+// predicated instead of selected on, so that nothing reads its result (and waits for the
+// round trip to L2) before that result is resolved, an item later.
+__device__ __forceinline__ int claim_async(int* counter, bool want)
+{
+    int v = -1;
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p atom.global.add.u32 %0, [%1], 1;\n\t}"
+                 : "+r"(v)
+                 : "l"(counter), "r"((unsigned)want)
+                 : "memory");
+    return v;
+}
+
 // acquire fence at GPU scope (after relaxed reads of flags that were set by release stores)
 __device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
@@ -152,6 +181,27 @@ template <int N>
 __device__ __forceinline__ void bulk_wait_group()
 {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// wait until at most N committed bulk stores are still reading their shared-memory source
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_group()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// A wait of one role of the state scan: bounded like every wait, and it also gives up at once
+// when another role has recorded an abort, so that one failure does not cost each role a
+// full time-out.  The waiting thread sleeps between tests (up to 20 us each, woken when the
+// phase completes), so that waiting warps take no issue slots from working ones.
+__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, const int* s_abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (*reinterpret_cast<const volatile int*>(s_abort) != 0 || globaltimer_ns() - t0 > kWaitNs) return false;
+    }
 }
 
 // order this thread's generic-proxy and async-proxy accesses to global memory
@@ -206,6 +256,7 @@ constexpr size_t A_SMEM_BYTES = A_USED + 1024;   // slack for 1024-byte alignmen
 static_assert(A_USED <= B_BAR, "the prep layout ends below the scan's word block, which the single launch's "
                                 "TMEM slot occupies from the start");
 static_assert(A_SMEM_BYTES <= 232448, "prep shared memory");
+static_assert(B_BAR >= A_USED, "the scan's barrier block lies past the chunk prep's shared memory");
 static_assert(OFF_V1 + 16384 == A_STAGE + 32768, "staging buffer");
 static_assert(A_KG2 % 1024 == 0 && A_BETA2 % 16 == 0 && A_INFO % 8 == 0, "second K_Gamma, beta, info buffers");
 
@@ -336,14 +387,16 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
     uint64_t* bar_qg = bar_k + 1;
     uint64_t* bar_mma = bar_k + 2;
     int* s_abort = reinterpret_cast<int*>(sm + OFF_BAR + 36);
-    int* s_seq = reinterpret_cast<int*>(sm + OFF_BAR + 40);   // item indices claimed by thread 0
+    int* s_seq = reinterpret_cast<int*>(sm + OFF_BAR + 40);   // claimed item indices (kDyn)
     int2* s_info = reinterpret_cast<int2*>(sm + A_INFO);
     const uint32_t sbase = smem_u32(sm);
     const int H = p.num_heads;
     const int items = __ldg(sp.chunk_off + p.num_seqs) * H;
     const int G = gridDim.x;
-    bool stop = false;                   // thread 0 (kDyn): no more claims
-    int claim_raw = -1;                  // thread 0 (kDyn): a claim issued an item ago, unresolved
+    // kDyn: thread 0 claims the first two items; from then on the claims are kStorer's, one per
+    // item, issued during the solve and resolved at the next item's top
+    bool stop = false;                   // kStorer: no more claims
+    int claim_raw = -1;                  // kStorer: a claim issued during the last solve, unresolved
 
     if (t == 0) {
         mbar_init(bar_k, 1);
@@ -357,27 +410,31 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if constexpr (kDyn) {
             s_seq[0] = resolve_claim(atomicAdd(sp.counter, 1), items, limit, stop);
             s_seq[1] = stop ? -1 : resolve_claim(atomicAdd(sp.counter, 1), items, limit, stop);
-            claim_raw = stop ? -1 : atomicAdd(sp.counter, 1);   // resolved at the first item
         }
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
 
+    // The tile loads are issued, the image pieces stored, waited for and published, and the
+    // items claimed by kStorer, a thread of the warps that only write the seed during the
+    // solve, so that this work fits in their idle time instead of delaying thread 0 (which
+    // issues the MMAs).
+    constexpr int kStorer = kSolveThreads;
     // the current and next items (index -1: none); the one after is looked up an item ahead
     // of its use, so that its chunk-table load is never waited for
     int item, nidx;
     if constexpr (kDyn) {
         item = s_seq[0];
         nidx = s_seq[1];
+        if (t == kStorer) {   // thread 0's stop, and the claim resolved at the first item
+            stop = nidx < 0 || nidx >= limit;
+            claim_raw = claim_async(sp.counter, !stop);
+        }
     } else {
         item = (int)blockIdx.x < items ? (int)blockIdx.x : -1;
         nidx = (item >= 0 && item + G < items) ? item + G : -1;
     }
-    // The tile loads are issued, and the image pieces stored, waited for and published, by
-    // kStorer, a thread of the warps that only write the seed during the solve, so that this
-    // work fits in their idle time instead of delaying thread 0 (which issues the MMAs).
-    constexpr int kStorer = kSolveThreads;
     bool k_pending = false, qg_pending = false;   // kStorer: a load issued, not yet waited for
     int pub2 = -1, pub1 = -1;                     // kStorer (kDyn): done, not yet published
     Item cur{}, nxt{};
@@ -441,12 +498,8 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             if ((pro & kProBeta) && t < BT) sbeta_buf(li & 1)[t] = sigmoid_fast(sbeta_buf(li & 1)[t]);
         }
         if constexpr (kDyn) {
-            if (t == 0) {
-                // the item after next: the claim issued an item ago (its latency hidden by that
-                // item's work); then the next claim, resolved at the next item
-                s_seq[2] = has_next ? resolve_claim(claim_raw, items, limit, stop) : -1;
-                claim_raw = (has_next && !stop && s_seq[2] >= 0) ? atomicAdd(sp.counter, 1) : -1;
-            }
+            // the item after next: the claim issued during the last item's solve
+            if (t == kStorer) s_seq[2] = has_next ? resolve_claim(claim_raw, items, limit, stop) : -1;
         }
         tc_fence_before_sync();
         __syncthreads();
@@ -527,6 +580,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             phase3_seed(sm, vec, tm, L, 2 * (part - 2) + 1, quarter, BT);
             tmem_wait_st();
             if (t == kStorer) {
+                if constexpr (kDyn) claim_raw = claim_async(sp.counter, !stop && n2 >= 0);   // resolved at the next top
                 bulk_wait_read();   // the K~ piece has left the staging buffer ([Tb; M] goes there next)
                 if constexpr (kDyn) {
                     if (pub2 >= 0) {   // the item two back: its pieces are older than the last three
@@ -722,24 +776,58 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
 }
 
 // ---------------------------------------------------------------- step 3: the state scan
-// The scan of one (sequence, head) unit by one CTA, 16 warps (warp w: TMEM lanes
-// [32 (w % 4), +32), column part w / 4).  The front image of chunk c+1 is fetched once chunk
-// c's D1 MMAs have read theirs, the back image once its state update has; v two chunks ahead
-// into the freed buffer, and the images of chunk c+2 are prefetched into L2 at the same time.
-// With kFlags (the single-launch form) each image is fetched only once its item's flag is
-// set.  `tm`: at least 256 allocated TMEM columns.
+// The scan of one (sequence, head) unit by one CTA.  It keeps the state transposed, S^T
+// [128 dv lanes][128 dk] fp32 in tensor memory, and forms every product of a chunk step
+// transposed, so that the operands the CUDA cores write (S^T hi/lo, W^T hi/lo) are A
+// operands in tensor memory and the chunk's images, as they are, are the K-major B operands:
+//   D1^T = V^T [Tb; M]^T (hi, lo)            A: v from shared memory (MN-major); B: [Tb; M]
+//        + S^T_hi [-Wk; Q']^T + S^T_hi Q'_lo^T (the last into O's columns only, N = 64)
+//        + S^T_lo [-Wk; Q']^T                A: S^T hi / lo from tensor memory; B: the images
+//   S^T <- gamma_C S^T + W^T_hi K~_hi + W^T_lo K~_hi + W^T_hi K~_lo
+//                                            A: W^T hi / lo from tensor memory; B: K~^T
+// with D1^T [dv lanes][128]: columns 0-63 W^T (tokens), 64-127 O^T.  Each output element is
+// the same sum of the same products as in the one-CTA-per-unit kernel.  Shared memory then
+// carries only the images and v, and O leaves straight from the registers: a warp stores
+// one token's 32 consecutive dv values at a time.  The CTA is split by role:
+//   14 CUDA warps (all but kIssuerWarp and kProducerWarp; warp w reads TMEM lanes
+//     [32 (w % 4), +32); 4 warps share a lane quarter's columns on lanes 0-63, 3 on lanes
+//     64-127): per chunk, S^T_hi, then S^T_lo = bf16(S^T - S^T_hi) and S^T <- S^T gamma_C;
+//     once D1 is in, W^T (hi + lo) into tensor memory and O to global memory;
+//   lane 0 of kIssuerWarp issues every MMA: V^T [Tb; M]^T at the chunk's top, the S^T_hi
+//     products once S^T_hi is written, the S^T_lo product once S^T_lo is, and the state update
+//     once W^T is;
+//   lane 0 of kProducerWarp issues every copy: [Tb; M] of chunk c+1 and v two chunks ahead
+//     once chunk c's V^T [Tb; M]^T MMAs are done, gamma_C of c+1 and the back image of c once
+//     S^T_lo of c is formed (the update of c-1 has read the last back image), [-Wk; Q'] and
+//     Q' lo of c+1 once D1 of c is in; the images of chunk c+2 are prefetched into L2.
+// The roles signal one another through mbarriers (one arrival per warp), never through a
+// barrier of the whole CTA: issuing an MMA waits while the tensor pipe's queue is full, which
+// then holds up no CUDA warp; the S^T_lo pass runs under the S^T_hi MMAs, the O stores under
+// the state update.  Every wait is bounded and gives up early once another role has recorded
+// an abort.  With kFlags (the single-launch form) each image is fetched only once its item's
+// flag is set.  `tm`: 512 allocated TMEM columns.
+constexpr int kIssuerWarp = 10, kProducerWarp = 11;
 template <bool kFlags>
 __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, uint32_t tm, int unit)
 {
     const TcParams& p = sp.p;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int quarter = warp & 3, part = warp >> 2;
-    const int L = 32 * quarter + lane;
-    uint64_t* bar_f = reinterpret_cast<uint64_t*>(sm + B_BAR);
-    uint64_t* bar_b = bar_f + 1;
-    uint64_t* bar_v = bar_f + 2;   // two, one per v buffer
-    uint64_t* bar_mma = bar_f + 4;
-    uint64_t* bar_z = reinterpret_cast<uint64_t*>(sm + B_BAR + B_WORD_BARZ);   // the gate's logits
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + B_BAR + B_BARS);
+    uint64_t* bar_f = bars + B_BAR_FRONT;          // [-Wk; Q'] and Q' lo are in
+    uint64_t* bar_tb = bars + B_BAR_TB;            // [Tb; M] hi + lo are in
+    uint64_t* bar_b = bars + B_BAR_BACK;           // K~^T hi + lo are in
+    uint64_t* bar_v = bars + B_BAR_V;              // v, two, one per buffer
+    uint64_t* bar_g = bars + B_BAR_GAMMA;          // gamma_C is in
+    uint64_t* bar_mma = bars + B_BAR_MMA;          // D1 is done, then the state update
+    uint64_t* bar_vdone = bars + B_BAR_VDONE;      // the V^T [Tb; M]^T MMAs are done
+    uint64_t* bar_shi = bars + B_BAR_SHI;          // S^T_hi is written (14 warps)
+    uint64_t* bar_slo = bars + B_BAR_SLO;          // S^T_lo is written and S^T decayed (14 warps)
+    uint64_t* bar_wready = bars + B_BAR_WREADY;    // W^T is written (14 warps)
+    uint64_t* bar_dread = bars + B_BAR_DREAD;      // D1 is read out (14 warps)
+    uint64_t* bar_end = bars + B_BAR_END;          // the MMA issuer's last commit
+    uint64_t* bar_ostaged = bars + B_BAR_OSTAGED;  // O is staged (14 warps)
+    uint64_t* bar_sfree = bars + B_BAR_SFREE;      // an O store has read its staging buffer
+    uint64_t* bar_z = bars + B_BAR_Z;              // the gate logits are in an O staging buffer, two
     int* s_abort = reinterpret_cast<int*>(sm + B_BAR + B_WORD_ABORT);
     const uint32_t sbase = smem_u32(sm);
     const float* sgam = reinterpret_cast<const float*>(sm + B_GAM);
@@ -752,358 +840,450 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
     const int gc0 = __ldg(sp.chunk_off + n);
     const size_t sbase_g = ((size_t)n * H + h) * 128 * 128;
     auto image = [&](int c) { return sp.ops + ((size_t)(gc0 + c) * H + h) * IMG_BYTES; };
-    // kFlags: the producer fetches chunk c's images only once its item is published.  It reads
-    // the flags of up to 16 chunks ahead with relaxed loads and takes one acquire (and proxy)
-    // fence for all that are set, so that a fence is paid per batch, not per fetch; it blocks
-    // (bounded) only when chunk c itself is not yet published.
-    int known = -1;   // producer: chunks <= known are published and acquired
-    auto ready = [&](int c) {
-        if constexpr (kFlags) {
-            if (c <= known) return true;
-            const int* f = sp.flags + (size_t)gc0 * H + h;
-            if (!ld_relaxed_gpu(f + (size_t)c * H) && !wait_flag(f + (size_t)c * H)) return false;
-            int fl[15];   // the next 15 chunks' flags, loaded together
-#pragma unroll
-            for (int i = 0; i < 15; ++i) fl[i] = (c + 1 + i < nchunks) ? ld_relaxed_gpu(f + (size_t)(c + 1 + i) * H) : 0;
-            int k = c;
-#pragma unroll
-            for (int i = 0; i < 15; ++i)
-                if (k == c + i && fl[i]) k = c + 1 + i;
-            fence_acquire_gpu();
-            fence_proxy_async_global();
-            known = k;
-        }
-        return true;
-    };
 
     if (t == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(bar_f + i, 1);
-        mbar_init(bar_z, 1);
+        for (int i = 0; i < B_BAR_COUNT; ++i) {
+            const bool all = i == B_BAR_SHI || i == B_BAR_SLO || i == B_BAR_WREADY || i == B_BAR_DREAD ||
+                             i == B_BAR_OSTAGED;
+            mbar_init(bars + i, all ? 14u : 1u);
+        }
         mbar_fence_init();
         *s_abort = 0;
         tma_prefetch_desc(&p.tm_v);
         tma_prefetch_desc(&p.tm_o);
         if (p.gate) tma_prefetch_desc(&p.tm_z);
     }
-    // rows 0-63 of the [0; Q' lo] operand: zeros in both K blocks, written once
-    st_shared_v4(sbase + B_A1L + ((t >> 8) << 14) + 16 * (t & 255), 0u, 0u, 0u, 0u);
-    st_shared_v4(sbase + B_A1L + ((t >> 8) << 14) + 16 * (t & 255) + 4096, 0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-
-    // The copies into shared memory are issued by one producer thread (kProducer, in a warp
-    // of the O half, which has slack when they are due); it counts what it issued so that,
-    // on abort, it can wait for the last copy on each barrier.  It also issues the O stores,
-    // once the O warps have staged them.  Thread 0 issues the MMAs.
-    constexpr int kProducer = 64;
-    bool o_pending = false;   // producer
-    bool mma_open = false;    // thread 0
-    int n_front = 0, n_back = 0, n_v[2] = {0, 0}, n_z = 0;   // producer
-    auto fetch_front = [&](int c) {
-        if (!ready(c)) {   // never published: give up (the waits on bar_f then run out)
-            atomicExch(s_abort, 1);
-            return;
-        }
-        mbar_arrive_expect_tx(bar_f, IMG_FRONT + 16384u);
-        bulk_load(sm + B_A1, image(c), IMG_FRONT, bar_f);
-        bulk_load(sm + B_A1L + 8192, image(c) + IMG_QLO, 8192u, bar_f);    // rows 64-127, K block 0
-        bulk_load(sm + B_A1L + 24576, image(c) + IMG_QLO + 8192, 8192u, bar_f);   // K block 1
-        ++n_front;
-    };
-    auto fetch_back = [&](int c) {
-        if (!ready(c)) {
-            atomicExch(s_abort, 1);
-            return;
-        }
-        mbar_arrive_expect_tx(bar_b, IMG_BACK);
-        bulk_load(sm + B_KTH, image(c) + IMG_KTH, IMG_BACK, bar_b);
-        ++n_back;
-    };
-    auto fetch_v = [&](int c) {   // [64 tok][128 ch] as two 64-channel TMA boxes
-        uint64_t* bar = bar_v + (c & 1);
-        uint8_t* dst = sm + ((c & 1) ? B_V1 : B_V0);
-        mbar_arrive_expect_tx(bar, 16384u);
-        tma_load_3d(dst, &p.tm_v, bar, 0, h, bos + 64 * c);
-        tma_load_3d(dst + 8192, &p.tm_v, bar, 64, h, bos + 64 * c);
-        if (c & 1) ++n_v[1];
-        else ++n_v[0];
-    };
-    if (t == kProducer && nchunks > 0) {
-        fetch_front(0);
-        fetch_back(0);
-        fetch_v(0);
-        if (p.gate) tma_prefetch_3d(&p.tm_z, 0, h, bos);   // the first chunk's logits into L2
-        if (nchunks > 1) {
-            fetch_v(1);
-            prefetch_l2(image(1), IMG_BYTES);
-        }
-    }
-
-    // initial state -> TMEM: lane L = key channel, columns [32 part, 32 part + 32)
+    // initial state -> S^T in TMEM, all 16 warps: lane dv = 32 (w % 4) + laneid, dk columns
+    // [32 (w / 4), +32); a warp reads one dk row's 32 consecutive dv values at a time
     {
+        const int L = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
         float v[32];
         if (p.init_state) {
-            const float4* src = reinterpret_cast<const float4*>(p.init_state + sbase_g + (size_t)L * 128 + 32 * part);
+            const float* src = p.init_state + sbase_g + (size_t)c0 * 128 + L;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 f = __ldg(src + i);
-                v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
-            }
+            for (int i = 0; i < 32; ++i) v[i] = __ldg(src + (size_t)i * 128);
         } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
-        tmem_st32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), v);
+        tmem_st32(tmem_addr(tm, 32 * (warp & 3), B_TM_S + c0), v);
         tmem_wait_st();
     }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
 
-    uint32_t f_par = 0, b_par = 0, v_par = 0, mma_par = 0, z_par = 0;   // v_par: bit b = buffer b's parity
-    bool ok = true;
+    // a snapshot of the state after `done` tokens is due when a full chunk ends there
+    auto snapshot_due = [&](int done) {
+        return p.checkpoints != nullptr && done > 0 && done % p.ckpt_interval == 0 &&
+               done / p.ckpt_interval <= p.ckpt_slots;
+    };
+    // state element (dk, dv) of a snapshot slot: [dk][dv] fp32
+    auto snapshot_at = [&](int done, int dk, int dv) {
+        const int slot = done / p.ckpt_interval - 1;
+        return p.checkpoints + (((size_t)n * H + h) * p.ckpt_slots + slot) * 128 * 128 + (size_t)dk * 128 + dv;
+    };
+    auto fail = [&]() { atomicExch(s_abort, 1); };
     KDA_CLK_DECL(clk);
-    for (int ci = 0; ci < nchunks; ++ci) {
-        const int t0 = bos + 64 * ci;
-        const int BT = min(64, eos - t0);
-        const int vb = ci & 1;
-        if (!mbar_wait_bounded(bar_f, f_par, kWaitNs)) atomicExch(s_abort, 1);
-        if (t == kProducer && o_pending) {   // the previous chunk's O staging (over S hi) has been read out
-            bulk_wait_read();
-            o_pending = false;
-        }
-        tc_fence_before_sync();
-        __syncthreads();
-        tc_fence_after_sync();
-        if (*s_abort) {
-            ok = false;
-            break;
-        }
-        f_par ^= 1u;
-        KDA_CLK(clk, 16);   // front image in, last O staging read out
 
-        // D1 = [Tb; M] V (hi + lo), the half that does not depend on the state, at once
-        bool v_ok = true;   // thread 0
-        if (t == 0) {
+    if (warp != kIssuerWarp && warp != kProducerWarp) {
+        // ------------------------------------------------ the CUDA warps
+        // a warp's columns as 16-column groups: S^T (dk) groups [sbeg, send) of 8; W^T (token)
+        // groups [wbeg, wend) and O^T groups [obeg, oend) of 4 each.  Every warp loads the same
+        // number of groups (the spare loads repeat its last one and are not used), which keeps
+        // the loaded values in registers.
+        const int quarter = warp & 3, slot = warp >> 2;
+        const bool four = quarter < 2;   // lanes 0-63: 4 warps; lanes 64-127: 3 (the roles take one each)
+        const int s3 = slot == 3 ? 2 : slot;
+        const int sbeg = four ? 2 * slot : 3 * s3, send = four ? sbeg + 2 : min(sbeg + 3, 8);
+        const int wbeg = four ? slot : (s3 == 0 ? 0 : s3 + 1), wend = four ? slot + 1 : (s3 == 0 ? 2 : s3 + 2);
+        const int obeg = four ? slot : (s3 == 0 ? 0 : 2 * s3 - 1), oend = four ? slot + 1 : (s3 == 0 ? 1 : s3 == 1 ? 3 : 4);
+        const int L = 32 * quarter + lane;   // dv
+        const float* const gate = p.gate;
+        uint32_t m_par = 0, g_par = 0, sf_par = 0, z_par = 0;   // z_par: bit b = buffer b's parity
+        bool ok = true;
+        for (int ci = 0; ci < nchunks && ok; ++ci) {
+            const int t0 = bos + 64 * ci;
+            const int BT = min(64, eos - t0);
+            const bool snap = snapshot_due(64 * ci);   // the state entering this chunk
+            if (ci > 0) {   // the last chunk's state update is done
+                if (!(ok = role_wait(bar_mma, m_par, s_abort))) break;
+                m_par ^= 1u;
+            }
             tc_fence_after_sync();
-            if (!mbar_wait_bounded(bar_v + vb, (v_par >> vb) & 1u, kWaitNs)) {
-                atomicExch(s_abort, 1);
-                v_ok = false;
-            } else {
-                v_par ^= 1u << vb;
-                const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
-                const uint32_t vt = sbase + (vb ? B_V1 : B_V0);
+            KDA_CLK(clk, 16);   // the last update waited for
+            {
+                float a[3][16];
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_TBH, 128, ks), desc_mnmajor(vt, 64, ks), idesc,
-                              ks > 0 ? 1u : 0u);
+                for (int jj = 0; jj < 3; ++jj)
+                    tmem_ld16(tmem_addr(tm, 32 * quarter, B_TM_S + 16 * min(sbeg + jj, send - 1)), a[jj]);
+                tmem_wait_ld();
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_TBL, 128, ks), desc_mnmajor(vt, 64, ks), idesc, 1u);
-                mma_open = true;
+                for (int jj = 0; jj < 3; ++jj) {   // S^T_hi: bf16 pairs along dk
+                    const int j = sbeg + jj;
+                    if (j < send) {
+                        if (snap) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) *snapshot_at(64 * ci, 16 * j + i, L) = a[jj][i];
+                        }
+                        uint32_t hi[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) hi[i] = pack_bf16x2(a[jj][2 * i], a[jj][2 * i + 1]);
+                        tmem_st8u(tmem_addr(tm, 32 * quarter, B_TM_SH + 8 * j), hi);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_shi);
+                KDA_CLK(clk, 17);   // S^T_hi
+                if (!(ok = role_wait(bar_g, g_par, s_abort))) break;   // gamma_C of this chunk
+                g_par ^= 1u;
+                // S^T again (nothing is held in registers across the wait)
+#pragma unroll
+                for (int jj = 0; jj < 3; ++jj)
+                    tmem_ld16(tmem_addr(tm, 32 * quarter, B_TM_S + 16 * min(sbeg + jj, send - 1)), a[jj]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 3; ++jj) {   // S^T_lo = bf16(S^T - S^T_hi), then S^T <- S^T gamma_C
+                    const int j = sbeg + jj;
+                    if (j < send) {
+                        uint32_t lo[8], d[16];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float2 h2 = bf2_to_f2(pack_bf16x2(a[jj][2 * i], a[jj][2 * i + 1]));
+                            lo[i] = pack_bf16x2(a[jj][2 * i] - h2.x, a[jj][2 * i + 1] - h2.y);
+                        }
+                        tmem_st8u(tmem_addr(tm, 32 * quarter, B_TM_SL + 8 * j), lo);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) d[i] = __float_as_uint(a[jj][i] * sgam[16 * j + i]);
+                        tmem_st16u(tmem_addr(tm, 32 * quarter, B_TM_S + 16 * j), d);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_slo);
+                KDA_CLK(clk, 18);   // S^T_lo and the decay
             }
-        }
-
-        // the state's bf16 B operands: S_hi first, so that the MMAs that read it start while
-        // S_lo = bf16(S - S_hi) is formed; S <- gamma_C S (this chunk's decay, before its update)
-        // then runs while the D1 MMAs, which read only the bf16 copies, execute
-        float a[32];
-        tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), a);
-        tmem_wait_ld();
-        uint32_t hi[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) hi[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
-        store_row32_bf16(sbase + B_SB, L, 4 * part, 128, hi);
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-        KDA_CLK(clk, 17);   // V half of D1 issued, S_hi
-        // D1 += [-Wk; Q'] S_hi + [0; Q' lo] S_hi
-        if (t == 0) {
+            if (!(ok = role_wait(bar_mma, m_par, s_abort))) break;   // D1
+            m_par ^= 1u;
             tc_fence_after_sync();
-            if (v_ok) {
-                const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+            KDA_CLK(clk, 19);   // D1 waited for
+            {
+                float w[2][16];
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_A1, 128, ks), desc_mnmajor(sbase + B_SB, 128, ks),
-                              idesc, 1u);
+                for (int jj = 0; jj < 2; ++jj)
+                    tmem_ld16(tmem_addr(tm, 32 * quarter, B_TM_D1 + 16 * min(wbeg + jj, wend - 1)), w[jj]);
+                tmem_wait_ld();
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_A1L, 128, ks), desc_mnmajor(sbase + B_SB, 128, ks),
-                              idesc, 1u);
+                for (int jj = 0; jj < 2; ++jj) {   // W^T (hi + lo): bf16 pairs along the tokens
+                    const int j = wbeg + jj;
+                    if (j < wend) {
+                        uint32_t hi[8], lo[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) split_bf16x2(w[jj][2 * i], w[jj][2 * i + 1], hi[i], lo[i]);
+                        tmem_st8u(tmem_addr(tm, 32 * quarter, B_TM_WH + 8 * j), hi);
+                        tmem_st8u(tmem_addr(tm, 32 * quarter, B_TM_WL + 8 * j), lo);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_wready);   // W^T written
             }
-        }
-        {
-            uint32_t lo[16];
+            KDA_CLK(clk, 20);   // W^T split
+            float o[2][16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float2 h2 = bf2_to_f2(hi[i]);
-                lo[i] = pack_bf16x2(a[2 * i] - h2.x, a[2 * i + 1] - h2.y);
-            }
-            store_row32_bf16(sbase + B_SL, L, 4 * part, 128, lo);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-        KDA_CLK(clk, 18);   // S_lo (under the S_hi MMAs)
-        // D1 += [-Wk; Q'] S_lo
-        if (t == 0) {
-            tc_fence_after_sync();
-            if (v_ok) {
-                const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+            for (int jj = 0; jj < 2; ++jj)
+                tmem_ld16(tmem_addr(tm, 32 * quarter, B_TM_D1 + 64 + 16 * min(obeg + jj, oend - 1)), o[jj]);
+            tmem_wait_ld();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_dread);   // D1 read out: the next chunk's MMAs may overwrite it
+            if (BT == 64) {   // O staged for the TMA store: token r, dv L in box L / 32 (a warp: one row per store)
+                if (ci >= 2) {   // the store of two chunks back has read this buffer
+                    if (!(ok = role_wait(bar_sfree, sf_par, s_abort))) break;
+                    sf_par ^= 1u;
+                }
+                // (the parameters are read once: the asm stores' memory clobbers would reload them)
+                const uint32_t box = sbase + B_OST + 32768u * (ci & 1) + 8192u * (L >> 5);
+                if (gate) {   // the logits TMA put in the same positions of the buffer
+                    if (!(ok = role_wait(bar_z + (ci & 1), (z_par >> (ci & 1)) & 1u, s_abort))) break;
+                    z_par ^= 1u << (ci & 1);
+                }
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    umma_bf16(tm + B_TM_D1, desc_kmajor(sbase + B_A1, 128, ks), desc_mnmajor(sbase + B_SL, 128, ks),
-                              idesc, 1u);
-                umma_commit(bar_mma);
-                mma_open = true;
-            }
-        }
-        {
-            const float gc = sgam[L];
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int j = obeg + jj;
+                    if (j < oend) {
+                        uint32_t at[16];
+                        float v[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] *= gc;
-            tmem_st32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), a);
-            tmem_wait_st();
-        }
-        if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
-        mma_par ^= 1u;
-        tc_fence_after_sync();
-        KDA_CLK(clk, 19);   // decay, D1 complete
-        if (t == 0) mma_open = false;
-        if (t == kProducer) {   // the front image and this v buffer have been read
-            if (p.gate && BT == 64) {   // this chunk's gate logits into the O staging boxes (S_hi is read)
-                mbar_arrive_expect_tx(bar_z, 32768u);
+                        for (int i = 0; i < 16; ++i) {
+                            at[i] = box + sw128_off_f32(16 * j + i, L & 31, 64);
+                            v[i] = o[jj][i];
+                        }
+                        if (gate) {   // out = o * sigmoid(z)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) tma_load_3d(sm + B_OST + 8192 * j, &p.tm_z, bar_z, 32 * j, h, t0);
-                ++n_z;
-                if (ci + 1 < nchunks) {   // and the next chunk's into L2
+                            for (int i = 0; i < 16; ++i) v[i] = gate1(v[i], ld_shared_f32(at[i]));
+                        }
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) tma_prefetch_3d(&p.tm_z, 32 * j, h, t0 + 64);
+                        for (int i = 0; i < 16; ++i) st_shared_f32(at[i], v[i]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_ostaged);
+            } else {   // a sequence's ragged last chunk: direct stores, token t0 + r, dv L
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int j = obeg + jj;
+                    if (j < oend) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int r = 16 * j + i;
+                            if (r < BT) {
+                                const size_t o0 = ((size_t)(t0 + r) * H + h) * 128 + L;
+                                p.out[o0] = p.gate ? gate1(o[jj][i], __ldg(p.gate + o0)) : o[jj][i];
+                            }
+                        }
+                    }
                 }
             }
-            if (ci + 1 < nchunks) fetch_front(ci + 1);
+            KDA_CLK(clk, 21);   // O stored
+            KDA_CLK_COUNT(clk, 30);
+        }
+        if (ok && nchunks > 0) {   // the last chunk's state update
+            ok = role_wait(bar_mma, m_par, s_abort);
+            m_par ^= 1u;
+        }
+        if (!ok) fail();
+    } else if (t == 32 * kIssuerWarp) {
+        // ------------------------------------------------ the MMA issuer
+        uint32_t shi_par = 0, slo_par = 0, wr_par = 0, dr_par = 0, f_par = 0, tb_par = 0, b_par = 0, v_par = 0;
+        bool ok = true;
+        const uint32_t idesc_v = idesc_bf16_f32(128, 128, 1, 0);   // A (v) MN-major, B K-major
+        const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+        const uint32_t idesc64 = idesc_bf16_f32(128, 64, 0, 0);
+        const uint32_t d1 = tm + B_TM_D1;
+        for (int ci = 0; ci < nchunks && ok; ++ci) {
+            const int vb = ci & 1;
+            // V^T [Tb; M]^T (hi, lo): needs this chunk's [Tb; M] and v, and the last chunk's D1
+            // read out
+            if (ci > 0) {
+                if (!(ok = role_wait(bar_dread, dr_par, s_abort))) break;
+                dr_par ^= 1u;
+            }
+            if (!(ok = role_wait(bar_tb, tb_par, s_abort) && role_wait(bar_v + vb, (v_par >> vb) & 1u, s_abort))) break;
+            tb_par ^= 1u;
+            v_par ^= 1u << vb;
+            tc_fence_after_sync();
+            const uint32_t vt = sbase + (vb ? B_V1 : B_V0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16(d1, desc_mnmajor(vt, 64, ks), desc_kmajor(sbase + B_TBH, 128, ks), idesc_v, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16(d1, desc_mnmajor(vt, 64, ks), desc_kmajor(sbase + B_TBL, 128, ks), idesc_v, 1u);
+            umma_commit(bar_vdone);
+            // S^T_hi [-Wk; Q']^T, and S^T_hi Q'_lo^T into O's columns, once S^T_hi is written
+            if (!(ok = role_wait(bar_shi, shi_par, s_abort) && role_wait(bar_f, f_par, s_abort))) break;
+            shi_par ^= 1u;
+            f_par ^= 1u;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                umma_bf16_tmem_a(d1, tm + B_TM_SH + 8 * ks, desc_kmajor(sbase + B_A1, 128, ks), idesc, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                umma_bf16_tmem_a(d1 + 64, tm + B_TM_SH + 8 * ks, desc_kmajor(sbase + B_QLO, 64, ks), idesc64, 1u);
+            // S^T_lo [-Wk; Q']^T, once S^T_lo is written
+            if (!(ok = role_wait(bar_slo, slo_par, s_abort))) break;
+            slo_par ^= 1u;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                umma_bf16_tmem_a(d1, tm + B_TM_SL + 8 * ks, desc_kmajor(sbase + B_A1, 128, ks), idesc, 1u);
+            umma_commit(bar_mma);
+            // S^T += W^T_hi K~_hi + W^T_lo K~_hi + W^T_hi K~_lo, once W^T is written
+            if (!(ok = role_wait(bar_wready, wr_par, s_abort) && role_wait(bar_b, b_par, s_abort))) break;
+            wr_par ^= 1u;
+            b_par ^= 1u;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + B_TM_S, tm + B_TM_WH + 8 * ks, desc_kmajor(sbase + B_KTH, 128, ks), idesc, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + B_TM_S, tm + B_TM_WL + 8 * ks, desc_kmajor(sbase + B_KTH, 128, ks), idesc, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16_tmem_a(tm + B_TM_S, tm + B_TM_WH + 8 * ks, desc_kmajor(sbase + B_KTL, 128, ks), idesc, 1u);
+            umma_commit(bar_mma);
+        }
+        if (!ok) fail();
+        // every MMA issued has completed before the CTA moves on (bounded)
+        umma_commit(bar_end);
+        if (!mbar_wait_bounded(bar_end, 0u, kWaitNs)) fail();
+    } else if (t == 32 * kProducerWarp) {
+        // ------------------------------------------------ the copy producer
+        // kFlags: chunk c's images are fetched only once its item is published.  The flags of up
+        // to 16 chunks ahead are read with relaxed loads and one acquire (and proxy) fence covers
+        // all that are set, so that a fence is paid per batch, not per fetch; the producer
+        // blocks (bounded) only when chunk c itself is not yet published.
+        int known = -1;   // chunks <= known are published and acquired
+        auto ready = [&](int c) {
+            if constexpr (kFlags) {
+                if (c <= known) return true;
+                const int* f = sp.flags + (size_t)gc0 * H + h;
+                if (!ld_relaxed_gpu(f + (size_t)c * H) && !wait_flag(f + (size_t)c * H)) return false;
+                int fl[15];   // the next 15 chunks' flags, loaded together
+#pragma unroll
+                for (int i = 0; i < 15; ++i)
+                    fl[i] = (c + 1 + i < nchunks) ? ld_relaxed_gpu(f + (size_t)(c + 1 + i) * H) : 0;
+                int k = c;
+#pragma unroll
+                for (int i = 0; i < 15; ++i)
+                    if (k == c + i && fl[i]) k = c + 1 + i;
+                fence_acquire_gpu();
+                fence_proxy_async_global();
+                known = k;
+            }
+            return true;
+        };
+        int n_front = 0, n_tb = 0, n_back = 0, n_gam = 0, n_v[2] = {0, 0}, n_z[2] = {0, 0};
+        auto fetch_z = [&](int c) {   // a full chunk's gate logits into its O staging buffer (free by now)
+            if (p.gate && c < nchunks && eos - (bos + 64 * c) >= 64) {
+                uint64_t* bar = bar_z + (c & 1);
+                mbar_arrive_expect_tx(bar, 32768u);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    tma_load_3d(sm + B_OST + 32768u * (c & 1) + 8192 * j, &p.tm_z, bar, 32 * j, h, bos + 64 * c);
+                if (c & 1) ++n_z[1];
+                else ++n_z[0];
+            }
+        };
+        auto fetch_gamma = [&](int c) {   // gamma_C: read by the S^T_lo pass
+            if (!ready(c)) return false;
+            mbar_arrive_expect_tx(bar_g, 512u);
+            bulk_load(sm + B_GAM, image(c) + IMG_GAM, 512u, bar_g);
+            ++n_gam;
+            return true;
+        };
+        auto fetch_tb = [&](int c) {   // [Tb; M] hi + lo: read by the V^T [Tb; M]^T MMAs
+            if (!ready(c)) return false;
+            mbar_arrive_expect_tx(bar_tb, 32768u);
+            bulk_load(sm + B_TBH, image(c) + IMG_TBH, 32768u, bar_tb);
+            ++n_tb;
+            return true;
+        };
+        auto fetch_front = [&](int c) {   // [-Wk; Q'] and Q' lo: read by the S^T MMAs of D1
+            if (!ready(c)) return false;
+            mbar_arrive_expect_tx(bar_f, 32768u + 16384u);
+            bulk_load(sm + B_A1, image(c), 32768u, bar_f);
+            bulk_load(sm + B_QLO, image(c) + IMG_QLO, 16384u, bar_f);
+            ++n_front;
+            return true;
+        };
+        auto fetch_back = [&](int c) {   // K~^T hi + lo: read by the state update
+            if (!ready(c)) return false;
+            mbar_arrive_expect_tx(bar_b, IMG_BACK);
+            bulk_load(sm + B_KTH, image(c) + IMG_KTH, IMG_BACK, bar_b);
+            ++n_back;
+            return true;
+        };
+        auto fetch_v = [&](int c) {   // [64 tok][128 ch] as two 64-channel TMA boxes
+            uint64_t* bar = bar_v + (c & 1);
+            uint8_t* dst = sm + ((c & 1) ? B_V1 : B_V0);
+            mbar_arrive_expect_tx(bar, 16384u);
+            tma_load_3d(dst, &p.tm_v, bar, 0, h, bos + 64 * c);
+            tma_load_3d(dst + 8192, &p.tm_v, bar, 64, h, bos + 64 * c);
+            if (c & 1) ++n_v[1];
+            else ++n_v[0];
+        };
+        bool ok = true;
+        if (nchunks > 0) {
+            ok = fetch_tb(0) && fetch_gamma(0) && fetch_front(0) && fetch_back(0);
+            fetch_v(0);
+            fetch_z(0);
+            fetch_z(1);
+            if (nchunks > 1) {
+                fetch_v(1);
+                prefetch_l2(image(1), IMG_BYTES);
+            }
+        }
+        uint32_t vd_par = 0, slo_par = 0, wr_par = 0, os_par = 0;
+        for (int ci = 0; ci < nchunks && ok; ++ci) {
+            const int t0 = bos + 64 * ci;
+            const bool full = eos - t0 >= 64;
+            // the V^T [Tb; M]^T MMAs are done: [Tb; M] and this v buffer have been read
+            if (!(ok = role_wait(bar_vdone, vd_par, s_abort))) break;
+            vd_par ^= 1u;
+            if (ci + 1 < nchunks && !(ok = fetch_tb(ci + 1))) break;
             if (ci + 2 < nchunks) {
                 fetch_v(ci + 2);
                 prefetch_l2(image(ci + 2), IMG_BYTES);   // so that the next fetches come from L2
             }
-        }
-
-        // rows 0-63 -> W (hi + lo) B operands (over S lo, which D1 has read), and S += K~^T W as
-        // soon as the 8 warps holding them are done; rows 64-127 = O staged (over S hi) for TMA
-        // stores meanwhile
-        tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_D1 + 32 * part), a);
-        tmem_wait_ld();
-        if (quarter < 2) {
-            uint32_t hi[16], lo[16];
+            // S^T_lo is formed: gamma_C has been read, and the last update has read the back image
+            if (!(ok = role_wait(bar_slo, slo_par, s_abort))) break;
+            slo_par ^= 1u;
+            if (ci > 0 && !(ok = fetch_back(ci))) break;
+            if (ci + 1 < nchunks && !(ok = fetch_gamma(ci + 1))) break;
+            // D1 is in: [-Wk; Q'] and Q' lo have been read
+            if (!(ok = role_wait(bar_wready, wr_par, s_abort))) break;
+            wr_par ^= 1u;
+            if (ci + 1 < nchunks && !(ok = fetch_front(ci + 1))) break;
+            if (p.gate && ci + 2 < nchunks) {   // the gate logits of two chunks ahead into L2
 #pragma unroll
-            for (int i = 0; i < 16; ++i) split_bf16x2(a[2 * i], a[2 * i + 1], hi[i], lo[i]);
-            store_row32_bf16(sbase + B_WH, L, 4 * part, 64, hi);
-            store_row32_bf16(sbase + B_WL, L, 4 * part, 64, lo);
-            fence_proxy_async_smem();
-            named_sync(1, 256);
-            if (t == 0) {   // S += K~^T W (hi hi + hi lo + lo hi)
-                tc_fence_after_sync();
-                if (!mbar_wait_bounded(bar_b, b_par, kWaitNs)) {
-                    atomicExch(s_abort, 1);
-                } else {
-                    b_par ^= 1u;
-                    const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        umma_bf16(tm + B_TM_S, desc_kmajor(sbase + B_KTH, 128, ks),
-                                  desc_mnmajor(sbase + B_WH, 64, ks), idesc, 1u);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        umma_bf16(tm + B_TM_S, desc_kmajor(sbase + B_KTH, 128, ks),
-                                  desc_mnmajor(sbase + B_WL, 64, ks), idesc, 1u);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        umma_bf16(tm + B_TM_S, desc_kmajor(sbase + B_KTL, 128, ks),
-                                  desc_mnmajor(sbase + B_WH, 64, ks), idesc, 1u);
-                    umma_commit(bar_mma);
-                    mma_open = true;
-                }
+                for (int j = 0; j < 4; ++j) tma_prefetch_3d(&p.tm_z, 32 * j, h, t0 + 128);
             }
-        } else {   // O row r = token t0 + r, dv columns [32 part, +32)
-            const int r = L - 64;
-            const size_t o0 = ((size_t)(t0 + r) * H + h) * 128 + 32 * part;
-            if (BT == 64) {   // box `part` = dv columns [32 part, +32)
-                const uint32_t box = sbase + B_OST + 8192 * part;
-                if (p.gate) {   // the output gate, o * sigmoid(z), on the logits TMA put in the boxes
-                    if (!mbar_wait_bounded(bar_z, z_par, kWaitNs)) atomicExch(s_abort, 1);
-                    z_par ^= 1u;
-                    stage_gated_row(box, r, a);
-                } else {
+            if (full) {   // O staged: stored from its buffer; the last chunk's buffer is then free once read
+                if (!(ok = role_wait(bar_ostaged, os_par, s_abort))) break;
+                os_par ^= 1u;
+                uint8_t* buf = sm + B_OST + 32768u * (ci & 1);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        st_shared_f4(box + sw128_off_f32(r, 4 * q, 64), a[4 * q], a[4 * q + 1], a[4 * q + 2],
-                                     a[4 * q + 3]);
-                }
-                fence_proxy_async_smem();
-                named_sync(3, 256);   // the 8 O warps: the boxes are complete
-                if (t == kProducer) {   // stored now, so that they are read out before the next S build
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) tma_store_3d(&p.tm_o, sm + B_OST + 8192 * j, 32 * j, h, t0);
-                    bulk_commit();
-                    o_pending = true;
-                }
-            } else if (r < BT) {   // a sequence's ragged last chunk: direct stores
-                float4* dst = reinterpret_cast<float4*>(p.out + o0);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 o = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
-                    dst[i] = p.gate ? gate4(o, p.gate + o0 + 4 * i) : o;
+                for (int j = 0; j < 4; ++j) tma_store_3d(&p.tm_o, buf + 8192 * j, 32 * j, h, t0);
+                bulk_commit();
+                if (ci >= 1) {
+                    bulk_wait_read_group<1>();
+                    mbar_arrive(bar_sfree);
+                    fetch_z(ci + 1);   // into the buffer the store of chunk ci - 1 has just read
                 }
             }
         }
-        if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
-        mma_par ^= 1u;
-        KDA_CLK(clk, 20);   // W split, state update (O staged alongside)
-        if (t == kProducer && ci + 1 < nchunks) fetch_back(ci + 1);
-        if (t == 0) mma_open = false;
-        // state snapshot after a full chunk that ends on a checkpoint boundary
-        {
-            const int done = t0 + 64 - bos;
-            if (p.checkpoints && BT == 64 && done % p.ckpt_interval == 0 && done / p.ckpt_interval <= p.ckpt_slots) {
-                tc_fence_after_sync();
-                const int slot = done / p.ckpt_interval - 1;
-                float v[32];
-                tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), v);
-                tmem_wait_ld();
-                float4* dst = reinterpret_cast<float4*>(
-                    p.checkpoints + (((size_t)n * H + h) * p.ckpt_slots + slot) * 128 * 128 + (size_t)L * 128 + 32 * part);
+        bulk_wait_all();   // the staged O fully written before the CTA's shared memory goes away
+        if (!ok) {   // record it, and let the copies in flight land (bounded): the last on each barrier
+            fail();
+            if (n_front > 0) mbar_wait_bounded(bar_f, (uint32_t)(n_front - 1) & 1u, kWaitNs);
+            if (n_tb > 0) mbar_wait_bounded(bar_tb, (uint32_t)(n_tb - 1) & 1u, kWaitNs);
+            if (n_back > 0) mbar_wait_bounded(bar_b, (uint32_t)(n_back - 1) & 1u, kWaitNs);
+            if (n_gam > 0) mbar_wait_bounded(bar_g, (uint32_t)(n_gam - 1) & 1u, kWaitNs);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                tc_fence_before_sync();
+            for (int i = 0; i < 2; ++i) {
+                if (n_v[i] > 0) mbar_wait_bounded(bar_v + i, (uint32_t)(n_v[i] - 1) & 1u, kWaitNs);
+                if (n_z[i] > 0) mbar_wait_bounded(bar_z + i, (uint32_t)(n_z[i] - 1) & 1u, kWaitNs);
             }
         }
-        KDA_CLK(clk, 21);   // checkpoint
-        KDA_CLK_COUNT(clk, 30);
     }
-
-    if (t == kProducer) bulk_wait_all();   // staged O fully written before the CTA's shared memory goes away
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    if (ok && p.final_state) {
-        float v[32];
-        tmem_ld32(tmem_addr(tm, 32 * quarter, B_TM_S + 32 * part), v);
-        tmem_wait_ld();
-        float4* dst = reinterpret_cast<float4*>(p.final_state + sbase_g + (size_t)L * 128 + 32 * part);
+    const bool ok = *reinterpret_cast<volatile int*>(s_abort) == 0;
+    if (ok) {   // the last chunk's snapshot, if due, and the final state: all 16 warps
+        const int L = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
+        const bool snap = nchunks > 0 && eos - bos == 64 * nchunks && snapshot_due(64 * nchunks);
+        if (snap || p.final_state) {
+            float v[32];
+            tmem_ld32(tmem_addr(tm, 32 * (warp & 3), B_TM_S + c0), v);
+            tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    }
-    if (!ok && t == 0) {
-        // a wait gave up: record it, let in-flight MMAs land (bounded), then leave
+            for (int i = 0; i < 32; ++i) {
+                if (snap) *snapshot_at(64 * nchunks, c0 + i, L) = v[i];
+                if (p.final_state) p.final_state[sbase_g + (size_t)(c0 + i) * 128 + L] = v[i];
+            }
+        }
+    } else if (t == 0) {
         report_status(p.status, kDevTimeout);
-        if (mma_open) mbar_wait_bounded(bar_mma, mma_par, kWaitNs);
-    }
-    if (!ok && t == kProducer) {   // and the copies: the last one issued on each barrier (bounded)
-        if (n_front > 0) mbar_wait_bounded(bar_f, (uint32_t)(n_front - 1) & 1u, kWaitNs);
-        if (n_back > 0) mbar_wait_bounded(bar_b, (uint32_t)(n_back - 1) & 1u, kWaitNs);
-        for (int i = 0; i < 2; ++i)
-            if (n_v[i] > 0) mbar_wait_bounded(bar_v + i, (uint32_t)(n_v[i] - 1) & 1u, kWaitNs);
-        if (n_z > 0) mbar_wait_bounded(bar_z, (uint32_t)(n_z - 1) & 1u, kWaitNs);
     }
     tc_fence_before_sync();
     __syncthreads();

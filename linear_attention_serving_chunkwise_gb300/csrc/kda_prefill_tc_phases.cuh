@@ -183,6 +183,18 @@ __device__ __forceinline__ void st_shared_f4(uint32_t saddr, float a, float b, f
     st_shared_v4(saddr, __float_as_uint(a), __float_as_uint(b), __float_as_uint(c), __float_as_uint(d));
 }
 
+__device__ __forceinline__ float ld_shared_f32(uint32_t saddr)
+{
+    float a;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(a) : "r"(saddr) : "memory");
+    return a;
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t saddr, float a)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(saddr), "f"(a) : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr)
 {
     uint4 v;

@@ -30,8 +30,8 @@ PREP_SPANS = ["loop top: claims, beta", "off-diagonal rows", "A/P tf32 MMA, K~ s
               "solve (seed, image stores, publication alongside)", "Tb operands", "M = P Tb, Tb rows",
               "M rows, [Tb; M] staged", "next item's phase 1 under the [Wk; -Q'] MMA", "wait for that MMA",
               "[-Wk; Q'] hi, Q' lo staged"]
-SCAN_SPANS = ["front image in, last O staging read", "V half of D1 issued, S_hi", "S_lo (under the S_hi MMAs)",
-              "decay, D1 complete", "W split, state update (O staged alongside)", "checkpoint"]
+SCAN_SPANS = ["waited for the last update", "S^T_hi into tensor memory", "gamma_C waited for, S^T_lo and the decay",
+              "waited for D1", "W^T split into tensor memory", "O read out and stored"]
 
 
 def _measure(lib, reader, seqlens, heads, prologue=0):

@@ -46,7 +46,8 @@ def test_plan_selects_the_path(cuda_lib):
     assert _plan(cuda_lib, 1, 8192, 112)["kernel_launches"] >= 2
     assert _plan(cuda_lib, 1, 8192, 124)["kernel_launches"] == 3
     assert _plan(cuda_lib, 1, 8192, 128)["kernel_launches"] == 3
-    assert _plan(cuda_lib, 1, 8192, 136)["kernel_launches"] == 1
+    assert _plan(cuda_lib, 1, 8192, 136)["kernel_launches"] == 3
+    assert _plan(cuda_lib, 1, 8192, 144)["kernel_launches"] == 1
     assert _plan(cuda_lib, 2, 8192, 96)["kernel_launches"] >= 2   # 192 units: a second wave of 40
     long = _plan(cuda_lib, 1, 64 * 400, 96)     # 38,496 items: over the workspace cap
     assert long["kernel_launches"] == 1 and long["workspace_bytes"] == 0
