@@ -607,7 +607,7 @@ def run_cuda(args, world, rank, local):
         cp_ms = _max_over_ranks(k0.elapsed_time(k1) / cp_steps, world)
         cp.update({"ms_per_call": cp_ms, "tokens_per_s": tokens_per_step / (cp_ms / 1e3),
                    "vs_plain_call": ms_per_step / cp_ms, "steps": cp_steps,
-                   "gpu_launches_per_call": "3 prefill calls (2 launches each at these 192 units), 1 kda_state_combine"})
+                   "gpu_launches_per_call": "3 prefill calls (3 launches each at these 192 units: offsets, prep, scan), 1 kda_state_combine"})
     except Exception as exc:   # noqa: BLE001 -- recorded in the line instead of ending the run
         cp["error"] = f"{type(exc).__name__}: {exc}"
     clocks = sampler.stop()

@@ -90,6 +90,11 @@ def main(argv=None):
         print("the same with the input prologue (raw draws, every prologue bit)")
         _table("chunk prep, per item", v, PREP_SPANS, 0, 31)
         _table("state scan, per chunk", v, SCAN_SPANS, 16, 30)
+    # the same path as separate prep and scan launches (124 units): the scan's table without
+    # waits on items still being prepared
+    v = _measure(lib, "kda_phase_clocks_split", [8192], 124)
+    print("chunk-parallel path, B=1 H=124 T=8192 (separate prep and scan launches, CTA 0 of each)")
+    _table("state scan, per chunk", v, SCAN_SPANS, 16, 30)
     # one CTA per unit: 4 sequences x 2048 tokens, H=38 (152 units, one wave)
     v = _measure(lib, "kda_phase_clocks_tc", [2048] * 4, 38)
     print("one CTA per (sequence, head), 4 x 2048 tokens, H=38, dk=dv=128 bf16 (CTA 0)")
