@@ -1302,7 +1302,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_scan_kernel(const __gri
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tm = *tslot;
-    scan_unit<false>(sp, sm, tm, blockIdx.x);
+    // the units longest sequence first (the scratch: the O staging, unused until the scan)
+    const int H = sp.p.num_heads;
+    const int n = unit_sequence(sp.p.cu_seqlens, sp.p.num_seqs, (int)blockIdx.x / H, reinterpret_cast<int*>(sm + B_OST));
+    scan_unit<false>(sp, sm, tm, n * H + (int)blockIdx.x % H);
     tc_fence_before_sync();
     __syncthreads();
     if ((threadIdx.x >> 5) == 0) tmem_dealloc(tm, B_TM_COLS);

@@ -72,7 +72,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     const uint32_t sbase = smem_u32(sm);
 
     const int H = p.num_heads;
-    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    const int n = unit_sequence(p.cu_seqlens, p.num_seqs, (int)blockIdx.x / H, reinterpret_cast<int*>(sm + OFF_X));
+    const int h = blockIdx.x % H;
     int bos, eos;
     if (!seq_bounds(p.cu_seqlens, n, p.num_seqs, p.total_tokens, p.status, bos, eos)) return;
     const int nchunks = (eos - bos + 63) >> 6;

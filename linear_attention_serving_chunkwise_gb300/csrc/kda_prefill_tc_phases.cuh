@@ -292,6 +292,36 @@ __device__ __forceinline__ void stage_gated_row(uint32_t box, int r, const float
     }
 }
 
+// ---------------------------------------------------------------- unit order
+// The sequence a CTA of a one-CTA-per-unit launch takes: CTA b runs rank b / H of the
+// sequences ordered longest first (ties by index), so that, as the CTAs of later waves start
+// where earlier ones finish, no long sequence starts last (largest-first list scheduling).
+// All threads of the CTA call it, before anything else uses `scratch` (N + 1 ints of shared
+// memory).  Batches of more than kUnitOrderMaxSeqs sequences keep their order: ranking them
+// would cost each CTA more than it saves.  Malformed cu_seqlens still give a permutation
+// (the bounds check that follows reports them).
+constexpr int kUnitOrderMaxSeqs = 256;
+__device__ __noinline__ int unit_sequence(const int32_t* cu_seqlens, int num_seqs, int rank, int* scratch)
+{
+    if (cu_seqlens == nullptr || num_seqs <= 1 || num_seqs > kUnitOrderMaxSeqs) return rank;
+    const int t = threadIdx.x;
+    if (t < num_seqs) scratch[t] = __ldg(cu_seqlens + t + 1) - __ldg(cu_seqlens + t);
+    __syncthreads();
+    if (t < num_seqs) {
+        const int mine = scratch[t];
+        int r = 0;
+        for (int j = 0; j < num_seqs; ++j) {
+            const int other = scratch[j];
+            r += (other > mine || (other == mine && j < t)) ? 1 : 0;
+        }
+        if (r == rank) scratch[kUnitOrderMaxSeqs] = t;
+    }
+    __syncthreads();
+    const int n = scratch[kUnitOrderMaxSeqs];
+    __syncthreads();   // the scratch is free again
+    return n;
+}
+
 // ---------------------------------------------------------------- phase 1a: per-channel cumsum
 // Thread (c = t % 128, J = t / 128) forms the sub-tile-local cumsum
 // lambda_r = sum_{s = 16J}^{r} g_s log2(e) of sub-tile J of column c (rows past the chunk's
