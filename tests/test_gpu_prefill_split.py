@@ -179,6 +179,30 @@ def test_split_separate_launches_sampled(cuda_lib):
     check("separate-launch split final state", fin[0, heads].cpu(), rs, tol_for(torch.bfloat16))
 
 
+@pytest.mark.parametrize("gated", [False, True], ids=["plain", "gated"])
+def test_split_separate_launches_uneven_sequences(cuda_lib, gated):
+    """5 uneven sequences x 32 heads = 160 units: separate prep and scan launches, whose scan
+    CTAs take their sequences longest first; every unit against the oracle (the state scan's
+    ragged last chunks, one-chunk sequences, and with the gate its logits loaded into the O
+    staging buffers a chunk ahead)."""
+    import oracle
+    lens = [700, 64, 1300, 200, 900]
+    H = 32
+    cfg = W.random_prefill_config(lens, H, 128, torch.bfloat16, init="normal")
+    assert _plan(cuda_lib, len(lens), cfg.total_tokens, H)["kernel_launches"] == 3
+    d = W.make_prefill_inputs(cfg, seed=99)
+    g = to_device(d)
+    z = W.make_gate_logits((cfg.total_tokens, H, 128), seed=100, device="cuda") if gated else None
+    out, fin = cuda_lib.prefill(g["q"], g["k"], g["v"], g["g"], g["beta"], g["cu_seqlens"], g["init_state"], gate=z)
+    torch.cuda.synchronize()
+    assert cuda_lib.last_device_status() == cuda_lib.KDA_OK
+    ref_o, ref_s = oracle_full(d)
+    if gated:
+        ref_o = oracle.output_gate(ref_o, z.cpu())
+    check("separate-launch varlen out", out.cpu(), ref_o, tol_for(torch.bfloat16))
+    check("separate-launch varlen final state", fin.cpu(), ref_s, tol_for(torch.bfloat16))
+
+
 def test_concurrent_calls_on_two_streams(cuda_lib):
     """Two single-launch prefills on two streams with their own workspaces, and a decode on a
     third stream, in flight together: each equals its run alone, bit for bit (cooperative
