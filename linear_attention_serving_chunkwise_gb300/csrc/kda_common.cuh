@@ -40,7 +40,9 @@ __device__ __forceinline__ float l2_scale(float x, float inv, __nv_bfloat16)
 {
     return __bfloat162float(__float2bfloat16_rn(x * inv));
 }
-__device__ __forceinline__ float l2_inv(float sumsq) { return 1.f / fmaxf(sqrtf(sumsq), kL2Eps); }
+// 1 / max(||x||, eps) = rsqrt(max(||x||^2, eps^2)) (eps^2 = 1e-24 is a normal float), by the
+// fast reciprocal square root: a few ulp of fp32, far below the bf16 rounding that follows
+__device__ __forceinline__ float l2_inv(float sumsq) { return rsqrtf(fmaxf(sumsq, kL2Eps * kL2Eps)); }
 
 // Output gate (llm-atlas Q08, read as an elementwise sigmoid over the read-out channels):
 // o <- o * sigmoid(z), with the fast sigmoid (it runs on every output element, in the O

@@ -323,39 +323,70 @@ __device__ __noinline__ int unit_sequence(const int32_t* cu_seqlens, int num_seq
 }
 
 // ---------------------------------------------------------------- phase 1a: per-channel cumsum
+// sigmoid(z_i) for the prologue's four decay logits with one reciprocal: d_i = 1 + e^{-z_i}
+// and 1/d_0 = d_1 d_2 d_3 / (d_0 d_1 d_2 d_3), likewise for the others.  z is clamped below at
+// -20, where sigmoid(z) < 2.1e-9 (a decay e^{-5 sigmoid(z)} within 1.1e-8 of 1 either way) and
+// the product of four d_i stays below 5.5e34, a normal float with a normal reciprocal.  Each
+// result is a few ulp of fp32 from the exact value.
+__device__ __forceinline__ void sigmoid4(float (&z)[4])
+{
+    float d[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = 1.f + ex2f(-fmaxf(z[i], -20.f) * kLog2e);
+    const float p01 = d[0] * d[1], p23 = d[2] * d[3];
+    const float r = rcpf(p01 * p23);
+    const float r01 = r * p23, r23 = r * p01;   // 1 / (d_0 d_1), 1 / (d_2 d_3)
+    z[0] = d[1] * r01;
+    z[1] = d[0] * r01;
+    z[2] = d[3] * r23;
+    z[3] = d[2] * r23;
+}
+
 // Thread (c = t % 128, J = t / 128) forms the sub-tile-local cumsum
 // lambda_r = sum_{s = 16J}^{r} g_s log2(e) of sub-tile J of column c (rows past the chunk's
 // end count as 0), replaces g_r in the tile by x_r = 2^{lambda_r} = e^{Gamma_r - rho_J}
 // (in (0, 1], a normal float since g >= -5) and stores D_J = 2^{s_J}, the last x of the
 // sub-tile (s_J: the sub-tile's sum).
-// With the prologue's kProG bit the tile holds logits z and g = -5 sigmoid(z) is used.
+// With the prologue's kProG bit the tile holds logits z and g = -5 sigmoid(z) is used
+// (sigmoid4 on four rows at a time; the step adds sigmoid(z) (-5 log2(e)) in one rounding).
 template <bool kHoist = false>
 __device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, int BT, int prologue = 0)
 {
     const int c = t & 127, J = t >> 7;
+    const bool logits = (prologue & kProG) != 0;
+    const float step = logits ? kGMin * kLog2e : kLog2e;
     float acc = 0.f, x = 1.f;
-    if constexpr (kHoist) {   // the 16 loads first (16 more registers live)
-        float gv[16];
+    // rows [16 J + 4 m, +4) of the column: g, or sigmoid(z); 0 past the chunk's end
+    auto quad = [&](int m, float (&w)[4]) {
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            const int r = 16 * J + rr;
-            gv[rr] = (r < BT) ? g_of(*reinterpret_cast<const float*>(sm + OFF_G + g_off(r, c)), prologue) : 0.f;
-        }
+        for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const float*>(sm + OFF_G + g_off(16 * J + 4 * m + i, c));
+        if (logits) sigmoid4(w);
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            acc = fmaf(gv[rr], kLog2e, acc);
-            x = ex2f(acc);
-            *reinterpret_cast<float*>(sm + OFF_G + g_off(16 * J + rr, c)) = x;
-        }
+        for (int i = 0; i < 4; ++i) w[i] = (16 * J + 4 * m + i < BT) ? w[i] : 0.f;
+    };
+    if constexpr (kHoist) {   // all 16 loads first (16 more registers live)
+        float w[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) quad(m, w[m]);
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc = fmaf(w[m][i], step, acc);
+                x = ex2f(acc);
+                *reinterpret_cast<float*>(sm + OFF_G + g_off(16 * J + 4 * m + i, c)) = x;
+            }
     } else {
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            const int r = 16 * J + rr;
-            float* gp = reinterpret_cast<float*>(sm + OFF_G + g_off(r, c));
-            const float gv = (r < BT) ? g_of(*gp, prologue) : 0.f;
-            acc = fmaf(gv, kLog2e, acc);
-            x = ex2f(acc);
-            *gp = x;
+        for (int m = 0; m < 4; ++m) {
+            float w[4];
+            quad(m, w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc = fmaf(w[i], step, acc);
+                x = ex2f(acc);
+                *reinterpret_cast<float*>(sm + OFF_G + g_off(16 * J + 4 * m + i, c)) = x;
+            }
         }
     }
     vec[(V_D + J) * 128 + c] = x;
@@ -377,9 +408,10 @@ __device__ __forceinline__ void phase0_normalise_qk(uint8_t* sm, int t)
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[8 * i + e] = v8[e];
     }
-    float ss = 0.f;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};   // four partial sums: a chain of 8 dependent FMAs, not 32
 #pragma unroll
-    for (int e = 0; e < 32; ++e) ss = fmaf(x[e], x[e], ss);
+    for (int e = 0; e < 32; ++e) s4[e & 3] = fmaf(x[e], x[e], s4[e & 3]);
+    float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
     const float inv = l2_inv(ss);
