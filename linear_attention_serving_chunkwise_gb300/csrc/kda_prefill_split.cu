@@ -83,7 +83,7 @@ constexpr int B_BAR_WREADY = 10;   // W^T is written (14 warps)
 constexpr int B_BAR_DREAD = 11;    // D1 is read out (14 warps)
 constexpr int B_BAR_END = 12;      // the MMA issuer's last commit
 constexpr int B_BAR_OSTAGED = 13;  // O of a chunk is staged (14 warps)
-constexpr int B_BAR_SFREE = 14;    // the O store of a chunk has read its staging buffer
+constexpr int B_BAR_SFREE = 14;    // a chunk's staged O taken (its store issued, the one before read)
 constexpr int B_BAR_Z = 15;        // the gate logits of a chunk are in its O staging buffer, one per buffer (2)
 constexpr int B_BAR_COUNT = 17;
 static_assert(B_WORD_TSLOT1 + 4 <= B_BARS && B_BARS + 8 * B_BAR_COUNT <= 256, "scan word block");
@@ -787,19 +787,23 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
 //                                            A: W^T hi / lo from tensor memory; B: K~^T
 // with D1^T [dv lanes][128]: columns 0-63 W^T (tokens), 64-127 O^T.  Each output element is
 // the same sum of the same products as in the one-CTA-per-unit kernel.  Shared memory then
-// carries only the images and v, and O leaves straight from the registers: a warp stores
-// one token's 32 consecutive dv values at a time.  The CTA is split by role:
+// carries only the images, v and two O staging buffers.  The CTA is split by role:
 //   14 CUDA warps (all but kIssuerWarp and kProducerWarp; warp w reads TMEM lanes
 //     [32 (w % 4), +32); 4 warps share a lane quarter's columns on lanes 0-63, 3 on lanes
 //     64-127): per chunk, S^T_hi, then S^T_lo = bf16(S^T - S^T_hi) and S^T <- S^T gamma_C;
-//     once D1 is in, W^T (hi + lo) into tensor memory and O to global memory;
+//     once D1 is in, W^T (hi + lo) into tensor memory and O (times sigmoid of the gate
+//     logits, which the producer loaded into the same buffer) into staging buffer c % 2, once
+//     the producer has taken chunk c-1's O; a sequence's ragged last chunk goes straight
+//     from the registers to global memory;
 //   lane 0 of kIssuerWarp issues every MMA: V^T [Tb; M]^T at the chunk's top, the S^T_hi
 //     products once S^T_hi is written, the S^T_lo product once S^T_lo is, and the state update
 //     once W^T is;
 //   lane 0 of kProducerWarp issues every copy: [Tb; M] of chunk c+1 and v two chunks ahead
 //     once chunk c's V^T [Tb; M]^T MMAs are done, gamma_C of c+1 and the back image of c once
 //     S^T_lo of c is formed (the update of c-1 has read the last back image), [-Wk; Q'] and
-//     Q' lo of c+1 once D1 of c is in; the images of chunk c+2 are prefetched into L2.
+//     Q' lo of c+1 once D1 of c is in; the images of chunk c+2 are prefetched into L2; chunk
+//     c's staged O goes out by TMA store, after which the gate logits of c+1 go into the
+//     buffer that chunk c-1's store has finished reading.
 // The roles signal one another through mbarriers (one arrival per warp), never through a
 // barrier of the whole CTA: issuing an MMA waits while the tensor pipe's queue is full, which
 // then holds up no CUDA warp; the S^T_lo pass runs under the S^T_hi MMAs, the O stores under
@@ -826,7 +830,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
     uint64_t* bar_dread = bars + B_BAR_DREAD;      // D1 is read out (14 warps)
     uint64_t* bar_end = bars + B_BAR_END;          // the MMA issuer's last commit
     uint64_t* bar_ostaged = bars + B_BAR_OSTAGED;  // O is staged (14 warps)
-    uint64_t* bar_sfree = bars + B_BAR_SFREE;      // an O store has read its staging buffer
+    uint64_t* bar_sfree = bars + B_BAR_SFREE;      // a staged O taken; the buffer of the one before free
     uint64_t* bar_z = bars + B_BAR_Z;              // the gate logits are in an O staging buffer, two
     int* s_abort = reinterpret_cast<int*>(sm + B_BAR + B_WORD_ABORT);
     const uint32_t sbase = smem_u32(sm);
@@ -1002,7 +1006,8 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_dread);   // D1 read out: the next chunk's MMAs may overwrite it
             if (BT == 64) {   // O staged for the TMA store: token r, dv L in box L / 32 (a warp: one row per store)
-                if (ci >= 2) {   // the store of two chunks back has read this buffer
+                if (ci >= 1) {   // the last chunk's O is being stored, and the store of two chunks
+                                 // back has read this buffer (the producer's arrival for chunk ci - 1)
                     if (!(ok = role_wait(bar_sfree, sf_par, s_abort))) break;
                     sf_par ^= 1u;
                 }
@@ -1246,9 +1251,13 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
                 bulk_commit();
                 if (ci >= 1) {
                     bulk_wait_read_group<1>();
-                    mbar_arrive(bar_sfree);
                     fetch_z(ci + 1);   // into the buffer the store of chunk ci - 1 has just read
                 }
+                // one arrival per full chunk, waited for by the CUDA warps before they stage the
+                // next chunk: they never stage chunk ci + 1 (and arrive on ostaged again) before
+                // this thread has taken chunk ci's arrivals, so neither barrier runs two phases
+                // ahead of its waiter
+                mbar_arrive(bar_sfree);
             }
         }
         bulk_wait_all();   // the staged O fully written before the CTA's shared memory goes away

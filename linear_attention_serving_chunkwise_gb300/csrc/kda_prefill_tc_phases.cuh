@@ -769,18 +769,23 @@ __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
         *reinterpret_cast<float2*>(sT + (r0 + i) * LDA + c0 + j2) = make_float2(-(acc.x + acc2.x), -(acc.y + acc2.y));
     }
     named_sync(1, kSolveThreads);
-    // steps 3a/3b: thread (row i of the lower half, columns [8 jg, 8 jg + 8), q parity qh); the
-    // two q parities of an output sit 16 lanes apart and are summed with one shuffle.
+    // steps 3a/3b: a thread sums over one parity qh of the inner index and the two parities of
+    // an output sit 16 lanes apart, summed with one shuffle.
     const int lane = t & 31, w = t >> 5;
-    const int jg = lane & 3, i = 4 * w + ((lane >> 2) & 3), qh = lane >> 4;
     float acc[8];
-    {   // 3a: Y = A[32:64, 0:32] H0
+    {   // 3a: Y = A[32:64, 0:32] H0.  Warp w takes columns [8 jg, 8 jg + 8) of rows
+        // [16 (w / 4), +16) (lane % 16 the row).  H0 is lower triangular, so only the inner
+        // indices k >= 8 jg contribute (the skipped terms are exact zeros): 16 - 4 jg pair
+        // steps, with jg = w for warps 0-3 and 7 - w for warps 4-7, so that the two warps that
+        // share an SM sub-partition (w and w + 4) take 20 steps between them.
+        const int jg = w < 4 ? w : 7 - w, i = 16 * (w >> 2) + (lane & 15), qh = lane >> 4;
         const float* arow = sA + (32 + i) * LDA + qh;
         const float* hcol = sT + qh * LDA + 8 * jg;
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
+            if (k < 4 * jg) continue;
             const float a = arow[2 * k];
             const float4 h0 = *reinterpret_cast<const float4*>(hcol + 2 * k * LDA);
             const float4 h1 = *reinterpret_cast<const float4*>(hcol + 2 * k * LDA + 4);
@@ -797,12 +802,19 @@ __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
         }
     }
     named_sync(1, kSolveThreads);
-    {   // 3b: T[32:64, 0:32] = -H1 Y; rows 0-15 of H1 are zero past column 15
+    {   // 3b: T[32:64, 0:32] = -H1 Y.  Warp w takes rows [4 g, 4 g + 4) (columns [8 jg, +8),
+        // jg = lane % 4).  H1 is lower triangular, so only k <= 4 g + 3 contribute (the skipped
+        // terms are exact zeros): 2 g + 2 pair steps, with g = w for warps 0-3 and 11 - w for
+        // warps 4-7, so that warps w and w + 4 take 18 steps between them.
+        const int g = w < 4 ? w : 11 - w;
+        const int jg = lane & 3, i = 4 * g + ((lane >> 2) & 3), qh = lane >> 4;
         const float* hrow = sT + (32 + i) * LDA + 32 + qh;
         const float* y = sY + qh * LDY + 8 * jg;
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        auto step = [&](int k) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (k > 2 * g + 1) continue;
             const float a = hrow[2 * k];
             const float4 y0 = *reinterpret_cast<const float4*>(y + 2 * k * LDY);
             const float4 y1 = *reinterpret_cast<const float4*>(y + 2 * k * LDY + 4);
@@ -810,13 +822,6 @@ __device__ __forceinline__ void phase3_solve(uint8_t* sm, int t)
             acc[2] = fmaf(a, y0.z, acc[2]); acc[3] = fmaf(a, y0.w, acc[3]);
             acc[4] = fmaf(a, y1.x, acc[4]); acc[5] = fmaf(a, y1.y, acc[5]);
             acc[6] = fmaf(a, y1.z, acc[6]); acc[7] = fmaf(a, y1.w, acc[7]);
-        };
-        if (w < 4) {   // i < 16
-#pragma unroll
-            for (int k = 0; k < 8; ++k) step(k);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) step(k);
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
