@@ -139,9 +139,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         const int t0 = bos + 64 * ci;
         const int BT = min(64, eos - t0);
         if (t < 64) sbeta[t] = beta_next;
-        // this chunk's inputs (one barrier for the three copies)
+        // chunks after the first had their q and g tiles in, and their cumsums and factors
+        // formed, under the previous chunk's [Wk; -Q'] and D1 MMAs
+        const bool pre_done = ci > 0;
+        // this chunk's inputs (one barrier for the copies)
         if (!(mbar_wait_bounded(bar_v, v_par, kWaitNs) && mbar_wait_bounded(bar_k, k_par, kWaitNs) &&
-              mbar_wait_bounded(bar_qg, qg_par, kWaitNs)))
+              (pre_done || mbar_wait_bounded(bar_qg, qg_par, kWaitNs))))
             atomicExch(s_abort, 1);
         tc_fence_before_sync();
         __syncthreads();
@@ -153,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         KDA_CLK(clk, 0);   // this chunk's inputs in
         v_par ^= 1u;
         k_par ^= 1u;
-        qg_par ^= 1u;
+        if (!pre_done) qg_par ^= 1u;
         if (t == 0) v_pending = k_pending = qg_pending = false;
         if (t < 64) {
             const int tn = t0 + 64 + t;
@@ -165,9 +168,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             __syncthreads();
         }
         // ---- phase 1: decayed operands
-        phase1_cumsum(sm, vec, t, BT, pro);
-        __syncthreads();
-        if (t < 128) phase1_factors(vec, t);
+        if (!pre_done) {
+            phase1_cumsum(sm, vec, t, BT, pro);
+            __syncthreads();
+            if (t < 128) phase1_factors(vec, t);
+        }
         if (t == 0 && o_pending) {   // the previous chunk's O staging must be read out before reuse
             bulk_wait_read();
             o_pending = false;
@@ -226,10 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         __syncthreads();
         tc_fence_after_sync();
         KDA_CLK(clk, 4);   // solve, with the state operand and the seed alongside
-        // the k tile of this chunk is no longer read: fetch the next chunk's
+        // the q, k and g tiles of this chunk are no longer read: fetch the next chunk's
         if (t == 0 && ci + 1 < nchunks) {
             issue_k_loads(p, sm, bar_k, t0 + 64, h);
-            k_pending = true;
+            issue_qg_loads(p, sm, bar_qg, t0 + 64, h);
+            k_pending = qg_pending = true;
         }
         phase3_tb_operands(sm, t, sbeta);
         fence_proxy_async_smem();
@@ -284,11 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         // state-independent half of D1, [Tb; M] V (hi + lo), queued right behind it
         if (t == 0) {
             tc_fence_after_sync();
-            // the q and g tiles of this chunk are no longer read: fetch the next chunk's
-            if (ci + 1 < nchunks) {
-                issue_qg_loads(p, sm, bar_qg, t0 + 64, h);
-                qg_pending = true;
-            }
             const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
@@ -305,6 +306,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             for (int ks = 0; ks < 4; ++ks)
                 umma_bf16_tmem_a(tm + TM_D1, tm + TM_TPL + 8 * ks, desc_mnmajor(vb, 64, ks), idesc, 1u);
             mma_open = true;   // committed with phase 5b's MMAs
+        }
+        // meanwhile the next chunk's cumsums (its q and g tiles were fetched after the solve;
+        // this chunk no longer reads the g tile or vec[V_D]), its factors under the D1 MMAs of
+        // phase 5b; gamma_C of this chunk is kept in a register, as those overwrite vec
+        const float gamma_c = vec[V_GC * 128 + L];
+        if (ci + 1 < nchunks) {
+            if (!mbar_wait_bounded(bar_qg, qg_par, kWaitNs)) atomicExch(s_abort, 1);
+            qg_par ^= 1u;
+            if (t == 0) qg_pending = false;
+            phase1_cumsum(sm, vec, t, min(64, eos - t0 - 64), pro);
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
@@ -346,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             for (int ks = 0; ks < 8; ++ks)
                 umma_bf16_tmem_a(tm + TM_D1, tm + TM_A1L + 8 * ks, desc_mnmajor(sh, 128, ks), idesc, 1u);
         }
-        state_lo_and_decay(sm, vec, tm, L, part, quarter);   // and S <- gamma_C S
+        state_lo_and_decay(sm, gamma_c, tm, L, part, quarter);   // and S <- gamma_C S
         fence_proxy_async_smem();
         tmem_wait_st();
         tc_fence_before_sync();
@@ -361,6 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             umma_commit(bar_mma);
             mma_open = false;
         }
+        // while the D1 MMAs run: the next chunk's factors (its cumsums were formed under the
+        // [Wk; -Q'] MMA, several barriers ago)
+        if (t < 128 && ci + 1 < nchunks) phase1_factors(vec, t);
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
         tc_fence_after_sync();

@@ -552,11 +552,10 @@ __device__ __forceinline__ void build_state_operand(uint8_t* sm, uint32_t tm, in
 // the same layout (the history read-out Q' S is formed as Q'_hi S_hi + Q'_hi S_lo +
 // Q'_lo S_hi, so that its operands carry ~16 mantissa bits), then S <- gamma_C[c] S (the
 // chunk decay, applied before the state update accumulates).
-__device__ __forceinline__ void state_lo_and_decay(uint8_t* sm, const float* vec, uint32_t tm, int c, int part,
+__device__ __forceinline__ void state_lo_and_decay(uint8_t* sm, float gc, uint32_t tm, int c, int part,
                                                    int quarter)
 {
     const uint32_t sbase = smem_u32(sm);
-    const float gc = vec[V_GC * 128 + c];
     float a[32];
     tmem_ld32(tmem_addr(tm, 32 * quarter, TM_S + 32 * part), a);
     tmem_wait_ld();

@@ -20,10 +20,10 @@ import torch
 from . import _lib
 from .build import build
 
-TC_SPANS = ["inputs in (loop top)", "phase 1: cumsum, factors, token rows, off-diagonal rows",
+TC_SPANS = ["inputs in (loop top)", "phase 1: token rows, off-diagonal rows (the first chunk: cumsum, factors)",
             "A/P tf32 MMA, K~ alongside", "A/P read-out", "solve (state operand and seed alongside)",
-            "Tb operands, M = P Tb, [Tb; M] hi/lo", "[Wk; -Q'] MMA",
-            "[-Wk; Q'] hi/lo operands", "S half of D1 (state lo and decay alongside)", "W hi/lo",
+            "Tb operands, M = P Tb, [Tb; M] hi/lo", "[Wk; -Q'] MMA, the next chunk's cumsum alongside",
+            "[-Wk; Q'] hi/lo operands", "S half of D1 (state lo and decay, the next chunk's factors alongside)", "W hi/lo",
             "state update, O staged",
             "checkpoint, O stores issued"]
 PREP_SPANS = ["loop top: claims, beta", "off-diagonal rows", "A/P tf32 MMA, K~ staged alongside", "A/P read-out",
