@@ -480,7 +480,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             phase0_normalise_qk(sm, t);
             __syncthreads();
         }
-        phase1_tokens<true>(sm, vec, tm, L, part, quarter, BTn, kg_buf(b));
+        phase1_tokens(sm, vec, tm, L, part, quarter, BTn, kg_buf(b));
         return true;
     };
     bool ok = item < 0 || phase1ab(cur, 0);

@@ -202,6 +202,13 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr)
     return v;
 }
 
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t saddr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr));
+    return v;
+}
+
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t saddr)
 {
     const uint4 v = ld_shared_v4(saddr);
@@ -576,10 +583,8 @@ __device__ __forceinline__ void state_lo_and_decay(uint8_t* sm, float gc, uint32
 // channels [32p, 32p + 32).  Writes the tf32 row operand [K_r; Q_r] (TMEM).  Token r's
 // diagonal-tile column operand is split between the k-row and the q-row thread (channels
 // c0..c0+3 and c0+4..c0+7 of each group of 8), so that the two halves, which run on
-// different SMSPs, carry the same number of reciprocals.  Its K_Gamma B operand is
-// written by the q-row thread, or with kSplitKG split the same way (the same values; more
-// registers, which the one-CTA-per-head kernel cannot spare).
-template <bool kSplitKG = false>
+// different SMSPs, carry the same number of reciprocals; its K_Gamma B operand is split
+// the same way.
 __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uint32_t tm, int L, int part,
                                               int quarter, int BT, uint32_t kg_off = OFF_KG)
 {
@@ -615,32 +620,24 @@ __device__ __forceinline__ void phase1_tokens(uint8_t* sm, const float* vec, uin
             st_shared_f4(kc + sw128_off_f32(rj, c0, KC_ROWS), tf32_round(xv[0] * rcpf(xs[0])),
                          tf32_round(xv[1] * rcpf(xs[1])), tf32_round(xv[2] * rcpf(xs[2])),
                          tf32_round(xv[3] * rcpf(xs[3])));
-            if constexpr (kSplitKG) {
-                const float4 e4 = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
-                st_shared_v2(kg, pack_bf16x2(xv[0] * xs[0] * e4.x, xv[1] * xs[1] * e4.y),
-                             pack_bf16x2(xv[2] * xs[2] * e4.z, xv[3] * xs[3] * e4.w));
-            }
+            const float4 e4 = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
+            st_shared_v2(kg, pack_bf16x2(xv[0] * xs[0] * e4.x, xv[1] * xs[1] * e4.y),
+                         pack_bf16x2(xv[2] * xs[2] * e4.z, xv[3] * xs[3] * e4.w));
         } else {
+            // channels c0 + 4 .. c0 + 7 of k_r: the upper half of the 16-byte chunk
+            const uint2 k2 = ld_shared_v2(sbase + OFF_K + sw128_chunk(r, c0 >> 3, 64) + 8u);
+            const float2 ka = bf2_to_f2(k2.x), kb = bf2_to_f2(k2.y);
             float kv[8];
-            unpack8(ld_shared_v4(sbase + OFF_K + sw128_chunk(r, c0 >> 3, 64)), kv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) kv[e] = valid ? kv[e] : 0.f;
+            kv[4] = valid ? ka.x : 0.f;
+            kv[5] = valid ? ka.y : 0.f;
+            kv[6] = valid ? kb.x : 0.f;
+            kv[7] = valid ? kb.y : 0.f;
             st_shared_f4(kc + sw128_off_f32(rj, c0 + 4, KC_ROWS), tf32_round(kv[4] * rcpf(xs[4])),
                          tf32_round(kv[5] * rcpf(xs[5])), tf32_round(kv[6] * rcpf(xs[6])),
                          tf32_round(kv[7] * rcpf(xs[7])));
-            if constexpr (kSplitKG) {
-                const float4 e4 = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
-                st_shared_v2(kg + 8u, pack_bf16x2(kv[4] * xs[4] * e4.x, kv[5] * xs[5] * e4.y),
-                             pack_bf16x2(kv[6] * xs[6] * e4.z, kv[7] * xs[7] * e4.w));
-            } else {
-                const float4 e4a = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0);
-                const float4 e4b = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
-                const float ev[8] = {e4a.x, e4a.y, e4a.z, e4a.w, e4b.x, e4b.y, e4b.z, e4b.w};
-#pragma unroll
-                for (int e = 0; e < 8; ++e) kv[e] = kv[e] * xs[e] * ev[e];
-                st_shared_v4(kg, pack_bf16x2(kv[0], kv[1]), pack_bf16x2(kv[2], kv[3]), pack_bf16x2(kv[4], kv[5]),
-                             pack_bf16x2(kv[6], kv[7]));
-            }
+            const float4 e4 = *reinterpret_cast<const float4*>(vec + (V_E + J) * 128 + c0 + 4);
+            st_shared_v2(kg + 8u, pack_bf16x2(kv[4] * xs[4] * e4.x, kv[5] * xs[5] * e4.y),
+                         pack_bf16x2(kv[6] * xs[6] * e4.z, kv[7] * xs[7] * e4.w));
         }
     }
     tmem_st32(tmem_addr(tm, 32 * quarter, TM_KQ + 32 * part), kq);
