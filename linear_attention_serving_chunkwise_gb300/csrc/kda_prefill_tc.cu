@@ -24,26 +24,37 @@
 //
 // One CTA owns one (sequence, head) and walks its chunks in order; the fp32 state
 // lives in tensor memory for the whole sequence.  Per chunk:
-//   1  g cumsum per channel; decayed operands to TMEM (A operands) and shared
-//      memory (B operands); TMA prefetch of the next chunk's v.
+//   1  decayed operands to TMEM (A operands) and shared memory (B operands) from the
+//      per-channel g cumsums and factors (the first chunk's formed here, the others'
+//      under the previous chunk's MMAs).
 //   2  A and P by one tf32 MMA over the four sub-tile references side by side, while
-//      all warps build K~^T (TMEM).
+//      all warps build K~^T (TMEM); TMA prefetch of the next chunk's v once the last
+//      chunk's O store has read its staging.
 //   3  T = (I + A)^-1 in fp32 on CUDA cores (8 warps) while the other 8 build the
 //      state's bf16 B operand, apply the chunk decay to S and seed the next
-//      accumulator with [0; -Q_Gamma]; M = P Tb by three bf16 MMAs (hi/lo splits);
-//      TMA prefetch of the next chunk's k.
-//   4  [Wk; -Q'] by MMA onto the seed, and the state-independent half of D1,
-//      [Tb; M] V, queued behind it; then the [-Wk; Q'] operand over the read
-//      accumulator; TMA prefetch of the next chunk's q and g.
-//   5  D1 += [-Wk; Q'] S by MMA: rows 0-63 are W, rows 64-127 are O; W to shared
-//      memory; S += K~^T W by MMA while O is staged in shared memory and written by
-//      TMA bulk stores (direct stores for a sequence's ragged last chunk).
+//      accumulator with [0; -Q_Gamma]; TMA prefetch of the next chunk's q, k and g;
+//      M = P Tb by three bf16 MMAs (hi/lo splits).
+//   4  [Wk; -Q'] by MMA onto the seed (the next chunk's cumsums alongside), and the
+//      state-independent half of D1, [Tb; M] V, queued behind it; then the [-Wk; Q']
+//      operand over the read accumulator.
+//   5  D1 += [-Wk; Q'] S by MMA (the next chunk's factors alongside): rows 0-63 are W,
+//      rows 64-127 are O; W to shared memory; S += K~^T W by MMA while O is staged in
+//      shared memory (two boxes past the shared map, two in the chunk's v buffer) and
+//      written by TMA bulk stores (direct stores for a sequence's ragged last chunk).
 #include "kda_prefill_tc_phases.cuh"
 
 namespace kda {
 namespace {
 
 using namespace sm100;
+
+// O staging boxes 0-1 (dv columns 0-63: 2 x [64 tok][32] fp32, 128-byte swizzle) past the
+// shared map (boxes 2-3 go to the chunk's v buffer): phase 1 then writes the X region without
+// waiting for the last chunk's O store, which only has to have read its boxes before the next
+// v load (phase 2).
+constexpr uint32_t T_OST = ((uint32_t)SMEM_USED + 1023u) & ~1023u;
+constexpr size_t TC_SMEM_BYTES = T_OST + 16384 + 1024;   // + slack for 1024-byte alignment
+static_assert(TC_SMEM_BYTES <= 232448, "one-CTA-per-unit shared memory");
 
 // ---------------------------------------------------------------- the kernel
 // 16 warps: warp w reaches TMEM lanes [32 (w % 4), +32) and works on column part w / 4.
@@ -172,12 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             phase1_cumsum<true>(sm, vec, t, BT, pro);
             __syncthreads();
             if (t < 128) phase1_factors(vec, t);
+            __syncthreads();
         }
-        if (t == 0 && o_pending) {   // the previous chunk's O staging must be read out before reuse
-            bulk_wait_read();
-            o_pending = false;
-        }
-        __syncthreads();
         phase1_tokens(sm, vec, tm, L, part, quarter, BT);
         __syncthreads();
         phase1_offdiag<true>(sm, vec, t);
@@ -190,10 +197,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         // ---- next chunk's v, then phase 2: A and P by one tf32 MMA
         if (t == 0) {
             tc_fence_after_sync();
-            if (ci + 1 < nchunks) {
-                issue_v_loads(p, sm, bar_v, (ci + 1) & 1, t0 + 64, h);
-                v_pending = true;
-            }
             // all four references at once: N = 160 columns, reference m in columns [8m(m+1), 8(m+1)(m+2))
             const uint32_t idesc = idesc_tf32_f32(128, KC_ROWS);
             const uint32_t kc = sbase + OFF_X;
@@ -202,6 +205,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
                 umma_tf32_tmem_a(tm + TM_AP, tm + TM_KQ + 8 * ks, desc_kmajor(kc, KC_ROWS, ks), idesc,
                                  ks > 0 ? 1u : 0u);
             umma_commit(bar_mma);
+            if (o_pending) {   // the last chunk's O store has read its boxes (one is the v buffer loaded next)
+                bulk_wait_read();
+                o_pending = false;
+            }
+            if (ci + 1 < nchunks) {
+                issue_v_loads(p, sm, bar_v, (ci + 1) & 1, t0 + 64, h);
+                v_pending = true;
+            }
         }
         build_ktilde(sm, vec, tm, L, part, quarter, BT);   // overlaps the MMA above
         tmem_wait_st();
@@ -382,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         if (t == 0 && p.gate && BT == 64) {   // the gate's logits into the O staging boxes (now free)
             const uint8_t* vbz = sm + ((ci & 1) ? OFF_V1 : OFF_V0);
             mbar_arrive_expect_tx(bar_z, 32768u);
-            tma_load_3d(sm + OFF_X + X_OST, &p.tm_z, bar_z, 0, h, t0);
-            tma_load_3d(sm + OFF_X + X_OST + 8192, &p.tm_z, bar_z, 32, h, t0);
+            tma_load_3d(sm + T_OST, &p.tm_z, bar_z, 0, h, t0);
+            tma_load_3d(sm + T_OST + 8192, &p.tm_z, bar_z, 32, h, t0);
             tma_load_3d(const_cast<uint8_t*>(vbz), &p.tm_z, bar_z, 64, h, t0);
             tma_load_3d(const_cast<uint8_t*>(vbz) + 8192, &p.tm_z, bar_z, 96, h, t0);
             z_pending = true;
@@ -436,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             if (BT == 64) {
                 // stage in 128-byte-swizzled [64 tok][32] fp32 boxes, one TMA store per box:
                 // boxes 0-1 in the free top of the X region, 2-3 in this chunk's v buffer
-                const uint32_t box = (part < 2) ? sbase + OFF_X + X_OST + 8192 * part
+                const uint32_t box = (part < 2) ? sbase + T_OST + 8192 * part
                                                 : sbase + ((ci & 1) ? OFF_V1 : OFF_V0) + 8192 * (part - 2);
                 if (p.gate) {   // the output gate, o * sigmoid(z), on the logits TMA put in the boxes
                     if (!mbar_wait_bounded(bar_z, z_par, kWaitNs)) atomicExch(s_abort, 1);
@@ -484,8 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         }
         if (t == 0 && BT == 64) {
             const uint8_t* vb = sm + ((ci & 1) ? OFF_V1 : OFF_V0);
-            tma_store_3d(&p.tm_o, sm + OFF_X + X_OST, 0, h, t0);
-            tma_store_3d(&p.tm_o, sm + OFF_X + X_OST + 8192, 32, h, t0);
+            tma_store_3d(&p.tm_o, sm + T_OST, 0, h, t0);
+            tma_store_3d(&p.tm_o, sm + T_OST + 8192, 32, h, t0);
             tma_store_3d(&p.tm_o, vb, 64, h, t0);
             tma_store_3d(&p.tm_o, vb + 8192, 96, h, t0);
             bulk_commit();
@@ -552,10 +563,10 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream)
     p.prologue = a.prologue;
     p.gate = a.gate;
     auto kern = a.prologue ? kda_prefill_tc_kernel<true> : kda_prefill_tc_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const long long units = (long long)a.num_seqs * a.num_heads;
-    kern<<<(unsigned)units, kThreads, SMEM_BYTES, stream>>>(p);
+    kern<<<(unsigned)units, kThreads, TC_SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -68,8 +68,6 @@ constexpr uint32_t X_TBH = 0;          // Tb hi, MN-major B [64 i][64 j] bf16 (8
 constexpr uint32_t X_TBL = 8192;       // Tb lo
 constexpr uint32_t X_ST = 17408;       // T fp32 [64][68]
 constexpr uint32_t X_SY = 34816;       // solve scratch fp32 [32][LDY]
-constexpr uint32_t X_OST = 65536;      // O staging, dv columns 0-63: 2 x [64 tok][32] fp32 boxes (phase 5,
-                                       // after the MMA that reads S bf16 has completed)
 constexpr uint32_t X_SB = 40960;       // S hi bf16, MN-major B [128 dk][128 dv] (phases 3-5b)
 constexpr uint32_t X_SL = 0;           // S lo bf16, same layout (phases 4-5b; the W tiles take it over in 5c)
 constexpr uint32_t X_WH = 0;           // W hi bf16, MN-major B [64 tok][128 dv] (phase 5)
