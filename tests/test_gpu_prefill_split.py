@@ -276,3 +276,26 @@ def test_beta_zero_read_out_on_both_paths(cuda_lib):
     check("split final state", s_split, ref_s, tol)
     check("one CTA per unit out", o_one[:T0], ref_o, tol)
     check("one CTA per unit final state", s_one[:len(lens)], ref_s, tol)
+
+
+@pytest.mark.parametrize("launches", [2, 3], ids=["single-launch", "separate-launches"])
+def test_split_repeated_calls_are_deterministic(cuda_lib, launches):
+    """The chunk-parallel path, gated, 40 times over on uneven sequences: every call completes
+    (no bounded wait runs out) and gives the same bits as the first, whatever order its CTAs
+    claimed the items and however its roles interleaved (the state scan's barriers are waited
+    for with parity, so a signaller two phases ahead of its waiter would hang the waiter)."""
+    lens, H = ([700, 64, 1300, 200, 900], 32) if launches == 3 else ([700, 64, 1300, 200, 900], 16)
+    cfg = W.random_prefill_config(lens, H, 128, torch.bfloat16, init="normal")
+    assert _plan(cuda_lib, len(lens), cfg.total_tokens, H)["kernel_launches"] == launches
+    g = to_device(W.make_prefill_inputs(cfg, seed=101))
+    z = W.make_gate_logits((cfg.total_tokens, H, 128), seed=102, device="cuda")
+    first = None
+    for i in range(40):
+        out, fin = cuda_lib.prefill(g["q"], g["k"], g["v"], g["g"], g["beta"], g["cu_seqlens"], g["init_state"],
+                                    gate=z)
+        torch.cuda.synchronize()
+        assert cuda_lib.last_device_status() == cuda_lib.KDA_OK, f"call {i}"
+        if first is None:
+            first = (out.clone(), fin.clone())
+        else:
+            assert torch.equal(out, first[0]) and torch.equal(fin, first[1]), f"call {i} differs from the first"
