@@ -468,7 +468,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
         if (*s_abort) return false;
         qg_par ^= 1u;
         if (t == kStorer) qg_pending = false;
-        phase1_cumsum<true>(sm, vec, t, BTn, pro);
+        phase1_cumsum(sm, vec, t, BTn, pro);
         __syncthreads();
         if (t < 128) phase1_factors(vec, t);
         if (!mbar_wait_bounded(bar_k, k_par, kWaitNs)) atomicExch(s_abort, 1);
@@ -521,7 +521,7 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
             cp_async_commit();
         }
         // ---- phase 1: decayed operands (all but the off-diagonal rows are done)
-        phase1_offdiag<true>(sm, vec, t);
+        phase1_offdiag(sm, vec, t);
         fence_proxy_async_smem();
         tmem_wait_st();
         if (t == kStorer) bulk_wait_read();   // the previous item's pieces have left the staging buffer

@@ -180,14 +180,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         }
         // ---- phase 1: decayed operands
         if (!pre_done) {
-            phase1_cumsum<true>(sm, vec, t, BT, pro);
+            phase1_cumsum(sm, vec, t, BT, pro);
             __syncthreads();
             if (t < 128) phase1_factors(vec, t);
             __syncthreads();
         }
         phase1_tokens(sm, vec, tm, L, part, quarter, BT);
         __syncthreads();
-        phase1_offdiag<true>(sm, vec, t);
+        phase1_offdiag(sm, vec, t);
         fence_proxy_async_smem();
         tmem_wait_st();
         tc_fence_before_sync();
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
             if (!mbar_wait_bounded(bar_qg, qg_par, kWaitNs)) atomicExch(s_abort, 1);
             qg_par ^= 1u;
             if (t == 0) qg_pending = false;
-            phase1_cumsum<true>(sm, vec, t, min(64, eos - t0 - 64), pro);
+            phase1_cumsum(sm, vec, t, min(64, eos - t0 - 64), pro);
         }
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;

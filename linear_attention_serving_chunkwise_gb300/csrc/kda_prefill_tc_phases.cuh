@@ -354,46 +354,32 @@ __device__ __forceinline__ void sigmoid4(float (&z)[4])
 // sub-tile (s_J: the sub-tile's sum).
 // With the prologue's kProG bit the tile holds logits z and g = -5 sigmoid(z) is used
 // (sigmoid4 on four rows at a time; the step adds sigmoid(z) (-5 log2(e)) in one rounding).
-template <bool kHoist = false>
 __device__ __forceinline__ void phase1_cumsum(uint8_t* sm, float* vec, int t, int BT, int prologue = 0)
 {
     const int c = t & 127, J = t >> 7;
     const bool logits = (prologue & kProG) != 0;
     const float step = logits ? kGMin * kLog2e : kLog2e;
     float acc = 0.f, x = 1.f;
-    // rows [16 J + 4 m, +4) of the column: g, or sigmoid(z); 0 past the chunk's end
-    auto quad = [&](int m, float (&w)[4]) {
+    // rows [16 J + 4 m, +4) of the column: g, or sigmoid(z); 0 past the chunk's end.  All 16
+    // loads go first, so that their latencies overlap.
+    float w[4][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const float*>(sm + OFF_G + g_off(16 * J + 4 * m + i, c));
-        if (logits) sigmoid4(w);
+    for (int m = 0; m < 4; ++m) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = (16 * J + 4 * m + i < BT) ? w[i] : 0.f;
-    };
-    if constexpr (kHoist) {   // all 16 loads first (16 more registers live)
-        float w[4][4];
+        for (int i = 0; i < 4; ++i)
+            w[m][i] = *reinterpret_cast<const float*>(sm + OFF_G + g_off(16 * J + 4 * m + i, c));
+        if (logits) sigmoid4(w[m]);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) quad(m, w[m]);
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc = fmaf(w[m][i], step, acc);
-                x = ex2f(acc);
-                *reinterpret_cast<float*>(sm + OFF_G + g_off(16 * J + 4 * m + i, c)) = x;
-            }
-    } else {
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            float w[4];
-            quad(m, w);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc = fmaf(w[i], step, acc);
-                x = ex2f(acc);
-                *reinterpret_cast<float*>(sm + OFF_G + g_off(16 * J + 4 * m + i, c)) = x;
-            }
-        }
+        for (int i = 0; i < 4; ++i) w[m][i] = (16 * J + 4 * m + i < BT) ? w[m][i] : 0.f;
     }
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc = fmaf(w[m][i], step, acc);
+            x = ex2f(acc);
+            *reinterpret_cast<float*>(sm + OFF_G + g_off(16 * J + 4 * m + i, c)) = x;
+        }
     vec[(V_D + J) * 128 + c] = x;
 }
 
@@ -461,41 +447,27 @@ __device__ __forceinline__ void phase1_factors(float* vec, int c)
 // i16 = t % 16 and channels [4 cq, 4 cq + 4), cq = t / 16, of all six (m, J) pairs (a
 // warp: 16 tokens x 2 channel quads, so its factor loads are broadcasts); the row of each
 // pair is a compile-time offset from the thread's own swizzled base.
-template <bool kHoist = false>
 __device__ __forceinline__ void phase1_offdiag(uint8_t* sm, const float* vec, int t)
 {
     const int i16 = t & 15, cq = (t >> 4) & 31, c0 = 4 * cq;
     // sw128_off_f32(row, c0, KC_ROWS) with row % 8 == i16 % 8 for every row used below
     const uint32_t base = smem_u32(sm) + OFF_X + (cq >> 3) * (KC_ROWS * 128u) + i16 * 128u +
                           ((uint32_t)((cq & 7) ^ (i16 & 7)) << 4);
-    if constexpr (kHoist) {
-        // the rows read (diagonal tiles) and written (off-diagonal ones) are disjoint: all
-        // loads first, so that their latencies overlap (more registers live at once)
-        uint4 d[3];
-        float4 f[6];
+    // the rows read (diagonal tiles) and written (off-diagonal ones) are disjoint: all loads
+    // first, so that their latencies overlap
+    uint4 d[3];
+    float4 f[6];
 #pragma unroll
-        for (int J = 0; J < 3; ++J) d[J] = ld_shared_v4(base + (kc_row(J) + 16 * J) * 128u);
+    for (int J = 0; J < 3; ++J) d[J] = ld_shared_v4(base + (kc_row(J) + 16 * J) * 128u);
 #pragma unroll
-        for (int b = 0; b < 6; ++b) f[b] = *reinterpret_cast<const float4*>(vec + (V_DF + b) * 128 + c0);
+    for (int b = 0; b < 6; ++b) f[b] = *reinterpret_cast<const float4*>(vec + (V_DF + b) * 128 + c0);
 #pragma unroll
-        for (int b = 0; b < 6; ++b) {
-            const int m = (b == 0) ? 1 : ((b < 3) ? 2 : 3);
-            const int J = b - m * (m - 1) / 2;
-            st_shared_f4(base + (kc_row(m) + 16 * J) * 128u, tf32_round(__uint_as_float(d[J].x) * f[b].x),
-                         tf32_round(__uint_as_float(d[J].y) * f[b].y), tf32_round(__uint_as_float(d[J].z) * f[b].z),
-                         tf32_round(__uint_as_float(d[J].w) * f[b].w));
-        }
-    } else {
-#pragma unroll
-        for (int b = 0; b < 6; ++b) {
-            const int m = (b == 0) ? 1 : ((b < 3) ? 2 : 3);
-            const int J = b - m * (m - 1) / 2;
-            const uint4 d = ld_shared_v4(base + (kc_row(J) + 16 * J) * 128u);
-            const float4 f = *reinterpret_cast<const float4*>(vec + (V_DF + b) * 128 + c0);
-            st_shared_f4(base + (kc_row(m) + 16 * J) * 128u, tf32_round(__uint_as_float(d.x) * f.x),
-                         tf32_round(__uint_as_float(d.y) * f.y), tf32_round(__uint_as_float(d.z) * f.z),
-                         tf32_round(__uint_as_float(d.w) * f.w));
-        }
+    for (int b = 0; b < 6; ++b) {
+        const int m = (b == 0) ? 1 : ((b < 3) ? 2 : 3);
+        const int J = b - m * (m - 1) / 2;
+        st_shared_f4(base + (kc_row(m) + 16 * J) * 128u, tf32_round(__uint_as_float(d[J].x) * f[b].x),
+                     tf32_round(__uint_as_float(d[J].y) * f[b].y), tf32_round(__uint_as_float(d[J].z) * f[b].z),
+                     tf32_round(__uint_as_float(d[J].w) * f[b].w));
     }
 }
 
