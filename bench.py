@@ -92,6 +92,47 @@ def decode_algorithmic(cfg: W.DecodeConfig):
     return state, state + small
 
 
+def _link_floor(h2d: int, d2h: int, dev) -> dict:
+    """The host-device link as this box gives it: pinned 256 MB copies host-to-device,
+    device-to-host and both at once (two streams), CUDA events, best of 5; and the floor
+    they set for an e2e step of h2d bytes up and d2h bytes down, max(up alone, both
+    directions at the combined rate).  The e2e number is read against this floor."""
+    n = 256 << 20
+    hbuf = [torch.empty(n, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    dbuf = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(2)]
+    s0, s1 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def best(fn):
+        ts = []
+        for _ in range(5):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            ts.append(time.perf_counter() - t0)
+        return min(ts)
+
+    def up():
+        with torch.cuda.stream(s0):
+            dbuf[0].copy_(hbuf[0], non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(s1):
+            hbuf[1].copy_(dbuf[1], non_blocking=True)
+
+    def both():
+        up()
+        down()
+
+    t_up, t_down, t_both = best(up), best(down), best(both)
+    h2d_gbs, d2h_gbs, both_gbs = n / t_up / 1e9, n / t_down / 1e9, 2 * n / t_both / 1e9
+    floor_ms = max(h2d / (h2d_gbs * 1e9), (h2d + d2h) / (both_gbs * 1e9)) * 1e3
+    del hbuf, dbuf
+    return {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "both_directions_gbs": both_gbs, "floor_ms": floor_ms,
+            "how": "pinned 256 MB copies, best of 5 (host wall clock around synchronised copies); floor = "
+                   "max(bytes up / up rate, all bytes / both-directions rate)"}
+
+
 def _src_hash(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -390,7 +431,8 @@ def run_cuda(args, world, rank, local):
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
     e2e = {"value": tokens_per_step / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
-           "api": "kda_prefill_host", "segment_tokens": seg}
+           "api": "kda_prefill_host", "segment_tokens": seg,
+           "link": _link_floor(h2d, d2h, dev)}
     del host, host_out, host_fin, ws
 
     # ---------------- decode: 64 consecutive in-place steps
