@@ -85,7 +85,8 @@ constexpr int B_BAR_END = 12;      // the MMA issuer's last commit
 constexpr int B_BAR_OSTAGED = 13;  // O of a chunk is staged (14 warps)
 constexpr int B_BAR_SFREE = 14;    // a chunk's staged O taken (its store issued, the one before read)
 constexpr int B_BAR_Z = 15;        // the gate logits of a chunk are in its O staging buffer, one per buffer (2)
-constexpr int B_BAR_COUNT = 17;
+constexpr int B_BAR_UPD = 17;      // a chunk's state update is done (for the producer: the back image is free)
+constexpr int B_BAR_COUNT = 18;
 static_assert(B_WORD_TSLOT1 + 4 <= B_BARS && B_BARS + 8 * B_BAR_COUNT <= 256, "scan word block");
 // tensor memory (columns), everything transposed: lane = dv
 constexpr uint32_t B_TM_S = 0;          // S^T [128 dv][128 dk] fp32
@@ -795,12 +796,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
 //     logits, which the producer loaded into the same buffer) into staging buffer c % 2, once
 //     the producer has taken chunk c-1's O; a sequence's ragged last chunk goes straight
 //     from the registers to global memory;
-//   lane 0 of kIssuerWarp issues every MMA: V^T [Tb; M]^T at the chunk's top, the S^T_hi
-//     products once S^T_hi is written, the S^T_lo product once S^T_lo is, and the state update
-//     once W^T is;
+//   lane 0 of kIssuerWarp issues every MMA: the S^T_hi products once S^T_hi is written, the
+//     S^T_lo product once S^T_lo is, the state update once W^T is, and right behind it the
+//     next chunk's V^T [Tb; M]^T (chunk 0's before the loop), which needs no state;
 //   lane 0 of kProducerWarp issues every copy: [Tb; M] of chunk c+1 and v two chunks ahead
-//     once chunk c's V^T [Tb; M]^T MMAs are done, gamma_C of c+1 and the back image of c once
-//     S^T_lo of c is formed (the update of c-1 has read the last back image), [-Wk; Q'] and
+//     once chunk c's V^T [Tb; M]^T MMAs are done, the back image of c once the update of c-1
+//     (which read the last one) is done, gamma_C of c+1 once S^T_lo of c is formed, [-Wk; Q'] and
 //     Q' lo of c+1 once D1 of c is in; the images of chunk c+2 are prefetched into L2; chunk
 //     c's staged O goes out by TMA store, after which the gate logits of c+1 go into the
 //     buffer that chunk c-1's store has finished reading.
@@ -832,6 +833,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
     uint64_t* bar_ostaged = bars + B_BAR_OSTAGED;  // O is staged (14 warps)
     uint64_t* bar_sfree = bars + B_BAR_SFREE;      // a staged O taken; the buffer of the one before free
     uint64_t* bar_z = bars + B_BAR_Z;              // the gate logits are in an O staging buffer, two
+    uint64_t* bar_upd = bars + B_BAR_UPD;          // the state update is done (the producer's copy of bar_mma's second phase)
     int* s_abort = reinterpret_cast<int*>(sm + B_BAR + B_WORD_ABORT);
     const uint32_t sbase = smem_u32(sm);
     const float* sgam = reinterpret_cast<const float*>(sm + B_GAM);
@@ -1071,15 +1073,18 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
         const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
         const uint32_t idesc64 = idesc_bf16_f32(128, 64, 0, 0);
         const uint32_t d1 = tm + B_TM_D1;
-        for (int ci = 0; ci < nchunks && ok; ++ci) {
-            const int vb = ci & 1;
-            // V^T [Tb; M]^T (hi, lo): needs this chunk's [Tb; M] and v, and the last chunk's D1
-            // read out
-            if (ci > 0) {
-                if (!(ok = role_wait(bar_dread, dr_par, s_abort))) break;
+        // V^T [Tb; M]^T (hi, lo) of chunk c into D1: needs chunk c's [Tb; M] and v, and chunk
+        // c-1's D1 read out.  It depends on no state, so chunk c+1's is issued right behind
+        // chunk c's state update, and runs while the CUDA warps wait for that update and form
+        // S^T_hi: the tensor pipe is then free for the S^T_hi products as soon as they can go.
+        auto issue_v = [&](int c) -> bool {
+            const int vb = c & 1;
+            if (c > 0) {
+                if (!role_wait(bar_dread, dr_par, s_abort)) return false;
                 dr_par ^= 1u;
             }
-            if (!(ok = role_wait(bar_tb, tb_par, s_abort) && role_wait(bar_v + vb, (v_par >> vb) & 1u, s_abort))) break;
+            if (!(role_wait(bar_tb, tb_par, s_abort) && role_wait(bar_v + vb, (v_par >> vb) & 1u, s_abort)))
+                return false;
             tb_par ^= 1u;
             v_par ^= 1u << vb;
             tc_fence_after_sync();
@@ -1091,6 +1096,10 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
             for (int ks = 0; ks < 4; ++ks)
                 umma_bf16(d1, desc_mnmajor(vt, 64, ks), desc_kmajor(sbase + B_TBL, 128, ks), idesc_v, 1u);
             umma_commit(bar_vdone);
+            return true;
+        };
+        if (nchunks > 0) ok = issue_v(0);
+        for (int ci = 0; ci < nchunks && ok; ++ci) {
             // S^T_hi [-Wk; Q']^T, and S^T_hi Q'_lo^T into O's columns, once S^T_hi is written
             if (!(ok = role_wait(bar_shi, shi_par, s_abort) && role_wait(bar_f, f_par, s_abort))) break;
             shi_par ^= 1u;
@@ -1125,6 +1134,8 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
             for (int ks = 0; ks < 4; ++ks)
                 umma_bf16_tmem_a(tm + B_TM_S, tm + B_TM_WH + 8 * ks, desc_kmajor(sbase + B_KTL, 128, ks), idesc, 1u);
             umma_commit(bar_mma);
+            umma_commit(bar_upd);   // the same MMAs, for the producer
+            if (ci + 1 < nchunks && !(ok = issue_v(ci + 1))) break;
         }
         if (!ok) fail();
         // every MMA issued has completed before the CTA moves on (bounded)
@@ -1217,10 +1228,18 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
                 prefetch_l2(image(1), IMG_BYTES);
             }
         }
-        uint32_t vd_par = 0, slo_par = 0, wr_par = 0, os_par = 0;
+        uint32_t vd_par = 0, slo_par = 0, wr_par = 0, os_par = 0, upd_par = 0;
         for (int ci = 0; ci < nchunks && ok; ++ci) {
             const int t0 = bos + 64 * ci;
             const bool full = eos - t0 >= 64;
+            // the last chunk's state update is done: it has read the back image, whose copy for
+            // this chunk goes out first (the update waits for it at the end of the chunk).
+            // Chunk ci's update needs this copy, so bar_upd cannot run a phase ahead of here.
+            if (ci > 0) {
+                if (!(ok = role_wait(bar_upd, upd_par, s_abort))) break;
+                upd_par ^= 1u;
+                if (!(ok = fetch_back(ci))) break;
+            }
             // the V^T [Tb; M]^T MMAs are done: [Tb; M] and this v buffer have been read
             if (!(ok = role_wait(bar_vdone, vd_par, s_abort))) break;
             vd_par ^= 1u;
@@ -1229,10 +1248,9 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
                 fetch_v(ci + 2);
                 prefetch_l2(image(ci + 2), IMG_BYTES);   // so that the next fetches come from L2
             }
-            // S^T_lo is formed: gamma_C has been read, and the last update has read the back image
+            // S^T_lo is formed: gamma_C has been read
             if (!(ok = role_wait(bar_slo, slo_par, s_abort))) break;
             slo_par ^= 1u;
-            if (ci > 0 && !(ok = fetch_back(ci))) break;
             if (ci + 1 < nchunks && !(ok = fetch_gamma(ci + 1))) break;
             // D1 is in: [-Wk; Q'] and Q' lo have been read
             if (!(ok = role_wait(bar_wready, wr_par, s_abort))) break;
