@@ -86,7 +86,8 @@ constexpr int B_BAR_OSTAGED = 13;  // O of a chunk is staged (14 warps)
 constexpr int B_BAR_SFREE = 14;    // a chunk's staged O taken (its store issued, the one before read)
 constexpr int B_BAR_Z = 15;        // the gate logits of a chunk are in its O staging buffer, one per buffer (2)
 constexpr int B_BAR_UPD = 17;      // a chunk's state update is done (for the producer: the back image is free)
-constexpr int B_BAR_COUNT = 18;
+constexpr int B_BAR_D1P = 18;      // a chunk's D1 is done (for the producer: the front image is free)
+constexpr int B_BAR_COUNT = 19;
 static_assert(B_WORD_TSLOT1 + 4 <= B_BARS && B_BARS + 8 * B_BAR_COUNT <= 256, "scan word block");
 // tensor memory (columns), everything transposed: lane = dv
 constexpr uint32_t B_TM_S = 0;          // S^T [128 dv][128 dk] fp32
@@ -802,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_prep_kernel(const __gri
 //   lane 0 of kProducerWarp issues every copy: [Tb; M] of chunk c+1 and v two chunks ahead
 //     once chunk c's V^T [Tb; M]^T MMAs are done, the back image of c once the update of c-1
 //     (which read the last one) is done, gamma_C of c+1 once S^T_lo of c is formed, [-Wk; Q'] and
-//     Q' lo of c+1 once D1 of c is in; the images of chunk c+2 are prefetched into L2; chunk
+//     Q' lo of c+1 once D1 of c is done; the images of chunk c+2 are prefetched into L2; chunk
 //     c's staged O goes out by TMA store, after which the gate logits of c+1 go into the
 //     buffer that chunk c-1's store has finished reading.
 // The roles signal one another through mbarriers (one arrival per warp), never through a
@@ -834,6 +835,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
     uint64_t* bar_sfree = bars + B_BAR_SFREE;      // a staged O taken; the buffer of the one before free
     uint64_t* bar_z = bars + B_BAR_Z;              // the gate logits are in an O staging buffer, two
     uint64_t* bar_upd = bars + B_BAR_UPD;          // the state update is done (the producer's copy of bar_mma's second phase)
+    uint64_t* bar_d1p = bars + B_BAR_D1P;          // D1 is done (the producer's copy of bar_mma's first phase)
     int* s_abort = reinterpret_cast<int*>(sm + B_BAR + B_WORD_ABORT);
     const uint32_t sbase = smem_u32(sm);
     const float* sgam = reinterpret_cast<const float*>(sm + B_GAM);
@@ -1119,6 +1121,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
             for (int ks = 0; ks < 8; ++ks)
                 umma_bf16_tmem_a(d1, tm + B_TM_SL + 8 * ks, desc_kmajor(sbase + B_A1, 128, ks), idesc, 1u);
             umma_commit(bar_mma);
+            umma_commit(bar_d1p);   // the same MMAs, for the producer
             // S^T += W^T_hi K~_hi + W^T_lo K~_hi + W^T_hi K~_lo, once W^T is written
             if (!(ok = role_wait(bar_wready, wr_par, s_abort) && role_wait(bar_b, b_par, s_abort))) break;
             wr_par ^= 1u;
@@ -1228,7 +1231,7 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
                 prefetch_l2(image(1), IMG_BYTES);
             }
         }
-        uint32_t vd_par = 0, slo_par = 0, wr_par = 0, os_par = 0, upd_par = 0;
+        uint32_t vd_par = 0, slo_par = 0, d1_par = 0, os_par = 0, upd_par = 0;
         for (int ci = 0; ci < nchunks && ok; ++ci) {
             const int t0 = bos + 64 * ci;
             const bool full = eos - t0 >= 64;
@@ -1252,9 +1255,10 @@ __device__ __forceinline__ void scan_unit(const SplitParams& sp, uint8_t* sm, ui
             if (!(ok = role_wait(bar_slo, slo_par, s_abort))) break;
             slo_par ^= 1u;
             if (ci + 1 < nchunks && !(ok = fetch_gamma(ci + 1))) break;
-            // D1 is in: [-Wk; Q'] and Q' lo have been read
-            if (!(ok = role_wait(bar_wready, wr_par, s_abort))) break;
-            wr_par ^= 1u;
+            // D1 is done: [-Wk; Q'] and Q' lo have been read.  (Chunk ci+1's D1 needs the copy
+            // made here, so bar_d1p cannot run a phase ahead of this wait.)
+            if (!(ok = role_wait(bar_d1p, d1_par, s_abort))) break;
+            d1_par ^= 1u;
             if (ci + 1 < nchunks && !(ok = fetch_front(ci + 1))) break;
             if (p.gate && ci + 2 < nchunks) {   // the gate logits of two chunks ahead into L2
 #pragma unroll
