@@ -24,11 +24,14 @@ constexpr int kSlice = 32;   // value columns per CTA
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kAld = kChunk + 1;  // padded row stride of A and P
+constexpr int kCt = kChunk + 1;   // odd row stride of the transposed column operand of A and P
+constexpr int kTiles = 136;       // 4 x 4 tiles on and below the diagonal of a 64 x 64 chunk
 
 template <int D>
 constexpr size_t simt_smem_bytes()
 {
-    return sizeof(float) * (4 * kChunk * D + 2 * kChunk * kAld + kChunk * kSlice + D * kSlice + kChunk);
+    return sizeof(float) *
+           (4 * kChunk * D + 2 * kChunk * kAld + kChunk * kSlice + D * kSlice + kChunk + D * kCt + 7 * D);
 }
 
 template <typename Tin, int D>
@@ -44,6 +47,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
     float* sV = sP + kChunk * kAld;    // [C][kSlice]  beta v, then U, then W
     float* sS = sV + kChunk * kSlice;  // [D][kSlice]  state slice
     float* sB = sS + D * kSlice;       // [C] beta
+    float* sCt = sB + kChunk;          // [D][kCt]  k_i e^{rho_J' - Gamma_i}, transposed (A and P only)
+    float* sF = sCt + D * kCt;         // [7][D]    e^{rho_J - rho_J'} per sub-tile pair J > J', then ones
 
     const int n = blockIdx.x, h = blockIdx.y, js = blockIdx.z * kSlice;
     const int H = a.num_heads;
@@ -100,32 +105,82 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
         }
         __syncthreads();
 
-        // A and P, one warp per (r, i) pair, lanes over key channels
-        const int npairs = BT * (BT + 1) / 2;
-        for (int pidx = warp; pidx < npairs; pidx += kWarps) {
-            int r = (int)((sqrtf(8.f * pidx + 1.f) - 1.f) * 0.5f);
-            while (r * (r + 1) / 2 > pidx) --r;
-            while ((r + 1) * (r + 2) / 2 <= pidx) ++r;
-            const int i = pidx - r * (r + 1) / 2;
-            float kk = 0.f, qk = 0.f;
-#pragma unroll
-            for (int u = 0; u < D / 32; ++u) {
-                const int c = lane + 32 * u;
-                const float e = expf(sG[r * D + c] - sG[i * D + c]);
-                const float ki = sK[i * D + c] * e;
-                kk += sK[r * D + c] * ki;
-                qk += sQ[r * D + c] * ki;
+        // A and P as register-tiled products over bounded per-token factors (g >= -5, llm-atlas
+        // Q06's bounded decay).  For token r in 16-token sub-tile J, with base rho_J =
+        // Gamma_{16J-1} (0 for J = 0) and J' the sub-tile of i <= r,
+        //   e^{Gamma_r - Gamma_i} = e^{Gamma_r - rho_J} e^{rho_J - rho_J'} e^{rho_J' - Gamma_i},
+        // factors <= 1, <= 1 and <= e^{80}.  The row operand (k_r, then q_r, times the first
+        // factor) goes to sKg (free until the right-hand sides below), the column operand k_i
+        // e^{rho_J' - Gamma_i} transposed to sCt, the middle factors to sF; each of 136 threads
+        // then sums one 4 x 4 tile of the lower triangle over the key channels, A in a first
+        // pass and P in a second.
+        const auto rho_of = [&](int J, int c) { return J ? sG[(16 * J - 1) * D + c] : 0.f; };
+        for (int idx = t; idx < kChunk * D; idx += kThreads) {
+            const int r = idx / D, c = idx % D;
+            float rv = 0.f, cv = 0.f;
+            if (r < BT) {
+                const float rho = rho_of(r >> 4, c), gr = sG[idx], kr = sK[idx];
+                rv = kr * expf(gr - rho);
+                cv = kr * expf(rho - gr);
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                kk += __shfl_xor_sync(0xffffffffu, kk, o);
-                qk += __shfl_xor_sync(0xffffffffu, qk, o);
+            sKg[idx] = rv;
+            sCt[c * kCt + r] = cv;
+        }
+        for (int idx = t; idx < 7 * D; idx += kThreads) {
+            const int pr = idx / D, c = idx % D;   // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2), then ones
+            const int J = pr < 1 ? 1 : (pr < 3 ? 2 : 3), Jp = pr - J * (J - 1) / 2;
+            sF[idx] = pr == 6 ? 1.f : (16 * J - 1 < BT ? expf(rho_of(J, c) - rho_of(Jp, c)) : 0.f);
+        }
+        __syncthreads();
+        int rb = 0;   // this thread's tile: rows [4 rb, +4), columns [4 ib, +4), ib <= rb
+        while ((rb + 1) * (rb + 2) / 2 <= t) ++rb;
+        const int ib = t - rb * (rb + 1) / 2;
+        for (int pass = 0; pass < 2; ++pass) {
+            if (pass == 1) {   // the row operand of P, over that of A
+                __syncthreads();
+                for (int idx = t; idx < kChunk * D; idx += kThreads) {
+                    const int r = idx / D, c = idx % D;
+                    sKg[idx] = r < BT ? sQ[idx] * expf(sG[idx] - rho_of(r >> 4, c)) : 0.f;
+                }
+                __syncthreads();
             }
-            if (lane == 0) {
-                sA[r * kAld + i] = (i < r) ? sB[r] * kk : 0.f;
-                sP[r * kAld + i] = qk;
+            if (t < kTiles) {
+                const int Jr = rb >> 2, Ji = ib >> 2;
+                const float* fr = sF + (Jr == Ji ? 6 : Jr * (Jr - 1) / 2 + Ji) * D;
+                float acc[4][4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+                // the channel order starts at 4 rb, so that row blocks read different banks
+                for (int kx = 0; kx < D; ++kx) {
+                    const int c = (4 * rb + kx) & (D - 1);
+                    const float f = fr[c];
+                    float cv[4], rv[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) cv[j] = sCt[c * kCt + 4 * ib + j] * f;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) rv[i] = sKg[(4 * rb + i) * D + c];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(rv[i], cv[j], acc[i][j]);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 4 * rb + i;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int col = 4 * ib + j;
+                        if (col <= r && r < BT) {
+                            if (pass == 0) sA[r * kAld + col] = (col < r) ? sB[r] * acc[i][j] : 0.f;
+                            else sP[r * kAld + col] = acc[i][j];
+                        }
+                    }
+                }
             }
         }
+        __syncthreads();
         // right-hand sides diag(beta) [V | K exp(Gamma)]
         for (int idx = t; idx < BT * D; idx += kThreads) {
             const int r = idx / D;
