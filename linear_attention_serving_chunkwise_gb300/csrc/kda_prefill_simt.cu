@@ -23,7 +23,8 @@ constexpr int kChunk = 64;
 constexpr int kSlice = 32;   // value columns per CTA
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kAld = kChunk + 1;  // padded row stride of A and P
+constexpr int kAld = kChunk + 1;  // padded row stride of P
+constexpr int kAt = kChunk + 4;   // row stride of A transposed (A^T[i][r]; 16-byte aligned rows)
 constexpr int kCt = kChunk + 1;   // odd row stride of the transposed column operand of A and P
 constexpr int kTiles = 136;       // 4 x 4 tiles on and below the diagonal of a 64 x 64 chunk
 
@@ -31,7 +32,17 @@ template <int D>
 constexpr size_t simt_smem_bytes()
 {
     return sizeof(float) *
-           (4 * kChunk * D + 2 * kChunk * kAld + kChunk * kSlice + D * kSlice + kChunk + D * kCt + 7 * D);
+           (4 * kChunk * D + kChunk * kAt + kChunk * kAld + kChunk * kSlice + D * kSlice + kChunk + D * kCt + 7 * D);
+}
+
+// Four consecutive elements (16-byte aligned for fp32, 8-byte for bf16) as fp32.
+__device__ __forceinline__ float4 load4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p)
+{
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
 }
 
 template <typename Tin, int D>
@@ -42,8 +53,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
     float* sK = sQ + kChunk * D;       // [C][D]  k, then k * exp(Gamma_n - Gamma)
     float* sG = sK + kChunk * D;       // [C][D]  g, then Gamma
     float* sKg = sG + kChunk * D;      // [C][D]  beta k exp(Gamma), then Wk
-    float* sA = sKg + kChunk * D;      // [C][C+1]
-    float* sP = sA + kChunk * kAld;    // [C][C+1]
+    float* sA = sKg + kChunk * D;      // [C][kAt]  A transposed: sA[i * kAt + r] = A[r][i]
+    float* sP = sA + kChunk * kAt;     // [C][C+1]
     float* sV = sP + kChunk * kAld;    // [C][kSlice]  beta v, then U, then W
     float* sS = sV + kChunk * kSlice;  // [D][kSlice]  state slice
     float* sB = sS + D * kSlice;       // [C] beta
@@ -69,16 +80,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
     for (int c0 = bos; c0 < eos; c0 += kChunk) {
         const int BT = min(kChunk, eos - c0);
         __syncthreads();
-        for (int idx = t; idx < BT * D; idx += kThreads) {
+        // inputs four channels at a time, the loads of several rows in flight together
+#pragma unroll 4
+        for (int idx = 4 * t; idx < BT * D; idx += 4 * kThreads) {
             const int r = idx / D, c = idx % D;
             const size_t gi = ((size_t)(c0 + r) * H + h) * D + c;
-            sQ[idx] = to_f32(q[gi]);
-            sK[idx] = to_f32(k[gi]);
-            sG[idx] = g_of(a.g[gi], a.prologue);
+            const float4 qv = load4(q + gi), kv = load4(k + gi), gv = load4(a.g + gi);
+            *reinterpret_cast<float4*>(sQ + idx) = qv;
+            *reinterpret_cast<float4*>(sK + idx) = kv;
+            *reinterpret_cast<float4*>(sG + idx) =
+                make_float4(g_of(gv.x, a.prologue), g_of(gv.y, a.prologue), g_of(gv.z, a.prologue), g_of(gv.w, a.prologue));
         }
-        for (int idx = t; idx < BT * kSlice; idx += kThreads) {
+        for (int idx = 4 * t; idx < BT * kSlice; idx += 4 * kThreads) {
             const int r = idx / kSlice, j = idx % kSlice;
-            sV[idx] = to_f32(v[((size_t)(c0 + r) * H + h) * D + js + j]);
+            *reinterpret_cast<float4*>(sV + idx) = load4(v + ((size_t)(c0 + r) * H + h) * D + js + j);
         }
         if (t < BT) sB[t] = beta_of(a.beta[(size_t)(c0 + t) * H + h], a.prologue);
         __syncthreads();
@@ -173,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
                     for (int j = 0; j < 4; ++j) {
                         const int col = 4 * ib + j;
                         if (col <= r && r < BT) {
-                            if (pass == 0) sA[r * kAld + col] = (col < r) ? sB[r] * acc[i][j] : 0.f;
+                            if (pass == 0) sA[col * kAt + r] = (col < r) ? sB[r] * acc[i][j] : 0.f;
                             else sP[r * kAld + col] = acc[i][j];
                         }
                     }
@@ -193,10 +208,28 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
         for (int col = t; col < kSlice + D; col += kThreads) {
             float* X = (col < kSlice) ? (sV + col) : (sKg + (col - kSlice));
             const int ld = (col < kSlice) ? kSlice : D;
-            for (int r = 1; r < BT; ++r) {
-                float acc = X[r * ld];
-                for (int i = 0; i < r; ++i) acc -= sA[r * kAld + i] * X[i * ld];
-                X[r * ld] = acc;
+            // four rows at a time: each solved value X[i] meets the four rows' A[r][i] in one
+            // float4 of A^T, then the block's own lower triangle in registers (rows past the
+            // chunk's end are formed from whatever they hold and never stored)
+            for (int r0 = 0; r0 < BT; r0 += 4) {
+                float x[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) x[j] = (r0 + j < BT) ? X[(r0 + j) * ld] : 0.f;
+                for (int i = 0; i < r0; ++i) {
+                    const float xi = X[i * ld];
+                    const float4 a4 = *reinterpret_cast<const float4*>(sA + i * kAt + r0);
+                    x[0] -= a4.x * xi;
+                    x[1] -= a4.y * xi;
+                    x[2] -= a4.z * xi;
+                    x[3] -= a4.w * xi;
+                }
+#pragma unroll
+                for (int j = 1; j < 4; ++j)
+#pragma unroll
+                    for (int jj = 0; jj < j; ++jj) x[j] -= sA[(r0 + jj) * kAt + r0 + j] * x[jj];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (r0 + j < BT) X[(r0 + j) * ld] = x[j];
             }
         }
         __syncthreads();
