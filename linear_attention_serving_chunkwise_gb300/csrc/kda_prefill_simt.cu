@@ -23,7 +23,7 @@ constexpr int kChunk = 64;
 constexpr int kSlice = 32;   // value columns per CTA
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kAld = kChunk + 1;  // padded row stride of P
+constexpr int kAld = kChunk + 4;  // row stride of P (16-byte aligned rows)
 constexpr int kAt = kChunk + 4;   // row stride of A transposed (A^T[i][r]; 16-byte aligned rows)
 constexpr int kCt = kChunk + 1;   // odd row stride of the transposed column operand of A and P
 constexpr int kTiles = 136;       // 4 x 4 tiles on and below the diagonal of a 64 x 64 chunk
@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
     float* sG = sK + kChunk * D;       // [C][D]  g, then Gamma
     float* sKg = sG + kChunk * D;      // [C][D]  beta k exp(Gamma), then Wk
     float* sA = sKg + kChunk * D;      // [C][kAt]  A transposed: sA[i * kAt + r] = A[r][i]
-    float* sP = sA + kChunk * kAt;     // [C][C+1]
+    float* sP = sA + kChunk * kAt;     // [C][kAld]
     float* sV = sP + kChunk * kAld;    // [C][kSlice]  beta v, then U, then W
     float* sS = sV + kChunk * kSlice;  // [D][kSlice]  state slice
     float* sB = sS + D * kSlice;       // [C] beta
@@ -234,7 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
         }
         __syncthreads();
 
-        // decayed operands in place; W = U - Wk S (in place in sV, row r by warp)
+        // decayed operands in place; W = U - Wk S (in place in sV).  In the three products
+        // below, warp w takes 8 consecutive rows (or D / 8 consecutive state rows) at once,
+        // so that each value of S, W or V it loads serves all of them, and reads the other
+        // operand's rows four channels at a time (each sum still runs in its own order).
         const float* gl = sG + (BT - 1) * D;
         for (int idx = t; idx < BT * D; idx += kThreads) {
             const int c = idx % D;
@@ -242,40 +245,103 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
             sQ[idx] *= expf(e);
             sK[idx] *= expf(gl[c] - e);
         }
-        for (int r = warp; r < BT; r += kWarps) {
-            float acc = sV[r * kSlice + lane];
-            for (int c = 0; c < D; ++c) acc -= sKg[r * D + c] * sS[c * kSlice + lane];
-            sV[r * kSlice + lane] = acc;
+        const int r8 = 8 * warp;   // this warp's rows [r8, r8 + 8)
+        {
+            float acc[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) acc[m] = sV[(r8 + m) * kSlice + lane];
+            for (int c = 0; c < D; c += 4) {
+                float s4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) s4[u] = sS[(c + u) * kSlice + lane];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const float4 w4 = *reinterpret_cast<const float4*>(sKg + (r8 + m) * D + c);
+                    acc[m] = fmaf(-w4.x, s4[0], acc[m]);
+                    acc[m] = fmaf(-w4.y, s4[1], acc[m]);
+                    acc[m] = fmaf(-w4.z, s4[2], acc[m]);
+                    acc[m] = fmaf(-w4.w, s4[3], acc[m]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+                if (r8 + m < BT) sV[(r8 + m) * kSlice + lane] = acc[m];
         }
         __syncthreads();
 
         // O = Q_Gamma S + P W, written in fp32
-        for (int r = warp; r < BT; r += kWarps) {
-            float acc = 0.f;
-            for (int c = 0; c < D; ++c) acc += sQ[r * D + c] * sS[c * kSlice + lane];
-            for (int i = 0; i <= r; ++i) acc += sP[r * kAld + i] * sV[i * kSlice + lane];
-            const size_t oi = ((size_t)(c0 + r) * H + h) * D + js + lane;
-            a.out[oi] = a.gate ? gate1(acc, __ldg(a.gate + oi)) : acc;
-        }
-        // S <- Diag(exp Gamma_n) S + K~^T W
-        float snew[D / kWarps];
+        {
+            float acc[8];
 #pragma unroll
-        for (int m = 0; m < D / kWarps; ++m) {
-            const int c = warp + kWarps * m;
-            float acc = expf(gl[c]) * sS[c * kSlice + lane];
-            for (int r = 0; r < BT; ++r) acc += sK[r * D + c] * sV[r * kSlice + lane];
-            snew[m] = acc;
+            for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+            for (int c = 0; c < D; c += 4) {
+                float s4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) s4[u] = sS[(c + u) * kSlice + lane];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const float4 q4 = *reinterpret_cast<const float4*>(sQ + (r8 + m) * D + c);
+                    acc[m] = fmaf(q4.x, s4[0], acc[m]);
+                    acc[m] = fmaf(q4.y, s4[1], acc[m]);
+                    acc[m] = fmaf(q4.z, s4[2], acc[m]);
+                    acc[m] = fmaf(q4.w, s4[3], acc[m]);
+                }
+            }
+            for (int i = 0; i < r8; i += 4) {   // tokens before the warp's rows: every row takes them
+                float v4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v4[u] = sV[(i + u) * kSlice + lane];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const float4 p4 = *reinterpret_cast<const float4*>(sP + (r8 + m) * kAld + i);
+                    acc[m] = fmaf(p4.x, v4[0], acc[m]);
+                    acc[m] = fmaf(p4.y, v4[1], acc[m]);
+                    acc[m] = fmaf(p4.z, v4[2], acc[m]);
+                    acc[m] = fmaf(p4.w, v4[3], acc[m]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {   // the warp's own tokens: row r8 + m takes i <= r8 + m
+                const float v = sV[(r8 + u) * kSlice + lane];
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    if (u <= m) acc[m] = fmaf(sP[(r8 + m) * kAld + r8 + u], v, acc[m]);
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                if (r8 + m < BT) {
+                    const size_t oi = ((size_t)(c0 + r8 + m) * H + h) * D + js + lane;
+                    a.out[oi] = a.gate ? gate1(acc[m], __ldg(a.gate + oi)) : acc[m];
+                }
+            }
+        }
+        // S <- Diag(exp Gamma_n) S + K~^T W: warp w takes state rows [D/8 w, +D/8)
+        constexpr int kRows = D / kWarps;
+        const int cw = kRows * warp;
+        float snew[kRows];
+#pragma unroll
+        for (int m = 0; m < kRows; ++m) snew[m] = expf(gl[cw + m]) * sS[(cw + m) * kSlice + lane];
+        for (int r = 0; r < BT; ++r) {
+            const float v = sV[r * kSlice + lane];
+#pragma unroll
+            for (int m4 = 0; m4 < kRows; m4 += 4) {
+                const float4 k4 = *reinterpret_cast<const float4*>(sK + r * D + cw + m4);
+                snew[m4] = fmaf(k4.x, v, snew[m4]);
+                snew[m4 + 1] = fmaf(k4.y, v, snew[m4 + 1]);
+                snew[m4 + 2] = fmaf(k4.z, v, snew[m4 + 2]);
+                snew[m4 + 3] = fmaf(k4.w, v, snew[m4 + 3]);
+            }
         }
         __syncthreads();
 #pragma unroll
-        for (int m = 0; m < D / kWarps; ++m) sS[(warp + kWarps * m) * kSlice + lane] = snew[m];
+        for (int m = 0; m < kRows; ++m) sS[(cw + m) * kSlice + lane] = snew[m];
         // state snapshot after a full chunk that ends on a checkpoint boundary
         const int done = c0 + BT - bos;
         if (a.checkpoints && BT == kChunk && done % a.ckpt_interval == 0 && done / a.ckpt_interval <= a.ckpt_slots) {
             const int slot = done / a.ckpt_interval - 1;
             float* dst = a.checkpoints + (((size_t)n * H + h) * a.ckpt_slots + slot) * D * D;
 #pragma unroll
-            for (int m = 0; m < D / kWarps; ++m) dst[(size_t)(warp + kWarps * m) * D + js + lane] = snew[m];
+            for (int m = 0; m < kRows; ++m) dst[(size_t)(cw + m) * D + js + lane] = snew[m];
         }
     }
     __syncthreads();
