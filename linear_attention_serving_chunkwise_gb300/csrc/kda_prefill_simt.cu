@@ -25,7 +25,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kAld = kChunk + 4;  // row stride of P (16-byte aligned rows)
 constexpr int kAt = kChunk + 4;   // row stride of A transposed (A^T[i][r]; 16-byte aligned rows)
-constexpr int kCt = kChunk + 1;   // odd row stride of the transposed column operand of A and P
+constexpr int kCt = kChunk + 4;   // row stride of the transposed column operand of A and P (16-byte rows)
 constexpr int kTiles = 136;       // 4 x 4 tiles on and below the diagonal of a 64 x 64 chunk
 
 template <int D>
@@ -127,8 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
         // factors <= 1, <= 1 and <= e^{80}.  The row operand (k_r, then q_r, times the first
         // factor) goes to sKg (free until the right-hand sides below), the column operand k_i
         // e^{rho_J' - Gamma_i} transposed to sCt, the middle factors to sF; each of 136 threads
-        // then sums one 4 x 4 tile of the lower triangle over the key channels, A in a first
-        // pass and P in a second.
+        // then sums one 4 x 4 tile of the lower triangle over the key channels, four at a time
+        // (one 16-byte load per operand row), A in a first pass and P in a second.
         const auto rho_of = [&](int J, int c) { return J ? sG[(16 * J - 1) * D + c] : 0.f; };
         for (int idx = t; idx < kChunk * D; idx += kThreads) {
             const int r = idx / D, c = idx % D;
@@ -168,18 +168,24 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
                 // the channel order starts at 4 rb, so that row blocks read different banks
-                for (int kx = 0; kx < D; ++kx) {
+                for (int kx = 0; kx < D; kx += 4) {
                     const int c = (4 * rb + kx) & (D - 1);
-                    const float f = fr[c];
-                    float cv[4], rv[4];
+                    const float4 f4 = *reinterpret_cast<const float4*>(fr + c);
+                    float4 r4[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) cv[j] = sCt[c * kCt + 4 * ib + j] * f;
+                    for (int i = 0; i < 4; ++i) r4[i] = *reinterpret_cast<const float4*>(sKg + (4 * rb + i) * D + c);
+                    const float fu[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) rv[i] = sKg[(4 * rb + i) * D + c];
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 c4 = *reinterpret_cast<const float4*>(sCt + (c + u) * kCt + 4 * ib);
+                        const float cv[4] = {c4.x * fu[u], c4.y * fu[u], c4.z * fu[u], c4.w * fu[u]};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
+                        for (int i = 0; i < 4; ++i) {
+                            const float rv = u == 0 ? r4[i].x : u == 1 ? r4[i].y : u == 2 ? r4[i].z : r4[i].w;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(rv[i], cv[j], acc[i][j]);
+                            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(rv, cv[j], acc[i][j]);
+                        }
+                    }
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
