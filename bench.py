@@ -13,7 +13,8 @@ reported in the ``decode`` object, and K = 4 tokens per sequence through one
 state) every step.  ``prologue`` times the same prefill from the recipe's raw draws with the
 input prologue in the kernels, ``gate`` the same prefill through ``kda_prefill_gated`` (the
 output gate o * sigmoid(z)), ``checkpoints`` through ``kda_prefill_checkpointed`` (a state
-snapshot every 512 tokens) and ``context_parallel`` the same sequence as two token ranges
+snapshot every 512 tokens), ``fp32`` the same workload with fp32 q/k/v on the CUDA-core
+kernel (at most 10 calls), and ``context_parallel`` the same sequence as two token ranges
 emulated on this GPU (local passes, one fold, the rerun).  nvidia-smi clock samples are kept for the timed windows of
 every leg.
 
@@ -620,6 +621,52 @@ def run_cuda(args, world, rank, local):
     except Exception as exc:   # noqa: BLE001 -- recorded in the line instead of ending the run
         ckpt["error"] = f"{type(exc).__name__}: {exc}"
 
+    # ---------------- fp32 inputs: the headline workload with q, k, v in fp32, on the CUDA-core
+    # chunkwise kernel (the path of the 1e-4 bar); at most 10 timed calls, as each takes ~15 ms.
+    # Its bound is the fp32 FMA pipe: 152 SMs x 128 FMA lanes x 2 flop x 2.07 GHz (maximum SM clock).
+    fp32 = {"workload": cfg.name.replace("bf16", "fp32"), "kernel": "kda_prefill_simt_kernel"}
+    try:
+        fcfg = W.PrefillConfig(fp32["workload"], cfg.seqlens, cfg.num_heads, cfg.dk, cfg.dv, torch.float32,
+                               cfg.init_state)
+        fd = W.make_prefill_inputs(fcfg, seed=rank, device=dev)
+        fplan = kda.prefill_query(kda.make_desc(fcfg.num_seqs, fcfg.total_tokens, fcfg.num_heads, fcfg.dk,
+                                                fcfg.dv, kda.KDA_F32))
+        fws = torch.empty(max(fplan["workspace_bytes"], 16), dtype=torch.uint8, device=dev)
+        fargs = (fd["q"], fd["k"], fd["v"], fd["g"], fd["beta"], fd["cu_seqlens"], fd["init_state"])
+        fsteps = min(args.steps, 10)
+
+        def f32_call():
+            kda.prefill(*fargs, out=out, final_state=fin, workspace=fws, stream=stream)
+
+        for _ in range(min(args.warmup, 3)):
+            f32_call()
+        stream.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _barrier(world)
+        w0 = time.time()
+        f0.record(stream)
+        for _ in range(fsteps):
+            f32_call()
+        f1.record(stream)
+        stream.synchronize()
+        sampler.window("fp32", w0, time.time())
+        if kda.last_device_status(stream) != kda.KDA_OK:
+            raise RuntimeError("the fp32 prefill reported a device error")
+        f_ms = _max_over_ranks(f0.elapsed_time(f1) / fsteps, world)
+        f_bytes, f_flops = prefill_algorithmic(fcfg)
+        fp32_peak_tflops = 152 * 128 * 2 * 2.07e9 / 1e12
+        fp32.update({"ms_per_call": f_ms, "tokens_per_s": tokens_per_step / (f_ms / 1e3), "calls": fsteps,
+                     "vs_bf16_call": ms_per_step / f_ms,
+                     "roofline": {"bound": "alu", "achieved": f_flops / (f_ms / 1e3) / 1e12,
+                                  "peak": fp32_peak_tflops, "unit": "TFLOP/s",
+                                  "frac": f_flops / (f_ms / 1e3) / 1e12 / fp32_peak_tflops, "traffic": None,
+                                  "algorithmic_flops_per_launch": f_flops,
+                                  "hbm_gbs": f_bytes / (f_ms / 1e3) / 1e9},
+                     "gpu_launches": fsteps * fplan["kernel_launches"]})
+        del fd, fargs, fws
+    except Exception as exc:   # noqa: BLE001 -- recorded in the line instead of ending the run
+        fp32["error"] = f"{type(exc).__name__}: {exc}"
+
     # ---------------- context parallelism emulated on this GPU: the headline sequence as two
     # token ranges (local transition and zero-start passes of both as one varlen call each, the
     # fold, the rerun from the folded states).  Three prefill passes, so slower than one call on
@@ -663,7 +710,7 @@ def run_cuda(args, world, rank, local):
                        "parallelism": f"independent problem per GPU x{world}"},
             "roofline": roofline, "tensor": tensor, "e2e": e2e, "clocks": clocks,
             "gpu_launches": args.steps * plan["kernel_launches"], "decode": decode, "decode_multi": decode_multi,
-            "prologue": prologue, "gate": gate, "checkpoints": ckpt, "context_parallel": cp}
+            "prologue": prologue, "gate": gate, "checkpoints": ckpt, "fp32": fp32, "context_parallel": cp}
     if rank == 0 and world == 1:
         rate, dt, cores, sdesc = oracle_sample(cfg, heads=96, tokens=8192)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sdesc,
