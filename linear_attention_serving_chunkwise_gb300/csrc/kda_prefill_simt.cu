@@ -214,32 +214,30 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
         for (int col = t; col < kSlice + D; col += kThreads) {
             float* X = (col < kSlice) ? (sV + col) : (sKg + (col - kSlice));
             const int ld = (col < kSlice) ? kSlice : D;
-            // eight rows at a time: each solved value X[i] meets the eight rows' A[r][i] in two
-            // float4 of A^T, then the block's own lower triangle in registers (rows past the
-            // chunk's end are formed from whatever they hold and never stored)
-            for (int r0 = 0; r0 < BT; r0 += 8) {
-                float x[8];
+            // sixteen rows (one sub-tile) at a time: each solved value X[i] meets the block's
+            // A[r][i] in four float4 of A^T, then the block's own lower triangle in registers
+            // (rows past the chunk's end are formed from whatever they hold and never stored)
+            for (int r0 = 0; r0 < BT; r0 += 16) {
+                float x[16];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) x[j] = (r0 + j < BT) ? X[(r0 + j) * ld] : 0.f;
+                for (int j = 0; j < 16; ++j) x[j] = (r0 + j < BT) ? X[(r0 + j) * ld] : 0.f;
                 for (int i = 0; i < r0; ++i) {
                     const float xi = X[i * ld];
-                    const float4 a4 = *reinterpret_cast<const float4*>(sA + i * kAt + r0);
-                    const float4 b4 = *reinterpret_cast<const float4*>(sA + i * kAt + r0 + 4);
-                    x[0] -= a4.x * xi;
-                    x[1] -= a4.y * xi;
-                    x[2] -= a4.z * xi;
-                    x[3] -= a4.w * xi;
-                    x[4] -= b4.x * xi;
-                    x[5] -= b4.y * xi;
-                    x[6] -= b4.z * xi;
-                    x[7] -= b4.w * xi;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(sA + i * kAt + r0 + 4 * q4);
+                        x[4 * q4] -= a4.x * xi;
+                        x[4 * q4 + 1] -= a4.y * xi;
+                        x[4 * q4 + 2] -= a4.z * xi;
+                        x[4 * q4 + 3] -= a4.w * xi;
+                    }
                 }
 #pragma unroll
-                for (int j = 1; j < 8; ++j)
+                for (int j = 1; j < 16; ++j)
 #pragma unroll
                     for (int jj = 0; jj < j; ++jj) x[j] -= sA[(r0 + jj) * kAt + r0 + j] * x[jj];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < 16; ++j)
                     if (r0 + j < BT) X[(r0 + j) * ld] = x[j];
             }
         }
