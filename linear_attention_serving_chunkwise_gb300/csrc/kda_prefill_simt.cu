@@ -12,7 +12,12 @@
 // sums, each of which is <= 0 because g <= 0, so nothing overflows.
 //
 // One CTA per (sequence, head, 32-column slice of dv): the columns of S evolve
-// independently, so the slices need no communication.  fp32 throughout.
+// independently.  The slices of one (sequence, head) form a thread-block cluster and
+// share the work that does not depend on the slice: each forms A and P over its own
+// 32 key channels (the partial sums meet through distributed shared memory) and solves
+// for its own 32 columns of Wk (which it then reads from the others).  fp32 throughout.
+#include <cooperative_groups.h>
+
 #include "kda_common.cuh"
 #include "kda_launch.h"
 
@@ -28,11 +33,13 @@ constexpr int kAt = kChunk + 4;   // row stride of A transposed (A^T[i][r]; 16-b
 constexpr int kCt = kChunk + 4;   // row stride of the transposed column operand of A and P (16-byte rows)
 constexpr int kTiles = 136;       // 4 x 4 tiles on and below the diagonal of a 64 x 64 chunk
 
+constexpr int kDq = kSlice;       // key channels (A and P) and columns of Wk per CTA of a cluster
+
 template <int D>
 constexpr size_t simt_smem_bytes()
 {
     return sizeof(float) *
-           (4 * kChunk * D + kChunk * kAt + kChunk * kAld + kChunk * kSlice + D * kSlice + kChunk + D * kCt + 7 * D);
+           (4 * kChunk * D + kChunk * kAt + kChunk * kAld + kChunk * kSlice + D * kSlice + kChunk + kDq * kCt + 7 * kDq);
 }
 
 // Four consecutive elements (16-byte aligned for fp32, 8-byte for bf16) as fp32.
@@ -46,7 +53,7 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16* p)
 }
 
 template <typename Tin, int D>
-__global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillArgs a)
+__global__ void __cluster_dims__(1, 1, D / kSlice) __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillArgs a)
 {
     extern __shared__ float smem[];
     float* sQ = smem;                  // [C][D]  q, then q * exp(Gamma)
@@ -58,8 +65,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
     float* sV = sP + kChunk * kAld;    // [C][kSlice]  beta v, then U, then W
     float* sS = sV + kChunk * kSlice;  // [D][kSlice]  state slice
     float* sB = sS + D * kSlice;       // [C] beta
-    float* sCt = sB + kChunk;          // [D][kCt]  k_i e^{rho_J' - Gamma_i}, transposed (A and P only)
-    float* sF = sCt + D * kCt;         // [7][D]    e^{rho_J - rho_J'} per sub-tile pair J > J', then ones
+    float* sCt = sB + kChunk;          // [kDq][kCt] k_i e^{rho_J' - Gamma_i} of this CTA's channels, transposed
+    float* sF = sCt + kDq * kCt;       // [7][kDq]   e^{rho_J - rho_J'} per sub-tile pair J > J', then ones
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    constexpr int kNC = D / kSlice;    // CTAs in the cluster (the dv slices of this (sequence, head))
+    const int cq = (int)cluster.block_rank(), cc0 = kDq * cq;   // this CTA's key channels [cc0, +kDq)
 
     const int n = blockIdx.x, h = blockIdx.y, js = blockIdx.z * kSlice;
     const int H = a.num_heads;
@@ -124,25 +135,25 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
         // Q06's bounded decay).  For token r in 16-token sub-tile J, with base rho_J =
         // Gamma_{16J-1} (0 for J = 0) and J' the sub-tile of i <= r,
         //   e^{Gamma_r - Gamma_i} = e^{Gamma_r - rho_J} e^{rho_J - rho_J'} e^{rho_J' - Gamma_i},
-        // factors <= 1, <= 1 and <= e^{80}.  The row operand (k_r, then q_r, times the first
-        // factor) goes to sKg (free until the right-hand sides below), the column operand k_i
-        // e^{rho_J' - Gamma_i} transposed to sCt, the middle factors to sF; each of 136 threads
-        // then sums one 4 x 4 tile of the lower triangle over the key channels, four at a time
-        // (one 16-byte load per operand row), A in a first pass and P in a second.
+        // factors <= 1, <= 1 and <= e^{80}.  Over this CTA's 32 key channels: the row operand
+        // (k_r, then q_r, times the first factor) to sKg as [64][32] (free until the right-hand
+        // sides below), the column operand k_i e^{rho_J' - Gamma_i} transposed to sCt, the
+        // middle factors to sF; each of 136 threads sums one 4 x 4 tile of the lower triangle
+        // over those channels, four at a time, A's partial sums into sA and then P's into sP.
         const auto rho_of = [&](int J, int c) { return J ? sG[(16 * J - 1) * D + c] : 0.f; };
-        for (int idx = t; idx < kChunk * D; idx += kThreads) {
-            const int r = idx / D, c = idx % D;
+        for (int idx = t; idx < kChunk * kDq; idx += kThreads) {
+            const int r = idx / kDq, cl = idx % kDq, c = cc0 + cl;
             float rv = 0.f, cv = 0.f;
             if (r < BT) {
-                const float rho = rho_of(r >> 4, c), gr = sG[idx], kr = sK[idx];
+                const float rho = rho_of(r >> 4, c), gr = sG[r * D + c], kr = sK[r * D + c];
                 rv = kr * expf(gr - rho);
                 cv = kr * expf(rho - gr);
             }
             sKg[idx] = rv;
-            sCt[c * kCt + r] = cv;
+            sCt[cl * kCt + r] = cv;
         }
-        for (int idx = t; idx < 7 * D; idx += kThreads) {
-            const int pr = idx / D, c = idx % D;   // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2), then ones
+        for (int idx = t; idx < 7 * kDq; idx += kThreads) {
+            const int pr = idx / kDq, c = cc0 + idx % kDq;   // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2), then ones
             const int J = pr < 1 ? 1 : (pr < 3 ? 2 : 3), Jp = pr - J * (J - 1) / 2;
             sF[idx] = pr == 6 ? 1.f : (16 * J - 1 < BT ? expf(rho_of(J, c) - rho_of(Jp, c)) : 0.f);
         }
@@ -153,27 +164,27 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
         for (int pass = 0; pass < 2; ++pass) {
             if (pass == 1) {   // the row operand of P, over that of A
                 __syncthreads();
-                for (int idx = t; idx < kChunk * D; idx += kThreads) {
-                    const int r = idx / D, c = idx % D;
-                    sKg[idx] = r < BT ? sQ[idx] * expf(sG[idx] - rho_of(r >> 4, c)) : 0.f;
+                for (int idx = t; idx < kChunk * kDq; idx += kThreads) {
+                    const int r = idx / kDq, c = cc0 + idx % kDq;
+                    sKg[idx] = r < BT ? sQ[r * D + c] * expf(sG[r * D + c] - rho_of(r >> 4, c)) : 0.f;
                 }
                 __syncthreads();
             }
             if (t < kTiles) {
                 const int Jr = rb >> 2, Ji = ib >> 2;
-                const float* fr = sF + (Jr == Ji ? 6 : Jr * (Jr - 1) / 2 + Ji) * D;
+                const float* fr = sF + (Jr == Ji ? 6 : Jr * (Jr - 1) / 2 + Ji) * kDq;
                 float acc[4][4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
                 // the channel order starts at 4 rb, so that row blocks read different banks
-                for (int kx = 0; kx < D; kx += 4) {
-                    const int c = (4 * rb + kx) & (D - 1);
+                for (int kx = 0; kx < kDq; kx += 4) {
+                    const int c = (4 * rb + kx) & (kDq - 1);
                     const float4 f4 = *reinterpret_cast<const float4*>(fr + c);
                     float4 r4[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) r4[i] = *reinterpret_cast<const float4*>(sKg + (4 * rb + i) * D + c);
+                    for (int i = 0; i < 4; ++i) r4[i] = *reinterpret_cast<const float4*>(sKg + (4 * rb + i) * kDq + c);
                     const float fu[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -194,25 +205,79 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
                     for (int j = 0; j < 4; ++j) {
                         const int col = 4 * ib + j;
                         if (col <= r && r < BT) {
-                            if (pass == 0) sA[col * kAt + r] = (col < r) ? sB[r] * acc[i][j] : 0.f;
+                            if (pass == 0) sA[col * kAt + r] = acc[i][j];
                             else sP[r * kAld + col] = acc[i][j];
                         }
                     }
                 }
             }
         }
-        __syncthreads();
-        // right-hand sides diag(beta) [V | K exp(Gamma)]
-        for (int idx = t; idx < BT * D; idx += kThreads) {
-            const int r = idx / D;
-            sKg[idx] = sB[r] * sK[idx] * expf(sG[idx]);
+        // the partial sums of the cluster's CTAs, summed in rank order by the CTA that owns the
+        // rows ([64 / kNC rank, +64 / kNC)).  Every exchange is a store into another CTA's
+        // shared memory: the partial sums of the others' rows go to slots in their sKg (free
+        // from the end of the tiles to the right-hand sides), the owner sums, and the sums go
+        // to every CTA's sA and sP (where each CTA reads only the rows it owns meanwhile).
+        {
+            constexpr int kRows = kChunk / kNC, kPer = kRows * kChunk / kThreads;
+            // partial sums of sender s in receiver q's sKg: slot s - (s > q), A then P, [kRows][64]
+            const auto slot = [&](int s, int q, int ap) { return ((s - (s > q)) * 2 + ap) * kRows * kChunk; };
+            static_assert((kNC - 1) * 2 * kRows * kChunk <= kChunk * D, "partial-sum slots fit in sKg");
+            cluster.sync();   // every CTA's tiles are done: their sKg is free
+            for (int qo = 1; qo < kNC; ++qo) {
+                const int q = (cq + qo) % kNC;
+                float* dst = cluster.map_shared_rank(sKg, q);
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    const int e = t + kThreads * k, r = kRows * q + e / kChunk, col = e % kChunk;
+                    if (r < BT && col <= r) {
+                        dst[slot(cq, q, 0) + e] = sA[col * kAt + r];
+                        dst[slot(cq, q, 1) + e] = sP[r * kAld + col];
+                    }
+                }
+            }
+            cluster.sync();   // every partial sum is delivered
+            float va[kPer], vp[kPer];
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const int e = t + kThreads * k, r = kRows * cq + e / kChunk, col = e % kChunk;
+                float sa = 0.f, sp = 0.f;
+                if (r < BT && col <= r) {
+#pragma unroll
+                    for (int s = 0; s < kNC; ++s) {
+                        sa += s == cq ? sA[col * kAt + r] : sKg[slot(s, cq, 0) + e];
+                        sp += s == cq ? sP[r * kAld + col] : sKg[slot(s, cq, 1) + e];
+                    }
+                }
+                va[k] = (col < r) ? sB[r] * sa : 0.f;
+                vp[k] = sp;
+            }
+#pragma unroll
+            for (int q = 0; q < kNC; ++q) {
+                float* qa = cluster.map_shared_rank(sA, q);
+                float* qp = cluster.map_shared_rank(sP, q);
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    const int e = t + kThreads * k, r = kRows * cq + e / kChunk, col = e % kChunk;
+                    if (r < BT && col <= r) {
+                        qa[col * kAt + r] = va[k];
+                        qp[r * kAld + col] = vp[k];
+                    }
+                }
+            }
+            cluster.sync();   // A and P complete in every CTA; every slot read
+        }
+        // right-hand sides diag(beta) [V | K exp(Gamma)], K's over this CTA's columns of Wk
+        for (int idx = t; idx < BT * kDq; idx += kThreads) {
+            const int r = idx / kDq, c = cc0 + idx % kDq;
+            sKg[r * D + c] = sB[r] * sK[r * D + c] * expf(sG[r * D + c]);
         }
         for (int idx = t; idx < BT * kSlice; idx += kThreads) sV[idx] *= sB[idx / kSlice];
         __syncthreads();
 
-        // (I + A) X = RHS by forward substitution, one column per thread
-        for (int col = t; col < kSlice + D; col += kThreads) {
-            float* X = (col < kSlice) ? (sV + col) : (sKg + (col - kSlice));
+        // (I + A) X = RHS by forward substitution, one column per thread: U's 32 and this
+        // CTA's 32 of Wk
+        for (int col = t; col < kSlice + kDq; col += kThreads) {
+            float* X = (col < kSlice) ? (sV + col) : (sKg + cc0 + (col - kSlice));
             const int ld = (col < kSlice) ? kSlice : D;
             // sixteen rows (one sub-tile) at a time: each solved value X[i] meets the block's
             // A[r][i] in four float4 of A^T, then the block's own lower triangle in registers
@@ -241,7 +306,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_simt_kernel(PrefillAr
                     if (r0 + j < BT) X[(r0 + j) * ld] = x[j];
             }
         }
+        // this CTA's columns of Wk into the other CTAs' sKg (each solves only its own columns there)
         __syncthreads();
+        for (int qo = 1; qo < kNC; ++qo) {
+            float* dst = cluster.map_shared_rank(sKg, (cq + qo) % kNC);
+            for (int i4 = t; i4 < BT * kDq / 4; i4 += kThreads) {
+                const int o = (i4 / (kDq / 4)) * D + cc0 + 4 * (i4 % (kDq / 4));
+                *reinterpret_cast<float4*>(dst + o) = *reinterpret_cast<const float4*>(sKg + o);
+            }
+        }
+        cluster.sync();   // every CTA holds all of Wk
 
         // decayed operands in place; W = U - Wk S (in place in sV).  In the three products
         // below, warp w takes 8 consecutive rows (or D / 8 consecutive state rows) at once,
