@@ -8,14 +8,15 @@
 //   (I + A) [U | Wk] = diag(beta) [V | K*exp(Gamma)]     (forward substitution)
 //   W = U - Wk S;  O = (Q*exp(Gamma)) S + P W
 //   S <- Diag(exp Gamma_n) S + (K*exp(Gamma_n - Gamma))^T W
-// Every decay between two tokens is one exponential of a difference of prefix
-// sums, each of which is <= 0 because g <= 0, so nothing overflows.
+// In A and P the decay between two tokens is a product of three bounded factors through
+// 16-token sub-tile bases (g >= -5: each factor <= e^{80}); every other decay is one
+// exponential of a difference of prefix sums, which is <= 0 because g <= 0.
 //
 // One CTA per (sequence, head, 32-column slice of dv): the columns of S evolve
 // independently.  The slices of one (sequence, head) form a thread-block cluster and
 // share the work that does not depend on the slice: each forms A and P over its own
-// 32 key channels (the partial sums meet through distributed shared memory) and solves
-// for its own 32 columns of Wk (which it then reads from the others).  fp32 throughout.
+// 32 key channels and solves for its own 32 columns of Wk, and the partial sums and the
+// columns go to the other CTAs by stores into their shared memory.  fp32 throughout.
 #include <cooperative_groups.h>
 
 #include "kda_common.cuh"
@@ -59,7 +60,8 @@ __global__ void __cluster_dims__(1, 1, D / kSlice) __launch_bounds__(kThreads, 1
     float* sQ = smem;                  // [C][D]  q, then q * exp(Gamma)
     float* sK = sQ + kChunk * D;       // [C][D]  k, then k * exp(Gamma_n - Gamma)
     float* sG = sK + kChunk * D;       // [C][D]  g, then Gamma
-    float* sKg = sG + kChunk * D;      // [C][D]  beta k exp(Gamma), then Wk
+    float* sKg = sG + kChunk * D;      // [C][D]  A/P row operand [C][kDq], then other CTAs' partial sums;
+                                       //         then beta k exp(Gamma) (own columns), then Wk
     float* sA = sKg + kChunk * D;      // [C][kAt]  A transposed: sA[i * kAt + r] = A[r][i]
     float* sP = sA + kChunk * kAt;     // [C][kAld]
     float* sV = sP + kChunk * kAld;    // [C][kSlice]  beta v, then U, then W
