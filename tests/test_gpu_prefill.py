@@ -123,6 +123,21 @@ def test_prefill_workload_h96_t8192_sampled(cuda_lib):
     _sampled_check(cuda_lib, cfg, d, out, fin, units, 2e-2)
 
 
+def test_prefill_workload_fp32_h96_t8192_sampled(cuda_lib):
+    """The bench workload with fp32 q/k/v: the CUDA-core path, whose dv slices of a head share
+    A, P and Wk as a thread-block cluster; sampled heads against the oracle at the 1e-4 bar."""
+    base = W.prefill_config()
+    cfg = W.PrefillConfig(base.name.replace("bf16", "fp32"), base.seqlens, base.num_heads, base.dk, base.dv,
+                          torch.float32, base.init_state)
+    d = W.make_prefill_inputs(cfg, seed=3, device="cuda")
+    out, fin = cuda_lib.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_state"])
+    torch.cuda.synchronize()
+    assert cuda_lib.last_device_status() == cuda_lib.KDA_OK
+    assert torch.isfinite(out).all() and torch.isfinite(fin).all()
+    units = sampled_units(1, 96, 4, seed=3, must=[(0, 0), (0, 95)])
+    _sampled_check(cuda_lib, cfg, d, out, fin, units, 1e-4)
+
+
 def test_varlen_workload_32_seqs_sampled(cuda_lib):
     cfg = W.varlen_config(0)
     d = W.make_prefill_inputs(cfg, seed=0, device="cuda")
