@@ -275,6 +275,49 @@ __device__ __forceinline__ void cp_async8(void* smem_dst, const void* gsrc)
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// K~^T hi + lo into the prep's staging buffer (the back image's layout: K-major [128 dk rows]
+// [64 tokens], 128-byte swizzle), each value as ktilde_pairs forms it.  Thread t takes key
+// channels c, c + 1 (c = 2 (t % 64)) and tokens [8 g, 8 g + 8) (g = t / 64): one 4-byte load of
+// k and one 8-byte load of x per token serve both channels.  A warp's stores land on rows of
+// every residue mod 8 (lanes 4-7 of each group of 8 store row c + 1 first), so that each store
+// instruction meets no more bank conflicts than its 512 bytes need.
+__device__ __forceinline__ void ktilde_stage(uint8_t* sm, const float* vec, int t, int BT, uint32_t stage)
+{
+    const int cp = t & 63, g = t >> 6, c = 2 * cp, J = g >> 1;
+    const uint32_t sbase = smem_u32(sm);
+    const float2 dj = *reinterpret_cast<const float2*>(vec + (V_D + J) * 128 + c);
+    const float2 gj = *reinterpret_cast<const float2*>(vec + (V_G + J) * 128 + c);
+    const float f0 = dj.x * gj.x, f1 = dj.y * gj.y;
+    float v0[8], v1[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const int r = 8 * g + e;
+        uint32_t kk;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(kk) : "r"(sbase + OFF_K + sw128_off(r, c, 64)));
+        const float2 x = *reinterpret_cast<const float2*>(sm + OFF_G + sw128_off_f32(r, c, 64));
+        const float k0 = (r < BT) ? __uint_as_float(kk << 16) : 0.f;
+        const float k1 = (r < BT) ? __uint_as_float(kk & 0xffff0000u) : 0.f;
+        v0[e] = k0 * (f0 * rcpf(x.x));
+        v1[e] = k1 * (f1 * rcpf(x.y));
+    }
+    uint32_t h0[4], l0[4], h1[4], l1[4];
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+        split_bf16x2(v0[2 * pr], v0[2 * pr + 1], h0[pr], l0[pr]);
+        split_bf16x2(v1[2 * pr], v1[2 * pr + 1], h1[pr], l1[pr]);
+    }
+    const bool odd_first = (t >> 2) & 1;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        const bool one = (s == 0) == odd_first;   // this store writes channel c + 1
+        const uint32_t row = c + (one ? 1 : 0);
+        const uint32_t* h = one ? h1 : h0;
+        const uint32_t* l = one ? l1 : l0;
+        st_shared_v4(stage + sw128_chunk(row, g, 128), h[0], h[1], h[2], h[3]);
+        st_shared_v4(stage + 16384 + sw128_chunk(row, g, 128), l[0], l[1], l[2], l[3]);
+    }
+}
+
 // ---------------------------------------------------------------- step 1: chunk offsets
 // One CTA of 1024 threads: chunk_off[n] = sum over m < n of ceil(len_m / 64), lengths of
 // sequences that fail the cu_seqlens check counted as 0 (and the failure reported); then
@@ -542,18 +585,8 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
                                  ks > 0 ? 1u : 0u);
             umma_commit(bar_mma);
         }
-        {
-            uint32_t hi[8], lo[8];
-            ktilde_pairs(sm, vec, L, part, BT, hi, lo);
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                st_shared_v4(sbase + A_STAGE + sw128_chunk(L, 2 * part + cc, 128), hi[4 * cc], hi[4 * cc + 1],
-                             hi[4 * cc + 2], hi[4 * cc + 3]);
-                st_shared_v4(sbase + A_STAGE + 16384 + sw128_chunk(L, 2 * part + cc, 128), lo[4 * cc],
-                             lo[4 * cc + 1], lo[4 * cc + 2], lo[4 * cc + 3]);
-            }
-            fence_proxy_async_smem();
-        }
+        ktilde_stage(sm, vec, t, BT, sbase + A_STAGE);
+        fence_proxy_async_smem();
         if (t < 128) reinterpret_cast<float*>(img + IMG_GAM)[t] = vec[V_GC * 128 + t];
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
         mma_par ^= 1u;
