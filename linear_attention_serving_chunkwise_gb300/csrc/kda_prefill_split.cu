@@ -585,7 +585,19 @@ __device__ __forceinline__ void prep_items(const SplitParams& sp, uint8_t* sm, u
                                  ks > 0 ? 1u : 0u);
             umma_commit(bar_mma);
         }
-        ktilde_stage(sm, vec, t, BT, sbase + A_STAGE);
+        if constexpr (kPro) {   // the prologue instance keeps one key channel per thread (measured faster there)
+            uint32_t hi[8], lo[8];
+            ktilde_pairs(sm, vec, L, part, BT, hi, lo);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                st_shared_v4(sbase + A_STAGE + sw128_chunk(L, 2 * part + cc, 128), hi[4 * cc], hi[4 * cc + 1],
+                             hi[4 * cc + 2], hi[4 * cc + 3]);
+                st_shared_v4(sbase + A_STAGE + 16384 + sw128_chunk(L, 2 * part + cc, 128), lo[4 * cc],
+                             lo[4 * cc + 1], lo[4 * cc + 2], lo[4 * cc + 3]);
+            }
+        } else {
+            ktilde_stage(sm, vec, t, BT, sbase + A_STAGE);
+        }
         fence_proxy_async_smem();
         if (t < 128) reinterpret_cast<float*>(img + IMG_GAM)[t] = vec[V_GC * 128 + t];
         if (!(ok = wait_all(bar_mma, mma_par, s_abort))) break;
